@@ -1,0 +1,384 @@
+"""Benchmark of the NVFP4 MoE expert layer (libnvfp4moe) on GB300.
+
+One step = one forward of the whole layer (route, quantise, permute, gate/up
+GEMM with fused SwiGLU + requantisation, down GEMM, finalize) over one batch
+of seeded synthetic tokens whose inputs are resident in HBM.  Prints one
+JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+With N > 1 (torchrun) every rank runs an independent replica of the layer:
+the layer has no exchange step, so there is no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from nvfp4_block_scaled_07_gb300 import workloads as W  # noqa: E402
+
+METRIC = "NVFP4 MoE layer TFLOPS, HBM GB/s, tokens/s, % of GB300 roofline (1 GPU)"
+DEFAULT_WORKLOAD = "decode_t128"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 / BF16 tensor ratio
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ----------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# the CUDA path
+# ----------------------------------------------------------------------------
+def timed_step_with_kernel_events(B, layer, x, logits, ev):
+    """One layer forward with events between the library calls (same calls,
+    same order as MoELayer.forward, all on the current stream)."""
+    p = layer.perm
+    T = x.shape[0]
+    ev[0].record()
+    B.moe_route_topk(logits, layer.k, layer.score_fn, layer.renormalize, layer.bias, layer.topk_idx, layer.topk_w)
+    ev[1].record()
+    B.moe_quantize_nvfp4(x, global_scale=layer.x_gscale, compute_global=True, packed=layer.xq, scales=layer.xs,
+                         workspace=layer.q_ws)
+    ev[2].record()
+    B.moe_permute(layer.topk_idx, layer.E, layer.xq, layer.xs, out=p, workspace=layer.p_ws)
+    ev[3].record()
+    B.moe_grouped_gemm_nvfp4(p.a_packed, p.a_scales, layer.x_gscale, p.counts, p.row_offsets, layer.w_gu_packed,
+                             layer.w_gu_scales, layer.w_gu_gscale, B.EPI_SWIGLU_NVFP4, c_gscale=layer.h_scale,
+                             m_total=T * layer.k, tile_n=layer.tile_n[0], out=layer.hq, out_scales=layer.hs)
+    ev[4].record()
+    B.moe_grouped_gemm_nvfp4(layer.hq, layer.hs, layer.h_scale, p.counts, p.row_offsets, layer.w_d_packed,
+                             layer.w_d_scales, layer.w_d_gscale, B.EPI_BF16, m_total=T * layer.k,
+                             tile_n=layer.tile_n[1], out=layer.y)
+    ev[5].record()
+    B.moe_finalize(layer.y, p.flat_to_perm, layer.topk_w, out=layer.out)
+    ev[6].record()
+
+
+KERNEL_NAMES = ["route", "quantize", "permute", "gemm_gate_up_swiglu", "gemm_down", "finalize"]
+
+
+def run_ours(args, w):
+    from nvfp4_block_scaled_07_gb300 import binding as B
+    world, rank, local = dist_setup(args.gpus)
+    B.device_check()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = W.device_inputs(w, seed=args.seed + rank, device=dev)
+    layer = B.MoELayer(inp["w_gu"], inp["w_d"], w.k, w.score, w.renormalize, w.h_scale, bias=inp["bias"],
+                       T=w.T, tile_n=(args.tile_gate_up, args.tile_down))
+    del inp["w_gu"], inp["w_d"]
+    torch.cuda.empty_cache()
+    x, logits = inp["x"], inp["logits"]
+    for _ in range(args.warmup):
+        layer(x, logits)
+    B.sync_status()
+    counts = layer.perm.counts.cpu().numpy()
+    n_active = int((counts > 0).sum())
+
+    # ---- device-timed region: inputs resident in HBM ----
+    stream = torch.cuda.current_stream()
+    n_ev = 7
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        start.record(stream)
+        for s in range(args.steps):
+            timed_step_with_kernel_events(B, layer, x, logits, evs[s])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    B.sync_status()
+    ms_total = start.elapsed_time(stop)
+    ms_step = max_over_ranks(ms_total / args.steps, world)
+    per_kernel = np.array([[evs[s][i].elapsed_time(evs[s][i + 1]) for i in range(n_ev - 1)]
+                           for s in range(args.steps)])
+    kern_ms = per_kernel.mean(axis=0)
+
+    # ---- end to end: pinned host inputs in, result out, every step ----
+    x_h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x)
+    lg_h = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True).copy_(logits)
+    out_h = torch.empty((w.T, w.H), dtype=torch.bfloat16, pin_memory=True)
+    x_d, lg_d = torch.empty_like(x), torch.empty_like(logits)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        out = layer(x_d, lg_d)
+        out_h.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    h2d = x_h.numel() * x_h.element_size() + lg_h.numel() * lg_h.element_size()
+    d2h = out_h.numel() * out_h.element_size()
+
+    # ---- derived numbers ----
+    hbm_peak, bf16_peak, peak_kind = measured_peaks()
+    fp4_peak = bf16_peak * FP4_OVER_BF16
+    R = w.T * w.k
+    flops = W.algorithmic_flops(w)
+    w_bytes_active = n_active * W.nvfp4_bytes(3 * w.H * w.I)
+    alg_bytes = w_bytes_active + 2 * w.T * w.H * 2
+    tokens_s = w.T * world / (ms_step * 1e-3)
+    gu_ms = kern_ms[3]
+    gu_bytes = n_active * W.nvfp4_bytes(2 * w.I * w.H) + W.nvfp4_bytes(R * w.H) + W.nvfp4_bytes(R * w.I)
+    gu_flops = 4.0 * R * w.H * w.I
+    gu_hbm_time = gu_bytes / (hbm_peak * 1e9)
+    gu_tc_time = gu_flops / (fp4_peak * 1e12)
+    bound = "hbm" if gu_hbm_time >= gu_tc_time else "tensor"
+    if bound == "hbm":
+        achieved, peak, unit = gu_bytes / (gu_ms * 1e-3) / 1e9, hbm_peak, "GB/s"
+    else:
+        achieved, peak, unit = gu_flops / (gu_ms * 1e-3) / 1e12, fp4_peak, "TFLOP/s"
+    layer_frac = max(alg_bytes / (hbm_peak * 1e9), flops / (fp4_peak * 1e12)) / (ms_step * 1e-3)
+    res = {
+        "metric": METRIC, "value": round(tokens_s, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4 (e2m1 x ue4m3 scales, fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": w.name, **w.describe(), "active_experts": n_active,
+                   "l2": "inputs larger than L2: %.2f GB of NVFP4 weights streamed per step" % (w_bytes_active / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tflops": round(flops * world / (ms_step * 1e-3) / 1e12, 2),
+        "hbm_gbs": round(alg_bytes * world / (ms_step * 1e-3) / 1e9, 1),
+        "layer_roofline_frac": round(layer_frac, 4),
+        "kernels_ms": {n: round(float(v), 4) for n, v in zip(KERNEL_NAMES, kern_ms)},
+        "roofline": {"kernel": "gemm_gate_up_swiglu", "bound": bound, "achieved": round(achieved, 1),
+                     "peak": round(peak, 1), "unit": unit, "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if bound == "hbm" else
+                     f"{peak_kind} bf16 x {FP4_OVER_BF16:g} nominal fp4/bf16 ratio"},
+        "e2e": {"value": round(w.T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clk.summary(),
+        "gpu_launches": B.MoELayer.LAUNCHES_PER_FORWARD * args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, args, layer_inputs=(x, logits, inp["bias"], layer))
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# the CPU oracle on a bounded sample (baseline and reference arm)
+# ----------------------------------------------------------------------------
+def oracle_sample(w, x, logits, bias, w_gu_dev, w_d_dev, experts):
+    """Oracle layer on the routed rows of `experts` (weights quantised by the
+    oracle beforehand, untimed).  Returns (seconds, rows processed)."""
+    from oracle import nvfp4_moe_oracle as O
+    q = {}
+    for e in experts:
+        for name, src in (("gu", w_gu_dev), ("d", w_d_dev)):
+            a = src[e].float().cpu().numpy()
+            g = O.global_scale(a)
+            p, s = O.quantize_nvfp4(a, g)
+            q[(name, e)] = (p, s, g)
+    x32 = x.float().cpu().numpy()
+    lg = logits.cpu().numpy()
+    b = None if bias is None else bias.cpu().numpy()
+    t0 = time.perf_counter()
+    idx, wts = O.route_topk(lg, b, w.k, w.score, w.renormalize)
+    s_x = O.global_scale(x32)
+    xq, xs = O.quantize_nvfp4(x32, s_x)
+    counts, offsets, p2f, f2p = O.permute(idx, w.E)
+    out = np.zeros((w.T, w.H))
+    rows = 0
+    for e in experts:
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 == r0:
+            continue
+        tok = p2f[r0:r1] // w.k
+        gp, gs, gg = q[("gu", e)]
+        dp, ds, dg = q[("d", e)]
+        sub = np.array([0, r1 - r0])
+        gu = O.grouped_gemm(xq[tok], xs[tok], s_x, sub, gp[None], gs[None], np.array([gg]))
+        h = O.swiglu(gu, w.I).astype(np.float32)
+        hq, hs = O.quantize_nvfp4(h, np.float32(w.h_scale))
+        y = O.round_to_bf16(O.grouped_gemm(hq, hs, np.float32(w.h_scale), sub, dp[None], ds[None], np.array([dg])))
+        np.add.at(out, tok, wts.reshape(-1)[p2f[r0:r1]][:, None] * y)
+        rows += r1 - r0
+    O.round_to_bf16(out)
+    return time.perf_counter() - t0, rows
+
+
+def cpu_baseline(w, args, layer_inputs):
+    x, logits, bias, layer = layer_inputs
+    counts = layer.perm.counts.cpu().numpy()
+    active = np.nonzero(counts)[0]
+    n = min(len(active), args.cpu_experts)
+    experts = active[np.linspace(0, len(active) - 1, n).astype(int)]
+    # weights in bf16 for the sampled experts, regenerated from the same seed
+    inp = W.device_inputs(w, seed=args.seed, device=x.device)
+    secs, rows = oracle_sample(w, x, logits, bias, inp["w_gu"], inp["w_d"], experts)
+    del inp
+    torch.cuda.empty_cache()
+    full = secs * len(active) / n
+    return {"value": round(w.T / full, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} of {len(active)} active experts ({rows} routed rows) through the float64 oracle in "
+                      f"{secs:.1f} s; layer time extrapolated by active experts (x{len(active) / n:.1f}); "
+                      f"elementwise steps on one thread, float64 matmuls on the BLAS pool"}
+
+
+def run_reference(args, w):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    inp = W.device_inputs(w, seed=args.seed, device=dev)
+    from oracle import nvfp4_moe_oracle as O
+    idx, _ = O.route_topk(inp["logits"].cpu().numpy(), None if inp["bias"] is None else inp["bias"].cpu().numpy(),
+                          w.k, w.score, w.renormalize)
+    active = np.unique(idx)
+    times = []
+    for s in range(args.warmup + args.steps):
+        e = int(active[s % len(active)])
+        secs, _ = oracle_sample(w, inp["x"], inp["logits"], inp["bias"], inp["w_gu"], inp["w_d"], [e])
+        if s >= args.warmup:
+            times.append(secs * len(active))   # one expert per step, extrapolated to the layer
+    ms = float(np.mean(times)) * 1e3
+    val = w.T / (ms * 1e-3)
+    res = {"metric": METRIC, "impl": "reference", "value": round(val, 4), "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": w.name, **w.describe(), "active_experts": int(len(active))},
+           "cpu_baseline": {"value": round(val, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                            "sample": "one active expert's routed rows per step through the float64 oracle, "
+                                      "extrapolated by the number of active experts"},
+           "e2e": {"value": round(val, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--tile-gate-up", type=int, default=0)
+    ap.add_argument("--tile-down", type=int, default=0)
+    ap.add_argument("--cpu-experts", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

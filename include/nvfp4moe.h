@@ -1,0 +1,227 @@
+/*
+ * libnvfp4moe -- the NVFP4 block-scaled Mixture-of-Experts expert layer on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The layer (route -> quantise -> permute -> grouped GEMM gate/up with fused
+ * SwiGLU and NVFP4 requantisation -> grouped GEMM down -> weighted finalize)
+ * is the hot path of the GLM-5-NVFP4 MoE deployment described on the source
+ * pages:
+ *   "SM120 FP4 Kernel Research Campaign"                      (page A)
+ *   "Discovering SM120-Specific CUTLASS MoE Kernels"          (page B)
+ *   "Uncovering SM120 CUTLASS Collective Implementations"     (page C)
+ * Each call below cites the passage that defines its operation.
+ *
+ * NVFP4 (page A, section 1: the block-scaled MMA takes e2m1 data and ue4m3
+ * scales, four scales per 64 K elements): values are FP4 E2M1 codes, two per
+ * byte, element 2i in the LOW nibble of byte i; one unsigned E4M3 scale byte
+ * per 16 consecutive elements along K; one FP32 per-tensor scale.  The value
+ * of an element is e2m1(code) * ue4m3(scale) * s.
+ *
+ * Scale layouts.  "Row-major" scales are uint8 [rows, cols/16].  "Blocked"
+ * scales are the tensor-core layout: rows are grouped in blocks of 128 and K
+ * in blocks of 64 elements (4 scales); block (rb, kb) is 512 contiguous
+ * bytes at offset (rb * (cols/64) + kb) * 512, and inside it the 4 scales of
+ * row r (r = 0..127 within the block) sit at (r % 32) * 16 + (r / 32) * 4.
+ * A blocked buffer holds ceil(rows/128)*128 rows (nvfp4moe_blocked_scales_bytes).
+ *
+ * Conventions for every call:
+ *   - C ABI, returns a status code (NVFP4MOE_OK = 0 on success).  A non-zero
+ *     status means nothing was launched; nvfp4moe_last_error_detail() gives
+ *     a per-thread message.
+ *   - Pointers marked "device" are device memory owned by the caller; the
+ *     library never allocates, frees or keeps them.  Host pointers are
+ *     marked "host".  Buffers must be 16-byte aligned.
+ *   - Work is enqueued on `stream` and never synchronises.  Data-dependent
+ *     scalars (global scales, counts) stay on the device.
+ *   - Device-side checks (an expert id out of range, a pipeline wait that
+ *     exceeded its time limit) do not fault: they skip the offending work and
+ *     raise a sticky device flag that nvfp4moe_sync_status() reports.
+ *   - Only compute capability 10.3 (GB300) is supported.
+ */
+#ifndef NVFP4MOE_H
+#define NVFP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define NVFP4MOE_OK                 0
+#define NVFP4MOE_ERR_INVALID_ARG    1  /* null/misaligned pointer, bad enum, negative size */
+#define NVFP4MOE_ERR_UNSUPPORTED    2  /* shape outside the supported set, or device is not cc 10.3 */
+#define NVFP4MOE_ERR_SMEM           3  /* tile pipeline does not fit the device's opt-in shared memory */
+#define NVFP4MOE_ERR_WORKSPACE      4  /* workspace smaller than the matching *_workspace_size() */
+#define NVFP4MOE_ERR_CUDA           5  /* CUDA runtime error (launch failure, driver entry point missing) */
+#define NVFP4MOE_ERR_TIMEOUT        6  /* a device pipeline wait ran out of time (sticky, see sync_status) */
+#define NVFP4MOE_ERR_DEVICE_DATA    7  /* device data out of range, e.g. an expert id >= E (sticky) */
+
+/* ---- enums ------------------------------------------------------------- */
+#define NVFP4MOE_SCORE_SOFTMAX      0
+#define NVFP4MOE_SCORE_SIGMOID      1
+
+#define NVFP4MOE_QUANT_COMPUTE_GLOBAL  1  /* compute s = amax/2688 into *global_scale */
+#define NVFP4MOE_QUANT_SCALES_BLOCKED  2  /* write scales in the blocked layout */
+
+#define NVFP4MOE_EPI_BF16           0  /* C = bf16(acc * s_a * s_w[e]) */
+#define NVFP4MOE_EPI_SWIGLU_NVFP4   1  /* h = silu(gate) * up, requantised to NVFP4 */
+#define NVFP4MOE_EPI_SWIGLU_F32     2  /* h = silu(gate) * up as float32 (unfused check) */
+
+/* ---- library and device ------------------------------------------------- */
+
+/* Version as major*10000 + minor*100 + patch. */
+int nvfp4moe_version(void);
+
+/* Static description of a status code (never NULL). */
+const char* nvfp4moe_status_string(int status);
+
+/* Message of the last failed call on the calling host thread ("" if none). */
+const char* nvfp4moe_last_error_detail(void);
+
+/* Checks that `device` is a compute capability 10.3 GPU and caches its SM
+ * count and opt-in shared memory.  Returns OK, UNSUPPORTED or CUDA. */
+int nvfp4moe_device_check(int device);
+
+/* Synchronises `stream`, then reads and clears the sticky device flags
+ * raised by earlier calls on the current device.  Returns OK, TIMEOUT,
+ * DEVICE_DATA or CUDA. */
+int nvfp4moe_sync_status(cudaStream_t stream);
+
+/* Bytes of a blocked scale buffer for a [rows, cols] NVFP4 matrix
+ * (cols % 64 == 0): ceil(rows/128) * 128 * cols / 16.  0 on bad input. */
+size_t nvfp4moe_blocked_scales_bytes(int64_t rows, int64_t cols);
+
+/* ---- a1: routing ---------------------------------------------------------
+ * Top-k expert selection with sigmoid scoring (page A, key finding 8 and its
+ * closing paragraph: "OEA with proper sigmoid scoring" of the GLM-5 router)
+ * or softmax.  Selection compares float32 v = logits + bias, descending, the
+ * lower expert index first on ties; slot j of a token holds its j-th
+ * largest v.  Weights (computed in float64, stored float32):
+ *   softmax: exp(v_j - max v) / sum over the k selected (renormalize = 1)
+ *            or over all E (renormalize = 0);
+ *   sigmoid: sigma(v_j), divided by the sum over the k selected when
+ *            renormalize = 1.
+ * logits  device float32 [T, E] row-major; bias device float32 [E] or NULL;
+ * topk_idx device int32 [T, k]; topk_w device float32 [T, k].
+ * Limits: 1 <= E <= 1024, 1 <= k <= min(E, 32), T >= 0 (T = 0 is a no-op).
+ * NaN logits give an unspecified (but in-range) selection. */
+int moe_route_topk(const float* logits, const float* bias, int T, int E, int k,
+                   int score_fn, int renormalize,
+                   int32_t* topk_idx, float* topk_w, cudaStream_t stream);
+
+/* ---- a2: quantisation ----------------------------------------------------
+ * bf16 -> NVFP4 (page A, section 1 operand types; four ue4m3 scales per k64
+ * MMA step means one scale per 16 elements).  Per 16-element block along a
+ * row: a = max|x|, t = (a / 6) / s in float32, scale byte b = t rounded to
+ * the nearest ue4m3 (ties to even, saturating at 448), d = ue4m3(b) * s,
+ * code = x / d rounded to the nearest E2M1 (ties to even, saturating at 6)
+ * with the sign bit of x; b == 0 gives code 0 for the block.
+ * x device bf16 [rows, cols] row-major, cols % 16 == 0
+ *   (cols % 64 == 0 with NVFP4MOE_QUANT_SCALES_BLOCKED).
+ * global_scale device float32 [1]: read as s, or, with
+ *   NVFP4MOE_QUANT_COMPUTE_GLOBAL, written with s = amax(|x|)/2688 (1 if
+ *   the tensor is zero) and then used.
+ * packed device uint8 [rows, cols/2]; scales device uint8, row-major
+ *   [rows, cols/16] or blocked (nvfp4moe_blocked_scales_bytes(rows, cols);
+ *   padding rows of the last block are written as 0).
+ * ws device workspace of moe_quantize_nvfp4_workspace_size() bytes (may be
+ *   NULL when that is 0).  rows = 0 is a no-op (global_scale untouched).
+ * NaN or infinite inputs are not supported. */
+size_t moe_quantize_nvfp4_workspace_size(int64_t rows, int64_t cols, int flags);
+int moe_quantize_nvfp4(const void* x_bf16, int64_t rows, int64_t cols,
+                       float* global_scale, int flags,
+                       uint8_t* packed, uint8_t* scales,
+                       void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Row-major scales [rows, cols/16] -> blocked layout (cols % 64 == 0), for
+ * NVFP4 data quantised elsewhere.  Padding rows are written as 0. */
+int moe_scales_to_blocked(const uint8_t* scales_row_major, int64_t rows, int64_t cols,
+                          uint8_t* scales_blocked, cudaStream_t stream);
+
+/* ---- a3: permutation -----------------------------------------------------
+ * Expert-first layout with token reordering (page A, section 6: "expert-
+ * first layout", "token reordering with fused reduction").  Flat id
+ * f = t*k + j.  Expert e's rows are the flat ids routed to e in ascending
+ * f.  Each expert's rows start at a multiple of 128 in the permuted
+ * buffers ("row_offsets"), so that a tensor-core tile never mixes experts.
+ * Inputs: topk_idx device int32 [T, k]; xq device uint8 [T, H/2] and
+ *   xs device uint8 [T, H/16] (row-major scales) from moe_quantize_nvfp4.
+ * Outputs (device):
+ *   expert_counts int32 [E]; expert_offsets int32 [E+1] (exclusive scan of
+ *   the counts: the unpadded expert-first order); row_offsets int32 [E+1]
+ *   (exclusive scan of counts rounded up to 128);
+ *   perm_to_flat int32 [rows_capacity]: flat id held by each padded row,
+ *   -1 for padding rows; flat_to_perm int32 [T*k]: padded row of each flat id;
+ *   a_packed uint8 [rows_capacity, H/2]: row row_offsets[e] + r is the
+ *   quantised token of expert e's r-th flat id (padding rows untouched);
+ *   a_scales uint8, blocked layout over rows_capacity rows.
+ * rows_capacity = moe_permute_rows_capacity(T, E, k).
+ * Limits: H % 64 == 0, 1 <= E <= 1024, 1 <= k <= E.  An expert id outside
+ * [0, E) is skipped and raises NVFP4MOE_ERR_DEVICE_DATA (sticky). */
+int64_t moe_permute_rows_capacity(int T, int E, int k);
+size_t moe_permute_workspace_size(int T, int E, int k);
+int moe_permute(const int32_t* topk_idx, int T, int E, int k,
+                const uint8_t* xq, const uint8_t* xs, int H,
+                int32_t* expert_counts, int32_t* expert_offsets, int32_t* row_offsets,
+                int32_t* perm_to_flat, int32_t* flat_to_perm,
+                uint8_t* a_packed, uint8_t* a_scales,
+                void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ---- a4/a5: grouped GEMM ---------------------------------------------------
+ * The grouped ("array") block-scaled GEMM over experts (page C, Context and
+ * the sm120_mma_array_tma_blockwise_scaling collective it finds; page A,
+ * section 7: warp-specialised schedules).  For every expert e and every
+ * valid row r of e (row = row_offsets[e] + r, r < expert_counts[e]):
+ *   acc[row, n] = sum_K A[row, :] * W[e, n, :]   (dequantised, fp32 accumulate)
+ * scaled by a_gscale[0] * w_gscale[e].  Epilogues:
+ *   NVFP4MOE_EPI_BF16:        c_out bf16 [rows_capacity, N] = bf16(acc).
+ *   NVFP4MOE_EPI_SWIGLU_NVFP4: N = 2*I, W rows [0, I) are the gate and
+ *       [I, 2I) the up projection; h = silu(gate) * up (float32) is
+ *       quantised with per-tensor scale c_gscale[0] exactly as
+ *       moe_quantize_nvfp4 does: c_out uint8 [rows_capacity, I/2] packed,
+ *       c_scales blocked over rows_capacity rows with I columns.
+ *   NVFP4MOE_EPI_SWIGLU_F32:  h as float32, c_out [rows_capacity, I].
+ * Padding rows of the outputs are left untouched.
+ * a_packed device uint8 [rows_capacity, K/2]; a_scales device blocked;
+ * a_gscale device float32 [1]; expert_counts / row_offsets device int32 as
+ * written by moe_permute; w_packed device uint8 [E, N, K/2]; w_scales
+ * device, blocked per expert ([E] x nvfp4moe_blocked_scales_bytes(N, K));
+ * w_gscale device float32 [E].
+ * m_total = number of routed rows (T*k), used only to pick the tile width;
+ * tile_n = 0 (auto) or the token-tile width 32, 64, 128 (and 256 for BF16).
+ * Limits: K % 64 == 0; N % 128 == 0 (BF16) or N % 256 == 0 (SwiGLU);
+ * 1 <= E <= 1024; rows_capacity % 128 == 0.  A pipeline that does not fit the
+ * device's opt-in shared memory is refused with NVFP4MOE_ERR_SMEM (the
+ * message gives the bytes required and the limit, cf. the OutOfResources
+ * failure quoted on page A, section "The Research Task").
+ * No workspace is used; ws may be NULL. */
+size_t moe_grouped_gemm_nvfp4_workspace_size(int E, int N, int K, int epilogue);
+int moe_grouped_gemm_nvfp4(const uint8_t* a_packed, const uint8_t* a_scales, const float* a_gscale,
+                           const int32_t* expert_counts, const int32_t* row_offsets,
+                           int E, int64_t rows_capacity, int64_t m_total,
+                           const uint8_t* w_packed, const uint8_t* w_scales, const float* w_gscale,
+                           int N, int K, int epilogue, const float* c_gscale,
+                           void* c_out, uint8_t* c_scales, int tile_n,
+                           void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ---- a6: finalize ----------------------------------------------------------
+ * Router-weighted reduce back to token order (page A, section 6: "token
+ * reordering with fused reduction"; page C, Context: the finalize
+ * epilogue): out[t, :] = sum_{j<k} topk_w[t, j] * y[flat_to_perm[t*k + j], :]
+ * accumulated in float32 in slot order, stored as bf16.
+ * y device bf16 [rows_capacity, H]; flat_to_perm device int32 [T*k];
+ * topk_w device float32 [T, k]; out device bf16 [T, H].  H % 8 == 0.
+ * A row index outside [0, rows_capacity) contributes nothing and raises
+ * NVFP4MOE_ERR_DEVICE_DATA (sticky). */
+int moe_finalize(const void* y_bf16, const int32_t* flat_to_perm, const float* topk_w,
+                 int T, int k, int H, int64_t rows_capacity,
+                 void* out_bf16, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4MOE_H */

@@ -1,0 +1,362 @@
+"""Python binding of libnvfp4moe (ctypes).
+
+Argument marshalling only: every function checks tensor dtypes, shapes and
+devices, allocates output tensors with torch when the caller passes none,
+and calls the C entry point of the same name on the current CUDA stream.
+All arithmetic of the layer runs in the library's CUDA kernels; there is no
+CPU or PyTorch fallback, and importing this module fails loudly when the
+shared library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libnvfp4moe.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libnvfp4moe.so is not built at {LIB_PATH}; build it with `python -c 'import __graft_entry__ as g; "
+        f"g.build()'` (nvcc, sm_103a). There is no fallback implementation.")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+# ---- constants (mirror include/nvfp4moe.h) ---------------------------------
+OK = 0
+ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_SMEM, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_DATA = range(1, 8)
+SCORE = {"softmax": 0, "sigmoid": 1}
+QUANT_COMPUTE_GLOBAL = 1
+QUANT_SCALES_BLOCKED = 2
+EPI_BF16, EPI_SWIGLU_NVFP4, EPI_SWIGLU_F32 = 0, 1, 2
+
+_i, _i64, _sz, _p, _f = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
+_SIGS = {
+    "nvfp4moe_version": (_i, []),
+    "nvfp4moe_status_string": (ctypes.c_char_p, [_i]),
+    "nvfp4moe_last_error_detail": (ctypes.c_char_p, []),
+    "nvfp4moe_device_check": (_i, [_i]),
+    "nvfp4moe_sync_status": (_i, [_p]),
+    "nvfp4moe_blocked_scales_bytes": (_sz, [_i64, _i64]),
+    "moe_route_topk": (_i, [_p, _p, _i, _i, _i, _i, _i, _p, _p, _p]),
+    "moe_quantize_nvfp4_workspace_size": (_sz, [_i64, _i64, _i]),
+    "moe_quantize_nvfp4": (_i, [_p, _i64, _i64, _p, _i, _p, _p, _p, _sz, _p]),
+    "moe_scales_to_blocked": (_i, [_p, _i64, _i64, _p, _p]),
+    "moe_permute_rows_capacity": (_i64, [_i, _i, _i]),
+    "moe_permute_workspace_size": (_sz, [_i, _i, _i]),
+    "moe_permute": (_i, [_p, _i, _i, _i, _p, _p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
+    "moe_grouped_gemm_nvfp4_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "moe_grouped_gemm_nvfp4": (_i, [_p, _p, _p, _p, _p, _i, _i64, _i64, _p, _p, _p, _i, _i, _i, _p, _p, _p, _i,
+                                    _p, _sz, _p]),
+    "moe_finalize": (_i, [_p, _p, _p, _i, _i, _i, _i64, _p, _p]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class Nvfp4MoeError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        msg = _lib.nvfp4moe_status_string(status).decode()
+        detail = _lib.nvfp4moe_last_error_detail().decode()
+        super().__init__(f"{where}: status {status} ({msg}): {detail}")
+
+
+def _check(status, where):
+    if status != OK:
+        raise Nvfp4MoeError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _need(t, dtype, shape=None, name="tensor"):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t
+
+
+def _empty(shape, dtype, device):
+    return torch.empty(shape, dtype=dtype, device=device)
+
+
+# ---- library / device --------------------------------------------------------
+def version():
+    return _lib.nvfp4moe_version()
+
+
+def device_check(device=None):
+    dev = torch.cuda.current_device() if device is None else int(device)
+    _check(_lib.nvfp4moe_device_check(dev), "nvfp4moe_device_check")
+
+
+def sync_status():
+    """Synchronise the current stream and raise on sticky device flags."""
+    _check(_lib.nvfp4moe_sync_status(_stream()), "nvfp4moe_sync_status")
+
+
+def blocked_scales_bytes(rows, cols):
+    return int(_lib.nvfp4moe_blocked_scales_bytes(rows, cols))
+
+
+# ---- a1 ------------------------------------------------------------------------
+def moe_route_topk(logits, k, score_fn="sigmoid", renormalize=True, bias=None, topk_idx=None, topk_w=None):
+    T, E = logits.shape
+    _need(logits, torch.float32, name="logits")
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    if topk_idx is None:
+        topk_idx = _empty((T, k), torch.int32, logits.device)
+    if topk_w is None:
+        topk_w = _empty((T, k), torch.float32, logits.device)
+    _need(topk_idx, torch.int32, (T, k), "topk_idx")
+    _need(topk_w, torch.float32, (T, k), "topk_w")
+    _check(_lib.moe_route_topk(_ptr(logits), _ptr(bias), T, E, k, SCORE[score_fn], int(bool(renormalize)),
+                               _ptr(topk_idx), _ptr(topk_w), _stream()), "moe_route_topk")
+    return topk_idx, topk_w
+
+
+# ---- a2 ------------------------------------------------------------------------
+def moe_quantize_nvfp4(x, global_scale=None, compute_global=None, blocked=False, packed=None, scales=None,
+                       workspace=None):
+    """Returns (packed [rows, cols/2] u8, scales u8, global_scale f32 [1])."""
+    _need(x, torch.bfloat16, name="x")
+    rows, cols = x.shape
+    dev = x.device
+    if compute_global is None:
+        compute_global = global_scale is None
+    if global_scale is None:
+        global_scale = _empty((1,), torch.float32, dev)
+    _need(global_scale, torch.float32, (1,), "global_scale")
+    flags = (QUANT_COMPUTE_GLOBAL if compute_global else 0) | (QUANT_SCALES_BLOCKED if blocked else 0)
+    if packed is None:
+        packed = _empty((rows, cols // 2), torch.uint8, dev)
+    if scales is None:
+        scales = _empty((blocked_scales_bytes(rows, cols),) if blocked else (rows, cols // 16), torch.uint8, dev)
+    _need(packed, torch.uint8, name="packed")
+    _need(scales, torch.uint8, name="scales")
+    ws_bytes = int(_lib.moe_quantize_nvfp4_workspace_size(rows, cols, flags))
+    if ws_bytes and workspace is None:
+        workspace = _empty((ws_bytes,), torch.uint8, dev)
+    _check(_lib.moe_quantize_nvfp4(_ptr(x), rows, cols, _ptr(global_scale), flags, _ptr(packed), _ptr(scales),
+                                   _ptr(workspace) if ws_bytes else None,
+                                   workspace.numel() if (ws_bytes and workspace is not None) else 0, _stream()),
+           "moe_quantize_nvfp4")
+    return packed, scales, global_scale
+
+
+def moe_scales_to_blocked(scales, cols, out=None):
+    _need(scales, torch.uint8, name="scales")
+    rows = scales.shape[0]
+    if out is None:
+        out = _empty((blocked_scales_bytes(rows, cols),), torch.uint8, scales.device)
+    _check(_lib.moe_scales_to_blocked(_ptr(scales), rows, cols, _ptr(out), _stream()), "moe_scales_to_blocked")
+    return out
+
+
+def quantize_expert_weights(w):
+    """bf16 [E, N, K] -> (packed [E, N, K/2], blocked scales [E, bytes], per-expert scales [E]).
+
+    One moe_quantize_nvfp4 call per expert matrix, each computing its own
+    per-tensor scale."""
+    _need(w, torch.bfloat16, name="w")
+    E, N, K = w.shape
+    dev = w.device
+    packed = _empty((E, N, K // 2), torch.uint8, dev)
+    scales = _empty((E, blocked_scales_bytes(N, K)), torch.uint8, dev)
+    gscale = _empty((E,), torch.float32, dev)
+    ws = _empty((64,), torch.uint8, dev)
+    for e in range(E):
+        moe_quantize_nvfp4(w[e], global_scale=gscale[e:e + 1], compute_global=True, blocked=True,
+                           packed=packed[e], scales=scales[e], workspace=ws)
+    return packed, scales, gscale
+
+
+# ---- a3 ------------------------------------------------------------------------
+def moe_permute_rows_capacity(T, E, k):
+    return int(_lib.moe_permute_rows_capacity(T, E, k))
+
+
+@dataclass
+class Permutation:
+    counts: torch.Tensor
+    offsets: torch.Tensor
+    row_offsets: torch.Tensor
+    perm_to_flat: torch.Tensor
+    flat_to_perm: torch.Tensor
+    a_packed: torch.Tensor
+    a_scales: torch.Tensor
+    rows_capacity: int
+
+
+def alloc_permutation(T, E, k, H, device):
+    cap = moe_permute_rows_capacity(T, E, k)
+    return Permutation(
+        counts=_empty((E,), torch.int32, device), offsets=_empty((E + 1,), torch.int32, device),
+        row_offsets=_empty((E + 1,), torch.int32, device), perm_to_flat=_empty((cap,), torch.int32, device),
+        flat_to_perm=_empty((T * k,), torch.int32, device), a_packed=_empty((cap, H // 2), torch.uint8, device),
+        a_scales=_empty((blocked_scales_bytes(cap, H),), torch.uint8, device), rows_capacity=cap)
+
+
+def moe_permute_workspace_size(T, E, k):
+    return int(_lib.moe_permute_workspace_size(T, E, k))
+
+
+def moe_permute(topk_idx, E, xq, xs, out: Permutation = None, workspace=None):
+    _need(topk_idx, torch.int32, name="topk_idx")
+    T, k = topk_idx.shape
+    H = xq.shape[1] * 2
+    _need(xq, torch.uint8, (T, H // 2), "xq")
+    _need(xs, torch.uint8, (T, H // 16), "xs")
+    dev = topk_idx.device
+    if out is None:
+        out = alloc_permutation(T, E, k, H, dev)
+    ws_bytes = moe_permute_workspace_size(T, E, k)
+    if workspace is None:
+        workspace = _empty((ws_bytes,), torch.uint8, dev)
+    _check(_lib.moe_permute(_ptr(topk_idx), T, E, k, _ptr(xq), _ptr(xs), H, _ptr(out.counts), _ptr(out.offsets),
+                            _ptr(out.row_offsets), _ptr(out.perm_to_flat), _ptr(out.flat_to_perm),
+                            _ptr(out.a_packed), _ptr(out.a_scales), _ptr(workspace), workspace.numel(), _stream()),
+           "moe_permute")
+    return out
+
+
+# ---- a4/a5 ---------------------------------------------------------------------
+def moe_grouped_gemm_nvfp4(a_packed, a_scales, a_gscale, counts, row_offsets, w_packed, w_scales, w_gscale,
+                           epilogue=EPI_BF16, c_gscale=None, m_total=None, tile_n=0, out=None, out_scales=None):
+    """Returns c_out (and c_scales for EPI_SWIGLU_NVFP4)."""
+    E, N, Kh = w_packed.shape
+    K = 2 * Kh
+    cap = a_packed.shape[0]
+    dev = a_packed.device
+    _need(a_packed, torch.uint8, (cap, K // 2), "a_packed")
+    _need(a_scales, torch.uint8, name="a_scales")
+    _need(a_gscale, torch.float32, (1,), "a_gscale")
+    _need(counts, torch.int32, (E,), "counts")
+    _need(row_offsets, torch.int32, (E + 1,), "row_offsets")
+    _need(w_packed, torch.uint8, name="w_packed")
+    _need(w_scales, torch.uint8, name="w_scales")
+    _need(w_gscale, torch.float32, (E,), "w_gscale")
+    if a_scales.numel() < blocked_scales_bytes(cap, K) or w_scales.numel() < E * blocked_scales_bytes(N, K):
+        raise ValueError("scale buffers smaller than the blocked layout needs")
+    if epilogue == EPI_BF16:
+        if out is None:
+            out = _empty((cap, N), torch.bfloat16, dev)
+        _need(out, torch.bfloat16, (cap, N), "out")
+    elif epilogue == EPI_SWIGLU_NVFP4:
+        I = N // 2
+        if out is None:
+            out = _empty((cap, I // 2), torch.uint8, dev)
+        if out_scales is None:
+            out_scales = _empty((blocked_scales_bytes(cap, I),), torch.uint8, dev)
+        _need(out, torch.uint8, (cap, I // 2), "out")
+        _need(out_scales, torch.uint8, name="out_scales")
+        _need(c_gscale, torch.float32, (1,), "c_gscale")
+    elif epilogue == EPI_SWIGLU_F32:
+        if out is None:
+            out = _empty((cap, N // 2), torch.float32, dev)
+        _need(out, torch.float32, (cap, N // 2), "out")
+    else:
+        raise ValueError(f"epilogue {epilogue}")
+    if m_total is None:
+        m_total = cap
+    _check(_lib.moe_grouped_gemm_nvfp4(_ptr(a_packed), _ptr(a_scales), _ptr(a_gscale), _ptr(counts),
+                                       _ptr(row_offsets), E, cap, int(m_total), _ptr(w_packed), _ptr(w_scales),
+                                       _ptr(w_gscale), N, K, epilogue, _ptr(c_gscale), _ptr(out),
+                                       _ptr(out_scales), int(tile_n), None, 0, _stream()),
+           "moe_grouped_gemm_nvfp4")
+    return (out, out_scales) if epilogue == EPI_SWIGLU_NVFP4 else out
+
+
+# ---- a6 ------------------------------------------------------------------------
+def moe_finalize(y, flat_to_perm, topk_w, out=None):
+    _need(y, torch.bfloat16, name="y")
+    T, k = topk_w.shape
+    cap, H = y.shape
+    _need(flat_to_perm, torch.int32, (T * k,), "flat_to_perm")
+    _need(topk_w, torch.float32, name="topk_w")
+    if out is None:
+        out = _empty((T, H), torch.bfloat16, y.device)
+    _need(out, torch.bfloat16, (T, H), "out")
+    _check(_lib.moe_finalize(_ptr(y), _ptr(flat_to_perm), _ptr(topk_w), T, k, H, cap, _ptr(out), _stream()),
+           "moe_finalize")
+    return out
+
+
+# ---- the whole layer -------------------------------------------------------------
+class MoELayer:
+    """NVFP4 expert weights plus every buffer of one layer shape.
+
+    forward() enqueues the six library calls (route, quantise, permute,
+    gate/up GEMM with SwiGLU + requantisation, down GEMM, finalize) on the
+    current stream and allocates nothing."""
+
+    def __init__(self, w_gu, w_d, k, score_fn="sigmoid", renormalize=True, h_scale=2.0 ** -4, bias=None,
+                 T=None, tile_n=(0, 0)):
+        self.E, two_i, self.H = w_gu.shape
+        self.I = two_i // 2
+        self.k, self.score_fn, self.renormalize = k, score_fn, renormalize
+        self.device = w_gu.device
+        self.bias = bias
+        self.tile_n = tile_n
+        self.w_gu_packed, self.w_gu_scales, self.w_gu_gscale = quantize_expert_weights(w_gu)
+        self.w_d_packed, self.w_d_scales, self.w_d_gscale = quantize_expert_weights(w_d)
+        self.h_scale = torch.full((1,), h_scale, dtype=torch.float32, device=self.device)
+        self.T = None
+        if T is not None:
+            self._alloc(T)
+
+    def _alloc(self, T):
+        dev, E, k, H, I = self.device, self.E, self.k, self.H, self.I
+        self.T = T
+        self.topk_idx = _empty((T, k), torch.int32, dev)
+        self.topk_w = _empty((T, k), torch.float32, dev)
+        self.x_gscale = _empty((1,), torch.float32, dev)
+        self.xq = _empty((T, H // 2), torch.uint8, dev)
+        self.xs = _empty((T, H // 16), torch.uint8, dev)
+        self.q_ws = _empty((64,), torch.uint8, dev)
+        self.perm = alloc_permutation(T, E, k, H, dev)
+        self.p_ws = _empty((moe_permute_workspace_size(T, E, k),), torch.uint8, dev)
+        cap = self.perm.rows_capacity
+        self.hq = _empty((cap, I // 2), torch.uint8, dev)
+        self.hs = _empty((blocked_scales_bytes(cap, I),), torch.uint8, dev)
+        self.y = _empty((cap, H), torch.bfloat16, dev)
+        self.out = _empty((T, H), torch.bfloat16, dev)
+
+    def forward(self, x, logits, out=None):
+        T = x.shape[0]
+        if self.T != T:
+            self._alloc(T)
+        p = self.perm
+        moe_route_topk(logits, self.k, self.score_fn, self.renormalize, self.bias, self.topk_idx, self.topk_w)
+        moe_quantize_nvfp4(x, global_scale=self.x_gscale, compute_global=True, packed=self.xq, scales=self.xs,
+                           workspace=self.q_ws)
+        moe_permute(self.topk_idx, self.E, self.xq, self.xs, out=p, workspace=self.p_ws)
+        moe_grouped_gemm_nvfp4(p.a_packed, p.a_scales, self.x_gscale, p.counts, p.row_offsets, self.w_gu_packed,
+                               self.w_gu_scales, self.w_gu_gscale, EPI_SWIGLU_NVFP4, c_gscale=self.h_scale,
+                               m_total=T * self.k, tile_n=self.tile_n[0], out=self.hq, out_scales=self.hs)
+        moe_grouped_gemm_nvfp4(self.hq, self.hs, self.h_scale, p.counts, p.row_offsets, self.w_d_packed,
+                               self.w_d_scales, self.w_d_gscale, EPI_BF16, m_total=T * self.k,
+                               tile_n=self.tile_n[1], out=self.y)
+        return moe_finalize(self.y, p.flat_to_perm, self.topk_w, out=self.out if out is None else out)
+
+    __call__ = forward
+
+    # kernels launched by one forward(): route 1, quantise 2, permute 3, GEMMs 2, finalize 1
+    LAUNCHES_PER_FORWARD = 9

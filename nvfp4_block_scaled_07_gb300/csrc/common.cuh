@@ -1,0 +1,64 @@
+// Device helpers shared by the libnvfp4moe kernels (sm_103a only).
+//
+// NVFP4 codec: E2M1 codes with one unsigned E4M3 (ue4m3) scale per 16
+// elements and a float32 per-tensor scale -- the operand types of the
+// block-scaled MMA ("SM120 FP4 Kernel Research Campaign", section 1).
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace nvfp4moe {
+
+constexpr float kE2M1Max = 6.0f;
+constexpr float kGlobalScaleDivisor = 2688.0f;   // 6 * 448: largest E2M1 * largest ue4m3
+
+// Offset of the 4-byte scale group (row, kb) in the blocked scale layout:
+// blocks of 128 rows x 64 K elements, 512 bytes each, row r of a block at
+// (r % 32) * 16 + (r / 32) * 4.  kblocks = cols / 64.
+__host__ __device__ __forceinline__ int64_t blocked_sf_offset(int64_t row, int64_t kb, int64_t kblocks) {
+  return ((row >> 7) * kblocks + kb) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;
+}
+
+// Round a non-negative float to the nearest ue4m3 byte, ties to even,
+// saturating at 448 (0x7E).  Works on the float32 bit pattern.
+__device__ __forceinline__ uint32_t f32_to_ue4m3(float t) {
+  if (!(t < 448.0f)) return 0x7Eu;                  // also catches +inf
+  const uint32_t bits = __float_as_uint(t);
+  const int e = int(bits >> 23) - 127;              // unbiased exponent of t
+  if (e < -6) {
+    // ue4m3 subnormal range: value = m * 2^-9, m in 0..8 (8 is the first normal)
+    return uint32_t(__float2int_rn(t * 512.0f));    // exact scaling, RNE to integer
+  }
+  const uint32_t mant = bits & 0x7FFFFFu;
+  uint32_t m3 = mant >> 20;
+  const uint32_t rest = mant & 0xFFFFFu;
+  if (rest > 0x80000u || (rest == 0x80000u && (m3 & 1u))) ++m3;   // RNE on the dropped 20 bits
+  uint32_t code = (uint32_t(e + 7) << 3) + m3;                      // mantissa carry bumps the exponent
+  return code > 0x7Eu ? 0x7Eu : code;
+}
+
+// Value of a ue4m3 byte (valid bytes 0..0x7E).
+__device__ __forceinline__ float ue4m3_to_f32(uint32_t b) {
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  if (e == 0) return float(m) * (1.0f / 512.0f);
+  return __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// E2M1 magnitude code of |q|: nearest of {0, .5, 1, 1.5, 2, 3, 4, 6},
+// ties to the even code, saturating at 6.  The comparisons sit on the exact
+// midpoints; strict/non-strict choice implements ties-to-even.
+__device__ __forceinline__ uint32_t e2m1_mag_code(float a) {
+  return uint32_t(a > 0.25f) + uint32_t(a >= 0.75f) + uint32_t(a > 1.25f) + uint32_t(a >= 1.75f) +
+         uint32_t(a > 2.5f) + uint32_t(a >= 3.5f) + uint32_t(a > 5.0f);
+}
+
+// Code of one element given the block's dequantisation step d = ue4m3(b) * s.
+__device__ __forceinline__ uint32_t e2m1_code(float x, float d) {
+  if (d == 0.0f) return 0u;
+  const uint32_t sign = (__float_as_uint(x) >> 31) << 3;
+  return e2m1_mag_code(fabsf(x) / d) | sign;
+}
+
+}  // namespace nvfp4moe

@@ -1,0 +1,509 @@
+// Grouped NVFP4 block-scaled GEMM over experts on the 5th-generation tensor
+// core (tcgen05, sm_103a), with the SwiGLU + NVFP4 requantisation epilogue of
+// the gate/up projection fused in.
+//
+// Source of the operation: "Uncovering SM120 CUTLASS Collective
+// Implementations" (Context: the grouped "array" block-scaled GEMM with a
+// finalize epilogue, tile shapes limited by shared memory) and "SM120 FP4
+// Kernel Research Campaign" (section 1: the block-scaled MMA with e2m1 data
+// and ue4m3 scales; section 7: warp-specialised producer/consumer schedules;
+// the SM100 column of its hardware table: tcgen05.mma, 256 KB of tensor
+// memory, 228 KB of shared memory).  The SM120 kernels the pages study use
+// mma.sync in 100 KB of shared memory; this kernel is designed for the GB300
+// instead: one 128-row tcgen05 MMA per k64 step with the accumulator in
+// tensor memory, operands staged by TMA through a deep mbarrier ring that
+// uses the whole opt-in shared memory.
+//
+// Orientation ("swap AB"): the weight rows of one expert form the 128-row
+// M side, the expert's tokens form the N side (BN = 32..256).  Decode-sized
+// experts (a handful to ~64 tokens) then fill whole MMAs along M and the
+// kernel streams every weight tile from HBM exactly once.
+//
+// Warp roles (192 threads, one CTA per SM, persistent):
+//   warp 0     TMA producer: weight tile(s), token tile, their scale blocks
+//   warp 1     tensor-memory owner and MMA issuer (one elected lane)
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator, scaling, SwiGLU,
+//              requantisation or bf16 conversion, global stores
+// Tiles are (expert, M tile, N tile) with N innermost, striped over the
+// CTAs, so the CTAs working at the same time share a weight tile through L2.
+//
+// Every mbarrier wait is bounded (2 s); on expiry the kernel raises a sticky
+// flag, drains its own copies and MMAs, frees tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/nvfp4moe.h"
+#include "common.cuh"
+#include "internal.h"
+#include "sm103_ptx.cuh"
+
+namespace nvfp4moe {
+namespace {
+
+__device__ unsigned g_gemm_flags = 0;
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;           // MMA M (weight rows per tile)
+constexpr int kBKBytes = 128;      // bytes of K per stage and row = 256 E2M1 elements
+constexpr int kATile = kBM * kBKBytes;
+constexpr int kSfTile = 2048;      // 4 k64 blocks x 512-byte scale blocks
+constexpr int kTmemCols = 512;
+constexpr int kSfColBase = 384;    // two 64-column scale-factor buffers at 384 and 448
+constexpr int kMaxStages = 8;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+struct Params {
+  const uint8_t* w_scales;
+  const uint8_t* a_scales;
+  const float* a_gscale;
+  const float* w_gscale;
+  const int32_t* counts;
+  const int32_t* row_offsets;
+  const float* c_gscale;
+  void* c_out;
+  uint8_t* c_scales;
+  int E, N, K, epi, stages;
+  int64_t rows_cap;
+};
+
+template <int BN, bool SWIGLU>
+struct Cfg {
+  static constexpr int NA = SWIGLU ? 2 : 1;          // weight tiles per stage (gate, up)
+  static constexpr int BTile = BN * kBKBytes;
+  static constexpr int NSFB = BN > 128 ? 2 : 1;      // 128-row scale blocks per token tile
+  static constexpr int OffB = NA * kATile;
+  static constexpr int OffSfa = OffB + BTile;
+  static constexpr int OffSfb = OffSfa + NA * kSfTile;
+  static constexpr int Stage = OffSfb + NSFB * kSfTile;
+  static constexpr int AccCols = NA * BN;            // fp32 accumulator columns per tile
+  static constexpr int AccBufs = (2 * AccCols <= kSfColBase) ? 2 : 1;
+  static constexpr int SfCols = NA * 16 + NSFB * 16;
+  static_assert(AccBufs * AccCols <= kSfColBase, "accumulators overlap the scale-factor columns");
+  static_assert(SfCols <= 64, "scale-factor buffer overflow");
+  static_assert(Stage % 1024 == 0, "stages must stay 1024-byte aligned for the 128B swizzle");
+};
+
+size_t ctrl_bytes(int E) {
+  return size_t(2 * kMaxStages + 5) * 8 + 16 + (3 * size_t(E) + 1) * 4;
+}
+
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        atomicOr(&g_gemm_flags, kFlagTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Short bounded wait used only while draining after an abort.
+__device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > kTimeoutNs) return;
+  }
+}
+
+__device__ __forceinline__ void decode_tile(int t, const int* s_prefix, const int* s_count, int E, int BN, int& e,
+                                            int& mb, int& nb) {
+  int lo = 0, hi = E - 1;  // largest e with s_prefix[e] <= t (has >= 1 tile)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_prefix[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  e = lo;
+  const int ntn = (s_count[e] + BN - 1) / BN;
+  const int local = t - s_prefix[e];
+  mb = local / ntn;
+  nb = local - mb * ntn;
+}
+
+template <int BN, bool SWIGLU>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
+                        const Params p) {
+  using C = Cfg<BN, SWIGLU>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = p.stages;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(S) * C::Stage);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_prefix = reinterpret_cast<int*>(tmem_slot + 4);
+  int* s_count = s_prefix + p.E + 1;
+  int* s_rowoff = s_count + p.E;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t smem_base = ptx::smem_u32(smem);
+  const uint32_t bar0 = ptx::smem_u32(bars);
+  // full[s] = bar0 + 8s, empty[s] = bar0 + 8(S+s), acc_full[b], acc_empty[b], drain
+  auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (uint32_t(S) + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * uint32_t(2 * S + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * uint32_t(2 * S + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * uint32_t(2 * S + 4);
+
+  const int MT = (SWIGLU ? p.N / 2 : p.N) / kBM;  // M tiles per expert
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(accf_bar(b), 1);
+      ptx::mbar_init(acce_bar(b), 4);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+    ptx::prefetch_tmap(&tmap_w);
+    ptx::prefetch_tmap(&tmap_a);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 2) {
+    // Per-expert tile counts and their exclusive scan; experts whose rows
+    // would leave the padded buffers are skipped and flagged.
+    const int per = (p.E + 31) / 32;
+    const int beg = min(lane * per, p.E), end = min(beg + per, p.E);
+    int sum = 0;
+    for (int e = beg; e < end; ++e) {
+      int c = p.counts[e];
+      const int ro = p.row_offsets[e];
+      const int64_t padded = (int64_t(c) + 127) / 128 * 128;
+      if (c < 0 || ro < 0 || (ro & 127) || int64_t(ro) + padded > p.rows_cap) {
+        atomicOr(&g_gemm_flags, kFlagBadData);
+        c = 0;
+      }
+      s_count[e] = c;
+      s_rowoff[e] = ro;
+      sum += MT * ((c + BN - 1) / BN);
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(kFull, incl, off);
+      if (lane >= off) incl += o;
+    }
+    int run = incl - sum;
+    for (int e = beg; e < end; ++e) {
+      s_prefix[e] = run;
+      run += MT * ((s_count[e] + BN - 1) / BN);
+    }
+    if (lane == 31) s_prefix[p.E] = incl;
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int total = s_prefix[p.E];
+  const int kblocks = p.K / 64;
+  const int nkt = (kblocks + 3) / 4;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    const uint64_t pol_w = ptx::policy_evict_first();  // weights stream through once
+    const uint64_t pol_a = ptx::policy_evict_last();   // token tiles are re-read by every M tile
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+      int e, mb, nb;
+      decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb);
+      const int arow = s_rowoff[e] + nb * BN;
+      const int valid = s_count[e] - nb * BN;
+      const int sfb_chunks = (C::NSFB == 2 && valid <= 128) ? 1 : C::NSFB;
+      const int wrow0 = e * p.N + mb * kBM;
+      for (int kt = 0; kt < nkt; ++kt, ++it) {
+        const uint32_t s = it % uint32_t(S), ph = (it / uint32_t(S)) & 1u;
+        if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int nkb = min(4, kblocks - 4 * kt);
+        const uint32_t bytes = uint32_t(C::NA * kATile + C::BTile + (C::NA + sfb_chunks) * nkb * 512);
+        ptx::mbar_arrive_expect_tx(full_bar(s), bytes);
+        const uint32_t st = smem_base + s * uint32_t(C::Stage);
+#pragma unroll
+        for (int j = 0; j < C::NA; ++j)
+          ptx::tma_load_2d(st + j * kATile, &tmap_w, full_bar(s), kt * kBKBytes, wrow0 + j * (p.N / 2), pol_w);
+        ptx::tma_load_2d(st + C::OffB, &tmap_a, full_bar(s), kt * kBKBytes, arow, pol_a);
+#pragma unroll
+        for (int j = 0; j < C::NA; ++j) {
+          const int rb = SWIGLU ? (j * (p.N / 2) + mb * kBM) / kBM : mb;
+          const uint8_t* src = p.w_scales + ((size_t(e) * (p.N / kBM) + rb) * kblocks + 4 * kt) * 512;
+          ptx::bulk_load(st + C::OffSfa + j * kSfTile, src, uint32_t(nkb * 512), full_bar(s), pol_w);
+        }
+        for (int c = 0; c < sfb_chunks; ++c) {
+          const uint8_t* src = p.a_scales + ((size_t(arow / kBM) + c) * kblocks + 4 * kt) * 512;
+          ptx::bulk_load(st + C::OffSfb + c * kSfTile, src, uint32_t(nkb * 512), full_bar(s), pol_a);
+        }
+      }
+    }
+    if (!ok) {
+      // Let every copy this thread issued land before the CTA can exit.
+      const uint32_t first = it > uint32_t(S) ? it - uint32_t(S) : 0u;
+      for (uint32_t i = first; i < it; ++i) drain_phase(full_bar(i % uint32_t(S)), (i / uint32_t(S)) & 1u);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    constexpr uint32_t idesc = ptx::idesc_nvfp4(kBM, BN);
+    uint32_t it = 0;
+    int tile_i = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++tile_i) {
+      int e, mb, nb;
+      decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb);
+      const int buf = C::AccBufs == 2 ? (tile_i & 1) : 0;
+      const uint32_t acc_ph = uint32_t(C::AccBufs == 2 ? (tile_i >> 1) : tile_i) & 1u;
+      if (!wait_phase(acce_bar(buf), acc_ph ^ 1u, abort_flag)) break;
+      ptx::tc_fence_after();
+      const uint32_t d0 = tmem + uint32_t(buf * C::AccCols);
+      // A token tile narrower than 128 rows sits inside a 128-row scale block.
+      const uint32_t sfb_sub = BN < 128 ? uint32_t(((nb * BN) & 127) >> 5) : 0u;
+      for (int kt = 0; kt < nkt; ++kt, ++it) {
+        const uint32_t s = it % uint32_t(S), ph = (it / uint32_t(S)) & 1u;
+        if (!wait_phase(full_bar(s), ph, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t st = smem_base + s * uint32_t(C::Stage);
+        const uint32_t sf = tmem + uint32_t(kSfColBase + (it & 1u) * 64);
+        const int nkb = min(4, kblocks - 4 * kt);
+        for (int kb = 0; kb < nkb; ++kb) {
+#pragma unroll
+          for (int j = 0; j < C::NA; ++j)
+            ptx::tc_cp_32x128b_x4(sf + j * 16 + kb * 4, ptx::desc_sf_block(st + C::OffSfa + j * kSfTile + kb * 512));
+#pragma unroll
+          for (int c = 0; c < C::NSFB; ++c)
+            ptx::tc_cp_32x128b_x4(sf + C::NA * 16 + kb * 4 * C::NSFB + c * 4,
+                                  ptx::desc_sf_block(st + C::OffSfb + c * kSfTile + kb * 512));
+        }
+        const uint64_t bdesc = ptx::desc_kmajor_sw128(st + C::OffB);
+        for (int kb = 0; kb < nkb; ++kb) {
+#pragma unroll
+          for (int j = 0; j < C::NA; ++j) {
+            const uint64_t adesc = ptx::desc_kmajor_sw128(st + j * kATile);
+            ptx::tc_mma_nvfp4(d0 + j * BN, adesc + 2 * kb, bdesc + 2 * kb, idesc, sf + j * 16 + kb * 4,
+                              sf + C::NA * 16 + kb * 4 * C::NSFB + sfb_sub, (kt | kb) != 0 ? 1u : 0u);
+          }
+        }
+        ptx::tc_commit(empty_bar(s));  // frees the stage once these MMAs have read it
+      }
+      if (!ok) break;
+      ptx::tc_commit(accf_bar(buf));
+    }
+    ptx::tc_commit(drain_bar);  // every MMA of this CTA done before tensor memory is freed
+    drain_phase(drain_bar, 0);
+  } else if (warp >= 2) {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;            // tensor-memory lane quarter this warp may access
+    const int lrow = q * 32 + lane;    // accumulator row = output feature within the tile
+    const float a_gs = *p.a_gscale;
+    const bool f32_out = p.epi == NVFP4MOE_EPI_SWIGLU_F32;
+    const float s_h = (SWIGLU && !f32_out) ? *p.c_gscale : 1.0f;
+    const int n_out = SWIGLU ? p.N / 2 : p.N;
+    int tile_i = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++tile_i) {
+      int e, mb, nb;
+      decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb);
+      const int buf = C::AccBufs == 2 ? (tile_i & 1) : 0;
+      const uint32_t acc_ph = uint32_t(C::AccBufs == 2 ? (tile_i >> 1) : tile_i) & 1u;
+      if (!wait_phase(accf_bar(buf), acc_ph, abort_flag)) break;
+      ptx::tc_fence_after();
+      const int valid = min(BN, s_count[e] - nb * BN);
+      const int64_t row0 = int64_t(s_rowoff[e]) + int64_t(nb) * BN;
+      const float scale = a_gs * p.w_gscale[e];
+      const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + uint32_t(buf * C::AccCols);
+      const int f = mb * kBM + lrow;  // output column
+      for (int c0 = 0; c0 < valid; c0 += 32) {
+        uint32_t g[32];
+        ptx::tmem_ld_32x32b_x32(tbase + c0, g);
+        if constexpr (SWIGLU) {
+          uint32_t u[32];
+          ptx::tmem_ld_32x32b_x32(tbase + BN + c0, u);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (c0 + i < valid) {  // uniform across the warp
+              const float gf = __uint_as_float(g[i]) * scale;
+              const float uf = __uint_as_float(u[i]) * scale;
+              const float h = gf / (1.0f + expf(-gf)) * uf;
+              const int64_t row = row0 + c0 + i;
+              if (f32_out) {
+                static_cast<float*>(p.c_out)[row * n_out + f] = h;
+              } else {
+                float a = fabsf(h);
+                a = fmaxf(a, __shfl_xor_sync(kFull, a, 1));
+                a = fmaxf(a, __shfl_xor_sync(kFull, a, 2));
+                a = fmaxf(a, __shfl_xor_sync(kFull, a, 4));
+                a = fmaxf(a, __shfl_xor_sync(kFull, a, 8));
+                const uint32_t sb = f32_to_ue4m3((a / kE2M1Max) / s_h);
+                const float d = ue4m3_to_f32(sb) * s_h;
+                uint32_t word = e2m1_code(h, d) << (4 * (lane & 7));
+                word |= __shfl_xor_sync(kFull, word, 1);
+                word |= __shfl_xor_sync(kFull, word, 2);
+                word |= __shfl_xor_sync(kFull, word, 4);
+                if ((lane & 7) == 0)
+                  *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.c_out) + row * (n_out / 2) + f / 2) = word;
+                if ((lane & 15) == 0)
+                  p.c_scales[blocked_sf_offset(row, f >> 6, n_out / 64) + ((f >> 4) & 3)] = uint8_t(sb);
+              }
+            }
+          }
+        } else {
+          ptx::tmem_ld_wait();
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.c_out);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c0 + i < valid) out[(row0 + c0 + i) * n_out + f] = __float2bfloat16_rn(__uint_as_float(g[i]) * scale);
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(acce_bar(buf));
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D byte tensor [rows, row_bytes] -> TMA map with a [box_rows, 128 B] box, 128B swizzle.
+bool encode_kmajor_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cuuint64_t(row_bytes), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(row_bytes)};
+  cuuint32_t box[2] = {cuuint32_t(kBKBytes), cuuint32_t(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, bool SWIGLU>
+int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st) {
+  using C = Cfg<BN, SWIGLU>;
+  const size_t fixed = 1024 + ((ctrl_bytes(a.E) + 15) & ~size_t(15));
+  const int64_t avail = int64_t(smem_optin) - int64_t(fixed);
+  const int stages = int(std::min<int64_t>(kMaxStages, avail > 0 ? avail / C::Stage : 0));
+  if (stages < 2) {
+    set_error_detail(
+        "grouped GEMM tile 128x%d (%s) needs %zu bytes of shared memory for a 2-stage pipeline; Hardware limit: %d",
+        BN, SWIGLU ? "gate/up" : "down", fixed + 2 * size_t(C::Stage), smem_optin);
+    return NVFP4MOE_ERR_SMEM;
+  }
+  const size_t smem = fixed + size_t(stages) * C::Stage;
+  CUtensorMap tw, ta;
+  if (!encode_kmajor_map(&tw, a.w_packed, int64_t(a.E) * a.N, a.K / 2, kBM) ||
+      !encode_kmajor_map(&ta, a.a_packed, a.rows_capacity, a.K / 2, BN)) {
+    set_error_detail("cuTensorMapEncodeTiled failed or is unavailable");
+    return NVFP4MOE_ERR_CUDA;
+  }
+  cudaError_t err =
+      cudaFuncSetAttribute(grouped_gemm_kernel<BN, SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (err != cudaSuccess) {
+    set_error_detail("cudaFuncSetAttribute: %s", cudaGetErrorString(err));
+    return NVFP4MOE_ERR_CUDA;
+  }
+  Params p;
+  p.w_scales = a.w_scales;
+  p.a_scales = a.a_scales;
+  p.a_gscale = a.a_gscale;
+  p.w_gscale = a.w_gscale;
+  p.counts = a.counts;
+  p.row_offsets = a.row_offsets;
+  p.c_gscale = a.c_gscale;
+  p.c_out = a.c_out;
+  p.c_scales = a.c_scales;
+  p.E = a.E;
+  p.N = a.N;
+  p.K = a.K;
+  p.epi = a.epilogue;
+  p.stages = stages;
+  p.rows_cap = a.rows_capacity;
+  grouped_gemm_kernel<BN, SWIGLU><<<num_sms, kThreads, smem, st>>>(tw, ta, p);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) {
+    set_error_detail("grouped GEMM launch: %s", cudaGetErrorString(err));
+    return NVFP4MOE_ERR_CUDA;
+  }
+  return NVFP4MOE_OK;
+}
+
+}  // namespace
+
+int launch_grouped_gemm(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st) {
+  const bool swiglu = a.epilogue != NVFP4MOE_EPI_BF16;
+  int bn = a.tile_n;
+  if (bn == 0) {
+    const int64_t avg = (a.m_total + a.E - 1) / a.E;
+    bn = avg <= 16 ? 32 : avg <= 48 ? 64 : 128;
+  }
+  if (swiglu) {
+    switch (bn) {
+      case 32: return launch_impl<32, true>(a, num_sms, smem_optin, st);
+      case 64: return launch_impl<64, true>(a, num_sms, smem_optin, st);
+      case 128: return launch_impl<128, true>(a, num_sms, smem_optin, st);
+      default: break;
+    }
+  } else {
+    switch (bn) {
+      case 32: return launch_impl<32, false>(a, num_sms, smem_optin, st);
+      case 64: return launch_impl<64, false>(a, num_sms, smem_optin, st);
+      case 128: return launch_impl<128, false>(a, num_sms, smem_optin, st);
+      case 256: return launch_impl<256, false>(a, num_sms, smem_optin, st);
+      default: break;
+    }
+  }
+  set_error_detail("tile_n %d is not supported for this epilogue", a.tile_n);
+  return NVFP4MOE_ERR_UNSUPPORTED;
+}
+
+cudaError_t gemm_read_and_clear_flags(unsigned* flags) {
+  unsigned zero = 0;
+  cudaError_t err = cudaMemcpyFromSymbol(flags, g_gemm_flags, sizeof(unsigned));
+  if (err != cudaSuccess) return err;
+  return cudaMemcpyToSymbol(g_gemm_flags, &zero, sizeof(unsigned));
+}
+
+}  // namespace nvfp4moe

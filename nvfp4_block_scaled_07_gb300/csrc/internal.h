@@ -1,0 +1,67 @@
+// Host-side launchers shared between the translation units of libnvfp4moe.
+// Arguments are validated by the C entry points (api.cu) before any launcher
+// is called; launchers only configure grids and enqueue kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nvfp4moe {
+
+// Device flag bits (sticky until nvfp4moe_sync_status reads them).
+constexpr unsigned kFlagTimeout = 1u;
+constexpr unsigned kFlagBadData = 2u;
+
+// Segment of flat ids ranked by one warp in the permutation.
+constexpr int kPermuteSegment = 1024;
+
+cudaError_t launch_route_topk(const float* logits, const float* bias, int T, int E, int k, int score_fn,
+                              int renormalize, int32_t* idx, float* w, cudaStream_t st);
+
+cudaError_t launch_quantize(const void* x, int64_t rows, int64_t cols, float* global_scale, bool compute_global,
+                            bool blocked, uint8_t* packed, uint8_t* scales, unsigned* amax_ws, int num_sms,
+                            cudaStream_t st);
+
+cudaError_t launch_scales_to_blocked(const uint8_t* src, int64_t rows, int64_t cols, uint8_t* dst,
+                                     int num_sms, cudaStream_t st);
+
+cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, const uint8_t* xq, const uint8_t* xs,
+                           int H, int32_t* counts, int32_t* offsets, int32_t* row_offsets, int32_t* perm_to_flat,
+                           int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales, int64_t rows_capacity,
+                           int32_t* ws_rank, int32_t* ws_seg_count, int32_t* ws_seg_base, int num_sms,
+                           cudaStream_t st);
+
+cudaError_t launch_finalize(const void* y, const int32_t* flat_to_perm, const float* w, int T, int k, int H,
+                            int64_t rows_capacity, void* out, cudaStream_t st);
+
+// Reads and clears the sticky device flags of the kernels in kernels_prep.cu.
+cudaError_t prep_read_and_clear_flags(unsigned* flags);
+
+struct GemmArgs {
+  const uint8_t* a_packed;
+  const uint8_t* a_scales;
+  const float* a_gscale;
+  const int32_t* counts;
+  const int32_t* row_offsets;
+  int E;
+  int64_t rows_capacity;
+  int64_t m_total;
+  const uint8_t* w_packed;
+  const uint8_t* w_scales;
+  const float* w_gscale;
+  int N, K, epilogue;
+  const float* c_gscale;
+  void* c_out;
+  uint8_t* c_scales;
+  int tile_n;
+};
+
+// Returns 0 on success or an NVFP4MOE_ERR_* code (message via set_error_detail).
+int launch_grouped_gemm(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st);
+cudaError_t gemm_read_and_clear_flags(unsigned* flags);
+
+// Per-thread error message used by nvfp4moe_last_error_detail().
+void set_error_detail(const char* fmt, ...);
+
+}  // namespace nvfp4moe

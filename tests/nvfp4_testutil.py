@@ -1,0 +1,86 @@
+"""Test-side helpers: the blocked scale layout as a pure index map, NVFP4 code
+comparisons and the floating-point tolerances.
+
+The blocked layout (declared in include/nvfp4moe.h): rows in blocks of 128,
+K in blocks of 64 elements; block (rb, kb) is 512 bytes at
+(rb * cols/64 + kb) * 512; row r of a block keeps its 4 scales at
+(r % 32) * 16 + (r / 32) * 4.
+"""
+import numpy as np
+
+from oracle import nvfp4_moe_oracle as O
+
+# Floating-point parity bar for GEMM and layer outputs (bf16): relative
+# Frobenius error and per-element error relative to max(|ref|, rms(ref)).
+FROB_TOL = 5e-3
+ELEM_TOL = 2e-2
+
+
+def ceil_to(a, b):
+    return -(-a // b) * b
+
+
+def blocked_index(rows_pad, cols):
+    r = np.arange(rows_pad, dtype=np.int64)[:, None]
+    c = np.arange(cols // 16, dtype=np.int64)[None, :]
+    return ((r // 128) * (cols // 64) + c // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (c % 4)
+
+
+def to_blocked(scales, cols):
+    rows = scales.shape[0]
+    rp = max(ceil_to(rows, 128), 128)
+    out = np.zeros(rp * (cols // 16), dtype=np.uint8)
+    out[blocked_index(rp, cols)[:rows].ravel()] = np.asarray(scales, dtype=np.uint8).ravel()
+    return out
+
+
+def from_blocked(buf, rows, cols):
+    rp = max(ceil_to(rows, 128), 128)
+    return np.asarray(buf)[blocked_index(rp, cols)[:rows]]
+
+
+def signed_rank(codes):
+    """Position of each E2M1 code on the ordered value line (-7..7; +-0 -> 0)."""
+    c = np.asarray(codes).astype(np.int64)
+    mag = c & 7
+    return np.where((c >> 3) & 1, -mag, mag)
+
+
+def check_close(got, ref, frob_tol=FROB_TOL, elem_tol=ELEM_TOL, what="output"):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    rms = np.sqrt(np.mean(ref ** 2)) if ref.size else 0.0
+    frob = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300)
+    worst = np.max(np.abs(got - ref) / np.maximum(np.abs(ref), rms)) if ref.size else 0.0
+    assert frob <= frob_tol, f"{what}: relative Frobenius error {frob:.3e} > {frob_tol}"
+    assert worst <= elem_tol, f"{what}: worst element error {worst:.3e} > {elem_tol} (x max(|ref|, rms))"
+    return frob, worst
+
+
+def check_requant(got_codes, got_scales, ref_codes, ref_scales, max_flip_frac=0.01, min_scale_eq=0.99):
+    """Fused SwiGLU requantisation vs the oracle's: float32 accumulation order
+    may move a value across an E2M1 or ue4m3 midpoint, so codes may differ by
+    one step on a small fraction of elements and scales may differ in a
+    small fraction of blocks."""
+    eq = np.mean(np.asarray(got_scales) == np.asarray(ref_scales)) if np.size(ref_scales) else 1.0
+    assert eq >= min_scale_eq, f"only {eq:.4f} of block scales equal"
+    same_scale = np.repeat(np.asarray(got_scales) == np.asarray(ref_scales), 16, axis=-1)
+    d = np.abs(signed_rank(got_codes) - signed_rank(ref_codes))
+    d = d[same_scale]
+    assert d.size == 0 or d.max() <= 1, f"a code differs by {d.max()} steps"
+    frac = np.mean(d != 0) if d.size else 0.0
+    assert frac <= max_flip_frac, f"{frac:.4f} of codes differ by one step"
+    return eq, frac
+
+
+def oracle_quantize_experts(w_bf16):
+    """Oracle NVFP4 quantisation of bf16 expert weights [E, N, K] (CPU tensor)."""
+    ps, ss, gs = [], [], []
+    for e in range(w_bf16.shape[0]):
+        a = w_bf16[e].float().numpy()
+        g = O.global_scale(a)
+        p, s = O.quantize_nvfp4(a, g)
+        ps.append(p), ss.append(s), gs.append(g)
+    return np.stack(ps), np.stack(ss), np.array(gs, np.float32)

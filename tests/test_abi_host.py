@@ -1,0 +1,98 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads,
+exports every entry point declared in include/nvfp4moe.h, and its pure host
+functions (sizes, status strings, argument validation) behave as declared."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4moe.h")
+
+
+@pytest.fixture(scope="session")
+def lib():
+    from nvfp4_block_scaled_07_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?((?:moe|nvfp4moe)_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_layer_calls():
+    names = declared_functions()
+    for n in ["moe_route_topk", "moe_quantize_nvfp4", "moe_permute", "moe_grouped_gemm_nvfp4", "moe_finalize"]:
+        assert n in names
+    assert len(names) >= 16
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(lib):
+    lib.nvfp4moe_status_string.restype = ctypes.c_char_p
+    for s in range(8):
+        assert lib.nvfp4moe_status_string(s).decode()
+    assert lib.nvfp4moe_status_string(99).decode() == "unknown status"
+    assert lib.nvfp4moe_version() >= 10000
+
+
+def test_size_queries(lib):
+    lib.nvfp4moe_blocked_scales_bytes.restype = ctypes.c_size_t
+    lib.nvfp4moe_blocked_scales_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    assert lib.nvfp4moe_blocked_scales_bytes(1, 64) == 128 * 4
+    assert lib.nvfp4moe_blocked_scales_bytes(129, 6144) == 256 * 384
+    assert lib.nvfp4moe_blocked_scales_bytes(10, 100) == 0
+    lib.moe_permute_rows_capacity.restype = ctypes.c_int64
+    # each expert may add up to 127 padding rows; capacity is a multiple of 128
+    assert lib.moe_permute_rows_capacity(128, 256, 8) == ((1024 + 256 * 127 + 127) // 128) * 128
+    assert lib.moe_permute_rows_capacity(16, 8, 2) % 128 == 0
+    lib.moe_permute_workspace_size.restype = ctypes.c_size_t
+    assert lib.moe_permute_workspace_size(16384, 64, 8) >= 16384 * 8 * 4
+    lib.moe_quantize_nvfp4_workspace_size.restype = ctypes.c_size_t
+    lib.moe_quantize_nvfp4_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int]
+    assert lib.moe_quantize_nvfp4_workspace_size(4, 64, 0) == 0
+    assert lib.moe_quantize_nvfp4_workspace_size(4, 64, 1) >= 4
+
+
+def test_argument_validation_before_any_device_work(lib):
+    p = ctypes.c_void_p
+    lib.moe_route_topk.argtypes = [p, p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, p, p, p]
+    assert lib.moe_route_topk(None, None, 4, 2048, 2, 1, 1, None, None, None) == 2    # E > 1024
+    assert lib.moe_route_topk(None, None, 4, 8, 9, 1, 1, None, None, None) == 2       # k > E
+    assert lib.moe_route_topk(None, None, 4, 8, 2, 7, 1, None, None, None) == 1       # bad score_fn
+    assert lib.moe_route_topk(None, None, 0, 8, 2, 1, 1, None, None, None) == 0       # T = 0 is a no-op
+    g = lib.moe_grouped_gemm_nvfp4
+    g.argtypes = [p, p, p, p, p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, p, p, p, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, p, p, p, ctypes.c_int, p, ctypes.c_size_t, p]
+    dummy = p(256)
+    assert g(dummy, dummy, dummy, dummy, dummy, 8, 1024, 32, dummy, dummy, dummy, 256, 100, 0, None, dummy, None, 0,
+             None, 0, None) == 2      # K % 64 != 0
+    assert g(dummy, dummy, dummy, dummy, dummy, 8, 1024, 32, dummy, dummy, dummy, 384, 256, 1, dummy, dummy, dummy, 0,
+             None, 0, None) == 2      # SwiGLU N % 256 != 0
+    assert g(dummy, dummy, dummy, dummy, dummy, 8, 1000, 32, dummy, dummy, dummy, 256, 256, 0, None, dummy, None, 0,
+             None, 0, None) == 1      # rows_capacity % 128 != 0
+    assert g(dummy, dummy, dummy, dummy, dummy, 8, 1024, 32, dummy, dummy, dummy, 256, 256, 7, None, dummy, None, 0,
+             None, 0, None) == 1      # bad epilogue
+    assert g(dummy, dummy, dummy, dummy, dummy, 8, 1024, 32, dummy, dummy, dummy, 256, 256, 1, None, dummy, None, 0,
+             None, 0, None) == 1      # SWIGLU_NVFP4 without its scale pointers
+    q = lib.moe_quantize_nvfp4
+    q.argtypes = [p, ctypes.c_int64, ctypes.c_int64, p, ctypes.c_int, p, p, p, ctypes.c_size_t, p]
+    assert q(dummy, 4, 40, dummy, 0, dummy, dummy, None, 0, None) == 2     # cols % 16
+    assert q(dummy, 4, 96, dummy, 2, dummy, dummy, None, 0, None) == 2     # blocked needs cols % 64
+    assert q(dummy, 4, 64, dummy, 1, dummy, dummy, None, 0, None) == 4     # global amax needs workspace
+    assert q(p(8), 4, 64, dummy, 0, dummy, dummy, None, 0, None) == 1      # misaligned x
+
+
+def test_binding_imports_and_names_match_header():
+    from nvfp4_block_scaled_07_gb300 import binding
+    for n in ["moe_route_topk", "moe_quantize_nvfp4", "moe_permute", "moe_grouped_gemm_nvfp4", "moe_finalize",
+              "moe_scales_to_blocked"]:
+        assert callable(getattr(binding, n))
