@@ -190,8 +190,11 @@ int moe_permute(const int32_t* topk_idx, int T, int E, int k,
  * written by moe_permute; w_packed device uint8 [E, N, K/2]; w_scales
  * device, blocked per expert ([E] x nvfp4moe_blocked_scales_bytes(N, K));
  * w_gscale device float32 [E].
- * m_total = number of routed rows (T*k), used only to pick the tile width;
- * tile_n = 0 (auto) or the token-tile width 32, 64, 128 (and 256 for BF16).
+ * m_total = number of routed rows (T*k); informational.
+ * tile_n = the widest token tile: 0 or 128, or 256 with NVFP4MOE_EPI_BF16.
+ * Token tiles start on 128-row boundaries of an expert's rows; each tile's
+ * MMA width is the smallest of 32, 64, 128, 256 covering the rows left
+ * (capped at tile_n), so a decode expert with 4 rows runs 128 x 32 MMAs.
  * Limits: K % 64 == 0; N % 128 == 0 (BF16) or N % 256 == 0 (SwiGLU);
  * 1 <= E <= 1024; rows_capacity % 128 == 0.  A pipeline that does not fit the
  * device's opt-in shared memory is refused with NVFP4MOE_ERR_SMEM (the

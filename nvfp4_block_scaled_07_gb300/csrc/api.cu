@@ -279,8 +279,8 @@ int moe_grouped_gemm_nvfp4(const uint8_t* a_packed, const uint8_t* a_scales, con
                    NVFP4MOE_ERR_INVALID_ARG, "rows_capacity %lld must be a positive multiple of 128",
                    (long long)rows_capacity);
   NVFP4MOE_REQUIRE(m_total >= 0, NVFP4MOE_ERR_INVALID_ARG, "m_total < 0");
-  NVFP4MOE_REQUIRE(tile_n == 0 || tile_n == 32 || tile_n == 64 || tile_n == 128 || (!swiglu && tile_n == 256),
-                   NVFP4MOE_ERR_UNSUPPORTED, "tile_n %d", tile_n);
+  NVFP4MOE_REQUIRE(tile_n == 0 || tile_n == 128 || (!swiglu && tile_n == 256), NVFP4MOE_ERR_UNSUPPORTED,
+                   "tile_n %d (expected 0, 128, or 256 for the bf16 epilogue)", tile_n);
   NVFP4MOE_REQUIRE(a_packed && a_scales && a_gscale && expert_counts && row_offsets && w_packed && w_scales &&
                        w_gscale && c_out,
                    NVFP4MOE_ERR_INVALID_ARG, "null pointer");

@@ -15,9 +15,12 @@
 // uses the whole opt-in shared memory.
 //
 // Orientation ("swap AB"): the weight rows of one expert form the 128-row
-// M side, the expert's tokens form the N side (BN = 32..256).  Decode-sized
-// experts (a handful to ~64 tokens) then fill whole MMAs along M and the
-// kernel streams every weight tile from HBM exactly once.
+// M side, the expert's tokens form the N side.  Decode-sized experts (a
+// handful to ~64 tokens) then fill whole MMAs along M and the kernel
+// streams every weight tile from HBM exactly once.  Token tiles start on
+// 128-row boundaries (so every scale-factor address in tensor memory stays
+// 4-column aligned) and each tile's MMA width is the power of two >= 32 that
+// covers the expert's remaining rows, up to BN (128 or 256).
 //
 // Warp roles (192 threads, one CTA per SM, persistent):
 //   warp 0     TMA producer: weight tile(s), token tile, their scale blocks
@@ -52,6 +55,7 @@ constexpr int kBKBytes = 128;      // bytes of K per stage and row = 256 E2M1 el
 constexpr int kATile = kBM * kBKBytes;
 constexpr int kSfTile = 2048;      // 4 k64 blocks x 512-byte scale blocks
 constexpr int kTmemCols = 512;
+constexpr int kAccSlotCols = 192;  // two accumulator slots at columns 0 and 192
 constexpr int kSfColBase = 384;    // two 64-column scale-factor buffers at 384 and 448
 constexpr int kMaxStages = 8;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -74,16 +78,15 @@ struct Params {
 template <int BN, bool SWIGLU>
 struct Cfg {
   static constexpr int NA = SWIGLU ? 2 : 1;          // weight tiles per stage (gate, up)
-  static constexpr int BTile = BN * kBKBytes;
+  static constexpr int BTile = BN * kBKBytes;        // room for the widest token tile
   static constexpr int NSFB = BN > 128 ? 2 : 1;      // 128-row scale blocks per token tile
   static constexpr int OffB = NA * kATile;
   static constexpr int OffSfa = OffB + BTile;
   static constexpr int OffSfb = OffSfa + NA * kSfTile;
   static constexpr int Stage = OffSfb + NSFB * kSfTile;
-  static constexpr int AccCols = NA * BN;            // fp32 accumulator columns per tile
-  static constexpr int AccBufs = (2 * AccCols <= kSfColBase) ? 2 : 1;
   static constexpr int SfCols = NA * 16 + NSFB * 16;
-  static_assert(AccBufs * AccCols <= kSfColBase, "accumulators overlap the scale-factor columns");
+  static_assert(BN == 128 || BN == 256, "token tiles must start on 128-row scale blocks");
+  static_assert(NA * BN <= 2 * kAccSlotCols, "accumulator does not fit the two slots");
   static_assert(SfCols <= 64, "scale-factor buffer overflow");
   static_assert(Stage % 1024 == 0, "stages must stay 1024-byte aligned for the 128B swizzle");
 };
@@ -116,8 +119,10 @@ __device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Tile t -> expert e, M tile mb, N tile nb and the tile's MMA width w: the
+// smallest power of two >= 32 covering the rows left, capped at BN.
 __device__ __forceinline__ void decode_tile(int t, const int* s_prefix, const int* s_count, int E, int BN, int& e,
-                                            int& mb, int& nb) {
+                                            int& mb, int& nb, int& w) {
   int lo = 0, hi = E - 1;  // largest e with s_prefix[e] <= t (has >= 1 tile)
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -129,7 +134,34 @@ __device__ __forceinline__ void decode_tile(int t, const int* s_prefix, const in
   const int local = t - s_prefix[e];
   mb = local / ntn;
   nb = local - mb * ntn;
+  const int rem = s_count[e] - nb * BN;
+  w = 32;
+  while (w < rem && w < BN) w <<= 1;
 }
+
+// Accumulator slots of one tile: a tile whose accumulator fits 192 columns
+// takes the next slot (alternating), a wider one takes both, starting at 0.
+// Producer (MMA) and consumer (epilogue) walk the same sequence.
+struct SlotSeq {
+  uint32_t use0 = 0u, use1 = 0u;  // completed uses per slot (phase parity source)
+  int next = 0;
+  __device__ __forceinline__ uint32_t parity(int slot) const { return (slot ? use1 : use0) & 1u; }
+  __device__ __forceinline__ void pick(int cols, int& s0, int& s1) {
+    if (cols <= kAccSlotCols) {
+      s0 = next;
+      s1 = -1;
+      next ^= 1;
+    } else {
+      s0 = 0;
+      s1 = 1;
+      next = 0;
+    }
+  }
+  __device__ __forceinline__ void done(int s0, int s1) {
+    if (s0 == 0 || s1 == 0) ++use0;
+    if (s0 == 1 || s1 == 1) ++use1;
+  }
+};
 
 template <int BN, bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -222,11 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-      int e, mb, nb;
-      decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb);
+      int e, mb, nb, w;
+      decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
       const int arow = s_rowoff[e] + nb * BN;
-      const int valid = s_count[e] - nb * BN;
-      const int sfb_chunks = (C::NSFB == 2 && valid <= 128) ? 1 : C::NSFB;
+      const int sfb_chunks = w > 128 ? 2 : 1;
       const int wrow0 = e * p.N + mb * kBM;
       for (int kt = 0; kt < nkt; ++kt, ++it) {
         const uint32_t s = it % uint32_t(S), ph = (it / uint32_t(S)) & 1u;
@@ -235,13 +266,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const int nkb = min(4, kblocks - 4 * kt);
-        const uint32_t bytes = uint32_t(C::NA * kATile + C::BTile + (C::NA + sfb_chunks) * nkb * 512);
+        const uint32_t bytes = uint32_t(C::NA * kATile + w * kBKBytes + (C::NA + sfb_chunks) * nkb * 512);
         ptx::mbar_arrive_expect_tx(full_bar(s), bytes);
         const uint32_t st = smem_base + s * uint32_t(C::Stage);
 #pragma unroll
         for (int j = 0; j < C::NA; ++j)
           ptx::tma_load_2d(st + j * kATile, &tmap_w, full_bar(s), kt * kBKBytes, wrow0 + j * (p.N / 2), pol_w);
-        ptx::tma_load_2d(st + C::OffB, &tmap_a, full_bar(s), kt * kBKBytes, arow, pol_a);
+        for (int r = 0; r < w; r += 32)  // the token tile in 32-row boxes
+          ptx::tma_load_2d(st + C::OffB + r * kBKBytes, &tmap_a, full_bar(s), kt * kBKBytes, arow + r, pol_a);
 #pragma unroll
         for (int j = 0; j < C::NA; ++j) {
           const int rb = SWIGLU ? (j * (p.N / 2) + mb * kBM) / kBM : mb;
@@ -261,20 +293,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
-    constexpr uint32_t idesc = ptx::idesc_nvfp4(kBM, BN);
     uint32_t it = 0;
-    int tile_i = 0;
+    SlotSeq slots;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++tile_i) {
-      int e, mb, nb;
-      decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb);
-      const int buf = C::AccBufs == 2 ? (tile_i & 1) : 0;
-      const uint32_t acc_ph = uint32_t(C::AccBufs == 2 ? (tile_i >> 1) : tile_i) & 1u;
-      if (!wait_phase(acce_bar(buf), acc_ph ^ 1u, abort_flag)) break;
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+      int e, mb, nb, w;
+      decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
+      int s0, s1;
+      slots.pick(C::NA * w, s0, s1);
+      if (!wait_phase(acce_bar(s0), slots.parity(s0) ^ 1u, abort_flag)) break;
+      if (s1 >= 0 && !wait_phase(acce_bar(s1), slots.parity(s1) ^ 1u, abort_flag)) break;
       ptx::tc_fence_after();
-      const uint32_t d0 = tmem + uint32_t(buf * C::AccCols);
-      // A token tile narrower than 128 rows sits inside a 128-row scale block.
-      const uint32_t sfb_sub = BN < 128 ? uint32_t(((nb * BN) & 127) >> 5) : 0u;
+      const uint32_t idesc = ptx::idesc_nvfp4(kBM, w);
+      const int sfb_chunks = w > 128 ? 2 : 1;
+      const uint32_t d0 = tmem + uint32_t(s0 * kAccSlotCols);
       for (int kt = 0; kt < nkt; ++kt, ++it) {
         const uint32_t s = it % uint32_t(S), ph = (it / uint32_t(S)) & 1u;
         if (!wait_phase(full_bar(s), ph, abort_flag)) {
@@ -285,12 +317,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = smem_base + s * uint32_t(C::Stage);
         const uint32_t sf = tmem + uint32_t(kSfColBase + (it & 1u) * 64);
         const int nkb = min(4, kblocks - 4 * kt);
+        // Scale factors: every address below is a multiple of 4 columns.
         for (int kb = 0; kb < nkb; ++kb) {
 #pragma unroll
           for (int j = 0; j < C::NA; ++j)
             ptx::tc_cp_32x128b_x4(sf + j * 16 + kb * 4, ptx::desc_sf_block(st + C::OffSfa + j * kSfTile + kb * 512));
-#pragma unroll
-          for (int c = 0; c < C::NSFB; ++c)
+          for (int c = 0; c < sfb_chunks; ++c)
             ptx::tc_cp_32x128b_x4(sf + C::NA * 16 + kb * 4 * C::NSFB + c * 4,
                                   ptx::desc_sf_block(st + C::OffSfb + c * kSfTile + kb * 512));
         }
@@ -299,14 +331,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < C::NA; ++j) {
             const uint64_t adesc = ptx::desc_kmajor_sw128(st + j * kATile);
-            ptx::tc_mma_nvfp4(d0 + j * BN, adesc + 2 * kb, bdesc + 2 * kb, idesc, sf + j * 16 + kb * 4,
-                              sf + C::NA * 16 + kb * 4 * C::NSFB + sfb_sub, (kt | kb) != 0 ? 1u : 0u);
+            ptx::tc_mma_nvfp4(d0 + j * w, adesc + 2 * kb, bdesc + 2 * kb, idesc, sf + j * 16 + kb * 4,
+                              sf + C::NA * 16 + kb * 4 * C::NSFB, (kt | kb) != 0 ? 1u : 0u);
           }
         }
         ptx::tc_commit(empty_bar(s));  // frees the stage once these MMAs have read it
       }
       if (!ok) break;
-      ptx::tc_commit(accf_bar(buf));
+      ptx::tc_commit(accf_bar(s0));
+      if (s1 >= 0) ptx::tc_commit(accf_bar(s1));
+      slots.done(s0, s1);
     }
     ptx::tc_commit(drain_bar);  // every MMA of this CTA done before tensor memory is freed
     drain_phase(drain_bar, 0);
@@ -318,25 +352,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool f32_out = p.epi == NVFP4MOE_EPI_SWIGLU_F32;
     const float s_h = (SWIGLU && !f32_out) ? *p.c_gscale : 1.0f;
     const int n_out = SWIGLU ? p.N / 2 : p.N;
-    int tile_i = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++tile_i) {
-      int e, mb, nb;
-      decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb);
-      const int buf = C::AccBufs == 2 ? (tile_i & 1) : 0;
-      const uint32_t acc_ph = uint32_t(C::AccBufs == 2 ? (tile_i >> 1) : tile_i) & 1u;
-      if (!wait_phase(accf_bar(buf), acc_ph, abort_flag)) break;
+    SlotSeq slots;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      int e, mb, nb, w;
+      decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
+      int s0, s1;
+      slots.pick(C::NA * w, s0, s1);
+      if (!wait_phase(accf_bar(s0), slots.parity(s0), abort_flag)) break;
+      if (s1 >= 0 && !wait_phase(accf_bar(s1), slots.parity(s1), abort_flag)) break;
       ptx::tc_fence_after();
-      const int valid = min(BN, s_count[e] - nb * BN);
+      const int valid = min(w, s_count[e] - nb * BN);
       const int64_t row0 = int64_t(s_rowoff[e]) + int64_t(nb) * BN;
       const float scale = a_gs * p.w_gscale[e];
-      const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + uint32_t(buf * C::AccCols);
+      const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + uint32_t(s0 * kAccSlotCols);
       const int f = mb * kBM + lrow;  // output column
       for (int c0 = 0; c0 < valid; c0 += 32) {
         uint32_t g[32];
         ptx::tmem_ld_32x32b_x32(tbase + c0, g);
         if constexpr (SWIGLU) {
           uint32_t u[32];
-          ptx::tmem_ld_32x32b_x32(tbase + BN + c0, u);
+          ptx::tmem_ld_32x32b_x32(tbase + w + c0, u);
           ptx::tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -376,7 +411,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(acce_bar(buf));
+      if (lane == 0) {
+        ptx::mbar_arrive(acce_bar(s0));
+        if (s1 >= 0) ptx::mbar_arrive(acce_bar(s1));
+      }
+      slots.done(s0, s1);
     }
   }
 
@@ -435,7 +474,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   const size_t smem = fixed + size_t(stages) * C::Stage;
   CUtensorMap tw, ta;
   if (!encode_kmajor_map(&tw, a.w_packed, int64_t(a.E) * a.N, a.K / 2, kBM) ||
-      !encode_kmajor_map(&ta, a.a_packed, a.rows_capacity, a.K / 2, BN)) {
+      !encode_kmajor_map(&ta, a.a_packed, a.rows_capacity, a.K / 2, 32)) {
     set_error_detail("cuTensorMapEncodeTiled failed or is unavailable");
     return NVFP4MOE_ERR_CUDA;
   }
@@ -474,27 +513,10 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
 
 int launch_grouped_gemm(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st) {
   const bool swiglu = a.epilogue != NVFP4MOE_EPI_BF16;
-  int bn = a.tile_n;
-  if (bn == 0) {
-    const int64_t avg = (a.m_total + a.E - 1) / a.E;
-    bn = avg <= 16 ? 32 : avg <= 48 ? 64 : 128;
-  }
-  if (swiglu) {
-    switch (bn) {
-      case 32: return launch_impl<32, true>(a, num_sms, smem_optin, st);
-      case 64: return launch_impl<64, true>(a, num_sms, smem_optin, st);
-      case 128: return launch_impl<128, true>(a, num_sms, smem_optin, st);
-      default: break;
-    }
-  } else {
-    switch (bn) {
-      case 32: return launch_impl<32, false>(a, num_sms, smem_optin, st);
-      case 64: return launch_impl<64, false>(a, num_sms, smem_optin, st);
-      case 128: return launch_impl<128, false>(a, num_sms, smem_optin, st);
-      case 256: return launch_impl<256, false>(a, num_sms, smem_optin, st);
-      default: break;
-    }
-  }
+  const int bn = a.tile_n == 0 ? 128 : a.tile_n;
+  if (swiglu && bn == 128) return launch_impl<128, true>(a, num_sms, smem_optin, st);
+  if (!swiglu && bn == 128) return launch_impl<128, false>(a, num_sms, smem_optin, st);
+  if (!swiglu && bn == 256) return launch_impl<256, false>(a, num_sms, smem_optin, st);
   set_error_detail("tile_n %d is not supported for this epilogue", a.tile_n);
   return NVFP4MOE_ERR_UNSUPPORTED;
 }

@@ -221,14 +221,15 @@ def gemm_case(E, N, K, counts, seed):
 
 
 GEMM_SHAPES = [
-    # E, N, K, counts, tile_n
-    (3, 256, 256, [5, 0, 40], 32),
-    (4, 384, 448, [1, 33, 64, 129], 64),        # partial last K tile, 3 M tiles
-    (2, 128, 128, [7, 200], 128),               # K below one stage
-    (2, 256, 1024, [300, 17], 256),             # 256-wide token tiles, a one-block tail
+    # E, N, K, counts, tile_n (widest token tile); tile widths follow the counts
+    (3, 256, 256, [5, 0, 40], 0),                 # widths 32 and 64
+    (4, 384, 448, [1, 33, 64, 129], 0),           # partial last K tile, 3 M tiles, 128 + 32
+    (2, 128, 128, [7, 200], 128),                 # K below one stage
+    (2, 256, 1024, [300, 17], 256),               # a 256-wide tile, a one-block tail
     (5, 128, 64, [3, 3, 3, 3, 3], 0),
-    (2, 512, 2048, [64, 64], 64),
-    (8, 256, 768, [0, 1, 2, 3, 130, 0, 31, 257], 32),
+    (2, 512, 2048, [64, 64], 0),
+    (8, 256, 768, [0, 1, 2, 3, 130, 0, 31, 257], 0),
+    (3, 128, 512, [256, 129, 96], 256),           # 256, 128 + 32 ... under the 256 cap
 ]
 
 
@@ -245,9 +246,9 @@ def test_grouped_gemm_bf16(B, E, N, K, counts, tile_n):
 
 SWIGLU_SHAPES = [
     # E, I, K, counts, tile_n
-    (3, 128, 512, [9, 70, 0], 32),
-    (2, 256, 320, [130, 1], 64),
-    (4, 128, 1024, [128, 5, 64, 200], 128),
+    (3, 128, 512, [9, 70, 0], 0),                 # one single-slot and one double-slot tile
+    (2, 256, 320, [130, 1], 0),
+    (4, 128, 1024, [128, 5, 64, 200], 128),       # slot sequence mixes 32/64/128-wide tiles
     (2, 384, 256, [40, 41], 0),
 ]
 
