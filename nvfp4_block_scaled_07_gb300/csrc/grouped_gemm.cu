@@ -55,7 +55,7 @@ constexpr int kBKBytes = 128;      // bytes of K per stage and row = 256 E2M1 el
 constexpr int kATile = kBM * kBKBytes;
 constexpr int kSfTile = 2048;      // 4 k64 blocks x 512-byte scale blocks
 constexpr int kTmemCols = 512;
-constexpr int kAccSlotCols = 192;  // two accumulator slots at columns 0 and 192
+constexpr int kAccSlotCols = 128;  // two accumulator slots at columns 0 and 128
 constexpr int kSfColBase = 384;    // two 64-column scale-factor buffers at 384 and 448
 constexpr int kMaxStages = 8;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -139,7 +139,7 @@ __device__ __forceinline__ void decode_tile(int t, const int* s_prefix, const in
   while (w < rem && w < BN) w <<= 1;
 }
 
-// Accumulator slots of one tile: a tile whose accumulator fits 192 columns
+// Accumulator slots of one tile: a tile whose accumulator fits 128 columns
 // takes the next slot (alternating), a wider one takes both, starting at 0.
 // Producer (MMA) and consumer (epilogue) walk the same sequence.
 struct SlotSeq {
