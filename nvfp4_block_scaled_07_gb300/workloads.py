@@ -66,7 +66,7 @@ WORKLOADS = {
 # several tiles per expert, ragged expert sizes and a partial K tile.
 TEST_WORKLOADS = {
     "ragged_small": Workload("ragged_small", T=96, E=8, k=2, H=512, I=384, score="sigmoid"),
-    "many_experts": Workload("many_experts", T=64, E=32, k=4, H=320, I=256, score="sigmoid"),
+    "many_experts": Workload("many_experts", T=64, E=32, k=4, H=384, I=256, score="sigmoid"),
     "wide_experts": Workload("wide_experts", T=300, E=4, k=2, H=1024, I=256, score="softmax"),
     "zipf_small": Workload("zipf_small", T=256, E=16, k=4, H=384, I=128, score="sigmoid", zipf_s=1.1),
 }
