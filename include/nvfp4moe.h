@@ -170,6 +170,30 @@ int moe_permute(const int32_t* topk_idx, int T, int E, int k,
                 uint8_t* a_packed, uint8_t* a_scales,
                 void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* moe_permute without a workspace argument.  No counterpart on the source
+ * pages: it exists for callers that cannot allocate device memory when they
+ * call -- code running inside a fixed device-memory arena it may not grow,
+ * plugins or foreign-function callers that are handed tensors but no
+ * allocator, and hot loops where any cudaMalloc/cudaFree (which can
+ * synchronise the device) is not acceptable.
+ * Same arguments, outputs and limits as moe_permute, minus ws/ws_bytes.  The
+ * scratch is a 1 MiB array inside the library (a file-scope device array,
+ * resident on every GPU that loads the library until the process exits):
+ * at most 131072 routed rows (T*k) and 65536 segment-expert counters
+ * (ceil(T*k/1024) * E); larger calls return NVFP4MOE_ERR_UNSUPPORTED
+ * without launching.  Nothing is allocated or freed.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call shares the one array and overwrites
+ * the part it uses, so no state carries over between calls, but calls whose
+ * work overlaps on the GPU (other streams, other host threads) race on it:
+ * serialise them. */
+int moe_permute_no_alloc(const int32_t* topk_idx, int T, int E, int k,
+                         const uint8_t* xq, const uint8_t* xs, int H,
+                         int32_t* expert_counts, int32_t* expert_offsets, int32_t* row_offsets,
+                         int32_t* perm_to_flat, int32_t* flat_to_perm,
+                         uint8_t* a_packed, uint8_t* a_scales, cudaStream_t stream);
+
 /* ---- a4/a5: grouped GEMM ---------------------------------------------------
  * The grouped ("array") block-scaled GEMM over experts (page C, Context and
  * the sm120_mma_array_tma_blockwise_scaling collective it finds; page A,

@@ -48,6 +48,7 @@ _SIGS = {
     "moe_permute_rows_capacity": (_i64, [_i, _i, _i]),
     "moe_permute_workspace_size": (_sz, [_i, _i, _i]),
     "moe_permute": (_i, [_p, _i, _i, _i, _p, _p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
+    "moe_permute_no_alloc": (_i, [_p, _i, _i, _i, _p, _p, _i, _p, _p, _p, _p, _p, _p, _p, _p]),
     "moe_grouped_gemm_nvfp4_workspace_size": (_sz, [_i, _i, _i, _i]),
     "moe_grouped_gemm_nvfp4": (_i, [_p, _p, _p, _p, _p, _i, _i64, _i64, _p, _p, _p, _i, _i, _i, _p, _p, _p, _i,
                                     _p, _sz, _p]),
@@ -234,6 +235,25 @@ def moe_permute(topk_idx, E, xq, xs, out: Permutation = None, workspace=None):
                             _ptr(out.row_offsets), _ptr(out.perm_to_flat), _ptr(out.flat_to_perm),
                             _ptr(out.a_packed), _ptr(out.a_scales), _ptr(workspace), workspace.numel(), _stream()),
            "moe_permute")
+    return out
+
+
+def moe_permute_no_alloc(topk_idx, E, xq, xs, out: Permutation = None):
+    """moe_permute on the library's own scratch (no workspace argument).
+
+    For callers that cannot allocate device memory at call time; the C call
+    allocates nothing (pass `out` to make the whole call allocation-free)."""
+    _need(topk_idx, torch.int32, name="topk_idx")
+    T, k = topk_idx.shape
+    H = xq.shape[1] * 2
+    _need(xq, torch.uint8, (T, H // 2), "xq")
+    _need(xs, torch.uint8, (T, H // 16), "xs")
+    if out is None:
+        out = alloc_permutation(T, E, k, H, topk_idx.device)
+    _check(_lib.moe_permute_no_alloc(_ptr(topk_idx), T, E, k, _ptr(xq), _ptr(xs), H, _ptr(out.counts),
+                                     _ptr(out.offsets), _ptr(out.row_offsets), _ptr(out.perm_to_flat),
+                                     _ptr(out.flat_to_perm), _ptr(out.a_packed), _ptr(out.a_scales), _stream()),
+           "moe_permute_no_alloc")
     return out
 
 

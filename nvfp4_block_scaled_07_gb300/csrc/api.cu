@@ -249,6 +249,37 @@ int moe_permute(const int32_t* topk_idx, int T, int E, int k, const uint8_t* xq,
                      "permute launch");
 }
 
+int moe_permute_no_alloc(const int32_t* topk_idx, int T, int E, int k, const uint8_t* xq, const uint8_t* xs, int H,
+                         int32_t* expert_counts, int32_t* expert_offsets, int32_t* row_offsets,
+                         int32_t* perm_to_flat, int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales,
+                         cudaStream_t stream) {
+  t_detail[0] = 0;
+  NVFP4MOE_REQUIRE(T >= 0, NVFP4MOE_ERR_INVALID_ARG, "T = %d", T);
+  NVFP4MOE_REQUIRE(E >= 1 && E <= 1024, NVFP4MOE_ERR_UNSUPPORTED, "E = %d outside [1, 1024]", E);
+  NVFP4MOE_REQUIRE(k >= 1 && k <= E, NVFP4MOE_ERR_UNSUPPORTED, "k = %d outside [1, E]", k);
+  NVFP4MOE_REQUIRE(H > 0 && H % 64 == 0, NVFP4MOE_ERR_UNSUPPORTED, "H = %d must be a positive multiple of 64", H);
+  const int64_t R = int64_t(T) * k;
+  const int64_t seg_experts = ceil_div(R, kPermuteSegment) * E;
+  NVFP4MOE_REQUIRE(R <= kNoAllocMaxRoutedRows && seg_experts <= kNoAllocMaxSegmentExperts, NVFP4MOE_ERR_UNSUPPORTED,
+                   "T*k = %lld routed rows and %lld segment-expert counters exceed the library's static scratch "
+                   "(at most %lld routed rows and %lld counters); use moe_permute with a workspace",
+                   (long long)R, (long long)seg_experts, (long long)kNoAllocMaxRoutedRows,
+                   (long long)kNoAllocMaxSegmentExperts);
+  NVFP4MOE_REQUIRE(expert_counts && expert_offsets && row_offsets && perm_to_flat, NVFP4MOE_ERR_INVALID_ARG,
+                   "null pointer");
+  NVFP4MOE_REQUIRE(T == 0 || (topk_idx && xq && xs && flat_to_perm && a_packed && a_scales),
+                   NVFP4MOE_ERR_INVALID_ARG, "null pointer");
+  NVFP4MOE_REQUIRE(T == 0 || (aligned16(xq) && aligned16(a_packed) && aligned16(a_scales) &&
+                              (reinterpret_cast<uintptr_t>(xs) & 3) == 0),
+                   NVFP4MOE_ERR_INVALID_ARG, "misaligned pointer");
+  DeviceInfo d;
+  if (int st = current_device(&d)) return st;
+  return cuda_status(launch_permute_static_scratch(topk_idx, T, E, k, xq, xs, H, expert_counts, expert_offsets,
+                                                   row_offsets, perm_to_flat, flat_to_perm, a_packed, a_scales,
+                                                   moe_permute_rows_capacity(T, E, k), d.num_sms, stream),
+                     "permute (static scratch) launch");
+}
+
 // ---- a4/a5 ------------------------------------------------------------------
 size_t moe_grouped_gemm_nvfp4_workspace_size(int E, int N, int K, int epilogue) {
   (void)E;

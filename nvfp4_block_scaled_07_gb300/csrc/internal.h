@@ -32,6 +32,17 @@ cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, const u
                            int32_t* ws_rank, int32_t* ws_seg_count, int32_t* ws_seg_base, int num_sms,
                            cudaStream_t st);
 
+// Limits of the permutation that runs on library-owned scratch: routed rows
+// (T*k) and per-segment expert counters (ceil(T*k/1024) * E).
+constexpr int64_t kNoAllocMaxRoutedRows = 131072;
+constexpr int64_t kNoAllocMaxSegmentExperts = 65536;
+
+cudaError_t launch_permute_static_scratch(const int32_t* topk_idx, int T, int E, int k, const uint8_t* xq,
+                                          const uint8_t* xs, int H, int32_t* counts, int32_t* offsets,
+                                          int32_t* row_offsets, int32_t* perm_to_flat, int32_t* flat_to_perm,
+                                          uint8_t* a_packed, uint8_t* a_scales, int64_t rows_capacity, int num_sms,
+                                          cudaStream_t st);
+
 cudaError_t launch_finalize(const void* y, const int32_t* flat_to_perm, const float* w, int T, int k, int H,
                             int64_t rows_capacity, void* out, cudaStream_t st);
 

@@ -6,6 +6,7 @@
 #include <cfloat>
 #include <climits>
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -466,6 +467,48 @@ cudaError_t launch_finalize(const void* y, const int32_t* flat_to_perm, const fl
   finalize_kernel<<<grid, block, 0, st>>>(static_cast<const uint4*>(y), flat_to_perm, w, T, k, H, rows_capacity,
                                           static_cast<uint4*>(out));
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Permutation with library-owned scratch, for callers that cannot allocate
+// device memory at call time.  The scratch is one file-scope device array,
+// present on every GPU that loads the library until the process exits.
+// Host code may not use the array's name as a device address, so its
+// address is looked up once per device with cudaGetSymbolAddress.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocMaxRoutedRows + 2 * kNoAllocMaxSegmentExperts];
+
+namespace {
+constexpr int kScratchDevices = 64;
+std::mutex g_scratch_mutex;
+int32_t* g_scratch_addr[kScratchDevices] = {};
+}  // namespace
+
+cudaError_t launch_permute_static_scratch(const int32_t* topk_idx, int T, int E, int k, const uint8_t* xq,
+                                          const uint8_t* xs, int H, int32_t* counts, int32_t* offsets,
+                                          int32_t* row_offsets, int32_t* perm_to_flat, int32_t* flat_to_perm,
+                                          uint8_t* a_packed, uint8_t* a_scales, int64_t rows_capacity, int num_sms,
+                                          cudaStream_t st) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kScratchDevices) return cudaErrorInvalidDevice;
+  int32_t* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+      void* p = nullptr;
+      err = cudaGetSymbolAddress(&p, g_permute_scratch);  // device `dev` is current here
+      if (err != cudaSuccess) return err;
+      g_scratch_addr[dev] = static_cast<int32_t*>(p);
+    }
+    base = g_scratch_addr[dev];
+  }
+  int32_t* rank = base;
+  int32_t* seg_count = rank + kNoAllocMaxRoutedRows;
+  int32_t* seg_base = seg_count + kNoAllocMaxSegmentExperts;
+  return launch_permute(topk_idx, T, E, k, xq, xs, H, counts, offsets, row_offsets, perm_to_flat, flat_to_perm,
+                        a_packed, a_scales, rows_capacity, rank, seg_count, seg_base, num_sms, st);
 }
 
 cudaError_t prep_read_and_clear_flags(unsigned* flags) {
