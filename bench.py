@@ -364,7 +364,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS) + sorted(W.PROFILE_WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--tile-gate-up", type=int, default=0)
     ap.add_argument("--tile-down", type=int, default=0)
@@ -373,7 +373,7 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    w = W.WORKLOADS[args.workload]
+    w = {**W.WORKLOADS, **W.PROFILE_WORKLOADS}[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
     else:

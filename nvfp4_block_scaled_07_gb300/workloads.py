@@ -62,6 +62,14 @@ WORKLOADS = {
     "prefill_t16384": Workload("prefill_t16384", T=16384, E=64, k=8, H=7168, I=4096, score="sigmoid"),
 }
 
+# A small decode-regime layer for profiler captures: the decode shape with
+# 16 experts (~4 rows each, 340 MB of NVFP4 weights: larger than L2, small
+# enough for multi-pass counter collection).
+PROFILE_WORKLOADS = {
+    "profile_decode_e16": Workload("profile_decode_e16", T=8, E=16, k=8, H=6144, I=2048, score="sigmoid"),
+    "profile_prefill_e8": Workload("profile_prefill_e8", T=2048, E=8, k=8, H=7168, I=4096, score="sigmoid"),
+}
+
 # Medium shapes that the oracle finishes in seconds but that still span
 # several tiles per expert, ragged expert sizes and a partial K tile.
 TEST_WORKLOADS = {
@@ -155,6 +163,6 @@ def ceil_div(a, b):
     return -(-a // b)
 
 
-__all__ = ["Workload", "WORKLOADS", "TEST_WORKLOADS", "host_inputs", "device_inputs",
+__all__ = ["Workload", "WORKLOADS", "PROFILE_WORKLOADS", "TEST_WORKLOADS", "host_inputs", "device_inputs",
            "random_nvfp4_operand", "random_routing", "zipf_bias", "algorithmic_flops",
            "nvfp4_bytes", "ceil_div"]
