@@ -68,12 +68,21 @@ def barrier(world):
 
 
 def max_over_ranks(v, world):
+    """The slowest rank's value: every rank's timed region must end before
+    the job's does."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank, world, ms_per_step):
+    """Whole-job rate: the units every replica processed in one step over the
+    slowest rank's step time."""
+    return units_per_rank * world / (ms_per_step * 1e-3)
 
 
 # ----------------------------------------------------------------------------
@@ -226,7 +235,7 @@ def run_ours(args, w):
     flops = W.algorithmic_flops(w)
     w_bytes_active = n_active * W.nvfp4_bytes(3 * w.H * w.I)
     alg_bytes = w_bytes_active + 2 * w.T * w.H * 2
-    tokens_s = w.T * world / (ms_step * 1e-3)
+    tokens_s = job_throughput(w.T, world, ms_step)
     gu_ms = kern_ms[3]
     gu_bytes = n_active * W.nvfp4_bytes(2 * w.I * w.H) + W.nvfp4_bytes(R * w.H) + W.nvfp4_bytes(R * w.I)
     gu_flops = 4.0 * R * w.H * w.I
@@ -253,7 +262,7 @@ def run_ours(args, w):
                      "peak": round(peak, 1), "unit": unit, "frac": round(achieved / peak, 4), "traffic": None,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if bound == "hbm" else
                      f"{peak_kind} bf16 x {FP4_OVER_BF16:g} nominal fp4/bf16 ratio"},
-        "e2e": {"value": round(w.T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_throughput(w.T, world, e2e_ms), 1), "unit": "tokens/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clk.summary(),
         "gpu_launches": B.MoELayer.LAUNCHES_PER_FORWARD * args.steps,
