@@ -22,11 +22,13 @@
 // 4-column aligned) and each tile's MMA width is the power of two >= 32 that
 // covers the expert's remaining rows, up to BN (128 or 256).
 //
-// Warp roles (192 threads, one CTA per SM, persistent):
+// Warp roles (320 threads, one CTA per SM, persistent):
 //   warp 0     TMA producer: weight tile(s), token tile, their scale blocks
 //   warp 1     tensor-memory owner and MMA issuer (one elected lane)
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator, scaling, SwiGLU,
 //              requantisation or bf16 conversion, global stores
+//   warps 6-9  scale factors: shared memory -> tensor memory (tcgen05.st)
+//              into a ring of slots the MMAs read their block scales from
 // Tiles are (expert, M tile, N tile) with N innermost, striped over the
 // CTAs, so the CTAs working at the same time share a weight tile through L2.
 //
@@ -37,6 +39,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 
 #include "../../include/nvfp4moe.h"
@@ -49,15 +52,19 @@ namespace {
 
 __device__ unsigned g_gemm_flags = 0;
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kBM = 128;           // MMA M (weight rows per tile)
 constexpr int kBKBytes = 128;      // bytes of K per stage and row = 256 E2M1 elements
 constexpr int kATile = kBM * kBKBytes;
 constexpr int kSfTile = 2048;      // 4 k64 blocks x 512-byte scale blocks
 constexpr int kTmemCols = 512;
 constexpr int kAccSlotCols = 128;  // two accumulator slots at columns 0 and 128
-constexpr int kSfColBase = 384;    // two 64-column scale-factor buffers at 384 and 448
-constexpr int kMaxStages = 8;
+constexpr int kSfColBase = 256;    // scale-factor ring: columns 256..511
+constexpr int kSfRingCols = 256;
+constexpr int kMaxSfSlots = 8;
+constexpr int kMaxStages = 16;
+// mbarriers: full/empty per stage, acc full/empty per slot, drain, sf full/empty per ring slot
+constexpr int kNumBars = 2 * kMaxStages + 5 + 2 * kMaxSfSlots;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
@@ -71,28 +78,34 @@ struct Params {
   const float* c_gscale;
   void* c_out;
   uint8_t* c_scales;
-  int E, N, K, epi, stages;
+  int E, N, K, epi;
+  int smem_bytes;   // dynamic shared memory of the launch (after 1024-byte alignment slack)
+  int stage_cap;    // most pipeline stages to use (2..kMaxStages)
   int64_t rows_cap;
 };
 
 template <int BN, bool SWIGLU>
 struct Cfg {
   static constexpr int NA = SWIGLU ? 2 : 1;          // weight tiles per stage (gate, up)
-  static constexpr int BTile = BN * kBKBytes;        // room for the widest token tile
   static constexpr int NSFB = BN > 128 ? 2 : 1;      // 128-row scale blocks per token tile
-  static constexpr int OffB = NA * kATile;
-  static constexpr int OffSfa = OffB + BTile;
-  static constexpr int OffSfb = OffSfa + NA * kSfTile;
-  static constexpr int Stage = OffSfb + NSFB * kSfTile;
-  static constexpr int SfCols = NA * 16 + NSFB * 16;
+  static constexpr int SfCols = NA * 16 + NSFB * 16;  // tensor-memory columns of one stage's scales
+  static constexpr int SfSlots = kSfRingCols / SfCols < kMaxSfSlots ? kSfRingCols / SfCols : kMaxSfSlots;
   static_assert(BN == 128 || BN == 256, "token tiles must start on 128-row scale blocks");
   static_assert(NA * BN <= 2 * kAccSlotCols, "accumulator does not fit the two slots");
   static_assert(SfCols <= 64, "scale-factor buffer overflow");
-  static_assert(Stage % 1024 == 0, "stages must stay 1024-byte aligned for the 128B swizzle");
+  // Bytes of one pipeline stage when the widest token tile is `wmax` rows:
+  // weight tile(s), token tile, their scale blocks; a multiple of 2048, so
+  // every stage and every tile in it stays 1024-byte aligned (128B swizzle).
+  __host__ __device__ static constexpr int stage_bytes(int wmax) {
+    return NA * kATile + wmax * kBKBytes + NA * kSfTile + (wmax > 128 ? 2 : 1) * kSfTile;
+  }
 };
 
-size_t ctrl_bytes(int E) {
-  return size_t(2 * kMaxStages + 5) * 8 + 16 + (3 * size_t(E) + 1) * 4;
+// Control block at the start of shared memory: mbarriers, the tensor-memory
+// address, flags and the per-expert tile scan; stages start after it on a
+// 1024-byte boundary.
+__host__ __device__ constexpr int ctrl_bytes(int E) {
+  return (kNumBars * 8 + 16 + (3 * E + 1) * 4 + 1023) / 1024 * 1024;
 }
 
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -170,27 +183,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<BN, SWIGLU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int S = p.stages;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(S) * C::Stage);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_wmax = reinterpret_cast<int*>(tmem_slot + 2);
   int* s_prefix = reinterpret_cast<int*>(tmem_slot + 4);
   int* s_count = s_prefix + p.E + 1;
   int* s_rowoff = s_count + p.E;
+  const int ctrl = ctrl_bytes(p.E);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t smem_base = ptx::smem_u32(smem);
   const uint32_t bar0 = ptx::smem_u32(bars);
-  // full[s] = bar0 + 8s, empty[s] = bar0 + 8(S+s), acc_full[b], acc_empty[b], drain
+  // full[s] = bar0 + 8s, empty[s] = bar0 + 8(kMaxStages+s), acc_full[b], acc_empty[b], drain
   auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (uint32_t(S) + s); };
-  auto accf_bar = [&](int b) { return bar0 + 8u * uint32_t(2 * S + b); };
-  auto acce_bar = [&](int b) { return bar0 + 8u * uint32_t(2 * S + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * uint32_t(2 * S + 4);
+  auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (uint32_t(kMaxStages) + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * uint32_t(2 * kMaxStages + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * uint32_t(2 * kMaxStages + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * uint32_t(2 * kMaxStages + 4);
+  auto sff_bar = [&](uint32_t r) { return bar0 + 8u * (uint32_t(2 * kMaxStages + 5) + r); };
+  auto sfe_bar = [&](uint32_t r) { return bar0 + 8u * (uint32_t(2 * kMaxStages + 5 + kMaxSfSlots) + r); };
 
   const int MT = (SWIGLU ? p.N / 2 : p.N) / kBM;  // M tiles per expert
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < kMaxStages; ++s) {
       ptx::mbar_init(full_bar(s), 1);
       ptx::mbar_init(empty_bar(s), 1);
     }
@@ -199,6 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(acce_bar(b), 4);
     }
     ptx::mbar_init(drain_bar, 1);
+    for (int r = 0; r < kMaxSfSlots; ++r) {
+      ptx::mbar_init(sff_bar(r), 4);  // one arrival per scale-factor warp
+      ptx::mbar_init(sfe_bar(r), 1);  // MMA completion
+    }
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::prefetch_tmap(&tmap_w);
@@ -209,11 +228,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_relinquish();
   }
   if (warp == 2) {
-    // Per-expert tile counts and their exclusive scan; experts whose rows
-    // would leave the padded buffers are skipped and flagged.
+    // Per-expert tile counts and their exclusive scan, and the widest token
+    // tile of the launch; experts whose rows would leave the padded buffers
+    // are skipped and flagged.
     const int per = (p.E + 31) / 32;
     const int beg = min(lane * per, p.E), end = min(beg + per, p.E);
-    int sum = 0;
+    int sum = 0, wmax = 32;
     for (int e = beg; e < end; ++e) {
       int c = p.counts[e];
       const int ro = p.row_offsets[e];
@@ -225,19 +245,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_count[e] = c;
       s_rowoff[e] = ro;
       sum += MT * ((c + BN - 1) / BN);
+      int w = 32;
+      while (w < c && w < BN) w <<= 1;
+      if (c > 0) wmax = max(wmax, w);
     }
     int incl = sum;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int o = __shfl_up_sync(kFull, incl, off);
       if (lane >= off) incl += o;
+      wmax = max(wmax, __shfl_xor_sync(kFull, wmax, off));
     }
     int run = incl - sum;
     for (int e = beg; e < end; ++e) {
       s_prefix[e] = run;
       run += MT * ((s_count[e] + BN - 1) / BN);
     }
-    if (lane == 31) s_prefix[p.E] = incl;
+    if (lane == 31) {
+      s_prefix[p.E] = incl;
+      *s_wmax = wmax;
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -246,6 +273,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = s_prefix[p.E];
   const int kblocks = p.K / 64;
   const int nkt = (kblocks + 3) / 4;
+  // Stage geometry for this launch: as many stages as fit once the token
+  // slot is sized for the widest tile actually present.
+  const int wmax = *s_wmax;
+  const int stage = C::stage_bytes(wmax);
+  const int off_b = C::NA * kATile;
+  const int off_sfa = off_b + wmax * kBKBytes;
+  const int off_sfb = off_sfa + C::NA * kSfTile;
+  const int S = min(p.stage_cap, (p.smem_bytes - ctrl) / stage);
+  const uint32_t smem_base = ptx::smem_u32(smem) + uint32_t(ctrl);
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
@@ -268,21 +304,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nkb = min(4, kblocks - 4 * kt);
         const uint32_t bytes = uint32_t(C::NA * kATile + w * kBKBytes + (C::NA + sfb_chunks) * nkb * 512);
         ptx::mbar_arrive_expect_tx(full_bar(s), bytes);
-        const uint32_t st = smem_base + s * uint32_t(C::Stage);
+        const uint32_t st = smem_base + s * uint32_t(stage);
 #pragma unroll
         for (int j = 0; j < C::NA; ++j)
           ptx::tma_load_2d(st + j * kATile, &tmap_w, full_bar(s), kt * kBKBytes, wrow0 + j * (p.N / 2), pol_w);
         for (int r = 0; r < w; r += 32)  // the token tile in 32-row boxes
-          ptx::tma_load_2d(st + C::OffB + r * kBKBytes, &tmap_a, full_bar(s), kt * kBKBytes, arow + r, pol_a);
+          ptx::tma_load_2d(st + off_b + r * kBKBytes, &tmap_a, full_bar(s), kt * kBKBytes, arow + r, pol_a);
 #pragma unroll
         for (int j = 0; j < C::NA; ++j) {
           const int rb = SWIGLU ? (j * (p.N / 2) + mb * kBM) / kBM : mb;
           const uint8_t* src = p.w_scales + ((size_t(e) * (p.N / kBM) + rb) * kblocks + 4 * kt) * 512;
-          ptx::bulk_load(st + C::OffSfa + j * kSfTile, src, uint32_t(nkb * 512), full_bar(s), pol_w);
+          ptx::bulk_load(st + off_sfa + j * kSfTile, src, uint32_t(nkb * 512), full_bar(s), pol_w);
         }
         for (int c = 0; c < sfb_chunks; ++c) {
           const uint8_t* src = p.a_scales + ((size_t(arow / kBM) + c) * kblocks + 4 * kt) * 512;
-          ptx::bulk_load(st + C::OffSfb + c * kSfTile, src, uint32_t(nkb * 512), full_bar(s), pol_a);
+          ptx::bulk_load(st + off_sfb + c * kSfTile, src, uint32_t(nkb * 512), full_bar(s), pol_a);
         }
       }
     }
@@ -305,28 +341,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (s1 >= 0 && !wait_phase(acce_bar(s1), slots.parity(s1) ^ 1u, abort_flag)) break;
       ptx::tc_fence_after();
       const uint32_t idesc = ptx::idesc_nvfp4(kBM, w);
-      const int sfb_chunks = w > 128 ? 2 : 1;
       const uint32_t d0 = tmem + uint32_t(s0 * kAccSlotCols);
       for (int kt = 0; kt < nkt; ++kt, ++it) {
         const uint32_t s = it % uint32_t(S), ph = (it / uint32_t(S)) & 1u;
-        if (!wait_phase(full_bar(s), ph, abort_flag)) {
+        // The stage's scales are in tensor memory once the scale-factor
+        // warps arrive, which they do only after its copies have landed; the
+        // stage's own barrier is complete by then and is checked as well.
+        const uint32_t r = it % uint32_t(C::SfSlots), rph = (it / uint32_t(C::SfSlots)) & 1u;
+        if (!wait_phase(sff_bar(r), rph, abort_flag) || !wait_phase(full_bar(s), ph, abort_flag)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t st = smem_base + s * uint32_t(C::Stage);
-        const uint32_t sf = tmem + uint32_t(kSfColBase + (it & 1u) * 64);
+        const uint32_t st = smem_base + s * uint32_t(stage);
+        const uint32_t sf = tmem + uint32_t(kSfColBase + r * C::SfCols);
         const int nkb = min(4, kblocks - 4 * kt);
-        // Scale factors: every address below is a multiple of 4 columns.
-        for (int kb = 0; kb < nkb; ++kb) {
-#pragma unroll
-          for (int j = 0; j < C::NA; ++j)
-            ptx::tc_cp_32x128b_x4(sf + j * 16 + kb * 4, ptx::desc_sf_block(st + C::OffSfa + j * kSfTile + kb * 512));
-          for (int c = 0; c < sfb_chunks; ++c)
-            ptx::tc_cp_32x128b_x4(sf + C::NA * 16 + kb * 4 * C::NSFB + c * 4,
-                                  ptx::desc_sf_block(st + C::OffSfb + c * kSfTile + kb * 512));
-        }
-        const uint64_t bdesc = ptx::desc_kmajor_sw128(st + C::OffB);
+        const uint64_t bdesc = ptx::desc_kmajor_sw128(st + off_b);
         for (int kb = 0; kb < nkb; ++kb) {
 #pragma unroll
           for (int j = 0; j < C::NA; ++j) {
@@ -336,6 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         ptx::tc_commit(empty_bar(s));  // frees the stage once these MMAs have read it
+        ptx::tc_commit(sfe_bar(r));    // and the scale-factor ring slot
       }
       if (!ok) break;
       ptx::tc_commit(accf_bar(s0));
@@ -344,6 +375,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::tc_commit(drain_bar);  // every MMA of this CTA done before tensor memory is freed
     drain_phase(drain_bar, 0);
+  } else if (warp >= 6) {
+    // ---------------- scale factors: shared memory -> tensor memory ----------------
+    // Each of the four warps writes its 32-lane quarter of every scale block
+    // (the tensor core reads the 512-byte block of 128 rows as four 32-bit
+    // columns per lane, the same in every quarter): lane i loads the block's
+    // 16-byte row i and stores it as 4 columns.  Doing this with tcgen05.st
+    // from these warps keeps the MMA issue stream free of copies, which would
+    // otherwise serialise with the MMAs of the previous stage.
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+    uint32_t it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      int e, mb, nb, w;
+      decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
+      const int sfb_chunks = w > 128 ? 2 : 1;
+      bool ok = true;
+      for (int kt = 0; kt < nkt; ++kt, ++it) {
+        const uint32_t s = it % uint32_t(S), ph = (it / uint32_t(S)) & 1u;
+        const uint32_t r = it % uint32_t(C::SfSlots), rph = (it / uint32_t(C::SfSlots)) & 1u;
+        if (!wait_phase(sfe_bar(r), rph ^ 1u, abort_flag) || !wait_phase(full_bar(s), ph, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t st = smem_base + s * uint32_t(stage);
+        const uint32_t sf = tmem + lane_base + uint32_t(kSfColBase + r * C::SfCols);
+        const int nkb = min(4, kblocks - 4 * kt);
+        for (int kb = 0; kb < nkb; ++kb) {
+#pragma unroll
+          for (int j = 0; j < C::NA; ++j) {
+            const uint4 v = ptx::lds128(st + off_sfa + j * kSfTile + kb * 512 + lane * 16);
+            ptx::tmem_st_32x32b_x4(sf + j * 16 + kb * 4, v.x, v.y, v.z, v.w);
+          }
+          for (int c = 0; c < sfb_chunks; ++c) {
+            const uint4 v = ptx::lds128(st + off_sfb + c * kSfTile + kb * 512 + lane * 16);
+            ptx::tmem_st_32x32b_x4(sf + C::NA * 16 + kb * 4 * C::NSFB + c * 4, v.x, v.y, v.z, v.w);
+          }
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(sff_bar(r));
+      }
+      if (!ok) break;
+    }
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
     const int q = warp & 3;            // tensor-memory lane quarter this warp may access
@@ -459,19 +534,32 @@ bool encode_kmajor_map(CUtensorMap* m, const void* base, int64_t rows, int64_t r
   return r == CUDA_SUCCESS;
 }
 
+// Stage cap: NVFP4MOE_STAGE_CAP in the environment (2..16) overrides the
+// default of as many stages as fit, for pipeline-depth studies.
+int stage_cap_from_env() {
+  static const int cap = [] {
+    const char* v = std::getenv("NVFP4MOE_STAGE_CAP");
+    const int c = v ? std::atoi(v) : kMaxStages;
+    return c < 2 ? 2 : (c > kMaxStages ? kMaxStages : c);
+  }();
+  return cap;
+}
+
 template <int BN, bool SWIGLU>
 int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st) {
   using C = Cfg<BN, SWIGLU>;
-  const size_t fixed = 1024 + ((ctrl_bytes(a.E) + 15) & ~size_t(15));
-  const int64_t avail = int64_t(smem_optin) - int64_t(fixed);
-  const int stages = int(std::min<int64_t>(kMaxStages, avail > 0 ? avail / C::Stage : 0));
-  if (stages < 2) {
+  // The whole opt-in shared memory is requested; the kernel sizes its stages
+  // for the widest token tile present.  Two stages of the widest possible
+  // tile must fit.
+  const int64_t usable = int64_t(smem_optin) - 1024 - ctrl_bytes(a.E);
+  const int worst = C::stage_bytes(BN);
+  if (usable < 2 * int64_t(worst)) {
     set_error_detail(
-        "grouped GEMM tile 128x%d (%s) needs %zu bytes of shared memory for a 2-stage pipeline; Hardware limit: %d",
-        BN, SWIGLU ? "gate/up" : "down", fixed + 2 * size_t(C::Stage), smem_optin);
+        "grouped GEMM tile 128x%d (%s) needs %lld bytes of shared memory for a 2-stage pipeline; Hardware limit: %d",
+        BN, SWIGLU ? "gate/up" : "down", (long long)(1024 + ctrl_bytes(a.E) + 2 * int64_t(worst)), smem_optin);
     return NVFP4MOE_ERR_SMEM;
   }
-  const size_t smem = fixed + size_t(stages) * C::Stage;
+  const size_t smem = size_t(smem_optin);
   CUtensorMap tw, ta;
   if (!encode_kmajor_map(&tw, a.w_packed, int64_t(a.E) * a.N, a.K / 2, kBM) ||
       !encode_kmajor_map(&ta, a.a_packed, a.rows_capacity, a.K / 2, 32)) {
@@ -498,7 +586,8 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   p.N = a.N;
   p.K = a.K;
   p.epi = a.epilogue;
-  p.stages = stages;
+  p.smem_bytes = int(smem) - 1024;
+  p.stage_cap = stage_cap_from_env();
   p.rows_cap = a.rows_capacity;
   grouped_gemm_kernel<BN, SWIGLU><<<num_sms, kThreads, smem, st>>>(tw, ta, p);
   err = cudaGetLastError();

@@ -225,15 +225,20 @@ __global__ void __launch_bounds__(kRankWarps * 32) permute_rank_kernel(const int
   __syncwarp();
   const unsigned lt = (1u << lane) - 1u;
   const int64_t base = int64_t(seg) * kPermuteSegment;
+  // All ids of the segment first, so their loads are in flight together.
+  int ids[kPermuteSegment / 32];
+#pragma unroll
   for (int it = 0; it < kPermuteSegment / 32; ++it) {
     const int64_t f = base + it * 32 + lane;
-    int e = -1;
-    if (f < R) {
-      e = idx[f];
-      if (e < 0 || e >= E) {
-        atomicOr(&g_prep_flags, kFlagBadData);
-        e = -1;
-      }
+    ids[it] = f < R ? idx[f] : -1;
+  }
+#pragma unroll
+  for (int it = 0; it < kPermuteSegment / 32; ++it) {
+    const int64_t f = base + it * 32 + lane;
+    int e = ids[it];
+    if (f < R && (e < 0 || e >= E)) {
+      atomicOr(&g_prep_flags, kFlagBadData);
+      e = -1;
     }
     const unsigned grp = __match_any_sync(kFull, e);
     int r = -1;
@@ -282,6 +287,7 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(const int32_t* __res
                                                             int64_t rows_capacity) {
   __shared__ int warp_tot[32];
   __shared__ int tail_start;
+  __shared__ int s_cnt[1024], s_roff[1024];
   const int e = threadIdx.x;
   int run = 0;
   if (e < E) {
@@ -299,7 +305,8 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(const int32_t* __res
     counts[e] = cnt;
     offsets[e] = off;
     row_offsets[e] = roff;
-    for (int r = cnt; r < padded; ++r) perm_to_flat[roff + r] = -1;
+    s_cnt[e] = cnt;
+    s_roff[e] = roff;
   }
   if (e == E - 1) {
     offsets[E] = off + cnt;
@@ -307,6 +314,12 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(const int32_t* __res
     tail_start = roff + padded;
   }
   __syncthreads();
+  // Padding rows of each expert (one warp per expert, coalesced), then the tail.
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int x = warp; x < E; x += 32) {
+    const int c = s_cnt[x], pad = (c + 127) & ~127;
+    for (int r = c + lane; r < pad; r += 32) perm_to_flat[s_roff[x] + r] = -1;
+  }
   for (int64_t p = int64_t(tail_start) + threadIdx.x; p < rows_capacity; p += blockDim.x) perm_to_flat[p] = -1;
 }
 
