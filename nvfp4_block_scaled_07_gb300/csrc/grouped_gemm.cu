@@ -84,9 +84,11 @@ struct Params {
   int64_t rows_cap;
 };
 
-template <int BN, bool SWIGLU>
+template <int BN, int NA_, bool SWIGLU>
 struct Cfg {
-  static constexpr int NA = SWIGLU ? 2 : 1;          // weight tiles per stage (gate, up)
+  static constexpr int NA = NA_;  // 128-row weight tiles per stage: gate and up, or NA consecutive row blocks
+  static_assert(!SWIGLU || NA == 2, "the SwiGLU epilogue pairs a gate tile with an up tile");
+  static_assert(NA == 1 || NA == 2, "one or two weight tiles per stage");
   static constexpr int NSFB = BN > 128 ? 2 : 1;      // 128-row scale blocks per token tile
   static constexpr int SfCols = NA * 16 + NSFB * 16;  // tensor-memory columns of one stage's scales
   static constexpr int SfSlots = kSfRingCols / SfCols < kMaxSfSlots ? kSfRingCols / SfCols : kMaxSfSlots;
@@ -176,11 +178,11 @@ struct SlotSeq {
   }
 };
 
-template <int BN, bool SWIGLU>
+template <int BN, int NA, bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                         const Params p) {
-  using C = Cfg<BN, SWIGLU>;
+  using C = Cfg<BN, NA, SWIGLU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -203,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto sff_bar = [&](uint32_t r) { return bar0 + 8u * (uint32_t(2 * kMaxStages + 5) + r); };
   auto sfe_bar = [&](uint32_t r) { return bar0 + 8u * (uint32_t(2 * kMaxStages + 5 + kMaxSfSlots) + r); };
 
-  const int MT = (SWIGLU ? p.N / 2 : p.N) / kBM;  // M tiles per expert
+  const int MT = SWIGLU ? p.N / 2 / kBM : p.N / (kBM * NA);  // M tiles per expert
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
       ptx::mbar_init(full_bar(s), 1);
@@ -294,7 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
       const int arow = s_rowoff[e] + nb * BN;
       const int sfb_chunks = w > 128 ? 2 : 1;
-      const int wrow0 = e * p.N + mb * kBM;
+      // weight rows of tile j: gate/up pairs rows f and I + f; otherwise NA consecutive 128-row blocks
+      const int wrow0 = SWIGLU ? e * p.N + mb * kBM : e * p.N + mb * kBM * NA;
+      const int wstep = SWIGLU ? p.N / 2 : kBM;
       for (int kt = 0; kt < nkt; ++kt, ++it) {
         const uint32_t s = it % uint32_t(S), ph = (it / uint32_t(S)) & 1u;
         if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag)) {
@@ -307,12 +311,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = smem_base + s * uint32_t(stage);
 #pragma unroll
         for (int j = 0; j < C::NA; ++j)
-          ptx::tma_load_2d(st + j * kATile, &tmap_w, full_bar(s), kt * kBKBytes, wrow0 + j * (p.N / 2), pol_w);
+          ptx::tma_load_2d(st + j * kATile, &tmap_w, full_bar(s), kt * kBKBytes, wrow0 + j * wstep, pol_w);
         for (int r = 0; r < w; r += 32)  // the token tile in 32-row boxes
           ptx::tma_load_2d(st + off_b + r * kBKBytes, &tmap_a, full_bar(s), kt * kBKBytes, arow + r, pol_a);
 #pragma unroll
         for (int j = 0; j < C::NA; ++j) {
-          const int rb = SWIGLU ? (j * (p.N / 2) + mb * kBM) / kBM : mb;
+          const int rb = SWIGLU ? (j * (p.N / 2) + mb * kBM) / kBM : mb * NA + j;
           const uint8_t* src = p.w_scales + ((size_t(e) * (p.N / kBM) + rb) * kblocks + 4 * kt) * 512;
           ptx::bulk_load(st + off_sfa + j * kSfTile, src, uint32_t(nkb * 512), full_bar(s), pol_w);
         }
@@ -440,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t row0 = int64_t(s_rowoff[e]) + int64_t(nb) * BN;
       const float scale = a_gs * p.w_gscale[e];
       const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + uint32_t(s0 * kAccSlotCols);
-      const int f = mb * kBM + lrow;  // output column
+      const int f = (SWIGLU ? mb : mb * NA) * kBM + lrow;  // output column (of tile 0)
       for (int c0 = 0; c0 < valid; c0 += 32) {
         uint32_t g[32];
         ptx::tmem_ld_32x32b_x32(tbase + c0, g);
@@ -482,6 +486,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (c0 + i < valid) out[(row0 + c0 + i) * n_out + f] = __float2bfloat16_rn(__uint_as_float(g[i]) * scale);
+          if constexpr (NA == 2) {  // the second 128-row block of the tile
+            ptx::tmem_ld_32x32b_x32(tbase + w + c0, g);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c0 + i < valid)
+                out[(row0 + c0 + i) * n_out + f + kBM] = __float2bfloat16_rn(__uint_as_float(g[i]) * scale);
+          }
         }
       }
       ptx::tc_fence_before();
@@ -545,9 +557,9 @@ int stage_cap_from_env() {
   return cap;
 }
 
-template <int BN, bool SWIGLU>
+template <int BN, int NA, bool SWIGLU>
 int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st) {
-  using C = Cfg<BN, SWIGLU>;
+  using C = Cfg<BN, NA, SWIGLU>;
   // The whole opt-in shared memory is requested; the kernel sizes its stages
   // for the widest token tile present.  Two stages of the widest possible
   // tile must fit.
@@ -555,8 +567,8 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   const int worst = C::stage_bytes(BN);
   if (usable < 2 * int64_t(worst)) {
     set_error_detail(
-        "grouped GEMM tile 128x%d (%s) needs %lld bytes of shared memory for a 2-stage pipeline; Hardware limit: %d",
-        BN, SWIGLU ? "gate/up" : "down", (long long)(1024 + ctrl_bytes(a.E) + 2 * int64_t(worst)), smem_optin);
+        "grouped GEMM tile %dx%d (%s) needs %lld bytes of shared memory for a 2-stage pipeline; Hardware limit: %d",
+        kBM * NA, BN, SWIGLU ? "gate/up" : "down", (long long)(1024 + ctrl_bytes(a.E) + 2 * int64_t(worst)), smem_optin);
     return NVFP4MOE_ERR_SMEM;
   }
   const size_t smem = size_t(smem_optin);
@@ -567,7 +579,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
     return NVFP4MOE_ERR_CUDA;
   }
   cudaError_t err =
-      cudaFuncSetAttribute(grouped_gemm_kernel<BN, SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+      cudaFuncSetAttribute(grouped_gemm_kernel<BN, NA, SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (err != cudaSuccess) {
     set_error_detail("cudaFuncSetAttribute: %s", cudaGetErrorString(err));
     return NVFP4MOE_ERR_CUDA;
@@ -589,7 +601,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   p.smem_bytes = int(smem) - 1024;
   p.stage_cap = stage_cap_from_env();
   p.rows_cap = a.rows_capacity;
-  grouped_gemm_kernel<BN, SWIGLU><<<num_sms, kThreads, smem, st>>>(tw, ta, p);
+  grouped_gemm_kernel<BN, NA, SWIGLU><<<num_sms, kThreads, smem, st>>>(tw, ta, p);
   err = cudaGetLastError();
   if (err != cudaSuccess) {
     set_error_detail("grouped GEMM launch: %s", cudaGetErrorString(err));
@@ -603,9 +615,13 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
 int launch_grouped_gemm(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st) {
   const bool swiglu = a.epilogue != NVFP4MOE_EPI_BF16;
   const int bn = a.tile_n == 0 ? 128 : a.tile_n;
-  if (swiglu && bn == 128) return launch_impl<128, true>(a, num_sms, smem_optin, st);
-  if (!swiglu && bn == 128) return launch_impl<128, false>(a, num_sms, smem_optin, st);
-  if (!swiglu && bn == 256) return launch_impl<256, false>(a, num_sms, smem_optin, st);
+  // Small experts (decode): two 128-row weight tiles per stage, so each stage
+  // carries twice the weight bytes and two independent accumulation chains.
+  const bool pair = a.N % (2 * kBM) == 0 && a.m_total <= int64_t(64) * a.E;
+  if (swiglu && bn == 128) return launch_impl<128, 2, true>(a, num_sms, smem_optin, st);
+  if (!swiglu && bn == 128 && pair) return launch_impl<128, 2, false>(a, num_sms, smem_optin, st);
+  if (!swiglu && bn == 128) return launch_impl<128, 1, false>(a, num_sms, smem_optin, st);
+  if (!swiglu && bn == 256) return launch_impl<256, 1, false>(a, num_sms, smem_optin, st);
   set_error_detail("tile_n %d is not supported for this epilogue", a.tile_n);
   return NVFP4MOE_ERR_UNSUPPORTED;
 }
