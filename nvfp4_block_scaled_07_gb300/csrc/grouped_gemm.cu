@@ -178,6 +178,63 @@ struct SlotSeq {
   }
 };
 
+// NVFP4 requantisation of a 32-token x 32-feature chunk of the SwiGLU output
+// held one feature per lane (lane = feature f0 + lane, h[t] = token t), with
+// the rounding rules of the quantiser kernel.  The two 16-feature blocks of
+// the warp (lanes 0-15 and 16-31) need one scale per token each: a
+// reduce-scatter butterfly over the 16 lanes of a block leaves the block
+// amax of tokens 2l and 2l+1 in lane l, which computes their scales once and
+// shares the dequantisation step back with one shuffle per element.
+__device__ __forceinline__ void requant_swiglu_chunk(const float (&h)[32], int lane, float s_h, int64_t row0,
+                                                     int nvalid, int f, int n_out, uint8_t* out_codes,
+                                                     uint8_t* out_scales) {
+  float a[16];
+  {
+    const bool hi = lane & 8;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      const float keep = hi ? fabsf(h[t + 16]) : fabsf(h[t]);
+      const float give = hi ? fabsf(h[t]) : fabsf(h[t + 16]);
+      a[t] = fmaxf(keep, __shfl_xor_sync(kFull, give, 8));
+    }
+  }
+#pragma unroll
+  for (int step = 4; step >= 1; step >>= 1) {   // 16 -> 8 -> 4 -> 2 tokens per lane
+    const bool hi = lane & step;
+    const int half = 2 * step;                   // tokens kept after this step
+#pragma unroll
+    for (int t = 0; t < half; ++t) {
+      const float keep = hi ? a[t + half] : a[t];
+      const float give = hi ? a[t] : a[t + half];
+      a[t] = fmaxf(keep, __shfl_xor_sync(kFull, give, step));
+    }
+  }
+  // lane l of a block now holds the amax of tokens 2(l % 16) and 2(l % 16) + 1
+  const int t0 = 2 * (lane & 15);
+  uint32_t sb[2];
+  float d[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    sb[k] = f32_to_ue4m3((a[k] / kE2M1Max) / s_h);
+    d[k] = ue4m3_to_f32(sb[k]) * s_h;
+  }
+  const int fb = (f & ~31) + (lane & 16);        // first feature of this lane's block
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+    if (t0 + k < nvalid)
+      out_scales[blocked_sf_offset(row0 + t0 + k, fb >> 6, n_out / 64) + ((fb >> 4) & 3)] = uint8_t(sb[k]);
+  uint8_t* row_ptr = out_codes + row0 * (n_out / 2) + (f & ~7) / 2;
+#pragma unroll
+  for (int t = 0; t < 32; ++t) {
+    const float dt = __shfl_sync(kFull, d[t & 1], (lane & 16) + (t >> 1));
+    uint32_t word = e2m1_code(h[t], dt) << (4 * (lane & 7));
+    word |= __shfl_xor_sync(kFull, word, 1);
+    word |= __shfl_xor_sync(kFull, word, 2);
+    word |= __shfl_xor_sync(kFull, word, 4);
+    if ((lane & 7) == 0 && t < nvalid) *reinterpret_cast<uint32_t*>(row_ptr + int64_t(t) * (n_out / 2)) = word;
+  }
+}
+
 template <int BN, int NA, bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
@@ -452,33 +509,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t u[32];
           ptx::tmem_ld_32x32b_x32(tbase + w + c0, u);
           ptx::tmem_ld_wait();
+          // h = silu(gate) * up for 32 tokens of this lane's feature.
+          float h[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            if (c0 + i < valid) {  // uniform across the warp
-              const float gf = __uint_as_float(g[i]) * scale;
-              const float uf = __uint_as_float(u[i]) * scale;
-              const float h = gf / (1.0f + expf(-gf)) * uf;
-              const int64_t row = row0 + c0 + i;
-              if (f32_out) {
-                static_cast<float*>(p.c_out)[row * n_out + f] = h;
-              } else {
-                float a = fabsf(h);
-                a = fmaxf(a, __shfl_xor_sync(kFull, a, 1));
-                a = fmaxf(a, __shfl_xor_sync(kFull, a, 2));
-                a = fmaxf(a, __shfl_xor_sync(kFull, a, 4));
-                a = fmaxf(a, __shfl_xor_sync(kFull, a, 8));
-                const uint32_t sb = f32_to_ue4m3((a / kE2M1Max) / s_h);
-                const float d = ue4m3_to_f32(sb) * s_h;
-                uint32_t word = e2m1_code(h, d) << (4 * (lane & 7));
-                word |= __shfl_xor_sync(kFull, word, 1);
-                word |= __shfl_xor_sync(kFull, word, 2);
-                word |= __shfl_xor_sync(kFull, word, 4);
-                if ((lane & 7) == 0)
-                  *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.c_out) + row * (n_out / 2) + f / 2) = word;
-                if ((lane & 15) == 0)
-                  p.c_scales[blocked_sf_offset(row, f >> 6, n_out / 64) + ((f >> 4) & 3)] = uint8_t(sb);
-              }
-            }
+            const float gf = __uint_as_float(g[i]) * scale;
+            const float uf = __uint_as_float(u[i]) * scale;
+            h[i] = gf * __frcp_rn(1.0f + __expf(-gf)) * uf;
+          }
+          if (f32_out) {
+            float* out = static_cast<float*>(p.c_out) + (row0 + c0) * n_out + f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c0 + i < valid) out[int64_t(i) * n_out] = h[i];
+          } else {
+            requant_swiglu_chunk(h, lane, s_h, row0 + c0, valid - c0, f, n_out, static_cast<uint8_t*>(p.c_out),
+                                 p.c_scales);
           }
         } else {
           ptx::tmem_ld_wait();
