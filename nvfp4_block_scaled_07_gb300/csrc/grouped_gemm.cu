@@ -418,13 +418,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sf = tmem + uint32_t(kSfColBase + r * C::SfCols);
         const int nkb = min(4, kblocks - 4 * kt);
         const uint64_t bdesc = ptx::desc_kmajor_sw128(st + off_b);
-        for (int kb = 0; kb < nkb; ++kb) {
+        // The tensor core pipelines MMAs only when they are issued back to
+        // back; any loop overhead in between makes each one wait for the
+        // previous.  A full stage (4 k64 blocks) is therefore issued from a
+        // fully unrolled sequence; only a partial last K tile takes the loop.
+        auto mma_block = [&](int kb) {
 #pragma unroll
-          for (int j = 0; j < C::NA; ++j) {
-            const uint64_t adesc = ptx::desc_kmajor_sw128(st + j * kATile);
-            ptx::tc_mma_nvfp4(d0 + j * w, adesc + 2 * kb, bdesc + 2 * kb, idesc, sf + j * 16 + kb * 4,
-                              sf + C::NA * 16 + kb * 4 * C::NSFB, (kt | kb) != 0 ? 1u : 0u);
-          }
+          for (int j = 0; j < C::NA; ++j)
+            ptx::tc_mma_nvfp4(d0 + j * w, ptx::desc_kmajor_sw128(st + j * kATile) + 2 * kb, bdesc + 2 * kb, idesc,
+                              sf + j * 16 + kb * 4, sf + C::NA * 16 + kb * 4 * C::NSFB, (kt | kb) != 0 ? 1u : 0u);
+        };
+        if (nkb == 4) {
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb) mma_block(kb);
+        } else {
+          for (int kb = 0; kb < nkb; ++kb) mma_block(kb);
         }
         ptx::tc_commit(empty_bar(s));  // frees the stage once these MMAs have read it
         ptx::tc_commit(sfe_bar(r));    // and the scale-factor ring slot
