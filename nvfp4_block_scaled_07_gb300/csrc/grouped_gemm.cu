@@ -22,12 +22,13 @@
 // 4-column aligned) and each tile's MMA width is the power of two >= 32 that
 // covers the expert's remaining rows, up to BN (128 or 256).
 //
-// Warp roles (320 threads, one CTA per SM, persistent):
+// Warp roles (one CTA per SM, persistent):
 //   warp 0     TMA producer: weight tile(s), token tile, their scale blocks
 //   warp 1     tensor-memory owner and MMA issuer (one elected lane)
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator, scaling, SwiGLU,
-//              requantisation or bf16 conversion, global stores
-//   warps 6-9  scale factors: shared memory -> tensor memory (tcgen05.st)
+//   next 4/8   epilogue: tcgen05.ld of the accumulator, scaling, SwiGLU,
+//              requantisation or bf16 conversion, global stores (8 warps
+//              for SwiGLU, two per lane quarter)
+//   last 4     scale factors: shared memory -> tensor memory (tcgen05.st)
 //              into a ring of slots the MMAs read their block scales from
 // Tiles are (expert, M tile, N tile) with N innermost, striped over the
 // CTAs, so the CTAs working at the same time share a weight tile through L2.
@@ -52,7 +53,12 @@ namespace {
 
 __device__ unsigned g_gemm_flags = 0;
 
-constexpr int kThreads = 320;
+// Epilogue warps: the SwiGLU requantisation is a long dependent chain per
+// token, so two warps per tensor-memory lane quarter split the token chunks
+// to hide its latency; the bf16 epilogue needs one warp per quarter.
+__host__ __device__ constexpr int epi_warps(bool swiglu) { return swiglu ? 8 : 4; }
+// warp 0 producer, warp 1 MMA, then the epilogue warps, then 4 scale-factor warps
+__host__ __device__ constexpr int num_threads(bool swiglu) { return 32 * (2 + epi_warps(swiglu) + 4); }
 constexpr int kBM = 128;           // MMA M (weight rows per tile)
 constexpr int kBKBytes = 128;      // bytes of K per stage and row = 256 E2M1 elements
 constexpr int kATile = kBM * kBKBytes;
@@ -236,7 +242,7 @@ __device__ __forceinline__ void requant_swiglu_chunk(const float (&h)[32], int l
 }
 
 template <int BN, int NA, bool SWIGLU>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                         const Params p) {
   using C = Cfg<BN, NA, SWIGLU>;
@@ -270,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(accf_bar(b), 1);
-      ptx::mbar_init(acce_bar(b), 4);
+      ptx::mbar_init(acce_bar(b), epi_warps(SWIGLU));
     }
     ptx::mbar_init(drain_bar, 1);
     for (int r = 0; r < kMaxSfSlots; ++r) {
@@ -444,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::tc_commit(drain_bar);  // every MMA of this CTA done before tensor memory is freed
     drain_phase(drain_bar, 0);
-  } else if (warp >= 6) {
+  } else if (warp >= 2 + epi_warps(SWIGLU)) {
     // ---------------- scale factors: shared memory -> tensor memory ----------------
     // Each of the four warps writes its 32-lane quarter of every scale block
     // (the tensor core reads the 512-byte block of 128 rows as four 32-bit
@@ -491,6 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
     const int q = warp & 3;            // tensor-memory lane quarter this warp may access
+    constexpr int kParts = epi_warps(SWIGLU) / 4;  // warps sharing a quarter split the token chunks
+    const int part = (warp - 2) / 4;
     const int lrow = q * 32 + lane;    // accumulator row = output feature within the tile
     const float a_gs = *p.a_gscale;
     const bool f32_out = p.epi == NVFP4MOE_EPI_SWIGLU_F32;
@@ -510,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float scale = a_gs * p.w_gscale[e];
       const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + uint32_t(s0 * kAccSlotCols);
       const int f = (SWIGLU ? mb : mb * NA) * kBM + lrow;  // output column (of tile 0)
-      for (int c0 = 0; c0 < valid; c0 += 32) {
+      for (int c0 = 32 * part; c0 < valid; c0 += 32 * kParts) {
         uint32_t g[32];
         ptx::tmem_ld_32x32b_x32(tbase + c0, g);
         if constexpr (SWIGLU) {
@@ -655,7 +663,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   p.smem_bytes = int(smem) - 1024;
   p.stage_cap = stage_cap_from_env();
   p.rows_cap = a.rows_capacity;
-  grouped_gemm_kernel<BN, NA, SWIGLU><<<num_sms, kThreads, smem, st>>>(tw, ta, p);
+  grouped_gemm_kernel<BN, NA, SWIGLU><<<num_sms, num_threads(SWIGLU), smem, st>>>(tw, ta, p);
   err = cudaGetLastError();
   if (err != cudaSuccess) {
     set_error_detail("grouped GEMM launch: %s", cudaGetErrorString(err));
