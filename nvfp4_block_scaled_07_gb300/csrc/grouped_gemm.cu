@@ -70,8 +70,7 @@ constexpr int kSfRingCols = 256;
 constexpr int kMaxSfSlots = 8;
 constexpr int kMaxStages = 16;
 // mbarriers: full/empty per stage, acc full/empty per slot, drain, sf full/empty per ring slot
-// and the epilogue exchange: 4 gate/up warp pairs x 2 buffers
-constexpr int kNumBars = 2 * kMaxStages + 5 + 2 * kMaxSfSlots + 8;
+constexpr int kNumBars = 2 * kMaxStages + 5 + 2 * kMaxSfSlots;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
@@ -93,19 +92,12 @@ struct Params {
 
 template <int BN, int NA_, bool SWIGLU>
 struct Cfg {
-  // NA 128-row weight tiles per stage.  bf16: NA consecutive 128-row blocks.
-  // SwiGLU: each tile is 64 gate rows (features f..f+63) over the 64 up rows
-  // of the same features, so one accumulator holds both halves and a tile
-  // covers 64 features.
-  static constexpr int NA = NA_;
+  static constexpr int NA = NA_;  // 128-row weight tiles per stage: gate and up, or NA consecutive row blocks
+  static_assert(!SWIGLU || NA == 2, "the SwiGLU epilogue pairs a gate tile with an up tile");
   static_assert(NA == 1 || NA == 2, "one or two weight tiles per stage");
-  static constexpr int SFA_CHUNKS = SWIGLU ? 2 : 1;   // 128-row scale blocks behind one weight tile
-  static constexpr int FEAT = SWIGLU ? kBM / 2 : kBM;  // output features per weight tile
   static constexpr int NSFB = BN > 128 ? 2 : 1;      // 128-row scale blocks per token tile
   static constexpr int SfCols = NA * 16 + NSFB * 16;  // tensor-memory columns of one stage's scales
   static constexpr int SfSlots = kSfRingCols / SfCols < kMaxSfSlots ? kSfRingCols / SfCols : kMaxSfSlots;
-  // shared memory through which a gate warp and an up warp swap half a chunk
-  static constexpr int XCHG = SWIGLU ? 4 * 2 * 2 * 16 * 32 * 4 : 0;  // pairs x buffers x directions x 16x32 floats
   static_assert(BN == 128 || BN == 256, "token tiles must start on 128-row scale blocks");
   static_assert(NA * BN <= 2 * kAccSlotCols, "accumulator does not fit the two slots");
   static_assert(SfCols <= 64, "scale-factor buffer overflow");
@@ -113,13 +105,13 @@ struct Cfg {
   // weight tile(s), token tile, their scale blocks; a multiple of 2048, so
   // every stage and every tile in it stays 1024-byte aligned (128B swizzle).
   __host__ __device__ static constexpr int stage_bytes(int wmax) {
-    return NA * kATile + wmax * kBKBytes + NA * SFA_CHUNKS * kSfTile + (wmax > 128 ? 2 : 1) * kSfTile;
+    return NA * kATile + wmax * kBKBytes + NA * kSfTile + (wmax > 128 ? 2 : 1) * kSfTile;
   }
 };
 
 // Control block at the start of shared memory: mbarriers, the tensor-memory
-// address, flags and the per-expert tile scan; stages start after it (and
-// after the epilogue exchange buffer) on a 1024-byte boundary.
+// address, flags and the per-expert tile scan; stages start after it on a
+// 1024-byte boundary.
 __host__ __device__ constexpr int ctrl_bytes(int E) {
   return (kNumBars * 8 + 16 + (3 * E + 1) * 4 + 1023) / 1024 * 1024;
 }
@@ -192,52 +184,55 @@ struct SlotSeq {
   }
 };
 
-// NVFP4 requantisation of an NT-token x 32-feature chunk of the SwiGLU
-// output held one feature per lane (lane = feature f0 + lane, h[t] = token
-// t), with the rounding rules of the quantiser kernel.  The two 16-feature
-// blocks of the warp (lanes 0-15 and 16-31) need one scale per token each: a
-// reduce-scatter butterfly over the 16 lanes of a block leaves the block amax
-// of tokens NT/16 * (l % 16) + k in lane l, which computes their scales once
-// and shares the dequantisation step back with one shuffle per element.
-template <int NT>
-__device__ __forceinline__ void requant_swiglu_chunk(const float (&h)[NT], int lane, float s_h, int64_t row0,
+// NVFP4 requantisation of a 32-token x 32-feature chunk of the SwiGLU output
+// held one feature per lane (lane = feature f0 + lane, h[t] = token t), with
+// the rounding rules of the quantiser kernel.  The two 16-feature blocks of
+// the warp (lanes 0-15 and 16-31) need one scale per token each: a
+// reduce-scatter butterfly over the 16 lanes of a block leaves the block
+// amax of tokens 2l and 2l+1 in lane l, which computes their scales once and
+// shares the dequantisation step back with one shuffle per element.
+__device__ __forceinline__ void requant_swiglu_chunk(const float (&h)[32], int lane, float s_h, int64_t row0,
                                                      int nvalid, int f, int n_out, uint8_t* out_codes,
                                                      uint8_t* out_scales) {
-  static_assert(NT == 16 || NT == 32, "16 or 32 tokens");
-  constexpr int TPL = NT / 16;  // tokens per lane after the butterfly
-  float a[NT];
+  float a[16];
+  {
+    const bool hi = lane & 8;
 #pragma unroll
-  for (int t = 0; t < NT; ++t) a[t] = fabsf(h[t]);
-#pragma unroll
-  for (int step = 8; step >= 1; step >>= 1) {  // NT -> NT/2 -> ... -> TPL tokens per lane
-    const bool hi = lane & step;
-    const int keep = NT * step / 16;
-#pragma unroll
-    for (int t = 0; t < NT / 2; ++t) {
-      if (t < keep) {
-        const float mine = hi ? a[t + keep] : a[t];
-        const float give = hi ? a[t] : a[t + keep];
-        a[t] = fmaxf(mine, __shfl_xor_sync(kFull, give, step));
-      }
+    for (int t = 0; t < 16; ++t) {
+      const float keep = hi ? fabsf(h[t + 16]) : fabsf(h[t]);
+      const float give = hi ? fabsf(h[t]) : fabsf(h[t + 16]);
+      a[t] = fmaxf(keep, __shfl_xor_sync(kFull, give, 8));
     }
   }
-  const int t0 = TPL * (lane & 15);
-  uint32_t sb[TPL];
-  float d[TPL];
 #pragma unroll
-  for (int k = 0; k < TPL; ++k) {
+  for (int step = 4; step >= 1; step >>= 1) {   // 16 -> 8 -> 4 -> 2 tokens per lane
+    const bool hi = lane & step;
+    const int half = 2 * step;                   // tokens kept after this step
+#pragma unroll
+    for (int t = 0; t < half; ++t) {
+      const float keep = hi ? a[t + half] : a[t];
+      const float give = hi ? a[t] : a[t + half];
+      a[t] = fmaxf(keep, __shfl_xor_sync(kFull, give, step));
+    }
+  }
+  // lane l of a block now holds the amax of tokens 2(l % 16) and 2(l % 16) + 1
+  const int t0 = 2 * (lane & 15);
+  uint32_t sb[2];
+  float d[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
     sb[k] = f32_to_ue4m3((a[k] / kE2M1Max) / s_h);
     d[k] = ue4m3_to_f32(sb[k]) * s_h;
   }
-  const int fb = (f & ~31) + (lane & 16);  // first feature of this lane's block
+  const int fb = (f & ~31) + (lane & 16);        // first feature of this lane's block
 #pragma unroll
-  for (int k = 0; k < TPL; ++k)
+  for (int k = 0; k < 2; ++k)
     if (t0 + k < nvalid)
       out_scales[blocked_sf_offset(row0 + t0 + k, fb >> 6, n_out / 64) + ((fb >> 4) & 3)] = uint8_t(sb[k]);
   uint8_t* row_ptr = out_codes + row0 * (n_out / 2) + (f & ~7) / 2;
 #pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    const float dt = __shfl_sync(kFull, d[t % TPL], (lane & 16) + t / TPL);
+  for (int t = 0; t < 32; ++t) {
+    const float dt = __shfl_sync(kFull, d[t & 1], (lane & 16) + (t >> 1));
     uint32_t word = e2m1_code(h[t], dt) << (4 * (lane & 7));
     word |= __shfl_xor_sync(kFull, word, 1);
     word |= __shfl_xor_sync(kFull, word, 2);
@@ -260,8 +255,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   int* s_prefix = reinterpret_cast<int*>(tmem_slot + 4);
   int* s_count = s_prefix + p.E + 1;
   int* s_rowoff = s_count + p.E;
-  const int ctrl = ctrl_bytes(p.E) + C::XCHG;
-  float* xchg = reinterpret_cast<float*>(smem + ctrl_bytes(p.E));
+  const int ctrl = ctrl_bytes(p.E);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bar0 = ptx::smem_u32(bars);
@@ -273,11 +267,8 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   const uint32_t drain_bar = bar0 + 8u * uint32_t(2 * kMaxStages + 4);
   auto sff_bar = [&](uint32_t r) { return bar0 + 8u * (uint32_t(2 * kMaxStages + 5) + r); };
   auto sfe_bar = [&](uint32_t r) { return bar0 + 8u * (uint32_t(2 * kMaxStages + 5 + kMaxSfSlots) + r); };
-  auto xchg_bar = [&](int pair, uint32_t b) {
-    return bar0 + 8u * (uint32_t(2 * kMaxStages + 5 + 2 * kMaxSfSlots + 2 * pair) + b);
-  };
 
-  const int MT = (SWIGLU ? p.N / 2 : p.N) / (C::FEAT * NA);  // tiles per expert along the output features
+  const int MT = SWIGLU ? p.N / 2 / kBM : p.N / (kBM * NA);  // M tiles per expert
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
       ptx::mbar_init(full_bar(s), 1);
@@ -292,7 +283,6 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       ptx::mbar_init(sff_bar(r), 4);  // one arrival per scale-factor warp
       ptx::mbar_init(sfe_bar(r), 1);  // MMA completion
     }
-    for (int x = 0; x < 8; ++x) ptx::mbar_init(xchg_bar(x >> 1, uint32_t(x & 1)), 2);  // both warps of a pair
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::prefetch_tmap(&tmap_w);
@@ -354,7 +344,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   const int stage = C::stage_bytes(wmax);
   const int off_b = C::NA * kATile;
   const int off_sfa = off_b + wmax * kBKBytes;
-  const int off_sfb = off_sfa + C::NA * C::SFA_CHUNKS * kSfTile;
+  const int off_sfb = off_sfa + C::NA * kSfTile;
   const int S = min(p.stage_cap, (p.smem_bytes - ctrl) / stage);
   const uint32_t smem_base = ptx::smem_u32(smem) + uint32_t(ctrl);
 
@@ -369,7 +359,9 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
       const int arow = s_rowoff[e] + nb * BN;
       const int sfb_chunks = w > 128 ? 2 : 1;
-      const int f0 = mb * NA * C::FEAT;  // first output feature of the tile
+      // weight rows of tile j: gate/up pairs rows f and I + f; otherwise NA consecutive 128-row blocks
+      const int wrow0 = SWIGLU ? e * p.N + mb * kBM : e * p.N + mb * kBM * NA;
+      const int wstep = SWIGLU ? p.N / 2 : kBM;
       for (int kt = 0; kt < nkt; ++kt, ++it) {
         const uint32_t s = it % uint32_t(S), ph = (it / uint32_t(S)) & 1u;
         if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag)) {
@@ -377,32 +369,19 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
           break;
         }
         const int nkb = min(4, kblocks - 4 * kt);
-        const uint32_t bytes =
-            uint32_t(C::NA * kATile + w * kBKBytes + (C::NA * C::SFA_CHUNKS + sfb_chunks) * nkb * 512);
+        const uint32_t bytes = uint32_t(C::NA * kATile + w * kBKBytes + (C::NA + sfb_chunks) * nkb * 512);
         ptx::mbar_arrive_expect_tx(full_bar(s), bytes);
         const uint32_t st = smem_base + s * uint32_t(stage);
 #pragma unroll
-        for (int j = 0; j < C::NA; ++j) {
-          const int fj = f0 + j * C::FEAT;
-          if constexpr (SWIGLU) {  // 64 gate rows over the 64 up rows of the same features
-            ptx::tma_load_2d(st + j * kATile, &tmap_w, full_bar(s), kt * kBKBytes, e * p.N + fj, pol_w);
-            ptx::tma_load_2d(st + j * kATile + kATile / 2, &tmap_w, full_bar(s), kt * kBKBytes,
-                             e * p.N + p.N / 2 + fj, pol_w);
-          } else {
-            ptx::tma_load_2d(st + j * kATile, &tmap_w, full_bar(s), kt * kBKBytes, e * p.N + fj, pol_w);
-          }
-        }
+        for (int j = 0; j < C::NA; ++j)
+          ptx::tma_load_2d(st + j * kATile, &tmap_w, full_bar(s), kt * kBKBytes, wrow0 + j * wstep, pol_w);
         for (int r = 0; r < w; r += 32)  // the token tile in 32-row boxes
           ptx::tma_load_2d(st + off_b + r * kBKBytes, &tmap_a, full_bar(s), kt * kBKBytes, arow + r, pol_a);
 #pragma unroll
         for (int j = 0; j < C::NA; ++j) {
-#pragma unroll
-          for (int h = 0; h < C::SFA_CHUNKS; ++h) {  // the scale block of the gate rows, then of the up rows
-            const int rb = (f0 + j * C::FEAT + h * (p.N / 2)) / kBM;
-            const uint8_t* src = p.w_scales + ((size_t(e) * (p.N / kBM) + rb) * kblocks + 4 * kt) * 512;
-            ptx::bulk_load(st + off_sfa + (j * C::SFA_CHUNKS + h) * kSfTile, src, uint32_t(nkb * 512), full_bar(s),
-                           pol_w);
-          }
+          const int rb = SWIGLU ? (j * (p.N / 2) + mb * kBM) / kBM : mb * NA + j;
+          const uint8_t* src = p.w_scales + ((size_t(e) * (p.N / kBM) + rb) * kblocks + 4 * kt) * 512;
+          ptx::bulk_load(st + off_sfa + j * kSfTile, src, uint32_t(nkb * 512), full_bar(s), pol_w);
         }
         for (int c = 0; c < sfb_chunks; ++c) {
           const uint8_t* src = p.a_scales + ((size_t(arow / kBM) + c) * kblocks + 4 * kt) * 512;
@@ -500,20 +479,8 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         for (int kb = 0; kb < nkb; ++kb) {
 #pragma unroll
           for (int j = 0; j < C::NA; ++j) {
-            if constexpr (SWIGLU) {
-              // Tile rows 0-63 are gate rows f..f+63, 64-127 the up rows of the
-              // same features: columns 0-1 come from the gate block, 2-3 from
-              // the up block, each from the half that holds those rows.
-              const uint4 gv = ptx::lds128(st + off_sfa + (2 * j) * kSfTile + kb * 512 + lane * 16);
-              const uint4 uv = ptx::lds128(st + off_sfa + (2 * j + 1) * kSfTile + kb * 512 + lane * 16);
-              if (((mb * NA + j) * C::FEAT) & 64)
-                ptx::tmem_st_32x32b_x4(sf + j * 16 + kb * 4, gv.z, gv.w, uv.z, uv.w);
-              else
-                ptx::tmem_st_32x32b_x4(sf + j * 16 + kb * 4, gv.x, gv.y, uv.x, uv.y);
-            } else {
-              const uint4 v = ptx::lds128(st + off_sfa + j * kSfTile + kb * 512 + lane * 16);
-              ptx::tmem_st_32x32b_x4(sf + j * 16 + kb * 4, v.x, v.y, v.z, v.w);
-            }
+            const uint4 v = ptx::lds128(st + off_sfa + j * kSfTile + kb * 512 + lane * 16);
+            ptx::tmem_st_32x32b_x4(sf + j * 16 + kb * 4, v.x, v.y, v.z, v.w);
           }
           for (int c = 0; c < sfb_chunks; ++c) {
             const uint4 v = ptx::lds128(st + off_sfb + c * kSfTile + kb * 512 + lane * 16);
@@ -532,12 +499,11 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     const int q = warp & 3;            // tensor-memory lane quarter this warp may access
     constexpr int kParts = epi_warps(SWIGLU) / 4;  // warps sharing a quarter split the token chunks
     const int part = (warp - 2) / 4;
-    const int lrow = q * 32 + lane;    // accumulator row of this thread
+    const int lrow = q * 32 + lane;    // accumulator row = output feature within the tile
     const float a_gs = *p.a_gscale;
     const bool f32_out = p.epi == NVFP4MOE_EPI_SWIGLU_F32;
     const float s_h = (SWIGLU && !f32_out) ? *p.c_gscale : 1.0f;
     const int n_out = SWIGLU ? p.N / 2 : p.N;
-    uint32_t xc = 0;  // exchange chunks done by this warp (its pair partner counts the same chunks)
     SlotSeq slots;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       int e, mb, nb, w;
@@ -551,64 +517,44 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       const int64_t row0 = int64_t(s_rowoff[e]) + int64_t(nb) * BN;
       const float scale = a_gs * p.w_gscale[e];
       const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + uint32_t(s0 * kAccSlotCols);
-      if constexpr (SWIGLU) {
-        // A gate warp (lane quarters 0-1) and the up warp of the same 32
-        // features (quarters 2-3) form a pair; each takes 16 of every 32
-        // tokens and receives the other half's values through shared memory.
-        const bool is_up = q >= 2;
-        const int pair = (q & 1) + 2 * part;
-        bool ok = true;
-        for (int j = 0; ok && j < NA; ++j) {
-          const int f = (mb * NA + j) * C::FEAT + 32 * (q & 1) + lane;  // output feature
-          for (int c0 = 32 * part; c0 < valid; c0 += 32 * kParts, ++xc) {
-            uint32_t v[32];
-            ptx::tmem_ld_32x32b_x32(tbase + j * w + c0, v);
-            ptx::tmem_ld_wait();
-            // buffer xc % 2: gate values of tokens 16..31, then up values of tokens 0..15, [t][lane]
-            float* to_up = xchg + (pair * 2 + (xc & 1u)) * 1024;
-            float* to_gate = to_up + 512;
-            float* send = is_up ? to_gate : to_up;
+      const int f = (SWIGLU ? mb : mb * NA) * kBM + lrow;  // output column (of tile 0)
+      for (int c0 = 32 * part; c0 < valid; c0 += 32 * kParts) {
+        uint32_t g[32];
+        ptx::tmem_ld_32x32b_x32(tbase + c0, g);
+        if constexpr (SWIGLU) {
+          uint32_t u[32];
+          ptx::tmem_ld_32x32b_x32(tbase + w + c0, u);
+          ptx::tmem_ld_wait();
+          // h = silu(gate) * up for 32 tokens of this lane's feature.
+          float h[32];
 #pragma unroll
-            for (int t = 0; t < 16; ++t) send[t * 32 + lane] = __uint_as_float(is_up ? v[t] : v[16 + t]);
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(xchg_bar(pair, xc & 1u));
-            if (!wait_phase(xchg_bar(pair, xc & 1u), (xc >> 1) & 1u, abort_flag)) {
-              ok = false;
-              break;
-            }
-            float h[16];
-#pragma unroll
-            for (int t = 0; t < 16; ++t) {
-              const float gv = is_up ? to_up[t * 32 + lane] : __uint_as_float(v[t]);
-              const float uv = is_up ? __uint_as_float(v[16 + t]) : to_gate[t * 32 + lane];
-              const float gf = gv * scale, uf = uv * scale;
-              h[t] = gf * __frcp_rn(1.0f + __expf(-gf)) * uf;
-            }
-            const int tok0 = c0 + (is_up ? 16 : 0);
-            if (f32_out) {
-              float* out = static_cast<float*>(p.c_out) + (row0 + tok0) * n_out + f;
-#pragma unroll
-              for (int t = 0; t < 16; ++t)
-                if (tok0 + t < valid) out[int64_t(t) * n_out] = h[t];
-            } else {
-              requant_swiglu_chunk<16>(h, lane, s_h, row0 + tok0, valid - tok0, f, n_out,
-                                       static_cast<uint8_t*>(p.c_out), p.c_scales);
-            }
+          for (int i = 0; i < 32; ++i) {
+            const float gf = __uint_as_float(g[i]) * scale;
+            const float uf = __uint_as_float(u[i]) * scale;
+            h[i] = gf * __frcp_rn(1.0f + __expf(-gf)) * uf;
           }
-        }
-      } else {
-        const int f = mb * NA * kBM + lrow;  // output column of the first 128-row block
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.c_out);
-        for (int c0 = 32 * part; c0 < valid; c0 += 32 * kParts) {
+          if (f32_out) {
+            float* out = static_cast<float*>(p.c_out) + (row0 + c0) * n_out + f;
 #pragma unroll
-          for (int j = 0; j < NA; ++j) {
-            uint32_t g[32];
-            ptx::tmem_ld_32x32b_x32(tbase + j * w + c0, g);
+            for (int i = 0; i < 32; ++i)
+              if (c0 + i < valid) out[int64_t(i) * n_out] = h[i];
+          } else {
+            requant_swiglu_chunk(h, lane, s_h, row0 + c0, valid - c0, f, n_out, static_cast<uint8_t*>(p.c_out),
+                                 p.c_scales);
+          }
+        } else {
+          ptx::tmem_ld_wait();
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.c_out);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c0 + i < valid) out[(row0 + c0 + i) * n_out + f] = __float2bfloat16_rn(__uint_as_float(g[i]) * scale);
+          if constexpr (NA == 2) {  // the second 128-row block of the tile
+            ptx::tmem_ld_32x32b_x32(tbase + w + c0, g);
             ptx::tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               if (c0 + i < valid)
-                out[(row0 + c0 + i) * n_out + f + j * kBM] = __float2bfloat16_rn(__uint_as_float(g[i]) * scale);
+                out[(row0 + c0 + i) * n_out + f + kBM] = __float2bfloat16_rn(__uint_as_float(g[i]) * scale);
           }
         }
       }
@@ -679,17 +625,17 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   // The whole opt-in shared memory is requested; the kernel sizes its stages
   // for the widest token tile present.  Two stages of the widest possible
   // tile must fit.
-  const int64_t usable = int64_t(smem_optin) - 1024 - ctrl_bytes(a.E) - C::XCHG;
+  const int64_t usable = int64_t(smem_optin) - 1024 - ctrl_bytes(a.E);
   const int worst = C::stage_bytes(BN);
   if (usable < 2 * int64_t(worst)) {
     set_error_detail(
         "grouped GEMM tile %dx%d (%s) needs %lld bytes of shared memory for a 2-stage pipeline; Hardware limit: %d",
-        kBM * NA, BN, SWIGLU ? "gate/up" : "down", (long long)(1024 + ctrl_bytes(a.E) + C::XCHG + 2 * int64_t(worst)), smem_optin);
+        kBM * NA, BN, SWIGLU ? "gate/up" : "down", (long long)(1024 + ctrl_bytes(a.E) + 2 * int64_t(worst)), smem_optin);
     return NVFP4MOE_ERR_SMEM;
   }
   const size_t smem = size_t(smem_optin);
   CUtensorMap tw, ta;
-  if (!encode_kmajor_map(&tw, a.w_packed, int64_t(a.E) * a.N, a.K / 2, SWIGLU ? kBM / 2 : kBM) ||
+  if (!encode_kmajor_map(&tw, a.w_packed, int64_t(a.E) * a.N, a.K / 2, kBM) ||
       !encode_kmajor_map(&ta, a.a_packed, a.rows_capacity, a.K / 2, 32)) {
     set_error_detail("cuTensorMapEncodeTiled failed or is unavailable");
     return NVFP4MOE_ERR_CUDA;
@@ -734,12 +680,7 @@ int launch_grouped_gemm(const GemmArgs& a, int num_sms, int smem_optin, cudaStre
   // Small experts (decode): two 128-row weight tiles per stage, so each stage
   // carries twice the weight bytes and two independent accumulation chains.
   const bool pair = a.N % (2 * kBM) == 0 && a.m_total <= int64_t(64) * a.E;
-  // SwiGLU: two paired gate/up tiles per stage at decode sizes; one per stage
-  // when experts are large, so a 128-token tile needs a single accumulator
-  // slot and its epilogue overlaps the next tile's MMAs.
-  const bool swiglu_pair = a.m_total <= int64_t(32) * a.E;
-  if (swiglu && bn == 128 && swiglu_pair) return launch_impl<128, 2, true>(a, num_sms, smem_optin, st);
-  if (swiglu && bn == 128) return launch_impl<128, 1, true>(a, num_sms, smem_optin, st);
+  if (swiglu && bn == 128) return launch_impl<128, 2, true>(a, num_sms, smem_optin, st);
   if (!swiglu && bn == 128 && pair) return launch_impl<128, 2, false>(a, num_sms, smem_optin, st);
   if (!swiglu && bn == 128) return launch_impl<128, 1, false>(a, num_sms, smem_optin, st);
   if (!swiglu && bn == 256) return launch_impl<256, 1, false>(a, num_sms, smem_optin, st);
