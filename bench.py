@@ -36,6 +36,22 @@ FALLBACK_BF16_TFLOPS = 1900.0
 FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense FP4 / BF16 tensor ratio
 
 
+def recorded_traffic(workload, kernel):
+    """DRAM bytes per launch of `kernel` from the ncu record in profiles/, or
+    None when there is none for this workload or the kernel sources changed
+    since it was taken."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    src = "".join(open(os.path.join(ROOT, n)).read() for n in rec.get("source_files", []))
+    if hashlib.sha256(src.encode()).hexdigest() != rec.get("source_sha256"):
+        return None
+    return rec.get(workload, {}).get(kernel)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -259,7 +275,8 @@ def run_ours(args, w):
         "layer_roofline_frac": round(layer_frac, 4),
         "kernels_ms": {n: round(float(v), 4) for n, v in zip(KERNEL_NAMES, kern_ms)},
         "roofline": {"kernel": "gemm_gate_up_swiglu", "bound": bound, "achieved": round(achieved, 1),
-                     "peak": round(peak, 1), "unit": unit, "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak": round(peak, 1), "unit": unit, "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(w.name, "gemm_gate_up_swiglu"),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if bound == "hbm" else
                      f"{peak_kind} bf16 x {FP4_OVER_BF16:g} nominal fp4/bf16 ratio"},
         "e2e": {"value": round(job_throughput(w.T, world, e2e_ms), 1), "unit": "tokens/s",
