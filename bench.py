@@ -117,7 +117,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
         return self
@@ -157,32 +157,50 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # the CUDA path
 # ----------------------------------------------------------------------------
-def timed_step_with_kernel_events(B, layer, x, logits, ev):
-    """One layer forward with events between the library calls (same calls,
-    same order as MoELayer.forward, all on the current stream)."""
+def step_with_kernel_events(B, layer, x, logits, ev):
+    """One layer forward with events between the library calls (the same
+    calls, in the same order, as MoELayer.forward, on the current stream).
+    An event between two kernels ends their launch overlap, so these
+    per-kernel durations are those of isolated launches."""
     p = layer.perm
     T = x.shape[0]
-    ev[0].record()
-    B.moe_route_topk(logits, layer.k, layer.score_fn, layer.renormalize, layer.bias, layer.topk_idx, layer.topk_w)
-    ev[1].record()
-    B.moe_quantize_nvfp4(x, global_scale=layer.x_gscale, compute_global=True, packed=layer.xq, scales=layer.xs,
-                         workspace=layer.q_ws)
-    ev[2].record()
-    B.moe_permute(layer.topk_idx, layer.E, layer.xq, layer.xs, out=p, workspace=layer.p_ws)
-    ev[3].record()
+    i = 0
+    ev[i].record()
+    if layer.fused_prepare:
+        B.moe_prepare(logits, x, layer.k, layer.score_fn, layer.renormalize, layer.bias, layer.topk_idx,
+                      layer.topk_w, layer.x_gscale, layer.xq, layer.xs, out=p, workspace=layer.prep_ws)
+        i += 1
+        ev[i].record()
+    else:
+        B.moe_route_topk(logits, layer.k, layer.score_fn, layer.renormalize, layer.bias, layer.topk_idx,
+                         layer.topk_w)
+        i += 1
+        ev[i].record()
+        B.moe_quantize_nvfp4(x, global_scale=layer.x_gscale, compute_global=True, packed=layer.xq,
+                             scales=layer.xs, workspace=layer.q_ws)
+        i += 1
+        ev[i].record()
+        B.moe_permute(layer.topk_idx, layer.E, layer.xq, layer.xs, out=p, workspace=layer.p_ws)
+        i += 1
+        ev[i].record()
     B.moe_grouped_gemm_nvfp4(p.a_packed, p.a_scales, layer.x_gscale, p.counts, p.row_offsets, layer.w_gu_packed,
                              layer.w_gu_scales, layer.w_gu_gscale, B.EPI_SWIGLU_NVFP4, c_gscale=layer.h_scale,
                              m_total=T * layer.k, tile_n=layer.tile_n[0], out=layer.hq, out_scales=layer.hs)
-    ev[4].record()
+    i += 1
+    ev[i].record()
     B.moe_grouped_gemm_nvfp4(layer.hq, layer.hs, layer.h_scale, p.counts, p.row_offsets, layer.w_d_packed,
                              layer.w_d_scales, layer.w_d_gscale, B.EPI_BF16, m_total=T * layer.k,
                              tile_n=layer.tile_n[1], out=layer.y)
-    ev[5].record()
+    i += 1
+    ev[i].record()
     B.moe_finalize(layer.y, p.flat_to_perm, layer.topk_w, out=layer.out)
-    ev[6].record()
+    i += 1
+    ev[i].record()
 
 
-KERNEL_NAMES = ["route", "quantize", "permute", "gemm_gate_up_swiglu", "gemm_down", "finalize"]
+def kernel_names(fused_prepare):
+    head = ["prepare"] if fused_prepare else ["route", "quantize", "permute"]
+    return head + ["gemm_gate_up_swiglu", "gemm_down", "finalize"]
 
 
 def run_ours(args, w):
@@ -192,7 +210,7 @@ def run_ours(args, w):
     dev = torch.device("cuda", torch.cuda.current_device())
     inp = W.device_inputs(w, seed=args.seed + rank, device=dev)
     layer = B.MoELayer(inp["w_gu"], inp["w_d"], w.k, w.score, w.renormalize, w.h_scale, bias=inp["bias"],
-                       T=w.T, tile_n=(args.tile_gate_up, args.tile_down))
+                       T=w.T, tile_n=(args.tile_gate_up, args.tile_down), fused_prepare=not args.separate_prepare)
     del inp["w_gu"], inp["w_d"]
     torch.cuda.empty_cache()
     x, logits = inp["x"], inp["logits"]
@@ -201,27 +219,37 @@ def run_ours(args, w):
     B.sync_status()
     counts = layer.perm.counts.cpu().numpy()
     n_active = int((counts > 0).sum())
-
-    # ---- device-timed region: inputs resident in HBM ----
     stream = torch.cuda.current_stream()
-    n_ev = 7
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+
+    # ---- device-timed region: inputs resident in HBM, the layer as a user calls it ----
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
         start.record(stream)
-        for s in range(args.steps):
-            timed_step_with_kernel_events(B, layer, x, logits, evs[s])
+        for _ in range(args.steps):
+            layer(x, logits)
         stop.record(stream)
         torch.cuda.synchronize()
     barrier(world)
     B.sync_status()
-    ms_total = start.elapsed_time(stop)
-    ms_step = max_over_ranks(ms_total / args.steps, world)
+    ms_step = max_over_ranks(start.elapsed_time(stop) / args.steps, world)
+
+    # ---- kernel-timing region: the same steps with events between the calls ----
+    names = kernel_names(layer.fused_prepare)
+    n_ev = len(names) + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for s in range(args.steps):
+        step_with_kernel_events(B, layer, x, logits, evs[s])
+    torch.cuda.synchronize()
+    barrier(world)
+    B.sync_status()
     per_kernel = np.array([[evs[s][i].elapsed_time(evs[s][i + 1]) for i in range(n_ev - 1)]
                            for s in range(args.steps)])
     kern_ms = per_kernel.mean(axis=0)
+    ms_step_events = float(per_kernel.sum(axis=1).mean())
 
     # ---- end to end: pinned host inputs in, result out, every step ----
     x_h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x)
@@ -252,7 +280,7 @@ def run_ours(args, w):
     w_bytes_active = n_active * W.nvfp4_bytes(3 * w.H * w.I)
     alg_bytes = w_bytes_active + 2 * w.T * w.H * 2
     tokens_s = job_throughput(w.T, world, ms_step)
-    gu_ms = kern_ms[3]
+    gu_ms = kern_ms[names.index("gemm_gate_up_swiglu")]
     gu_bytes = n_active * W.nvfp4_bytes(2 * w.I * w.H) + W.nvfp4_bytes(R * w.H) + W.nvfp4_bytes(R * w.I)
     gu_flops = 4.0 * R * w.H * w.I
     gu_hbm_time = gu_bytes / (hbm_peak * 1e9)
@@ -273,7 +301,9 @@ def run_ours(args, w):
         "tflops": round(flops * world / (ms_step * 1e-3) / 1e12, 2),
         "hbm_gbs": round(alg_bytes * world / (ms_step * 1e-3) / 1e9, 1),
         "layer_roofline_frac": round(layer_frac, 4),
-        "kernels_ms": {n: round(float(v), 4) for n, v in zip(KERNEL_NAMES, kern_ms)},
+        "kernels_ms": {n: round(float(v), 4) for n, v in zip(names, kern_ms)},
+        "ms_per_step_with_events": round(ms_step_events, 4),
+        "prepare": "fused (one launch)" if layer.fused_prepare else "separate (route, quantise, permute)",
         "roofline": {"kernel": "gemm_gate_up_swiglu", "bound": bound, "achieved": round(achieved, 1),
                      "peak": round(peak, 1), "unit": unit, "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic(w.name, "gemm_gate_up_swiglu"),
@@ -282,7 +312,7 @@ def run_ours(args, w):
         "e2e": {"value": round(job_throughput(w.T, world, e2e_ms), 1), "unit": "tokens/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clk.summary(),
-        "gpu_launches": B.MoELayer.LAUNCHES_PER_FORWARD * args.steps,
+        "gpu_launches": layer.launches_per_forward * args.steps,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, args, layer_inputs=(x, logits, inp["bias"], layer))
@@ -296,43 +326,63 @@ def run_ours(args, w):
 # ----------------------------------------------------------------------------
 # the CPU oracle on a bounded sample (baseline and reference arm)
 # ----------------------------------------------------------------------------
-def oracle_sample(w, x, logits, bias, w_gu_dev, w_d_dev, experts):
-    """Oracle layer on the routed rows of `experts` (weights quantised by the
-    oracle beforehand, untimed).  Returns (seconds, rows processed)."""
+def oracle_quantized_weights(w_gu_dev, w_d_dev, experts):
+    """Oracle NVFP4 quantisation of the weights of `experts` (untimed setup)."""
     from oracle import nvfp4_moe_oracle as O
     q = {}
     for e in experts:
         for name, src in (("gu", w_gu_dev), ("d", w_d_dev)):
-            a = src[e].float().cpu().numpy()
+            a = src[int(e)].float().cpu().numpy()
             g = O.global_scale(a)
             p, s = O.quantize_nvfp4(a, g)
-            q[(name, e)] = (p, s, g)
-    x32 = x.float().cpu().numpy()
-    lg = logits.cpu().numpy()
-    b = None if bias is None else bias.cpu().numpy()
+            q[(name, int(e))] = (p, s, g)
+    return q
+
+
+def oracle_sample(w, x32, lg, b, q, experts, islice=None):
+    """The oracle layer restricted to the routed rows of `experts`.
+
+    Times separately the batch-wide steps (routing of every token, the global
+    scale of x, the permutation) and the per-expert steps (quantising the
+    expert's token rows, gate/up GEMM, SwiGLU, requantisation, down GEMM and
+    the weighted scatter into the output).  With islice = (a, b) only the
+    intermediate columns [a, b) of each expert are computed: gate rows
+    [a, b), up rows [I + a, I + b) and the down GEMM over that K range (a
+    partial sum of the expert's output); a and b are multiples of 64.
+    Returns (batch seconds, expert seconds, rows processed, number of active
+    experts)."""
+    from oracle import nvfp4_moe_oracle as O
     t0 = time.perf_counter()
     idx, wts = O.route_topk(lg, b, w.k, w.score, w.renormalize)
     s_x = O.global_scale(x32)
-    xq, xs = O.quantize_nvfp4(x32, s_x)
     counts, offsets, p2f, f2p = O.permute(idx, w.E)
+    t1 = time.perf_counter()
     out = np.zeros((w.T, w.H))
     rows = 0
     for e in experts:
+        e = int(e)
         r0, r1 = int(offsets[e]), int(offsets[e + 1])
         if r1 == r0:
             continue
         tok = p2f[r0:r1] // w.k
+        xq, xs = O.quantize_nvfp4(x32[tok], s_x)
         gp, gs, gg = q[("gu", e)]
         dp, ds, dg = q[("d", e)]
+        a, c = (0, w.I) if islice is None else islice
+        if (a, c) != (0, w.I):
+            sel = np.r_[a:c, w.I + a:w.I + c]
+            gp, gs = gp[sel], gs[sel]
+            dp, ds = dp[:, a // 2:c // 2], ds[:, a // 16:c // 16]
         sub = np.array([0, r1 - r0])
-        gu = O.grouped_gemm(xq[tok], xs[tok], s_x, sub, gp[None], gs[None], np.array([gg]))
-        h = O.swiglu(gu, w.I).astype(np.float32)
+        gu = O.grouped_gemm(xq, xs, s_x, sub, gp[None], gs[None], np.array([gg]))
+        h = O.swiglu(gu, c - a).astype(np.float32)
         hq, hs = O.quantize_nvfp4(h, np.float32(w.h_scale))
         y = O.round_to_bf16(O.grouped_gemm(hq, hs, np.float32(w.h_scale), sub, dp[None], ds[None], np.array([dg])))
         np.add.at(out, tok, wts.reshape(-1)[p2f[r0:r1]][:, None] * y)
         rows += r1 - r0
     O.round_to_bf16(out)
-    return time.perf_counter() - t0, rows
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1, rows, int((counts > 0).sum())
 
 
 def cpu_baseline(w, args, layer_inputs):
@@ -343,14 +393,18 @@ def cpu_baseline(w, args, layer_inputs):
     experts = active[np.linspace(0, len(active) - 1, n).astype(int)]
     # weights in bf16 for the sampled experts, regenerated from the same seed
     inp = W.device_inputs(w, seed=args.seed, device=x.device)
-    secs, rows = oracle_sample(w, x, logits, bias, inp["w_gu"], inp["w_d"], experts)
+    q = oracle_quantized_weights(inp["w_gu"], inp["w_d"], experts)
     del inp
     torch.cuda.empty_cache()
-    full = secs * len(active) / n
+    x32 = x.float().cpu().numpy()
+    lg = logits.cpu().numpy()
+    b = None if bias is None else bias.cpu().numpy()
+    t_batch, t_exp, rows, n_active = oracle_sample(w, x32, lg, b, q, experts)
+    full = t_batch + t_exp * n_active / n
     return {"value": round(w.T / full, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{n} of {len(active)} active experts ({rows} routed rows) through the float64 oracle in "
-                      f"{secs:.1f} s; layer time extrapolated by active experts (x{len(active) / n:.1f}); "
-                      f"elementwise steps on one thread, float64 matmuls on the BLAS pool"}
+            "sample": f"batch-wide steps ({t_batch:.2f} s) plus {n} of {n_active} active experts ({rows} routed "
+                      f"rows, {t_exp:.1f} s) through the float64 oracle; layer time = batch steps + expert time "
+                      f"x {n_active / n:.1f}; elementwise steps on one thread, float64 matmuls on the BLAS pool"}
 
 
 def run_reference(args, w):
@@ -362,15 +416,26 @@ def run_reference(args, w):
     dev = torch.device("cuda", 0)
     inp = W.device_inputs(w, seed=args.seed, device=dev)
     from oracle import nvfp4_moe_oracle as O
-    idx, _ = O.route_topk(inp["logits"].cpu().numpy(), None if inp["bias"] is None else inp["bias"].cpu().numpy(),
-                          w.k, w.score, w.renormalize)
+    x32 = inp["x"].float().cpu().numpy()
+    lg = inp["logits"].cpu().numpy()
+    b = None if inp["bias"] is None else inp["bias"].cpu().numpy()
+    idx, _ = O.route_topk(lg, b, w.k, w.score, w.renormalize)
     active = np.unique(idx)
+    # a small fixed set of experts, quantised once (untimed) and cycled through the steps
+    cycle = active[np.linspace(0, len(active) - 1, min(len(active), 4)).astype(int)]
+    q = oracle_quantized_weights(inp["w_gu"], inp["w_d"], cycle)
+    del inp
+    torch.cuda.empty_cache()
     times = []
+    width = min(w.I, 256)
+    nsl = w.I // width
     for s in range(args.warmup + args.steps):
-        e = int(active[s % len(active)])
-        secs, _ = oracle_sample(w, inp["x"], inp["logits"], inp["bias"], inp["w_gu"], inp["w_d"], [e])
+        j = s % (len(cycle) * nsl)
+        sl = ((j % nsl) * width, (j % nsl + 1) * width)
+        t_batch, t_exp, _, n_active = oracle_sample(w, x32, lg, b, q, [cycle[j // nsl]], islice=sl)
         if s >= args.warmup:
-            times.append(secs * len(active))   # one expert per step, extrapolated to the layer
+            # one slice of one expert per step, extrapolated to the layer
+            times.append(t_batch + t_exp * nsl * n_active)
     ms = float(np.mean(times)) * 1e3
     val = w.T / (ms * 1e-3)
     res = {"metric": METRIC, "impl": "reference", "value": round(val, 4), "unit": "tokens/s", "n_gpus": world,
@@ -378,8 +443,11 @@ def run_reference(args, w):
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": w.name, **w.describe(), "active_experts": int(len(active))},
            "cpu_baseline": {"value": round(val, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-                            "sample": "one active expert's routed rows per step through the float64 oracle, "
-                                      "extrapolated by the number of active experts"},
+                            "sample": f"per step: the batch-wide steps (routing, global scale, permutation) "
+                                      f"plus one {width}-column slice of the intermediate dimension of one active "
+                                      f"expert (of a cycled set of 4) for its routed rows through the float64 "
+                                      f"oracle; the expert part multiplied by {nsl} slices and the number of "
+                                      f"active experts"},
            "e2e": {"value": round(val, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
 
@@ -387,8 +455,8 @@ def run_reference(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS) + sorted(W.PROFILE_WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
@@ -396,6 +464,8 @@ def main():
     ap.add_argument("--tile-down", type=int, default=0)
     ap.add_argument("--cpu-experts", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--separate-prepare", action="store_true",
+                    help="route, quantise and permute as separate calls instead of moe_prepare")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

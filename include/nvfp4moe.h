@@ -37,6 +37,12 @@
  *     exceeded its time limit) do not fault: they skip the offending work and
  *     raise a sticky device flag that nvfp4moe_sync_status() reports.
  *   - Only compute capability 10.3 (GB300) is supported.
+ *   - Kernels other than the grouped GEMM (and the cooperative moe_prepare
+ *     kernel) are launched with programmatic dependent launch: such a kernel
+ *     may be scheduled while the kernel before it in the stream drains, and
+ *     waits for that kernel's completion before it reads or writes any
+ *     buffer.  Stream order is therefore kept for every caller.
+ *     NVFP4MOE_PDL=0 in the environment turns the overlap off.
  */
 #ifndef NVFP4MOE_H
 #define NVFP4MOE_H
@@ -193,6 +199,40 @@ int moe_permute_no_alloc(const int32_t* topk_idx, int T, int E, int k,
                          int32_t* expert_counts, int32_t* expert_offsets, int32_t* row_offsets,
                          int32_t* perm_to_flat, int32_t* flat_to_perm,
                          uint8_t* a_packed, uint8_t* a_scales, cudaStream_t stream);
+
+/* ---- a1 + a2 + a3 in one launch -------------------------------------------
+ * moe_route_topk, moe_quantize_nvfp4 (NVFP4MOE_QUANT_COMPUTE_GLOBAL,
+ * row-major scales) and moe_permute fused into one cooperative kernel, for
+ * decode-sized batches where each separate launch costs more than its work
+ * (page A, Research Report sections 2-4 and Key Findings item 8: a MoE path
+ * that is fast at large batch loses at interactive batch sizes to its
+ * preprocessing; page B, Discovery: the fused-MoE module's enable_pdl
+ * option).  The kernel keeps every CTA resident and separates the steps by
+ * grid-wide barriers: route and the partial amax of x, then the global scale,
+ * quantisation and segment ranks, then the expert scan, then placement and
+ * the gather.  Every output is bit-identical to the three separate calls:
+ *   topk_idx, topk_w [T, k] as moe_route_topk (logits device float32 [T, E],
+ *     bias device float32 [E] or NULL, score_fn, renormalize);
+ *   x_gscale device float32 [1], xq uint8 [T, H/2], xs uint8 [T, H/16] as
+ *     moe_quantize_nvfp4 of x (device bf16 [T, H]);
+ *   expert_counts .. a_scales as moe_permute (rows_capacity =
+ *     moe_permute_rows_capacity(T, E, k)).
+ * Limits: T >= 0, 1 <= E <= 1024, 1 <= k <= min(E, 32), H % 64 == 0,
+ * T*k <= 2^30.  ws: device, at least moe_prepare_workspace_size(T, E, k)
+ * bytes, 256-byte aligned, ZERO-FILLED before its first use (its first 256
+ * bytes hold the grid-barrier words; every call that completes leaves them
+ * ready for the next call, so zero it once).  After a call that raised
+ * NVFP4MOE_ERR_TIMEOUT, zero it again.  Calls sharing one workspace must not
+ * overlap on the GPU.  A barrier wait that exceeds its time limit abandons
+ * the kernel and raises NVFP4MOE_ERR_TIMEOUT (sticky). */
+size_t moe_prepare_workspace_size(int T, int E, int k);
+int moe_prepare(const float* logits, const float* bias, const void* x_bf16,
+                int T, int E, int k, int H, int score_fn, int renormalize,
+                int32_t* topk_idx, float* topk_w, float* x_gscale, uint8_t* xq, uint8_t* xs,
+                int32_t* expert_counts, int32_t* expert_offsets, int32_t* row_offsets,
+                int32_t* perm_to_flat, int32_t* flat_to_perm,
+                uint8_t* a_packed, uint8_t* a_scales,
+                void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ---- a4/a5: grouped GEMM ---------------------------------------------------
  * The grouped ("array") block-scaled GEMM over experts (page C, Context and

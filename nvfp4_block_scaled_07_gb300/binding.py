@@ -49,6 +49,9 @@ _SIGS = {
     "moe_permute_workspace_size": (_sz, [_i, _i, _i]),
     "moe_permute": (_i, [_p, _i, _i, _i, _p, _p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
     "moe_permute_no_alloc": (_i, [_p, _i, _i, _i, _p, _p, _i, _p, _p, _p, _p, _p, _p, _p, _p]),
+    "moe_prepare_workspace_size": (_sz, [_i, _i, _i]),
+    "moe_prepare": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p,
+                         _sz, _p]),
     "moe_grouped_gemm_nvfp4_workspace_size": (_sz, [_i, _i, _i, _i]),
     "moe_grouped_gemm_nvfp4": (_i, [_p, _p, _p, _p, _p, _i, _i64, _i64, _p, _p, _p, _i, _i, _i, _p, _p, _p, _i,
                                     _p, _sz, _p]),
@@ -257,6 +260,55 @@ def moe_permute_no_alloc(topk_idx, E, xq, xs, out: Permutation = None):
     return out
 
 
+# ---- a1 + a2 + a3 in one launch ------------------------------------------------------
+def moe_prepare_workspace_size(T, E, k):
+    return int(_lib.moe_prepare_workspace_size(T, E, k))
+
+
+def alloc_prepare_workspace(T, E, k, device):
+    """Zero-filled workspace for moe_prepare (its barrier words must start at 0)."""
+    return torch.zeros((moe_prepare_workspace_size(T, E, k),), dtype=torch.uint8, device=device)
+
+
+def moe_prepare(logits, x, k, score_fn="sigmoid", renormalize=True, bias=None, topk_idx=None, topk_w=None,
+                x_gscale=None, xq=None, xs=None, out: Permutation = None, workspace=None):
+    """Route, quantise and permute in one launch.
+
+    Returns (topk_idx, topk_w, x_gscale, xq, xs, Permutation), each equal bit
+    for bit to moe_route_topk + moe_quantize_nvfp4 + moe_permute."""
+    _need(logits, torch.float32, name="logits")
+    _need(x, torch.bfloat16, name="x")
+    T, E = logits.shape
+    H = x.shape[1]
+    if x.shape[0] != T:
+        raise ValueError(f"x has {x.shape[0]} rows, logits {T}")
+    dev = x.device
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    topk_idx = _empty((T, k), torch.int32, dev) if topk_idx is None else topk_idx
+    topk_w = _empty((T, k), torch.float32, dev) if topk_w is None else topk_w
+    x_gscale = _empty((1,), torch.float32, dev) if x_gscale is None else x_gscale
+    xq = _empty((T, H // 2), torch.uint8, dev) if xq is None else xq
+    xs = _empty((T, H // 16), torch.uint8, dev) if xs is None else xs
+    _need(topk_idx, torch.int32, (T, k), "topk_idx")
+    _need(topk_w, torch.float32, (T, k), "topk_w")
+    _need(x_gscale, torch.float32, (1,), "x_gscale")
+    _need(xq, torch.uint8, (T, H // 2), "xq")
+    _need(xs, torch.uint8, (T, H // 16), "xs")
+    if out is None:
+        out = alloc_permutation(T, E, k, H, dev)
+    if workspace is None:
+        workspace = alloc_prepare_workspace(T, E, k, dev)
+    _need(workspace, torch.uint8, name="workspace")
+    _check(_lib.moe_prepare(_ptr(logits), _ptr(bias), _ptr(x), T, E, k, H, SCORE[score_fn], int(bool(renormalize)),
+                            _ptr(topk_idx), _ptr(topk_w), _ptr(x_gscale), _ptr(xq), _ptr(xs), _ptr(out.counts),
+                            _ptr(out.offsets), _ptr(out.row_offsets), _ptr(out.perm_to_flat),
+                            _ptr(out.flat_to_perm), _ptr(out.a_packed), _ptr(out.a_scales), _ptr(workspace),
+                            workspace.numel(), _stream()),
+           "moe_prepare")
+    return topk_idx, topk_w, x_gscale, xq, xs, out
+
+
 # ---- a4/a5 ---------------------------------------------------------------------
 def moe_grouped_gemm_nvfp4(a_packed, a_scales, a_gscale, counts, row_offsets, w_packed, w_scales, w_gscale,
                            epilogue=EPI_BF16, c_gscale=None, m_total=None, tile_n=0, out=None, out_scales=None):
@@ -323,12 +375,15 @@ def moe_finalize(y, flat_to_perm, topk_w, out=None):
 class MoELayer:
     """NVFP4 expert weights plus every buffer of one layer shape.
 
-    forward() enqueues the six library calls (route, quantise, permute,
-    gate/up GEMM with SwiGLU + requantisation, down GEMM, finalize) on the
-    current stream and allocates nothing."""
+    forward() enqueues the layer on the current stream and allocates
+    nothing: with fused_prepare (the default) four launches -- moe_prepare
+    (route + quantise + permute), gate/up GEMM with SwiGLU and
+    requantisation, down GEMM, finalize -- otherwise the six separate calls
+    (nine launches and one memset)."""
 
     def __init__(self, w_gu, w_d, k, score_fn="sigmoid", renormalize=True, h_scale=2.0 ** -4, bias=None,
-                 T=None, tile_n=(0, 0)):
+                 T=None, tile_n=(0, 0), fused_prepare=True):
+        self.fused_prepare = bool(fused_prepare)
         self.E, two_i, self.H = w_gu.shape
         self.I = two_i // 2
         self.k, self.score_fn, self.renormalize = k, score_fn, renormalize
@@ -353,6 +408,7 @@ class MoELayer:
         self.q_ws = _empty((64,), torch.uint8, dev)
         self.perm = alloc_permutation(T, E, k, H, dev)
         self.p_ws = _empty((moe_permute_workspace_size(T, E, k),), torch.uint8, dev)
+        self.prep_ws = alloc_prepare_workspace(T, E, k, dev)
         cap = self.perm.rows_capacity
         self.hq = _empty((cap, I // 2), torch.uint8, dev)
         self.hs = _empty((blocked_scales_bytes(cap, I),), torch.uint8, dev)
@@ -364,10 +420,14 @@ class MoELayer:
         if self.T != T:
             self._alloc(T)
         p = self.perm
-        moe_route_topk(logits, self.k, self.score_fn, self.renormalize, self.bias, self.topk_idx, self.topk_w)
-        moe_quantize_nvfp4(x, global_scale=self.x_gscale, compute_global=True, packed=self.xq, scales=self.xs,
-                           workspace=self.q_ws)
-        moe_permute(self.topk_idx, self.E, self.xq, self.xs, out=p, workspace=self.p_ws)
+        if self.fused_prepare:
+            moe_prepare(logits, x, self.k, self.score_fn, self.renormalize, self.bias, self.topk_idx, self.topk_w,
+                        self.x_gscale, self.xq, self.xs, out=p, workspace=self.prep_ws)
+        else:
+            moe_route_topk(logits, self.k, self.score_fn, self.renormalize, self.bias, self.topk_idx, self.topk_w)
+            moe_quantize_nvfp4(x, global_scale=self.x_gscale, compute_global=True, packed=self.xq,
+                               scales=self.xs, workspace=self.q_ws)
+            moe_permute(self.topk_idx, self.E, self.xq, self.xs, out=p, workspace=self.p_ws)
         moe_grouped_gemm_nvfp4(p.a_packed, p.a_scales, self.x_gscale, p.counts, p.row_offsets, self.w_gu_packed,
                                self.w_gu_scales, self.w_gu_gscale, EPI_SWIGLU_NVFP4, c_gscale=self.h_scale,
                                m_total=T * self.k, tile_n=self.tile_n[0], out=self.hq, out_scales=self.hs)
@@ -378,5 +438,8 @@ class MoELayer:
 
     __call__ = forward
 
-    # kernels launched by one forward(): route 1, quantise 2, permute 3, GEMMs 2, finalize 1
-    LAUNCHES_PER_FORWARD = 9
+    # kernels launched by one forward(): fused prepare 1 (else route 1, quantise 2, permute 3),
+    # GEMMs 2, finalize 1
+    @property
+    def launches_per_forward(self):
+        return 4 if self.fused_prepare else 9

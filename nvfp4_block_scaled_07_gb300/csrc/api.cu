@@ -280,6 +280,46 @@ int moe_permute_no_alloc(const int32_t* topk_idx, int T, int E, int k, const uin
                      "permute (static scratch) launch");
 }
 
+// ---- a1 + a2 + a3 -----------------------------------------------------------
+size_t moe_prepare_workspace_size(int T, int E, int k) {
+  if (T < 0 || E < 1 || k < 1) return 0;
+  return size_t(prepare_layout(T, E, k).bytes);
+}
+
+int moe_prepare(const float* logits, const float* bias, const void* x_bf16, int T, int E, int k, int H,
+                int score_fn, int renormalize, int32_t* topk_idx, float* topk_w, float* x_gscale, uint8_t* xq,
+                uint8_t* xs, int32_t* expert_counts, int32_t* expert_offsets, int32_t* row_offsets,
+                int32_t* perm_to_flat, int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales, void* ws,
+                size_t ws_bytes, cudaStream_t stream) {
+  t_detail[0] = 0;
+  NVFP4MOE_REQUIRE(T >= 0, NVFP4MOE_ERR_INVALID_ARG, "T = %d must be >= 0", T);
+  NVFP4MOE_REQUIRE(E >= 1 && E <= 1024, NVFP4MOE_ERR_UNSUPPORTED, "E = %d outside [1, 1024]", E);
+  NVFP4MOE_REQUIRE(k >= 1 && k <= E && k <= 32, NVFP4MOE_ERR_UNSUPPORTED, "k = %d outside [1, min(E, 32)]", k);
+  NVFP4MOE_REQUIRE(H > 0 && H % 64 == 0, NVFP4MOE_ERR_UNSUPPORTED, "H = %d must be a positive multiple of 64", H);
+  NVFP4MOE_REQUIRE(int64_t(T) * k <= (int64_t(1) << 30), NVFP4MOE_ERR_UNSUPPORTED, "T*k too large");
+  NVFP4MOE_REQUIRE(score_fn == NVFP4MOE_SCORE_SOFTMAX || score_fn == NVFP4MOE_SCORE_SIGMOID,
+                   NVFP4MOE_ERR_INVALID_ARG, "score_fn %d", score_fn);
+  NVFP4MOE_REQUIRE(x_gscale && expert_counts && expert_offsets && row_offsets && perm_to_flat,
+                   NVFP4MOE_ERR_INVALID_ARG, "null pointer");
+  NVFP4MOE_REQUIRE(T == 0 || (logits && x_bf16 && topk_idx && topk_w && xq && xs && flat_to_perm && a_packed &&
+                              a_scales),
+                   NVFP4MOE_ERR_INVALID_ARG, "null pointer");
+  NVFP4MOE_REQUIRE(T == 0 || (aligned16(x_bf16) && aligned16(xq) && aligned16(a_packed) && aligned16(a_scales) &&
+                              (reinterpret_cast<uintptr_t>(xs) & 3) == 0),
+                   NVFP4MOE_ERR_INVALID_ARG, "misaligned pointer");
+  const size_t need = moe_prepare_workspace_size(T, E, k);
+  NVFP4MOE_REQUIRE(ws && ws_bytes >= need, NVFP4MOE_ERR_WORKSPACE, "workspace %zu < %zu", ws_bytes, need);
+  NVFP4MOE_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255) == 0, NVFP4MOE_ERR_INVALID_ARG,
+                   "workspace must be 256-byte aligned");
+  DeviceInfo d;
+  if (int st = current_device(&d)) return st;
+  return cuda_status(launch_prepare(logits, bias, x_bf16, T, E, k, H, score_fn, renormalize ? 1 : 0, topk_idx, topk_w,
+                                    x_gscale, xq, xs, expert_counts, expert_offsets, row_offsets, perm_to_flat,
+                                    flat_to_perm, a_packed, a_scales, moe_permute_rows_capacity(T, E, k), ws,
+                                    d.num_sms, stream),
+                     "prepare launch");
+}
+
 // ---- a4/a5 ------------------------------------------------------------------
 size_t moe_grouped_gemm_nvfp4_workspace_size(int E, int N, int K, int epilogue) {
   (void)E;

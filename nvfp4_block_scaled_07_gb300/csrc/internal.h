@@ -43,6 +43,26 @@ cudaError_t launch_permute_static_scratch(const int32_t* topk_idx, int T, int E,
                                           uint8_t* a_packed, uint8_t* a_scales, int64_t rows_capacity, int num_sms,
                                           cudaStream_t st);
 
+// Route + quantise + permute in one cooperative launch.  Workspace layout
+// (bytes from the start, 256-byte aligned pieces): grid-barrier words,
+// per-CTA partial amax, segment ranks [T*k], per-segment expert counts and
+// bases [nseg*E] each.  Segments are 256 flat ids up to
+// kPrepareShortMaxRows routed rows, 1024 above.
+constexpr int64_t kPrepareShortMaxRows = 16384;
+constexpr int kPrepareMaxGrid = 1024;
+
+struct PrepareLayout {
+  int64_t seg_len, nseg;
+  int64_t bar_off, amax_off, rank_off, seg_count_off, seg_base_off, bytes;
+};
+PrepareLayout prepare_layout(int T, int E, int k);
+
+cudaError_t launch_prepare(const float* logits, const float* bias, const void* x, int T, int E, int k, int H,
+                           int score_fn, int renormalize, int32_t* idx, float* w, float* gscale, uint8_t* xq,
+                           uint8_t* xs, int32_t* counts, int32_t* offsets, int32_t* row_offsets, int32_t* perm_to_flat,
+                           int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales, int64_t rows_capacity,
+                           void* ws, int num_sms, cudaStream_t st);
+
 cudaError_t launch_finalize(const void* y, const int32_t* flat_to_perm, const float* w, int T, int k, int H,
                             int64_t rows_capacity, void* out, cudaStream_t st);
 

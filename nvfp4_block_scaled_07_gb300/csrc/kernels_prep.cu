@@ -10,6 +10,8 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "launch.cuh"
+#include "sm103_ptx.cuh"
 
 namespace nvfp4moe {
 
@@ -35,13 +37,9 @@ __device__ __forceinline__ double warp_sum(double v) {
 // lower expert index winning ties.
 // ---------------------------------------------------------------------------
 template <int VPL>
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits,
-                                                         const float* __restrict__ bias, int T, int E, int k,
-                                                         int score_fn, int renorm, int32_t* __restrict__ idx_out,
-                                                         float* __restrict__ w_out) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;  // uniform per warp
+__device__ __forceinline__ void route_token(const float* __restrict__ logits, const float* __restrict__ bias, int t,
+                                            int E, int k, int score_fn, int renorm, int32_t* __restrict__ idx_out,
+                                            float* __restrict__ w_out, int lane) {
   const float* row = logits + int64_t(t) * E;
   float v[VPL];
 #pragma unroll
@@ -99,9 +97,13 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
       den = warp_sum(part);
     }
     wj = ex / den;
-  } else {  // sigmoid of the (biased) logit
-    const double sg = mine ? 1.0 / (1.0 + exp(-double(my_v))) : 0.0;
-    wj = renorm ? sg / warp_sum(sg) : sg;
+  } else {
+    // Sigmoid of the (biased) logit in float32 (expf is within 2 ulp), the
+    // sum over the k selected in float64: the weight is within ~7 ulp of the
+    // exact value, far below the 1e-6 relative bar, at a fraction of the
+    // float64 cost.
+    const float sg = mine ? 1.0f / (1.0f + expf(-my_v)) : 0.0f;
+    wj = renorm ? double(sg / float(warp_sum(double(sg)))) : double(sg);
   }
   if (mine) {
     idx_out[int64_t(t) * k + lane] = my_e;
@@ -109,20 +111,65 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   }
 }
 
+template <int VPL>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits,
+                                                         const float* __restrict__ bias, int T, int E, int k,
+                                                         int score_fn, int renorm, int32_t* __restrict__ idx_out,
+                                                         float* __restrict__ w_out) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;  // uniform per warp
+  route_token<VPL>(logits, bias, t, E, k, score_fn, renorm, idx_out, w_out, threadIdx.x & 31);
+}
+
 // ---------------------------------------------------------------------------
 // a2: bf16 -> NVFP4 ("SM120 FP4 Kernel Research Campaign", section 1 operand
 // types).  One thread per 16-element block: two 128-bit loads, block amax,
 // ue4m3 scale, 16 E2M1 codes packed into 8 bytes.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ float amax8(uint4 q, float m) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+  return m;
+}
+
+// The 16 bf16 values in (lo, hi) with per-tensor scale s -> ue4m3 block
+// scale (returned) and the packed codes, element 2i in the low nibble.
+__device__ __forceinline__ uint32_t nvfp4_block16(uint4 lo, uint4 hi, float s, uint2* packed) {
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  float f[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    f[2 * j] = bf16_lo(w[j]);
+    f[2 * j + 1] = bf16_hi(w[j]);
+  }
+  float a = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) a = fmaxf(a, fabsf(f[j]));
+  const float t = (a / kE2M1Max) / s;
+  const uint32_t sb = f32_to_ue4m3(t);
+  const float d = ue4m3_to_f32(sb) * s;
+  uint32_t p0 = 0, p1 = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    p0 |= e2m1_code(f[j], d) << (4 * j);
+    p1 |= e2m1_code(f[8 + j], d) << (4 * j);
+  }
+  *packed = make_uint2(p0, p1);
+  return sb;
+}
+
+__device__ __forceinline__ float global_scale_of(float amax) { return amax > 0.f ? amax / kGlobalScaleDivisor : 1.0f; }
+
 __global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ x, int64_t nvec,
                                                    unsigned* __restrict__ amax_bits) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   float m = 0.f;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += int64_t(gridDim.x) * blockDim.x) {
-    const uint4 q = x[i];
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
-  }
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += int64_t(gridDim.x) * blockDim.x)
+    m = amax8(x[i], m);
 #pragma unroll
   for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
   __shared__ float red[8];
@@ -139,10 +186,11 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__
                                                        const unsigned* __restrict__ amax_bits,
                                                        float* __restrict__ gscale_out, uint8_t* __restrict__ packed,
                                                        uint8_t* __restrict__ scales, int blocked) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   float s;
   if (amax_bits) {
-    const float a = __uint_as_float(*amax_bits);
-    s = a > 0.f ? a / kGlobalScaleDivisor : 1.0f;
+    s = global_scale_of(__uint_as_float(*amax_bits));
     if (blockIdx.x == 0 && threadIdx.x == 0) *gscale_out = s;
   } else {
     s = *gscale_in;
@@ -156,27 +204,9 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__
     const int64_t row = b / bpr, c16 = b - row * bpr;
     uint32_t sb = 0;
     if (b < nblk) {
-      const uint4 lo = x[2 * b], hi = x[2 * b + 1];
-      const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-      float f[16];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        f[2 * j] = bf16_lo(w[j]);
-        f[2 * j + 1] = bf16_hi(w[j]);
-      }
-      float a = 0.f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) a = fmaxf(a, fabsf(f[j]));
-      const float t = (a / kE2M1Max) / s;
-      sb = f32_to_ue4m3(t);
-      const float d = ue4m3_to_f32(sb) * s;
-      uint32_t p0 = 0, p1 = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        p0 |= e2m1_code(f[j], d) << (4 * j);
-        p1 |= e2m1_code(f[8 + j], d) << (4 * j);
-      }
-      *reinterpret_cast<uint2*>(packed + 8 * b) = make_uint2(p0, p1);
+      uint2 pk;
+      sb = nvfp4_block16(x[2 * b], x[2 * b + 1], s, &pk);
+      *reinterpret_cast<uint2*>(packed + 8 * b) = pk;
     }
     if (blocked)
       scales[blocked_sf_offset(row, c16 >> 2, kblocks) + (c16 & 3)] = uint8_t(sb);
@@ -188,6 +218,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__
 // Row-major [rows, cols/16] scales -> blocked layout, one 4-byte group per thread.
 __global__ void __launch_bounds__(256) scales_to_blocked_kernel(const uint8_t* __restrict__ src, int64_t rows,
                                                                 int64_t cols, uint8_t* __restrict__ dst) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   const int64_t kblocks = cols / 64;
   const int64_t total = ((rows + 127) / 128) * 128 * kblocks;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
@@ -202,38 +234,33 @@ __global__ void __launch_bounds__(256) scales_to_blocked_kernel(const uint8_t* _
 // a3: expert-first permutation ("SM120 FP4 Kernel Research Campaign",
 // section 6: expert-first layout and token reordering).  Stable counting
 // sort of the flat ids by expert in three steps:
-//   rank  - each warp ranks a segment of 1024 flat ids: __match_any groups
-//           equal experts inside 32 ids, a per-warp shared counter carries
-//           the running count across the segment;
+//   rank  - each warp ranks a segment of 32*ITERS flat ids: __match_any
+//           groups equal experts inside 32 ids, a per-warp shared counter
+//           carries the running count across the segment;
 //   scan  - one block turns per-segment counts into per-segment bases,
 //           expert counts, offsets and 128-aligned row offsets (warp scans);
 //   place - one warp per flat id writes the maps and gathers the packed row
 //           and its scales into the expert-padded buffers.
+// Data written earlier in the same grid (the fused prepare kernel) is read
+// with ld.global.cg, which does not allocate in the non-coherent L1.
 // ---------------------------------------------------------------------------
-constexpr int kRankWarps = 8;
-
-__global__ void __launch_bounds__(kRankWarps * 32) permute_rank_kernel(const int32_t* __restrict__ idx, int64_t R,
-                                                                       int E, int nseg,
-                                                                       int32_t* __restrict__ rank,
-                                                                       int32_t* __restrict__ seg_count) {
-  extern __shared__ int32_t cnt_all[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int seg = blockIdx.x * kRankWarps + warp;
-  if (seg >= nseg) return;  // uniform per warp; no block-wide barrier below
-  int32_t* cnt = cnt_all + warp * E;
+template <int ITERS>
+__device__ __forceinline__ void rank_segment(const int32_t* idx, int64_t R, int E, int64_t seg, int32_t* cnt,
+                                             int32_t* __restrict__ rank, int32_t* __restrict__ seg_count,
+                                             int lane) {
   for (int e = lane; e < E; e += 32) cnt[e] = 0;
   __syncwarp();
   const unsigned lt = (1u << lane) - 1u;
-  const int64_t base = int64_t(seg) * kPermuteSegment;
+  const int64_t base = seg * (ITERS * 32);
   // All ids of the segment first, so their loads are in flight together.
-  int ids[kPermuteSegment / 32];
+  int ids[ITERS];
 #pragma unroll
-  for (int it = 0; it < kPermuteSegment / 32; ++it) {
+  for (int it = 0; it < ITERS; ++it) {
     const int64_t f = base + it * 32 + lane;
-    ids[it] = f < R ? idx[f] : -1;
+    ids[it] = f < R ? __ldcg(idx + f) : -1;
   }
 #pragma unroll
-  for (int it = 0; it < kPermuteSegment / 32; ++it) {
+  for (int it = 0; it < ITERS; ++it) {
     const int64_t f = base + it * 32 + lane;
     int e = ids[it];
     if (f < R && (e < 0 || e >= E)) {
@@ -248,7 +275,23 @@ __global__ void __launch_bounds__(kRankWarps * 32) permute_rank_kernel(const int
     __syncwarp();
     if (f < R) rank[f] = r;
   }
-  for (int e = lane; e < E; e += 32) seg_count[int64_t(seg) * E + e] = cnt[e];
+  for (int e = lane; e < E; e += 32) seg_count[seg * E + e] = cnt[e];
+  __syncwarp();
+}
+
+constexpr int kRankWarps = 8;
+
+__global__ void __launch_bounds__(kRankWarps * 32) permute_rank_kernel(const int32_t* __restrict__ idx, int64_t R,
+                                                                       int E, int nseg,
+                                                                       int32_t* __restrict__ rank,
+                                                                       int32_t* __restrict__ seg_count) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  extern __shared__ int32_t cnt_all[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int seg = blockIdx.x * kRankWarps + warp;
+  if (seg >= nseg) return;  // uniform per warp; no block-wide barrier below
+  rank_segment<kPermuteSegment / 32>(idx, R, E, seg, cnt_all + warp * E, rank, seg_count, lane);
 }
 
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot) {
@@ -278,21 +321,29 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot) {
   return res;
 }
 
-__global__ void __launch_bounds__(1024) permute_scan_kernel(const int32_t* __restrict__ seg_count, int nseg, int E,
-                                                            int32_t* __restrict__ seg_base,
-                                                            int32_t* __restrict__ counts,
-                                                            int32_t* __restrict__ offsets,
-                                                            int32_t* __restrict__ row_offsets,
-                                                            int32_t* __restrict__ perm_to_flat,
-                                                            int64_t rows_capacity) {
-  __shared__ int warp_tot[32];
-  __shared__ int tail_start;
-  __shared__ int s_cnt[1024], s_roff[1024];
+// One block of 1024 threads, thread e = expert e (E <= 1024): per-segment
+// bases, counts, offsets [E+1] and 128-aligned row offsets [E+1].  Returns
+// this thread's expert count and row offset.
+__device__ __forceinline__ void scan_experts(const int32_t* seg_count, int nseg, int E, int32_t* __restrict__ seg_base,
+                                             int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                             int32_t* __restrict__ row_offsets, int* warp_tot, int* cnt_out,
+                                             int* roff_out) {
   const int e = threadIdx.x;
   int run = 0;
   if (e < E) {
-    for (int s = 0; s < nseg; ++s) {
-      const int c = seg_count[int64_t(s) * E + e];
+    int s = 0;
+    for (; s + 8 <= nseg; s += 8) {
+      int c[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) c[j] = __ldcg(seg_count + int64_t(s + j) * E + e);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        seg_base[int64_t(s + j) * E + e] = run;
+        run += c[j];
+      }
+    }
+    for (; s < nseg; ++s) {
+      const int c = __ldcg(seg_count + int64_t(s) * E + e);
       seg_base[int64_t(s) * E + e] = run;
       run += c;
     }
@@ -305,14 +356,35 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(const int32_t* __res
     counts[e] = cnt;
     offsets[e] = off;
     row_offsets[e] = roff;
-    s_cnt[e] = cnt;
-    s_roff[e] = roff;
   }
   if (e == E - 1) {
     offsets[E] = off + cnt;
     row_offsets[E] = roff + padded;
-    tail_start = roff + padded;
   }
+  *cnt_out = cnt;
+  *roff_out = roff;
+}
+
+__global__ void __launch_bounds__(1024) permute_scan_kernel(const int32_t* __restrict__ seg_count, int nseg, int E,
+                                                            int32_t* __restrict__ seg_base,
+                                                            int32_t* __restrict__ counts,
+                                                            int32_t* __restrict__ offsets,
+                                                            int32_t* __restrict__ row_offsets,
+                                                            int32_t* __restrict__ perm_to_flat,
+                                                            int64_t rows_capacity) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  __shared__ int warp_tot[32];
+  __shared__ int tail_start;
+  __shared__ int s_cnt[1024], s_roff[1024];
+  int cnt, roff;
+  scan_experts(seg_count, nseg, E, seg_base, counts, offsets, row_offsets, warp_tot, &cnt, &roff);
+  const int e = threadIdx.x;
+  if (e < E) {
+    s_cnt[e] = cnt;
+    s_roff[e] = roff;
+  }
+  if (e == E - 1) tail_start = roff + ((cnt + 127) & ~127);
   __syncthreads();
   // Padding rows of each expert (one warp per expert, coalesced), then the tail.
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -321,6 +393,45 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(const int32_t* __res
     for (int r = c + lane; r < pad; r += 32) perm_to_flat[s_roff[x] + r] = -1;
   }
   for (int64_t p = int64_t(tail_start) + threadIdx.x; p < rows_capacity; p += blockDim.x) perm_to_flat[p] = -1;
+}
+
+// Flat id f (token f / k, slot f % k): its row in the expert-padded layout,
+// both maps, and a copy of the token's packed row and scales.
+__device__ __forceinline__ void place_flat(int64_t f, const int32_t* idx, int k, int E, int seg_len,
+                                           const int32_t* rank, const int32_t* seg_base, const int32_t* row_offsets,
+                                           const uint8_t* xq, const uint8_t* xs, int H,
+                                           int32_t* __restrict__ perm_to_flat, int32_t* __restrict__ flat_to_perm,
+                                           uint8_t* __restrict__ a_packed, uint8_t* __restrict__ a_scales,
+                                           int lane) {
+  const int e = __ldcg(idx + f);
+  if (e < 0 || e >= E) return;  // flagged by the rank step
+  const int64_t seg = f / seg_len;
+  const int64_t row = int64_t(__ldcg(row_offsets + e)) + __ldcg(seg_base + seg * E + e) + __ldcg(rank + f);
+  if (lane == 0) {
+    perm_to_flat[row] = int32_t(f);
+    flat_to_perm[f] = int32_t(row);
+  }
+  const int64_t t = f / k;
+  const uint4* src = reinterpret_cast<const uint4*>(xq + t * (H / 2));
+  uint4* dst = reinterpret_cast<uint4*>(a_packed + row * (H / 2));
+  const int nv = H / 32;  // 16-byte chunks of one packed row
+  for (int c0 = 0; c0 < nv; c0 += 128) {
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = c0 + 32 * j + lane;
+      if (c < nv) v[j] = __ldcg(src + c);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = c0 + 32 * j + lane;
+      if (c < nv) dst[c] = v[j];
+    }
+  }
+  const int64_t kblocks = H / 64;
+  const unsigned* ssrc = reinterpret_cast<const unsigned*>(xs + t * (H / 16));
+  for (int kb = lane; kb < kblocks; kb += 32)
+    *reinterpret_cast<uint32_t*>(a_scales + blocked_sf_offset(row, kb, kblocks)) = __ldcg(ssrc + kb);
 }
 
 __global__ void __launch_bounds__(256) permute_place_kernel(const int32_t* __restrict__ idx, int64_t R, int k, int E,
@@ -333,26 +444,177 @@ __global__ void __launch_bounds__(256) permute_place_kernel(const int32_t* __res
                                                             int32_t* __restrict__ flat_to_perm,
                                                             uint8_t* __restrict__ a_packed,
                                                             uint8_t* __restrict__ a_scales) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
-  const int64_t kblocks = H / 64;
-  for (int64_t f = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); f < R; f += nwarps) {
-    const int e = idx[f];
-    if (e < 0 || e >= E) continue;  // flagged by the rank step
-    const int64_t seg = f / kPermuteSegment;
-    const int64_t row = int64_t(row_offsets[e]) + seg_base[seg * E + e] + rank[f];
-    if (lane == 0) {
-      perm_to_flat[row] = int32_t(f);
-      flat_to_perm[f] = int32_t(row);
+  for (int64_t f = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); f < R; f += nwarps)
+    place_flat(f, idx, k, E, kPermuteSegment, rank, seg_base, row_offsets, xq, xs, H, perm_to_flat, flat_to_perm,
+               a_packed, a_scales, lane);
+}
+
+// ---------------------------------------------------------------------------
+// a1 + a2 + a3 in one cooperative launch.  Four phases separated by grid
+// barriers (every CTA resident, bounded waits):
+//   A  route (one warp per token) and per-CTA partial amax of x;
+//   B  global scale from the partials, quantisation of x, segment ranks;
+//   C  CTA 0 scans the segment counts;
+//   D  padding rows, placement and the gather of packed rows and scales.
+// Each step is the same device code as in the separate kernels above, so the
+// results are identical bit for bit.
+// ---------------------------------------------------------------------------
+struct PrepareParams {
+  const float* logits;
+  const float* bias;
+  const uint4* x;
+  int T, E, k, H, score_fn, renorm, nseg;
+  int32_t* idx;
+  float* w;
+  float* gscale;
+  uint8_t* xq;
+  uint8_t* xs;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* row_offsets;
+  int32_t* perm_to_flat;
+  int32_t* flat_to_perm;
+  uint8_t* a_packed;
+  uint8_t* a_scales;
+  int64_t rows_cap;
+  uint32_t* bar;  // [0] arrivals, [32] generation: separate 128-byte lines
+  float* amax_part;
+  int32_t* rank;
+  int32_t* seg_count;
+  int32_t* seg_base;
+};
+
+constexpr int kPrepThreads = 1024;
+constexpr uint64_t kPrepTimeoutNs = 2000000000ull;
+
+// All CTAs of the grid meet here.  Thread 0 of each CTA arrives on a
+// device-scope counter; the last arrival resets it and bumps the generation
+// word the others poll (bounded by kPrepTimeoutNs).  Returns false, the same
+// in every thread of the CTA, if the wait gave up or the counter held a
+// value no launch leaves behind; the caller then abandons the kernel.
+__device__ __forceinline__ bool grid_barrier(uint32_t* bar, int* s_ok) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    uint32_t* count = bar;
+    uint32_t* gen = bar + 32;
+    const uint32_t g = ptx::ld_acquire_gpu(gen);
+    __threadfence();
+    const uint32_t arrived = atomicAdd(count, 1u) + 1u;
+    if (arrived == gridDim.x) {
+      atomicExch(count, 0u);
+      __threadfence();
+      ptx::red_release_gpu_add(gen, 1u);
+    } else if (arrived > gridDim.x) {
+      atomicOr(&g_prep_flags, kFlagBadData);
+      ok = 0;
+    } else {
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (ptx::ld_acquire_gpu(gen) == g) {
+        if (ptx::globaltimer_ns() - t0 > kPrepTimeoutNs) {
+          atomicOr(&g_prep_flags, kFlagTimeout);
+          ok = 0;
+          break;
+        }
+      }
     }
-    const int64_t t = f / k;
-    const uint4* src = reinterpret_cast<const uint4*>(xq + t * (H / 2));
-    uint4* dst = reinterpret_cast<uint4*>(a_packed + row * (H / 2));
-    for (int c = lane; c < H / 32; c += 32) dst[c] = src[c];
-    const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(xs + t * (H / 16));
-    for (int kb = lane; kb < kblocks; kb += 32)
-      *reinterpret_cast<uint32_t*>(a_scales + blocked_sf_offset(row, kb, kblocks)) = ssrc[kb];
+    __threadfence();
+    *s_ok = ok;
   }
+  __syncthreads();
+  return *s_ok != 0;
+}
+
+template <int VPL, int ITERS>
+__global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareParams p) {
+  extern __shared__ int32_t s_rank_cnt[];  // kRankWarps x E
+  __shared__ float s_red[32];
+  __shared__ int s_ok;
+  __shared__ int warp_tot[32];
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarp = kPrepThreads / 32;
+  const int64_t tid = int64_t(blockIdx.x) * kPrepThreads + threadIdx.x;
+  const int64_t nthreads = int64_t(gridDim.x) * kPrepThreads;
+  const int64_t gw0 = int64_t(warp) * gridDim.x + blockIdx.x;  // warps interleaved across CTAs
+  const int64_t gw_stride = int64_t(gridDim.x) * nwarp;
+  const int64_t R = int64_t(p.T) * p.k;
+
+  // ---- A: routing and partial amax -----------------------------------------
+  for (int64_t t = gw0; t < p.T; t += gw_stride)
+    route_token<VPL>(p.logits, p.bias, int(t), p.E, p.k, p.score_fn, p.renorm, p.idx, p.w, lane);
+  {
+    float m = 0.f;
+    const int64_t nvec = int64_t(p.T) * p.H / 8;
+    int64_t i = tid;
+    for (; i + 3 * nthreads < nvec; i += 4 * nthreads) {
+      const uint4 q0 = __ldg(p.x + i), q1 = __ldg(p.x + i + nthreads);
+      const uint4 q2 = __ldg(p.x + i + 2 * nthreads), q3 = __ldg(p.x + i + 3 * nthreads);
+      m = amax8(q3, amax8(q2, amax8(q1, amax8(q0, m))));
+    }
+    for (; i < nvec; i += nthreads) m = amax8(__ldg(p.x + i), m);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+    if (lane == 0) s_red[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+      m = s_red[lane];
+#pragma unroll
+      for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+      if (lane == 0) p.amax_part[blockIdx.x] = m;
+    }
+  }
+  if (!grid_barrier(p.bar, &s_ok)) return;
+
+  // ---- B: segment ranks, global scale, quantisation --------------------------
+  // The rank warps start at once; warp kRankWarps reduces the amax partials
+  // meanwhile, and the quantisation waits for its result.
+  if (warp < kRankWarps)
+    for (int64_t seg = int64_t(warp) * gridDim.x + blockIdx.x; seg < p.nseg; seg += int64_t(gridDim.x) * kRankWarps)
+      rank_segment<ITERS>(p.idx, R, p.E, seg, s_rank_cnt + warp * p.E, p.rank, p.seg_count, lane);
+  if (warp == kRankWarps) {
+    float m = 0.f;
+    for (int i = lane; i < int(gridDim.x); i += 32) m = fmaxf(m, __ldcg(p.amax_part + i));
+#pragma unroll
+    for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+    if (lane == 0) s_red[0] = global_scale_of(m);
+  }
+  __syncthreads();
+  const float s = s_red[0];
+  if (blockIdx.x == 0 && threadIdx.x == 0) *p.gscale = s;
+  {
+    const int64_t nblk = int64_t(p.T) * (p.H / 16);
+    for (int64_t b = tid; b < nblk; b += nthreads) {
+      uint2 pk;
+      const uint32_t sb = nvfp4_block16(__ldg(p.x + 2 * b), __ldg(p.x + 2 * b + 1), s, &pk);
+      *reinterpret_cast<uint2*>(p.xq + 8 * b) = pk;
+      p.xs[b] = uint8_t(sb);
+    }
+  }
+  if (!grid_barrier(p.bar, &s_ok)) return;
+
+  // ---- C: expert counts, offsets, row offsets --------------------------------
+  if (blockIdx.x == 0) {
+    int cnt, roff;
+    scan_experts(p.seg_count, p.nseg, p.E, p.seg_base, p.counts, p.offsets, p.row_offsets, warp_tot, &cnt, &roff);
+  }
+  if (!grid_barrier(p.bar, &s_ok)) return;
+
+  // ---- D: padding rows, placement and gather ---------------------------------
+  for (int64_t e = gw0; e < p.E; e += gw_stride) {
+    const int c = __ldcg(p.counts + e), ro = __ldcg(p.row_offsets + e);
+    const int pad = (c + 127) & ~127;
+    for (int r = c + lane; r < pad; r += 32) p.perm_to_flat[ro + r] = -1;
+  }
+  for (int64_t q = int64_t(__ldcg(p.row_offsets + p.E)) + tid; q < p.rows_cap; q += nthreads) p.perm_to_flat[q] = -1;
+  for (int64_t f = gw0; f < R; f += gw_stride)
+    place_flat(f, p.idx, p.k, p.E, ITERS * 32, p.rank, p.seg_base, p.row_offsets, p.xq, p.xs, p.H, p.perm_to_flat,
+               p.flat_to_perm, p.a_packed, p.a_scales, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -364,6 +626,8 @@ __global__ void __launch_bounds__(256) permute_place_kernel(const int32_t* __res
 __global__ void __launch_bounds__(128) finalize_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ f2p,
                                                        const float* __restrict__ w, int T, int k, int H,
                                                        int64_t rows_capacity, uint4* __restrict__ out) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   const int t = blockIdx.x;
   const int c8 = blockIdx.y * blockDim.x + threadIdx.x;  // column group of 8
   if (c8 * 8 >= H) return;
@@ -406,9 +670,9 @@ cudaError_t launch_route_topk(const float* logits, const float* bias, int T, int
   const int warps = 8;
   const dim3 grid((T + warps - 1) / warps), block(warps * 32);
   const int vpl = (E + 31) / 32;
-#define NVFP4MOE_ROUTE(V)                                                                          \
-  route_topk_kernel<V><<<grid, block, 0, st>>>(logits, bias, T, E, k, score_fn, renormalize, idx, w); \
-  break;
+#define NVFP4MOE_ROUTE(V)                                                                                      \
+  return launch_kernel(route_topk_kernel<V>, grid, block, 0, st, false, logits, bias, T, E, k, score_fn,      \
+                       renormalize, idx, w);
   switch (vpl <= 1 ? 1 : vpl <= 2 ? 2 : vpl <= 4 ? 4 : vpl <= 8 ? 8 : vpl <= 16 ? 16 : 32) {
     case 1: NVFP4MOE_ROUTE(1)
     case 2: NVFP4MOE_ROUTE(2)
@@ -418,7 +682,6 @@ cudaError_t launch_route_topk(const float* logits, const float* bias, int T, int
     default: NVFP4MOE_ROUTE(32)
   }
 #undef NVFP4MOE_ROUTE
-  return cudaGetLastError();
 }
 
 cudaError_t launch_quantize(const void* x, int64_t rows, int64_t cols, float* global_scale, bool compute_global,
@@ -426,25 +689,27 @@ cudaError_t launch_quantize(const void* x, int64_t rows, int64_t cols, float* gl
                             cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   const int64_t nblk = rows * (cols / 16);
+  const uint4* xv = static_cast<const uint4*>(x);
   if (compute_global) {
     cudaError_t err = cudaMemsetAsync(amax_ws, 0, sizeof(unsigned), st);
     if (err != cudaSuccess) return err;
-    amax_kernel<<<grid_for(nblk * 2, 256, num_sms, 8), 256, 0, st>>>(static_cast<const uint4*>(x), nblk * 2,
-                                                                       amax_ws);
+    err = launch_kernel(amax_kernel, dim3(grid_for(nblk * 2, 256, num_sms, 8)), dim3(256), 0, st, false, xv,
+                        nblk * 2, amax_ws);
+    if (err != cudaSuccess) return err;
   }
   const int64_t work = blocked ? ((rows + 127) / 128) * 128 * (cols / 16) : nblk;
-  quantize_kernel<<<grid_for(work, 256, num_sms, 8), 256, 0, st>>>(
-      static_cast<const uint4*>(x), rows, cols, global_scale, compute_global ? amax_ws : nullptr, global_scale,
-      packed, scales, blocked ? 1 : 0);
-  return cudaGetLastError();
+  return launch_kernel(quantize_kernel, dim3(grid_for(work, 256, num_sms, 8)), dim3(256), 0, st, false, xv, rows,
+                       cols, static_cast<const float*>(global_scale),
+                       static_cast<const unsigned*>(compute_global ? amax_ws : nullptr), global_scale, packed, scales,
+                       blocked ? 1 : 0);
 }
 
 cudaError_t launch_scales_to_blocked(const uint8_t* src, int64_t rows, int64_t cols, uint8_t* dst, int num_sms,
                                      cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   const int64_t total = ((rows + 127) / 128) * 128 * (cols / 64);
-  scales_to_blocked_kernel<<<grid_for(total, 256, num_sms, 8), 256, 0, st>>>(src, rows, cols, dst);
-  return cudaGetLastError();
+  return launch_kernel(scales_to_blocked_kernel, dim3(grid_for(total, 256, num_sms, 8)), dim3(256), 0, st, false,
+                       src, rows, cols, dst);
 }
 
 cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, const uint8_t* xq, const uint8_t* xs,
@@ -454,32 +719,117 @@ cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, const u
                            cudaStream_t st) {
   const int64_t R = int64_t(T) * k;
   const int nseg = int((R + kPermuteSegment - 1) / kPermuteSegment);
+  cudaError_t err;
   if (nseg > 0) {
     const size_t smem = size_t(kRankWarps) * E * sizeof(int32_t);
     if (smem > 48 * 1024) {
-      cudaError_t err =
-          cudaFuncSetAttribute(permute_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+      err = cudaFuncSetAttribute(permute_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
       if (err != cudaSuccess) return err;
     }
-    permute_rank_kernel<<<(nseg + kRankWarps - 1) / kRankWarps, kRankWarps * 32, smem, st>>>(topk_idx, R, E, nseg,
-                                                                                           ws_rank, ws_seg_count);
+    err = launch_kernel(permute_rank_kernel, dim3((nseg + kRankWarps - 1) / kRankWarps), dim3(kRankWarps * 32), smem,
+                        st, false, topk_idx, R, E, nseg, ws_rank, ws_seg_count);
+    if (err != cudaSuccess) return err;
   }
-  permute_scan_kernel<<<1, 1024, 0, st>>>(ws_seg_count, nseg, E, ws_seg_base, counts, offsets, row_offsets,
-                                          perm_to_flat, rows_capacity);
-  if (R > 0)
-    permute_place_kernel<<<grid_for(R * 32, 256, num_sms, 8), 256, 0, st>>>(
-        topk_idx, R, k, E, ws_rank, ws_seg_base, row_offsets, xq, xs, H, perm_to_flat, flat_to_perm, a_packed,
-        a_scales);
-  return cudaGetLastError();
+  err = launch_kernel(permute_scan_kernel, dim3(1), dim3(1024), 0, st, false,
+                      static_cast<const int32_t*>(ws_seg_count), nseg, E, ws_seg_base, counts, offsets, row_offsets,
+                      perm_to_flat, rows_capacity);
+  if (err != cudaSuccess || R == 0) return err;
+  return launch_kernel(permute_place_kernel, dim3(grid_for(R * 32, 256, num_sms, 8)), dim3(256), 0, st, false,
+                       topk_idx, R, k, E, static_cast<const int32_t*>(ws_rank),
+                       static_cast<const int32_t*>(ws_seg_base), static_cast<const int32_t*>(row_offsets), xq, xs, H,
+                       perm_to_flat, flat_to_perm, a_packed, a_scales);
+}
+
+PrepareLayout prepare_layout(int T, int E, int k) {
+  PrepareLayout L;
+  const int64_t R = int64_t(T) * k;
+  L.seg_len = R <= kPrepareShortMaxRows ? 256 : 1024;
+  L.nseg = (R + L.seg_len - 1) / L.seg_len;
+  auto up = [](int64_t b) { return (b + 255) / 256 * 256; };
+  L.bar_off = 0;
+  L.amax_off = 256;
+  L.rank_off = L.amax_off + up(int64_t(kPrepareMaxGrid) * 4);
+  L.seg_count_off = L.rank_off + up(R * 4);
+  L.seg_base_off = L.seg_count_off + up(L.nseg * E * 4);
+  L.bytes = L.seg_base_off + up(L.nseg * E * 4);
+  return L;
+}
+
+namespace {
+
+template <int VPL, int ITERS>
+cudaError_t launch_prepare_impl(const PrepareParams& p, int num_sms, cudaStream_t st) {
+  const size_t smem = size_t(kRankWarps) * p.E * sizeof(int32_t);
+  // The grid barriers need every CTA resident: one CTA per SM must fit.
+  int per_sm = 0;
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prepare_kernel<VPL, ITERS>, kPrepThreads,
+                                                                  smem);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+  const int grid = num_sms < kPrepareMaxGrid ? num_sms : kPrepareMaxGrid;
+  return launch_kernel(prepare_kernel<VPL, ITERS>, dim3(grid), dim3(kPrepThreads), smem, st, true, p);
+}
+
+}  // namespace
+
+cudaError_t launch_prepare(const float* logits, const float* bias, const void* x, int T, int E, int k, int H,
+                           int score_fn, int renormalize, int32_t* idx, float* w, float* gscale, uint8_t* xq,
+                           uint8_t* xs, int32_t* counts, int32_t* offsets, int32_t* row_offsets, int32_t* perm_to_flat,
+                           int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales, int64_t rows_capacity,
+                           void* ws, int num_sms, cudaStream_t st) {
+  const PrepareLayout L = prepare_layout(T, E, k);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  PrepareParams p;
+  p.logits = logits;
+  p.bias = bias;
+  p.x = static_cast<const uint4*>(x);
+  p.T = T;
+  p.E = E;
+  p.k = k;
+  p.H = H;
+  p.score_fn = score_fn;
+  p.renorm = renormalize;
+  p.nseg = int(L.nseg);
+  p.idx = idx;
+  p.w = w;
+  p.gscale = gscale;
+  p.xq = xq;
+  p.xs = xs;
+  p.counts = counts;
+  p.offsets = offsets;
+  p.row_offsets = row_offsets;
+  p.perm_to_flat = perm_to_flat;
+  p.flat_to_perm = flat_to_perm;
+  p.a_packed = a_packed;
+  p.a_scales = a_scales;
+  p.rows_cap = rows_capacity;
+  p.bar = reinterpret_cast<uint32_t*>(base + L.bar_off);
+  p.amax_part = reinterpret_cast<float*>(base + L.amax_off);
+  p.rank = reinterpret_cast<int32_t*>(base + L.rank_off);
+  p.seg_count = reinterpret_cast<int32_t*>(base + L.seg_count_off);
+  p.seg_base = reinterpret_cast<int32_t*>(base + L.seg_base_off);
+  const int vpl = (E + 31) / 32;
+  const int v = vpl <= 1 ? 1 : vpl <= 2 ? 2 : vpl <= 4 ? 4 : vpl <= 8 ? 8 : vpl <= 16 ? 16 : 32;
+  const bool short_seg = L.seg_len == 256;
+#define NVFP4MOE_PREP(V)                                                                           \
+  return short_seg ? launch_prepare_impl<V, 8>(p, num_sms, st) : launch_prepare_impl<V, 32>(p, num_sms, st);
+  switch (v) {
+    case 1: NVFP4MOE_PREP(1)
+    case 2: NVFP4MOE_PREP(2)
+    case 4: NVFP4MOE_PREP(4)
+    case 8: NVFP4MOE_PREP(8)
+    case 16: NVFP4MOE_PREP(16)
+    default: NVFP4MOE_PREP(32)
+  }
+#undef NVFP4MOE_PREP
 }
 
 cudaError_t launch_finalize(const void* y, const int32_t* flat_to_perm, const float* w, int T, int k, int H,
                             int64_t rows_capacity, void* out, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   const dim3 block(128), grid(T, (H / 8 + 127) / 128);
-  finalize_kernel<<<grid, block, 0, st>>>(static_cast<const uint4*>(y), flat_to_perm, w, T, k, H, rows_capacity,
-                                          static_cast<uint4*>(out));
-  return cudaGetLastError();
+  return launch_kernel(finalize_kernel, grid, block, 0, st, false, static_cast<const uint4*>(y), flat_to_perm, w, T,
+                       k, H, rows_capacity, static_cast<uint4*>(out));
 }
 
 // ---------------------------------------------------------------------------

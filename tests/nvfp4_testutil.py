@@ -84,3 +84,35 @@ def oracle_quantize_experts(w_bf16):
         p, s = O.quantize_nvfp4(a, g)
         ps.append(p), ss.append(s), gs.append(g)
     return np.stack(ps), np.stack(ss), np.array(gs, np.float32)
+
+
+def check_permutation(out, idx, E, xq, xs):
+    """A Permutation (CUDA) against the oracle's stable expert-first order
+    of `idx` [T, k], with the gathered packed rows `xq` and row-major scales
+    `xs` of the tokens: counts, offsets, 128-aligned row offsets, both maps,
+    -1 on every padding row, and the gathered rows and blocked scales."""
+    T, k = idx.shape
+    H = xq.shape[1] * 2
+    counts, offsets, p2f, f2p = O.permute(idx, E)
+    np.testing.assert_array_equal(out.counts.cpu().numpy(), counts)
+    np.testing.assert_array_equal(out.offsets.cpu().numpy(), offsets)
+    roff = out.row_offsets.cpu().numpy()
+    np.testing.assert_array_equal(roff, np.concatenate([[0], np.cumsum(ceil_to(counts, 128))]))
+    g_p2f = out.perm_to_flat.cpu().numpy()
+    g_f2p = out.flat_to_perm.cpu().numpy()
+    cap = out.rows_capacity
+    assert g_p2f.shape == (cap,)
+    valid = np.zeros(cap, bool)
+    for e in range(E):
+        rows = roff[e] + np.arange(counts[e])
+        valid[rows] = True
+        np.testing.assert_array_equal(g_p2f[rows], p2f[offsets[e]:offsets[e + 1]])
+    assert np.all(g_p2f[~valid] == -1)
+    if T * k == 0:
+        return
+    e_of = idx.reshape(-1)
+    np.testing.assert_array_equal(g_f2p - roff[e_of] + offsets[e_of], f2p)
+    a = out.a_packed.cpu().numpy()
+    np.testing.assert_array_equal(a[g_f2p], xq[np.arange(T * k) // k])
+    sc = from_blocked(out.a_scales.cpu().numpy(), cap, H)
+    np.testing.assert_array_equal(sc[g_f2p], xs[np.arange(T * k) // k])
