@@ -168,12 +168,17 @@ def step_with_kernel_events(B, layer, x, logits, ev):
     ev[i].record()
     if layer.fused_prepare:
         B.moe_prepare(logits, x, layer.k, layer.score_fn, layer.renormalize, layer.bias, layer.topk_idx,
-                      layer.topk_w, layer.x_gscale, layer.xq, layer.xs, out=p, workspace=layer.prep_ws)
+                      layer.topk_w, layer.x_gscale, layer.xq, layer.xs, out=p, workspace=layer.prep_ws,
+                      k_primary=layer.k_primary)
         i += 1
         ev[i].record()
     else:
-        B.moe_route_topk(logits, layer.k, layer.score_fn, layer.renormalize, layer.bias, layer.topk_idx,
-                         layer.topk_w)
+        if layer.k_primary < layer.k:
+            B.moe_route_batch_aware(logits, layer.k, layer.k_primary, layer.score_fn, layer.renormalize, layer.bias,
+                                    layer.topk_idx, layer.topk_w, workspace=layer.r_ws)
+        else:
+            B.moe_route_topk(logits, layer.k, layer.score_fn, layer.renormalize, layer.bias, layer.topk_idx,
+                             layer.topk_w)
         i += 1
         ev[i].record()
         B.moe_quantize_nvfp4(x, global_scale=layer.x_gscale, compute_global=True, packed=layer.xq,
@@ -210,7 +215,8 @@ def run_ours(args, w):
     dev = torch.device("cuda", torch.cuda.current_device())
     inp = W.device_inputs(w, seed=args.seed + rank, device=dev)
     layer = B.MoELayer(inp["w_gu"], inp["w_d"], w.k, w.score, w.renormalize, w.h_scale, bias=inp["bias"],
-                       T=w.T, tile_n=(args.tile_gate_up, args.tile_down), fused_prepare=not args.separate_prepare)
+                       T=w.T, tile_n=(args.tile_gate_up, args.tile_down), fused_prepare=not args.separate_prepare,
+                       k_primary=args.k_primary)
     del inp["w_gu"], inp["w_d"]
     torch.cuda.empty_cache()
     x, logits = inp["x"], inp["logits"]
@@ -304,6 +310,7 @@ def run_ours(args, w):
         "kernels_ms": {n: round(float(v), 4) for n, v in zip(names, kern_ms)},
         "ms_per_step_with_events": round(ms_step_events, 4),
         "prepare": "fused (one launch)" if layer.fused_prepare else "separate (route, quantise, permute)",
+        "routing": "top-k" if layer.k_primary == w.k else f"batch-aware, k_primary={layer.k_primary}",
         "roofline": {"kernel": "gemm_gate_up_swiglu", "bound": bound, "achieved": round(achieved, 1),
                      "peak": round(peak, 1), "unit": unit, "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic(w.name, "gemm_gate_up_swiglu"),
@@ -464,6 +471,8 @@ def main():
     ap.add_argument("--tile-down", type=int, default=0)
     ap.add_argument("--cpu-experts", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--k-primary", type=int, default=None,
+                    help="batch-aware routing: experts each token keeps by its own scores (default k: plain top-k)")
     ap.add_argument("--separate-prepare", action="store_true",
                     help="route, quantise and permute as separate calls instead of moe_prepare")
     args = ap.parse_args()

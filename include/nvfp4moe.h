@@ -118,6 +118,28 @@ int moe_route_topk(const float* logits, const float* bias, int T, int E, int k,
                    int score_fn, int renormalize,
                    int32_t* topk_idx, float* topk_w, cudaStream_t stream);
 
+/* Batch-aware ("opportunistic") expert routing (page A, Introduction, key
+ * finding 6 and section 6: batch-aware routing skips the experts a token
+ * would use with low probability at decode time and reuses the experts the
+ * batch activates anyway, so fewer experts' weights are streamed; the pages
+ * give no algorithm).  This library's reading:
+ *   1. each token's primary experts are its top-k_primary by logit + bias
+ *      (order and ties as moe_route_topk);
+ *   2. the batch's active set S is the union of all tokens' primary experts;
+ *   3. each token takes k experts ranked by (member of S first, then value
+ *      descending, then lower index): its best k within S, followed -- only
+ *      when S holds fewer than k experts -- by its best experts outside S;
+ *      slots keep that order;
+ *   4. weights as moe_route_topk over the chosen experts.
+ * k_primary == k is moe_route_topk.  Same arguments as moe_route_topk plus
+ * k_primary in [1, k] and ws: device scratch of at least
+ * moe_route_batch_aware_workspace_size(E) bytes, 4-byte aligned (the set S,
+ * cleared by the call).  Two kernels and one memset. */
+size_t moe_route_batch_aware_workspace_size(int E);
+int moe_route_batch_aware(const float* logits, const float* bias, int T, int E, int k, int k_primary,
+                          int score_fn, int renormalize, int32_t* topk_idx, float* topk_w,
+                          void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* ---- a2: quantisation ----------------------------------------------------
  * bf16 -> NVFP4 (page A, section 1 operand types; four ue4m3 scales per k64
  * MMA step means one scale per 16 elements).  Per 16-element block along a
@@ -212,7 +234,9 @@ int moe_permute_no_alloc(const int32_t* topk_idx, int T, int E, int k,
  * quantisation and segment ranks, then the expert scan, then placement and
  * the gather.  Every output is bit-identical to the three separate calls:
  *   topk_idx, topk_w [T, k] as moe_route_topk (logits device float32 [T, E],
- *     bias device float32 [E] or NULL, score_fn, renormalize);
+ *     bias device float32 [E] or NULL, score_fn, renormalize) when
+ *     k_primary == k, as moe_route_batch_aware when 1 <= k_primary < k (one
+ *     more grid barrier);
  *   x_gscale device float32 [1], xq uint8 [T, H/2], xs uint8 [T, H/16] as
  *     moe_quantize_nvfp4 of x (device bf16 [T, H]);
  *   expert_counts .. a_scales as moe_permute (rows_capacity =
@@ -227,7 +251,7 @@ int moe_permute_no_alloc(const int32_t* topk_idx, int T, int E, int k,
  * the kernel and raises NVFP4MOE_ERR_TIMEOUT (sticky). */
 size_t moe_prepare_workspace_size(int T, int E, int k);
 int moe_prepare(const float* logits, const float* bias, const void* x_bf16,
-                int T, int E, int k, int H, int score_fn, int renormalize,
+                int T, int E, int k, int k_primary, int H, int score_fn, int renormalize,
                 int32_t* topk_idx, float* topk_w, float* x_gscale, uint8_t* xq, uint8_t* xs,
                 int32_t* expert_counts, int32_t* expert_offsets, int32_t* row_offsets,
                 int32_t* perm_to_flat, int32_t* flat_to_perm,

@@ -42,6 +42,8 @@ _SIGS = {
     "nvfp4moe_sync_status": (_i, [_p]),
     "nvfp4moe_blocked_scales_bytes": (_sz, [_i64, _i64]),
     "moe_route_topk": (_i, [_p, _p, _i, _i, _i, _i, _i, _p, _p, _p]),
+    "moe_route_batch_aware_workspace_size": (_sz, [_i]),
+    "moe_route_batch_aware": (_i, [_p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _sz, _p]),
     "moe_quantize_nvfp4_workspace_size": (_sz, [_i64, _i64, _i]),
     "moe_quantize_nvfp4": (_i, [_p, _i64, _i64, _p, _i, _p, _p, _p, _sz, _p]),
     "moe_scales_to_blocked": (_i, [_p, _i64, _i64, _p, _p]),
@@ -50,8 +52,8 @@ _SIGS = {
     "moe_permute": (_i, [_p, _i, _i, _i, _p, _p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
     "moe_permute_no_alloc": (_i, [_p, _i, _i, _i, _p, _p, _i, _p, _p, _p, _p, _p, _p, _p, _p]),
     "moe_prepare_workspace_size": (_sz, [_i, _i, _i]),
-    "moe_prepare": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p,
-                         _sz, _p]),
+    "moe_prepare": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p,
+                         _p, _sz, _p]),
     "moe_grouped_gemm_nvfp4_workspace_size": (_sz, [_i, _i, _i, _i]),
     "moe_grouped_gemm_nvfp4": (_i, [_p, _p, _p, _p, _p, _i, _i64, _i64, _p, _p, _p, _i, _i, _i, _p, _p, _p, _i,
                                     _p, _sz, _p]),
@@ -133,6 +135,28 @@ def moe_route_topk(logits, k, score_fn="sigmoid", renormalize=True, bias=None, t
     _need(topk_w, torch.float32, (T, k), "topk_w")
     _check(_lib.moe_route_topk(_ptr(logits), _ptr(bias), T, E, k, SCORE[score_fn], int(bool(renormalize)),
                                _ptr(topk_idx), _ptr(topk_w), _stream()), "moe_route_topk")
+    return topk_idx, topk_w
+
+
+def moe_route_batch_aware(logits, k, k_primary, score_fn="sigmoid", renormalize=True, bias=None, topk_idx=None,
+                          topk_w=None, workspace=None):
+    """Batch-aware routing: each token's top-k_primary experts form the
+    batch's active set; each token then takes its best k experts, members of
+    the set first.  k_primary == k is moe_route_topk."""
+    T, E = logits.shape
+    _need(logits, torch.float32, name="logits")
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    dev = logits.device
+    topk_idx = _empty((T, k), torch.int32, dev) if topk_idx is None else topk_idx
+    topk_w = _empty((T, k), torch.float32, dev) if topk_w is None else topk_w
+    _need(topk_idx, torch.int32, (T, k), "topk_idx")
+    _need(topk_w, torch.float32, (T, k), "topk_w")
+    if workspace is None:
+        workspace = _empty((int(_lib.moe_route_batch_aware_workspace_size(E)),), torch.uint8, dev)
+    _check(_lib.moe_route_batch_aware(_ptr(logits), _ptr(bias), T, E, k, int(k_primary), SCORE[score_fn],
+                                      int(bool(renormalize)), _ptr(topk_idx), _ptr(topk_w), _ptr(workspace),
+                                      workspace.numel(), _stream()), "moe_route_batch_aware")
     return topk_idx, topk_w
 
 
@@ -271,11 +295,13 @@ def alloc_prepare_workspace(T, E, k, device):
 
 
 def moe_prepare(logits, x, k, score_fn="sigmoid", renormalize=True, bias=None, topk_idx=None, topk_w=None,
-                x_gscale=None, xq=None, xs=None, out: Permutation = None, workspace=None):
+                x_gscale=None, xq=None, xs=None, out: Permutation = None, workspace=None, k_primary=None):
     """Route, quantise and permute in one launch.
 
     Returns (topk_idx, topk_w, x_gscale, xq, xs, Permutation), each equal bit
-    for bit to moe_route_topk + moe_quantize_nvfp4 + moe_permute."""
+    for bit to moe_route_topk (moe_route_batch_aware when k_primary < k) +
+    moe_quantize_nvfp4 + moe_permute."""
+    k_primary = k if k_primary is None else int(k_primary)
     _need(logits, torch.float32, name="logits")
     _need(x, torch.bfloat16, name="x")
     T, E = logits.shape
@@ -300,7 +326,8 @@ def moe_prepare(logits, x, k, score_fn="sigmoid", renormalize=True, bias=None, t
     if workspace is None:
         workspace = alloc_prepare_workspace(T, E, k, dev)
     _need(workspace, torch.uint8, name="workspace")
-    _check(_lib.moe_prepare(_ptr(logits), _ptr(bias), _ptr(x), T, E, k, H, SCORE[score_fn], int(bool(renormalize)),
+    _check(_lib.moe_prepare(_ptr(logits), _ptr(bias), _ptr(x), T, E, k, k_primary, H, SCORE[score_fn],
+                            int(bool(renormalize)),
                             _ptr(topk_idx), _ptr(topk_w), _ptr(x_gscale), _ptr(xq), _ptr(xs), _ptr(out.counts),
                             _ptr(out.offsets), _ptr(out.row_offsets), _ptr(out.perm_to_flat),
                             _ptr(out.flat_to_perm), _ptr(out.a_packed), _ptr(out.a_scales), _ptr(workspace),
@@ -382,8 +409,10 @@ class MoELayer:
     (nine launches and one memset)."""
 
     def __init__(self, w_gu, w_d, k, score_fn="sigmoid", renormalize=True, h_scale=2.0 ** -4, bias=None,
-                 T=None, tile_n=(0, 0), fused_prepare=True):
+                 T=None, tile_n=(0, 0), fused_prepare=True, k_primary=None):
         self.fused_prepare = bool(fused_prepare)
+        # batch-aware routing when k_primary < k (moe_route_batch_aware)
+        self.k_primary = k if k_primary is None else int(k_primary)
         self.E, two_i, self.H = w_gu.shape
         self.I = two_i // 2
         self.k, self.score_fn, self.renormalize = k, score_fn, renormalize
@@ -406,6 +435,7 @@ class MoELayer:
         self.xq = _empty((T, H // 2), torch.uint8, dev)
         self.xs = _empty((T, H // 16), torch.uint8, dev)
         self.q_ws = _empty((64,), torch.uint8, dev)
+        self.r_ws = _empty((int(_lib.moe_route_batch_aware_workspace_size(E)),), torch.uint8, dev)
         self.perm = alloc_permutation(T, E, k, H, dev)
         self.p_ws = _empty((moe_permute_workspace_size(T, E, k),), torch.uint8, dev)
         self.prep_ws = alloc_prepare_workspace(T, E, k, dev)
@@ -422,9 +452,14 @@ class MoELayer:
         p = self.perm
         if self.fused_prepare:
             moe_prepare(logits, x, self.k, self.score_fn, self.renormalize, self.bias, self.topk_idx, self.topk_w,
-                        self.x_gscale, self.xq, self.xs, out=p, workspace=self.prep_ws)
+                        self.x_gscale, self.xq, self.xs, out=p, workspace=self.prep_ws, k_primary=self.k_primary)
         else:
-            moe_route_topk(logits, self.k, self.score_fn, self.renormalize, self.bias, self.topk_idx, self.topk_w)
+            if self.k_primary < self.k:
+                moe_route_batch_aware(logits, self.k, self.k_primary, self.score_fn, self.renormalize, self.bias,
+                                      self.topk_idx, self.topk_w, workspace=self.r_ws)
+            else:
+                moe_route_topk(logits, self.k, self.score_fn, self.renormalize, self.bias, self.topk_idx,
+                               self.topk_w)
             moe_quantize_nvfp4(x, global_scale=self.x_gscale, compute_global=True, packed=self.xq,
                                scales=self.xs, workspace=self.q_ws)
             moe_permute(self.topk_idx, self.E, self.xq, self.xs, out=p, workspace=self.p_ws)
@@ -442,4 +477,4 @@ class MoELayer:
     # GEMMs 2, finalize 1
     @property
     def launches_per_forward(self):
-        return 4 if self.fused_prepare else 9
+        return 4 if self.fused_prepare else (10 if self.k_primary < self.k else 9)

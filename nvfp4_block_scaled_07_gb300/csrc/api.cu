@@ -127,7 +127,7 @@ int nvfp4moe_sync_status(cudaStream_t stream) {
   st = cuda_status(gemm_read_and_clear_flags(&f2), "reading device flags");
   if (st) return st;
   const unsigned f = f1 | f2;
-  if (f & kFlagTimeout) return fail(NVFP4MOE_ERR_TIMEOUT, "a grouped GEMM pipeline wait exceeded its time limit");
+  if (f & kFlagTimeout) return fail(NVFP4MOE_ERR_TIMEOUT, "a device wait (grouped GEMM pipeline or prepare grid barrier) exceeded its time limit");
   if (f & kFlagBadData) return fail(NVFP4MOE_ERR_DEVICE_DATA, "an expert id or row index was out of range");
   return NVFP4MOE_OK;
 }
@@ -152,6 +152,34 @@ int moe_route_topk(const float* logits, const float* bias, int T, int E, int k, 
   if (int st = current_device(&d)) return st;
   return cuda_status(launch_route_topk(logits, bias, T, E, k, score_fn, renormalize ? 1 : 0, topk_idx, topk_w, stream),
                      "route launch");
+}
+
+size_t moe_route_batch_aware_workspace_size(int E) {
+  if (E < 1) return 0;
+  return size_t(ceil_div(E, 32)) * sizeof(uint32_t);
+}
+
+int moe_route_batch_aware(const float* logits, const float* bias, int T, int E, int k, int k_primary, int score_fn,
+                          int renormalize, int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
+                          cudaStream_t stream) {
+  t_detail[0] = 0;
+  NVFP4MOE_REQUIRE(T >= 0, NVFP4MOE_ERR_INVALID_ARG, "T = %d must be >= 0", T);
+  NVFP4MOE_REQUIRE(E >= 1 && E <= 1024, NVFP4MOE_ERR_UNSUPPORTED, "E = %d outside [1, 1024]", E);
+  NVFP4MOE_REQUIRE(k >= 1 && k <= E && k <= 32, NVFP4MOE_ERR_UNSUPPORTED, "k = %d outside [1, min(E, 32)]", k);
+  NVFP4MOE_REQUIRE(k_primary >= 1 && k_primary <= k, NVFP4MOE_ERR_INVALID_ARG, "k_primary = %d outside [1, k = %d]",
+                   k_primary, k);
+  NVFP4MOE_REQUIRE(score_fn == NVFP4MOE_SCORE_SOFTMAX || score_fn == NVFP4MOE_SCORE_SIGMOID,
+                   NVFP4MOE_ERR_INVALID_ARG, "score_fn %d", score_fn);
+  if (T == 0) return NVFP4MOE_OK;
+  NVFP4MOE_REQUIRE(logits && topk_idx && topk_w, NVFP4MOE_ERR_INVALID_ARG, "null pointer");
+  const size_t need = moe_route_batch_aware_workspace_size(E);
+  NVFP4MOE_REQUIRE(ws && ws_bytes >= need && (reinterpret_cast<uintptr_t>(ws) & 3) == 0, NVFP4MOE_ERR_WORKSPACE,
+                   "workspace %zu < %zu or misaligned", ws_bytes, need);
+  DeviceInfo d;
+  if (int st = current_device(&d)) return st;
+  return cuda_status(launch_route_batch_aware(logits, bias, T, E, k, k_primary, score_fn, renormalize ? 1 : 0,
+                                              topk_idx, topk_w, static_cast<uint32_t*>(ws), stream),
+                     "batch-aware route launch");
 }
 
 // ---- a2 ---------------------------------------------------------------------
@@ -286,8 +314,8 @@ size_t moe_prepare_workspace_size(int T, int E, int k) {
   return size_t(prepare_layout(T, E, k).bytes);
 }
 
-int moe_prepare(const float* logits, const float* bias, const void* x_bf16, int T, int E, int k, int H,
-                int score_fn, int renormalize, int32_t* topk_idx, float* topk_w, float* x_gscale, uint8_t* xq,
+int moe_prepare(const float* logits, const float* bias, const void* x_bf16, int T, int E, int k, int k_primary,
+                int H, int score_fn, int renormalize, int32_t* topk_idx, float* topk_w, float* x_gscale, uint8_t* xq,
                 uint8_t* xs, int32_t* expert_counts, int32_t* expert_offsets, int32_t* row_offsets,
                 int32_t* perm_to_flat, int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales, void* ws,
                 size_t ws_bytes, cudaStream_t stream) {
@@ -295,6 +323,8 @@ int moe_prepare(const float* logits, const float* bias, const void* x_bf16, int 
   NVFP4MOE_REQUIRE(T >= 0, NVFP4MOE_ERR_INVALID_ARG, "T = %d must be >= 0", T);
   NVFP4MOE_REQUIRE(E >= 1 && E <= 1024, NVFP4MOE_ERR_UNSUPPORTED, "E = %d outside [1, 1024]", E);
   NVFP4MOE_REQUIRE(k >= 1 && k <= E && k <= 32, NVFP4MOE_ERR_UNSUPPORTED, "k = %d outside [1, min(E, 32)]", k);
+  NVFP4MOE_REQUIRE(k_primary >= 1 && k_primary <= k, NVFP4MOE_ERR_INVALID_ARG, "k_primary = %d outside [1, k = %d]",
+                   k_primary, k);
   NVFP4MOE_REQUIRE(H > 0 && H % 64 == 0, NVFP4MOE_ERR_UNSUPPORTED, "H = %d must be a positive multiple of 64", H);
   NVFP4MOE_REQUIRE(int64_t(T) * k <= (int64_t(1) << 30), NVFP4MOE_ERR_UNSUPPORTED, "T*k too large");
   NVFP4MOE_REQUIRE(score_fn == NVFP4MOE_SCORE_SOFTMAX || score_fn == NVFP4MOE_SCORE_SIGMOID,
@@ -313,7 +343,8 @@ int moe_prepare(const float* logits, const float* bias, const void* x_bf16, int 
                    "workspace must be 256-byte aligned");
   DeviceInfo d;
   if (int st = current_device(&d)) return st;
-  return cuda_status(launch_prepare(logits, bias, x_bf16, T, E, k, H, score_fn, renormalize ? 1 : 0, topk_idx, topk_w,
+  return cuda_status(launch_prepare(logits, bias, x_bf16, T, E, k, k_primary, H, score_fn, renormalize ? 1 : 0,
+                                    topk_idx, topk_w,
                                     x_gscale, xq, xs, expert_counts, expert_offsets, row_offsets, perm_to_flat,
                                     flat_to_perm, a_packed, a_scales, moe_permute_rows_capacity(T, E, k), ws,
                                     d.num_sms, stream),

@@ -19,6 +19,12 @@ constexpr int kPermuteSegment = 1024;
 cudaError_t launch_route_topk(const float* logits, const float* bias, int T, int E, int k, int score_fn,
                               int renormalize, int32_t* idx, float* w, cudaStream_t st);
 
+// Batch-aware routing: active_set is a device scratch of ceil(E/32) words
+// (zeroed by the launcher).
+cudaError_t launch_route_batch_aware(const float* logits, const float* bias, int T, int E, int k, int k_primary,
+                                     int score_fn, int renormalize, int32_t* idx, float* w, uint32_t* active_set,
+                                     cudaStream_t st);
+
 cudaError_t launch_quantize(const void* x, int64_t rows, int64_t cols, float* global_scale, bool compute_global,
                             bool blocked, uint8_t* packed, uint8_t* scales, unsigned* amax_ws, int num_sms,
                             cudaStream_t st);
@@ -44,8 +50,8 @@ cudaError_t launch_permute_static_scratch(const int32_t* topk_idx, int T, int E,
                                           cudaStream_t st);
 
 // Route + quantise + permute in one cooperative launch.  Workspace layout
-// (bytes from the start, 256-byte aligned pieces): grid-barrier words,
-// per-CTA partial amax, segment ranks [T*k], per-segment expert counts and
+// (bytes from the start, 256-byte aligned pieces): grid-barrier words and
+// the batch-aware routing set (512 bytes), per-CTA partial amax, segment ranks [T*k], per-segment expert counts and
 // bases [nseg*E] each.  Segments are 256 flat ids up to
 // kPrepareShortMaxRows routed rows, 1024 above.
 constexpr int64_t kPrepareShortMaxRows = 16384;
@@ -57,8 +63,8 @@ struct PrepareLayout {
 };
 PrepareLayout prepare_layout(int T, int E, int k);
 
-cudaError_t launch_prepare(const float* logits, const float* bias, const void* x, int T, int E, int k, int H,
-                           int score_fn, int renormalize, int32_t* idx, float* w, float* gscale, uint8_t* xq,
+cudaError_t launch_prepare(const float* logits, const float* bias, const void* x, int T, int E, int k, int k_primary,
+                           int H, int score_fn, int renormalize, int32_t* idx, float* w, float* gscale, uint8_t* xq,
                            uint8_t* xs, int32_t* counts, int32_t* offsets, int32_t* row_offsets, int32_t* perm_to_flat,
                            int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales, int64_t rows_capacity,
                            void* ws, int num_sms, cudaStream_t st);

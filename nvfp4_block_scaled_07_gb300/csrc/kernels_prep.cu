@@ -35,13 +35,18 @@ __device__ __forceinline__ double warp_sum(double v) {
 // sigmoid expert scoring; softmax for the tiny layer).  One warp per token;
 // lane l holds experts l, l+32, ...; k rounds of a warp arg-max with the
 // lower expert index winning ties.
+//
+// Batch-aware routing (same page, key finding 6 and section 6: skip the
+// low-probability experts at decode time by reusing the experts the batch
+// activates anyway).  Pass 1 marks every token's top-k_primary experts in
+// a bit set S; pass 2 ranks each token's experts with members of S first
+// (then value, then index) and takes k of them.  Plain top-k is pass 2 with
+// every expert a member.
 // ---------------------------------------------------------------------------
 template <int VPL>
-__device__ __forceinline__ void route_token(const float* __restrict__ logits, const float* __restrict__ bias, int t,
-                                            int E, int k, int score_fn, int renorm, int32_t* __restrict__ idx_out,
-                                            float* __restrict__ w_out, int lane) {
+__device__ __forceinline__ void router_values(const float* __restrict__ logits, const float* __restrict__ bias, int t,
+                                              int E, int lane, float (&v)[VPL]) {
   const float* row = logits + int64_t(t) * E;
-  float v[VPL];
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const int e = lane + 32 * i;
@@ -52,16 +57,26 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, co
     }
     v[i] = x;
   }
+}
+
+// k rounds of a warp arg-max.  member_bits bit i: expert lane + 32 i is in
+// the preferred set; the first `nmem` rounds (the set's size across the
+// warp) choose among members, the rest among non-members.  Lane j < k ends
+// with the j-th choice in (my_e, my_v).
+template <int VPL>
+__device__ __forceinline__ void select_ranked(const float (&v)[VPL], uint32_t member_bits, int nmem, int E, int k,
+                                              int lane, int& my_e, float& my_v) {
   uint32_t used = 0;
-  int my_e = 0;
-  float my_v = -INFINITY;
+  my_e = 0;
+  my_v = -INFINITY;
   for (int j = 0; j < k; ++j) {
+    const uint32_t want = j < nmem ? member_bits : ~member_bits;
     float bv = -INFINITY;
     int be = INT_MAX;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && !((used >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
+      if (e < E && !((used >> i) & 1u) && ((want >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
         bv = v[i];
         be = e;
       }
@@ -81,9 +96,16 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, co
       my_v = bv;
     }
   }
+}
+
+// Weights of the k chosen experts (lane j < k holds choice j) and the stores.
+template <int VPL>
+__device__ __forceinline__ void route_weights_store(const float (&v)[VPL], int my_e, float my_v, int t, int E, int k,
+                                                   int score_fn, int renorm, int32_t* __restrict__ idx_out,
+                                                   float* __restrict__ w_out, int lane) {
   const bool mine = lane < k;
   double wj;
-  if (score_fn == 0) {  // softmax; slot 0 holds the largest value of all E
+  if (score_fn == 0) {  // softmax; slot 0 holds the token's largest value of all E
     const double vmax = double(__shfl_sync(kFull, my_v, 0));
     const double ex = mine ? exp(double(my_v) - vmax) : 0.0;
     double den;
@@ -111,16 +133,77 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, co
   }
 }
 
+// Lane's member bits of the set S (E/32 words, expert e = bit e % 32 of word e / 32).
+template <int VPL>
+__device__ __forceinline__ uint32_t member_bits_of(const uint32_t* set, int E, int lane) {
+  uint32_t bits = 0;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    if (lane + 32 * i < E) bits |= ((__ldcg(set + i) >> lane) & 1u) << i;
+  return bits;
+}
+
+template <int VPL>
+__device__ __forceinline__ int valid_bits_count(uint32_t bits, int E, int lane) {
+  uint32_t valid = 0;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    if (lane + 32 * i < E) valid |= 1u << i;
+  return int(__reduce_add_sync(kFull, unsigned(__popc(bits & valid))));
+}
+
+// Plain top-k (active_set == nullptr) or pass 2 of batch-aware routing.
+template <int VPL>
+__device__ __forceinline__ void route_token(const float* __restrict__ logits, const float* __restrict__ bias, int t,
+                                            int E, int k, int score_fn, int renorm, const uint32_t* active_set,
+                                            int32_t* __restrict__ idx_out, float* __restrict__ w_out, int lane) {
+  float v[VPL];
+  router_values<VPL>(logits, bias, t, E, lane, v);
+  uint32_t bits = ~0u;
+  int nmem = E;
+  if (active_set) {
+    bits = member_bits_of<VPL>(active_set, E, lane);
+    nmem = valid_bits_count<VPL>(bits, E, lane);
+  }
+  int my_e;
+  float my_v;
+  select_ranked<VPL>(v, bits, nmem, E, k, lane, my_e, my_v);
+  route_weights_store<VPL>(v, my_e, my_v, t, E, k, score_fn, renorm, idx_out, w_out, lane);
+}
+
+// Pass 1 of batch-aware routing: the token's top-k_primary join the set S.
+template <int VPL>
+__device__ __forceinline__ void mark_primary(const float* __restrict__ logits, const float* __restrict__ bias, int t,
+                                             int E, int k_primary, uint32_t* active_set, int lane) {
+  float v[VPL];
+  router_values<VPL>(logits, bias, t, E, lane, v);
+  int my_e;
+  float my_v;
+  select_ranked<VPL>(v, ~0u, E, E, k_primary, lane, my_e, my_v);
+  if (lane < k_primary) atomicOr(active_set + (my_e >> 5), 1u << (my_e & 31));
+}
+
 template <int VPL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits,
                                                          const float* __restrict__ bias, int T, int E, int k,
-                                                         int score_fn, int renorm, int32_t* __restrict__ idx_out,
-                                                         float* __restrict__ w_out) {
+                                                         int score_fn, int renorm, const uint32_t* active_set,
+                                                         int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;  // uniform per warp
-  route_token<VPL>(logits, bias, t, E, k, score_fn, renorm, idx_out, w_out, threadIdx.x & 31);
+  route_token<VPL>(logits, bias, t, E, k, score_fn, renorm, active_set, idx_out, w_out, threadIdx.x & 31);
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(256) route_mark_kernel(const float* __restrict__ logits,
+                                                         const float* __restrict__ bias, int T, int E, int k_primary,
+                                                         uint32_t* active_set) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;  // uniform per warp
+  mark_primary<VPL>(logits, bias, t, E, k_primary, active_set, threadIdx.x & 31);
 }
 
 // ---------------------------------------------------------------------------
@@ -467,7 +550,7 @@ struct PrepareParams {
   const float* logits;
   const float* bias;
   const uint4* x;
-  int T, E, k, H, score_fn, renorm, nseg;
+  int T, E, k, k_primary, H, score_fn, renorm, nseg;
   int32_t* idx;
   float* w;
   float* gscale;
@@ -482,6 +565,7 @@ struct PrepareParams {
   uint8_t* a_scales;
   int64_t rows_cap;
   uint32_t* bar;  // [0] arrivals, [32] generation: separate 128-byte lines
+  uint32_t* active_set;  // batch-aware routing: E bits, zero between calls
   float* amax_part;
   int32_t* rank;
   int32_t* seg_count;
@@ -545,9 +629,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
   const int64_t gw_stride = int64_t(gridDim.x) * nwarp;
   const int64_t R = int64_t(p.T) * p.k;
 
-  // ---- A: routing and partial amax -----------------------------------------
-  for (int64_t t = gw0; t < p.T; t += gw_stride)
-    route_token<VPL>(p.logits, p.bias, int(t), p.E, p.k, p.score_fn, p.renorm, p.idx, p.w, lane);
+  // ---- A: routing (batch-aware: its first pass) and partial amax ----------
+  const bool batch_aware = p.k_primary < p.k;
+  for (int64_t t = gw0; t < p.T; t += gw_stride) {
+    if (batch_aware)
+      mark_primary<VPL>(p.logits, p.bias, int(t), p.E, p.k_primary, p.active_set, lane);
+    else
+      route_token<VPL>(p.logits, p.bias, int(t), p.E, p.k, p.score_fn, p.renorm, nullptr, p.idx, p.w, lane);
+  }
   {
     float m = 0.f;
     const int64_t nvec = int64_t(p.T) * p.H / 8;
@@ -570,6 +659,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
     }
   }
   if (!grid_barrier(p.bar, &s_ok)) return;
+
+  // ---- A2 (batch-aware routing only): rank within the batch's active set ------
+  if (batch_aware) {
+    for (int64_t t = gw0; t < p.T; t += gw_stride)
+      route_token<VPL>(p.logits, p.bias, int(t), p.E, p.k, p.score_fn, p.renorm, p.active_set, p.idx, p.w, lane);
+    if (!grid_barrier(p.bar, &s_ok)) return;
+  }
 
   // ---- B: segment ranks, global scale, quantisation --------------------------
   // The rank warps start at once; warp kRankWarps reduces the amax partials
@@ -606,6 +702,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
   if (!grid_barrier(p.bar, &s_ok)) return;
 
   // ---- D: padding rows, placement and gather ---------------------------------
+  if (batch_aware && blockIdx.x == 0 && threadIdx.x < (p.E + 31) / 32) p.active_set[threadIdx.x] = 0u;  // read in A2 only
   for (int64_t e = gw0; e < p.E; e += gw_stride) {
     const int c = __ldcg(p.counts + e), ro = __ldcg(p.row_offsets + e);
     const int pad = (c + 127) & ~127;
@@ -672,7 +769,7 @@ cudaError_t launch_route_topk(const float* logits, const float* bias, int T, int
   const int vpl = (E + 31) / 32;
 #define NVFP4MOE_ROUTE(V)                                                                                      \
   return launch_kernel(route_topk_kernel<V>, grid, block, 0, st, false, logits, bias, T, E, k, score_fn,      \
-                       renormalize, idx, w);
+                       renormalize, static_cast<const uint32_t*>(nullptr), idx, w);
   switch (vpl <= 1 ? 1 : vpl <= 2 ? 2 : vpl <= 4 ? 4 : vpl <= 8 ? 8 : vpl <= 16 ? 16 : 32) {
     case 1: NVFP4MOE_ROUTE(1)
     case 2: NVFP4MOE_ROUTE(2)
@@ -682,6 +779,32 @@ cudaError_t launch_route_topk(const float* logits, const float* bias, int T, int
     default: NVFP4MOE_ROUTE(32)
   }
 #undef NVFP4MOE_ROUTE
+}
+
+cudaError_t launch_route_batch_aware(const float* logits, const float* bias, int T, int E, int k, int k_primary,
+                                     int score_fn, int renormalize, int32_t* idx, float* w, uint32_t* active_set,
+                                     cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  cudaError_t err = cudaMemsetAsync(active_set, 0, size_t((E + 31) / 32) * sizeof(uint32_t), st);
+  if (err != cudaSuccess) return err;
+  const int warps = 8;
+  const dim3 grid((T + warps - 1) / warps), block(warps * 32);
+  const int vpl = (E + 31) / 32;
+#define NVFP4MOE_ROUTE_BA(V)                                                                                   \
+  err = launch_kernel(route_mark_kernel<V>, grid, block, 0, st, false, logits, bias, T, E, k_primary,         \
+                      active_set);                                                                             \
+  if (err != cudaSuccess) return err;                                                                          \
+  return launch_kernel(route_topk_kernel<V>, grid, block, 0, st, false, logits, bias, T, E, k, score_fn,      \
+                       renormalize, static_cast<const uint32_t*>(active_set), idx, w);
+  switch (vpl <= 1 ? 1 : vpl <= 2 ? 2 : vpl <= 4 ? 4 : vpl <= 8 ? 8 : vpl <= 16 ? 16 : 32) {
+    case 1: NVFP4MOE_ROUTE_BA(1)
+    case 2: NVFP4MOE_ROUTE_BA(2)
+    case 4: NVFP4MOE_ROUTE_BA(4)
+    case 8: NVFP4MOE_ROUTE_BA(8)
+    case 16: NVFP4MOE_ROUTE_BA(16)
+    default: NVFP4MOE_ROUTE_BA(32)
+  }
+#undef NVFP4MOE_ROUTE_BA
 }
 
 cudaError_t launch_quantize(const void* x, int64_t rows, int64_t cols, float* global_scale, bool compute_global,
@@ -746,8 +869,8 @@ PrepareLayout prepare_layout(int T, int E, int k) {
   L.seg_len = R <= kPrepareShortMaxRows ? 256 : 1024;
   L.nseg = (R + L.seg_len - 1) / L.seg_len;
   auto up = [](int64_t b) { return (b + 255) / 256 * 256; };
-  L.bar_off = 0;
-  L.amax_off = 256;
+  L.bar_off = 0;        // barrier words at bytes 0 and 128, the active-expert set at 192 (<= 128 bytes)
+  L.amax_off = 512;
   L.rank_off = L.amax_off + up(int64_t(kPrepareMaxGrid) * 4);
   L.seg_count_off = L.rank_off + up(R * 4);
   L.seg_base_off = L.seg_count_off + up(L.nseg * E * 4);
@@ -772,8 +895,8 @@ cudaError_t launch_prepare_impl(const PrepareParams& p, int num_sms, cudaStream_
 
 }  // namespace
 
-cudaError_t launch_prepare(const float* logits, const float* bias, const void* x, int T, int E, int k, int H,
-                           int score_fn, int renormalize, int32_t* idx, float* w, float* gscale, uint8_t* xq,
+cudaError_t launch_prepare(const float* logits, const float* bias, const void* x, int T, int E, int k, int k_primary,
+                           int H, int score_fn, int renormalize, int32_t* idx, float* w, float* gscale, uint8_t* xq,
                            uint8_t* xs, int32_t* counts, int32_t* offsets, int32_t* row_offsets, int32_t* perm_to_flat,
                            int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales, int64_t rows_capacity,
                            void* ws, int num_sms, cudaStream_t st) {
@@ -786,6 +909,7 @@ cudaError_t launch_prepare(const float* logits, const float* bias, const void* x
   p.T = T;
   p.E = E;
   p.k = k;
+  p.k_primary = k_primary;
   p.H = H;
   p.score_fn = score_fn;
   p.renorm = renormalize;
@@ -804,6 +928,7 @@ cudaError_t launch_prepare(const float* logits, const float* bias, const void* x
   p.a_scales = a_scales;
   p.rows_cap = rows_capacity;
   p.bar = reinterpret_cast<uint32_t*>(base + L.bar_off);
+  p.active_set = reinterpret_cast<uint32_t*>(base + L.bar_off + 192);
   p.amax_part = reinterpret_cast<float*>(base + L.amax_off);
   p.rank = reinterpret_cast<int32_t*>(base + L.rank_off);
   p.seg_count = reinterpret_cast<int32_t*>(base + L.seg_count_off);

@@ -39,6 +39,11 @@ below names the readings it uses:
       h = silu(gate) * up with no clamp; h is rounded to float32 before
       requantisation; the down projection output and the layer output are
       rounded to bfloat16; the finalize sum runs in slot order.
+  R8  batch-aware routing (the pages name it, "skip low-probability experts
+      at decode time", without an algorithm): every token keeps its top
+      k_primary experts; the union of those over the batch is the active
+      set S; each token's k experts are its best within S (then, only if S
+      has fewer than k experts, its best outside S); see route_batch_aware.
 
 Precision: values are decoded exactly to float64, GEMMs accumulate in float64
 (numpy matmul on exactly dequantised operands), the few steps that must
@@ -223,15 +228,26 @@ def route_topk(logits, bias, k, score_fn, renormalize=True):
                renormalised.
     Returns (idx int32 [T,k], w float64 [T,k]).
     """
-    v = np.asarray(logits, dtype=np.float32)
-    if bias is not None:
-        v = (v + np.asarray(bias, dtype=np.float32)[None, :]).astype(np.float32)
+    v = _router_values(logits, bias)
     T, E = v.shape
     if not 1 <= k <= E:
         raise ValueError("need 1 <= k <= E")
     order = np.argsort(-v, axis=1, kind="stable")   # stable: equal values keep ascending index
     idx = order[:, :k].astype(np.int32)
-    vs = np.take_along_axis(v, idx, axis=1).astype(np.float64)
+    return idx, _route_weights(v, idx, score_fn, renormalize)
+
+
+def _router_values(logits, bias):
+    """v = logits + bias in float32 (reading R5)."""
+    v = np.asarray(logits, dtype=np.float32)
+    if bias is not None:
+        v = (v + np.asarray(bias, dtype=np.float32)[None, :]).astype(np.float32)
+    return v
+
+
+def _route_weights(v, idx, score_fn, renormalize):
+    """Routing weights of the selected experts idx [T, k] (see route_topk)."""
+    vs = np.take_along_axis(v, idx.astype(np.int64), axis=1).astype(np.float64)
     if score_fn == "softmax":
         vmax = v.max(axis=1, keepdims=True).astype(np.float64)
         num = np.exp(vs - vmax)
@@ -243,7 +259,41 @@ def route_topk(logits, bias, k, score_fn, renormalize=True):
         w = sig / sig.sum(axis=1, keepdims=True) if renormalize else sig
     else:
         raise ValueError(score_fn)
-    return idx, w
+    return w
+
+
+def route_batch_aware(logits, bias, k, k_primary, score_fn, renormalize=True):
+    """Batch-aware ("opportunistic") expert routing, reading R8.
+
+    "SM120 FP4 Kernel Research Campaign" (Introduction; key finding 6; section
+    6, batch-aware routing) names the technique -- at decode time, skip the
+    low-probability experts a token would activate on its own and reuse the
+    experts the batch activates anyway, so that fewer experts' weights are
+    streamed -- but gives no algorithm.  Reading R8, step by step:
+      1. each token's primary experts are its top-k_primary by
+         v = logit + bias (order and ties as in route_topk);
+      2. the batch's active set S is the union of every token's primary
+         experts;
+      3. each token takes k experts ranked by (member of S first, then v
+         descending, then lower index): its top-k within S, followed -- only
+         when S holds fewer than k experts -- by its best experts outside S;
+         slots keep that rank order;
+      4. weights as route_topk over the chosen experts.
+    k_primary == k gives route_topk.  Returns (idx int32 [T,k], w float64 [T,k]).
+    """
+    v = _router_values(logits, bias)
+    T, E = v.shape
+    if not 1 <= k_primary <= k <= E:
+        raise ValueError("need 1 <= k_primary <= k <= E")
+    order = np.argsort(-v, axis=1, kind="stable")          # per token: v descending, lower index first
+    in_s = np.zeros(E, dtype=bool)
+    in_s[order[:, :k_primary].reshape(-1)] = True           # steps 1-2
+    idx = np.empty((T, k), dtype=np.int32)
+    for t in range(T):                                       # step 3
+        members = [int(e) for e in order[t] if in_s[e]]
+        others = [int(e) for e in order[t] if not in_s[e]]
+        idx[t] = (members + others)[:k]
+    return idx, _route_weights(v, idx, score_fn, renormalize)   # step 4
 
 
 # ----------------------------------------------------------------------------
@@ -331,20 +381,24 @@ def finalize(y, flat_to_perm, w, T, k):
 
 
 def moe_layer(x, logits, bias, w_gu_packed, w_gu_scales, s_gu, w_d_packed, w_d_scales, s_d,
-              k, score_fn, s_h, renormalize=True, s_x=None, return_intermediates=False):
+              k, score_fn, s_h, renormalize=True, s_x=None, return_intermediates=False, k_primary=None):
     """The whole expert layer, steps in the pages' order (route, quantise,
     permute, gate/up GEMM + SwiGLU + requantise, down GEMM, finalize).
 
     x: float32 [T, H] (bf16 values); weights already NVFP4 with per-expert
     scales.  s_h is the static per-tensor scale of the SwiGLU output
-    (reading R1); s_x defaults to the dynamic amax/2688 of x.
+    (reading R1); s_x defaults to the dynamic amax/2688 of x.  k_primary
+    (None = k) selects batch-aware routing (route_batch_aware).
     Returns bf16-rounded float64 out [T, H] (and intermediates on request).
     """
     x = np.asarray(x, dtype=np.float32)
     T, H = x.shape
     E = w_gu_packed.shape[0]
     I = w_gu_packed.shape[1] // 2
-    idx, w = route_topk(logits, bias, k, score_fn, renormalize)
+    if k_primary is None or k_primary == k:
+        idx, w = route_topk(logits, bias, k, score_fn, renormalize)
+    else:
+        idx, w = route_batch_aware(logits, bias, k, k_primary, score_fn, renormalize)
     if s_x is None:
         s_x = global_scale(x)
     xq, xs = quantize_nvfp4(x, s_x)
@@ -362,19 +416,25 @@ def moe_layer(x, logits, bias, w_gu_packed, w_gu_scales, s_gu, w_d_packed, w_d_s
                      perm_to_flat=p2f, flat_to_perm=f2p, gu=gu, h=h, hq=hq, hs=hs, y=y)
 
 
-def moe_layer_tokens(token_ids, x, logits, bias, w_gu, w_d, k, score_fn, s_h, s_x, renormalize=True):
+def moe_layer_tokens(token_ids, x, logits, bias, w_gu, w_d, k, score_fn, s_h, s_x, renormalize=True,
+                     routing=None):
     """Layer output for a subset of tokens, computed one token at a time.
 
-    Each output row depends only on its own token once s_x is fixed, so this
-    equals the matching rows of moe_layer().  w_gu / w_d are callables
-    e -> (packed, scales, s) so that only the experts those tokens use are
-    ever quantised.  Returns bf16-rounded float64 [len(token_ids), H].
+    Each output row depends only on its own token once s_x and the routing
+    are fixed, so this equals the matching rows of moe_layer().  w_gu / w_d
+    are callables e -> (packed, scales, s) so that only the experts those
+    tokens use are ever quantised.  routing = (idx, w) of the whole batch
+    (needed for batch-aware routing); None routes each token by route_topk.
+    Returns bf16-rounded float64 [len(token_ids), H].
     """
     x = np.asarray(x, dtype=np.float32)
     I = None
     outs = []
     for t in token_ids:
-        idx, w = route_topk(logits[t:t + 1], bias, k, score_fn, renormalize)
+        if routing is None:
+            idx, w = route_topk(logits[t:t + 1], bias, k, score_fn, renormalize)
+        else:
+            idx, w = routing[0][t:t + 1], routing[1][t:t + 1]
         xq, xs = quantize_nvfp4(x[t:t + 1], s_x)
         xd = dequantize_nvfp4(xq, xs, s_x)
         acc = np.zeros(x.shape[1], dtype=np.float64)
