@@ -39,6 +39,12 @@ below names the readings it uses:
       h = silu(gate) * up with no clamp; h is rounded to float32 before
       requantisation; the down projection output and the layer output are
       rounded to bfloat16; the finalize sum runs in slot order.
+  R9  MXFP4 (the pages name an MXFP4 grouped GEMM and nothing more; the
+      format is the OCP microscaling one): E2M1 values, one E8M0 scale
+      2**X per 32 elements along K, X = floor(log2(block amax)) - 2 clamped
+      to [-127, 127] (-127 for an all-zero block), codes by reading R3 on
+      x / 2**X, no per-tensor scale; the layer's SwiGLU output is
+      requantised the same way.
   R8  batch-aware routing (the pages name it, "skip low-probability experts
       at decode time", without an algorithm): every token keeps its top
       k_primary experts; the union of those over the batch is the active
@@ -212,6 +218,61 @@ def dequantize_nvfp4(packed, scales, s):
 
 
 # ----------------------------------------------------------------------------
+# MXFP4: E2M1 values with one power-of-two (E8M0) scale per 32-element block
+# along K and no per-tensor scale -- the second block-scaled FP4 format for
+# grouped GEMMs the pages name ("SM120 FP4 Kernel Research Campaign",
+# section 2-4: FlashInfer's MXFP4 grouped GEMM).  Reading R9.
+# ----------------------------------------------------------------------------
+MX_BLOCK = 32
+E2M1_EMAX = 2          # 6 = 1.5 * 2**2: exponent of E2M1's largest normal
+
+
+def e8m0_decode(b):
+    """Value of E8M0 scale bytes: 2**(b - 127); 0xFF is NaN."""
+    b = np.asarray(b, dtype=np.int64)
+    return np.where(b == 255, np.nan, np.ldexp(1.0, b - 127))
+
+
+def mx_scale_exponent(amax):
+    """Shared exponent of an MX block from its float32 amax (reading R9):
+    X = floor(log2(amax)) - 2, clamped to the E8M0 range [-127, 127];
+    an all-zero block takes X = -127."""
+    a = np.asarray(amax, dtype=np.float32).astype(np.float64)
+    _, e = np.frexp(np.where(a > 0, a, 1.0))        # a = m * 2**e, m in [0.5, 1): floor(log2 a) = e - 1
+    x = np.where(a > 0, e - 1 - E2M1_EMAX, -127)
+    return np.clip(x, -127, 127).astype(np.int64)
+
+
+def quantize_mxfp4(x):
+    """Quantise rows of x (float32 values, [rows, cols], cols % 32 == 0) to MXFP4.
+
+    Per 32-element block along the row (reading R9): X = mx_scale_exponent(
+    max |x|), scale byte X + 127, q = x / 2**X (exact in float32), code =
+    round_to_e2m1(q) with the sign of x (reading R3: nearest, ties to the
+    even code, saturating at 6).  Packing as reading R4.
+    Returns (packed uint8 [rows, cols/2], scales uint8 [rows, cols/32]).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    rows, cols = x.shape
+    if cols % MX_BLOCK:
+        raise ValueError("cols must be a multiple of 32")
+    blk = x.reshape(rows, cols // MX_BLOCK, MX_BLOCK)
+    X = mx_scale_exponent(np.max(np.abs(blk), axis=-1))
+    q = (blk.astype(np.float64) * np.ldexp(1.0, -X)[..., None]).astype(np.float32)   # exact power-of-two scaling
+    codes = round_to_e2m1(q, np.signbit(blk)).reshape(rows, cols)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return packed, (X + 127).astype(np.uint8).reshape(rows, cols // MX_BLOCK)
+
+
+def dequantize_mxfp4(packed, scales):
+    """float64 values of MXFP4 data: e2m1(code) * 2**(scale - 127)."""
+    codes = unpack_codes(packed)
+    vals = e2m1_decode(codes)
+    sc = np.repeat(e8m0_decode(scales), MX_BLOCK, axis=-1)
+    return vals * sc
+
+
+# ----------------------------------------------------------------------------
 # Routing (key finding 8 / conclusion of the research page: sigmoid scoring;
 # softmax for the tiny configuration).  Reading R5.
 # ----------------------------------------------------------------------------
@@ -343,6 +404,20 @@ def grouped_gemm(a_packed, a_scales, s_a, offsets, w_packed, w_scales, s_w):
     return out
 
 
+def grouped_gemm_mx(a_packed, a_scales, offsets, w_packed, w_scales):
+    """grouped_gemm for MXFP4 operands (no per-tensor scales):
+    C[r, n] = sum_K A[r, :] * W[e, n, :] for rows r of expert e, float64."""
+    offsets = np.asarray(offsets, dtype=np.int64)
+    E = w_packed.shape[0]
+    out = np.zeros((a_packed.shape[0], w_packed.shape[1]), dtype=np.float64)
+    a = dequantize_mxfp4(a_packed, a_scales)
+    for e in range(E):
+        r0, r1 = offsets[e], offsets[e + 1]
+        if r1 > r0:
+            out[r0:r1] = a[r0:r1] @ dequantize_mxfp4(w_packed[e], w_scales[e]).T
+    return out
+
+
 def silu(z):
     """z / (1 + exp(-z)), float64 (reading R7: SwiGLU, no clamp, no alpha)."""
     z = np.asarray(z, dtype=np.float64)
@@ -414,6 +489,32 @@ def moe_layer(x, logits, bias, w_gu_packed, w_gu_scales, s_gu, w_d_packed, w_d_s
         return out
     return out, dict(idx=idx, w=w, s_x=np.float32(s_x), xq=xq, xs=xs, counts=counts, offsets=offsets,
                      perm_to_flat=p2f, flat_to_perm=f2p, gu=gu, h=h, hq=hq, hs=hs, y=y)
+
+
+def moe_layer_mx(x, logits, bias, w_gu_packed, w_gu_scales, w_d_packed, w_d_scales, k, score_fn,
+                 renormalize=True, k_primary=None, return_intermediates=False):
+    """moe_layer with MXFP4 operands (reading R9): x and the SwiGLU output
+    quantised by quantize_mxfp4 (no per-tensor scales), weights MXFP4."""
+    x = np.asarray(x, dtype=np.float32)
+    T, H = x.shape
+    E = w_gu_packed.shape[0]
+    I = w_gu_packed.shape[1] // 2
+    if k_primary is None or k_primary == k:
+        idx, w = route_topk(logits, bias, k, score_fn, renormalize)
+    else:
+        idx, w = route_batch_aware(logits, bias, k, k_primary, score_fn, renormalize)
+    xq, xs = quantize_mxfp4(x)
+    counts, offsets, p2f, f2p = permute(idx, E)
+    tok = p2f // k
+    gu = grouped_gemm_mx(xq[tok], xs[tok], offsets, w_gu_packed, w_gu_scales)
+    h = swiglu(gu, I).astype(np.float32)
+    hq, hs = quantize_mxfp4(h)
+    y = round_to_bf16(grouped_gemm_mx(hq, hs, offsets, w_d_packed, w_d_scales))
+    out = round_to_bf16(finalize(y, f2p, w, T, k))
+    if not return_intermediates:
+        return out
+    return out, dict(idx=idx, w=w, xq=xq, xs=xs, counts=counts, offsets=offsets, perm_to_flat=p2f,
+                     flat_to_perm=f2p, gu=gu, h=h, hq=hq, hs=hs, y=y)
 
 
 def moe_layer_tokens(token_ids, x, logits, bias, w_gu, w_d, k, score_fn, s_h, s_x, renormalize=True,
