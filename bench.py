@@ -166,6 +166,29 @@ def step_with_kernel_events(B, layer, x, logits, ev):
     T = x.shape[0]
     i = 0
     ev[i].record()
+    if layer.fmt == "mxfp4":
+        layer._route(logits)
+        i += 1
+        ev[i].record()
+        B.moe_quantize_mxfp4(x, packed=layer.xq, scales=layer.xs)
+        i += 1
+        ev[i].record()
+        B.moe_permute_mxfp4(layer.topk_idx, layer.E, layer.xq, layer.xs, out=p, workspace=layer.p_ws)
+        i += 1
+        ev[i].record()
+        B.moe_grouped_gemm_mxfp4(p.a_packed, p.a_scales, p.counts, p.row_offsets, layer.w_gu_packed,
+                                 layer.w_gu_scales, B.EPI_SWIGLU_MXFP4, m_total=T * layer.k, tile_n=layer.tile_n[0],
+                                 out=layer.hq, out_scales=layer.hs)
+        i += 1
+        ev[i].record()
+        B.moe_grouped_gemm_mxfp4(layer.hq, layer.hs, p.counts, p.row_offsets, layer.w_d_packed, layer.w_d_scales,
+                                 B.EPI_BF16, m_total=T * layer.k, tile_n=layer.tile_n[1], out=layer.y)
+        i += 1
+        ev[i].record()
+        B.moe_finalize(layer.y, p.flat_to_perm, layer.topk_w, out=layer.out)
+        i += 1
+        ev[i].record()
+        return
     if layer.fused_prepare:
         B.moe_prepare(logits, x, layer.k, layer.score_fn, layer.renormalize, layer.bias, layer.topk_idx,
                       layer.topk_w, layer.x_gscale, layer.xq, layer.xs, out=p, workspace=layer.prep_ws,
@@ -216,7 +239,7 @@ def run_ours(args, w):
     inp = W.device_inputs(w, seed=args.seed + rank, device=dev)
     layer = B.MoELayer(inp["w_gu"], inp["w_d"], w.k, w.score, w.renormalize, w.h_scale, bias=inp["bias"],
                        T=w.T, tile_n=(args.tile_gate_up, args.tile_down), fused_prepare=not args.separate_prepare,
-                       k_primary=args.k_primary)
+                       k_primary=args.k_primary, fmt=args.format)
     del inp["w_gu"], inp["w_d"]
     torch.cuda.empty_cache()
     x, logits = inp["x"], inp["logits"]
@@ -283,11 +306,12 @@ def run_ours(args, w):
     fp4_peak = bf16_peak * FP4_OVER_BF16
     R = w.T * w.k
     flops = W.algorithmic_flops(w)
-    w_bytes_active = n_active * W.nvfp4_bytes(3 * w.H * w.I)
+    fb = lambda n: W.fp4_bytes(n, layer.fmt)
+    w_bytes_active = n_active * fb(3 * w.H * w.I)
     alg_bytes = w_bytes_active + 2 * w.T * w.H * 2
     tokens_s = job_throughput(w.T, world, ms_step)
     gu_ms = kern_ms[names.index("gemm_gate_up_swiglu")]
-    gu_bytes = n_active * W.nvfp4_bytes(2 * w.I * w.H) + W.nvfp4_bytes(R * w.H) + W.nvfp4_bytes(R * w.I)
+    gu_bytes = n_active * fb(2 * w.I * w.H) + fb(R * w.H) + fb(R * w.I)
     gu_flops = 4.0 * R * w.H * w.I
     gu_hbm_time = gu_bytes / (hbm_peak * 1e9)
     gu_tc_time = gu_flops / (fp4_peak * 1e12)
@@ -300,7 +324,9 @@ def run_ours(args, w):
     res = {
         "metric": METRIC, "value": round(tokens_s, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "nvfp4 (e2m1 x ue4m3 scales, fp32 accumulate)", "data": "synthetic",
+        "vs_baseline": None, "data": "synthetic",
+        "dtype": "mxfp4 (e2m1 x ue8m0 scales per 32, fp32 accumulate)" if layer.fmt == "mxfp4" else
+                 "nvfp4 (e2m1 x ue4m3 scales, fp32 accumulate)",
         "config": {"workload": w.name, **w.describe(), "active_experts": n_active,
                    "l2": "inputs larger than L2: %.2f GB of NVFP4 weights streamed per step" % (w_bytes_active / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -313,7 +339,7 @@ def run_ours(args, w):
         "routing": "top-k" if layer.k_primary == w.k else f"batch-aware, k_primary={layer.k_primary}",
         "roofline": {"kernel": "gemm_gate_up_swiglu", "bound": bound, "achieved": round(achieved, 1),
                      "peak": round(peak, 1), "unit": unit, "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(w.name, "gemm_gate_up_swiglu"),
+                     "traffic": recorded_traffic(w.name, "gemm_gate_up_swiglu") if layer.fmt == "nvfp4" else None,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if bound == "hbm" else
                      f"{peak_kind} bf16 x {FP4_OVER_BF16:g} nominal fp4/bf16 ratio"},
         "e2e": {"value": round(job_throughput(w.T, world, e2e_ms), 1), "unit": "tokens/s",
@@ -473,6 +499,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--k-primary", type=int, default=None,
                     help="batch-aware routing: experts each token keeps by its own scores (default k: plain top-k)")
+    ap.add_argument("--format", choices=["nvfp4", "mxfp4"], default="nvfp4",
+                    help="operand format of the layer (mxfp4: E8M0 scale per 32 elements, no per-tensor scales)")
     ap.add_argument("--separate-prepare", action="store_true",
                     help="route, quantise and permute as separate calls instead of moe_prepare")
     args = ap.parse_args()

@@ -75,6 +75,7 @@ extern "C" {
 #define NVFP4MOE_EPI_BF16           0  /* C = bf16(acc * s_a * s_w[e]) */
 #define NVFP4MOE_EPI_SWIGLU_NVFP4   1  /* h = silu(gate) * up, requantised to NVFP4 */
 #define NVFP4MOE_EPI_SWIGLU_F32     2  /* h = silu(gate) * up as float32 (unfused check) */
+#define NVFP4MOE_EPI_SWIGLU_MXFP4   3  /* h = silu(gate) * up, requantised to MXFP4 (MXFP4 GEMM only) */
 
 /* ---- library and device ------------------------------------------------- */
 
@@ -99,6 +100,8 @@ int nvfp4moe_sync_status(cudaStream_t stream);
 /* Bytes of a blocked scale buffer for a [rows, cols] NVFP4 matrix
  * (cols % 64 == 0): ceil(rows/128) * 128 * cols / 16.  0 on bad input. */
 size_t nvfp4moe_blocked_scales_bytes(int64_t rows, int64_t cols);
+/* Bytes of an MXFP4 blocked scale buffer (see the MXFP4 section): 0 unless cols % 128 == 0. */
+size_t nvfp4moe_mxfp4_blocked_scales_bytes(int64_t rows, int64_t cols);
 
 /* ---- a1: routing ---------------------------------------------------------
  * Top-k expert selection with sigmoid scoring (page A, key finding 8 and its
@@ -297,6 +300,49 @@ int moe_grouped_gemm_nvfp4(const uint8_t* a_packed, const uint8_t* a_scales, con
                            int N, int K, int epilogue, const float* c_gscale,
                            void* c_out, uint8_t* c_scales, int tile_n,
                            void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ---- MXFP4 variant of a2, a3, a4/a5 -----------------------------------------
+ * MXFP4 (page A, sections 2-4: the MXFP4 grouped GEMM that works with
+ * specific tile parameters; the pages give the format's name only, so the
+ * library takes the OCP microscaling definition): E2M1 values, two per byte
+ * as for NVFP4, one E8M0 scale byte per 32 consecutive elements along K
+ * (value 2^(b - 127)), no per-tensor scale.  Quantisation of a 32-element
+ * block: X = floor(log2(amax)) - 2, clamped to [-127, 127] (-127 for an
+ * all-zero block), scale byte X + 127, codes = nearest E2M1 of x / 2^X,
+ * ties to the even code, saturating at 6, sign of x.
+ * Scale layouts: row-major uint8 [rows, cols/32], or blocked: blocks of 128
+ * rows x 128 K elements (4 scales per row), 512 contiguous bytes at
+ * (rb * (cols/128) + kb) * 512, row r's 4 scales at (r % 32) * 16 +
+ * (r / 32) * 4 (nvfp4moe_mxfp4_blocked_scales_bytes).
+ *
+ * moe_quantize_mxfp4: x device bf16 [rows, cols] -> packed [rows, cols/2],
+ *   scales row-major or blocked (flags NVFP4MOE_QUANT_SCALES_BLOCKED, which
+ *   needs cols % 128 == 0; padding rows of a blocked buffer get scale 0).
+ *   cols % 32 == 0.  No workspace.
+ * moe_permute_mxfp4: moe_permute for MXFP4 rows (xs row-major [T, H/32],
+ *   a_scales blocked MXFP4 over rows_capacity rows); H % 128 == 0; the
+ *   workspace is moe_permute_workspace_size(T, E, k).
+ * moe_grouped_gemm_mxfp4: moe_grouped_gemm_nvfp4 for MXFP4 operands
+ *   (kind::mxf4nvf4 with ue8m0 scales, scale_vec::2X): no a_gscale,
+ *   w_gscale or c_gscale; w_scales blocked per expert ([E] x
+ *   nvfp4moe_mxfp4_blocked_scales_bytes(N, K)); K % 128 == 0; epilogues
+ *   NVFP4MOE_EPI_BF16, NVFP4MOE_EPI_SWIGLU_MXFP4 (c_out packed [rows_capacity,
+ *   I/2], c_scales blocked MXFP4 over rows_capacity rows with I columns,
+ *   quantised as moe_quantize_mxfp4) or NVFP4MOE_EPI_SWIGLU_F32. */
+int moe_quantize_mxfp4(const void* x_bf16, int64_t rows, int64_t cols, int flags,
+                       uint8_t* packed, uint8_t* scales, cudaStream_t stream);
+int moe_permute_mxfp4(const int32_t* topk_idx, int T, int E, int k,
+                      const uint8_t* xq, const uint8_t* xs, int H,
+                      int32_t* expert_counts, int32_t* expert_offsets, int32_t* row_offsets,
+                      int32_t* perm_to_flat, int32_t* flat_to_perm,
+                      uint8_t* a_packed, uint8_t* a_scales,
+                      void* ws, size_t ws_bytes, cudaStream_t stream);
+int moe_grouped_gemm_mxfp4(const uint8_t* a_packed, const uint8_t* a_scales,
+                           const int32_t* expert_counts, const int32_t* row_offsets,
+                           int E, int64_t rows_capacity, int64_t m_total,
+                           const uint8_t* w_packed, const uint8_t* w_scales,
+                           int N, int K, int epilogue, void* c_out, uint8_t* c_scales, int tile_n,
+                           cudaStream_t stream);
 
 /* ---- a6: finalize ----------------------------------------------------------
  * Router-weighted reduce back to token order (page A, section 6: "token

@@ -31,7 +31,7 @@ ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_SMEM, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT
 SCORE = {"softmax": 0, "sigmoid": 1}
 QUANT_COMPUTE_GLOBAL = 1
 QUANT_SCALES_BLOCKED = 2
-EPI_BF16, EPI_SWIGLU_NVFP4, EPI_SWIGLU_F32 = 0, 1, 2
+EPI_BF16, EPI_SWIGLU_NVFP4, EPI_SWIGLU_F32, EPI_SWIGLU_MXFP4 = 0, 1, 2, 3
 
 _i, _i64, _sz, _p, _f = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
 _SIGS = {
@@ -41,6 +41,10 @@ _SIGS = {
     "nvfp4moe_device_check": (_i, [_i]),
     "nvfp4moe_sync_status": (_i, [_p]),
     "nvfp4moe_blocked_scales_bytes": (_sz, [_i64, _i64]),
+    "nvfp4moe_mxfp4_blocked_scales_bytes": (_sz, [_i64, _i64]),
+    "moe_quantize_mxfp4": (_i, [_p, _i64, _i64, _i, _p, _p, _p]),
+    "moe_permute_mxfp4": (_i, [_p, _i, _i, _i, _p, _p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
+    "moe_grouped_gemm_mxfp4": (_i, [_p, _p, _p, _p, _i, _i64, _i64, _p, _p, _i, _i, _i, _p, _p, _i, _p]),
     "moe_route_topk": (_i, [_p, _p, _i, _i, _i, _i, _i, _p, _p, _p]),
     "moe_route_batch_aware_workspace_size": (_sz, [_i]),
     "moe_route_batch_aware": (_i, [_p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _sz, _p]),
@@ -117,7 +121,9 @@ def sync_status():
     _check(_lib.nvfp4moe_sync_status(_stream()), "nvfp4moe_sync_status")
 
 
-def blocked_scales_bytes(rows, cols):
+def blocked_scales_bytes(rows, cols, fmt="nvfp4"):
+    if fmt == "mxfp4":
+        return int(_lib.nvfp4moe_mxfp4_blocked_scales_bytes(rows, cols))
     return int(_lib.nvfp4moe_blocked_scales_bytes(rows, cols))
 
 
@@ -216,6 +222,35 @@ def quantize_expert_weights(w):
     return packed, scales, gscale
 
 
+# ---- MXFP4 variant of a2 ---------------------------------------------------------
+def moe_quantize_mxfp4(x, blocked=False, packed=None, scales=None):
+    """MXFP4: returns (packed [rows, cols/2] u8, scales u8 row-major [rows, cols/32] or blocked)."""
+    _need(x, torch.bfloat16, name="x")
+    rows, cols = x.shape
+    dev = x.device
+    if packed is None:
+        packed = _empty((rows, cols // 2), torch.uint8, dev)
+    if scales is None:
+        scales = _empty((blocked_scales_bytes(rows, cols, "mxfp4"),) if blocked else (rows, cols // 32),
+                        torch.uint8, dev)
+    _need(packed, torch.uint8, name="packed")
+    _need(scales, torch.uint8, name="scales")
+    _check(_lib.moe_quantize_mxfp4(_ptr(x), rows, cols, QUANT_SCALES_BLOCKED if blocked else 0, _ptr(packed),
+                                   _ptr(scales), _stream()), "moe_quantize_mxfp4")
+    return packed, scales
+
+
+def quantize_expert_weights_mx(w):
+    """bf16 [E, N, K] -> MXFP4 (packed [E, N, K/2], blocked scales [E, bytes])."""
+    _need(w, torch.bfloat16, name="w")
+    E, N, K = w.shape
+    packed = _empty((E, N, K // 2), torch.uint8, w.device)
+    scales = _empty((E, blocked_scales_bytes(N, K, "mxfp4")), torch.uint8, w.device)
+    for e in range(E):
+        moe_quantize_mxfp4(w[e], blocked=True, packed=packed[e], scales=scales[e])
+    return packed, scales
+
+
 # ---- a3 ------------------------------------------------------------------------
 def moe_permute_rows_capacity(T, E, k):
     return int(_lib.moe_permute_rows_capacity(T, E, k))
@@ -233,13 +268,13 @@ class Permutation:
     rows_capacity: int
 
 
-def alloc_permutation(T, E, k, H, device):
+def alloc_permutation(T, E, k, H, device, fmt="nvfp4"):
     cap = moe_permute_rows_capacity(T, E, k)
     return Permutation(
         counts=_empty((E,), torch.int32, device), offsets=_empty((E + 1,), torch.int32, device),
         row_offsets=_empty((E + 1,), torch.int32, device), perm_to_flat=_empty((cap,), torch.int32, device),
         flat_to_perm=_empty((T * k,), torch.int32, device), a_packed=_empty((cap, H // 2), torch.uint8, device),
-        a_scales=_empty((blocked_scales_bytes(cap, H),), torch.uint8, device), rows_capacity=cap)
+        a_scales=_empty((blocked_scales_bytes(cap, H, fmt),), torch.uint8, device), rows_capacity=cap)
 
 
 def moe_permute_workspace_size(T, E, k):
@@ -262,6 +297,26 @@ def moe_permute(topk_idx, E, xq, xs, out: Permutation = None, workspace=None):
                             _ptr(out.row_offsets), _ptr(out.perm_to_flat), _ptr(out.flat_to_perm),
                             _ptr(out.a_packed), _ptr(out.a_scales), _ptr(workspace), workspace.numel(), _stream()),
            "moe_permute")
+    return out
+
+
+def moe_permute_mxfp4(topk_idx, E, xq, xs, out: Permutation = None, workspace=None):
+    """moe_permute for MXFP4 rows (xs row-major [T, H/32]; a_scales blocked MXFP4)."""
+    _need(topk_idx, torch.int32, name="topk_idx")
+    T, k = topk_idx.shape
+    H = xq.shape[1] * 2
+    _need(xq, torch.uint8, (T, H // 2), "xq")
+    _need(xs, torch.uint8, (T, H // 32), "xs")
+    dev = topk_idx.device
+    if out is None:
+        out = alloc_permutation(T, E, k, H, dev, "mxfp4")
+    ws_bytes = moe_permute_workspace_size(T, E, k)
+    if workspace is None:
+        workspace = _empty((ws_bytes,), torch.uint8, dev)
+    _check(_lib.moe_permute_mxfp4(_ptr(topk_idx), T, E, k, _ptr(xq), _ptr(xs), H, _ptr(out.counts),
+                                  _ptr(out.offsets), _ptr(out.row_offsets), _ptr(out.perm_to_flat),
+                                  _ptr(out.flat_to_perm), _ptr(out.a_packed), _ptr(out.a_scales), _ptr(workspace),
+                                  workspace.numel(), _stream()), "moe_permute_mxfp4")
     return out
 
 
@@ -383,6 +438,45 @@ def moe_grouped_gemm_nvfp4(a_packed, a_scales, a_gscale, counts, row_offsets, w_
     return (out, out_scales) if epilogue == EPI_SWIGLU_NVFP4 else out
 
 
+def moe_grouped_gemm_mxfp4(a_packed, a_scales, counts, row_offsets, w_packed, w_scales, epilogue=EPI_BF16,
+                           m_total=None, tile_n=0, out=None, out_scales=None):
+    """MXFP4 grouped GEMM.  Returns c_out (and c_scales for EPI_SWIGLU_MXFP4)."""
+    E, N, Kh = w_packed.shape
+    K = 2 * Kh
+    cap = a_packed.shape[0]
+    dev = a_packed.device
+    _need(a_packed, torch.uint8, (cap, K // 2), "a_packed")
+    _need(a_scales, torch.uint8, name="a_scales")
+    _need(counts, torch.int32, (E,), "counts")
+    _need(row_offsets, torch.int32, (E + 1,), "row_offsets")
+    _need(w_packed, torch.uint8, name="w_packed")
+    _need(w_scales, torch.uint8, name="w_scales")
+    if a_scales.numel() < blocked_scales_bytes(cap, K, "mxfp4") or \
+            w_scales.numel() < E * blocked_scales_bytes(N, K, "mxfp4"):
+        raise ValueError("scale buffers smaller than the MXFP4 blocked layout needs")
+    if epilogue == EPI_BF16:
+        out = _empty((cap, N), torch.bfloat16, dev) if out is None else out
+        _need(out, torch.bfloat16, (cap, N), "out")
+    elif epilogue == EPI_SWIGLU_MXFP4:
+        I = N // 2
+        out = _empty((cap, I // 2), torch.uint8, dev) if out is None else out
+        out_scales = _empty((blocked_scales_bytes(cap, I, "mxfp4"),), torch.uint8, dev) if out_scales is None \
+            else out_scales
+        _need(out, torch.uint8, (cap, I // 2), "out")
+        _need(out_scales, torch.uint8, name="out_scales")
+    elif epilogue == EPI_SWIGLU_F32:
+        out = _empty((cap, N // 2), torch.float32, dev) if out is None else out
+        _need(out, torch.float32, (cap, N // 2), "out")
+    else:
+        raise ValueError(f"epilogue {epilogue}")
+    if m_total is None:
+        m_total = cap
+    _check(_lib.moe_grouped_gemm_mxfp4(_ptr(a_packed), _ptr(a_scales), _ptr(counts), _ptr(row_offsets), E, cap,
+                                       int(m_total), _ptr(w_packed), _ptr(w_scales), N, K, epilogue, _ptr(out),
+                                       _ptr(out_scales), int(tile_n), _stream()), "moe_grouped_gemm_mxfp4")
+    return (out, out_scales) if epilogue == EPI_SWIGLU_MXFP4 else out
+
+
 # ---- a6 ------------------------------------------------------------------------
 def moe_finalize(y, flat_to_perm, topk_w, out=None):
     _need(y, torch.bfloat16, name="y")
@@ -400,17 +494,21 @@ def moe_finalize(y, flat_to_perm, topk_w, out=None):
 
 # ---- the whole layer -------------------------------------------------------------
 class MoELayer:
-    """NVFP4 expert weights plus every buffer of one layer shape.
+    """Quantised expert weights plus every buffer of one layer shape.
 
     forward() enqueues the layer on the current stream and allocates
-    nothing: with fused_prepare (the default) four launches -- moe_prepare
-    (route + quantise + permute), gate/up GEMM with SwiGLU and
+    nothing.  NVFP4 with fused_prepare (the default): four launches --
+    moe_prepare (route + quantise + permute), gate/up GEMM with SwiGLU and
     requantisation, down GEMM, finalize -- otherwise the six separate calls
-    (nine launches and one memset)."""
+    (nine launches and one memset).  fmt="mxfp4": the same layer on MXFP4
+    operands through the separate calls (eight launches)."""
 
     def __init__(self, w_gu, w_d, k, score_fn="sigmoid", renormalize=True, h_scale=2.0 ** -4, bias=None,
-                 T=None, tile_n=(0, 0), fused_prepare=True, k_primary=None):
-        self.fused_prepare = bool(fused_prepare)
+                 T=None, tile_n=(0, 0), fused_prepare=True, k_primary=None, fmt="nvfp4"):
+        if fmt not in ("nvfp4", "mxfp4"):
+            raise ValueError(f"fmt {fmt}")
+        self.fmt = fmt
+        self.fused_prepare = bool(fused_prepare) and fmt == "nvfp4"
         # batch-aware routing when k_primary < k (moe_route_batch_aware)
         self.k_primary = k if k_primary is None else int(k_primary)
         self.E, two_i, self.H = w_gu.shape
@@ -419,8 +517,13 @@ class MoELayer:
         self.device = w_gu.device
         self.bias = bias
         self.tile_n = tile_n
-        self.w_gu_packed, self.w_gu_scales, self.w_gu_gscale = quantize_expert_weights(w_gu)
-        self.w_d_packed, self.w_d_scales, self.w_d_gscale = quantize_expert_weights(w_d)
+        if fmt == "mxfp4":
+            self.w_gu_packed, self.w_gu_scales = quantize_expert_weights_mx(w_gu)
+            self.w_d_packed, self.w_d_scales = quantize_expert_weights_mx(w_d)
+            self.w_gu_gscale = self.w_d_gscale = None
+        else:
+            self.w_gu_packed, self.w_gu_scales, self.w_gu_gscale = quantize_expert_weights(w_gu)
+            self.w_d_packed, self.w_d_scales, self.w_d_gscale = quantize_expert_weights(w_d)
         self.h_scale = torch.full((1,), h_scale, dtype=torch.float32, device=self.device)
         self.T = None
         if T is not None:
@@ -433,15 +536,15 @@ class MoELayer:
         self.topk_w = _empty((T, k), torch.float32, dev)
         self.x_gscale = _empty((1,), torch.float32, dev)
         self.xq = _empty((T, H // 2), torch.uint8, dev)
-        self.xs = _empty((T, H // 16), torch.uint8, dev)
+        self.xs = _empty((T, H // (32 if self.fmt == "mxfp4" else 16)), torch.uint8, dev)
         self.q_ws = _empty((64,), torch.uint8, dev)
         self.r_ws = _empty((int(_lib.moe_route_batch_aware_workspace_size(E)),), torch.uint8, dev)
-        self.perm = alloc_permutation(T, E, k, H, dev)
+        self.perm = alloc_permutation(T, E, k, H, dev, self.fmt)
         self.p_ws = _empty((moe_permute_workspace_size(T, E, k),), torch.uint8, dev)
         self.prep_ws = alloc_prepare_workspace(T, E, k, dev)
         cap = self.perm.rows_capacity
         self.hq = _empty((cap, I // 2), torch.uint8, dev)
-        self.hs = _empty((blocked_scales_bytes(cap, I),), torch.uint8, dev)
+        self.hs = _empty((blocked_scales_bytes(cap, I, self.fmt),), torch.uint8, dev)
         self.y = _empty((cap, H), torch.bfloat16, dev)
         self.out = _empty((T, H), torch.bfloat16, dev)
 
@@ -450,16 +553,21 @@ class MoELayer:
         if self.T != T:
             self._alloc(T)
         p = self.perm
+        if self.fmt == "mxfp4":
+            self._route(logits)
+            moe_quantize_mxfp4(x, packed=self.xq, scales=self.xs)
+            moe_permute_mxfp4(self.topk_idx, self.E, self.xq, self.xs, out=p, workspace=self.p_ws)
+            moe_grouped_gemm_mxfp4(p.a_packed, p.a_scales, p.counts, p.row_offsets, self.w_gu_packed,
+                                   self.w_gu_scales, EPI_SWIGLU_MXFP4, m_total=T * self.k, tile_n=self.tile_n[0],
+                                   out=self.hq, out_scales=self.hs)
+            moe_grouped_gemm_mxfp4(self.hq, self.hs, p.counts, p.row_offsets, self.w_d_packed, self.w_d_scales,
+                                   EPI_BF16, m_total=T * self.k, tile_n=self.tile_n[1], out=self.y)
+            return moe_finalize(self.y, p.flat_to_perm, self.topk_w, out=self.out if out is None else out)
         if self.fused_prepare:
             moe_prepare(logits, x, self.k, self.score_fn, self.renormalize, self.bias, self.topk_idx, self.topk_w,
                         self.x_gscale, self.xq, self.xs, out=p, workspace=self.prep_ws, k_primary=self.k_primary)
         else:
-            if self.k_primary < self.k:
-                moe_route_batch_aware(logits, self.k, self.k_primary, self.score_fn, self.renormalize, self.bias,
-                                      self.topk_idx, self.topk_w, workspace=self.r_ws)
-            else:
-                moe_route_topk(logits, self.k, self.score_fn, self.renormalize, self.bias, self.topk_idx,
-                               self.topk_w)
+            self._route(logits)
             moe_quantize_nvfp4(x, global_scale=self.x_gscale, compute_global=True, packed=self.xq,
                                scales=self.xs, workspace=self.q_ws)
             moe_permute(self.topk_idx, self.E, self.xq, self.xs, out=p, workspace=self.p_ws)
@@ -473,8 +581,19 @@ class MoELayer:
 
     __call__ = forward
 
+    def _route(self, logits):
+        if self.k_primary < self.k:
+            moe_route_batch_aware(logits, self.k, self.k_primary, self.score_fn, self.renormalize, self.bias,
+                                  self.topk_idx, self.topk_w, workspace=self.r_ws)
+        else:
+            moe_route_topk(logits, self.k, self.score_fn, self.renormalize, self.bias, self.topk_idx, self.topk_w)
+
     # kernels launched by one forward(): fused prepare 1 (else route 1, quantise 2, permute 3),
     # GEMMs 2, finalize 1
     @property
     def launches_per_forward(self):
-        return 4 if self.fused_prepare else (10 if self.k_primary < self.k else 9)
+        if self.fused_prepare:
+            return 4
+        route = 2 if self.k_primary < self.k else 1
+        quantise = 1 if self.fmt == "mxfp4" else 2
+        return route + quantise + 3 + 2 + 1

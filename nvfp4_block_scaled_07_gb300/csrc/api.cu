@@ -137,6 +137,11 @@ size_t nvfp4moe_blocked_scales_bytes(int64_t rows, int64_t cols) {
   return size_t(ceil_div(rows, 128) * 128 * (cols / 16));
 }
 
+size_t nvfp4moe_mxfp4_blocked_scales_bytes(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols <= 0 || cols % 128) return 0;
+  return size_t(ceil_div(rows, 128) * 128 * (cols / 32));
+}
+
 // ---- a1 ---------------------------------------------------------------------
 int moe_route_topk(const float* logits, const float* bias, int T, int E, int k, int score_fn, int renormalize,
                    int32_t* topk_idx, float* topk_w, cudaStream_t stream) {
@@ -214,6 +219,27 @@ int moe_quantize_nvfp4(const void* x_bf16, int64_t rows, int64_t cols, float* gl
                      "quantize launch");
 }
 
+int moe_quantize_mxfp4(const void* x_bf16, int64_t rows, int64_t cols, int flags, uint8_t* packed, uint8_t* scales,
+                       cudaStream_t stream) {
+  t_detail[0] = 0;
+  NVFP4MOE_REQUIRE(rows >= 0 && cols > 0, NVFP4MOE_ERR_INVALID_ARG, "rows %lld cols %lld", (long long)rows,
+                   (long long)cols);
+  NVFP4MOE_REQUIRE((flags & ~NVFP4MOE_QUANT_SCALES_BLOCKED) == 0, NVFP4MOE_ERR_INVALID_ARG, "unknown flags 0x%x",
+                   flags);
+  const bool blocked = flags & NVFP4MOE_QUANT_SCALES_BLOCKED;
+  NVFP4MOE_REQUIRE(cols % 32 == 0, NVFP4MOE_ERR_UNSUPPORTED, "cols %lld is not a multiple of 32", (long long)cols);
+  NVFP4MOE_REQUIRE(!blocked || cols % 128 == 0, NVFP4MOE_ERR_UNSUPPORTED,
+                   "blocked scales need cols %% 128 == 0 (cols %lld)", (long long)cols);
+  if (rows == 0) return NVFP4MOE_OK;
+  NVFP4MOE_REQUIRE(x_bf16 && packed && scales, NVFP4MOE_ERR_INVALID_ARG, "null pointer");
+  NVFP4MOE_REQUIRE(aligned16(x_bf16) && aligned16(packed), NVFP4MOE_ERR_INVALID_ARG,
+                   "x and packed must be 16-byte aligned");
+  DeviceInfo d;
+  if (int st = current_device(&d)) return st;
+  return cuda_status(launch_quantize_mx(x_bf16, rows, cols, blocked, packed, scales, d.num_sms, stream),
+                     "MXFP4 quantize launch");
+}
+
 int moe_scales_to_blocked(const uint8_t* scales_row_major, int64_t rows, int64_t cols, uint8_t* scales_blocked,
                           cudaStream_t stream) {
   t_detail[0] = 0;
@@ -244,7 +270,7 @@ size_t moe_permute_workspace_size(int T, int E, int k) {
   return rank + 2 * seg + 256;
 }
 
-int moe_permute(const int32_t* topk_idx, int T, int E, int k, const uint8_t* xq, const uint8_t* xs, int H,
+static int permute_common(const int32_t* topk_idx, int T, int E, int k, const uint8_t* xq, const uint8_t* xs, int H, int scale_block,
                 int32_t* expert_counts, int32_t* expert_offsets, int32_t* row_offsets, int32_t* perm_to_flat,
                 int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales, void* ws, size_t ws_bytes,
                 cudaStream_t stream) {
@@ -252,7 +278,8 @@ int moe_permute(const int32_t* topk_idx, int T, int E, int k, const uint8_t* xq,
   NVFP4MOE_REQUIRE(T >= 0, NVFP4MOE_ERR_INVALID_ARG, "T = %d", T);
   NVFP4MOE_REQUIRE(E >= 1 && E <= 1024, NVFP4MOE_ERR_UNSUPPORTED, "E = %d outside [1, 1024]", E);
   NVFP4MOE_REQUIRE(k >= 1 && k <= E, NVFP4MOE_ERR_UNSUPPORTED, "k = %d outside [1, E]", k);
-  NVFP4MOE_REQUIRE(H > 0 && H % 64 == 0, NVFP4MOE_ERR_UNSUPPORTED, "H = %d must be a positive multiple of 64", H);
+  NVFP4MOE_REQUIRE(H > 0 && H % (4 * scale_block) == 0, NVFP4MOE_ERR_UNSUPPORTED,
+                   "H = %d must be a positive multiple of %d", H, 4 * scale_block);
   NVFP4MOE_REQUIRE(int64_t(T) * k <= (int64_t(1) << 30), NVFP4MOE_ERR_UNSUPPORTED, "T*k too large");
   NVFP4MOE_REQUIRE(expert_counts && expert_offsets && row_offsets && perm_to_flat, NVFP4MOE_ERR_INVALID_ARG,
                    "null pointer");
@@ -270,11 +297,27 @@ int moe_permute(const int32_t* topk_idx, int T, int E, int k, const uint8_t* xq,
   int32_t* rank = static_cast<int32_t*>(ws);
   int32_t* seg_count = rank + ceil_div(R, 64) * 64;
   int32_t* seg_base = seg_count + ceil_div(nseg * E, 64) * 64;
-  return cuda_status(launch_permute(topk_idx, T, E, k, xq, xs, H, expert_counts, expert_offsets, row_offsets,
+  return cuda_status(launch_permute(topk_idx, T, E, k, xq, xs, H, H / (4 * scale_block), expert_counts, expert_offsets, row_offsets,
                                     perm_to_flat, flat_to_perm, a_packed, a_scales,
                                     moe_permute_rows_capacity(T, E, k), rank, seg_count, seg_base, d.num_sms,
                                     stream),
                      "permute launch");
+}
+
+int moe_permute(const int32_t* topk_idx, int T, int E, int k, const uint8_t* xq, const uint8_t* xs, int H,
+                int32_t* expert_counts, int32_t* expert_offsets, int32_t* row_offsets, int32_t* perm_to_flat,
+                int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales, void* ws, size_t ws_bytes,
+                cudaStream_t stream) {
+  return permute_common(topk_idx, T, E, k, xq, xs, H, 16, expert_counts, expert_offsets, row_offsets, perm_to_flat,
+                        flat_to_perm, a_packed, a_scales, ws, ws_bytes, stream);
+}
+
+int moe_permute_mxfp4(const int32_t* topk_idx, int T, int E, int k, const uint8_t* xq, const uint8_t* xs, int H,
+                      int32_t* expert_counts, int32_t* expert_offsets, int32_t* row_offsets, int32_t* perm_to_flat,
+                      int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales, void* ws, size_t ws_bytes,
+                      cudaStream_t stream) {
+  return permute_common(topk_idx, T, E, k, xq, xs, H, 32, expert_counts, expert_offsets, row_offsets, perm_to_flat,
+                        flat_to_perm, a_packed, a_scales, ws, ws_bytes, stream);
 }
 
 int moe_permute_no_alloc(const int32_t* topk_idx, int T, int E, int k, const uint8_t* xq, const uint8_t* xs, int H,
@@ -360,19 +403,19 @@ size_t moe_grouped_gemm_nvfp4_workspace_size(int E, int N, int K, int epilogue) 
   return 0;
 }
 
-int moe_grouped_gemm_nvfp4(const uint8_t* a_packed, const uint8_t* a_scales, const float* a_gscale,
-                           const int32_t* expert_counts, const int32_t* row_offsets, int E, int64_t rows_capacity,
-                           int64_t m_total, const uint8_t* w_packed, const uint8_t* w_scales,
-                           const float* w_gscale, int N, int K, int epilogue, const float* c_gscale, void* c_out,
-                           uint8_t* c_scales, int tile_n, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
+static int grouped_gemm_common(bool mx, const uint8_t* a_packed, const uint8_t* a_scales, const float* a_gscale,
+                               const int32_t* expert_counts, const int32_t* row_offsets, int E, int64_t rows_capacity,
+                               int64_t m_total, const uint8_t* w_packed, const uint8_t* w_scales,
+                               const float* w_gscale, int N, int K, int epilogue, const float* c_gscale, void* c_out,
+                               uint8_t* c_scales, int tile_n, cudaStream_t stream) {
   t_detail[0] = 0;
-  NVFP4MOE_REQUIRE(epilogue == NVFP4MOE_EPI_BF16 || epilogue == NVFP4MOE_EPI_SWIGLU_NVFP4 ||
-                       epilogue == NVFP4MOE_EPI_SWIGLU_F32,
+  const int requant = mx ? NVFP4MOE_EPI_SWIGLU_MXFP4 : NVFP4MOE_EPI_SWIGLU_NVFP4;
+  NVFP4MOE_REQUIRE(epilogue == NVFP4MOE_EPI_BF16 || epilogue == requant || epilogue == NVFP4MOE_EPI_SWIGLU_F32,
                    NVFP4MOE_ERR_INVALID_ARG, "epilogue %d", epilogue);
   NVFP4MOE_REQUIRE(E >= 1 && E <= 1024, NVFP4MOE_ERR_UNSUPPORTED, "E = %d outside [1, 1024]", E);
-  NVFP4MOE_REQUIRE(K >= 64 && K % 64 == 0, NVFP4MOE_ERR_UNSUPPORTED, "K = %d must be a positive multiple of 64", K);
+  const int kq = mx ? 128 : 64;
+  NVFP4MOE_REQUIRE(K >= kq && K % kq == 0, NVFP4MOE_ERR_UNSUPPORTED, "K = %d must be a positive multiple of %d", K,
+                   kq);
   const bool swiglu = epilogue != NVFP4MOE_EPI_BF16;
   NVFP4MOE_REQUIRE(N > 0 && N % (swiglu ? 256 : 128) == 0, NVFP4MOE_ERR_UNSUPPORTED,
                    "N = %d must be a multiple of %d for this epilogue", N, swiglu ? 256 : 128);
@@ -383,11 +426,13 @@ int moe_grouped_gemm_nvfp4(const uint8_t* a_packed, const uint8_t* a_scales, con
   NVFP4MOE_REQUIRE(m_total >= 0, NVFP4MOE_ERR_INVALID_ARG, "m_total < 0");
   NVFP4MOE_REQUIRE(tile_n == 0 || tile_n == 128 || (!swiglu && tile_n == 256), NVFP4MOE_ERR_UNSUPPORTED,
                    "tile_n %d (expected 0, 128, or 256 for the bf16 epilogue)", tile_n);
-  NVFP4MOE_REQUIRE(a_packed && a_scales && a_gscale && expert_counts && row_offsets && w_packed && w_scales &&
-                       w_gscale && c_out,
+  NVFP4MOE_REQUIRE(a_packed && a_scales && expert_counts && row_offsets && w_packed && w_scales && c_out,
                    NVFP4MOE_ERR_INVALID_ARG, "null pointer");
+  NVFP4MOE_REQUIRE(mx || (a_gscale && w_gscale), NVFP4MOE_ERR_INVALID_ARG, "null per-tensor scale pointer");
   NVFP4MOE_REQUIRE(epilogue != NVFP4MOE_EPI_SWIGLU_NVFP4 || (c_gscale && c_scales), NVFP4MOE_ERR_INVALID_ARG,
                    "SWIGLU_NVFP4 needs c_gscale and c_scales");
+  NVFP4MOE_REQUIRE(epilogue != NVFP4MOE_EPI_SWIGLU_MXFP4 || c_scales, NVFP4MOE_ERR_INVALID_ARG,
+                   "SWIGLU_MXFP4 needs c_scales");
   NVFP4MOE_REQUIRE(aligned16(a_packed) && aligned16(a_scales) && aligned16(w_packed) && aligned16(w_scales) &&
                        aligned16(c_out),
                    NVFP4MOE_ERR_INVALID_ARG, "operands must be 16-byte aligned");
@@ -412,7 +457,28 @@ int moe_grouped_gemm_nvfp4(const uint8_t* a_packed, const uint8_t* a_scales, con
   a.c_out = c_out;
   a.c_scales = c_scales;
   a.tile_n = tile_n;
+  a.mx = mx;
   return launch_grouped_gemm(a, d.num_sms, d.smem_optin, stream);  // detail already set on failure
+}
+
+int moe_grouped_gemm_nvfp4(const uint8_t* a_packed, const uint8_t* a_scales, const float* a_gscale,
+                           const int32_t* expert_counts, const int32_t* row_offsets, int E, int64_t rows_capacity,
+                           int64_t m_total, const uint8_t* w_packed, const uint8_t* w_scales,
+                           const float* w_gscale, int N, int K, int epilogue, const float* c_gscale, void* c_out,
+                           uint8_t* c_scales, int tile_n, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  return grouped_gemm_common(false, a_packed, a_scales, a_gscale, expert_counts, row_offsets, E, rows_capacity,
+                             m_total, w_packed, w_scales, w_gscale, N, K, epilogue, c_gscale, c_out, c_scales, tile_n,
+                             stream);
+}
+
+int moe_grouped_gemm_mxfp4(const uint8_t* a_packed, const uint8_t* a_scales, const int32_t* expert_counts,
+                           const int32_t* row_offsets, int E, int64_t rows_capacity, int64_t m_total,
+                           const uint8_t* w_packed, const uint8_t* w_scales, int N, int K, int epilogue, void* c_out,
+                           uint8_t* c_scales, int tile_n, cudaStream_t stream) {
+  return grouped_gemm_common(true, a_packed, a_scales, nullptr, expert_counts, row_offsets, E, rows_capacity, m_total,
+                             w_packed, w_scales, nullptr, N, K, epilogue, nullptr, c_out, c_scales, tile_n, stream);
 }
 
 // ---- a6 ---------------------------------------------------------------------

@@ -61,4 +61,27 @@ __device__ __forceinline__ uint32_t e2m1_code(float x, float d) {
   return e2m1_mag_code(fabsf(x) / d) | sign;
 }
 
+// ---- MXFP4: E2M1 with one E8M0 scale 2^X per 32 elements ----------------------
+// X = floor(log2(amax)) - 2 (2 = exponent of E2M1's largest value, 6 = 1.5 * 2^2),
+// clamped to [-127, 127]; an all-zero block takes X = -127.  floor(log2) is
+// read off the float32 bits (normal or subnormal), so it is exact.
+__device__ __forceinline__ int mx_exponent(float amax) {
+  const uint32_t bits = __float_as_uint(amax);
+  if (bits == 0u) return -127;
+  const int e_field = int(bits >> 23);
+  const int fl = e_field ? e_field - 127 : (31 - __clz(int(bits))) - 149;
+  const int x = fl - 2;
+  return x < -127 ? -127 : (x > 127 ? 127 : x);
+}
+
+// 2^-X as a float32 (exact: X <= 125 for any finite bf16/float32 amax, and
+// 2^127 is representable for X = -127).
+__device__ __forceinline__ float mx_inv_step(int x) { return __uint_as_float(uint32_t(127 - x) << 23); }
+
+// Code of one element given 2^-X of its block: nearest E2M1 of x * 2^-X, sign of x.
+__device__ __forceinline__ uint32_t mx_code(float x, float inv_step) {
+  const uint32_t sign = (__float_as_uint(x) >> 31) << 3;
+  return e2m1_mag_code(fabsf(x) * inv_step) | sign;
+}
+
 }  // namespace nvfp4moe

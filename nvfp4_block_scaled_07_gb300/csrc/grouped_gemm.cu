@@ -241,7 +241,45 @@ __device__ __forceinline__ void requant_swiglu_chunk(const float (&h)[32], int l
   }
 }
 
-template <int BN, int NA, bool SWIGLU>
+// MXFP4 requantisation of a 32-token x 32-feature chunk of the SwiGLU output
+// (lane = feature f0 + lane with f0 % 32 == 0, h[t] = token t): the warp's
+// 32 features are one MX block per token.  A reduce-scatter butterfly over
+// the 32 lanes leaves token l's block amax in lane l, which derives the
+// token's shared exponent and scale byte; every element then takes its
+// token's 2^-X from lane t.
+__device__ __forceinline__ void requant_swiglu_chunk_mx(const float (&h)[32], int lane, int64_t row0, int nvalid,
+                                                        int f, int n_out, uint8_t* out_codes, uint8_t* out_scales) {
+  float a[32];
+#pragma unroll
+  for (int t = 0; t < 32; ++t) a[t] = fabsf(h[t]);
+#pragma unroll
+  for (int step = 16; step >= 1; step >>= 1) {   // 32 -> 16 -> ... -> 1 token per lane
+    const bool hi = lane & step;
+#pragma unroll
+    for (int t = 0; t < step; ++t) {
+      const float keep = hi ? a[t + step] : a[t];
+      const float give = hi ? a[t] : a[t + step];
+      a[t] = fmaxf(keep, __shfl_xor_sync(kFull, give, step));
+    }
+  }
+  const int X = mx_exponent(a[0]);               // token `lane`
+  const float inv = mx_inv_step(X);
+  const int f0 = f & ~31;
+  if (lane < nvalid)
+    out_scales[blocked_sf_offset(row0 + lane, f0 >> 7, n_out / 128) + ((f0 >> 5) & 3)] = uint8_t(X + 127);
+  uint8_t* row_ptr = out_codes + row0 * (n_out / 2) + (f & ~7) / 2;
+#pragma unroll
+  for (int t = 0; t < 32; ++t) {
+    const float it = __shfl_sync(kFull, inv, t);
+    uint32_t word = mx_code(h[t], it) << (4 * (lane & 7));
+    word |= __shfl_xor_sync(kFull, word, 1);
+    word |= __shfl_xor_sync(kFull, word, 2);
+    word |= __shfl_xor_sync(kFull, word, 4);
+    if ((lane & 7) == 0 && t < nvalid) *reinterpret_cast<uint32_t*>(row_ptr + int64_t(t) * (n_out / 2)) = word;
+  }
+}
+
+template <int BN, int NA, bool SWIGLU, bool MX>
 __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                         const Params p) {
@@ -342,6 +380,8 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   const int total = s_prefix[p.E];
   const int kblocks = p.K / 64;
   const int nkt = (kblocks + 3) / 4;
+  const int sf_k = MX ? p.K / 128 : kblocks;     // 512-byte scale blocks along K per 128 rows
+  const int sf_per_kt = MX ? 2 : 4;              // of them per 256-element K stage
   // Stage geometry for this launch: as many stages as fit once the token
   // slot is sized for the widest tile actually present.
   const int wmax = *s_wmax;
@@ -373,7 +413,10 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
           break;
         }
         const int nkb = min(4, kblocks - 4 * kt);
-        const uint32_t bytes = uint32_t(C::NA * kATile + w * kBKBytes + (C::NA + sfb_chunks) * nkb * 512);
+        // 512-byte scale blocks of this stage per 128 rows: one per k64 step
+        // (NVFP4) or per k128 step (MXFP4, K % 128 == 0)
+        const int nsf = MX ? nkb / 2 : nkb;
+        const uint32_t bytes = uint32_t(C::NA * kATile + w * kBKBytes + (C::NA + sfb_chunks) * nsf * 512);
         ptx::mbar_arrive_expect_tx(full_bar(s), bytes);
         const uint32_t st = smem_base + s * uint32_t(stage);
 #pragma unroll
@@ -384,12 +427,12 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
 #pragma unroll
         for (int j = 0; j < C::NA; ++j) {
           const int rb = SWIGLU ? (j * (p.N / 2) + mb * kBM) / kBM : mb * NA + j;
-          const uint8_t* src = p.w_scales + ((size_t(e) * (p.N / kBM) + rb) * kblocks + 4 * kt) * 512;
-          ptx::bulk_load(st + off_sfa + j * kSfTile, src, uint32_t(nkb * 512), full_bar(s), pol_w);
+          const uint8_t* src = p.w_scales + ((size_t(e) * (p.N / kBM) + rb) * sf_k + sf_per_kt * kt) * 512;
+          ptx::bulk_load(st + off_sfa + j * kSfTile, src, uint32_t(nsf * 512), full_bar(s), pol_w);
         }
         for (int c = 0; c < sfb_chunks; ++c) {
-          const uint8_t* src = p.a_scales + ((size_t(arow / kBM) + c) * kblocks + 4 * kt) * 512;
-          ptx::bulk_load(st + off_sfb + c * kSfTile, src, uint32_t(nkb * 512), full_bar(s), pol_a);
+          const uint8_t* src = p.a_scales + ((size_t(arow / kBM) + c) * sf_k + sf_per_kt * kt) * 512;
+          ptx::bulk_load(st + off_sfb + c * kSfTile, src, uint32_t(nsf * 512), full_bar(s), pol_a);
         }
       }
     }
@@ -411,7 +454,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       if (!wait_phase(acce_bar(s0), slots.parity(s0) ^ 1u, abort_flag)) break;
       if (s1 >= 0 && !wait_phase(acce_bar(s1), slots.parity(s1) ^ 1u, abort_flag)) break;
       ptx::tc_fence_after();
-      const uint32_t idesc = ptx::idesc_nvfp4(kBM, w);
+      const uint32_t idesc = ptx::idesc_nvfp4(kBM, w, MX);
       const uint32_t d0 = tmem + uint32_t(s0 * kAccSlotCols);
       for (int kt = 0; kt < nkt; ++kt, ++it) {
         const uint32_t s = it % uint32_t(S), ph = (it / uint32_t(S)) & 1u;
@@ -434,9 +477,14 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         // fully unrolled sequence; only a partial last K tile takes the loop.
         auto mma_block = [&](int kb) {
 #pragma unroll
-          for (int j = 0; j < C::NA; ++j)
-            ptx::tc_mma_nvfp4(d0 + j * w, ptx::desc_kmajor_sw128(st + j * kATile) + 2 * kb, bdesc + 2 * kb, idesc,
-                              sf + j * 16 + kb * 4, sf + C::NA * 16 + kb * 4 * C::NSFB, (kt | kb) != 0 ? 1u : 0u);
+          for (int j = 0; j < C::NA; ++j) {
+            if constexpr (MX)
+              ptx::tc_mma_mxfp4(d0 + j * w, ptx::desc_kmajor_sw128(st + j * kATile) + 2 * kb, bdesc + 2 * kb, idesc,
+                                sf + j * 16 + kb * 4, sf + C::NA * 16 + kb * 4 * C::NSFB, (kt | kb) != 0 ? 1u : 0u);
+            else
+              ptx::tc_mma_nvfp4(d0 + j * w, ptx::desc_kmajor_sw128(st + j * kATile) + 2 * kb, bdesc + 2 * kb, idesc,
+                                sf + j * 16 + kb * 4, sf + C::NA * 16 + kb * 4 * C::NSFB, (kt | kb) != 0 ? 1u : 0u);
+          }
         };
         if (nkb == 4) {
 #pragma unroll
@@ -480,15 +528,37 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         const uint32_t st = smem_base + s * uint32_t(stage);
         const uint32_t sf = tmem + lane_base + uint32_t(kSfColBase + r * C::SfCols);
         const int nkb = min(4, kblocks - 4 * kt);
-        for (int kb = 0; kb < nkb; ++kb) {
+        if constexpr (MX) {
+          // A 512-byte MXFP4 block holds 4 ue8m0 scales per row for 128 K
+          // elements: bytes 0-1 go to the k64 step 2m, bytes 2-3 to 2m + 1,
+          // each into bytes 0-1 of that step's cell.
+          for (int m = 0; m < nkb / 2; ++m) {
 #pragma unroll
-          for (int j = 0; j < C::NA; ++j) {
-            const uint4 v = ptx::lds128(st + off_sfa + j * kSfTile + kb * 512 + lane * 16);
-            ptx::tmem_st_32x32b_x4(sf + j * 16 + kb * 4, v.x, v.y, v.z, v.w);
+            for (int j = 0; j < C::NA; ++j) {
+              const uint4 v = ptx::lds128(st + off_sfa + j * kSfTile + m * 512 + lane * 16);
+              ptx::tmem_st_32x32b_x4(sf + j * 16 + (2 * m) * 4, v.x & 0xFFFFu, v.y & 0xFFFFu, v.z & 0xFFFFu,
+                                     v.w & 0xFFFFu);
+              ptx::tmem_st_32x32b_x4(sf + j * 16 + (2 * m + 1) * 4, v.x >> 16, v.y >> 16, v.z >> 16, v.w >> 16);
+            }
+            for (int c = 0; c < sfb_chunks; ++c) {
+              const uint4 v = ptx::lds128(st + off_sfb + c * kSfTile + m * 512 + lane * 16);
+              ptx::tmem_st_32x32b_x4(sf + C::NA * 16 + (2 * m) * 4 * C::NSFB + c * 4, v.x & 0xFFFFu, v.y & 0xFFFFu,
+                                     v.z & 0xFFFFu, v.w & 0xFFFFu);
+              ptx::tmem_st_32x32b_x4(sf + C::NA * 16 + (2 * m + 1) * 4 * C::NSFB + c * 4, v.x >> 16, v.y >> 16,
+                                     v.z >> 16, v.w >> 16);
+            }
           }
-          for (int c = 0; c < sfb_chunks; ++c) {
-            const uint4 v = ptx::lds128(st + off_sfb + c * kSfTile + kb * 512 + lane * 16);
-            ptx::tmem_st_32x32b_x4(sf + C::NA * 16 + kb * 4 * C::NSFB + c * 4, v.x, v.y, v.z, v.w);
+        } else {
+          for (int kb = 0; kb < nkb; ++kb) {
+#pragma unroll
+            for (int j = 0; j < C::NA; ++j) {
+              const uint4 v = ptx::lds128(st + off_sfa + j * kSfTile + kb * 512 + lane * 16);
+              ptx::tmem_st_32x32b_x4(sf + j * 16 + kb * 4, v.x, v.y, v.z, v.w);
+            }
+            for (int c = 0; c < sfb_chunks; ++c) {
+              const uint4 v = ptx::lds128(st + off_sfb + c * kSfTile + kb * 512 + lane * 16);
+              ptx::tmem_st_32x32b_x4(sf + C::NA * 16 + kb * 4 * C::NSFB + c * 4, v.x, v.y, v.z, v.w);
+            }
           }
         }
         ptx::tmem_st_wait();
@@ -504,9 +574,9 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     constexpr int kParts = epi_warps(SWIGLU) / 4;  // warps sharing a quarter split the token chunks
     const int part = (warp - 2) / 4;
     const int lrow = q * 32 + lane;    // accumulator row = output feature within the tile
-    const float a_gs = *p.a_gscale;
+    const float a_gs = MX ? 1.0f : *p.a_gscale;   // MXFP4 has no per-tensor scales
     const bool f32_out = p.epi == NVFP4MOE_EPI_SWIGLU_F32;
-    const float s_h = (SWIGLU && !f32_out) ? *p.c_gscale : 1.0f;
+    const float s_h = (SWIGLU && !f32_out && !MX) ? *p.c_gscale : 1.0f;
     const int n_out = SWIGLU ? p.N / 2 : p.N;
     SlotSeq slots;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -519,7 +589,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       ptx::tc_fence_after();
       const int valid = min(w, s_count[e] - nb * BN);
       const int64_t row0 = int64_t(s_rowoff[e]) + int64_t(nb) * BN;
-      const float scale = a_gs * p.w_gscale[e];
+      const float scale = MX ? 1.0f : a_gs * p.w_gscale[e];
       const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + uint32_t(s0 * kAccSlotCols);
       const int f = (SWIGLU ? mb : mb * NA) * kBM + lrow;  // output column (of tile 0)
       for (int c0 = 32 * part; c0 < valid; c0 += 32 * kParts) {
@@ -542,6 +612,9 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               if (c0 + i < valid) out[int64_t(i) * n_out] = h[i];
+          } else if constexpr (MX) {
+            requant_swiglu_chunk_mx(h, lane, row0 + c0, valid - c0, f, n_out, static_cast<uint8_t*>(p.c_out),
+                                    p.c_scales);
           } else {
             requant_swiglu_chunk(h, lane, s_h, row0 + c0, valid - c0, f, n_out, static_cast<uint8_t*>(p.c_out),
                                  p.c_scales);
@@ -623,7 +696,7 @@ int stage_cap_from_env() {
   return cap;
 }
 
-template <int BN, int NA, bool SWIGLU>
+template <int BN, int NA, bool SWIGLU, bool MX>
 int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st) {
   using C = Cfg<BN, NA, SWIGLU>;
   // The whole opt-in shared memory is requested; the kernel sizes its stages
@@ -645,7 +718,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
     return NVFP4MOE_ERR_CUDA;
   }
   cudaError_t err =
-      cudaFuncSetAttribute(grouped_gemm_kernel<BN, NA, SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+      cudaFuncSetAttribute(grouped_gemm_kernel<BN, NA, SWIGLU, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (err != cudaSuccess) {
     set_error_detail("cudaFuncSetAttribute: %s", cudaGetErrorString(err));
     return NVFP4MOE_ERR_CUDA;
@@ -672,7 +745,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   // slower per tile, more than the few microseconds of launch latency it
   // hides.  The kernel still starts with griddepcontrol.wait (a no-op here),
   // so the kernel after it may be launched with the attribute.
-  grouped_gemm_kernel<BN, NA, SWIGLU><<<num_sms, num_threads(SWIGLU), smem, st>>>(tw, ta, p);
+  grouped_gemm_kernel<BN, NA, SWIGLU, MX><<<num_sms, num_threads(SWIGLU), smem, st>>>(tw, ta, p);
   err = cudaGetLastError();
   if (err != cudaSuccess) {
     set_error_detail("grouped GEMM launch: %s", cudaGetErrorString(err));
@@ -683,18 +756,23 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
 
 }  // namespace
 
-int launch_grouped_gemm(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st) {
+template <bool MX>
+int launch_format(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st) {
   const bool swiglu = a.epilogue != NVFP4MOE_EPI_BF16;
   const int bn = a.tile_n == 0 ? 128 : a.tile_n;
   // Small experts (decode): two 128-row weight tiles per stage, so each stage
   // carries twice the weight bytes and two independent accumulation chains.
   const bool pair = a.N % (2 * kBM) == 0 && a.m_total <= int64_t(64) * a.E;
-  if (swiglu && bn == 128) return launch_impl<128, 2, true>(a, num_sms, smem_optin, st);
-  if (!swiglu && bn == 128 && pair) return launch_impl<128, 2, false>(a, num_sms, smem_optin, st);
-  if (!swiglu && bn == 128) return launch_impl<128, 1, false>(a, num_sms, smem_optin, st);
-  if (!swiglu && bn == 256) return launch_impl<256, 1, false>(a, num_sms, smem_optin, st);
+  if (swiglu && bn == 128) return launch_impl<128, 2, true, MX>(a, num_sms, smem_optin, st);
+  if (!swiglu && bn == 128 && pair) return launch_impl<128, 2, false, MX>(a, num_sms, smem_optin, st);
+  if (!swiglu && bn == 128) return launch_impl<128, 1, false, MX>(a, num_sms, smem_optin, st);
+  if (!swiglu && bn == 256) return launch_impl<256, 1, false, MX>(a, num_sms, smem_optin, st);
   set_error_detail("tile_n %d is not supported for this epilogue", a.tile_n);
   return NVFP4MOE_ERR_UNSUPPORTED;
+}
+
+int launch_grouped_gemm(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st) {
+  return a.mx ? launch_format<true>(a, num_sms, smem_optin, st) : launch_format<false>(a, num_sms, smem_optin, st);
 }
 
 cudaError_t gemm_read_and_clear_flags(unsigned* flags) {

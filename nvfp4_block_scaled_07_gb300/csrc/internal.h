@@ -32,11 +32,15 @@ cudaError_t launch_quantize(const void* x, int64_t rows, int64_t cols, float* gl
 cudaError_t launch_scales_to_blocked(const uint8_t* src, int64_t rows, int64_t cols, uint8_t* dst,
                                      int num_sms, cudaStream_t st);
 
+// sf_groups: 4-byte scale groups per row (H/64 for NVFP4, H/128 for MXFP4).
 cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, const uint8_t* xq, const uint8_t* xs,
-                           int H, int32_t* counts, int32_t* offsets, int32_t* row_offsets, int32_t* perm_to_flat,
-                           int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales, int64_t rows_capacity,
-                           int32_t* ws_rank, int32_t* ws_seg_count, int32_t* ws_seg_base, int num_sms,
-                           cudaStream_t st);
+                           int H, int sf_groups, int32_t* counts, int32_t* offsets, int32_t* row_offsets,
+                           int32_t* perm_to_flat, int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales,
+                           int64_t rows_capacity, int32_t* ws_rank, int32_t* ws_seg_count, int32_t* ws_seg_base,
+                           int num_sms, cudaStream_t st);
+
+cudaError_t launch_quantize_mx(const void* x, int64_t rows, int64_t cols, bool blocked, uint8_t* packed,
+                               uint8_t* scales, int num_sms, cudaStream_t st);
 
 // Limits of the permutation that runs on library-owned scratch: routed rows
 // (T*k) and per-segment expert counters (ceil(T*k/1024) * E).
@@ -92,6 +96,7 @@ struct GemmArgs {
   void* c_out;
   uint8_t* c_scales;
   int tile_n;
+  bool mx;  // MXFP4 operands (ue8m0 scale per 32 elements, no per-tensor scales)
 };
 
 // Returns 0 on success or an NVFP4MOE_ERR_* code (message via set_error_detail).

@@ -313,6 +313,55 @@ __global__ void __launch_bounds__(256) scales_to_blocked_kernel(const uint8_t* _
   }
 }
 
+// MXFP4 (E2M1 with one E8M0 scale per 32 elements, no per-tensor scale).
+// One thread per 32-element block: four 128-bit loads, block amax, shared
+// exponent, 32 codes packed into 16 bytes.  Scales row-major [rows, cols/32]
+// or blocked (128-row x 128-K blocks of 512 bytes, row r's four scales at
+// (r % 32) * 16 + (r / 32) * 4).
+__global__ void __launch_bounds__(256) quantize_mx_kernel(const uint4* __restrict__ x, int64_t rows, int64_t cols,
+                                                          uint8_t* __restrict__ packed, uint8_t* __restrict__ scales,
+                                                          int blocked) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  const int64_t bpr = cols / 32;  // blocks per row
+  const int64_t nblk = rows * bpr;
+  const int64_t nblk_pad = blocked ? ((rows + 127) / 128) * 128 * bpr : nblk;
+  const int64_t groups = cols / 128;
+  for (int64_t b = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; b < nblk_pad;
+       b += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t row = b / bpr, c32 = b - row * bpr;
+    uint32_t sb = 0;
+    if (b < nblk) {
+      uint4 q[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) q[j] = x[4 * b + j];
+      float a = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) a = amax8(q[j], a);
+      const int X = mx_exponent(a);
+      sb = uint32_t(X + 127);
+      const float inv = mx_inv_step(X);
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t v[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+        uint32_t word = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          word |= mx_code(bf16_lo(v[i]), inv) << (8 * i);
+          word |= mx_code(bf16_hi(v[i]), inv) << (8 * i + 4);
+        }
+        w[j] = word;
+      }
+      reinterpret_cast<uint4*>(packed)[b] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    if (blocked)
+      scales[blocked_sf_offset(row, c32 >> 2, groups) + (c32 & 3)] = uint8_t(sb);
+    else
+      scales[b] = uint8_t(sb);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // a3: expert-first permutation ("SM120 FP4 Kernel Research Campaign",
 // section 6: expert-first layout and token reordering).  Stable counting
@@ -480,9 +529,10 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(const int32_t* __res
 
 // Flat id f (token f / k, slot f % k): its row in the expert-padded layout,
 // both maps, and a copy of the token's packed row and scales.
+// sf_groups = 4-byte scale groups per row: H/64 for NVFP4, H/128 for MXFP4.
 __device__ __forceinline__ void place_flat(int64_t f, const int32_t* idx, int k, int E, int seg_len,
                                            const int32_t* rank, const int32_t* seg_base, const int32_t* row_offsets,
-                                           const uint8_t* xq, const uint8_t* xs, int H,
+                                           const uint8_t* xq, const uint8_t* xs, int H, int sf_groups,
                                            int32_t* __restrict__ perm_to_flat, int32_t* __restrict__ flat_to_perm,
                                            uint8_t* __restrict__ a_packed, uint8_t* __restrict__ a_scales,
                                            int lane) {
@@ -511,10 +561,9 @@ __device__ __forceinline__ void place_flat(int64_t f, const int32_t* idx, int k,
       if (c < nv) dst[c] = v[j];
     }
   }
-  const int64_t kblocks = H / 64;
-  const unsigned* ssrc = reinterpret_cast<const unsigned*>(xs + t * (H / 16));
-  for (int kb = lane; kb < kblocks; kb += 32)
-    *reinterpret_cast<uint32_t*>(a_scales + blocked_sf_offset(row, kb, kblocks)) = __ldcg(ssrc + kb);
+  const unsigned* ssrc = reinterpret_cast<const unsigned*>(xs + t * (4 * int64_t(sf_groups)));
+  for (int kb = lane; kb < sf_groups; kb += 32)
+    *reinterpret_cast<uint32_t*>(a_scales + blocked_sf_offset(row, kb, sf_groups)) = __ldcg(ssrc + kb);
 }
 
 __global__ void __launch_bounds__(256) permute_place_kernel(const int32_t* __restrict__ idx, int64_t R, int k, int E,
@@ -522,7 +571,7 @@ __global__ void __launch_bounds__(256) permute_place_kernel(const int32_t* __res
                                                             const int32_t* __restrict__ seg_base,
                                                             const int32_t* __restrict__ row_offsets,
                                                             const uint8_t* __restrict__ xq,
-                                                            const uint8_t* __restrict__ xs, int H,
+                                                            const uint8_t* __restrict__ xs, int H, int sf_groups,
                                                             int32_t* __restrict__ perm_to_flat,
                                                             int32_t* __restrict__ flat_to_perm,
                                                             uint8_t* __restrict__ a_packed,
@@ -532,8 +581,8 @@ __global__ void __launch_bounds__(256) permute_place_kernel(const int32_t* __res
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
   for (int64_t f = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); f < R; f += nwarps)
-    place_flat(f, idx, k, E, kPermuteSegment, rank, seg_base, row_offsets, xq, xs, H, perm_to_flat, flat_to_perm,
-               a_packed, a_scales, lane);
+    place_flat(f, idx, k, E, kPermuteSegment, rank, seg_base, row_offsets, xq, xs, H, sf_groups, perm_to_flat,
+               flat_to_perm, a_packed, a_scales, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -710,8 +759,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
   }
   for (int64_t q = int64_t(__ldcg(p.row_offsets + p.E)) + tid; q < p.rows_cap; q += nthreads) p.perm_to_flat[q] = -1;
   for (int64_t f = gw0; f < R; f += gw_stride)
-    place_flat(f, p.idx, p.k, p.E, ITERS * 32, p.rank, p.seg_base, p.row_offsets, p.xq, p.xs, p.H, p.perm_to_flat,
-               p.flat_to_perm, p.a_packed, p.a_scales, lane);
+    place_flat(f, p.idx, p.k, p.E, ITERS * 32, p.rank, p.seg_base, p.row_offsets, p.xq, p.xs, p.H, p.H / 64,
+               p.perm_to_flat, p.flat_to_perm, p.a_packed, p.a_scales, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -827,6 +876,14 @@ cudaError_t launch_quantize(const void* x, int64_t rows, int64_t cols, float* gl
                        blocked ? 1 : 0);
 }
 
+cudaError_t launch_quantize_mx(const void* x, int64_t rows, int64_t cols, bool blocked, uint8_t* packed,
+                               uint8_t* scales, int num_sms, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  const int64_t work = (blocked ? ((rows + 127) / 128) * 128 : rows) * (cols / 32);
+  return launch_kernel(quantize_mx_kernel, dim3(grid_for(work, 256, num_sms, 8)), dim3(256), 0, st, false,
+                       static_cast<const uint4*>(x), rows, cols, packed, scales, blocked ? 1 : 0);
+}
+
 cudaError_t launch_scales_to_blocked(const uint8_t* src, int64_t rows, int64_t cols, uint8_t* dst, int num_sms,
                                      cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
@@ -836,10 +893,10 @@ cudaError_t launch_scales_to_blocked(const uint8_t* src, int64_t rows, int64_t c
 }
 
 cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, const uint8_t* xq, const uint8_t* xs,
-                           int H, int32_t* counts, int32_t* offsets, int32_t* row_offsets, int32_t* perm_to_flat,
-                           int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales, int64_t rows_capacity,
-                           int32_t* ws_rank, int32_t* ws_seg_count, int32_t* ws_seg_base, int num_sms,
-                           cudaStream_t st) {
+                           int H, int sf_groups, int32_t* counts, int32_t* offsets, int32_t* row_offsets,
+                           int32_t* perm_to_flat, int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales,
+                           int64_t rows_capacity, int32_t* ws_rank, int32_t* ws_seg_count, int32_t* ws_seg_base,
+                           int num_sms, cudaStream_t st) {
   const int64_t R = int64_t(T) * k;
   const int nseg = int((R + kPermuteSegment - 1) / kPermuteSegment);
   cudaError_t err;
@@ -860,7 +917,7 @@ cudaError_t launch_permute(const int32_t* topk_idx, int T, int E, int k, const u
   return launch_kernel(permute_place_kernel, dim3(grid_for(R * 32, 256, num_sms, 8)), dim3(256), 0, st, false,
                        topk_idx, R, k, E, static_cast<const int32_t*>(ws_rank),
                        static_cast<const int32_t*>(ws_seg_base), static_cast<const int32_t*>(row_offsets), xq, xs, H,
-                       perm_to_flat, flat_to_perm, a_packed, a_scales);
+                       sf_groups, perm_to_flat, flat_to_perm, a_packed, a_scales);
 }
 
 PrepareLayout prepare_layout(int T, int E, int k) {
@@ -995,8 +1052,8 @@ cudaError_t launch_permute_static_scratch(const int32_t* topk_idx, int T, int E,
   int32_t* rank = base;
   int32_t* seg_count = rank + kNoAllocMaxRoutedRows;
   int32_t* seg_base = seg_count + kNoAllocMaxSegmentExperts;
-  return launch_permute(topk_idx, T, E, k, xq, xs, H, counts, offsets, row_offsets, perm_to_flat, flat_to_perm,
-                        a_packed, a_scales, rows_capacity, rank, seg_count, seg_base, num_sms, st);
+  return launch_permute(topk_idx, T, E, k, xq, xs, H, H / 64, counts, offsets, row_offsets, perm_to_flat,
+                        flat_to_perm, a_packed, a_scales, rows_capacity, rank, seg_count, seg_base, num_sms, st);
 }
 
 cudaError_t prep_read_and_clear_flags(unsigned* flags) {

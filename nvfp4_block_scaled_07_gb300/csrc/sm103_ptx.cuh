@@ -116,6 +116,20 @@ __device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
+// MXFP4: D[tmem] (+)= A[smem] * B[smem]^T with E2M1 operands and two ue8m0
+// scales per row and 64-element K step (scale_vec::2X), held in bytes 0 and
+// 1 of the row's 32-bit scale-factor cell; float32 accumulate.
+__device__ __forceinline__ void tc_mma_mxfp4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T with E2M1 operands and ue4m3 block scales
 // (one scale per 16 K elements, K = 64 per instruction), float32 accumulate.
 __device__ __forceinline__ void tc_mma_nvfp4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -182,12 +196,14 @@ __device__ __forceinline__ uint64_t desc_sf_block(uint32_t saddr) {
 }
 
 // Instruction descriptor for kind::mxf4nvf4: E2M1 x E2M1, both K-major,
-// ue4m3 scale factors, dense, M x N tile.
-__host__ __device__ constexpr uint32_t idesc_nvfp4(int M, int N) {
+// dense, M x N tile; scale format bit 23: 0 = ue4m3 (NVFP4, 16-element
+// blocks), 1 = ue8m0 (MXFP4, 32-element blocks).  Scale-factor IDs 0.
+__host__ __device__ constexpr uint32_t idesc_nvfp4(int M, int N, bool ue8m0 = false) {
   return (1u << 7)                      // A format: E2M1
          | (1u << 10)                   // B format: E2M1
          | (uint32_t(N >> 3) << 17)     // N / 8
-         | (uint32_t(M >> 4) << 24);    // M / 16; scale format bit 23 = 0 (ue4m3)
+         | (uint32_t(ue8m0 ? 1u : 0u) << 23)
+         | (uint32_t(M >> 4) << 24);    // M / 16
 }
 
 }  // namespace ptx

@@ -159,6 +159,15 @@ def nvfp4_bytes(n_elems):
     return n_elems * (0.5 + 1.0 / 16.0)
 
 
+def mxfp4_bytes(n_elems):
+    """Bytes of n MXFP4 elements with their scales: 0.5 + 1/32 per element."""
+    return n_elems * (0.5 + 1.0 / 32.0)
+
+
+def fp4_bytes(n_elems, fmt="nvfp4"):
+    return mxfp4_bytes(n_elems) if fmt == "mxfp4" else nvfp4_bytes(n_elems)
+
+
 def ceil_div(a, b):
     return -(-a // b)
 

@@ -20,23 +20,25 @@ def ceil_to(a, b):
     return -(-a // b) * b
 
 
-def blocked_index(rows_pad, cols):
+def blocked_index(rows_pad, cols, block=16):
+    """Byte offset of scale (row, c) in the blocked layout; block = elements
+    per scale (16 for NVFP4, 32 for MXFP4), four scales per 512-byte group row."""
     r = np.arange(rows_pad, dtype=np.int64)[:, None]
-    c = np.arange(cols // 16, dtype=np.int64)[None, :]
-    return ((r // 128) * (cols // 64) + c // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (c % 4)
+    c = np.arange(cols // block, dtype=np.int64)[None, :]
+    return ((r // 128) * (cols // (4 * block)) + c // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (c % 4)
 
 
-def to_blocked(scales, cols):
+def to_blocked(scales, cols, block=16):
     rows = scales.shape[0]
     rp = max(ceil_to(rows, 128), 128)
-    out = np.zeros(rp * (cols // 16), dtype=np.uint8)
-    out[blocked_index(rp, cols)[:rows].ravel()] = np.asarray(scales, dtype=np.uint8).ravel()
+    out = np.zeros(rp * (cols // block), dtype=np.uint8)
+    out[blocked_index(rp, cols, block)[:rows].ravel()] = np.asarray(scales, dtype=np.uint8).ravel()
     return out
 
 
-def from_blocked(buf, rows, cols):
+def from_blocked(buf, rows, cols, block=16):
     rp = max(ceil_to(rows, 128), 128)
-    return np.asarray(buf)[blocked_index(rp, cols)[:rows]]
+    return np.asarray(buf)[blocked_index(rp, cols, block)[:rows]]
 
 
 def signed_rank(codes):
@@ -59,20 +61,29 @@ def check_close(got, ref, frob_tol=FROB_TOL, elem_tol=ELEM_TOL, what="output"):
     return frob, worst
 
 
-def check_requant(got_codes, got_scales, ref_codes, ref_scales, max_flip_frac=0.01, min_scale_eq=0.99):
+def check_requant(got_codes, got_scales, ref_codes, ref_scales, max_flip_frac=0.01, min_scale_eq=0.99, block=16):
     """Fused SwiGLU requantisation vs the oracle's: float32 accumulation order
     may move a value across an E2M1 or ue4m3 midpoint, so codes may differ by
     one step on a small fraction of elements and scales may differ in a
     small fraction of blocks."""
     eq = np.mean(np.asarray(got_scales) == np.asarray(ref_scales)) if np.size(ref_scales) else 1.0
     assert eq >= min_scale_eq, f"only {eq:.4f} of block scales equal"
-    same_scale = np.repeat(np.asarray(got_scales) == np.asarray(ref_scales), 16, axis=-1)
+    same_scale = np.repeat(np.asarray(got_scales) == np.asarray(ref_scales), block, axis=-1)
     d = np.abs(signed_rank(got_codes) - signed_rank(ref_codes))
     d = d[same_scale]
     assert d.size == 0 or d.max() <= 1, f"a code differs by {d.max()} steps"
     frac = np.mean(d != 0) if d.size else 0.0
     assert frac <= max_flip_frac, f"{frac:.4f} of codes differ by one step"
     return eq, frac
+
+
+def oracle_quantize_experts_mx(w_bf16):
+    """Oracle MXFP4 quantisation of bf16 expert weights [E, N, K] (CPU tensor)."""
+    ps, ss = [], []
+    for e in range(w_bf16.shape[0]):
+        p, s = O.quantize_mxfp4(w_bf16[e].float().numpy())
+        ps.append(p), ss.append(s)
+    return np.stack(ps), np.stack(ss)
 
 
 def oracle_quantize_experts(w_bf16):
@@ -86,7 +97,7 @@ def oracle_quantize_experts(w_bf16):
     return np.stack(ps), np.stack(ss), np.array(gs, np.float32)
 
 
-def check_permutation(out, idx, E, xq, xs):
+def check_permutation(out, idx, E, xq, xs, block=16):
     """A Permutation (CUDA) against the oracle's stable expert-first order
     of `idx` [T, k], with the gathered packed rows `xq` and row-major scales
     `xs` of the tokens: counts, offsets, 128-aligned row offsets, both maps,
@@ -114,5 +125,5 @@ def check_permutation(out, idx, E, xq, xs):
     np.testing.assert_array_equal(g_f2p - roff[e_of] + offsets[e_of], f2p)
     a = out.a_packed.cpu().numpy()
     np.testing.assert_array_equal(a[g_f2p], xq[np.arange(T * k) // k])
-    sc = from_blocked(out.a_scales.cpu().numpy(), cap, H)
+    sc = from_blocked(out.a_scales.cpu().numpy(), cap, H, block)
     np.testing.assert_array_equal(sc[g_f2p], xs[np.arange(T * k) // k])
