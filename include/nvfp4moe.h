@@ -122,10 +122,9 @@ int moe_route_topk(const float* logits, const float* bias, int T, int E, int k,
                    int32_t* topk_idx, float* topk_w, cudaStream_t stream);
 
 /* Batch-aware ("opportunistic") expert routing (page A, Introduction, key
- * finding 6 and section 6: batch-aware routing skips the experts a token
- * would use with low probability at decode time and reuses the experts the
- * batch activates anyway, so fewer experts' weights are streamed; the pages
- * give no algorithm).  This library's reading:
+ * finding 6 and section 6: during decode a token trades the experts it
+ * weights least for experts other tokens of the batch use already, so
+ * fewer experts' weights are streamed; the pages give no algorithm).  This library's reading:
  *   1. each token's primary experts are its top-k_primary by logit + bias
  *      (order and ties as moe_route_topk);
  *   2. the batch's active set S is the union of all tokens' primary experts;

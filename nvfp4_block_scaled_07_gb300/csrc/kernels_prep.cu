@@ -36,9 +36,9 @@ __device__ __forceinline__ double warp_sum(double v) {
 // lane l holds experts l, l+32, ...; k rounds of a warp arg-max with the
 // lower expert index winning ties.
 //
-// Batch-aware routing (same page, key finding 6 and section 6: skip the
-// low-probability experts at decode time by reusing the experts the batch
-// activates anyway).  Pass 1 marks every token's top-k_primary experts in
+// Batch-aware routing (same page, key finding 6 and section 6: during
+// decode a token gives up the experts it weights least in favour of experts
+// other tokens of the batch already use).  Pass 1 marks every token's top-k_primary experts in
 // a bit set S; pass 2 ranks each token's experts with members of S first
 // (then value, then index) and takes k of them.  Plain top-k is pass 2 with
 // every expert a member.

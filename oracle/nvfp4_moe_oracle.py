@@ -39,17 +39,18 @@ below names the readings it uses:
       h = silu(gate) * up with no clamp; h is rounded to float32 before
       requantisation; the down projection output and the layer output are
       rounded to bfloat16; the finalize sum runs in slot order.
+  R8  batch-aware routing (the pages name the technique -- at decode, a token
+      trades its least-weighted experts for experts the batch already uses --
+      but give no algorithm): every token keeps its top
+      k_primary experts; the union of those over the batch is the active
+      set S; each token's k experts are its best within S (then, only if S
+      has fewer than k experts, its best outside S); see route_batch_aware.
   R9  MXFP4 (the pages name an MXFP4 grouped GEMM and nothing more; the
       format is the OCP microscaling one): E2M1 values, one E8M0 scale
       2**X per 32 elements along K, X = floor(log2(block amax)) - 2 clamped
       to [-127, 127] (-127 for an all-zero block), codes by reading R3 on
       x / 2**X, no per-tensor scale; the layer's SwiGLU output is
       requantised the same way.
-  R8  batch-aware routing (the pages name it, "skip low-probability experts
-      at decode time", without an algorithm): every token keeps its top
-      k_primary experts; the union of those over the batch is the active
-      set S; each token's k experts are its best within S (then, only if S
-      has fewer than k experts, its best outside S); see route_batch_aware.
 
 Precision: values are decoded exactly to float64, GEMMs accumulate in float64
 (numpy matmul on exactly dequantised operands), the few steps that must
@@ -327,10 +328,10 @@ def route_batch_aware(logits, bias, k, k_primary, score_fn, renormalize=True):
     """Batch-aware ("opportunistic") expert routing, reading R8.
 
     "SM120 FP4 Kernel Research Campaign" (Introduction; key finding 6; section
-    6, batch-aware routing) names the technique -- at decode time, skip the
-    low-probability experts a token would activate on its own and reuse the
-    experts the batch activates anyway, so that fewer experts' weights are
-    streamed -- but gives no algorithm.  Reading R8, step by step:
+    6, batch-aware routing) names the technique -- during decode a token
+    trades the experts it weights least for experts other tokens of the
+    batch use already, so fewer experts' weights are streamed -- but gives
+    no algorithm.  Reading R8, step by step:
       1. each token's primary experts are its top-k_primary by
          v = logit + bias (order and ties as in route_topk);
       2. the batch's active set S is the union of every token's primary
