@@ -178,11 +178,12 @@ def step_with_kernel_events(B, layer, x, logits, ev):
         ev[i].record()
         B.moe_grouped_gemm_mxfp4(p.a_packed, p.a_scales, p.counts, p.row_offsets, layer.w_gu_packed,
                                  layer.w_gu_scales, B.EPI_SWIGLU_MXFP4, m_total=T * layer.k, tile_n=layer.tile_n[0],
-                                 out=layer.hq, out_scales=layer.hs)
+                                 out=layer.hq, out_scales=layer.hs, workspace=layer.g_ws)
         i += 1
         ev[i].record()
         B.moe_grouped_gemm_mxfp4(layer.hq, layer.hs, p.counts, p.row_offsets, layer.w_d_packed, layer.w_d_scales,
-                                 B.EPI_BF16, m_total=T * layer.k, tile_n=layer.tile_n[1], out=layer.y)
+                                 B.EPI_BF16, m_total=T * layer.k, tile_n=layer.tile_n[1], out=layer.y,
+                                 workspace=layer.g_ws)
         i += 1
         ev[i].record()
         B.moe_finalize(layer.y, p.flat_to_perm, layer.topk_w, out=layer.out)
@@ -213,12 +214,13 @@ def step_with_kernel_events(B, layer, x, logits, ev):
         ev[i].record()
     B.moe_grouped_gemm_nvfp4(p.a_packed, p.a_scales, layer.x_gscale, p.counts, p.row_offsets, layer.w_gu_packed,
                              layer.w_gu_scales, layer.w_gu_gscale, B.EPI_SWIGLU_NVFP4, c_gscale=layer.h_scale,
-                             m_total=T * layer.k, tile_n=layer.tile_n[0], out=layer.hq, out_scales=layer.hs)
+                             m_total=T * layer.k, tile_n=layer.tile_n[0], out=layer.hq, out_scales=layer.hs,
+                             workspace=layer.g_ws)
     i += 1
     ev[i].record()
     B.moe_grouped_gemm_nvfp4(layer.hq, layer.hs, layer.h_scale, p.counts, p.row_offsets, layer.w_d_packed,
                              layer.w_d_scales, layer.w_d_gscale, B.EPI_BF16, m_total=T * layer.k,
-                             tile_n=layer.tile_n[1], out=layer.y)
+                             tile_n=layer.tile_n[1], out=layer.y, workspace=layer.g_ws)
     i += 1
     ev[i].record()
     B.moe_finalize(layer.y, p.flat_to_perm, layer.topk_w, out=layer.out)
@@ -239,7 +241,7 @@ def run_ours(args, w):
     inp = W.device_inputs(w, seed=args.seed + rank, device=dev)
     layer = B.MoELayer(inp["w_gu"], inp["w_d"], w.k, w.score, w.renormalize, w.h_scale, bias=inp["bias"],
                        T=w.T, tile_n=(args.tile_gate_up, args.tile_down), fused_prepare=not args.separate_prepare,
-                       k_primary=args.k_primary, fmt=args.format)
+                       k_primary=args.k_primary, fmt=args.format, dynamic_schedule=not args.static_schedule)
     del inp["w_gu"], inp["w_d"]
     torch.cuda.empty_cache()
     x, logits = inp["x"], inp["logits"]
@@ -337,6 +339,7 @@ def run_ours(args, w):
         "ms_per_step_with_events": round(ms_step_events, 4),
         "prepare": "fused (one launch)" if layer.fused_prepare else "separate (route, quantise, permute)",
         "routing": "top-k" if layer.k_primary == w.k else f"batch-aware, k_primary={layer.k_primary}",
+        "gemm_schedule": "dynamic" if layer.g_ws is not None else "static",
         "roofline": {"kernel": "gemm_gate_up_swiglu", "bound": bound, "achieved": round(achieved, 1),
                      "peak": round(peak, 1), "unit": unit, "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic(w.name, "gemm_gate_up_swiglu") if layer.fmt == "nvfp4" else None,
@@ -501,6 +504,8 @@ def main():
                     help="batch-aware routing: experts each token keeps by its own scores (default k: plain top-k)")
     ap.add_argument("--format", choices=["nvfp4", "mxfp4"], default="nvfp4",
                     help="operand format of the layer (mxfp4: E8M0 scale per 32 elements, no per-tensor scales)")
+    ap.add_argument("--static-schedule", action="store_true",
+                    help="grouped GEMMs on static tile stripes instead of the dynamic tile counter")
     ap.add_argument("--separate-prepare", action="store_true",
                     help="route, quantise and permute as separate calls instead of moe_prepare")
     args = ap.parse_args()

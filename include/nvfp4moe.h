@@ -290,7 +290,13 @@ int moe_prepare(const float* logits, const float* bias, const void* x_bf16,
  * device's opt-in shared memory is refused with NVFP4MOE_ERR_SMEM (the
  * message gives the bytes required and the limit, cf. the OutOfResources
  * failure quoted on page A, section "The Research Task").
- * No workspace is used; ws may be NULL. */
+ * ws: NULL, or a device workspace of moe_grouped_gemm_nvfp4_workspace_size()
+ * bytes (256), 256-byte aligned and ZERO-FILLED before its first use.  With a
+ * workspace the persistent CTAs claim tiles from a launch-wide counter
+ * (dynamic schedule: faster SMs take more tiles); the last CTA to finish
+ * leaves the workspace zeroed for the next call, also after a timeout.
+ * Without one, CTA c takes tiles c, c + #SMs, ...  Results are identical
+ * either way.  Calls sharing a workspace must not overlap on the GPU. */
 size_t moe_grouped_gemm_nvfp4_workspace_size(int E, int N, int K, int epilogue);
 int moe_grouped_gemm_nvfp4(const uint8_t* a_packed, const uint8_t* a_scales, const float* a_gscale,
                            const int32_t* expert_counts, const int32_t* row_offsets,
@@ -327,7 +333,8 @@ int moe_grouped_gemm_nvfp4(const uint8_t* a_packed, const uint8_t* a_scales, con
  *   nvfp4moe_mxfp4_blocked_scales_bytes(N, K)); K % 128 == 0; epilogues
  *   NVFP4MOE_EPI_BF16, NVFP4MOE_EPI_SWIGLU_MXFP4 (c_out packed [rows_capacity,
  *   I/2], c_scales blocked MXFP4 over rows_capacity rows with I columns,
- *   quantised as moe_quantize_mxfp4) or NVFP4MOE_EPI_SWIGLU_F32. */
+ *   quantised as moe_quantize_mxfp4) or NVFP4MOE_EPI_SWIGLU_F32; ws as for
+ *   moe_grouped_gemm_nvfp4. */
 int moe_quantize_mxfp4(const void* x_bf16, int64_t rows, int64_t cols, int flags,
                        uint8_t* packed, uint8_t* scales, cudaStream_t stream);
 int moe_permute_mxfp4(const int32_t* topk_idx, int T, int E, int k,
@@ -341,7 +348,7 @@ int moe_grouped_gemm_mxfp4(const uint8_t* a_packed, const uint8_t* a_scales,
                            int E, int64_t rows_capacity, int64_t m_total,
                            const uint8_t* w_packed, const uint8_t* w_scales,
                            int N, int K, int epilogue, void* c_out, uint8_t* c_scales, int tile_n,
-                           cudaStream_t stream);
+                           void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ---- a6: finalize ----------------------------------------------------------
  * Router-weighted reduce back to token order (page A, section 6: "token

@@ -44,7 +44,7 @@ _SIGS = {
     "nvfp4moe_mxfp4_blocked_scales_bytes": (_sz, [_i64, _i64]),
     "moe_quantize_mxfp4": (_i, [_p, _i64, _i64, _i, _p, _p, _p]),
     "moe_permute_mxfp4": (_i, [_p, _i, _i, _i, _p, _p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
-    "moe_grouped_gemm_mxfp4": (_i, [_p, _p, _p, _p, _i, _i64, _i64, _p, _p, _i, _i, _i, _p, _p, _i, _p]),
+    "moe_grouped_gemm_mxfp4": (_i, [_p, _p, _p, _p, _i, _i64, _i64, _p, _p, _i, _i, _i, _p, _p, _i, _p, _sz, _p]),
     "moe_route_topk": (_i, [_p, _p, _i, _i, _i, _i, _i, _p, _p, _p]),
     "moe_route_batch_aware_workspace_size": (_sz, [_i]),
     "moe_route_batch_aware": (_i, [_p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _sz, _p]),
@@ -392,9 +392,24 @@ def moe_prepare(logits, x, k, score_fn="sigmoid", renormalize=True, bias=None, t
 
 
 # ---- a4/a5 ---------------------------------------------------------------------
+def alloc_gemm_workspace(device):
+    """Zero-filled tile-scheduler workspace for the grouped GEMMs (dynamic schedule)."""
+    return torch.zeros((int(_lib.moe_grouped_gemm_nvfp4_workspace_size(1, 128, 64, EPI_BF16)),), dtype=torch.uint8,
+                       device=device)
+
+
+def _ws_args(workspace):
+    if workspace is None:
+        return None, 0
+    _need(workspace, torch.uint8, name="workspace")
+    return _ptr(workspace), workspace.numel()
+
+
 def moe_grouped_gemm_nvfp4(a_packed, a_scales, a_gscale, counts, row_offsets, w_packed, w_scales, w_gscale,
-                           epilogue=EPI_BF16, c_gscale=None, m_total=None, tile_n=0, out=None, out_scales=None):
-    """Returns c_out (and c_scales for EPI_SWIGLU_NVFP4)."""
+                           epilogue=EPI_BF16, c_gscale=None, m_total=None, tile_n=0, out=None, out_scales=None,
+                           workspace=None):
+    """Returns c_out (and c_scales for EPI_SWIGLU_NVFP4).  workspace: a zeroed
+    alloc_gemm_workspace() for the dynamic tile schedule, None for static."""
     E, N, Kh = w_packed.shape
     K = 2 * Kh
     cap = a_packed.shape[0]
@@ -430,16 +445,17 @@ def moe_grouped_gemm_nvfp4(a_packed, a_scales, a_gscale, counts, row_offsets, w_
         raise ValueError(f"epilogue {epilogue}")
     if m_total is None:
         m_total = cap
+    ws_p, ws_n = _ws_args(workspace)
     _check(_lib.moe_grouped_gemm_nvfp4(_ptr(a_packed), _ptr(a_scales), _ptr(a_gscale), _ptr(counts),
                                        _ptr(row_offsets), E, cap, int(m_total), _ptr(w_packed), _ptr(w_scales),
                                        _ptr(w_gscale), N, K, epilogue, _ptr(c_gscale), _ptr(out),
-                                       _ptr(out_scales), int(tile_n), None, 0, _stream()),
+                                       _ptr(out_scales), int(tile_n), ws_p, ws_n, _stream()),
            "moe_grouped_gemm_nvfp4")
     return (out, out_scales) if epilogue == EPI_SWIGLU_NVFP4 else out
 
 
 def moe_grouped_gemm_mxfp4(a_packed, a_scales, counts, row_offsets, w_packed, w_scales, epilogue=EPI_BF16,
-                           m_total=None, tile_n=0, out=None, out_scales=None):
+                           m_total=None, tile_n=0, out=None, out_scales=None, workspace=None):
     """MXFP4 grouped GEMM.  Returns c_out (and c_scales for EPI_SWIGLU_MXFP4)."""
     E, N, Kh = w_packed.shape
     K = 2 * Kh
@@ -471,9 +487,11 @@ def moe_grouped_gemm_mxfp4(a_packed, a_scales, counts, row_offsets, w_packed, w_
         raise ValueError(f"epilogue {epilogue}")
     if m_total is None:
         m_total = cap
+    ws_p, ws_n = _ws_args(workspace)
     _check(_lib.moe_grouped_gemm_mxfp4(_ptr(a_packed), _ptr(a_scales), _ptr(counts), _ptr(row_offsets), E, cap,
                                        int(m_total), _ptr(w_packed), _ptr(w_scales), N, K, epilogue, _ptr(out),
-                                       _ptr(out_scales), int(tile_n), _stream()), "moe_grouped_gemm_mxfp4")
+                                       _ptr(out_scales), int(tile_n), ws_p, ws_n, _stream()),
+           "moe_grouped_gemm_mxfp4")
     return (out, out_scales) if epilogue == EPI_SWIGLU_MXFP4 else out
 
 
@@ -504,10 +522,12 @@ class MoELayer:
     operands through the separate calls (eight launches)."""
 
     def __init__(self, w_gu, w_d, k, score_fn="sigmoid", renormalize=True, h_scale=2.0 ** -4, bias=None,
-                 T=None, tile_n=(0, 0), fused_prepare=True, k_primary=None, fmt="nvfp4"):
+                 T=None, tile_n=(0, 0), fused_prepare=True, k_primary=None, fmt="nvfp4", dynamic_schedule=True):
         if fmt not in ("nvfp4", "mxfp4"):
             raise ValueError(f"fmt {fmt}")
         self.fmt = fmt
+        # one zeroed tile-scheduler workspace for both GEMMs (they run in sequence)
+        self.g_ws = alloc_gemm_workspace(w_gu.device) if dynamic_schedule else None
         self.fused_prepare = bool(fused_prepare) and fmt == "nvfp4"
         # batch-aware routing when k_primary < k (moe_route_batch_aware)
         self.k_primary = k if k_primary is None else int(k_primary)
@@ -559,9 +579,10 @@ class MoELayer:
             moe_permute_mxfp4(self.topk_idx, self.E, self.xq, self.xs, out=p, workspace=self.p_ws)
             moe_grouped_gemm_mxfp4(p.a_packed, p.a_scales, p.counts, p.row_offsets, self.w_gu_packed,
                                    self.w_gu_scales, EPI_SWIGLU_MXFP4, m_total=T * self.k, tile_n=self.tile_n[0],
-                                   out=self.hq, out_scales=self.hs)
+                                   out=self.hq, out_scales=self.hs, workspace=self.g_ws)
             moe_grouped_gemm_mxfp4(self.hq, self.hs, p.counts, p.row_offsets, self.w_d_packed, self.w_d_scales,
-                                   EPI_BF16, m_total=T * self.k, tile_n=self.tile_n[1], out=self.y)
+                                   EPI_BF16, m_total=T * self.k, tile_n=self.tile_n[1], out=self.y,
+                                   workspace=self.g_ws)
             return moe_finalize(self.y, p.flat_to_perm, self.topk_w, out=self.out if out is None else out)
         if self.fused_prepare:
             moe_prepare(logits, x, self.k, self.score_fn, self.renormalize, self.bias, self.topk_idx, self.topk_w,
@@ -573,10 +594,11 @@ class MoELayer:
             moe_permute(self.topk_idx, self.E, self.xq, self.xs, out=p, workspace=self.p_ws)
         moe_grouped_gemm_nvfp4(p.a_packed, p.a_scales, self.x_gscale, p.counts, p.row_offsets, self.w_gu_packed,
                                self.w_gu_scales, self.w_gu_gscale, EPI_SWIGLU_NVFP4, c_gscale=self.h_scale,
-                               m_total=T * self.k, tile_n=self.tile_n[0], out=self.hq, out_scales=self.hs)
+                               m_total=T * self.k, tile_n=self.tile_n[0], out=self.hq, out_scales=self.hs,
+                               workspace=self.g_ws)
         moe_grouped_gemm_nvfp4(self.hq, self.hs, self.h_scale, p.counts, p.row_offsets, self.w_d_packed,
                                self.w_d_scales, self.w_d_gscale, EPI_BF16, m_total=T * self.k,
-                               tile_n=self.tile_n[1], out=self.y)
+                               tile_n=self.tile_n[1], out=self.y, workspace=self.g_ws)
         return moe_finalize(self.y, p.flat_to_perm, self.topk_w, out=self.out if out is None else out)
 
     __call__ = forward

@@ -400,15 +400,18 @@ size_t moe_grouped_gemm_nvfp4_workspace_size(int E, int N, int K, int epilogue) 
   (void)N;
   (void)K;
   (void)epilogue;
-  return 0;
+  return kGemmWorkspaceBytes;
 }
 
 static int grouped_gemm_common(bool mx, const uint8_t* a_packed, const uint8_t* a_scales, const float* a_gscale,
                                const int32_t* expert_counts, const int32_t* row_offsets, int E, int64_t rows_capacity,
                                int64_t m_total, const uint8_t* w_packed, const uint8_t* w_scales,
                                const float* w_gscale, int N, int K, int epilogue, const float* c_gscale, void* c_out,
-                               uint8_t* c_scales, int tile_n, cudaStream_t stream) {
+                               uint8_t* c_scales, int tile_n, void* ws, size_t ws_bytes, cudaStream_t stream) {
   t_detail[0] = 0;
+  NVFP4MOE_REQUIRE(!ws || (ws_bytes >= kGemmWorkspaceBytes && (reinterpret_cast<uintptr_t>(ws) & 255) == 0),
+                   NVFP4MOE_ERR_WORKSPACE, "workspace must be NULL or %zu bytes, 256-byte aligned (got %zu)",
+                   kGemmWorkspaceBytes, ws_bytes);
   const int requant = mx ? NVFP4MOE_EPI_SWIGLU_MXFP4 : NVFP4MOE_EPI_SWIGLU_NVFP4;
   NVFP4MOE_REQUIRE(epilogue == NVFP4MOE_EPI_BF16 || epilogue == requant || epilogue == NVFP4MOE_EPI_SWIGLU_F32,
                    NVFP4MOE_ERR_INVALID_ARG, "epilogue %d", epilogue);
@@ -458,6 +461,7 @@ static int grouped_gemm_common(bool mx, const uint8_t* a_packed, const uint8_t* 
   a.c_scales = c_scales;
   a.tile_n = tile_n;
   a.mx = mx;
+  a.sched = ws;
   return launch_grouped_gemm(a, d.num_sms, d.smem_optin, stream);  // detail already set on failure
 }
 
@@ -466,19 +470,18 @@ int moe_grouped_gemm_nvfp4(const uint8_t* a_packed, const uint8_t* a_scales, con
                            int64_t m_total, const uint8_t* w_packed, const uint8_t* w_scales,
                            const float* w_gscale, int N, int K, int epilogue, const float* c_gscale, void* c_out,
                            uint8_t* c_scales, int tile_n, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
   return grouped_gemm_common(false, a_packed, a_scales, a_gscale, expert_counts, row_offsets, E, rows_capacity,
                              m_total, w_packed, w_scales, w_gscale, N, K, epilogue, c_gscale, c_out, c_scales, tile_n,
-                             stream);
+                             ws, ws_bytes, stream);
 }
 
 int moe_grouped_gemm_mxfp4(const uint8_t* a_packed, const uint8_t* a_scales, const int32_t* expert_counts,
                            const int32_t* row_offsets, int E, int64_t rows_capacity, int64_t m_total,
                            const uint8_t* w_packed, const uint8_t* w_scales, int N, int K, int epilogue, void* c_out,
-                           uint8_t* c_scales, int tile_n, cudaStream_t stream) {
+                           uint8_t* c_scales, int tile_n, void* ws, size_t ws_bytes, cudaStream_t stream) {
   return grouped_gemm_common(true, a_packed, a_scales, nullptr, expert_counts, row_offsets, E, rows_capacity, m_total,
-                             w_packed, w_scales, nullptr, N, K, epilogue, nullptr, c_out, c_scales, tile_n, stream);
+                             w_packed, w_scales, nullptr, N, K, epilogue, nullptr, c_out, c_scales, tile_n, ws,
+                             ws_bytes, stream);
 }
 
 // ---- a6 ---------------------------------------------------------------------

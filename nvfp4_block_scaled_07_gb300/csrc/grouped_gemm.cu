@@ -70,7 +70,11 @@ constexpr int kSfRingCols = 256;
 constexpr int kMaxSfSlots = 8;
 constexpr int kMaxStages = 16;
 // mbarriers: full/empty per stage, acc full/empty per slot, drain, sf full/empty per ring slot
-constexpr int kNumBars = 2 * kMaxStages + 5 + 2 * kMaxSfSlots;
+// Ring of claimed tile ids (dynamic schedule): the producer claims ids from
+// a launch-wide counter and passes them to the other roles.
+constexpr int kTileRing = 32;
+__host__ __device__ constexpr int tile_consumers(bool swiglu) { return 1 + 4 + epi_warps(swiglu); }  // MMA, SF and epilogue warps
+constexpr int kNumBars = 2 * kMaxStages + 5 + 2 * kMaxSfSlots + 2 * kTileRing;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
@@ -87,6 +91,7 @@ struct Params {
   int E, N, K, epi;
   int smem_bytes;   // dynamic shared memory of the launch (after 1024-byte alignment slack)
   int stage_cap;    // most pipeline stages to use (2..kMaxStages)
+  uint32_t* sched;  // [0] tile counter, [32] finished CTAs (zero between launches); null: static stripes
   int64_t rows_cap;
 };
 
@@ -113,7 +118,7 @@ struct Cfg {
 // address, flags and the per-expert tile scan; stages start after it on a
 // 1024-byte boundary.
 __host__ __device__ constexpr int ctrl_bytes(int E) {
-  return (kNumBars * 8 + 16 + (3 * E + 1) * 4 + 1023) / 1024 * 1024;
+  return (kNumBars * 8 + 16 + kTileRing * 4 + (3 * E + 1) * 4 + 1023) / 1024 * 1024;
 }
 
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -290,7 +295,8 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_wmax = reinterpret_cast<int*>(tmem_slot + 2);
-  int* s_prefix = reinterpret_cast<int*>(tmem_slot + 4);
+  volatile int* s_tq = reinterpret_cast<volatile int*>(tmem_slot + 4);   // claimed tile ids
+  int* s_prefix = reinterpret_cast<int*>(tmem_slot + 4 + kTileRing);
   int* s_count = s_prefix + p.E + 1;
   int* s_rowoff = s_count + p.E;
   const int ctrl = ctrl_bytes(p.E);
@@ -305,6 +311,10 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   const uint32_t drain_bar = bar0 + 8u * uint32_t(2 * kMaxStages + 4);
   auto sff_bar = [&](uint32_t r) { return bar0 + 8u * (uint32_t(2 * kMaxStages + 5) + r); };
   auto sfe_bar = [&](uint32_t r) { return bar0 + 8u * (uint32_t(2 * kMaxStages + 5 + kMaxSfSlots) + r); };
+  auto tqf_bar = [&](uint32_t q) { return bar0 + 8u * (uint32_t(2 * kMaxStages + 5 + 2 * kMaxSfSlots) + q); };
+  auto tqe_bar = [&](uint32_t q) {
+    return bar0 + 8u * (uint32_t(2 * kMaxStages + 5 + 2 * kMaxSfSlots + kTileRing) + q);
+  };
 
   const int MT = SWIGLU ? p.N / 2 / kBM : p.N / (kBM * NA);  // M tiles per expert
   if (threadIdx.x == 0) {
@@ -320,6 +330,10 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     for (int r = 0; r < kMaxSfSlots; ++r) {
       ptx::mbar_init(sff_bar(r), 4);  // one arrival per scale-factor warp
       ptx::mbar_init(sfe_bar(r), 1);  // MMA completion
+    }
+    for (int q = 0; q < kTileRing; ++q) {
+      ptx::mbar_init(tqf_bar(q), 1);
+      ptx::mbar_init(tqe_bar(q), tile_consumers(SWIGLU));
     }
     *abort_flag = 0;
     ptx::fence_barrier_init();
@@ -392,13 +406,46 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   const int S = min(p.stage_cap, (p.smem_bytes - ctrl) / stage);
   const uint32_t smem_base = ptx::smem_u32(smem) + uint32_t(ctrl);
 
+  // The i-th tile of this CTA: the static stripe blockIdx.x + i * gridDim.x,
+  // or (dynamic schedule) the i-th id the producer claimed, read from the
+  // ring; lane 0 of a warp role reads it and releases the slot.  Returns -1
+  // if the wait was abandoned.
+  auto next_tile = [&](uint32_t i, bool whole_warp) -> int {
+    if (!p.sched) return int(blockIdx.x + i * gridDim.x);
+    const uint32_t q = i % uint32_t(kTileRing), ph = (i / uint32_t(kTileRing)) & 1u;
+    int t = -1;
+    if (!whole_warp || lane == 0) {
+      if (wait_phase(tqf_bar(q), ph, abort_flag)) {
+        t = s_tq[q];
+        ptx::mbar_arrive(tqe_bar(q));
+      }
+    }
+    if (whole_warp) t = __shfl_sync(kFull, t, 0);
+    return t;
+  };
+
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
     const uint64_t pol_w = ptx::policy_evict_first();  // weights stream through once
     const uint64_t pol_a = ptx::policy_evict_last();   // token tiles are re-read by every M tile
     uint32_t it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+    // Dynamic schedule: the next id is claimed one tile ahead, so the atomic's
+    // latency overlaps the current tile's copies.
+    int next = p.sched ? int(atomicAdd(p.sched, 1u)) : int(blockIdx.x);
+    for (uint32_t i = 0; ok; ++i) {
+      const int t = next;
+      if (p.sched) {
+        const uint32_t q = i % uint32_t(kTileRing), ph = (i / uint32_t(kTileRing)) & 1u;
+        if (!wait_phase(tqe_bar(q), ph ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        s_tq[q] = t;
+        ptx::mbar_arrive(tqf_bar(q));
+      }
+      if (t >= total) break;
+      next = p.sched ? int(atomicAdd(p.sched, 1u)) : t + int(gridDim.x);
       int e, mb, nb, w;
       decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
       const int arow = s_rowoff[e] + nb * BN;
@@ -446,7 +493,9 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     uint32_t it = 0;
     SlotSeq slots;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+    for (uint32_t i = 0; ok; ++i) {
+      const int t = next_tile(i, false);
+      if (t < 0 || t >= total) break;
       int e, mb, nb, w;
       decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
       int s0, s1;
@@ -512,7 +561,9 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     // otherwise serialise with the MMAs of the previous stage.
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
     uint32_t it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (uint32_t i = 0;; ++i) {
+      const int t = next_tile(i, true);
+      if (t < 0 || t >= total) break;
       int e, mb, nb, w;
       decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
       const int sfb_chunks = w > 128 ? 2 : 1;
@@ -579,7 +630,9 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     const float s_h = (SWIGLU && !f32_out && !MX) ? *p.c_gscale : 1.0f;
     const int n_out = SWIGLU ? p.N / 2 : p.N;
     SlotSeq slots;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (uint32_t i = 0;; ++i) {
+      const int t = next_tile(i, true);
+      if (t < 0 || t >= total) break;
       int e, mb, nb, w;
       decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
       int s0, s1;
@@ -651,6 +704,15 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     __syncwarp();
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+  // Dynamic schedule: the last CTA to finish (every producer has stopped
+  // claiming by then) leaves both counters at zero for the next launch.
+  if (p.sched && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.sched + 32, 1u) == gridDim.x - 1) {
+      atomicExch(p.sched, 0u);
+      atomicExch(p.sched + 32, 0u);
+    }
   }
 }
 
@@ -740,6 +802,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   p.smem_bytes = int(smem) - 1024;
   p.stage_cap = stage_cap_from_env();
   p.rows_cap = a.rows_capacity;
+  p.sched = static_cast<uint32_t*>(a.sched);
   // Launched without programmatic dependent launch: measured on GB300, a
   // grouped GEMM launched with it streamed its weight tiles about 2.5%
   // slower per tile, more than the few microseconds of launch latency it

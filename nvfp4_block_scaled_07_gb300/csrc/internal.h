@@ -97,7 +97,10 @@ struct GemmArgs {
   uint8_t* c_scales;
   int tile_n;
   bool mx;  // MXFP4 operands (ue8m0 scale per 32 elements, no per-tensor scales)
+  void* sched;  // zero-filled 256-byte tile-scheduler workspace, or null for the static schedule
 };
+
+constexpr size_t kGemmWorkspaceBytes = 256;
 
 // Returns 0 on success or an NVFP4MOE_ERR_* code (message via set_error_detail).
 int launch_grouped_gemm(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st);

@@ -270,3 +270,33 @@ def test_grouped_gemm_swiglu(B, E, I, K, counts, tile_n):
     codes = O.unpack_codes(hq.cpu().numpy()[pos])
     scales = U.from_blocked(hs.cpu().numpy(), cap, I)[pos]
     U.check_requant(codes, scales, O.unpack_codes(rq), rs)
+
+
+@pytest.mark.parametrize("E,N,K,counts,tile_n", GEMM_SHAPES[:4])
+def test_grouped_gemm_dynamic_schedule_matches_static(B, E, N, K, counts, tile_n):
+    """Tiles claimed from the launch-wide counter give the same bits as the
+    static stripes (each tile's arithmetic does not depend on its CTA), and
+    the workspace is left zeroed for the next call."""
+    g, ref, pos, R = gemm_case(E, N, K, counts, seed=E * 55 + K)
+    args = (g["a_packed"], g["a_scales"], g["a_gscale"], g["counts"], g["row_offsets"], g["w_packed"],
+            g["w_scales"], g["w_gscale"])
+    ws = B.alloc_gemm_workspace(torch.device("cuda"))
+    static = B.moe_grouped_gemm_nvfp4(*args, B.EPI_BF16, m_total=R, tile_n=tile_n)
+    for _ in range(3):
+        dyn = B.moe_grouped_gemm_nvfp4(*args, B.EPI_BF16, m_total=R, tile_n=tile_n, workspace=ws)
+        B.sync_status()
+        assert not ws.any().item()
+        assert torch.equal(dyn[torch.from_numpy(pos).cuda()], static[torch.from_numpy(pos).cuda()])
+    I = N // 2
+    if N % 256 == 0:
+        hq0, hs0 = B.moe_grouped_gemm_nvfp4(*args, B.EPI_SWIGLU_NVFP4, c_gscale=dev(torch.tensor([2.0 ** -4])),
+                                            m_total=R)
+        hq1, hs1 = B.moe_grouped_gemm_nvfp4(*args, B.EPI_SWIGLU_NVFP4, c_gscale=dev(torch.tensor([2.0 ** -4])),
+                                            m_total=R, workspace=ws)
+        B.sync_status()
+        rows = torch.from_numpy(pos).cuda()
+        assert torch.equal(hq0[rows], hq1[rows])
+        cap = hq0.shape[0]
+        np.testing.assert_array_equal(U.from_blocked(hs0.cpu().numpy(), cap, I)[pos],
+                                      U.from_blocked(hs1.cpu().numpy(), cap, I)[pos])
+        assert not ws.any().item()

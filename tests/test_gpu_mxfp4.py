@@ -166,3 +166,15 @@ def test_layer_mx_matches_oracle(B, w):
                     block=32)
     U.check_close(layer.y.float().cpu().numpy()[pos], it["y"], what="MXFP4 down projection")
     U.check_close(out, ref, what="MXFP4 layer output")
+
+
+def test_grouped_gemm_mx_dynamic_schedule(B):
+    g, ref, pos, R = gemm_case_mx(4, 256, 512, [3, 300, 0, 77], seed=9)
+    args = (g["a_packed"], g["a_scales"], g["counts"], g["row_offsets"], g["w_packed"], g["w_scales"])
+    ws = B.alloc_gemm_workspace(torch.device("cuda"))
+    a = B.moe_grouped_gemm_mxfp4(*args, B.EPI_BF16, m_total=R)
+    b = B.moe_grouped_gemm_mxfp4(*args, B.EPI_BF16, m_total=R, workspace=ws)
+    B.sync_status()
+    rows = torch.from_numpy(pos).cuda()
+    assert torch.equal(a[rows], b[rows]) and not ws.any().item()
+    U.check_close(b.float().cpu().numpy()[pos], O.round_to_bf16(ref), what="MXFP4 GEMM, dynamic schedule")
