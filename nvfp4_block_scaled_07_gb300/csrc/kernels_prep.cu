@@ -527,43 +527,53 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(const int32_t* __res
   for (int64_t p = int64_t(tail_start) + threadIdx.x; p < rows_capacity; p += blockDim.x) perm_to_flat[p] = -1;
 }
 
-// Flat id f (token f / k, slot f % k): its row in the expert-padded layout,
-// both maps, and a copy of the token's packed row and scales.
+// Placement of up to 32 flat ids by one warp: lane l takes f = f0 + l * step
+// (token f / k, slot f % k), finds its row in the expert-padded layout and
+// writes both maps; then the warp copies each of those tokens' packed row
+// and scales, all of a row's 16-byte chunks in flight at once.  The
+// metadata loads of the 32 ids overlap, so a row costs one round trip.
 // sf_groups = 4-byte scale groups per row: H/64 for NVFP4, H/128 for MXFP4.
-__device__ __forceinline__ void place_flat(int64_t f, const int32_t* idx, int k, int E, int seg_len,
-                                           const int32_t* rank, const int32_t* seg_base, const int32_t* row_offsets,
-                                           const uint8_t* xq, const uint8_t* xs, int H, int sf_groups,
-                                           int32_t* __restrict__ perm_to_flat, int32_t* __restrict__ flat_to_perm,
-                                           uint8_t* __restrict__ a_packed, uint8_t* __restrict__ a_scales,
-                                           int lane) {
-  const int e = __ldcg(idx + f);
-  if (e < 0 || e >= E) return;  // flagged by the rank step
-  const int64_t seg = f / seg_len;
-  const int64_t row = int64_t(__ldcg(row_offsets + e)) + __ldcg(seg_base + seg * E + e) + __ldcg(rank + f);
-  if (lane == 0) {
-    perm_to_flat[row] = int32_t(f);
-    flat_to_perm[f] = int32_t(row);
+__device__ __forceinline__ void place_rows(int64_t f0, int64_t step, int64_t R, const int32_t* idx, int k, int E,
+                                           int seg_len, const int32_t* rank, const int32_t* seg_base,
+                                           const int32_t* row_offsets, const uint8_t* xq, const uint8_t* xs, int H,
+                                           int sf_groups, int32_t* __restrict__ perm_to_flat,
+                                           int32_t* __restrict__ flat_to_perm, uint8_t* __restrict__ a_packed,
+                                           uint8_t* __restrict__ a_scales, int lane) {
+  const int64_t f = f0 + int64_t(lane) * step;
+  int64_t row = -1;
+  if (f < R) {
+    const int e = __ldcg(idx + f);
+    if (e >= 0 && e < E) {  // an id out of range is flagged by the rank step
+      const int r = __ldcg(rank + f);
+      row = int64_t(__ldcg(row_offsets + e)) + __ldcg(seg_base + (f / seg_len) * E + e) + r;
+      perm_to_flat[row] = int32_t(f);
+      flat_to_perm[f] = int32_t(row);
+    }
   }
-  const int64_t t = f / k;
-  const uint4* src = reinterpret_cast<const uint4*>(xq + t * (H / 2));
-  uint4* dst = reinterpret_cast<uint4*>(a_packed + row * (H / 2));
   const int nv = H / 32;  // 16-byte chunks of one packed row
-  for (int c0 = 0; c0 < nv; c0 += 128) {
-    uint4 v[4];
+  for (int j = 0; j < 32; ++j) {
+    const int64_t rj = __shfl_sync(kFull, row, j);
+    if (rj < 0) continue;  // uniform across the warp
+    const int64_t t = (f0 + int64_t(j) * step) / k;
+    const uint4* src = reinterpret_cast<const uint4*>(xq + t * (H / 2));
+    uint4* dst = reinterpret_cast<uint4*>(a_packed + rj * (H / 2));
+    for (int c0 = 0; c0 < nv; c0 += 256) {
+      uint4 v[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = c0 + 32 * j + lane;
-      if (c < nv) v[j] = __ldcg(src + c);
-    }
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + 32 * u + lane;
+        if (c < nv) v[u] = __ldcg(src + c);
+      }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = c0 + 32 * j + lane;
-      if (c < nv) dst[c] = v[j];
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + 32 * u + lane;
+        if (c < nv) dst[c] = v[u];
+      }
     }
+    const unsigned* ssrc = reinterpret_cast<const unsigned*>(xs + t * (4 * int64_t(sf_groups)));
+    for (int kb = lane; kb < sf_groups; kb += 32)
+      *reinterpret_cast<uint32_t*>(a_scales + blocked_sf_offset(rj, kb, sf_groups)) = __ldcg(ssrc + kb);
   }
-  const unsigned* ssrc = reinterpret_cast<const unsigned*>(xs + t * (4 * int64_t(sf_groups)));
-  for (int kb = lane; kb < sf_groups; kb += 32)
-    *reinterpret_cast<uint32_t*>(a_scales + blocked_sf_offset(row, kb, sf_groups)) = __ldcg(ssrc + kb);
 }
 
 __global__ void __launch_bounds__(256) permute_place_kernel(const int32_t* __restrict__ idx, int64_t R, int k, int E,
@@ -580,9 +590,10 @@ __global__ void __launch_bounds__(256) permute_place_kernel(const int32_t* __res
   ptx::grid_dep_launch();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
-  for (int64_t f = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); f < R; f += nwarps)
-    place_flat(f, idx, k, E, kPermuteSegment, rank, seg_base, row_offsets, xq, xs, H, sf_groups, perm_to_flat,
-               flat_to_perm, a_packed, a_scales, lane);
+  const int64_t w0 = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  for (int64_t f0 = w0; f0 < R; f0 += 32 * nwarps)
+    place_rows(f0, nwarps, R, idx, k, E, kPermuteSegment, rank, seg_base, row_offsets, xq, xs, H, sf_groups,
+               perm_to_flat, flat_to_perm, a_packed, a_scales, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -733,8 +744,22 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
   const float s = s_red[0];
   if (blockIdx.x == 0 && threadIdx.x == 0) *p.gscale = s;
   {
+    // two independent blocks per iteration: their four loads are in flight together
     const int64_t nblk = int64_t(p.T) * (p.H / 16);
-    for (int64_t b = tid; b < nblk; b += nthreads) {
+    int64_t b = tid;
+    for (; b + nthreads < nblk; b += 2 * nthreads) {
+      const int64_t b1 = b + nthreads;
+      const uint4 l0 = __ldg(p.x + 2 * b), h0 = __ldg(p.x + 2 * b + 1);
+      const uint4 l1 = __ldg(p.x + 2 * b1), h1 = __ldg(p.x + 2 * b1 + 1);
+      uint2 k0, k1;
+      const uint32_t s0 = nvfp4_block16(l0, h0, s, &k0);
+      const uint32_t s1 = nvfp4_block16(l1, h1, s, &k1);
+      *reinterpret_cast<uint2*>(p.xq + 8 * b) = k0;
+      *reinterpret_cast<uint2*>(p.xq + 8 * b1) = k1;
+      p.xs[b] = uint8_t(s0);
+      p.xs[b1] = uint8_t(s1);
+    }
+    if (b < nblk) {
       uint2 pk;
       const uint32_t sb = nvfp4_block16(__ldg(p.x + 2 * b), __ldg(p.x + 2 * b + 1), s, &pk);
       *reinterpret_cast<uint2*>(p.xq + 8 * b) = pk;
@@ -758,9 +783,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
     for (int r = c + lane; r < pad; r += 32) p.perm_to_flat[ro + r] = -1;
   }
   for (int64_t q = int64_t(__ldcg(p.row_offsets + p.E)) + tid; q < p.rows_cap; q += nthreads) p.perm_to_flat[q] = -1;
-  for (int64_t f = gw0; f < R; f += gw_stride)
-    place_flat(f, p.idx, p.k, p.E, ITERS * 32, p.rank, p.seg_base, p.row_offsets, p.xq, p.xs, p.H, p.H / 64,
-               p.perm_to_flat, p.flat_to_perm, p.a_packed, p.a_scales, lane);
+  for (int64_t f0 = gw0; f0 < R; f0 += 32 * gw_stride)
+    place_rows(f0, gw_stride, R, p.idx, p.k, p.E, ITERS * 32, p.rank, p.seg_base, p.row_offsets, p.xq, p.xs, p.H,
+               p.H / 64, p.perm_to_flat, p.flat_to_perm, p.a_packed, p.a_scales, lane);
 }
 
 // ---------------------------------------------------------------------------
