@@ -61,6 +61,18 @@ __device__ __forceinline__ uint32_t e2m1_code(float x, float d) {
   return e2m1_mag_code(fabsf(x) / d) | sign;
 }
 
+// Two E2M1 codes in one byte (lo in the low nibble) by the hardware
+// conversion: round to nearest E2M1 with ties to the even code, saturating
+// at +-6, the sign kept (so small negatives give -0, code 0x8) -- the same
+// rule as e2m1_mag_code plus the sign bit.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
 // ---- MXFP4: E2M1 with one E8M0 scale 2^X per 32 elements ----------------------
 // X = floor(log2(amax)) - 2 (2 = exponent of E2M1's largest value, 6 = 1.5 * 2^2),
 // clamped to [-127, 127]; an all-zero block takes X = -127.  floor(log2) is
@@ -82,6 +94,11 @@ __device__ __forceinline__ float mx_inv_step(int x) { return __uint_as_float(uin
 __device__ __forceinline__ uint32_t mx_code(float x, float inv_step) {
   const uint32_t sign = (__float_as_uint(x) >> 31) << 3;
   return e2m1_mag_code(fabsf(x) * inv_step) | sign;
+}
+
+// Two MXFP4 codes in one byte (x * 2^-X is exact, so the conversion rounds the true quotient).
+__device__ __forceinline__ uint32_t mx_code2(float lo, float hi, float inv_step) {
+  return e2m1x2(lo * inv_step, hi * inv_step);
 }
 
 }  // namespace nvfp4moe

@@ -223,23 +223,29 @@ __device__ __forceinline__ void requant_swiglu_chunk(const float (&h)[32], int l
   // lane l of a block now holds the amax of tokens 2(l % 16) and 2(l % 16) + 1
   const int t0 = 2 * (lane & 15);
   uint32_t sb[2];
-  float d[2];
+  float inv[2];  // 1 / step, 0 for a zero step (whose codes are all 0)
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     sb[k] = f32_to_ue4m3((a[k] / kE2M1Max) / s_h);
-    d[k] = ue4m3_to_f32(sb[k]) * s_h;
+    const float d = ue4m3_to_f32(sb[k]) * s_h;
+    inv[k] = d != 0.0f ? 1.0f / d : 0.0f;
   }
   const int fb = (f & ~31) + (lane & 16);        // first feature of this lane's block
 #pragma unroll
   for (int k = 0; k < 2; ++k)
     if (t0 + k < nvalid)
       out_scales[blocked_sf_offset(row0 + t0 + k, fb >> 6, n_out / 64) + ((fb >> 4) & 3)] = uint8_t(sb[k]);
+  // Codes: q = h * (1 / step) (within an ulp of h / step; the SwiGLU value is
+  // an accumulator result, so its codes are compared with the oracle's
+  // statistically) and the hardware conversion of the even/odd feature pair
+  // held by lanes 2i and 2i+1; four pairs make the 32-bit word of 8 features.
   uint8_t* row_ptr = out_codes + row0 * (n_out / 2) + (f & ~7) / 2;
 #pragma unroll
   for (int t = 0; t < 32; ++t) {
-    const float dt = __shfl_sync(kFull, d[t & 1], (lane & 16) + (t >> 1));
-    uint32_t word = e2m1_code(h[t], dt) << (4 * (lane & 7));
-    word |= __shfl_xor_sync(kFull, word, 1);
+    const float it = __shfl_sync(kFull, inv[t & 1], (lane & 16) + (t >> 1));
+    const float q = it != 0.0f ? h[t] * it : 0.0f;
+    const float qn = __shfl_xor_sync(kFull, q, 1);
+    uint32_t word = (lane & 1) ? 0u : e2m1x2(q, qn) << (8 * ((lane & 7) >> 1));
     word |= __shfl_xor_sync(kFull, word, 2);
     word |= __shfl_xor_sync(kFull, word, 4);
     if ((lane & 7) == 0 && t < nvalid) *reinterpret_cast<uint32_t*>(row_ptr + int64_t(t) * (n_out / 2)) = word;
@@ -275,9 +281,9 @@ __device__ __forceinline__ void requant_swiglu_chunk_mx(const float (&h)[32], in
   uint8_t* row_ptr = out_codes + row0 * (n_out / 2) + (f & ~7) / 2;
 #pragma unroll
   for (int t = 0; t < 32; ++t) {
-    const float it = __shfl_sync(kFull, inv, t);
-    uint32_t word = mx_code(h[t], it) << (4 * (lane & 7));
-    word |= __shfl_xor_sync(kFull, word, 1);
+    const float q = h[t] * __shfl_sync(kFull, inv, t);  // exact: 2^-X scaling
+    const float qn = __shfl_xor_sync(kFull, q, 1);
+    uint32_t word = (lane & 1) ? 0u : e2m1x2(q, qn) << (8 * ((lane & 7) >> 1));
     word |= __shfl_xor_sync(kFull, word, 2);
     word |= __shfl_xor_sync(kFull, word, 4);
     if ((lane & 7) == 0 && t < nvalid) *reinterpret_cast<uint32_t*>(row_ptr + int64_t(t) * (n_out / 2)) = word;
@@ -658,7 +664,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
           for (int i = 0; i < 32; ++i) {
             const float gf = __uint_as_float(g[i]) * scale;
             const float uf = __uint_as_float(u[i]) * scale;
-            h[i] = gf * __frcp_rn(1.0f + __expf(-gf)) * uf;
+            h[i] = gf * ptx::rcp_approx(1.0f + __expf(-gf)) * uf;
           }
           if (f32_out) {
             float* out = static_cast<float*>(p.c_out) + (row0 + c0) * n_out + f;

@@ -235,10 +235,13 @@ __device__ __forceinline__ uint32_t nvfp4_block16(uint4 lo, uint4 hi, float s, u
   const uint32_t sb = f32_to_ue4m3(t);
   const float d = ue4m3_to_f32(sb) * s;
   uint32_t p0 = 0, p1 = 0;
+  if (d != 0.0f) {  // a zero step gives code 0 for the whole block
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    p0 |= e2m1_code(f[j], d) << (4 * j);
-    p1 |= e2m1_code(f[8 + j], d) << (4 * j);
+    for (int j = 0; j < 4; ++j) {
+      // q = x / d exactly as a float32 division, then the nearest code
+      p0 |= e2m1x2(f[2 * j] / d, f[2 * j + 1] / d) << (8 * j);
+      p1 |= e2m1x2(f[8 + 2 * j] / d, f[8 + 2 * j + 1] / d) << (8 * j);
+    }
   }
   *packed = make_uint2(p0, p1);
   return sb;
@@ -347,10 +350,7 @@ __global__ void __launch_bounds__(256) quantize_mx_kernel(const uint4* __restric
         const uint32_t v[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
         uint32_t word = 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          word |= mx_code(bf16_lo(v[i]), inv) << (8 * i);
-          word |= mx_code(bf16_hi(v[i]), inv) << (8 * i + 4);
-        }
+        for (int i = 0; i < 4; ++i) word |= mx_code2(bf16_lo(v[i]), bf16_hi(v[i]), inv) << (8 * i);
         w[j] = word;
       }
       reinterpret_cast<uint4*>(packed)[b] = make_uint4(w[0], w[1], w[2], w[3]);
