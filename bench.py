@@ -167,15 +167,22 @@ def step_with_kernel_events(B, layer, x, logits, ev):
     i = 0
     ev[i].record()
     if layer.fmt == "mxfp4":
-        layer._route(logits)
-        i += 1
-        ev[i].record()
-        B.moe_quantize_mxfp4(x, packed=layer.xq, scales=layer.xs)
-        i += 1
-        ev[i].record()
-        B.moe_permute_mxfp4(layer.topk_idx, layer.E, layer.xq, layer.xs, out=p, workspace=layer.p_ws)
-        i += 1
-        ev[i].record()
+        if layer.fused_prepare:
+            B.moe_prepare_mxfp4(logits, x, layer.k, layer.score_fn, layer.renormalize, layer.bias, layer.topk_idx,
+                                layer.topk_w, layer.xq, layer.xs, out=p, workspace=layer.prep_ws,
+                                k_primary=layer.k_primary)
+            i += 1
+            ev[i].record()
+        else:
+            layer._route(logits)
+            i += 1
+            ev[i].record()
+            B.moe_quantize_mxfp4(x, packed=layer.xq, scales=layer.xs)
+            i += 1
+            ev[i].record()
+            B.moe_permute_mxfp4(layer.topk_idx, layer.E, layer.xq, layer.xs, out=p, workspace=layer.p_ws)
+            i += 1
+            ev[i].record()
         B.moe_grouped_gemm_mxfp4(p.a_packed, p.a_scales, p.counts, p.row_offsets, layer.w_gu_packed,
                                  layer.w_gu_scales, B.EPI_SWIGLU_MXFP4, m_total=T * layer.k, tile_n=layer.tile_n[0],
                                  out=layer.hq, out_scales=layer.hs, workspace=layer.g_ws)

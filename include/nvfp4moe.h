@@ -343,6 +343,18 @@ int moe_permute_mxfp4(const int32_t* topk_idx, int T, int E, int k,
                       int32_t* perm_to_flat, int32_t* flat_to_perm,
                       uint8_t* a_packed, uint8_t* a_scales,
                       void* ws, size_t ws_bytes, cudaStream_t stream);
+/* moe_prepare for the MXFP4 layer: route (as moe_prepare, k_primary
+ * included), quantise x by moe_quantize_mxfp4 (xq [T, H/2], row-major xs
+ * [T, H/32]; no global scale) and permute as moe_permute_mxfp4, in one
+ * cooperative launch.  H % 128 == 0; the workspace is
+ * moe_prepare_workspace_size(T, E, k), zero-filled once, as for moe_prepare. */
+int moe_prepare_mxfp4(const float* logits, const float* bias, const void* x_bf16,
+                      int T, int E, int k, int k_primary, int H, int score_fn, int renormalize,
+                      int32_t* topk_idx, float* topk_w, uint8_t* xq, uint8_t* xs,
+                      int32_t* expert_counts, int32_t* expert_offsets, int32_t* row_offsets,
+                      int32_t* perm_to_flat, int32_t* flat_to_perm,
+                      uint8_t* a_packed, uint8_t* a_scales,
+                      void* ws, size_t ws_bytes, cudaStream_t stream);
 int moe_grouped_gemm_mxfp4(const uint8_t* a_packed, const uint8_t* a_scales,
                            const int32_t* expert_counts, const int32_t* row_offsets,
                            int E, int64_t rows_capacity, int64_t m_total,

@@ -44,6 +44,8 @@ _SIGS = {
     "nvfp4moe_mxfp4_blocked_scales_bytes": (_sz, [_i64, _i64]),
     "moe_quantize_mxfp4": (_i, [_p, _i64, _i64, _i, _p, _p, _p]),
     "moe_permute_mxfp4": (_i, [_p, _i, _i, _i, _p, _p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
+    "moe_prepare_mxfp4": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p,
+                               _p, _sz, _p]),
     "moe_grouped_gemm_mxfp4": (_i, [_p, _p, _p, _p, _i, _i64, _i64, _p, _p, _i, _i, _i, _p, _p, _i, _p, _sz, _p]),
     "moe_route_topk": (_i, [_p, _p, _i, _i, _i, _i, _i, _p, _p, _p]),
     "moe_route_batch_aware_workspace_size": (_sz, [_i]),
@@ -391,6 +393,39 @@ def moe_prepare(logits, x, k, score_fn="sigmoid", renormalize=True, bias=None, t
     return topk_idx, topk_w, x_gscale, xq, xs, out
 
 
+def moe_prepare_mxfp4(logits, x, k, score_fn="sigmoid", renormalize=True, bias=None, topk_idx=None, topk_w=None,
+                      xq=None, xs=None, out: Permutation = None, workspace=None, k_primary=None):
+    """moe_prepare for MXFP4: returns (topk_idx, topk_w, xq, xs [T, H/32], Permutation)."""
+    k_primary = k if k_primary is None else int(k_primary)
+    _need(logits, torch.float32, name="logits")
+    _need(x, torch.bfloat16, name="x")
+    T, E = logits.shape
+    H = x.shape[1]
+    dev = x.device
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    topk_idx = _empty((T, k), torch.int32, dev) if topk_idx is None else topk_idx
+    topk_w = _empty((T, k), torch.float32, dev) if topk_w is None else topk_w
+    xq = _empty((T, H // 2), torch.uint8, dev) if xq is None else xq
+    xs = _empty((T, H // 32), torch.uint8, dev) if xs is None else xs
+    _need(topk_idx, torch.int32, (T, k), "topk_idx")
+    _need(topk_w, torch.float32, (T, k), "topk_w")
+    _need(xq, torch.uint8, (T, H // 2), "xq")
+    _need(xs, torch.uint8, (T, H // 32), "xs")
+    if out is None:
+        out = alloc_permutation(T, E, k, H, dev, "mxfp4")
+    if workspace is None:
+        workspace = alloc_prepare_workspace(T, E, k, dev)
+    _need(workspace, torch.uint8, name="workspace")
+    _check(_lib.moe_prepare_mxfp4(_ptr(logits), _ptr(bias), _ptr(x), T, E, k, k_primary, H, SCORE[score_fn],
+                                  int(bool(renormalize)), _ptr(topk_idx), _ptr(topk_w), _ptr(xq), _ptr(xs),
+                                  _ptr(out.counts), _ptr(out.offsets), _ptr(out.row_offsets), _ptr(out.perm_to_flat),
+                                  _ptr(out.flat_to_perm), _ptr(out.a_packed), _ptr(out.a_scales), _ptr(workspace),
+                                  workspace.numel(), _stream()),
+           "moe_prepare_mxfp4")
+    return topk_idx, topk_w, xq, xs, out
+
+
 # ---- a4/a5 ---------------------------------------------------------------------
 def alloc_gemm_workspace(device):
     """Zero-filled tile-scheduler workspace for the grouped GEMMs (dynamic schedule)."""
@@ -515,11 +550,10 @@ class MoELayer:
     """Quantised expert weights plus every buffer of one layer shape.
 
     forward() enqueues the layer on the current stream and allocates
-    nothing.  NVFP4 with fused_prepare (the default): four launches --
-    moe_prepare (route + quantise + permute), gate/up GEMM with SwiGLU and
-    requantisation, down GEMM, finalize -- otherwise the six separate calls
-    (nine launches and one memset).  fmt="mxfp4": the same layer on MXFP4
-    operands through the separate calls (eight launches)."""
+    nothing.  With fused_prepare (the default): four launches --
+    moe_prepare (route + quantise + permute; moe_prepare_mxfp4 for
+    fmt="mxfp4"), gate/up GEMM with SwiGLU and requantisation, down GEMM,
+    finalize -- otherwise the six separate calls."""
 
     def __init__(self, w_gu, w_d, k, score_fn="sigmoid", renormalize=True, h_scale=2.0 ** -4, bias=None,
                  T=None, tile_n=(0, 0), fused_prepare=True, k_primary=None, fmt="nvfp4", dynamic_schedule=True):
@@ -528,7 +562,7 @@ class MoELayer:
         self.fmt = fmt
         # one zeroed tile-scheduler workspace for both GEMMs (they run in sequence)
         self.g_ws = alloc_gemm_workspace(w_gu.device) if dynamic_schedule else None
-        self.fused_prepare = bool(fused_prepare) and fmt == "nvfp4"
+        self.fused_prepare = bool(fused_prepare)
         # batch-aware routing when k_primary < k (moe_route_batch_aware)
         self.k_primary = k if k_primary is None else int(k_primary)
         self.E, two_i, self.H = w_gu.shape
@@ -574,9 +608,13 @@ class MoELayer:
             self._alloc(T)
         p = self.perm
         if self.fmt == "mxfp4":
-            self._route(logits)
-            moe_quantize_mxfp4(x, packed=self.xq, scales=self.xs)
-            moe_permute_mxfp4(self.topk_idx, self.E, self.xq, self.xs, out=p, workspace=self.p_ws)
+            if self.fused_prepare:
+                moe_prepare_mxfp4(logits, x, self.k, self.score_fn, self.renormalize, self.bias, self.topk_idx,
+                                  self.topk_w, self.xq, self.xs, out=p, workspace=self.prep_ws, k_primary=self.k_primary)
+            else:
+                self._route(logits)
+                moe_quantize_mxfp4(x, packed=self.xq, scales=self.xs)
+                moe_permute_mxfp4(self.topk_idx, self.E, self.xq, self.xs, out=p, workspace=self.p_ws)
             moe_grouped_gemm_mxfp4(p.a_packed, p.a_scales, p.counts, p.row_offsets, self.w_gu_packed,
                                    self.w_gu_scales, EPI_SWIGLU_MXFP4, m_total=T * self.k, tile_n=self.tile_n[0],
                                    out=self.hq, out_scales=self.hs, workspace=self.g_ws)

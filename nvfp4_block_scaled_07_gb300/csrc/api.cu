@@ -357,22 +357,23 @@ size_t moe_prepare_workspace_size(int T, int E, int k) {
   return size_t(prepare_layout(T, E, k).bytes);
 }
 
-int moe_prepare(const float* logits, const float* bias, const void* x_bf16, int T, int E, int k, int k_primary,
-                int H, int score_fn, int renormalize, int32_t* topk_idx, float* topk_w, float* x_gscale, uint8_t* xq,
-                uint8_t* xs, int32_t* expert_counts, int32_t* expert_offsets, int32_t* row_offsets,
-                int32_t* perm_to_flat, int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales, void* ws,
-                size_t ws_bytes, cudaStream_t stream) {
+static int prepare_common(bool mx, const float* logits, const float* bias, const void* x_bf16, int T, int E, int k,
+                          int k_primary, int H, int score_fn, int renormalize, int32_t* topk_idx, float* topk_w,
+                          float* x_gscale, uint8_t* xq, uint8_t* xs, int32_t* expert_counts, int32_t* expert_offsets,
+                          int32_t* row_offsets, int32_t* perm_to_flat, int32_t* flat_to_perm, uint8_t* a_packed,
+                          uint8_t* a_scales, void* ws, size_t ws_bytes, cudaStream_t stream) {
   t_detail[0] = 0;
   NVFP4MOE_REQUIRE(T >= 0, NVFP4MOE_ERR_INVALID_ARG, "T = %d must be >= 0", T);
   NVFP4MOE_REQUIRE(E >= 1 && E <= 1024, NVFP4MOE_ERR_UNSUPPORTED, "E = %d outside [1, 1024]", E);
   NVFP4MOE_REQUIRE(k >= 1 && k <= E && k <= 32, NVFP4MOE_ERR_UNSUPPORTED, "k = %d outside [1, min(E, 32)]", k);
   NVFP4MOE_REQUIRE(k_primary >= 1 && k_primary <= k, NVFP4MOE_ERR_INVALID_ARG, "k_primary = %d outside [1, k = %d]",
                    k_primary, k);
-  NVFP4MOE_REQUIRE(H > 0 && H % 64 == 0, NVFP4MOE_ERR_UNSUPPORTED, "H = %d must be a positive multiple of 64", H);
+  const int hq = mx ? 128 : 64;
+  NVFP4MOE_REQUIRE(H > 0 && H % hq == 0, NVFP4MOE_ERR_UNSUPPORTED, "H = %d must be a positive multiple of %d", H, hq);
   NVFP4MOE_REQUIRE(int64_t(T) * k <= (int64_t(1) << 30), NVFP4MOE_ERR_UNSUPPORTED, "T*k too large");
   NVFP4MOE_REQUIRE(score_fn == NVFP4MOE_SCORE_SOFTMAX || score_fn == NVFP4MOE_SCORE_SIGMOID,
                    NVFP4MOE_ERR_INVALID_ARG, "score_fn %d", score_fn);
-  NVFP4MOE_REQUIRE(x_gscale && expert_counts && expert_offsets && row_offsets && perm_to_flat,
+  NVFP4MOE_REQUIRE((mx || x_gscale) && expert_counts && expert_offsets && row_offsets && perm_to_flat,
                    NVFP4MOE_ERR_INVALID_ARG, "null pointer");
   NVFP4MOE_REQUIRE(T == 0 || (logits && x_bf16 && topk_idx && topk_w && xq && xs && flat_to_perm && a_packed &&
                               a_scales),
@@ -387,11 +388,30 @@ int moe_prepare(const float* logits, const float* bias, const void* x_bf16, int 
   DeviceInfo d;
   if (int st = current_device(&d)) return st;
   return cuda_status(launch_prepare(logits, bias, x_bf16, T, E, k, k_primary, H, score_fn, renormalize ? 1 : 0,
-                                    topk_idx, topk_w,
-                                    x_gscale, xq, xs, expert_counts, expert_offsets, row_offsets, perm_to_flat,
-                                    flat_to_perm, a_packed, a_scales, moe_permute_rows_capacity(T, E, k), ws,
-                                    d.num_sms, stream),
+                                    topk_idx, topk_w, x_gscale, xq, xs, expert_counts, expert_offsets, row_offsets,
+                                    perm_to_flat, flat_to_perm, a_packed, a_scales,
+                                    moe_permute_rows_capacity(T, E, k), ws, mx, d.num_sms, stream),
                      "prepare launch");
+}
+
+int moe_prepare(const float* logits, const float* bias, const void* x_bf16, int T, int E, int k, int k_primary,
+                int H, int score_fn, int renormalize, int32_t* topk_idx, float* topk_w, float* x_gscale, uint8_t* xq,
+                uint8_t* xs, int32_t* expert_counts, int32_t* expert_offsets, int32_t* row_offsets,
+                int32_t* perm_to_flat, int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales, void* ws,
+                size_t ws_bytes, cudaStream_t stream) {
+  return prepare_common(false, logits, bias, x_bf16, T, E, k, k_primary, H, score_fn, renormalize, topk_idx, topk_w,
+                        x_gscale, xq, xs, expert_counts, expert_offsets, row_offsets, perm_to_flat, flat_to_perm,
+                        a_packed, a_scales, ws, ws_bytes, stream);
+}
+
+int moe_prepare_mxfp4(const float* logits, const float* bias, const void* x_bf16, int T, int E, int k,
+                      int k_primary, int H, int score_fn, int renormalize, int32_t* topk_idx, float* topk_w,
+                      uint8_t* xq, uint8_t* xs, int32_t* expert_counts, int32_t* expert_offsets,
+                      int32_t* row_offsets, int32_t* perm_to_flat, int32_t* flat_to_perm, uint8_t* a_packed,
+                      uint8_t* a_scales, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return prepare_common(true, logits, bias, x_bf16, T, E, k, k_primary, H, score_fn, renormalize, topk_idx, topk_w,
+                        nullptr, xq, xs, expert_counts, expert_offsets, row_offsets, perm_to_flat, flat_to_perm,
+                        a_packed, a_scales, ws, ws_bytes, stream);
 }
 
 // ---- a4/a5 ------------------------------------------------------------------

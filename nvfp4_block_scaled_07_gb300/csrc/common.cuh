@@ -46,25 +46,10 @@ __device__ __forceinline__ float ue4m3_to_f32(uint32_t b) {
   return __uint_as_float(((e + 120u) << 23) | (m << 20));
 }
 
-// E2M1 magnitude code of |q|: nearest of {0, .5, 1, 1.5, 2, 3, 4, 6},
-// ties to the even code, saturating at 6.  The comparisons sit on the exact
-// midpoints; strict/non-strict choice implements ties-to-even.
-__device__ __forceinline__ uint32_t e2m1_mag_code(float a) {
-  return uint32_t(a > 0.25f) + uint32_t(a >= 0.75f) + uint32_t(a > 1.25f) + uint32_t(a >= 1.75f) +
-         uint32_t(a > 2.5f) + uint32_t(a >= 3.5f) + uint32_t(a > 5.0f);
-}
-
-// Code of one element given the block's dequantisation step d = ue4m3(b) * s.
-__device__ __forceinline__ uint32_t e2m1_code(float x, float d) {
-  if (d == 0.0f) return 0u;
-  const uint32_t sign = (__float_as_uint(x) >> 31) << 3;
-  return e2m1_mag_code(fabsf(x) / d) | sign;
-}
-
 // Two E2M1 codes in one byte (lo in the low nibble) by the hardware
-// conversion: round to nearest E2M1 with ties to the even code, saturating
-// at +-6, the sign kept (so small negatives give -0, code 0x8) -- the same
-// rule as e2m1_mag_code plus the sign bit.
+// conversion: the nearest of {0, .5, 1, 1.5, 2, 3, 4, 6} in magnitude, ties
+// to the even code, saturating at 6, the sign kept (so small negatives give
+// -0, code 0x8).
 __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
   uint32_t r;
   asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
@@ -89,12 +74,6 @@ __device__ __forceinline__ int mx_exponent(float amax) {
 // 2^-X as a float32 (exact: X <= 125 for any finite bf16/float32 amax, and
 // 2^127 is representable for X = -127).
 __device__ __forceinline__ float mx_inv_step(int x) { return __uint_as_float(uint32_t(127 - x) << 23); }
-
-// Code of one element given 2^-X of its block: nearest E2M1 of x * 2^-X, sign of x.
-__device__ __forceinline__ uint32_t mx_code(float x, float inv_step) {
-  const uint32_t sign = (__float_as_uint(x) >> 31) << 3;
-  return e2m1_mag_code(fabsf(x) * inv_step) | sign;
-}
 
 // Two MXFP4 codes in one byte (x * 2^-X is exact, so the conversion rounds the true quotient).
 __device__ __forceinline__ uint32_t mx_code2(float lo, float hi, float inv_step) {

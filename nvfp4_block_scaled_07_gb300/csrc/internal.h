@@ -71,7 +71,7 @@ cudaError_t launch_prepare(const float* logits, const float* bias, const void* x
                            int H, int score_fn, int renormalize, int32_t* idx, float* w, float* gscale, uint8_t* xq,
                            uint8_t* xs, int32_t* counts, int32_t* offsets, int32_t* row_offsets, int32_t* perm_to_flat,
                            int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales, int64_t rows_capacity,
-                           void* ws, int num_sms, cudaStream_t st);
+                           void* ws, bool mx, int num_sms, cudaStream_t st);
 
 cudaError_t launch_finalize(const void* y, const int32_t* flat_to_perm, const float* w, int T, int k, int H,
                             int64_t rows_capacity, void* out, cudaStream_t st);

@@ -599,8 +599,9 @@ __global__ void __launch_bounds__(256) permute_place_kernel(const int32_t* __res
 // ---------------------------------------------------------------------------
 // a1 + a2 + a3 in one cooperative launch.  Four phases separated by grid
 // barriers (every CTA resident, bounded waits):
-//   A  route (one warp per token) and per-CTA partial amax of x;
-//   B  global scale from the partials, quantisation of x, segment ranks;
+//   A  route (one warp per token) and per-CTA partial amax of x (NVFP4);
+//   B  global scale from the partials, quantisation of x (NVFP4, or MXFP4
+//      with no global scale), segment ranks;
 //   C  CTA 0 scans the segment counts;
 //   D  padding rows, placement and the gather of packed rows and scales.
 // Each step is the same device code as in the separate kernels above, so the
@@ -611,6 +612,7 @@ struct PrepareParams {
   const float* bias;
   const uint4* x;
   int T, E, k, k_primary, H, score_fn, renorm, nseg;
+  int mx;  // MXFP4 (E8M0 scale per 32 elements, no global scale) instead of NVFP4
   int32_t* idx;
   float* w;
   float* gscale;
@@ -697,7 +699,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
     else
       route_token<VPL>(p.logits, p.bias, int(t), p.E, p.k, p.score_fn, p.renorm, nullptr, p.idx, p.w, lane);
   }
-  {
+  if (!p.mx) {
     float m = 0.f;
     const int64_t nvec = int64_t(p.T) * p.H / 8;
     int64_t i = tid;
@@ -729,11 +731,11 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
 
   // ---- B: segment ranks, global scale, quantisation --------------------------
   // The rank warps start at once; warp kRankWarps reduces the amax partials
-  // meanwhile, and the quantisation waits for its result.
+  // meanwhile (NVFP4), and the quantisation waits for its result.
   if (warp < kRankWarps)
     for (int64_t seg = int64_t(warp) * gridDim.x + blockIdx.x; seg < p.nseg; seg += int64_t(gridDim.x) * kRankWarps)
       rank_segment<ITERS>(p.idx, R, p.E, seg, s_rank_cnt + warp * p.E, p.rank, p.seg_count, lane);
-  if (warp == kRankWarps) {
+  if (warp == kRankWarps && !p.mx) {
     float m = 0.f;
     for (int i = lane; i < int(gridDim.x); i += 32) m = fmaxf(m, __ldcg(p.amax_part + i));
 #pragma unroll
@@ -741,9 +743,33 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
     if (lane == 0) s_red[0] = global_scale_of(m);
   }
   __syncthreads();
-  const float s = s_red[0];
-  if (blockIdx.x == 0 && threadIdx.x == 0) *p.gscale = s;
-  {
+  if (p.mx) {
+    // MXFP4: one thread per 32-element block, no global scale
+    const int64_t nblk = int64_t(p.T) * (p.H / 32);
+    for (int64_t b = tid; b < nblk; b += nthreads) {
+      uint4 q[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) q[j] = __ldg(p.x + 4 * b + j);
+      float a = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) a = amax8(q[j], a);
+      const int X = mx_exponent(a);
+      const float inv = mx_inv_step(X);
+      uint32_t wd[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t v[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+        uint32_t word = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) word |= mx_code2(bf16_lo(v[i]), bf16_hi(v[i]), inv) << (8 * i);
+        wd[j] = word;
+      }
+      reinterpret_cast<uint4*>(p.xq)[b] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+      p.xs[b] = uint8_t(X + 127);
+    }
+  } else {
+    const float s = s_red[0];
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.gscale = s;
     // two independent blocks per iteration: their four loads are in flight together
     const int64_t nblk = int64_t(p.T) * (p.H / 16);
     int64_t b = tid;
@@ -785,7 +811,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
   for (int64_t q = int64_t(__ldcg(p.row_offsets + p.E)) + tid; q < p.rows_cap; q += nthreads) p.perm_to_flat[q] = -1;
   for (int64_t f0 = gw0; f0 < R; f0 += 32 * gw_stride)
     place_rows(f0, gw_stride, R, p.idx, p.k, p.E, ITERS * 32, p.rank, p.seg_base, p.row_offsets, p.xq, p.xs, p.H,
-               p.H / 64, p.perm_to_flat, p.flat_to_perm, p.a_packed, p.a_scales, lane);
+               p.mx ? p.H / 128 : p.H / 64, p.perm_to_flat, p.flat_to_perm, p.a_packed, p.a_scales, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -981,7 +1007,7 @@ cudaError_t launch_prepare(const float* logits, const float* bias, const void* x
                            int H, int score_fn, int renormalize, int32_t* idx, float* w, float* gscale, uint8_t* xq,
                            uint8_t* xs, int32_t* counts, int32_t* offsets, int32_t* row_offsets, int32_t* perm_to_flat,
                            int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales, int64_t rows_capacity,
-                           void* ws, int num_sms, cudaStream_t st) {
+                           void* ws, bool mx, int num_sms, cudaStream_t st) {
   const PrepareLayout L = prepare_layout(T, E, k);
   uint8_t* base = static_cast<uint8_t*>(ws);
   PrepareParams p;
@@ -992,6 +1018,7 @@ cudaError_t launch_prepare(const float* logits, const float* bias, const void* x
   p.E = E;
   p.k = k;
   p.k_primary = k_primary;
+  p.mx = mx ? 1 : 0;
   p.H = H;
   p.score_fn = score_fn;
   p.renorm = renormalize;

@@ -1,6 +1,6 @@
 // Inline-PTX wrappers for the Blackwell (sm_103a) data path used by the
 // grouped GEMM: mbarriers, TMA (cp.async.bulk.tensor), the 5th-generation
-// tensor core (tcgen05.mma / tcgen05.cp / tcgen05.ld) and tensor memory.
+// tensor core (tcgen05.mma / tcgen05.ld / tcgen05.st) and tensor memory.
 // Written from the public PTX ISA; no library headers are involved.
 #pragma once
 
@@ -118,12 +118,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// Copy a 32-row x 16-byte block from shared memory into tensor memory,
-// replicated to all four 32-lane quarters (4 columns of 32 bits).
-__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 // MXFP4: D[tmem] (+)= A[smem] * B[smem]^T with E2M1 operands and two ue8m0
 // scales per row and 64-element K step (scale_vec::2X), held in bytes 0 and
 // 1 of the row's 32-bit scale-factor cell; float32 accumulate.
@@ -190,16 +184,6 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
   d |= uint64_t(1024 >> 4) << 32;                // stride offset   [32,46): 8 rows * 128 B
   d |= uint64_t(1) << 46;                        // descriptor version for tcgen05
   d |= uint64_t(2) << 61;                        // swizzle mode: 128 B
-  return d;
-}
-
-// Descriptor of a 32-row x 16-byte scale block stored contiguously
-// (no swizzle; 8-row groups every 128 bytes), the source of tcgen05.cp.
-__device__ __forceinline__ uint64_t desc_sf_block(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= uint64_t((saddr & 0x3FFFFu) >> 4);
-  d |= uint64_t(128 >> 4) << 32;                 // 8 rows * 16 B between 8-row groups
-  d |= uint64_t(1) << 46;
   return d;
 }
 

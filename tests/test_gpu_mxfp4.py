@@ -138,13 +138,42 @@ def test_grouped_gemm_mx_swiglu(B, E, I, K, counts):
                     O.unpack_codes(rq), rs, block=32)
 
 
+@pytest.mark.parametrize("T,E,k,H,k0", [(16, 8, 2, 256, None), (128, 256, 8, 6144, None), (2100, 64, 8, 128, None),
+                                        (300, 16, 4, 512, 1), (1, 4, 2, 128, None)])
+def test_prepare_mx_matches_separate_calls_and_oracle(B, T, E, k, H, k0):
+    rng = np.random.default_rng(T + H)
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16)
+    cuda = torch.device("cuda")
+    lg_d, x_d = torch.from_numpy(lg).to(cuda), x.to(cuda)
+    idx, w, xq, xs, perm = B.moe_prepare_mxfp4(lg_d, x_d, k, "sigmoid", True, k_primary=k0)
+    B.sync_status()
+    ridx, _ = (O.route_topk(lg, None, k, "sigmoid") if k0 is None else
+               O.route_batch_aware(lg, None, k, k0, "sigmoid"))
+    rxq, rxs = O.quantize_mxfp4(x.float().numpy())
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    np.testing.assert_array_equal(xq.cpu().numpy(), rxq)
+    np.testing.assert_array_equal(xs.cpu().numpy(), rxs)
+    U.check_permutation(perm, ridx, E, rxq, rxs, block=32)
+    sidx, sw = (B.moe_route_topk(lg_d, k, "sigmoid", True) if k0 is None else
+                B.moe_route_batch_aware(lg_d, k, k0, "sigmoid", True))
+    sxq, sxs = B.moe_quantize_mxfp4(x_d)
+    sperm = B.moe_permute_mxfp4(sidx, E, sxq, sxs)
+    B.sync_status()
+    assert torch.equal(idx, sidx) and torch.equal(w.view(torch.int32), sw.view(torch.int32))
+    assert torch.equal(xq, sxq) and torch.equal(xs, sxs)
+    for name in ("counts", "offsets", "row_offsets", "perm_to_flat", "flat_to_perm"):
+        assert torch.equal(getattr(perm, name), getattr(sperm, name)), name
+
+
+@pytest.mark.parametrize("fused", [True, False], ids=["fused_prepare", "separate_calls"])
 @pytest.mark.parametrize("w", [W.WORKLOADS["tiny"]] + list(W.TEST_WORKLOADS.values()), ids=lambda w: w.name)
-def test_layer_mx_matches_oracle(B, w):
+def test_layer_mx_matches_oracle(B, w, fused):
     inp = W.host_inputs(w, seed=2)
     cuda = torch.device("cuda")
     bias = inp["bias"]
     layer = B.MoELayer(inp["w_gu"].to(cuda), inp["w_d"].to(cuda), w.k, w.score, w.renormalize, w.h_scale,
-                       bias=None if bias is None else bias.to(cuda), fmt="mxfp4")
+                       bias=None if bias is None else bias.to(cuda), fmt="mxfp4", fused_prepare=fused)
     out = layer(inp["x"].to(cuda), inp["logits"].to(cuda)).float().cpu().numpy()
     B.sync_status()
     gq = U.oracle_quantize_experts_mx(inp["w_gu"])
