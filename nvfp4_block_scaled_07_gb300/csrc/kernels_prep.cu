@@ -829,19 +829,35 @@ __global__ void __launch_bounds__(128) finalize_kernel(const uint4* __restrict__
   const int c8 = blockIdx.y * blockDim.x + threadIdx.x;  // column group of 8
   if (c8 * 8 >= H) return;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int j = 0; j < k; ++j) {
-    const int64_t row = f2p[int64_t(t) * k + j];
-    const float wj = w[int64_t(t) * k + j];
-    if (row < 0 || row >= rows_capacity) {
-      if (c8 == 0) atomicOr(&g_prep_flags, kFlagBadData);
-      continue;
-    }
-    const uint4 q = y[(row * H) / 8 + c8];
-    const uint32_t v[4] = {q.x, q.y, q.z, q.w};
+  // Up to 8 slots at a time: their row indices, then their rows, are loaded
+  // together; the sum still runs in slot order.
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    const int n = min(8, k - j0);
+    int64_t row[8];
+    float wj[8];
+    uint4 q[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[2 * i] = fmaf(wj, bf16_lo(v[i]), acc[2 * i]);
-      acc[2 * i + 1] = fmaf(wj, bf16_hi(v[i]), acc[2 * i + 1]);
+    for (int j = 0; j < 8; ++j)
+      if (j < n) {
+        row[j] = f2p[int64_t(t) * k + j0 + j];
+        wj[j] = w[int64_t(t) * k + j0 + j];
+      }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < n && row[j] >= 0 && row[j] < rows_capacity) q[j] = y[(row[j] * H) / 8 + c8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j >= n) break;
+      if (row[j] < 0 || row[j] >= rows_capacity) {
+        if (c8 == 0) atomicOr(&g_prep_flags, kFlagBadData);
+        continue;
+      }
+      const uint32_t v[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(wj[j], bf16_lo(v[i]), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(wj[j], bf16_hi(v[i]), acc[2 * i + 1]);
+      }
     }
   }
   uint32_t o[4];
