@@ -63,19 +63,20 @@ __host__ __device__ constexpr int num_threads(bool swiglu) { return 32 * (2 + ep
 constexpr int kBM = 128;           // MMA M (weight rows per tile)
 constexpr int kBKBytes = 128;      // bytes of K per stage and row = 256 E2M1 elements
 constexpr int kATile = kBM * kBKBytes;
-constexpr int kSfTile = 2048;      // 4 k64 blocks x 512-byte scale blocks
 constexpr int kTmemCols = 512;
 constexpr int kAccSlotCols = 128;  // two accumulator slots at columns 0 and 128
+constexpr int kSfTile = 2048;      // 4 k64 blocks x 512-byte scale blocks
 constexpr int kSfColBase = 256;    // scale-factor ring: columns 256..511
 constexpr int kSfRingCols = 256;
 constexpr int kMaxSfSlots = 8;
 constexpr int kMaxStages = 16;
-// mbarriers: full/empty per stage, acc full/empty per slot, drain, sf full/empty per ring slot
+// mbarriers: full/empty per stage, acc full/empty per slot, drain, sf full/empty per ring slot,
+// the tile ring, and the scale copies of each stage
 // Ring of claimed tile ids (dynamic schedule): the producer claims ids from
 // a launch-wide counter and passes them to the other roles.
 constexpr int kTileRing = 32;
 __host__ __device__ constexpr int tile_consumers(bool swiglu) { return 1 + 4 + epi_warps(swiglu); }  // MMA, SF and epilogue warps
-constexpr int kNumBars = 2 * kMaxStages + 5 + 2 * kMaxSfSlots + 2 * kTileRing;
+constexpr int kNumBars = 3 * kMaxStages + 5 + 2 * kMaxSfSlots + 2 * kTileRing;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
@@ -122,11 +123,23 @@ __host__ __device__ constexpr int ctrl_bytes(int E) {
   return (kNumBars * 8 + 16 + kTileRing * 4 + (3 * E + 1) * 4 + 1023) / 1024 * 1024;
 }
 
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+// Bounded wait on an mbarrier phase.  SPIN polls with test_wait, which
+// never suspends the thread: the producer and the MMA issuer use it, since a
+// suspended try_wait resumed measurably late after the phase completed
+// (~0.2 us per stage at prefill); the other roles wait long stretches and
+// use try_wait, which leaves the issue slots to the warps that work.  The
+// slow path is kept out of line: a loop or call inlined between two groups
+// of MMAs measurably delays the issue of the second group.
+template <bool SPIN>
+__device__ __forceinline__ uint32_t poll_phase(uint32_t bar, uint32_t parity) {
+  return SPIN ? ptx::mbar_test_wait(bar, parity) : ptx::mbar_try_wait(bar, parity);
+}
+
+template <bool SPIN>
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t i = 0;; ++i) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (poll_phase<SPIN>(bar, parity)) return true;
     if ((i & 255u) == 255u) {
       if (*abort_flag) return false;
       if (ptx::globaltimer_ns() - t0 > kTimeoutNs) {
@@ -136,6 +149,12 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
       }
     }
   }
+}
+
+template <bool SPIN = false>
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (poll_phase<SPIN>(bar, parity)) return true;
+  return wait_phase_slow<SPIN>(bar, parity, abort_flag);
 }
 
 // Short bounded wait used only while draining after an abort.
@@ -322,12 +341,17 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   auto tqe_bar = [&](uint32_t q) {
     return bar0 + 8u * (uint32_t(2 * kMaxStages + 5 + 2 * kMaxSfSlots + kTileRing) + q);
   };
+  // the scale blocks of stage s, copied ahead of its operands
+  auto sfc_bar = [&](uint32_t s) {
+    return bar0 + 8u * (uint32_t(2 * kMaxStages + 5 + 2 * kMaxSfSlots + 2 * kTileRing) + s);
+  };
 
   const int MT = SWIGLU ? p.N / 2 / kBM : p.N / (kBM * NA);  // M tiles per expert
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
       ptx::mbar_init(full_bar(s), 1);
       ptx::mbar_init(empty_bar(s), 1);
+      ptx::mbar_init(sfc_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(accf_bar(b), 1);
@@ -422,7 +446,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     const uint32_t q = i % uint32_t(kTileRing), ph = (i / uint32_t(kTileRing)) & 1u;
     int t = -1;
     if (!whole_warp || lane == 0) {
-      if (wait_phase(tqf_bar(q), ph, abort_flag)) {
+      if (whole_warp ? wait_phase(tqf_bar(q), ph, abort_flag) : wait_phase<true>(tqf_bar(q), ph, abort_flag)) {
         t = s_tq[q];
         ptx::mbar_arrive(tqe_bar(q));
       }
@@ -444,7 +468,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       const int t = next;
       if (p.sched) {
         const uint32_t q = i % uint32_t(kTileRing), ph = (i / uint32_t(kTileRing)) & 1u;
-        if (!wait_phase(tqe_bar(q), ph ^ 1u, abort_flag)) {
+        if (!wait_phase<true>(tqe_bar(q), ph ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
@@ -462,42 +486,55 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       const int wstep = SWIGLU ? p.N / 2 : kBM;
       for (int kt = 0; kt < nkt; ++kt, ++it) {
         const uint32_t s = it % uint32_t(S), ph = (it / uint32_t(S)) & 1u;
-        if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag)) {
+        if (!wait_phase<true>(empty_bar(s), ph ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
+        const uint32_t st = smem_base + s * uint32_t(stage);
+        // The scale blocks first, on their own barrier: the scale-factor
+        // warps move them into tensor memory while the operands are in flight.
         const int nkb = min(4, kblocks - 4 * kt);
         // 512-byte scale blocks of this stage per 128 rows: one per k64 step
         // (NVFP4) or per k128 step (MXFP4, K % 128 == 0)
         const int nsf = MX ? nkb / 2 : nkb;
-        const uint32_t bytes = uint32_t(C::NA * kATile + w * kBKBytes + (C::NA + sfb_chunks) * nsf * 512);
-        ptx::mbar_arrive_expect_tx(full_bar(s), bytes);
-        const uint32_t st = smem_base + s * uint32_t(stage);
+        ptx::mbar_arrive_expect_tx(sfc_bar(s), uint32_t((C::NA + sfb_chunks) * nsf * 512));
+#pragma unroll
+        for (int j = 0; j < C::NA; ++j) {
+          const int rb = SWIGLU ? (j * (p.N / 2) + mb * kBM) / kBM : mb * NA + j;
+          const uint8_t* src = p.w_scales + ((size_t(e) * (p.N / kBM) + rb) * sf_k + sf_per_kt * kt) * 512;
+          ptx::bulk_load(st + off_sfa + j * kSfTile, src, uint32_t(nsf * 512), sfc_bar(s), pol_w);
+        }
+        for (int c = 0; c < sfb_chunks; ++c) {
+          const uint8_t* src = p.a_scales + ((size_t(arow / kBM) + c) * sf_k + sf_per_kt * kt) * 512;
+          ptx::bulk_load(st + off_sfb + c * kSfTile, src, uint32_t(nsf * 512), sfc_bar(s), pol_a);
+        }
+        ptx::mbar_arrive_expect_tx(full_bar(s), uint32_t(C::NA * kATile + w * kBKBytes));
 #pragma unroll
         for (int j = 0; j < C::NA; ++j)
           ptx::tma_load_2d(st + j * kATile, &tmap_w, full_bar(s), kt * kBKBytes, wrow0 + j * wstep, pol_w);
         for (int r = 0; r < w; r += 32)  // the token tile in 32-row boxes
           ptx::tma_load_2d(st + off_b + r * kBKBytes, &tmap_a, full_bar(s), kt * kBKBytes, arow + r, pol_a);
-#pragma unroll
-        for (int j = 0; j < C::NA; ++j) {
-          const int rb = SWIGLU ? (j * (p.N / 2) + mb * kBM) / kBM : mb * NA + j;
-          const uint8_t* src = p.w_scales + ((size_t(e) * (p.N / kBM) + rb) * sf_k + sf_per_kt * kt) * 512;
-          ptx::bulk_load(st + off_sfa + j * kSfTile, src, uint32_t(nsf * 512), full_bar(s), pol_w);
-        }
-        for (int c = 0; c < sfb_chunks; ++c) {
-          const uint8_t* src = p.a_scales + ((size_t(arow / kBM) + c) * sf_k + sf_per_kt * kt) * 512;
-          ptx::bulk_load(st + off_sfb + c * kSfTile, src, uint32_t(nsf * 512), full_bar(s), pol_a);
-        }
       }
     }
     if (!ok) {
       // Let every copy this thread issued land before the CTA can exit.
       const uint32_t first = it > uint32_t(S) ? it - uint32_t(S) : 0u;
-      for (uint32_t i = first; i < it; ++i) drain_phase(full_bar(i % uint32_t(S)), (i / uint32_t(S)) & 1u);
+      for (uint32_t i = first; i < it; ++i) {
+        drain_phase(sfc_bar(i % uint32_t(S)), (i / uint32_t(S)) & 1u);
+        drain_phase(full_bar(i % uint32_t(S)), (i / uint32_t(S)) & 1u);
+      }
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
-    uint32_t it = 0;
+    // The tensor core queues about one MMA, so whatever this thread does
+    // between two groups of MMAs (waits, commits, address arithmetic) leaves
+    // it idle.  The loop therefore keeps that work small: ring positions are
+    // wrap-around counters, both barriers of a stage are polled once with the
+    // bounded slow path out of line, and two K stages of a tile are waited
+    // for together and issued back to back (a probe on one SM: 904 -> 709
+    // cycles per 8 MMAs against 518 for MMAs alone).
+    uint32_t s = 0, ph = 0;  // pipeline stage and its phase parity
+    uint32_t r = 0, rph = 0;  // scale-factor ring slot and its parity
     SlotSeq slots;
     bool ok = true;
     for (uint32_t i = 0; ok; ++i) {
@@ -507,30 +544,16 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
       int s0, s1;
       slots.pick(C::NA * w, s0, s1);
-      if (!wait_phase(acce_bar(s0), slots.parity(s0) ^ 1u, abort_flag)) break;
-      if (s1 >= 0 && !wait_phase(acce_bar(s1), slots.parity(s1) ^ 1u, abort_flag)) break;
+      if (!wait_phase<true>(acce_bar(s0), slots.parity(s0) ^ 1u, abort_flag)) break;
+      if (s1 >= 0 && !wait_phase<true>(acce_bar(s1), slots.parity(s1) ^ 1u, abort_flag)) break;
       ptx::tc_fence_after();
       const uint32_t idesc = ptx::idesc_nvfp4(kBM, w, MX);
       const uint32_t d0 = tmem + uint32_t(s0 * kAccSlotCols);
-      for (int kt = 0; kt < nkt; ++kt, ++it) {
-        const uint32_t s = it % uint32_t(S), ph = (it / uint32_t(S)) & 1u;
-        // The stage's scales are in tensor memory once the scale-factor
-        // warps arrive, which they do only after its copies have landed; the
-        // stage's own barrier is complete by then and is checked as well.
-        const uint32_t r = it % uint32_t(C::SfSlots), rph = (it / uint32_t(C::SfSlots)) & 1u;
-        if (!wait_phase(sff_bar(r), rph, abort_flag) || !wait_phase(full_bar(s), ph, abort_flag)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        const uint32_t st = smem_base + s * uint32_t(stage);
-        const uint32_t sf = tmem + uint32_t(kSfColBase + r * C::SfCols);
+      // The MMAs of K stage kt from pipeline stage st and scale slot sf: a
+      // full stage (4 k64 blocks) is one fully unrolled sequence.
+      auto issue_stage = [&](int kt, uint32_t st, uint32_t sf) {
         const int nkb = min(4, kblocks - 4 * kt);
         const uint64_t bdesc = ptx::desc_kmajor_sw128(st + off_b);
-        // The tensor core pipelines MMAs only when they are issued back to
-        // back; any loop overhead in between makes each one wait for the
-        // previous.  A full stage (4 k64 blocks) is therefore issued from a
-        // fully unrolled sequence; only a partial last K tile takes the loop.
         auto mma_block = [&](int kb) {
 #pragma unroll
           for (int j = 0; j < C::NA; ++j) {
@@ -548,8 +571,39 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         } else {
           for (int kb = 0; kb < nkb; ++kb) mma_block(kb);
         }
+      };
+      for (int kt = 0; kt < nkt; kt += 2) {
+        const bool two = kt + 1 < nkt;
+        uint32_t s2 = s + 1, ph2 = ph, r2 = r + 1, rph2 = rph;
+        if (s2 == uint32_t(S)) s2 = 0, ph2 ^= 1u;
+        if (r2 == uint32_t(C::SfSlots)) r2 = 0, rph2 ^= 1u;
+        // A stage's scales are in tensor memory once the scale-factor warps
+        // arrive, which they do only after its copies have landed; the
+        // stage's own barrier is complete by then and is checked as well.
+        uint32_t ready = ptx::mbar_test_wait(sff_bar(r), rph) & ptx::mbar_test_wait(full_bar(s), ph);
+        if (two) ready &= ptx::mbar_test_wait(sff_bar(r2), rph2) & ptx::mbar_test_wait(full_bar(s2), ph2);
+        if (!ready) {
+          if (!wait_phase<true>(sff_bar(r), rph, abort_flag) || !wait_phase<true>(full_bar(s), ph, abort_flag) ||
+              (two && (!wait_phase<true>(sff_bar(r2), rph2, abort_flag) ||
+                       !wait_phase<true>(full_bar(s2), ph2, abort_flag)))) {
+            ok = false;
+            break;
+          }
+        }
+        ptx::tc_fence_after();
+        issue_stage(kt, smem_base + s * uint32_t(stage), tmem + uint32_t(kSfColBase + r * C::SfCols));
         ptx::tc_commit(empty_bar(s));  // frees the stage once these MMAs have read it
-        ptx::tc_commit(sfe_bar(r));    // and the scale-factor ring slot
+        ptx::tc_commit(sfe_bar(r));
+        if (two) {
+          issue_stage(kt + 1, smem_base + s2 * uint32_t(stage), tmem + uint32_t(kSfColBase + r2 * C::SfCols));
+          ptx::tc_commit(empty_bar(s2));
+          ptx::tc_commit(sfe_bar(r2));
+          s = s2 + 1, ph = ph2, r = r2 + 1, rph = rph2;
+        } else {
+          s = s2, ph = ph2, r = r2, rph = rph2;
+        }
+        if (s == uint32_t(S)) s = 0, ph ^= 1u;
+        if (r == uint32_t(C::SfSlots)) r = 0, rph ^= 1u;
       }
       if (!ok) break;
       ptx::tc_commit(accf_bar(s0));
@@ -565,20 +619,21 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     // columns per lane, the same in every quarter): lane i loads the block's
     // 16-byte row i and stores it as 4 columns.  Doing this with tcgen05.st
     // from these warps keeps the MMA issue stream free of copies, which would
-    // otherwise serialise with the MMAs of the previous stage.
+    // otherwise serialise with the MMAs of the previous stage.  The warps
+    // wait only for the stage's scale copies, which the producer issues
+    // ahead of its operands, so this work is off the path from the operand
+    // copies to the MMAs.
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
-    uint32_t it = 0;
-    for (uint32_t i = 0;; ++i) {
+    uint32_t s = 0, ph = 0, r = 0, rph = 0;
+    bool ok = true;
+    for (uint32_t i = 0; ok; ++i) {
       const int t = next_tile(i, true);
       if (t < 0 || t >= total) break;
       int e, mb, nb, w;
       decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
       const int sfb_chunks = w > 128 ? 2 : 1;
-      bool ok = true;
-      for (int kt = 0; kt < nkt; ++kt, ++it) {
-        const uint32_t s = it % uint32_t(S), ph = (it / uint32_t(S)) & 1u;
-        const uint32_t r = it % uint32_t(C::SfSlots), rph = (it / uint32_t(C::SfSlots)) & 1u;
-        if (!wait_phase(sfe_bar(r), rph ^ 1u, abort_flag) || !wait_phase(full_bar(s), ph, abort_flag)) {
+      for (int kt = 0; kt < nkt; ++kt) {
+        if (!wait_phase(sfe_bar(r), rph ^ 1u, abort_flag) || !wait_phase(sfc_bar(s), ph, abort_flag)) {
           ok = false;
           break;
         }
@@ -623,8 +678,9 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(sff_bar(r));
+        if (++s == uint32_t(S)) s = 0, ph ^= 1u;
+        if (++r == uint32_t(C::SfSlots)) r = 0, rph ^= 1u;
       }
-      if (!ok) break;
     }
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
@@ -657,28 +713,44 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         // lane quarter) into h = silu(gate) * up, release the accumulator so
         // the next tile's MMAs can start, then requantise from registers.
         static_assert(BN == 128 && kParts == 2, "two 32-token chunks per epilogue warp");
-        float hb[2][32];
+        // h = silu(gate) * up of a chunk, computed in place over the gate
+        // registers (the warp holds one raw chunk and one finished one).
+        auto swiglu = [&](uint32_t (&g)[32], const uint32_t (&u)[32]) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int c0 = 32 * part + 64 * j;
-          if (c0 < valid) {
-            uint32_t g[32], u[32];
-            ptx::tmem_ld_32x32b_x32(tbase + c0, g);
-            ptx::tmem_ld_32x32b_x32(tbase + w + c0, u);
-            ptx::tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float gf = __uint_as_float(g[i]) * scale;
-              const float uf = __uint_as_float(u[i]) * scale;
-              hb[j][i] = gf * ptx::rcp_approx(1.0f + __expf(-gf)) * uf;
-            }
+          for (int i = 0; i < 32; ++i) {
+            const float gf = __uint_as_float(g[i]) * scale;
+            const float uf = __uint_as_float(u[i]) * scale;
+            g[i] = __float_as_uint(gf * ptx::rcp_approx(1.0f + __expf(-gf)) * uf);
           }
+        };
+        // The accumulator is released once both chunks are in registers; the
+        // second chunk's SwiGLU (bound by the special-function units) runs
+        // after that.
+        uint32_t h0[32], g[32], u[32];
+        const bool have0 = 32 * part < valid, have1 = 32 * part + 64 < valid;
+        if (have0) {
+          ptx::tmem_ld_32x32b_x32(tbase + 32 * part, h0);
+          ptx::tmem_ld_32x32b_x32(tbase + w + 32 * part, u);
+          ptx::tmem_ld_wait();
+          swiglu(h0, u);
+        }
+        if (have1) {
+          ptx::tmem_ld_32x32b_x32(tbase + 32 * part + 64, g);
+          ptx::tmem_ld_32x32b_x32(tbase + w + 32 * part + 64, u);
+          ptx::tmem_ld_wait();
         }
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           ptx::mbar_arrive(acce_bar(s0));
           if (s1 >= 0) ptx::mbar_arrive(acce_bar(s1));
+        }
+        if (have1) swiglu(g, u);
+        float hb[2][32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          hb[0][i] = __uint_as_float(h0[i]);
+          hb[1][i] = __uint_as_float(g[i]);
         }
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
