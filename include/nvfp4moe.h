@@ -77,6 +77,9 @@ extern "C" {
 #define NVFP4MOE_EPI_SWIGLU_F32     2  /* h = silu(gate) * up as float32 (unfused check) */
 #define NVFP4MOE_EPI_SWIGLU_MXFP4   3  /* h = silu(gate) * up, requantised to MXFP4 (MXFP4 GEMM only) */
 
+/* Grouped GEMM tile_n value for token-major tiles (see moe_grouped_gemm_nvfp4). */
+#define NVFP4MOE_TILE_TOKEN_MAJOR   (-1)
+
 /* ---- library and device ------------------------------------------------- */
 
 /* Version as major*10000 + minor*100 + patch. */
@@ -280,11 +283,18 @@ int moe_prepare(const float* logits, const float* bias, const void* x_bf16,
  * written by moe_permute; w_packed device uint8 [E, N, K/2]; w_scales
  * device, blocked per expert ([E] x nvfp4moe_blocked_scales_bytes(N, K));
  * w_gscale device float32 [E].
- * m_total = number of routed rows (T*k); informational.
- * tile_n = the widest token tile: 0 or 128, or 256 with NVFP4MOE_EPI_BF16.
- * Token tiles start on 128-row boundaries of an expert's rows; each tile's
- * MMA width is the smallest of 32, 64, 128, 256 covering the rows left
- * (capped at tile_n), so a decode expert with 4 rows runs 128 x 32 MMAs.
+ * m_total = number of routed rows (T*k); it only guides the choice of tiles.
+ * tile_n selects the tile orientation.  128, or 256 with NVFP4MOE_EPI_BF16:
+ * the widest token tile with weight rows as the MMA's 128-row M side; token
+ * tiles start on 128-row boundaries of an expert's rows and each tile's MMA
+ * width is the smallest of 32, 64, 128, 256 covering the rows left (capped
+ * at tile_n), so a decode expert with 4 rows runs 128 x 32 MMAs.
+ * NVFP4MOE_TILE_TOKEN_MAJOR (N % 256 == 0): 128 tokens as M and two 128-row
+ * weight tiles (gate and up, or two consecutive output blocks) as one
+ * N = 256 operand, which reads each token tile once per K step (for experts
+ * with hundreds of rows; a partial tile still computes 128 token rows).
+ * 0: token-major when N % 256 == 0 and m_total >= 256 * E, else 128.
+ * The results do not depend on tile_n beyond float32 summation order.
  * Limits: K % 64 == 0; N % 128 == 0 (BF16) or N % 256 == 0 (SwiGLU);
  * 1 <= E <= 1024; rows_capacity % 128 == 0.  A pipeline that does not fit the
  * device's opt-in shared memory is refused with NVFP4MOE_ERR_SMEM (the

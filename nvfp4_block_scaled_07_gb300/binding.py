@@ -32,6 +32,7 @@ SCORE = {"softmax": 0, "sigmoid": 1}
 QUANT_COMPUTE_GLOBAL = 1
 QUANT_SCALES_BLOCKED = 2
 EPI_BF16, EPI_SWIGLU_NVFP4, EPI_SWIGLU_F32, EPI_SWIGLU_MXFP4 = 0, 1, 2, 3
+TILE_TOKEN_MAJOR = -1  # grouped GEMM tile_n: 128 tokens as M, two weight tiles as one N = 256 operand
 
 _i, _i64, _sz, _p, _f = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
 _SIGS = {

@@ -447,8 +447,12 @@ static int grouped_gemm_common(bool mx, const uint8_t* a_packed, const uint8_t* 
                    NVFP4MOE_ERR_INVALID_ARG, "rows_capacity %lld must be a positive multiple of 128",
                    (long long)rows_capacity);
   NVFP4MOE_REQUIRE(m_total >= 0, NVFP4MOE_ERR_INVALID_ARG, "m_total < 0");
-  NVFP4MOE_REQUIRE(tile_n == 0 || tile_n == 128 || (!swiglu && tile_n == 256), NVFP4MOE_ERR_UNSUPPORTED,
-                   "tile_n %d (expected 0, 128, or 256 for the bf16 epilogue)", tile_n);
+  NVFP4MOE_REQUIRE(tile_n == 0 || tile_n == 128 || (!swiglu && tile_n == 256) ||
+                       (tile_n == NVFP4MOE_TILE_TOKEN_MAJOR && N % 256 == 0),
+                   NVFP4MOE_ERR_UNSUPPORTED,
+                   "tile_n %d (expected 0, 128, 256 for the bf16 epilogue, or NVFP4MOE_TILE_TOKEN_MAJOR with "
+                   "N %% 256 == 0)",
+                   tile_n);
   NVFP4MOE_REQUIRE(a_packed && a_scales && expert_counts && row_offsets && w_packed && w_scales && c_out,
                    NVFP4MOE_ERR_INVALID_ARG, "null pointer");
   NVFP4MOE_REQUIRE(mx || (a_gscale && w_gscale), NVFP4MOE_ERR_INVALID_ARG, "null per-tensor scale pointer");
@@ -479,7 +483,8 @@ static int grouped_gemm_common(bool mx, const uint8_t* a_packed, const uint8_t* 
   a.c_gscale = c_gscale;
   a.c_out = c_out;
   a.c_scales = c_scales;
-  a.tile_n = tile_n;
+  // tile_n = 0: token-major tiles once experts average kTokenMajorMinRows rows
+  a.tile_n = tile_n == 0 && N % 256 == 0 && m_total >= kTokenMajorMinRows * E ? NVFP4MOE_TILE_TOKEN_MAJOR : tile_n;
   a.mx = mx;
   a.sched = ws;
   return launch_grouped_gemm(a, d.num_sms, d.smem_optin, stream);  // detail already set on failure

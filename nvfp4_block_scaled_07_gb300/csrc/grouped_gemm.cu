@@ -14,13 +14,19 @@
 // tensor memory, operands staged by TMA through a deep mbarrier ring that
 // uses the whole opt-in shared memory.
 //
-// Orientation ("swap AB"): the weight rows of one expert form the 128-row
-// M side, the expert's tokens form the N side.  Decode-sized experts (a
+// Orientation ("swap AB", the default): the weight rows of one expert form
+// the 128-row M side, the expert's tokens form the N side.  Decode-sized experts (a
 // handful to ~64 tokens) then fill whole MMAs along M and the kernel
 // streams every weight tile from HBM exactly once.  Token tiles start on
 // 128-row boundaries (so every scale-factor address in tensor memory stays
 // 4-column aligned) and each tile's MMA width is the power of two >= 32 that
 // covers the expert's remaining rows, up to BN (128 or 256).
+// Token-major orientation (TM, for experts with hundreds of rows): 128
+// tokens form M and the stage's two 128-row weight tiles (gate and up, or
+// two consecutive output blocks) form one N = 256 operand, so each k64 step
+// is a single MMA that reads the token tile once instead of once per weight
+// tile (48 instead of 64 KB of shared-memory reads per stage), and each
+// epilogue thread holds one token's features in consecutive columns.
 //
 // Warp roles (one CTA per SM, persistent):
 //   warp 0     TMA producer: weight tile(s), token tile, their scale blocks
@@ -310,11 +316,68 @@ __device__ __forceinline__ void requant_swiglu_chunk_mx(const float (&h)[32], in
   }
 }
 
-template <int BN, int NA, bool SWIGLU, bool MX>
+// Token-major epilogue: NVFP4 requantisation of 32 consecutive features of
+// one token row held by one thread (h[i] = feature f0 + i as float bits,
+// f0 % 32 == 0), two 16-feature blocks, with the rounding steps of
+// requant_swiglu_chunk.  The 16 code bytes are one 16-byte store.
+__device__ __forceinline__ void requant_row32(const uint32_t (&h)[32], float s_h, int64_t row, int f0, int n_out,
+                                              uint8_t* out_codes, uint8_t* out_scales) {
+  uint32_t wd[4];
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(__uint_as_float(h[16 * b + i])));
+    const uint32_t sb = f32_to_ue4m3((a / kE2M1Max) / s_h);
+    const float d = ue4m3_to_f32(sb) * s_h;
+    const float inv = d != 0.0f ? 1.0f / d : 0.0f;
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int pr = 0; pr < 4; ++pr) {
+        const int i = 16 * b + 8 * w + 2 * pr;
+        const float q0 = inv != 0.0f ? __uint_as_float(h[i]) * inv : 0.0f;
+        const float q1 = inv != 0.0f ? __uint_as_float(h[i + 1]) * inv : 0.0f;
+        word |= e2m1x2(q0, q1) << (8 * pr);
+      }
+      wd[2 * b + w] = word;
+    }
+    const int fb = f0 + 16 * b;
+    out_scales[blocked_sf_offset(row, fb >> 6, n_out / 64) + ((fb >> 4) & 3)] = uint8_t(sb);
+  }
+  *reinterpret_cast<uint4*>(out_codes + row * (n_out / 2) + f0 / 2) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+}
+
+// MXFP4 counterpart: the 32 features are one MX block (requant_swiglu_chunk_mx).
+__device__ __forceinline__ void requant_row32_mx(const uint32_t (&h)[32], int64_t row, int f0, int n_out,
+                                                 uint8_t* out_codes, uint8_t* out_scales) {
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(__uint_as_float(h[i])));
+  const int X = mx_exponent(a);
+  const float inv = mx_inv_step(X);
+  uint32_t wd[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int pr = 0; pr < 4; ++pr) {
+      const int i = 8 * w + 2 * pr;
+      word |= e2m1x2(__uint_as_float(h[i]) * inv, __uint_as_float(h[i + 1]) * inv) << (8 * pr);
+    }
+    wd[w] = word;
+  }
+  out_scales[blocked_sf_offset(row, f0 >> 7, n_out / 128) + ((f0 >> 5) & 3)] = uint8_t(X + 127);
+  *reinterpret_cast<uint4*>(out_codes + row * (n_out / 2) + f0 / 2) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+}
+
+template <int BN, int NA, bool SWIGLU, bool MX, bool TM>
 __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                         const Params p) {
   using C = Cfg<BN, NA, SWIGLU>;
+  static_assert(!TM || (BN == 128 && NA == 2), "token-major tiles: 128 tokens x two 128-row weight tiles");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -429,7 +492,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   const int sf_per_kt = MX ? 2 : 4;              // of them per 256-element K stage
   // Stage geometry for this launch: as many stages as fit once the token
   // slot is sized for the widest tile actually present.
-  const int wmax = *s_wmax;
+  const int wmax = TM ? kBM : *s_wmax;  // token-major: every token tile is 128 rows
   const int stage = C::stage_bytes(wmax);
   const int off_b = C::NA * kATile;
   const int off_sfa = off_b + wmax * kBKBytes;
@@ -479,6 +542,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       next = p.sched ? int(atomicAdd(p.sched, 1u)) : t + int(gridDim.x);
       int e, mb, nb, w;
       decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
+      if constexpr (TM) w = kBM;
       const int arow = s_rowoff[e] + nb * BN;
       const int sfb_chunks = w > 128 ? 2 : 1;
       // weight rows of tile j: gate/up pairs rows f and I + f; otherwise NA consecutive 128-row blocks
@@ -542,12 +606,13 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       if (t < 0 || t >= total) break;
       int e, mb, nb, w;
       decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
+      if constexpr (TM) w = kBM;
       int s0, s1;
       slots.pick(C::NA * w, s0, s1);
       if (!wait_phase<true>(acce_bar(s0), slots.parity(s0) ^ 1u, abort_flag)) break;
       if (s1 >= 0 && !wait_phase<true>(acce_bar(s1), slots.parity(s1) ^ 1u, abort_flag)) break;
       ptx::tc_fence_after();
-      const uint32_t idesc = ptx::idesc_nvfp4(kBM, w, MX);
+      const uint32_t idesc = TM ? ptx::idesc_nvfp4(kBM, C::NA * kBM, MX) : ptx::idesc_nvfp4(kBM, w, MX);
       const uint32_t d0 = tmem + uint32_t(s0 * kAccSlotCols);
       // The MMAs of K stage kt from pipeline stage st and scale slot sf: a
       // full stage (4 k64 blocks) is one fully unrolled sequence.
@@ -555,14 +620,25 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         const int nkb = min(4, kblocks - 4 * kt);
         const uint64_t bdesc = ptx::desc_kmajor_sw128(st + off_b);
         auto mma_block = [&](int kb) {
-#pragma unroll
-          for (int j = 0; j < C::NA; ++j) {
+          if constexpr (TM) {
+            // D[token][weight row] += tokens (A, M = 128) x weight tiles (B, N = 256);
+            // scales: tokens at column 32 + 4 kb, weights at 8 kb (+4 for the second tile)
+            const uint64_t adesc = ptx::desc_kmajor_sw128(st + off_b) + 2 * kb;
+            const uint64_t wdesc = ptx::desc_kmajor_sw128(st) + 2 * kb;
             if constexpr (MX)
-              ptx::tc_mma_mxfp4(d0 + j * w, ptx::desc_kmajor_sw128(st + j * kATile) + 2 * kb, bdesc + 2 * kb, idesc,
-                                sf + j * 16 + kb * 4, sf + C::NA * 16 + kb * 4 * C::NSFB, (kt | kb) != 0 ? 1u : 0u);
+              ptx::tc_mma_mxfp4(d0, adesc, wdesc, idesc, sf + C::NA * 16 + kb * 4, sf + kb * 8, (kt | kb) != 0 ? 1u : 0u);
             else
-              ptx::tc_mma_nvfp4(d0 + j * w, ptx::desc_kmajor_sw128(st + j * kATile) + 2 * kb, bdesc + 2 * kb, idesc,
-                                sf + j * 16 + kb * 4, sf + C::NA * 16 + kb * 4 * C::NSFB, (kt | kb) != 0 ? 1u : 0u);
+              ptx::tc_mma_nvfp4(d0, adesc, wdesc, idesc, sf + C::NA * 16 + kb * 4, sf + kb * 8, (kt | kb) != 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int j = 0; j < C::NA; ++j) {
+              if constexpr (MX)
+                ptx::tc_mma_mxfp4(d0 + j * w, ptx::desc_kmajor_sw128(st + j * kATile) + 2 * kb, bdesc + 2 * kb, idesc,
+                                  sf + j * 16 + kb * 4, sf + C::NA * 16 + kb * 4 * C::NSFB, (kt | kb) != 0 ? 1u : 0u);
+              else
+                ptx::tc_mma_nvfp4(d0 + j * w, ptx::desc_kmajor_sw128(st + j * kATile) + 2 * kb, bdesc + 2 * kb, idesc,
+                                  sf + j * 16 + kb * 4, sf + C::NA * 16 + kb * 4 * C::NSFB, (kt | kb) != 0 ? 1u : 0u);
+            }
           }
         };
         if (nkb == 4) {
@@ -624,6 +700,10 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     // ahead of its operands, so this work is off the path from the operand
     // copies to the MMAs.
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+    // column of weight tile j's scales for k64 step kb within a ring slot:
+    // per tile (swap AB, the tile is one MMA's A operand) or interleaved per
+    // step (token-major, the two tiles are one N = 256 B operand)
+    auto wcol = [](int j, int kb) { return TM ? kb * 8 + j * 4 : j * 16 + kb * 4; };
     uint32_t s = 0, ph = 0, r = 0, rph = 0;
     bool ok = true;
     for (uint32_t i = 0; ok; ++i) {
@@ -631,6 +711,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       if (t < 0 || t >= total) break;
       int e, mb, nb, w;
       decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
+      if constexpr (TM) w = kBM;
       const int sfb_chunks = w > 128 ? 2 : 1;
       for (int kt = 0; kt < nkt; ++kt) {
         if (!wait_phase(sfe_bar(r), rph ^ 1u, abort_flag) || !wait_phase(sfc_bar(s), ph, abort_flag)) {
@@ -649,9 +730,9 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
 #pragma unroll
             for (int j = 0; j < C::NA; ++j) {
               const uint4 v = ptx::lds128(st + off_sfa + j * kSfTile + m * 512 + lane * 16);
-              ptx::tmem_st_32x32b_x4(sf + j * 16 + (2 * m) * 4, v.x & 0xFFFFu, v.y & 0xFFFFu, v.z & 0xFFFFu,
+              ptx::tmem_st_32x32b_x4(sf + wcol(j, 2 * m), v.x & 0xFFFFu, v.y & 0xFFFFu, v.z & 0xFFFFu,
                                      v.w & 0xFFFFu);
-              ptx::tmem_st_32x32b_x4(sf + j * 16 + (2 * m + 1) * 4, v.x >> 16, v.y >> 16, v.z >> 16, v.w >> 16);
+              ptx::tmem_st_32x32b_x4(sf + wcol(j, 2 * m + 1), v.x >> 16, v.y >> 16, v.z >> 16, v.w >> 16);
             }
             for (int c = 0; c < sfb_chunks; ++c) {
               const uint4 v = ptx::lds128(st + off_sfb + c * kSfTile + m * 512 + lane * 16);
@@ -666,7 +747,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
 #pragma unroll
             for (int j = 0; j < C::NA; ++j) {
               const uint4 v = ptx::lds128(st + off_sfa + j * kSfTile + kb * 512 + lane * 16);
-              ptx::tmem_st_32x32b_x4(sf + j * 16 + kb * 4, v.x, v.y, v.z, v.w);
+              ptx::tmem_st_32x32b_x4(sf + wcol(j, kb), v.x, v.y, v.z, v.w);
             }
             for (int c = 0; c < sfb_chunks; ++c) {
               const uint4 v = ptx::lds128(st + off_sfb + c * kSfTile + kb * 512 + lane * 16);
@@ -698,6 +779,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       if (t < 0 || t >= total) break;
       int e, mb, nb, w;
       decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
+      if constexpr (TM) w = kBM;
       int s0, s1;
       slots.pick(C::NA * w, s0, s1);
       if (!wait_phase(accf_bar(s0), slots.parity(s0), abort_flag)) break;
@@ -708,21 +790,92 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       const float scale = MX ? 1.0f : a_gs * p.w_gscale[e];
       const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + uint32_t(s0 * kAccSlotCols);
       const int f = (SWIGLU ? mb : mb * NA) * kBM + lrow;  // output column (of tile 0)
-      if constexpr (SWIGLU) {
+      // h = silu(gate) * up of a chunk, computed in place over the gate
+      // registers (a warp holds one raw chunk and one finished one).
+      auto swiglu = [&](uint32_t (&g)[32], const uint32_t (&u)[32]) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float gf = __uint_as_float(g[i]) * scale;
+          const float uf = __uint_as_float(u[i]) * scale;
+          g[i] = __float_as_uint(gf * ptx::rcp_approx(1.0f + __expf(-gf)) * uf);
+        }
+      };
+      auto release = [&]() {
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(acce_bar(s0));
+          if (s1 >= 0) ptx::mbar_arrive(acce_bar(s1));
+        }
+      };
+      if constexpr (TM) {
+        // Token-major: accumulator lane = token row of the tile, column =
+        // weight row of the N = 256 operand.
+        const int64_t row = row0 + q * 32 + lane;
+        const bool row_ok = q * 32 + lane < valid;
+        if constexpr (SWIGLU) {
+          // Features [64 part, 64 part + 64) of the tile's 128: gate in
+          // columns c, up in 128 + c; two 32-feature chunks, the accumulator
+          // released once both are in registers.
+          static_assert(kParts == 2, "two epilogue warps per lane quarter");
+          const int c0 = 64 * part;
+          uint32_t h0[32], g[32], u[32];
+          ptx::tmem_ld_32x32b_x32(tbase + c0, h0);
+          ptx::tmem_ld_32x32b_x32(tbase + kBM + c0, u);
+          ptx::tmem_ld_wait();
+          swiglu(h0, u);
+          ptx::tmem_ld_32x32b_x32(tbase + c0 + 32, g);
+          ptx::tmem_ld_32x32b_x32(tbase + kBM + c0 + 32, u);
+          ptx::tmem_ld_wait();
+          release();
+          swiglu(g, u);
+          if (row_ok) {
+            const int fo = mb * kBM + c0;  // output feature of h0[0]
+            if (f32_out) {
+              float4* out = reinterpret_cast<float4*>(static_cast<float*>(p.c_out) + row * n_out + fo);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                out[i] = make_float4(__uint_as_float(h0[4 * i]), __uint_as_float(h0[4 * i + 1]),
+                                     __uint_as_float(h0[4 * i + 2]), __uint_as_float(h0[4 * i + 3]));
+                out[8 + i] = make_float4(__uint_as_float(g[4 * i]), __uint_as_float(g[4 * i + 1]),
+                                         __uint_as_float(g[4 * i + 2]), __uint_as_float(g[4 * i + 3]));
+              }
+            } else if constexpr (MX) {
+              requant_row32_mx(h0, row, fo, n_out, static_cast<uint8_t*>(p.c_out), p.c_scales);
+              requant_row32_mx(g, row, fo + 32, n_out, static_cast<uint8_t*>(p.c_out), p.c_scales);
+            } else {
+              requant_row32(h0, s_h, row, fo, n_out, static_cast<uint8_t*>(p.c_out), p.c_scales);
+              requant_row32(g, s_h, row, fo + 32, n_out, static_cast<uint8_t*>(p.c_out), p.c_scales);
+            }
+          }
+        } else {
+          // bf16: columns c = output features mb * 256 + c, 64 bytes per chunk and row
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.c_out) + row * n_out + mb * (C::NA * kBM);
+#pragma unroll 1
+          for (int c0 = 0; c0 < C::NA * kBM; c0 += 32) {
+            uint32_t g[32];
+            ptx::tmem_ld_32x32b_x32(tbase + c0, g);
+            ptx::tmem_ld_wait();
+            if (row_ok) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(g[2 * i]) * scale,
+                                                               __uint_as_float(g[2 * i + 1]) * scale);
+                pk[i] = *reinterpret_cast<const uint32_t*>(&v);
+              }
+              uint4* o = reinterpret_cast<uint4*>(out + c0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) o[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+          }
+          release();
+        }
+      } else if constexpr (SWIGLU) {
         // Drain this warp's chunks (at most two: BN = 128 and two warps per
         // lane quarter) into h = silu(gate) * up, release the accumulator so
         // the next tile's MMAs can start, then requantise from registers.
         static_assert(BN == 128 && kParts == 2, "two 32-token chunks per epilogue warp");
-        // h = silu(gate) * up of a chunk, computed in place over the gate
-        // registers (the warp holds one raw chunk and one finished one).
-        auto swiglu = [&](uint32_t (&g)[32], const uint32_t (&u)[32]) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float gf = __uint_as_float(g[i]) * scale;
-            const float uf = __uint_as_float(u[i]) * scale;
-            g[i] = __float_as_uint(gf * ptx::rcp_approx(1.0f + __expf(-gf)) * uf);
-          }
-        };
         // The accumulator is released once both chunks are in registers; the
         // second chunk's SwiGLU (bound by the special-function units) runs
         // after that.
@@ -739,12 +892,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
           ptx::tmem_ld_32x32b_x32(tbase + w + 32 * part + 64, u);
           ptx::tmem_ld_wait();
         }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          ptx::mbar_arrive(acce_bar(s0));
-          if (s1 >= 0) ptx::mbar_arrive(acce_bar(s1));
-        }
+        release();
         if (have1) swiglu(g, u);
         float hb[2][32];
 #pragma unroll
@@ -788,12 +936,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
                 out[(row0 + c0 + i) * n_out + f + kBM] = __float2bfloat16_rn(__uint_as_float(g[i]) * scale);
           }
         }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          ptx::mbar_arrive(acce_bar(s0));
-          if (s1 >= 0) ptx::mbar_arrive(acce_bar(s1));
-        }
+        release();
       }
       slots.done(s0, s1);
     }
@@ -859,7 +1002,7 @@ int stage_cap_from_env() {
   return cap;
 }
 
-template <int BN, int NA, bool SWIGLU, bool MX>
+template <int BN, int NA, bool SWIGLU, bool MX, bool TM = false>
 int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st) {
   using C = Cfg<BN, NA, SWIGLU>;
   // The whole opt-in shared memory is requested; the kernel sizes its stages
@@ -881,7 +1024,8 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
     return NVFP4MOE_ERR_CUDA;
   }
   cudaError_t err =
-      cudaFuncSetAttribute(grouped_gemm_kernel<BN, NA, SWIGLU, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+      cudaFuncSetAttribute(grouped_gemm_kernel<BN, NA, SWIGLU, MX, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(smem));
   if (err != cudaSuccess) {
     set_error_detail("cudaFuncSetAttribute: %s", cudaGetErrorString(err));
     return NVFP4MOE_ERR_CUDA;
@@ -909,7 +1053,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   // slower per tile, more than the few microseconds of launch latency it
   // hides.  The kernel still starts with griddepcontrol.wait (a no-op here),
   // so the kernel after it may be launched with the attribute.
-  grouped_gemm_kernel<BN, NA, SWIGLU, MX><<<num_sms, num_threads(SWIGLU), smem, st>>>(tw, ta, p);
+  grouped_gemm_kernel<BN, NA, SWIGLU, MX, TM><<<num_sms, num_threads(SWIGLU), smem, st>>>(tw, ta, p);
   err = cudaGetLastError();
   if (err != cudaSuccess) {
     set_error_detail("grouped GEMM launch: %s", cudaGetErrorString(err));
@@ -929,6 +1073,10 @@ int launch_format(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t s
   // loaded serves 256 output features (measured: the down GEMM at decode
   // 0.48 -> 0.30 ms, at 2048 rows per expert 4.02 -> 2.78 ms).
   const bool pair = a.N % (2 * kBM) == 0;
+  if (a.tile_n == NVFP4MOE_TILE_TOKEN_MAJOR && pair) {
+    if (swiglu) return launch_impl<128, 2, true, MX, true>(a, num_sms, smem_optin, st);
+    return launch_impl<128, 2, false, MX, true>(a, num_sms, smem_optin, st);
+  }
   if (swiglu && bn == 128) return launch_impl<128, 2, true, MX>(a, num_sms, smem_optin, st);
   if (!swiglu && bn == 128 && pair) return launch_impl<128, 2, false, MX>(a, num_sms, smem_optin, st);
   if (!swiglu && bn == 128) return launch_impl<128, 1, false, MX>(a, num_sms, smem_optin, st);

@@ -101,6 +101,9 @@ struct GemmArgs {
 };
 
 constexpr size_t kGemmWorkspaceBytes = 256;
+// tile_n = 0 picks token-major tiles from this many routed rows per expert
+// on average (m_total >= kTokenMajorMinRows * E).
+constexpr int64_t kTokenMajorMinRows = 256;
 
 // Returns 0 on success or an NVFP4MOE_ERR_* code (message via set_error_detail).
 int launch_grouped_gemm(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st);

@@ -272,6 +272,67 @@ def test_grouped_gemm_swiglu(B, E, I, K, counts, tile_n):
     U.check_requant(codes, scales, O.unpack_codes(rq), rs)
 
 
+TM = -1  # binding.TILE_TOKEN_MAJOR: 128 tokens as M, two 128-row weight tiles as one N = 256 operand
+TM_GEMM_SHAPES = [
+    # E, N, K, counts: partial token tiles, empty experts, several M tiles, a partial last K stage
+    (3, 256, 256, [5, 0, 40]),
+    (2, 512, 1024, [300, 17]),
+    (8, 256, 768, [0, 1, 2, 3, 130, 0, 31, 257]),
+    (2, 768, 320, [128, 129]),
+]
+
+
+@pytest.mark.parametrize("E,N,K,counts", TM_GEMM_SHAPES)
+def test_grouped_gemm_bf16_token_major(B, E, N, K, counts):
+    """Token-major tiles (tokens as M, N = 256 weight rows per MMA) against
+    the oracle: a partial token tile still computes 128 rows and stores only
+    the expert's."""
+    g, ref, pos, R = gemm_case(E, N, K, counts, seed=E * 1300 + K)
+    out = B.moe_grouped_gemm_nvfp4(g["a_packed"], g["a_scales"], g["a_gscale"], g["counts"], g["row_offsets"],
+                                   g["w_packed"], g["w_scales"], g["w_gscale"], B.EPI_BF16, m_total=R,
+                                   tile_n=B.TILE_TOKEN_MAJOR)
+    B.sync_status()
+    U.check_close(out.float().cpu().numpy()[pos], O.round_to_bf16(ref), what="bf16 GEMM, token-major")
+
+
+@pytest.mark.parametrize("E,I,K,counts", [(3, 128, 512, [9, 70, 0]), (2, 256, 320, [130, 1]),
+                                          (4, 128, 1024, [128, 5, 64, 200]), (2, 384, 256, [40, 41])])
+def test_grouped_gemm_swiglu_token_major(B, E, I, K, counts):
+    g, ref, pos, R = gemm_case(E, 2 * I, K, counts, seed=E * 701 + K)
+    h_ref = O.swiglu(ref, I)
+    args = (g["a_packed"], g["a_scales"], g["a_gscale"], g["counts"], g["row_offsets"], g["w_packed"],
+            g["w_scales"], g["w_gscale"])
+    hf = B.moe_grouped_gemm_nvfp4(*args, B.EPI_SWIGLU_F32, m_total=R, tile_n=B.TILE_TOKEN_MAJOR)
+    s_h = np.float32(2.0 ** -4)
+    hq, hs = B.moe_grouped_gemm_nvfp4(*args, B.EPI_SWIGLU_NVFP4, c_gscale=dev(torch.tensor([s_h])), m_total=R,
+                                      tile_n=B.TILE_TOKEN_MAJOR)
+    B.sync_status()
+    U.check_close(hf.cpu().numpy()[pos], h_ref, frob_tol=1e-5, elem_tol=1e-4, what="SwiGLU float32, token-major")
+    rq, rs = O.quantize_nvfp4(h_ref.astype(np.float32), s_h)
+    cap = hq.shape[0]
+    U.check_requant(O.unpack_codes(hq.cpu().numpy()[pos]), U.from_blocked(hs.cpu().numpy(), cap, I)[pos],
+                    O.unpack_codes(rq), rs)
+
+
+def test_grouped_gemm_token_major_chosen_automatically(B):
+    """tile_n = 0 picks token-major tiles once experts average 256 rows
+    (m_total >= 256 E); the result is the explicit token-major call's, bit for
+    bit, with the dynamic schedule as with static stripes."""
+    E, N, K, counts = 2, 512, 512, [300, 260]
+    g, ref, pos, R = gemm_case(E, N, K, counts, seed=91)
+    assert R >= 256 * E
+    args = (g["a_packed"], g["a_scales"], g["a_gscale"], g["counts"], g["row_offsets"], g["w_packed"],
+            g["w_scales"], g["w_gscale"])
+    ws = B.alloc_gemm_workspace(torch.device("cuda"))
+    auto = B.moe_grouped_gemm_nvfp4(*args, B.EPI_BF16, m_total=R, tile_n=0, workspace=ws)
+    tm = B.moe_grouped_gemm_nvfp4(*args, B.EPI_BF16, m_total=R, tile_n=B.TILE_TOKEN_MAJOR)
+    B.sync_status()
+    assert not ws.any().item()
+    rows = torch.from_numpy(pos).cuda()
+    assert torch.equal(auto[rows], tm[rows])
+    U.check_close(auto.float().cpu().numpy()[pos], O.round_to_bf16(ref), what="bf16 GEMM, automatic tiles")
+
+
 @pytest.mark.parametrize("E,N,K,counts,tile_n", GEMM_SHAPES[:4])
 def test_grouped_gemm_dynamic_schedule_matches_static(B, E, N, K, counts, tile_n):
     """Tiles claimed from the launch-wide counter give the same bits as the

@@ -122,14 +122,25 @@ def test_grouped_gemm_mx_bf16(B, E, N, K, counts, tile_n):
     U.check_close(out.float().cpu().numpy()[pos], O.round_to_bf16(ref), what="MXFP4 bf16 GEMM")
 
 
+@pytest.mark.parametrize("E,N,K,counts", [(3, 256, 256, [5, 0, 40]), (2, 256, 1024, [300, 17]),
+                                          (4, 512, 384, [1, 33, 64, 129])])
+def test_grouped_gemm_mx_bf16_token_major(B, E, N, K, counts):
+    g, ref, pos, R = gemm_case_mx(E, N, K, counts, seed=E * 170 + K)
+    out = B.moe_grouped_gemm_mxfp4(g["a_packed"], g["a_scales"], g["counts"], g["row_offsets"], g["w_packed"],
+                                   g["w_scales"], B.EPI_BF16, m_total=R, tile_n=B.TILE_TOKEN_MAJOR)
+    B.sync_status()
+    U.check_close(out.float().cpu().numpy()[pos], O.round_to_bf16(ref), what="MXFP4 bf16 GEMM, token-major")
+
+
+@pytest.mark.parametrize("tile_n", [0, -1])  # -1: binding.TILE_TOKEN_MAJOR
 @pytest.mark.parametrize("E,I,K,counts", [(3, 128, 512, [9, 70, 0]), (2, 256, 384, [130, 1]),
                                           (4, 128, 1024, [128, 5, 64, 200])])
-def test_grouped_gemm_mx_swiglu(B, E, I, K, counts):
+def test_grouped_gemm_mx_swiglu(B, E, I, K, counts, tile_n):
     g, ref, pos, R = gemm_case_mx(E, 2 * I, K, counts, seed=E * 31 + K)
     h_ref = O.swiglu(ref, I)
     args = (g["a_packed"], g["a_scales"], g["counts"], g["row_offsets"], g["w_packed"], g["w_scales"])
-    hf = B.moe_grouped_gemm_mxfp4(*args, B.EPI_SWIGLU_F32, m_total=R)
-    hq, hs = B.moe_grouped_gemm_mxfp4(*args, B.EPI_SWIGLU_MXFP4, m_total=R)
+    hf = B.moe_grouped_gemm_mxfp4(*args, B.EPI_SWIGLU_F32, m_total=R, tile_n=tile_n)
+    hq, hs = B.moe_grouped_gemm_mxfp4(*args, B.EPI_SWIGLU_MXFP4, m_total=R, tile_n=tile_n)
     B.sync_status()
     U.check_close(hf.cpu().numpy()[pos], h_ref, frob_tol=1e-5, elem_tol=1e-4, what="MXFP4 SwiGLU float32")
     rq, rs = O.quantize_mxfp4(h_ref.astype(np.float32))
