@@ -76,6 +76,10 @@ constexpr int kSfColBase = 256;    // scale-factor ring: columns 256..511
 constexpr int kSfRingCols = 256;
 constexpr int kMaxSfSlots = 8;
 constexpr int kMaxStages = 16;
+// Token-major bf16 epilogue: a 2 KB shared-memory buffer per epilogue warp
+// (32 rows x 64 bytes) from which a TMA store writes each chunk.
+constexpr int kOutChunkBytes = 2048;
+__host__ __device__ constexpr int out_stage_bytes(bool swiglu, bool tm) { return tm && !swiglu ? 4 * kOutChunkBytes : 0; }
 // mbarriers: full/empty per stage, acc full/empty per slot, drain, sf full/empty per ring slot,
 // the tile ring, and the scale copies of each stage
 // Ring of claimed tile ids (dynamic schedule): the producer claims ids from
@@ -375,7 +379,7 @@ __device__ __forceinline__ void requant_row32_mx(const uint32_t (&h)[32], int64_
 template <int BN, int NA, bool SWIGLU, bool MX, bool TM>
 __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
-                        const Params p) {
+                        const __grid_constant__ CUtensorMap tmap_c, const Params p) {
   using C = Cfg<BN, NA, SWIGLU>;
   static_assert(!TM || (BN == 128 && NA == 2), "token-major tiles: 128 tokens x two 128-row weight tiles");
   extern __shared__ uint8_t smem_raw[];
@@ -497,8 +501,9 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   const int off_b = C::NA * kATile;
   const int off_sfa = off_b + wmax * kBKBytes;
   const int off_sfb = off_sfa + C::NA * kSfTile;
-  const int S = min(p.stage_cap, (p.smem_bytes - ctrl) / stage);
+  const int S = min(p.stage_cap, (p.smem_bytes - ctrl - out_stage_bytes(SWIGLU, TM)) / stage);
   const uint32_t smem_base = ptx::smem_u32(smem) + uint32_t(ctrl);
+  const uint32_t out_base = smem_base + uint32_t(S * stage);  // token-major bf16 chunk buffers
 
   // The i-th tile of this CTA: the static stripe blockIdx.x + i * gridDim.x,
   // or (dynamic schedule) the i-th id the producer claimed, read from the
@@ -849,21 +854,40 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
             }
           }
         } else {
-          // bf16: columns c = output features mb * 256 + c, 64 bytes per chunk and row
+          // bf16: columns c = output features mb * 256 + c, 64 bytes per
+          // chunk and row.  A thread's row is 14 KB away from its neighbour's,
+          // so a chunk is staged in this warp's 2 KB buffer and written by a
+          // TMA store (full 64-byte row segments) when all 32 rows of the
+          // quarter belong to the expert; a partial quarter stores per thread
+          // and leaves the padding rows untouched.
+          const bool quarter_full = q * 32 + 32 <= valid;
+          const uint32_t obuf = out_base + uint32_t(q * kOutChunkBytes);
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.c_out) + row * n_out + mb * (C::NA * kBM);
 #pragma unroll 1
           for (int c0 = 0; c0 < C::NA * kBM; c0 += 32) {
             uint32_t g[32];
             ptx::tmem_ld_32x32b_x32(tbase + c0, g);
             ptx::tmem_ld_wait();
-            if (row_ok) {
-              uint32_t pk[16];
+            uint32_t pk[16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(g[2 * i]) * scale,
-                                                               __uint_as_float(g[2 * i + 1]) * scale);
-                pk[i] = *reinterpret_cast<const uint32_t*>(&v);
+            for (int i = 0; i < 16; ++i) {
+              const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(g[2 * i]) * scale,
+                                                             __uint_as_float(g[2 * i + 1]) * scale);
+              pk[i] = *reinterpret_cast<const uint32_t*>(&v);
+            }
+            if (quarter_full) {
+              if (lane == 0) ptx::bulk_wait_read_all();  // the previous chunk's store has read the buffer
+              __syncwarp();
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                ptx::sts128(obuf + uint32_t(lane * 64 + i * 16), pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              ptx::fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                ptx::tma_store_2d(&tmap_c, obuf, mb * (C::NA * kBM) + c0, int(row0 + q * 32));
+                ptx::bulk_commit();
               }
+            } else if (row_ok) {
               uint4* o = reinterpret_cast<uint4*>(out + c0);
 #pragma unroll
               for (int i = 0; i < 4; ++i) o[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
@@ -940,6 +964,9 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       }
       slots.done(s0, s1);
     }
+    if constexpr (TM && !SWIGLU) {
+      if (lane == 0) ptx::bulk_wait_all();  // this warp's TMA stores have completed
+    }
   }
 
   ptx::tc_fence_before();
@@ -991,6 +1018,21 @@ bool encode_kmajor_map(CUtensorMap* m, const void* base, int64_t rows, int64_t r
   return r == CUDA_SUCCESS;
 }
 
+// bf16 [rows, cols] output written by 32-row x 32-column TMA stores (64-byte
+// rows in shared memory, no swizzle).
+bool encode_bf16_store_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(cols * 2)};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Stage cap: NVFP4MOE_STAGE_CAP in the environment (2..16) overrides the
 // default of as many stages as fit, for pipeline-depth studies.
 int stage_cap_from_env() {
@@ -1010,16 +1052,19 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   // tile must fit.
   const int64_t usable = int64_t(smem_optin) - 1024 - ctrl_bytes(a.E);
   const int worst = C::stage_bytes(BN);
-  if (usable < 2 * int64_t(worst)) {
+  if (usable < 2 * int64_t(worst) + out_stage_bytes(SWIGLU, TM)) {
     set_error_detail(
         "grouped GEMM tile %dx%d (%s) needs %lld bytes of shared memory for a 2-stage pipeline; Hardware limit: %d",
-        kBM * NA, BN, SWIGLU ? "gate/up" : "down", (long long)(1024 + ctrl_bytes(a.E) + 2 * int64_t(worst)), smem_optin);
+        kBM * NA, BN, SWIGLU ? "gate/up" : "down",
+        (long long)(1024 + ctrl_bytes(a.E) + 2 * int64_t(worst) + out_stage_bytes(SWIGLU, TM)), smem_optin);
     return NVFP4MOE_ERR_SMEM;
   }
   const size_t smem = size_t(smem_optin);
-  CUtensorMap tw, ta;
+  CUtensorMap tw, ta, tc;
   if (!encode_kmajor_map(&tw, a.w_packed, int64_t(a.E) * a.N, a.K / 2, kBM) ||
-      !encode_kmajor_map(&ta, a.a_packed, a.rows_capacity, a.K / 2, 32)) {
+      !encode_kmajor_map(&ta, a.a_packed, a.rows_capacity, a.K / 2, 32) ||
+      !(out_stage_bytes(SWIGLU, TM) ? encode_bf16_store_map(&tc, a.c_out, a.rows_capacity, a.N)
+                                    : encode_kmajor_map(&tc, a.a_packed, a.rows_capacity, a.K / 2, 32))) {
     set_error_detail("cuTensorMapEncodeTiled failed or is unavailable");
     return NVFP4MOE_ERR_CUDA;
   }
@@ -1053,7 +1098,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   // slower per tile, more than the few microseconds of launch latency it
   // hides.  The kernel still starts with griddepcontrol.wait (a no-op here),
   // so the kernel after it may be launched with the attribute.
-  grouped_gemm_kernel<BN, NA, SWIGLU, MX, TM><<<num_sms, num_threads(SWIGLU), smem, st>>>(tw, ta, p);
+  grouped_gemm_kernel<BN, NA, SWIGLU, MX, TM><<<num_sms, num_threads(SWIGLU), smem, st>>>(tw, ta, tc, p);
   err = cudaGetLastError();
   if (err != cudaSuccess) {
     set_error_detail("grouped GEMM launch: %s", cudaGetErrorString(err));
