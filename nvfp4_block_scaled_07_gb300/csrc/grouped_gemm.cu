@@ -599,9 +599,9 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     // between two groups of MMAs (waits, commits, address arithmetic) leaves
     // it idle.  The loop therefore keeps that work small: ring positions are
     // wrap-around counters, both barriers of a stage are polled once with the
-    // bounded slow path out of line, and two K stages of a tile are waited
-    // for together and issued back to back (a probe on one SM: 904 -> 709
-    // cycles per 8 MMAs against 518 for MMAs alone).
+    // bounded slow path out of line, and (default orientation) two K stages
+    // of a tile are waited for together and issued back to back (a probe on
+    // one SM: 904 -> 709 cycles per 8 MMAs against 518 for MMAs alone).
     uint32_t s = 0, ph = 0;  // pipeline stage and its phase parity
     uint32_t r = 0, rph = 0;  // scale-factor ring slot and its parity
     SlotSeq slots;
@@ -653,8 +653,13 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
           for (int kb = 0; kb < nkb; ++kb) mma_block(kb);
         }
       };
-      for (int kt = 0; kt < nkt; kt += 2) {
-        const bool two = kt + 1 < nkt;
+      // Token-major stages carry four N = 256 MMAs each, which cover the
+      // per-round work, and each is issued as soon as it lands (waiting for a
+      // second stage measured 2 % slower on the down GEMM); the default
+      // orientation issues its N <= 128 MMAs two stages at a time.
+      constexpr bool kPairStages = !TM;
+      for (int kt = 0; kt < nkt; kt += kPairStages ? 2 : 1) {
+        const bool two = kPairStages && kt + 1 < nkt;
         uint32_t s2 = s + 1, ph2 = ph, r2 = r + 1, rph2 = rph;
         if (s2 == uint32_t(S)) s2 = 0, ph2 ^= 1u;
         if (r2 == uint32_t(C::SfSlots)) r2 = 0, rph2 ^= 1u;
