@@ -860,45 +860,58 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
           }
         } else {
           // bf16: columns c = output features mb * 256 + c, 64 bytes per
-          // chunk and row.  A thread's row is 14 KB away from its neighbour's,
-          // so a chunk is staged in this warp's 2 KB buffer and written by a
-          // TMA store (full 64-byte row segments) when all 32 rows of the
-          // quarter belong to the expert; a partial quarter stores per thread
-          // and leaves the padding rows untouched.
+          // chunk and row.  The whole row (256 columns) is packed to bf16 in
+          // registers, two chunks per tensor-memory round trip, and the
+          // accumulator released before any store.  A thread's row is 14 KB
+          // away from its neighbour's, so each chunk is staged in this warp's
+          // 2 KB buffer and written by a TMA store (full 64-byte row
+          // segments) when all 32 rows of the quarter belong to the expert;
+          // a partial quarter stores per thread and leaves the padding rows
+          // untouched.
+          constexpr int kChunks = C::NA * kBM / 32;
+          uint32_t pk[kChunks][16];
+#pragma unroll
+          for (int c = 0; c < kChunks; c += 2) {
+            uint32_t g0[32], g1[32];
+            ptx::tmem_ld_32x32b_x32(tbase + 32 * c, g0);
+            ptx::tmem_ld_32x32b_x32(tbase + 32 * c + 32, g1);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const __nv_bfloat162 v0 = __floats2bfloat162_rn(__uint_as_float(g0[2 * i]) * scale,
+                                                              __uint_as_float(g0[2 * i + 1]) * scale);
+              const __nv_bfloat162 v1 = __floats2bfloat162_rn(__uint_as_float(g1[2 * i]) * scale,
+                                                              __uint_as_float(g1[2 * i + 1]) * scale);
+              pk[c][i] = *reinterpret_cast<const uint32_t*>(&v0);
+              pk[c + 1][i] = *reinterpret_cast<const uint32_t*>(&v1);
+            }
+          }
+          release();
           const bool quarter_full = q * 32 + 32 <= valid;
           const uint32_t obuf = out_base + uint32_t(q * kOutChunkBytes);
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.c_out) + row * n_out + mb * (C::NA * kBM);
-#pragma unroll 1
-          for (int c0 = 0; c0 < C::NA * kBM; c0 += 32) {
-            uint32_t g[32];
-            ptx::tmem_ld_32x32b_x32(tbase + c0, g);
-            ptx::tmem_ld_wait();
-            uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(g[2 * i]) * scale,
-                                                             __uint_as_float(g[2 * i + 1]) * scale);
-              pk[i] = *reinterpret_cast<const uint32_t*>(&v);
-            }
+          for (int c = 0; c < kChunks; ++c) {
             if (quarter_full) {
               if (lane == 0) ptx::bulk_wait_read_all();  // the previous chunk's store has read the buffer
               __syncwarp();
 #pragma unroll
               for (int i = 0; i < 4; ++i)
-                ptx::sts128(obuf + uint32_t(lane * 64 + i * 16), pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                ptx::sts128(obuf + uint32_t(lane * 64 + i * 16), pk[c][4 * i], pk[c][4 * i + 1], pk[c][4 * i + 2],
+                            pk[c][4 * i + 3]);
               ptx::fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
-                ptx::tma_store_2d(&tmap_c, obuf, mb * (C::NA * kBM) + c0, int(row0 + q * 32));
+                ptx::tma_store_2d(&tmap_c, obuf, mb * (C::NA * kBM) + 32 * c, int(row0 + q * 32));
                 ptx::bulk_commit();
               }
             } else if (row_ok) {
-              uint4* o = reinterpret_cast<uint4*>(out + c0);
+              uint4* o = reinterpret_cast<uint4*>(out + 32 * c);
 #pragma unroll
-              for (int i = 0; i < 4; ++i) o[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              for (int i = 0; i < 4; ++i)
+                o[i] = make_uint4(pk[c][4 * i], pk[c][4 * i + 1], pk[c][4 * i + 2], pk[c][4 * i + 3]);
             }
           }
-          release();
         }
       } else if constexpr (SWIGLU) {
         // Drain this warp's chunks (at most two: BN = 128 and two warps per
