@@ -292,8 +292,8 @@ int moe_prepare(const float* logits, const float* bias, const void* x_bf16,
  * NVFP4MOE_TILE_TOKEN_MAJOR (N % 256 == 0): 128 tokens as M and two 128-row
  * weight tiles (gate and up, or two consecutive output blocks) as one
  * N = 256 operand, which reads each token tile once per K step (for experts
- * with hundreds of rows; a partial tile still computes 128 token rows).
- * 0: token-major when N % 256 == 0 and m_total >= 256 * E, else 128.
+ * with many rows; a partial tile still computes 128 token rows).
+ * 0: token-major when N % 256 == 0 and m_total >= 64 * E, else 128.
  * The results do not depend on tile_n beyond float32 summation order.
  * Limits: K % 64 == 0; N % 128 == 0 (BF16) or N % 256 == 0 (SwiGLU);
  * 1 <= E <= 1024; rows_capacity % 128 == 0.  A pipeline that does not fit the

@@ -102,8 +102,11 @@ struct GemmArgs {
 
 constexpr size_t kGemmWorkspaceBytes = 256;
 // tile_n = 0 picks token-major tiles from this many routed rows per expert
-// on average (m_total >= kTokenMajorMinRows * E).
-constexpr int64_t kTokenMajorMinRows = 256;
+// on average (m_total >= kTokenMajorMinRows * E).  Measured on GB300:
+// token-major is 10 % faster on the skewed 2048-token batch (64 rows per
+// expert on average, a few experts with hundreds) and 1 % slower at a
+// uniform 32 rows per expert, where its 128-token tiles are mostly padding.
+constexpr int64_t kTokenMajorMinRows = 64;
 
 // Returns 0 on success or an NVFP4MOE_ERR_* code (message via set_error_detail).
 int launch_grouped_gemm(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st);
