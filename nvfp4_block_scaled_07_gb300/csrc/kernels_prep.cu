@@ -538,7 +538,7 @@ __device__ __forceinline__ void place_rows(int64_t f0, int64_t step, int64_t R, 
                                            const int32_t* row_offsets, const uint8_t* xq, const uint8_t* xs, int H,
                                            int sf_groups, int32_t* __restrict__ perm_to_flat,
                                            int32_t* __restrict__ flat_to_perm, uint8_t* __restrict__ a_packed,
-                                           uint8_t* __restrict__ a_scales, int lane) {
+                                           uint8_t* __restrict__ a_scales, int lane, bool write_scales = true) {
   const int64_t f = f0 + int64_t(lane) * step;
   int64_t row = -1;
   if (f < R) {
@@ -570,6 +570,7 @@ __device__ __forceinline__ void place_rows(int64_t f0, int64_t step, int64_t R, 
         if (c < nv) dst[c] = v[u];
       }
     }
+    if (!write_scales) continue;  // uniform across the warp
     const unsigned* ssrc = reinterpret_cast<const unsigned*>(xs + t * (4 * int64_t(sf_groups)));
     for (int kb = lane; kb < sf_groups; kb += 32)
       *reinterpret_cast<uint32_t*>(a_scales + blocked_sf_offset(rj, kb, sf_groups)) = __ldcg(ssrc + kb);
@@ -809,9 +810,69 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
     for (int r = c + lane; r < pad; r += 32) p.perm_to_flat[ro + r] = -1;
   }
   for (int64_t q = int64_t(__ldcg(p.row_offsets + p.E)) + tid; q < p.rows_cap; q += nthreads) p.perm_to_flat[q] = -1;
+  // Large batches (long segments) write the rows' scales in phase E instead:
+  // scattered one 4-byte word per 512-byte block, they cost ~90 us of the
+  // prefill_t16384 prepare.
+  constexpr bool kScalesByBlock = ITERS * 32 > 256;
+  const int sfg = p.mx ? p.H / 128 : p.H / 64;  // 4-byte scale words per row
   for (int64_t f0 = gw0; f0 < R; f0 += 32 * gw_stride)
-    place_rows(f0, gw_stride, R, p.idx, p.k, p.E, ITERS * 32, p.rank, p.seg_base, p.row_offsets, p.xq, p.xs, p.H,
-               p.mx ? p.H / 128 : p.H / 64, p.perm_to_flat, p.flat_to_perm, p.a_packed, p.a_scales, lane);
+    place_rows(f0, gw_stride, R, p.idx, p.k, p.E, ITERS * 32, p.rank, p.seg_base, p.row_offsets, p.xq, p.xs, p.H, sfg,
+               p.perm_to_flat, p.flat_to_perm, p.a_packed, p.a_scales, lane, !kScalesByBlock);
+
+  // ---- E (large batches): row scales by destination block --------------------
+  // One warp per (128-row block, 16 scale words): lane i gathers the words of
+  // rows i, i + 32, i + 64, i + 96 of the block from the quantised token rows
+  // (perm_to_flat is complete after the barrier) and writes each 512-byte
+  // block's 16-byte row i, so a warp's stores are 512 contiguous bytes.
+  // Padding rows keep their bytes.
+  if constexpr (kScalesByBlock) {
+    if (!grid_barrier(p.bar, &s_ok)) return;
+    const int64_t nrb = int64_t(__ldcg(p.row_offsets + p.E)) / 128;
+    const int kchunks = (sfg + 15) / 16;
+    // 16-byte loads of 4 words when every row start is 16-byte aligned (xs
+    // itself need only be 4-byte aligned)
+    const bool vec = (sfg & 3) == 0 && (reinterpret_cast<uintptr_t>(p.xs) & 15) == 0;
+    const uint32_t* xs32 = reinterpret_cast<const uint32_t*>(p.xs);
+    for (int64_t item = gw0; item < nrb * kchunks; item += gw_stride) {
+      const int64_t rb = item / kchunks;
+      const int kb0 = int(item - rb * kchunks) * 16, kb1 = min(kb0 + 16, sfg);
+      int64_t src[4];
+      bool all = true;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int32_t f = __ldcg(p.perm_to_flat + rb * 128 + lane + 32 * j);
+        src[j] = f >= 0 ? int64_t(f / p.k) * sfg : -1;
+        all = all && f >= 0;
+      }
+      uint8_t* dst = p.a_scales + (rb * sfg) * 512 + lane * 16;
+      for (int kb = kb0; kb < kb1; kb += 4) {
+        uint32_t wv[4][4];  // [row j][word kb + u]
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (src[j] < 0) continue;
+          if (vec) {
+            const uint4 v = __ldcg(reinterpret_cast<const uint4*>(xs32 + src[j] + kb));
+            wv[j][0] = v.x, wv[j][1] = v.y, wv[j][2] = v.z, wv[j][3] = v.w;
+          } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) wv[j][u] = kb + u < kb1 ? __ldcg(xs32 + src[j] + kb + u) : 0u;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (kb + u >= kb1) break;
+          uint8_t* d = dst + int64_t(kb + u) * 512;
+          if (all) {
+            *reinterpret_cast<uint4*>(d) = make_uint4(wv[0][u], wv[1][u], wv[2][u], wv[3][u]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (src[j] >= 0) *reinterpret_cast<uint32_t*>(d + 4 * j) = wv[j][u];
+          }
+        }
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------

@@ -150,7 +150,7 @@ def test_grouped_gemm_mx_swiglu(B, E, I, K, counts, tile_n):
 
 
 @pytest.mark.parametrize("T,E,k,H,k0", [(16, 8, 2, 256, None), (128, 256, 8, 6144, None), (2100, 64, 8, 128, None),
-                                        (300, 16, 4, 512, 1), (1, 4, 2, 128, None)])
+                                        (2100, 64, 8, 512, None), (300, 16, 4, 512, 1), (1, 4, 2, 128, None)])
 def test_prepare_mx_matches_separate_calls_and_oracle(B, T, E, k, H, k0):
     rng = np.random.default_rng(T + H)
     lg = rng.standard_normal((T, E)).astype(np.float32)

@@ -40,7 +40,8 @@ CASES = [
     (33, 1, 1, 128, "softmax", True, False, False),      # one expert
     (40, 1024, 32, 64, "sigmoid", True, False, True),    # widest router (32 experts per lane), ties
     (700, 33, 5, 192, "sigmoid", False, True, True),     # ragged E, biased, unnormalised, ties
-    (2100, 64, 8, 128, "sigmoid", True, True, False),    # T*k = 16800: 1024-id segments
+    (2100, 64, 8, 128, "sigmoid", True, True, False),    # T*k = 16800: 1024-id segments, scales by block
+    (2100, 64, 8, 512, "sigmoid", True, False, False),   # the same with 16-byte scale gathers (8 words/row)
     (300, 4, 2, 1024, "softmax", True, False, False),    # few wide experts
 ]
 
