@@ -36,8 +36,9 @@
 //              for SwiGLU, two per lane quarter)
 //   last 4     scale factors: shared memory -> tensor memory (tcgen05.st)
 //              into a ring of slots the MMAs read their block scales from
-// Tiles are (expert, M tile, N tile) with N innermost, striped over the
-// CTAs, so the CTAs working at the same time share a weight tile through L2.
+// Tiles are (expert, M tile, N tile) with N innermost, so the CTAs working at
+// the same time share a weight tile through L2; experts with several token
+// tiles and experts with one alternate in the tile list (TileMap).
 //
 // Every mbarrier wait is bounded (2 s); on expiry the kernel raises a sticky
 // flag, drains its own copies and MMAs, frees tensor memory and returns.
@@ -84,7 +85,7 @@ __host__ __device__ constexpr int out_stage_bytes(bool swiglu, bool tm) { return
 // the tile ring, and the scale copies of each stage
 // Ring of claimed tile ids (dynamic schedule): the producer claims ids from
 // a launch-wide counter and passes them to the other roles.
-constexpr int kTileRing = 32;
+constexpr int kTileRing = 16;
 __host__ __device__ constexpr int tile_consumers(bool swiglu) { return 1 + 4 + epi_warps(swiglu); }  // MMA, SF and epilogue warps
 constexpr int kNumBars = 3 * kMaxStages + 5 + 2 * kMaxSfSlots + 2 * kTileRing;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -130,7 +131,7 @@ struct Cfg {
 // address, flags and the per-expert tile scan; stages start after it on a
 // 1024-byte boundary.
 __host__ __device__ constexpr int ctrl_bytes(int E) {
-  return (kNumBars * 8 + 16 + kTileRing * 4 + (3 * E + 1) * 4 + 1023) / 1024 * 1024;
+  return (kNumBars * 8 + 16 + kTileRing * 4 + (4 + 4 * E) * 4 + 1023) / 1024 * 1024;
 }
 
 // Bounded wait on an mbarrier phase.  SPIN polls with test_wait, which
@@ -177,20 +178,46 @@ __device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity) {
 
 // Tile t -> expert e, M tile mb, N tile nb and the tile's MMA width w: the
 // smallest power of two >= 32 covering the rows left, capped at BN.
-__device__ __forceinline__ void decode_tile(int t, const int* s_prefix, const int* s_count, int E, int BN, int& e,
-                                            int& mb, int& nb, int& w) {
-  int lo = 0, hi = E - 1;  // largest e with s_prefix[e] <= t (has >= 1 tile)
+// The launch's tile list.  Experts with two or more token tiles (their
+// weight tiles are re-read from L2 by every token tile: compute-heavy) form
+// class A, experts with one (each weight tile streamed from HBM once) class
+// B; each class lists its experts in index order and an expert's tiles M
+// tile by M tile, N (token) tile innermost.  Tile t alternates between the
+// classes (even t from A, odd from B) until the smaller one runs out, so on
+// a skewed batch the compute-heavy and the HBM-bound tiles run side by side
+// instead of in two phases; a batch of one class keeps plain expert order.
+struct TileMap {
+  const int* hdr;   // [0] class-A tiles, [1] class-B tiles, [2] class-A experts, [3] class-B experts
+  const int* pre;   // per position: first tile of the expert within its class
+  const int* expt;  // per position: expert id (class A first, then class B)
+  const int* count; // per expert: rows
+};
+
+// Tile t -> expert e, M tile mb, N tile nb and the tile's MMA width w: the
+// smallest power of two >= 32 covering the rows left, capped at BN.
+__device__ __forceinline__ void decode_tile(int t, const TileMap& m, int BN, int& e, int& mb, int& nb, int& w) {
+  const int tA = m.hdr[0], tB = m.hdr[1], nA = m.hdr[2], nB = m.hdr[3];
+  const int both = min(tA, tB);
+  int cls, local;
+  if (t < 2 * both) {
+    cls = t & 1;
+    local = t >> 1;
+  } else {
+    cls = tA > tB ? 0 : 1;
+    local = t - both;
+  }
+  int lo = cls ? nA : 0, hi = cls ? nA + nB - 1 : nA - 1;  // last position whose first tile <= local
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (s_prefix[mid] <= t) lo = mid;
+    if (m.pre[mid] <= local) lo = mid;
     else hi = mid - 1;
   }
-  e = lo;
-  const int ntn = (s_count[e] + BN - 1) / BN;
-  const int local = t - s_prefix[e];
-  mb = local / ntn;
-  nb = local - mb * ntn;
-  const int rem = s_count[e] - nb * BN;
+  e = m.expt[lo];
+  const int ntn = (m.count[e] + BN - 1) / BN;
+  const int in = local - m.pre[lo];
+  mb = in / ntn;
+  nb = in - mb * ntn;
+  const int rem = m.count[e] - nb * BN;
   w = 32;
   while (w < rem && w < BN) w <<= 1;
 }
@@ -389,9 +416,12 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_wmax = reinterpret_cast<int*>(tmem_slot + 2);
   volatile int* s_tq = reinterpret_cast<volatile int*>(tmem_slot + 4);   // claimed tile ids
-  int* s_prefix = reinterpret_cast<int*>(tmem_slot + 4 + kTileRing);
-  int* s_count = s_prefix + p.E + 1;
+  int* s_map = reinterpret_cast<int*>(tmem_slot + 4 + kTileRing);  // TileMap header
+  int* s_pre = s_map + 4;
+  int* s_expt = s_pre + p.E;
+  int* s_count = s_expt + p.E;
   int* s_rowoff = s_count + p.E;
+  const TileMap tiles{s_map, s_pre, s_expt, s_count};
   const int ctrl = ctrl_bytes(p.E);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -447,12 +477,13 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   if (warp == 2) {
-    // Per-expert tile counts and their exclusive scan, and the widest token
+    // The tile list (TileMap): per-expert token tiles, the class of each
+    // expert, each class's positions and tile prefixes, and the widest token
     // tile of the launch; experts whose rows would leave the padded buffers
     // are skipped and flagged.
     const int per = (p.E + 31) / 32;
     const int beg = min(lane * per, p.E), end = min(beg + per, p.E);
-    int sum = 0, wmax = 32;
+    int nA = 0, tA = 0, nB = 0, tB = 0, wmax = 32;
     for (int e = beg; e < end; ++e) {
       int c = p.counts[e];
       const int ro = p.row_offsets[e];
@@ -463,25 +494,35 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       }
       s_count[e] = c;
       s_rowoff[e] = ro;
-      sum += MT * ((c + BN - 1) / BN);
+      const int ntn = (c + BN - 1) / BN;
+      if (ntn >= 2) ++nA, tA += MT * ntn;
+      else if (ntn == 1) ++nB, tB += MT;
       int w = 32;
       while (w < c && w < BN) w <<= 1;
       if (c > 0) wmax = max(wmax, w);
     }
-    int incl = sum;
+    int inA = nA, itA = tA, inB = nB, itB = tB;  // inclusive scans over the lanes
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(kFull, incl, off);
-      if (lane >= off) incl += o;
+      const int a = __shfl_up_sync(kFull, inA, off), b = __shfl_up_sync(kFull, itA, off);
+      const int c = __shfl_up_sync(kFull, inB, off), d = __shfl_up_sync(kFull, itB, off);
+      if (lane >= off) inA += a, itA += b, inB += c, itB += d;
       wmax = max(wmax, __shfl_xor_sync(kFull, wmax, off));
     }
-    int run = incl - sum;
+    const int expertsA = __shfl_sync(kFull, inA, 31);
+    int posA = inA - nA, preA = itA - tA, posB = expertsA + inB - nB, preB = itB - tB;
     for (int e = beg; e < end; ++e) {
-      s_prefix[e] = run;
-      run += MT * ((s_count[e] + BN - 1) / BN);
+      const int ntn = (s_count[e] + BN - 1) / BN;
+      if (ntn >= 2) {
+        s_expt[posA] = e, s_pre[posA] = preA;
+        ++posA, preA += MT * ntn;
+      } else if (ntn == 1) {
+        s_expt[posB] = e, s_pre[posB] = preB;
+        ++posB, preB += MT;
+      }
     }
     if (lane == 31) {
-      s_prefix[p.E] = incl;
+      s_map[0] = itA, s_map[1] = itB, s_map[2] = inA, s_map[3] = inB;
       *s_wmax = wmax;
     }
   }
@@ -489,7 +530,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total = s_prefix[p.E];
+  const int total = s_map[0] + s_map[1];
   const int kblocks = p.K / 64;
   const int nkt = (kblocks + 3) / 4;
   const int sf_k = MX ? p.K / 128 : kblocks;     // 512-byte scale blocks along K per 128 rows
@@ -546,7 +587,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       if (t >= total) break;
       next = p.sched ? int(atomicAdd(p.sched, 1u)) : t + int(gridDim.x);
       int e, mb, nb, w;
-      decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
+      decode_tile(t, tiles, BN, e, mb, nb, w);
       if constexpr (TM) w = kBM;
       const int arow = s_rowoff[e] + nb * BN;
       const int sfb_chunks = w > 128 ? 2 : 1;
@@ -610,7 +651,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       const int t = next_tile(i, false);
       if (t < 0 || t >= total) break;
       int e, mb, nb, w;
-      decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
+      decode_tile(t, tiles, BN, e, mb, nb, w);
       if constexpr (TM) w = kBM;
       int s0, s1;
       slots.pick(C::NA * w, s0, s1);
@@ -720,7 +761,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       const int t = next_tile(i, true);
       if (t < 0 || t >= total) break;
       int e, mb, nb, w;
-      decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
+      decode_tile(t, tiles, BN, e, mb, nb, w);
       if constexpr (TM) w = kBM;
       const int sfb_chunks = w > 128 ? 2 : 1;
       for (int kt = 0; kt < nkt; ++kt) {
@@ -788,7 +829,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       const int t = next_tile(i, true);
       if (t < 0 || t >= total) break;
       int e, mb, nb, w;
-      decode_tile(t, s_prefix, s_count, p.E, BN, e, mb, nb, w);
+      decode_tile(t, tiles, BN, e, mb, nb, w);
       if constexpr (TM) w = kBM;
       int s0, s1;
       slots.pick(C::NA * w, s0, s1);
