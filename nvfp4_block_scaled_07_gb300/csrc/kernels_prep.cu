@@ -881,53 +881,72 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
 // Implementations", Context: the finalize epilogue).  Each thread owns 8
 // consecutive columns of one token and sums its k expert rows in slot order.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) finalize_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ f2p,
-                                                       const float* __restrict__ w, int T, int k, int H,
-                                                       int64_t rows_capacity, uint4* __restrict__ out) {
+constexpr int kFinThreads = 128;
+
+// A CTA covers 256 consecutive 8-column groups of one token; a thread sums
+// two of them (c and c + 128), so its k row indices and weights are read once
+// for both and up to 16 row loads are in flight together.  The sum still
+// runs in slot order for every element.
+__global__ void __launch_bounds__(kFinThreads) finalize_kernel(const uint4* __restrict__ y,
+                                                               const int32_t* __restrict__ f2p,
+                                                               const float* __restrict__ w, int T, int k, int H,
+                                                               int64_t rows_capacity, uint4* __restrict__ out) {
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   const int t = blockIdx.x;
-  const int c8 = blockIdx.y * blockDim.x + threadIdx.x;  // column group of 8
-  if (c8 * 8 >= H) return;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  // Up to 8 slots at a time: their row indices, then their rows, are loaded
-  // together; the sum still runs in slot order.
+  const int ncg = H / 8;  // 8-column groups of a row
+  const int ca = blockIdx.y * (2 * kFinThreads) + threadIdx.x;
+  if (ca >= ncg) return;
+  const int cb = ca + kFinThreads;
+  const bool has_b = cb < ncg;
+  float acc[2][8] = {};
   for (int j0 = 0; j0 < k; j0 += 8) {
     const int n = min(8, k - j0);
     int64_t row[8];
     float wj[8];
-    uint4 q[8];
+    uint4 q[2][8];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
       if (j < n) {
-        row[j] = f2p[int64_t(t) * k + j0 + j];
-        wj[j] = w[int64_t(t) * k + j0 + j];
+        row[j] = __ldg(f2p + int64_t(t) * k + j0 + j);
+        wj[j] = __ldg(w + int64_t(t) * k + j0 + j);
       }
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      if (j < n && row[j] >= 0 && row[j] < rows_capacity) q[j] = y[(row[j] * H) / 8 + c8];
+      if (j < n && row[j] >= 0 && row[j] < rows_capacity) {
+        q[0][j] = y[row[j] * ncg + ca];
+        if (has_b) q[1][j] = y[row[j] * ncg + cb];
+      }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (j >= n) break;
       if (row[j] < 0 || row[j] >= rows_capacity) {
-        if (c8 == 0) atomicOr(&g_prep_flags, kFlagBadData);
+        if (ca == 0) atomicOr(&g_prep_flags, kFlagBadData);
         continue;
       }
-      const uint32_t v[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[2 * i] = fmaf(wj[j], bf16_lo(v[i]), acc[2 * i]);
-        acc[2 * i + 1] = fmaf(wj[j], bf16_hi(v[i]), acc[2 * i + 1]);
+      for (int h = 0; h < 2; ++h) {
+        if (h == 1 && !has_b) break;
+        const uint32_t v[4] = {q[h][j].x, q[h][j].y, q[h][j].z, q[h][j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[h][2 * i] = fmaf(wj[j], bf16_lo(v[i]), acc[h][2 * i]);
+          acc[h][2 * i + 1] = fmaf(wj[j], bf16_hi(v[i]), acc[h][2 * i + 1]);
+        }
       }
     }
   }
-  uint32_t o[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __nv_bfloat162 p = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);  // .x = low half
-    o[i] = *reinterpret_cast<const uint32_t*>(&p);
+  for (int h = 0; h < 2; ++h) {
+    if (h == 1 && !has_b) break;
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 p = __floats2bfloat162_rn(acc[h][2 * i], acc[h][2 * i + 1]);  // .x = low half
+      o[i] = *reinterpret_cast<const uint32_t*>(&p);
+    }
+    out[int64_t(t) * ncg + (h ? cb : ca)] = make_uint4(o[0], o[1], o[2], o[3]);
   }
-  out[(int64_t(t) * H) / 8 + c8] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 int grid_for(int64_t work_items, int threads, int num_sms, int per_sm) {
@@ -1138,7 +1157,7 @@ cudaError_t launch_prepare(const float* logits, const float* bias, const void* x
 cudaError_t launch_finalize(const void* y, const int32_t* flat_to_perm, const float* w, int T, int k, int H,
                             int64_t rows_capacity, void* out, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  const dim3 block(128), grid(T, (H / 8 + 127) / 128);
+  const dim3 block(kFinThreads), grid(T, (H / 8 + 2 * kFinThreads - 1) / (2 * kFinThreads));
   return launch_kernel(finalize_kernel, grid, block, 0, st, false, static_cast<const uint4*>(y), flat_to_perm, w, T,
                        k, H, rows_capacity, static_cast<uint4*>(out));
 }
