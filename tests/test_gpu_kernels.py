@@ -230,6 +230,7 @@ GEMM_SHAPES = [
     (2, 512, 2048, [64, 64], 0),
     (8, 256, 768, [0, 1, 2, 3, 130, 0, 31, 257], 0),
     (3, 128, 512, [256, 129, 96], 256),           # 256, 128 + 32 ... under the 256 cap
+    (6, 256, 512, [200, 1, 2, 3, 4, 5], 0),       # tile order: one multi-tile expert among single-tile ones
 ]
 
 
@@ -279,6 +280,7 @@ TM_GEMM_SHAPES = [
     (2, 512, 1024, [300, 17]),
     (8, 256, 768, [0, 1, 2, 3, 130, 0, 31, 257]),
     (2, 768, 320, [128, 129]),
+    (6, 256, 512, [200, 1, 2, 3, 4, 5]),          # more single-tile than multi-tile work
 ]
 
 
