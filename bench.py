@@ -248,7 +248,8 @@ def run_ours(args, w):
     inp = W.device_inputs(w, seed=args.seed + rank, device=dev)
     layer = B.MoELayer(inp["w_gu"], inp["w_d"], w.k, w.score, w.renormalize, w.h_scale, bias=inp["bias"],
                        T=w.T, tile_n=(args.tile_gate_up, args.tile_down), fused_prepare=not args.separate_prepare,
-                       k_primary=args.k_primary, fmt=args.format, dynamic_schedule=not args.static_schedule)
+                       k_primary=args.k_primary, fmt=args.format, dynamic_schedule=not args.static_schedule,
+                       tiled_weights=args.weights == "tiled")
     del inp["w_gu"], inp["w_d"]
     torch.cuda.empty_cache()
     x, logits = inp["x"], inp["logits"]
@@ -347,6 +348,7 @@ def run_ours(args, w):
         "prepare": "fused (one launch)" if layer.fused_prepare else "separate (route, quantise, permute)",
         "routing": "top-k" if layer.k_primary == w.k else f"batch-aware, k_primary={layer.k_primary}",
         "gemm_schedule": "dynamic" if layer.g_ws is not None else "static",
+        "weights": "tiled" if isinstance(layer.w_gu_packed, B.TiledWeights) else "row-major",
         "roofline": {"kernel": "gemm_gate_up_swiglu", "bound": bound, "achieved": round(achieved, 1),
                      "peak": round(peak, 1), "unit": unit, "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic(w.name, "gemm_gate_up_swiglu") if layer.fmt == "nvfp4" else None,
@@ -511,6 +513,8 @@ def main():
                     help="batch-aware routing: experts each token keeps by its own scores (default k: plain top-k)")
     ap.add_argument("--format", choices=["nvfp4", "mxfp4"], default="nvfp4",
                     help="operand format of the layer (mxfp4: E8M0 scale per 32 elements, no per-tensor scales)")
+    ap.add_argument("--weights", choices=["tiled", "rowmajor"], default="tiled",
+                    help="expert weight layout of the grouped GEMMs (tiled: each 128 x 128-byte box contiguous)")
     ap.add_argument("--static-schedule", action="store_true",
                     help="grouped GEMMs on static tile stripes instead of the dynamic tile counter")
     ap.add_argument("--separate-prepare", action="store_true",

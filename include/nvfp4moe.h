@@ -106,6 +106,26 @@ size_t nvfp4moe_blocked_scales_bytes(int64_t rows, int64_t cols);
 /* Bytes of an MXFP4 blocked scale buffer (see the MXFP4 section): 0 unless cols % 128 == 0. */
 size_t nvfp4moe_mxfp4_blocked_scales_bytes(int64_t rows, int64_t cols);
 
+/* Tiled weight layout (NVFP4MOE_W_TILED), an offline re-layout of packed
+ * E2M1 weights (NVFP4 or MXFP4 codes alike) for the grouped GEMM: the
+ * grouped GEMM reads a weight tile 128 rows x 128 bytes at a time, which in
+ * the row-major layout are 128 strips K/2 bytes apart; tiled, each such box
+ * is 16384 contiguous bytes (measured on GB300: 6.9 TB/s for the strided
+ * boxes of a 3 KB-row matrix, 7.2 TB/s contiguous).  For packed [rows, K/2]
+ * (rows % 128 == 0, K % 64 == 0), KC = ceil(K / 256): block (rb, kc), rb <
+ * rows / 128, kc < KC, starts at byte (rb * KC + kc) * 16384 and holds
+ * bytes [kc * 128, kc * 128 + 128) of rows rb * 128 .. rb * 128 + 127, row by
+ * row; bytes past K/2 are zero.  Scales keep their layout. */
+#define NVFP4MOE_W_ROWMAJOR 0
+#define NVFP4MOE_W_TILED    1
+/* Bytes of the tiled copy of a [rows, K/2] packed matrix; 0 on bad input. */
+size_t nvfp4moe_tiled_weights_bytes(int64_t rows, int K);
+/* Writes the tiled copy of w_packed (device uint8 [rows, K/2], 16-byte
+ * aligned) to w_tiled (device, nvfp4moe_tiled_weights_bytes bytes, 16-byte
+ * aligned), asynchronously on `stream`.  Returns OK, INVALID_ARG,
+ * UNSUPPORTED (rows % 128 or K % 64) or CUDA. */
+int nvfp4moe_tile_weights(const uint8_t* w_packed, int64_t rows, int K, uint8_t* w_tiled, cudaStream_t stream);
+
 /* ---- a1: routing ---------------------------------------------------------
  * Top-k expert selection with sigmoid scoring (page A, key finding 8 and its
  * closing paragraph: "OEA with proper sigmoid scoring" of the GLM-5 router)
@@ -282,7 +302,9 @@ int moe_prepare(const float* logits, const float* bias, const void* x_bf16,
  * a_gscale device float32 [1]; expert_counts / row_offsets device int32 as
  * written by moe_permute; w_packed device uint8 [E, N, K/2]; w_scales
  * device, blocked per expert ([E] x nvfp4moe_blocked_scales_bytes(N, K));
- * w_gscale device float32 [E].
+ * w_gscale device float32 [E].  w_layout: NVFP4MOE_W_ROWMAJOR (w_packed as
+ * above) or NVFP4MOE_W_TILED (w_packed is nvfp4moe_tile_weights of that
+ * [E*N, K/2] matrix; the same results).
  * m_total = number of routed rows (T*k); it only guides the choice of tiles.
  * tile_n selects the tile orientation.  128, or 256 with NVFP4MOE_EPI_BF16:
  * the widest token tile with weight rows as the MMA's 128-row M side; token
@@ -313,7 +335,7 @@ int moe_grouped_gemm_nvfp4(const uint8_t* a_packed, const uint8_t* a_scales, con
                            int E, int64_t rows_capacity, int64_t m_total,
                            const uint8_t* w_packed, const uint8_t* w_scales, const float* w_gscale,
                            int N, int K, int epilogue, const float* c_gscale,
-                           void* c_out, uint8_t* c_scales, int tile_n,
+                           void* c_out, uint8_t* c_scales, int tile_n, int w_layout,
                            void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ---- MXFP4 variant of a2, a3, a4/a5 -----------------------------------------
@@ -370,7 +392,7 @@ int moe_grouped_gemm_mxfp4(const uint8_t* a_packed, const uint8_t* a_scales,
                            int E, int64_t rows_capacity, int64_t m_total,
                            const uint8_t* w_packed, const uint8_t* w_scales,
                            int N, int K, int epilogue, void* c_out, uint8_t* c_scales, int tile_n,
-                           void* ws, size_t ws_bytes, cudaStream_t stream);
+                           int w_layout, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ---- a6: finalize ----------------------------------------------------------
  * Router-weighted reduce back to token order (page A, section 6: "token

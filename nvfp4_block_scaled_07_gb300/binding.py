@@ -33,6 +33,7 @@ QUANT_COMPUTE_GLOBAL = 1
 QUANT_SCALES_BLOCKED = 2
 EPI_BF16, EPI_SWIGLU_NVFP4, EPI_SWIGLU_F32, EPI_SWIGLU_MXFP4 = 0, 1, 2, 3
 TILE_TOKEN_MAJOR = -1  # grouped GEMM tile_n: 128 tokens as M, two weight tiles as one N = 256 operand
+W_ROWMAJOR, W_TILED = 0, 1  # grouped GEMM weight layouts
 
 _i, _i64, _sz, _p, _f = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
 _SIGS = {
@@ -47,7 +48,9 @@ _SIGS = {
     "moe_permute_mxfp4": (_i, [_p, _i, _i, _i, _p, _p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
     "moe_prepare_mxfp4": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p,
                                _p, _sz, _p]),
-    "moe_grouped_gemm_mxfp4": (_i, [_p, _p, _p, _p, _i, _i64, _i64, _p, _p, _i, _i, _i, _p, _p, _i, _p, _sz, _p]),
+    "moe_grouped_gemm_mxfp4": (_i, [_p, _p, _p, _p, _i, _i64, _i64, _p, _p, _i, _i, _i, _p, _p, _i, _i, _p, _sz, _p]),
+    "nvfp4moe_tiled_weights_bytes": (_sz, [_i64, _i]),
+    "nvfp4moe_tile_weights": (_i, [_p, _i64, _i, _p, _p]),
     "moe_route_topk": (_i, [_p, _p, _i, _i, _i, _i, _i, _p, _p, _p]),
     "moe_route_batch_aware_workspace_size": (_sz, [_i]),
     "moe_route_batch_aware": (_i, [_p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _sz, _p]),
@@ -63,7 +66,7 @@ _SIGS = {
                          _p, _sz, _p]),
     "moe_grouped_gemm_nvfp4_workspace_size": (_sz, [_i, _i, _i, _i]),
     "moe_grouped_gemm_nvfp4": (_i, [_p, _p, _p, _p, _p, _i, _i64, _i64, _p, _p, _p, _i, _i, _i, _p, _p, _p, _i,
-                                    _p, _sz, _p]),
+                                    _i, _p, _sz, _p]),
     "moe_finalize": (_i, [_p, _p, _p, _i, _i, _i, _i64, _p, _p]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -252,6 +255,38 @@ def quantize_expert_weights_mx(w):
     for e in range(E):
         moe_quantize_mxfp4(w[e], blocked=True, packed=packed[e], scales=scales[e])
     return packed, scales
+
+
+@dataclass
+class TiledWeights:
+    """Packed expert weights [E, N, K/2] in the tiled layout (nvfp4moe_tile_weights):
+    each 128-row x 128-byte box the grouped GEMM loads is contiguous."""
+    data: torch.Tensor  # uint8, nvfp4moe_tiled_weights_bytes(E * N, K) bytes
+    E: int
+    N: int
+    K: int
+
+
+def tile_expert_weights(packed):
+    """Packed [E, N, K/2] (NVFP4 or MXFP4 codes) -> TiledWeights."""
+    _need(packed, torch.uint8, name="packed")
+    E, N, Kh = packed.shape
+    K = 2 * Kh
+    n = int(_lib.nvfp4moe_tiled_weights_bytes(E * N, K))
+    if n == 0:
+        raise ValueError(f"cannot tile [{E}, {N}, {Kh}] (E*N % 128, K % 64)")
+    out = _empty((n,), torch.uint8, packed.device)
+    _check(_lib.nvfp4moe_tile_weights(_ptr(packed), E * N, K, _ptr(out), _stream()), "nvfp4moe_tile_weights")
+    return TiledWeights(out, E, N, K)
+
+
+def _weights_args(w_packed):
+    """(E, N, K, pointer, layout) of row-major packed weights or TiledWeights."""
+    if isinstance(w_packed, TiledWeights):
+        return w_packed.E, w_packed.N, w_packed.K, _ptr(w_packed.data), W_TILED
+    _need(w_packed, torch.uint8, name="w_packed")
+    E, N, Kh = w_packed.shape
+    return E, N, 2 * Kh, _ptr(w_packed), W_ROWMAJOR
 
 
 # ---- a3 ------------------------------------------------------------------------
@@ -445,9 +480,9 @@ def moe_grouped_gemm_nvfp4(a_packed, a_scales, a_gscale, counts, row_offsets, w_
                            epilogue=EPI_BF16, c_gscale=None, m_total=None, tile_n=0, out=None, out_scales=None,
                            workspace=None):
     """Returns c_out (and c_scales for EPI_SWIGLU_NVFP4).  workspace: a zeroed
-    alloc_gemm_workspace() for the dynamic tile schedule, None for static."""
-    E, N, Kh = w_packed.shape
-    K = 2 * Kh
+    alloc_gemm_workspace() for the dynamic tile schedule, None for static.
+    w_packed: row-major [E, N, K/2] or TiledWeights."""
+    E, N, K, w_ptr, w_layout = _weights_args(w_packed)
     cap = a_packed.shape[0]
     dev = a_packed.device
     _need(a_packed, torch.uint8, (cap, K // 2), "a_packed")
@@ -455,7 +490,6 @@ def moe_grouped_gemm_nvfp4(a_packed, a_scales, a_gscale, counts, row_offsets, w_
     _need(a_gscale, torch.float32, (1,), "a_gscale")
     _need(counts, torch.int32, (E,), "counts")
     _need(row_offsets, torch.int32, (E + 1,), "row_offsets")
-    _need(w_packed, torch.uint8, name="w_packed")
     _need(w_scales, torch.uint8, name="w_scales")
     _need(w_gscale, torch.float32, (E,), "w_gscale")
     if a_scales.numel() < blocked_scales_bytes(cap, K) or w_scales.numel() < E * blocked_scales_bytes(N, K):
@@ -483,25 +517,24 @@ def moe_grouped_gemm_nvfp4(a_packed, a_scales, a_gscale, counts, row_offsets, w_
         m_total = cap
     ws_p, ws_n = _ws_args(workspace)
     _check(_lib.moe_grouped_gemm_nvfp4(_ptr(a_packed), _ptr(a_scales), _ptr(a_gscale), _ptr(counts),
-                                       _ptr(row_offsets), E, cap, int(m_total), _ptr(w_packed), _ptr(w_scales),
+                                       _ptr(row_offsets), E, cap, int(m_total), w_ptr, _ptr(w_scales),
                                        _ptr(w_gscale), N, K, epilogue, _ptr(c_gscale), _ptr(out),
-                                       _ptr(out_scales), int(tile_n), ws_p, ws_n, _stream()),
+                                       _ptr(out_scales), int(tile_n), w_layout, ws_p, ws_n, _stream()),
            "moe_grouped_gemm_nvfp4")
     return (out, out_scales) if epilogue == EPI_SWIGLU_NVFP4 else out
 
 
 def moe_grouped_gemm_mxfp4(a_packed, a_scales, counts, row_offsets, w_packed, w_scales, epilogue=EPI_BF16,
                            m_total=None, tile_n=0, out=None, out_scales=None, workspace=None):
-    """MXFP4 grouped GEMM.  Returns c_out (and c_scales for EPI_SWIGLU_MXFP4)."""
-    E, N, Kh = w_packed.shape
-    K = 2 * Kh
+    """MXFP4 grouped GEMM.  Returns c_out (and c_scales for EPI_SWIGLU_MXFP4).
+    w_packed: row-major [E, N, K/2] or TiledWeights."""
+    E, N, K, w_ptr, w_layout = _weights_args(w_packed)
     cap = a_packed.shape[0]
     dev = a_packed.device
     _need(a_packed, torch.uint8, (cap, K // 2), "a_packed")
     _need(a_scales, torch.uint8, name="a_scales")
     _need(counts, torch.int32, (E,), "counts")
     _need(row_offsets, torch.int32, (E + 1,), "row_offsets")
-    _need(w_packed, torch.uint8, name="w_packed")
     _need(w_scales, torch.uint8, name="w_scales")
     if a_scales.numel() < blocked_scales_bytes(cap, K, "mxfp4") or \
             w_scales.numel() < E * blocked_scales_bytes(N, K, "mxfp4"):
@@ -525,8 +558,8 @@ def moe_grouped_gemm_mxfp4(a_packed, a_scales, counts, row_offsets, w_packed, w_
         m_total = cap
     ws_p, ws_n = _ws_args(workspace)
     _check(_lib.moe_grouped_gemm_mxfp4(_ptr(a_packed), _ptr(a_scales), _ptr(counts), _ptr(row_offsets), E, cap,
-                                       int(m_total), _ptr(w_packed), _ptr(w_scales), N, K, epilogue, _ptr(out),
-                                       _ptr(out_scales), int(tile_n), ws_p, ws_n, _stream()),
+                                       int(m_total), w_ptr, _ptr(w_scales), N, K, epilogue, _ptr(out),
+                                       _ptr(out_scales), int(tile_n), w_layout, ws_p, ws_n, _stream()),
            "moe_grouped_gemm_mxfp4")
     return (out, out_scales) if epilogue == EPI_SWIGLU_MXFP4 else out
 
@@ -557,7 +590,8 @@ class MoELayer:
     finalize -- otherwise the six separate calls."""
 
     def __init__(self, w_gu, w_d, k, score_fn="sigmoid", renormalize=True, h_scale=2.0 ** -4, bias=None,
-                 T=None, tile_n=(0, 0), fused_prepare=True, k_primary=None, fmt="nvfp4", dynamic_schedule=True):
+                 T=None, tile_n=(0, 0), fused_prepare=True, k_primary=None, fmt="nvfp4", dynamic_schedule=True,
+                 tiled_weights=True):
         if fmt not in ("nvfp4", "mxfp4"):
             raise ValueError(f"fmt {fmt}")
         self.fmt = fmt
@@ -579,6 +613,11 @@ class MoELayer:
         else:
             self.w_gu_packed, self.w_gu_scales, self.w_gu_gscale = quantize_expert_weights(w_gu)
             self.w_d_packed, self.w_d_scales, self.w_d_gscale = quantize_expert_weights(w_d)
+        # Tiled weights: each GEMM weight box is one contiguous 16 KB block, which
+        # streams faster from HBM (the row-major copies are freed).
+        if tiled_weights:
+            self.w_gu_packed = tile_expert_weights(self.w_gu_packed)
+            self.w_d_packed = tile_expert_weights(self.w_d_packed)
         self.h_scale = torch.full((1,), h_scale, dtype=torch.float32, device=self.device)
         self.T = None
         if T is not None:

@@ -142,6 +142,22 @@ size_t nvfp4moe_mxfp4_blocked_scales_bytes(int64_t rows, int64_t cols) {
   return size_t(ceil_div(rows, 128) * 128 * (cols / 32));
 }
 
+size_t nvfp4moe_tiled_weights_bytes(int64_t rows, int K) {
+  if (rows <= 0 || rows % 128 || K <= 0 || K % 64) return 0;
+  return size_t((rows / 128) * ceil_div(int64_t(K), 256) * kWeightBoxBytes);
+}
+
+int nvfp4moe_tile_weights(const uint8_t* w_packed, int64_t rows, int K, uint8_t* w_tiled, cudaStream_t stream) {
+  t_detail[0] = 0;
+  NVFP4MOE_REQUIRE(rows > 0 && rows % 128 == 0 && K > 0 && K % 64 == 0, NVFP4MOE_ERR_UNSUPPORTED,
+                   "rows = %lld must be a positive multiple of 128 and K = %d of 64", (long long)rows, K);
+  NVFP4MOE_REQUIRE(w_packed && w_tiled && aligned16(w_packed) && aligned16(w_tiled), NVFP4MOE_ERR_INVALID_ARG,
+                   "null or misaligned pointer");
+  DeviceInfo d;
+  if (int st = current_device(&d)) return st;
+  return cuda_status(launch_tile_weights(w_packed, rows, K, w_tiled, d.num_sms, stream), "tile weights launch");
+}
+
 // ---- a1 ---------------------------------------------------------------------
 int moe_route_topk(const float* logits, const float* bias, int T, int E, int k, int score_fn, int renormalize,
                    int32_t* topk_idx, float* topk_w, cudaStream_t stream) {
@@ -427,8 +443,11 @@ static int grouped_gemm_common(bool mx, const uint8_t* a_packed, const uint8_t* 
                                const int32_t* expert_counts, const int32_t* row_offsets, int E, int64_t rows_capacity,
                                int64_t m_total, const uint8_t* w_packed, const uint8_t* w_scales,
                                const float* w_gscale, int N, int K, int epilogue, const float* c_gscale, void* c_out,
-                               uint8_t* c_scales, int tile_n, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                               uint8_t* c_scales, int tile_n, int w_layout, void* ws, size_t ws_bytes,
+                               cudaStream_t stream) {
   t_detail[0] = 0;
+  NVFP4MOE_REQUIRE(w_layout == NVFP4MOE_W_ROWMAJOR || w_layout == NVFP4MOE_W_TILED, NVFP4MOE_ERR_INVALID_ARG,
+                   "w_layout %d", w_layout);
   NVFP4MOE_REQUIRE(!ws || (ws_bytes >= kGemmWorkspaceBytes && (reinterpret_cast<uintptr_t>(ws) & 255) == 0),
                    NVFP4MOE_ERR_WORKSPACE, "workspace must be NULL or %zu bytes, 256-byte aligned (got %zu)",
                    kGemmWorkspaceBytes, ws_bytes);
@@ -486,6 +505,7 @@ static int grouped_gemm_common(bool mx, const uint8_t* a_packed, const uint8_t* 
   // tile_n = 0: token-major tiles once experts average kTokenMajorMinRows rows
   a.tile_n = tile_n == 0 && N % 256 == 0 && m_total >= kTokenMajorMinRows * E ? NVFP4MOE_TILE_TOKEN_MAJOR : tile_n;
   a.mx = mx;
+  a.w_tiled = w_layout == NVFP4MOE_W_TILED;
   a.sched = ws;
   return launch_grouped_gemm(a, d.num_sms, d.smem_optin, stream);  // detail already set on failure
 }
@@ -494,19 +514,21 @@ int moe_grouped_gemm_nvfp4(const uint8_t* a_packed, const uint8_t* a_scales, con
                            const int32_t* expert_counts, const int32_t* row_offsets, int E, int64_t rows_capacity,
                            int64_t m_total, const uint8_t* w_packed, const uint8_t* w_scales,
                            const float* w_gscale, int N, int K, int epilogue, const float* c_gscale, void* c_out,
-                           uint8_t* c_scales, int tile_n, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                           uint8_t* c_scales, int tile_n, int w_layout, void* ws, size_t ws_bytes,
+                           cudaStream_t stream) {
   return grouped_gemm_common(false, a_packed, a_scales, a_gscale, expert_counts, row_offsets, E, rows_capacity,
                              m_total, w_packed, w_scales, w_gscale, N, K, epilogue, c_gscale, c_out, c_scales, tile_n,
-                             ws, ws_bytes, stream);
+                             w_layout, ws, ws_bytes, stream);
 }
 
 int moe_grouped_gemm_mxfp4(const uint8_t* a_packed, const uint8_t* a_scales, const int32_t* expert_counts,
                            const int32_t* row_offsets, int E, int64_t rows_capacity, int64_t m_total,
                            const uint8_t* w_packed, const uint8_t* w_scales, int N, int K, int epilogue, void* c_out,
-                           uint8_t* c_scales, int tile_n, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                           uint8_t* c_scales, int tile_n, int w_layout, void* ws, size_t ws_bytes,
+                           cudaStream_t stream) {
   return grouped_gemm_common(true, a_packed, a_scales, nullptr, expert_counts, row_offsets, E, rows_capacity, m_total,
-                             w_packed, w_scales, nullptr, N, K, epilogue, nullptr, c_out, c_scales, tile_n, ws,
-                             ws_bytes, stream);
+                             w_packed, w_scales, nullptr, N, K, epilogue, nullptr, c_out, c_scales, tile_n, w_layout,
+                             ws, ws_bytes, stream);
 }
 
 // ---- a6 ---------------------------------------------------------------------

@@ -53,6 +53,7 @@
 #include "../../include/nvfp4moe.h"
 #include "common.cuh"
 #include "internal.h"
+#include "launch.cuh"
 #include "sm103_ptx.cuh"
 
 namespace nvfp4moe {
@@ -105,6 +106,8 @@ struct Params {
   int smem_bytes;   // dynamic shared memory of the launch (after 1024-byte alignment slack)
   int stage_cap;    // most pipeline stages to use (2..kMaxStages)
   uint32_t* sched;  // [0] tile counter, [32] finished CTAs (zero between launches); null: static stripes
+  int w_tiled;      // weights in the tiled layout: box (row block, K chunk) at row (block * w_kc + chunk) * 128
+  int w_kc;         // 128-byte K chunks per weight row (tiled layout)
   int64_t rows_cap;
 };
 
@@ -594,6 +597,16 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       // weight rows of tile j: gate/up pairs rows f and I + f; otherwise NA consecutive 128-row blocks
       const int wrow0 = SWIGLU ? e * p.N + mb * kBM : e * p.N + mb * kBM * NA;
       const int wstep = SWIGLU ? p.N / 2 : kBM;
+      // Weight box of tile j at K stage kt: (kt * wxs, wy[j] + kt * wys) in the
+      // tensor map -- row-major: column kt * 128 of row wrow; tiled: row
+      // ((wrow / 128) * kc + kt) * 128 of the 128-byte-wide box stack.
+      const int wxs = p.w_tiled ? 0 : kBKBytes, wys = p.w_tiled ? kBM : 0;
+      int wy[C::NA];
+#pragma unroll
+      for (int j = 0; j < C::NA; ++j) {
+        const int wrow = wrow0 + j * wstep;  // a multiple of 128
+        wy[j] = p.w_tiled ? (wrow / kBM) * p.w_kc * kBM : wrow;
+      }
       for (int kt = 0; kt < nkt; ++kt, ++it) {
         const uint32_t s = it % uint32_t(S), ph = (it / uint32_t(S)) & 1u;
         if (!wait_phase<true>(empty_bar(s), ph ^ 1u, abort_flag)) {
@@ -621,7 +634,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         ptx::mbar_arrive_expect_tx(full_bar(s), uint32_t(C::NA * kATile + w * kBKBytes));
 #pragma unroll
         for (int j = 0; j < C::NA; ++j)
-          ptx::tma_load_2d(st + j * kATile, &tmap_w, full_bar(s), kt * kBKBytes, wrow0 + j * wstep, pol_w);
+          ptx::tma_load_2d(st + j * kATile, &tmap_w, full_bar(s), kt * wxs, wy[j] + kt * wys, pol_w);
         for (int r = 0; r < w; r += 32)  // the token tile in 32-row boxes
           ptx::tma_load_2d(st + off_b + r * kBKBytes, &tmap_a, full_bar(s), kt * kBKBytes, arow + r, pol_a);
       }
@@ -1120,7 +1133,10 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   }
   const size_t smem = size_t(smem_optin);
   CUtensorMap tw, ta, tc;
-  if (!encode_kmajor_map(&tw, a.w_packed, int64_t(a.E) * a.N, a.K / 2, kBM) ||
+  const int w_kc = (a.K + 255) / 256;
+  const bool w_map_ok = a.w_tiled ? encode_kmajor_map(&tw, a.w_packed, int64_t(a.E) * a.N / kBM * w_kc * kBM, kBKBytes, kBM)
+                                  : encode_kmajor_map(&tw, a.w_packed, int64_t(a.E) * a.N, a.K / 2, kBM);
+  if (!w_map_ok ||
       !encode_kmajor_map(&ta, a.a_packed, a.rows_capacity, a.K / 2, 32) ||
       !(out_stage_bytes(SWIGLU, TM) ? encode_bf16_store_map(&tc, a.c_out, a.rows_capacity, a.N)
                                     : encode_kmajor_map(&tc, a.a_packed, a.rows_capacity, a.K / 2, 32))) {
@@ -1152,6 +1168,8 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   p.stage_cap = stage_cap_from_env();
   p.rows_cap = a.rows_capacity;
   p.sched = static_cast<uint32_t*>(a.sched);
+  p.w_tiled = a.w_tiled ? 1 : 0;
+  p.w_kc = w_kc;
   // Launched without programmatic dependent launch: measured on GB300, a
   // grouped GEMM launched with it streamed its weight tiles about 2.5%
   // slower per tile, more than the few microseconds of launch latency it
@@ -1187,6 +1205,37 @@ int launch_format(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t s
   if (!swiglu && bn == 256) return launch_impl<256, 1, false, MX>(a, num_sms, smem_optin, st);
   set_error_detail("tile_n %d is not supported for this epilogue", a.tile_n);
   return NVFP4MOE_ERR_UNSUPPORTED;
+}
+
+namespace {
+
+// Tiled weight layout: one thread per 16 bytes of the output.  Output unit u
+// is byte 16 * (u % 8) of row (u / 8) % 128 of box u / 1024; box b holds
+// row block b / kc, K chunk b % kc.  Bytes past the row's end are zero.
+__global__ void __launch_bounds__(256) tile_weights_kernel(const uint4* __restrict__ w, int64_t rows, int row_bytes,
+                                                           int kc, uint4* __restrict__ out) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  const int64_t units = rows / kBM * kc * (kWeightBoxBytes / 16);
+  const int row16 = row_bytes / 16;
+  for (int64_t u = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; u < units; u += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t box = u >> 10;
+    const int r = int(u >> 3) & 127, c16 = int(u & 7);
+    const int64_t rb = box / kc;
+    const int col16 = int(box - rb * kc) * 8 + c16;  // 16-byte column within the row
+    out[u] = col16 < row16 ? __ldg(w + (rb * kBM + r) * row16 + col16) : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_tile_weights(const uint8_t* w_packed, int64_t rows, int K, uint8_t* w_tiled, int num_sms,
+                                cudaStream_t st) {
+  const int kc = (K + 255) / 256;
+  const int64_t units = rows / kBM * kc * (kWeightBoxBytes / 16);
+  const int64_t want = (units + 255) / 256, cap = int64_t(num_sms) * 16;
+  return launch_kernel(tile_weights_kernel, dim3(unsigned(want < cap ? want : cap)), dim3(256), 0, st, false,
+                       reinterpret_cast<const uint4*>(w_packed), rows, K / 2, kc, reinterpret_cast<uint4*>(w_tiled));
 }
 
 int launch_grouped_gemm(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st) {

@@ -97,6 +97,7 @@ struct GemmArgs {
   uint8_t* c_scales;
   int tile_n;
   bool mx;  // MXFP4 operands (ue8m0 scale per 32 elements, no per-tensor scales)
+  bool w_tiled;  // w_packed in the tiled layout (NVFP4MOE_W_TILED)
   void* sched;  // zero-filled 256-byte tile-scheduler workspace, or null for the static schedule
 };
 
@@ -110,6 +111,11 @@ constexpr int64_t kTokenMajorMinRows = 64;
 
 // Returns 0 on success or an NVFP4MOE_ERR_* code (message via set_error_detail).
 int launch_grouped_gemm(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st);
+
+// One 128-row x 128-byte weight box of the tiled layout.
+constexpr int64_t kWeightBoxBytes = 128 * 128;
+cudaError_t launch_tile_weights(const uint8_t* w_packed, int64_t rows, int K, uint8_t* w_tiled, int num_sms,
+                                cudaStream_t st);
 cudaError_t gemm_read_and_clear_flags(unsigned* flags);
 
 // Per-thread error message used by nvfp4moe_last_error_detail().

@@ -41,6 +41,24 @@ def from_blocked(buf, rows, cols, block=16):
     return np.asarray(buf)[blocked_index(rp, cols, block)[:rows]]
 
 
+def untile_weights(tiled, E, N, K):
+    """Row-major [E, N, K/2] packed weights from the tiled layout (as the
+    library header defines it): box (rb, kc) of 128 rows x 128 bytes at byte
+    (rb * KC + kc) * 16384, KC = ceil(K / 256), bytes past K/2 zero."""
+    KC = (K + 255) // 256
+    t = np.asarray(tiled, dtype=np.uint8).reshape(E * N // 128, KC, 128, 128)
+    rows = t.transpose(0, 2, 1, 3).reshape(E * N, KC * 128)
+    assert not rows[:, K // 2:].any(), "bytes past K/2 must be zero"
+    return rows[:, :K // 2].reshape(E, N, K // 2)
+
+
+def packed_weights(w):
+    """Row-major [E, N, K/2] codes of a layer's packed weights (tiled or not)."""
+    if hasattr(w, "data") and hasattr(w, "K"):
+        return untile_weights(w.data.cpu().numpy(), w.E, w.N, w.K)
+    return w.cpu().numpy()
+
+
 def signed_rank(codes):
     """Position of each E2M1 code on the ordered value line (-7..7; +-0 -> 0)."""
     c = np.asarray(codes).astype(np.int64)

@@ -335,6 +335,37 @@ def test_grouped_gemm_token_major_chosen_automatically(B):
     U.check_close(auto.float().cpu().numpy()[pos], O.round_to_bf16(ref), what="bf16 GEMM, automatic tiles")
 
 
+@pytest.mark.parametrize("E,N,K,counts,tile_n", [(3, 256, 320, [5, 0, 140], 0), (2, 512, 1024, [300, 17], TM),
+                                                  (4, 384, 448, [1, 33, 64, 129], 0), (2, 256, 256, [7, 200], 256)])
+def test_grouped_gemm_tiled_weights(B, E, N, K, counts, tile_n):
+    """nvfp4moe_tile_weights writes the layout the header defines (checked by
+    undoing it), and the GEMMs read tiled weights to the same bits as
+    row-major ones: same operands, same arithmetic."""
+    g, ref, pos, R = gemm_case(E, N, K, counts, seed=E * 3 + K)
+    tiled = B.tile_expert_weights(g["w_packed"])
+    B.sync_status()
+    np.testing.assert_array_equal(U.untile_weights(tiled.data.cpu().numpy(), E, N, K), g["w_packed"].cpu().numpy())
+    args = (g["a_packed"], g["a_scales"], g["a_gscale"], g["counts"], g["row_offsets"])
+    rows = torch.from_numpy(pos).cuda()
+    y0 = B.moe_grouped_gemm_nvfp4(*args, g["w_packed"], g["w_scales"], g["w_gscale"], B.EPI_BF16, m_total=R,
+                                  tile_n=tile_n)
+    y1 = B.moe_grouped_gemm_nvfp4(*args, tiled, g["w_scales"], g["w_gscale"], B.EPI_BF16, m_total=R, tile_n=tile_n)
+    B.sync_status()
+    assert torch.equal(y0[rows], y1[rows])
+    U.check_close(y1.float().cpu().numpy()[pos], O.round_to_bf16(ref), what="bf16 GEMM, tiled weights")
+    if N % 256 == 0 and tile_n != 256:
+        s_h = dev(torch.tensor([2.0 ** -4]))
+        h0, hs0 = B.moe_grouped_gemm_nvfp4(*args, g["w_packed"], g["w_scales"], g["w_gscale"], B.EPI_SWIGLU_NVFP4,
+                                           c_gscale=s_h, m_total=R, tile_n=tile_n)
+        h1, hs1 = B.moe_grouped_gemm_nvfp4(*args, tiled, g["w_scales"], g["w_gscale"], B.EPI_SWIGLU_NVFP4,
+                                           c_gscale=s_h, m_total=R, tile_n=tile_n)
+        B.sync_status()
+        assert torch.equal(h0[rows], h1[rows])
+        cap = h0.shape[0]
+        np.testing.assert_array_equal(U.from_blocked(hs0.cpu().numpy(), cap, N // 2)[pos],
+                                      U.from_blocked(hs1.cpu().numpy(), cap, N // 2)[pos])
+
+
 @pytest.mark.parametrize("E,N,K,counts,tile_n", GEMM_SHAPES[:4])
 def test_grouped_gemm_dynamic_schedule_matches_static(B, E, N, K, counts, tile_n):
     """Tiles claimed from the launch-wide counter give the same bits as the

@@ -38,7 +38,8 @@ def test_layer_matches_oracle(B, w):
     gq = U.oracle_quantize_experts(inp["w_gu"])
     dq = U.oracle_quantize_experts(inp["w_d"])
     # the library's weight quantisation is bit-exact with the oracle's
-    np.testing.assert_array_equal(layer.w_gu_packed.cpu().numpy(), gq[0])
+    np.testing.assert_array_equal(U.packed_weights(layer.w_gu_packed), gq[0])
+    np.testing.assert_array_equal(U.packed_weights(layer.w_d_packed), dq[0])
     np.testing.assert_array_equal(layer.w_gu_gscale.cpu().numpy(), gq[2])
     for e in range(w.E):
         np.testing.assert_array_equal(U.from_blocked(layer.w_d_scales[e].cpu().numpy(), w.H, w.I), dq[1][e])

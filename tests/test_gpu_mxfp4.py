@@ -133,6 +133,21 @@ def test_grouped_gemm_mx_bf16_token_major(B, E, N, K, counts):
 
 
 @pytest.mark.parametrize("tile_n", [0, -1])  # -1: binding.TILE_TOKEN_MAJOR
+def test_grouped_gemm_mx_tiled_weights(B, tile_n):
+    """MXFP4 codes in the tiled layout: the same bits as row-major weights."""
+    E, N, K, counts = 3, 512, 640, [9, 140, 1]
+    g, ref, pos, R = gemm_case_mx(E, N, K, counts, seed=77)
+    tiled = B.tile_expert_weights(g["w_packed"])
+    args = (g["a_packed"], g["a_scales"], g["counts"], g["row_offsets"])
+    y0 = B.moe_grouped_gemm_mxfp4(*args, g["w_packed"], g["w_scales"], B.EPI_BF16, m_total=R, tile_n=tile_n)
+    y1 = B.moe_grouped_gemm_mxfp4(*args, tiled, g["w_scales"], B.EPI_BF16, m_total=R, tile_n=tile_n)
+    B.sync_status()
+    rows = torch.from_numpy(pos).cuda()
+    assert torch.equal(y0[rows], y1[rows])
+    U.check_close(y1.float().cpu().numpy()[pos], O.round_to_bf16(ref), what="MXFP4 bf16 GEMM, tiled weights")
+
+
+@pytest.mark.parametrize("tile_n", [0, -1])  # -1: binding.TILE_TOKEN_MAJOR
 @pytest.mark.parametrize("E,I,K,counts", [(3, 128, 512, [9, 70, 0]), (2, 256, 384, [130, 1]),
                                           (4, 128, 1024, [128, 5, 64, 200])])
 def test_grouped_gemm_mx_swiglu(B, E, I, K, counts, tile_n):
@@ -189,7 +204,8 @@ def test_layer_mx_matches_oracle(B, w, fused):
     B.sync_status()
     gq = U.oracle_quantize_experts_mx(inp["w_gu"])
     dq = U.oracle_quantize_experts_mx(inp["w_d"])
-    np.testing.assert_array_equal(layer.w_gu_packed.cpu().numpy(), gq[0])
+    np.testing.assert_array_equal(U.packed_weights(layer.w_gu_packed), gq[0])
+    np.testing.assert_array_equal(U.packed_weights(layer.w_d_packed), dq[0])
     for e in range(w.E):
         np.testing.assert_array_equal(U.from_blocked(layer.w_d_scales[e].cpu().numpy(), w.H, w.I, 32), dq[1][e])
     ref, it = O.moe_layer_mx(inp["x"].float().numpy(), inp["logits"].numpy(),
