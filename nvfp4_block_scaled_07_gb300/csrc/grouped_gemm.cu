@@ -635,8 +635,12 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
 #pragma unroll
         for (int j = 0; j < C::NA; ++j)
           ptx::tma_load_2d(st + j * kATile, &tmap_w, full_bar(s), kt * wxs, wy[j] + kt * wys, pol_w);
-        for (int r = 0; r < w; r += 32)  // the token tile in 32-row boxes
-          ptx::tma_load_2d(st + off_b + r * kBKBytes, &tmap_a, full_bar(s), kt * kBKBytes, arow + r, pol_a);
+        if constexpr (TM) {  // a 128-row token tile: one box (the map's box is 128 rows here)
+          ptx::tma_load_2d(st + off_b, &tmap_a, full_bar(s), kt * kBKBytes, arow, pol_a);
+        } else {
+          for (int r = 0; r < w; r += 32)  // the token tile in 32-row boxes
+            ptx::tma_load_2d(st + off_b + r * kBKBytes, &tmap_a, full_bar(s), kt * kBKBytes, arow + r, pol_a);
+        }
       }
     }
     if (!ok) {
@@ -1137,7 +1141,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   const bool w_map_ok = a.w_tiled ? encode_kmajor_map(&tw, a.w_packed, int64_t(a.E) * a.N / kBM * w_kc * kBM, kBKBytes, kBM)
                                   : encode_kmajor_map(&tw, a.w_packed, int64_t(a.E) * a.N, a.K / 2, kBM);
   if (!w_map_ok ||
-      !encode_kmajor_map(&ta, a.a_packed, a.rows_capacity, a.K / 2, 32) ||
+      !encode_kmajor_map(&ta, a.a_packed, a.rows_capacity, a.K / 2, TM ? kBM : 32) ||
       !(out_stage_bytes(SWIGLU, TM) ? encode_bf16_store_map(&tc, a.c_out, a.rows_capacity, a.N)
                                     : encode_kmajor_map(&tc, a.a_packed, a.rows_capacity, a.K / 2, 32))) {
     set_error_detail("cuTensorMapEncodeTiled failed or is unavailable");
