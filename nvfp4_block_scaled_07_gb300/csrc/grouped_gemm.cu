@@ -106,7 +106,7 @@ struct Params {
   int smem_bytes;   // dynamic shared memory of the launch (after 1024-byte alignment slack)
   int stage_cap;    // most pipeline stages to use (2..kMaxStages)
   uint32_t* sched;  // [0] tile counter, [32] finished CTAs (zero between launches); null: static stripes
-  int w_tiled;      // weights in the tiled layout: box (row block, K chunk) at row (block * w_kc + chunk) * 128
+  int w_tiled;      // weights in the tiled layout (5-D weight map coordinates below)
   int w_kc;         // 128-byte K chunks per weight row (tiled layout)
   int64_t rows_cap;
 };
@@ -594,19 +594,15 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       if constexpr (TM) w = kBM;
       const int arow = s_rowoff[e] + nb * BN;
       const int sfb_chunks = w > 128 ? 2 : 1;
-      // weight rows of tile j: gate/up pairs rows f and I + f; otherwise NA consecutive 128-row blocks
-      const int wrow0 = SWIGLU ? e * p.N + mb * kBM : e * p.N + mb * kBM * NA;
-      const int wstep = SWIGLU ? p.N / 2 : kBM;
-      // Weight box of tile j at K stage kt: (kt * wxs, wy[j] + kt * wys) in the
-      // tensor map -- row-major: column kt * 128 of row wrow; tiled: row
-      // ((wrow / 128) * kc + kt) * 128 of the 128-byte-wide box stack.
-      const int wxs = p.w_tiled ? 0 : kBKBytes, wys = p.w_tiled ? kBM : 0;
-      int wy[C::NA];
-#pragma unroll
-      for (int j = 0; j < C::NA; ++j) {
-        const int wrow = wrow0 + j * wstep;  // a multiple of 128
-        wy[j] = p.w_tiled ? (wrow / kBM) * p.w_kc * kBM : wrow;
-      }
+      // weight tiles: gate/up pair rows f and I + f; otherwise NA consecutive 128-row blocks
+      // The stage's NA weight tiles are one box of the 5-D weight map (see
+      // encode_weight_map): coordinates (kt * wdx, wc1, wc2 + kt * wdz, wc3, wc4).
+      const int wdx = p.w_tiled ? 0 : kBKBytes, wdz = p.w_tiled ? 1 : 0;
+      const int wblk = SWIGLU ? mb : e * (p.N / kBM) + mb * NA;  // first 128-row block of the tile
+      const int wc1 = (!p.w_tiled && SWIGLU) ? mb * kBM : 0;
+      const int wc2 = p.w_tiled ? 0 : (SWIGLU ? 2 * e : wblk);
+      const int wc3 = p.w_tiled ? wblk : 0;
+      const int wc4 = (p.w_tiled && SWIGLU) ? 2 * e : 0;
       for (int kt = 0; kt < nkt; ++kt, ++it) {
         const uint32_t s = it % uint32_t(S), ph = (it / uint32_t(S)) & 1u;
         if (!wait_phase<true>(empty_bar(s), ph ^ 1u, abort_flag)) {
@@ -632,9 +628,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
           ptx::bulk_load(st + off_sfb + c * kSfTile, src, uint32_t(nsf * 512), sfc_bar(s), pol_a);
         }
         ptx::mbar_arrive_expect_tx(full_bar(s), uint32_t(C::NA * kATile + w * kBKBytes));
-#pragma unroll
-        for (int j = 0; j < C::NA; ++j)
-          ptx::tma_load_2d(st + j * kATile, &tmap_w, full_bar(s), kt * wxs, wy[j] + kt * wys, pol_w);
+        ptx::tma_load_5d(st, &tmap_w, full_bar(s), kt * wdx, wc1, wc2 + kt * wdz, wc3, wc4, pol_w);
         if constexpr (TM) {  // a 128-row token tile: one box (the map's box is 128 rows here)
           ptx::tma_load_2d(st + off_b, &tmap_a, full_bar(s), kt * kBKBytes, arow, pol_a);
         } else {
@@ -1094,6 +1088,56 @@ bool encode_kmajor_map(CUtensorMap* m, const void* base, int64_t rows, int64_t r
   return r == CUDA_SUCCESS;
 }
 
+// Weight map: a 5-D byte view of the weights whose box {128 B, 128 rows, ...}
+// holds the NA weight tiles of one pipeline stage back to back (one copy per
+// stage).  Coordinates (kt * dx, c1, c2 + kt * dz, c3, c4):
+//   row-major, SwiGLU: [K/2 B][I rows][2E halves (gate, up)]   box {128, 128, 2}
+//                      at (128 kt, 128 mb, 2e)
+//   row-major, other:  [K/2 B][128 rows][E N / 128 blocks]      box {128, 128, NA}
+//                      at (128 kt, 0, first block)
+//   tiled, SwiGLU:     [128 B][128 rows][kc chunks][I / 128 blocks][2E halves]
+//                      box {128, 128, 1, 1, 2} at (0, 0, kt, mb, 2e)
+//   tiled, other:      [128 B][128 rows][kc chunks][E N / 128 blocks]
+//                      box {128, 128, 1, NA} at (0, 0, kt, first block)
+// Unit dimensions fill the view to 5-D.
+bool encode_weight_map(CUtensorMap* m, const GemmArgs& a, bool swiglu, int na) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const int64_t kh = a.K / 2, kc = (a.K + 255) / 256, nblk = int64_t(a.E) * a.N / kBM, half = a.N / 2;
+  cuuint64_t dims[5];
+  cuuint64_t strides[4];
+  cuuint32_t box[5] = {cuuint32_t(kBKBytes), cuuint32_t(kBM), 1, 1, 1};
+  if (!a.w_tiled) {
+    if (swiglu) {
+      dims[0] = kh, dims[1] = half, dims[2] = 2 * int64_t(a.E);
+      strides[0] = kh, strides[1] = half * kh;
+    } else {
+      dims[0] = kh, dims[1] = kBM, dims[2] = nblk;
+      strides[0] = kh, strides[1] = kBM * kh;
+    }
+    box[2] = cuuint32_t(swiglu ? 2 : na);
+    dims[3] = dims[4] = 1;
+    strides[2] = strides[3] = strides[1] * dims[2];
+  } else {
+    dims[0] = kBKBytes, dims[1] = kBM, dims[2] = kc;
+    strides[0] = kBKBytes, strides[1] = kWeightBoxBytes, strides[2] = kc * kWeightBoxBytes;
+    if (swiglu) {
+      dims[3] = half / kBM, dims[4] = 2 * int64_t(a.E);
+      strides[3] = (half / kBM) * kc * kWeightBoxBytes;
+      box[4] = 2;
+    } else {
+      dims[3] = nblk, dims[4] = 1;
+      strides[3] = nblk * kc * kWeightBoxBytes;
+      box[3] = cuuint32_t(na);
+    }
+  }
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<uint8_t*>(a.w_packed), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // bf16 [rows, cols] output written by 32-row x 32-column TMA stores (64-byte
 // rows in shared memory, no swizzle).
 bool encode_bf16_store_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
@@ -1138,9 +1182,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   const size_t smem = size_t(smem_optin);
   CUtensorMap tw, ta, tc;
   const int w_kc = (a.K + 255) / 256;
-  const bool w_map_ok = a.w_tiled ? encode_kmajor_map(&tw, a.w_packed, int64_t(a.E) * a.N / kBM * w_kc * kBM, kBKBytes, kBM)
-                                  : encode_kmajor_map(&tw, a.w_packed, int64_t(a.E) * a.N, a.K / 2, kBM);
-  if (!w_map_ok ||
+  if (!encode_weight_map(&tw, a, SWIGLU, NA) ||
       !encode_kmajor_map(&ta, a.a_packed, a.rows_capacity, a.K / 2, TM ? kBM : 32) ||
       !(out_stage_bytes(SWIGLU, TM) ? encode_bf16_store_map(&tc, a.c_out, a.rows_capacity, a.N)
                                     : encode_kmajor_map(&tc, a.a_packed, a.rows_capacity, a.K / 2, 32))) {
