@@ -571,7 +571,8 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     // ---------------- TMA producer ----------------
     const uint64_t pol_w = ptx::policy_evict_first();  // weights stream through once
     const uint64_t pol_a = ptx::policy_evict_last();   // token tiles are re-read by every M tile
-    uint32_t it = 0;
+    uint32_t it = 0;          // stages issued (for the drain after an abort)
+    uint32_t s = 0, ph = 0;   // ring position of stage it and its phase parity
     bool ok = true;
     // Dynamic schedule: the next id is claimed one tile ahead, so the atomic's
     // latency overlaps the current tile's copies.
@@ -603,8 +604,16 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       const int wc2 = p.w_tiled ? 0 : (SWIGLU ? 2 * e : wblk);
       const int wc3 = p.w_tiled ? wblk : 0;
       const int wc4 = (p.w_tiled && SWIGLU) ? 2 * e : 0;
+      // the tile's scale blocks at K stage 0 (a stage advances sf_per_kt blocks)
+      const uint8_t* wsf[C::NA];
+#pragma unroll
+      for (int j = 0; j < C::NA; ++j) {
+        const int rb = SWIGLU ? (j * (p.N / 2) + mb * kBM) / kBM : mb * NA + j;
+        wsf[j] = p.w_scales + (size_t(e) * (p.N / kBM) + rb) * sf_k * 512;
+      }
+      const uint8_t* asf = p.a_scales + size_t(arow / kBM) * sf_k * 512;
+      const uint32_t full_bytes = uint32_t(C::NA * kATile + w * kBKBytes);
       for (int kt = 0; kt < nkt; ++kt, ++it) {
-        const uint32_t s = it % uint32_t(S), ph = (it / uint32_t(S)) & 1u;
         if (!wait_phase<true>(empty_bar(s), ph ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -615,19 +624,16 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         const int nkb = min(4, kblocks - 4 * kt);
         // 512-byte scale blocks of this stage per 128 rows: one per k64 step
         // (NVFP4) or per k128 step (MXFP4, K % 128 == 0)
-        const int nsf = MX ? nkb / 2 : nkb;
-        ptx::mbar_arrive_expect_tx(sfc_bar(s), uint32_t((C::NA + sfb_chunks) * nsf * 512));
+        const uint32_t sf_bytes = uint32_t((MX ? nkb / 2 : nkb) * 512);
+        const size_t sf_off = size_t(kt) * (sf_per_kt * 512);
+        ptx::mbar_arrive_expect_tx(sfc_bar(s), (C::NA + sfb_chunks) * sf_bytes);
 #pragma unroll
-        for (int j = 0; j < C::NA; ++j) {
-          const int rb = SWIGLU ? (j * (p.N / 2) + mb * kBM) / kBM : mb * NA + j;
-          const uint8_t* src = p.w_scales + ((size_t(e) * (p.N / kBM) + rb) * sf_k + sf_per_kt * kt) * 512;
-          ptx::bulk_load(st + off_sfa + j * kSfTile, src, uint32_t(nsf * 512), sfc_bar(s), pol_w);
-        }
-        for (int c = 0; c < sfb_chunks; ++c) {
-          const uint8_t* src = p.a_scales + ((size_t(arow / kBM) + c) * sf_k + sf_per_kt * kt) * 512;
-          ptx::bulk_load(st + off_sfb + c * kSfTile, src, uint32_t(nsf * 512), sfc_bar(s), pol_a);
-        }
-        ptx::mbar_arrive_expect_tx(full_bar(s), uint32_t(C::NA * kATile + w * kBKBytes));
+        for (int j = 0; j < C::NA; ++j)
+          ptx::bulk_load(st + off_sfa + j * kSfTile, wsf[j] + sf_off, sf_bytes, sfc_bar(s), pol_w);
+        for (int c = 0; c < sfb_chunks; ++c)
+          ptx::bulk_load(st + off_sfb + c * kSfTile, asf + size_t(c) * sf_k * 512 + sf_off, sf_bytes, sfc_bar(s),
+                         pol_a);
+        ptx::mbar_arrive_expect_tx(full_bar(s), full_bytes);
         ptx::tma_load_5d(st, &tmap_w, full_bar(s), kt * wdx, wc1, wc2 + kt * wdz, wc3, wc4, pol_w);
         if constexpr (TM) {  // a 128-row token tile: one box (the map's box is 128 rows here)
           ptx::tma_load_2d(st + off_b, &tmap_a, full_bar(s), kt * kBKBytes, arow, pol_a);
@@ -635,6 +641,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
           for (int r = 0; r < w; r += 32)  // the token tile in 32-row boxes
             ptx::tma_load_2d(st + off_b + r * kBKBytes, &tmap_a, full_bar(s), kt * kBKBytes, arow + r, pol_a);
         }
+        if (++s == uint32_t(S)) s = 0, ph ^= 1u;
       }
     }
     if (!ok) {
