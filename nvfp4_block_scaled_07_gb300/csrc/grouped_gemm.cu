@@ -409,7 +409,8 @@ __device__ __forceinline__ void requant_row32_mx(const uint32_t (&h)[32], int64_
 template <int BN, int NA, bool SWIGLU, bool MX, bool TM>
 __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
-                        const __grid_constant__ CUtensorMap tmap_c, const Params p) {
+                        const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_sf,
+                        const Params p) {
   using C = Cfg<BN, NA, SWIGLU>;
   static_assert(!TM || (BN == 128 && NA == 2), "token-major tiles: 128 tokens x two 128-row weight tiles");
   extern __shared__ uint8_t smem_raw[];
@@ -604,13 +605,10 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       const int wc2 = p.w_tiled ? 0 : (SWIGLU ? 2 * e : wblk);
       const int wc3 = p.w_tiled ? wblk : 0;
       const int wc4 = (p.w_tiled && SWIGLU) ? 2 * e : 0;
-      // the tile's scale blocks at K stage 0 (a stage advances sf_per_kt blocks)
-      const uint8_t* wsf[C::NA];
-#pragma unroll
-      for (int j = 0; j < C::NA; ++j) {
-        const int rb = SWIGLU ? (j * (p.N / 2) + mb * kBM) / kBM : mb * NA + j;
-        wsf[j] = p.w_scales + (size_t(e) * (p.N / kBM) + rb) * sf_k * 512;
-      }
+      // The weight tiles' scale blocks of a stage are one box of the scale map
+      // (see encode_weight_scale_map) at (64 sf_per_kt kt, sc1, sc2): a stage
+      // advances sf_per_kt 512-byte blocks; the token tile's start at asf.
+      const int sc1 = SWIGLU ? mb : e * (p.N / kBM) + mb * NA, sc2 = SWIGLU ? 2 * e : 0;
       const uint8_t* asf = p.a_scales + size_t(arow / kBM) * sf_k * 512;
       const uint32_t full_bytes = uint32_t(C::NA * kATile + w * kBKBytes);
       for (int kt = 0; kt < nkt; ++kt, ++it) {
@@ -626,10 +624,9 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         // (NVFP4) or per k128 step (MXFP4, K % 128 == 0)
         const uint32_t sf_bytes = uint32_t((MX ? nkb / 2 : nkb) * 512);
         const size_t sf_off = size_t(kt) * (sf_per_kt * 512);
-        ptx::mbar_arrive_expect_tx(sfc_bar(s), (C::NA + sfb_chunks) * sf_bytes);
-#pragma unroll
-        for (int j = 0; j < C::NA; ++j)
-          ptx::bulk_load(st + off_sfa + j * kSfTile, wsf[j] + sf_off, sf_bytes, sfc_bar(s), pol_w);
+        // the weight scale box is always full (bytes past the scales read as zero)
+        ptx::mbar_arrive_expect_tx(sfc_bar(s), uint32_t(C::NA * kSfTile) + sfb_chunks * sf_bytes);
+        ptx::tma_load_3d(st + off_sfa, &tmap_sf, sfc_bar(s), kt * sf_per_kt * 64, sc1, sc2, pol_w);
         for (int c = 0; c < sfb_chunks; ++c)
           ptx::bulk_load(st + off_sfb + c * kSfTile, asf + size_t(c) * sf_k * 512 + sf_off, sf_bytes, sfc_bar(s),
                          pol_a);
@@ -1145,6 +1142,37 @@ bool encode_weight_map(CUtensorMap* m, const GemmArgs& a, bool swiglu, int na) {
   return r == CUDA_SUCCESS;
 }
 
+// Weight scale map: the blocked scales of the weights as 8-byte elements,
+// [sf_k * 64 elements per 128-row block][row blocks][halves], whose box
+// {256, 1, 2} (SwiGLU: gate and up blocks of the same features) or
+// {256, NA, 1} (NA consecutive blocks) is 2 KB per weight tile from the
+// stage's first block, at (64 sf_per_kt kt, block, half): an NVFP4 stage's
+// four blocks, or an MXFP4 stage's two and the next stage's (unused); past
+// the last K block the box reads zeros.
+bool encode_weight_scale_map(CUtensorMap* m, const GemmArgs& a, bool swiglu, int na) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const int64_t sf_k = a.mx ? a.K / 128 : a.K / 64;  // 512-byte blocks per 128-row block
+  const int64_t row_elems = sf_k * 64, nblk = int64_t(a.E) * a.N / kBM;
+  cuuint64_t dims[3], strides[2];
+  cuuint32_t box[3] = {cuuint32_t(kSfTile / 8), 1, 1};
+  dims[0] = row_elems;
+  strides[0] = sf_k * 512;
+  if (swiglu) {
+    dims[1] = a.N / 2 / kBM, dims[2] = 2 * int64_t(a.E);
+    box[2] = 2;
+  } else {
+    dims[1] = nblk, dims[2] = 1;
+    box[1] = cuuint32_t(na);
+  }
+  strides[1] = strides[0] * dims[1];
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<uint8_t*>(a.w_scales), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // bf16 [rows, cols] output written by 32-row x 32-column TMA stores (64-byte
 // rows in shared memory, no swizzle).
 bool encode_bf16_store_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
@@ -1187,9 +1215,9 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
     return NVFP4MOE_ERR_SMEM;
   }
   const size_t smem = size_t(smem_optin);
-  CUtensorMap tw, ta, tc;
+  CUtensorMap tw, ta, tc, tsf;
   const int w_kc = (a.K + 255) / 256;
-  if (!encode_weight_map(&tw, a, SWIGLU, NA) ||
+  if (!encode_weight_map(&tw, a, SWIGLU, NA) || !encode_weight_scale_map(&tsf, a, SWIGLU, NA) ||
       !encode_kmajor_map(&ta, a.a_packed, a.rows_capacity, a.K / 2, TM ? kBM : 32) ||
       !(out_stage_bytes(SWIGLU, TM) ? encode_bf16_store_map(&tc, a.c_out, a.rows_capacity, a.N)
                                     : encode_kmajor_map(&tc, a.a_packed, a.rows_capacity, a.K / 2, 32))) {
@@ -1228,7 +1256,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   // slower per tile, more than the few microseconds of launch latency it
   // hides.  The kernel still starts with griddepcontrol.wait (a no-op here),
   // so the kernel after it may be launched with the attribute.
-  grouped_gemm_kernel<BN, NA, SWIGLU, MX, TM><<<num_sms, num_threads(SWIGLU), smem, st>>>(tw, ta, tc, p);
+  grouped_gemm_kernel<BN, NA, SWIGLU, MX, TM><<<num_sms, num_threads(SWIGLU), smem, st>>>(tw, ta, tc, tsf, p);
   err = cudaGetLastError();
   if (err != cudaSuccess) {
     set_error_detail("grouped GEMM launch: %s", cudaGetErrorString(err));
