@@ -410,7 +410,7 @@ template <int BN, int NA, bool SWIGLU, bool MX, bool TM>
 __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_sf,
-                        const Params p) {
+                        const __grid_constant__ CUtensorMap tmap_asf, const Params p) {
   using C = Cfg<BN, NA, SWIGLU>;
   static_assert(!TM || (BN == 128 && NA == 2), "token-major tiles: 128 tokens x two 128-row weight tiles");
   extern __shared__ uint8_t smem_raw[];
@@ -624,12 +624,18 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         // (NVFP4) or per k128 step (MXFP4, K % 128 == 0)
         const uint32_t sf_bytes = uint32_t((MX ? nkb / 2 : nkb) * 512);
         const size_t sf_off = size_t(kt) * (sf_per_kt * 512);
-        // the weight scale box is always full (bytes past the scales read as zero)
-        ptx::mbar_arrive_expect_tx(sfc_bar(s), uint32_t(C::NA * kSfTile) + sfb_chunks * sf_bytes);
-        ptx::tma_load_3d(st + off_sfa, &tmap_sf, sfc_bar(s), kt * sf_per_kt * 64, sc1, sc2, pol_w);
-        for (int c = 0; c < sfb_chunks; ++c)
-          ptx::bulk_load(st + off_sfb + c * kSfTile, asf + size_t(c) * sf_k * 512 + sf_off, sf_bytes, sfc_bar(s),
-                         pol_a);
+        // scale boxes are always full (bytes past the scales read as zero)
+        if constexpr (BN == 128) {  // one 128-row token chunk: its scales are a box of the token scale map
+          ptx::mbar_arrive_expect_tx(sfc_bar(s), uint32_t((C::NA + 1) * kSfTile));
+          ptx::tma_load_3d(st + off_sfa, &tmap_sf, sfc_bar(s), kt * sf_per_kt * 64, sc1, sc2, pol_w);
+          ptx::tma_load_3d(st + off_sfb, &tmap_asf, sfc_bar(s), kt * sf_per_kt * 64, arow / kBM, 0, pol_a);
+        } else {
+          ptx::mbar_arrive_expect_tx(sfc_bar(s), uint32_t(C::NA * kSfTile) + sfb_chunks * sf_bytes);
+          ptx::tma_load_3d(st + off_sfa, &tmap_sf, sfc_bar(s), kt * sf_per_kt * 64, sc1, sc2, pol_w);
+          for (int c = 0; c < sfb_chunks; ++c)
+            ptx::bulk_load(st + off_sfb + c * kSfTile, asf + size_t(c) * sf_k * 512 + sf_off, sf_bytes, sfc_bar(s),
+                           pol_a);
+        }
         ptx::mbar_arrive_expect_tx(full_bar(s), full_bytes);
         ptx::tma_load_5d(st, &tmap_w, full_bar(s), kt * wdx, wc1, wc2 + kt * wdz, wc3, wc4, pol_w);
         if constexpr (TM) {  // a 128-row token tile: one box (the map's box is 128 rows here)
@@ -1173,6 +1179,24 @@ bool encode_weight_scale_map(CUtensorMap* m, const GemmArgs& a, bool swiglu, int
   return r == CUDA_SUCCESS;
 }
 
+// Token scale map: the blocked scales of the permuted activations as 8-byte
+// elements, [sf_k * 64 elements per 128-row block][row blocks], whose box
+// {256, 1, 1} is one stage's 2 KB for a 128-row token tile at
+// (64 sf_per_kt kt, row block, 0), zero-filled past the last K block.
+bool encode_token_scale_map(CUtensorMap* m, const GemmArgs& a) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const int64_t sf_k = a.mx ? a.K / 128 : a.K / 64;
+  cuuint64_t dims[3] = {cuuint64_t(sf_k * 64), cuuint64_t(a.rows_capacity / kBM), 1};
+  cuuint64_t strides[2] = {cuuint64_t(sf_k * 512), cuuint64_t(sf_k * 512 * (a.rows_capacity / kBM))};
+  cuuint32_t box[3] = {cuuint32_t(kSfTile / 8), 1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<uint8_t*>(a.a_scales), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // bf16 [rows, cols] output written by 32-row x 32-column TMA stores (64-byte
 // rows in shared memory, no swizzle).
 bool encode_bf16_store_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
@@ -1215,9 +1239,10 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
     return NVFP4MOE_ERR_SMEM;
   }
   const size_t smem = size_t(smem_optin);
-  CUtensorMap tw, ta, tc, tsf;
+  CUtensorMap tw, ta, tc, tsf, tasf;
   const int w_kc = (a.K + 255) / 256;
   if (!encode_weight_map(&tw, a, SWIGLU, NA) || !encode_weight_scale_map(&tsf, a, SWIGLU, NA) ||
+      !encode_token_scale_map(&tasf, a) ||
       !encode_kmajor_map(&ta, a.a_packed, a.rows_capacity, a.K / 2, TM ? kBM : 32) ||
       !(out_stage_bytes(SWIGLU, TM) ? encode_bf16_store_map(&tc, a.c_out, a.rows_capacity, a.N)
                                     : encode_kmajor_map(&tc, a.a_packed, a.rows_capacity, a.K / 2, 32))) {
@@ -1256,7 +1281,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   // slower per tile, more than the few microseconds of launch latency it
   // hides.  The kernel still starts with griddepcontrol.wait (a no-op here),
   // so the kernel after it may be launched with the attribute.
-  grouped_gemm_kernel<BN, NA, SWIGLU, MX, TM><<<num_sms, num_threads(SWIGLU), smem, st>>>(tw, ta, tc, tsf, p);
+  grouped_gemm_kernel<BN, NA, SWIGLU, MX, TM><<<num_sms, num_threads(SWIGLU), smem, st>>>(tw, ta, tc, tsf, tasf, p);
   err = cudaGetLastError();
   if (err != cudaSuccess) {
     set_error_detail("grouped GEMM launch: %s", cudaGetErrorString(err));
