@@ -56,6 +56,14 @@ def test_size_queries(lib):
     assert lib.moe_permute_rows_capacity(16, 8, 2) % 128 == 0
     lib.moe_permute_workspace_size.restype = ctypes.c_size_t
     assert lib.moe_permute_workspace_size(16384, 64, 8) >= 16384 * 8 * 4
+    # tiled weights: (rows / 128) * ceil(K / 256) boxes of 128 x 128 bytes
+    lib.nvfp4moe_tiled_weights_bytes.restype = ctypes.c_size_t
+    lib.nvfp4moe_tiled_weights_bytes.argtypes = [ctypes.c_int64, ctypes.c_int]
+    assert lib.nvfp4moe_tiled_weights_bytes(256 * 4096, 6144) == (256 * 4096 // 128) * 24 * 16384
+    assert lib.nvfp4moe_tiled_weights_bytes(128, 320) == 2 * 16384        # a partial last K chunk is padded
+    assert lib.nvfp4moe_tiled_weights_bytes(128, 6144) == 128 * 6144 // 2  # no padding when K % 256 == 0
+    assert lib.nvfp4moe_tiled_weights_bytes(100, 256) == 0
+    assert lib.nvfp4moe_tiled_weights_bytes(128, 96) == 0
     lib.moe_quantize_nvfp4_workspace_size.restype = ctypes.c_size_t
     lib.moe_quantize_nvfp4_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int]
     assert lib.moe_quantize_nvfp4_workspace_size(4, 64, 0) == 0
@@ -71,18 +79,27 @@ def test_argument_validation_before_any_device_work(lib):
     assert lib.moe_route_topk(None, None, 0, 8, 2, 1, 1, None, None, None) == 0       # T = 0 is a no-op
     g = lib.moe_grouped_gemm_nvfp4
     g.argtypes = [p, p, p, p, p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, p, p, p, ctypes.c_int, ctypes.c_int,
-                  ctypes.c_int, p, p, p, ctypes.c_int, p, ctypes.c_size_t, p]
+                  ctypes.c_int, p, p, p, ctypes.c_int, ctypes.c_int, p, ctypes.c_size_t, p]
     dummy = p(256)
     assert g(dummy, dummy, dummy, dummy, dummy, 8, 1024, 32, dummy, dummy, dummy, 256, 100, 0, None, dummy, None, 0,
-             None, 0, None) == 2      # K % 64 != 0
+             0, None, 0, None) == 2      # K % 64 != 0
     assert g(dummy, dummy, dummy, dummy, dummy, 8, 1024, 32, dummy, dummy, dummy, 384, 256, 1, dummy, dummy, dummy, 0,
-             None, 0, None) == 2      # SwiGLU N % 256 != 0
+             0, None, 0, None) == 2      # SwiGLU N % 256 != 0
     assert g(dummy, dummy, dummy, dummy, dummy, 8, 1000, 32, dummy, dummy, dummy, 256, 256, 0, None, dummy, None, 0,
-             None, 0, None) == 1      # rows_capacity % 128 != 0
+             0, None, 0, None) == 1      # rows_capacity % 128 != 0
     assert g(dummy, dummy, dummy, dummy, dummy, 8, 1024, 32, dummy, dummy, dummy, 256, 256, 7, None, dummy, None, 0,
-             None, 0, None) == 1      # bad epilogue
+             0, None, 0, None) == 1      # bad epilogue
     assert g(dummy, dummy, dummy, dummy, dummy, 8, 1024, 32, dummy, dummy, dummy, 256, 256, 1, None, dummy, None, 0,
-             None, 0, None) == 1      # SWIGLU_NVFP4 without its scale pointers
+             0, None, 0, None) == 1      # SWIGLU_NVFP4 without its scale pointers
+    assert g(dummy, dummy, dummy, dummy, dummy, 8, 1024, 32, dummy, dummy, dummy, 256, 256, 0, None, dummy, None, 0,
+             5, None, 0, None) == 1      # unknown weight layout
+    assert g(dummy, dummy, dummy, dummy, dummy, 8, 1024, 32, dummy, dummy, dummy, 384, 256, 0, None, dummy, None, -1,
+             0, None, 0, None) == 2      # token-major tiles need N % 256 == 0
+    t = lib.nvfp4moe_tile_weights
+    t.argtypes = [p, ctypes.c_int64, ctypes.c_int, p, p]
+    assert t(dummy, 100, 256, dummy, None) == 2     # rows % 128
+    assert t(dummy, 128, 96, dummy, None) == 2      # K % 64
+    assert t(p(8), 128, 256, dummy, None) == 1      # misaligned
     q = lib.moe_quantize_nvfp4
     q.argtypes = [p, ctypes.c_int64, ctypes.c_int64, p, ctypes.c_int, p, p, p, ctypes.c_size_t, p]
     assert q(dummy, 4, 40, dummy, 0, dummy, dummy, None, 0, None) == 2     # cols % 16
@@ -96,3 +113,24 @@ def test_binding_imports_and_names_match_header():
     for n in ["moe_route_topk", "moe_quantize_nvfp4", "moe_permute", "moe_grouped_gemm_nvfp4", "moe_finalize",
               "moe_scales_to_blocked"]:
         assert callable(getattr(binding, n))
+
+
+def test_untile_weights_inverts_the_documented_tiling():
+    """The test utility that reads tiled weights back (used against the
+    oracle's codes on the GPU) inverts the layout the header defines, checked
+    against a direct box-by-box construction."""
+    import numpy as np
+    from tests import nvfp4_testutil as U
+    rng = np.random.default_rng(3)
+    for E, N, K in [(2, 128, 320), (3, 256, 512), (1, 128, 64), (2, 384, 768)]:
+        w = rng.integers(0, 256, size=(E, N, K // 2), dtype=np.uint8)
+        kc = (K + 255) // 256
+        tiled = np.zeros(E * N // 128 * kc * 16384, np.uint8)
+        rows = w.reshape(E * N, K // 2)
+        for rb in range(E * N // 128):
+            for c in range(kc):
+                base = (rb * kc + c) * 16384
+                for r in range(128):
+                    seg = rows[rb * 128 + r, c * 128:c * 128 + 128]
+                    tiled[base + r * 128:base + r * 128 + len(seg)] = seg
+        np.testing.assert_array_equal(U.untile_weights(tiled, E, N, K), w)
