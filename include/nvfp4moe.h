@@ -128,8 +128,8 @@ int nvfp4moe_tile_weights(const uint8_t* w_packed, int64_t rows, int K, uint8_t*
 
 /* ---- a1: routing ---------------------------------------------------------
  * Top-k expert selection with sigmoid scoring (page A, key finding 8 and its
- * closing paragraph: "OEA with proper sigmoid scoring" of the GLM-5 router)
- * or softmax.  Selection compares float32 v = logits + bias, descending, the
+ * closing paragraph, which name sigmoid as the GLM-5 router's score
+ * function) or softmax.  Selection compares float32 v = logits + bias, descending, the
  * lower expert index first on ties; slot j of a token holds its j-th
  * largest v.  Weights (computed in float64, stored float32):
  *   softmax: exp(v_j - max v) / sum over the k selected (renormalize = 1)
@@ -195,8 +195,9 @@ int moe_scales_to_blocked(const uint8_t* scales_row_major, int64_t rows, int64_t
                           uint8_t* scales_blocked, cudaStream_t stream);
 
 /* ---- a3: permutation -----------------------------------------------------
- * Expert-first layout with token reordering (page A, section 6: "expert-
- * first layout", "token reordering with fused reduction").  Flat id
+ * Expert-first layout with token reordering (page A, section 6: two of its
+ * listed techniques, the expert-first layout and reordering tokens so that
+ * a fused reduction can gather them back).  Flat id
  * f = t*k + j.  Expert e's rows are the flat ids routed to e in ascending
  * f.  Each expert's rows start at a multiple of 128 in the permuted
  * buffers ("row_offsets"), so that a tensor-core tile never mixes experts.
