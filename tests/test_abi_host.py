@@ -134,3 +134,33 @@ def test_untile_weights_inverts_the_documented_tiling():
                     seg = rows[rb * 128 + r, c * 128:c * 128 + 128]
                     tiled[base + r * 128:base + r * 128 + len(seg)] = seg
         np.testing.assert_array_equal(U.untile_weights(tiled, E, N, K), w)
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """A copy of the package without libnvfp4moe.so does not import: there is
+    no fallback implementation to run instead."""
+    import shutil
+    import subprocess
+    import sys
+    src = os.path.join(ROOT, "nvfp4_block_scaled_07_gb300")
+    dst = tmp_path / "nvfp4_block_scaled_07_gb300"
+    dst.mkdir()
+    for name in ("__init__.py", "binding.py", "workloads.py"):
+        shutil.copy(os.path.join(src, name), dst / name)
+    r = subprocess.run([sys.executable, "-c", "import nvfp4_block_scaled_07_gb300.binding"], cwd=tmp_path,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "no fallback" in r.stderr
+
+
+def test_binding_rejects_host_tensors():
+    """Host (CPU) tensors are refused before any call into the library, so a
+    caller cannot end up with a host computation."""
+    import torch
+    from nvfp4_block_scaled_07_gb300 import binding as B
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        B.moe_route_topk(torch.zeros(4, 8), 2)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        B.moe_quantize_nvfp4(torch.zeros(4, 64, dtype=torch.bfloat16))
+    with pytest.raises(TypeError):
+        B.moe_quantize_nvfp4(torch.zeros(4, 64, dtype=torch.float64))
