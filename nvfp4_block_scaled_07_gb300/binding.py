@@ -481,7 +481,10 @@ def moe_grouped_gemm_nvfp4(a_packed, a_scales, a_gscale, counts, row_offsets, w_
                            workspace=None):
     """Returns c_out (and c_scales for EPI_SWIGLU_NVFP4).  workspace: a zeroed
     alloc_gemm_workspace() for the dynamic tile schedule, None for static.
-    w_packed: row-major [E, N, K/2] or TiledWeights."""
+    w_packed: row-major [E, N, K/2] or TiledWeights.  m_total: the routed
+    rows (T*k), not the padded capacity; it picks the tile orientation."""
+    if m_total is None:
+        raise ValueError("m_total (the routed rows, T*k) is required: it chooses the tile orientation")
     E, N, K, w_ptr, w_layout = _weights_args(w_packed)
     cap = a_packed.shape[0]
     dev = a_packed.device
@@ -513,8 +516,6 @@ def moe_grouped_gemm_nvfp4(a_packed, a_scales, a_gscale, counts, row_offsets, w_
         _need(out, torch.float32, (cap, N // 2), "out")
     else:
         raise ValueError(f"epilogue {epilogue}")
-    if m_total is None:
-        m_total = cap
     ws_p, ws_n = _ws_args(workspace)
     _check(_lib.moe_grouped_gemm_nvfp4(_ptr(a_packed), _ptr(a_scales), _ptr(a_gscale), _ptr(counts),
                                        _ptr(row_offsets), E, cap, int(m_total), w_ptr, _ptr(w_scales),
@@ -528,6 +529,8 @@ def moe_grouped_gemm_mxfp4(a_packed, a_scales, counts, row_offsets, w_packed, w_
                            m_total=None, tile_n=0, out=None, out_scales=None, workspace=None):
     """MXFP4 grouped GEMM.  Returns c_out (and c_scales for EPI_SWIGLU_MXFP4).
     w_packed: row-major [E, N, K/2] or TiledWeights."""
+    if m_total is None:
+        raise ValueError("m_total (the routed rows, T*k) is required: it chooses the tile orientation")
     E, N, K, w_ptr, w_layout = _weights_args(w_packed)
     cap = a_packed.shape[0]
     dev = a_packed.device
@@ -554,8 +557,6 @@ def moe_grouped_gemm_mxfp4(a_packed, a_scales, counts, row_offsets, w_packed, w_
         _need(out, torch.float32, (cap, N // 2), "out")
     else:
         raise ValueError(f"epilogue {epilogue}")
-    if m_total is None:
-        m_total = cap
     ws_p, ws_n = _ws_args(workspace)
     _check(_lib.moe_grouped_gemm_mxfp4(_ptr(a_packed), _ptr(a_scales), _ptr(counts), _ptr(row_offsets), E, cap,
                                        int(m_total), w_ptr, _ptr(w_scales), N, K, epilogue, _ptr(out),

@@ -164,3 +164,14 @@ def test_binding_rejects_host_tensors():
         B.moe_quantize_nvfp4(torch.zeros(4, 64, dtype=torch.bfloat16))
     with pytest.raises(TypeError):
         B.moe_quantize_nvfp4(torch.zeros(4, 64, dtype=torch.float64))
+
+
+def test_grouped_gemm_binding_requires_the_routed_row_count():
+    """The padded capacity would always pick token-major tiles, so the binding
+    asks for the routed rows instead of guessing them."""
+    import torch
+    from nvfp4_block_scaled_07_gb300 import binding as B
+    with pytest.raises(ValueError, match="m_total"):
+        B.moe_grouped_gemm_nvfp4(*([torch.zeros(1)] * 8))
+    with pytest.raises(ValueError, match="m_total"):
+        B.moe_grouped_gemm_mxfp4(*([torch.zeros(1)] * 6))
