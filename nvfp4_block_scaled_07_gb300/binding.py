@@ -584,8 +584,11 @@ def moe_finalize(y, flat_to_perm, topk_w, out=None):
 class MoELayer:
     """Quantised expert weights plus every buffer of one layer shape.
 
-    forward() enqueues the layer on the current stream and allocates
-    nothing.  With fused_prepare (the default): four launches --
+    forward() enqueues the layer on the current stream.  Buffers are
+    allocated for one batch size T (at construction when T is given, else at
+    the first call, and again when T changes); otherwise forward() allocates
+    nothing, and the tensor it returns is overwritten by the next call
+    unless the caller passes `out`.  With fused_prepare (the default): four launches --
     moe_prepare (route + quantise + permute; moe_prepare_mxfp4 for
     fmt="mxfp4"), gate/up GEMM with SwiGLU and requantisation, down GEMM,
     finalize -- otherwise the six separate calls."""
@@ -632,7 +635,8 @@ class MoELayer:
         self.x_gscale = _empty((1,), torch.float32, dev)
         self.xq = _empty((T, H // 2), torch.uint8, dev)
         self.xs = _empty((T, H // (32 if self.fmt == "mxfp4" else 16)), torch.uint8, dev)
-        self.q_ws = _empty((64,), torch.uint8, dev)
+        self.q_ws = _empty((max(1, int(_lib.moe_quantize_nvfp4_workspace_size(T, H, QUANT_COMPUTE_GLOBAL))),),
+                           torch.uint8, dev)
         self.r_ws = _empty((int(_lib.moe_route_batch_aware_workspace_size(E)),), torch.uint8, dev)
         self.perm = alloc_permutation(T, E, k, H, dev, self.fmt)
         self.p_ws = _empty((moe_permute_workspace_size(T, E, k),), torch.uint8, dev)
