@@ -507,7 +507,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--tile-gate-up", type=int, default=0)
     ap.add_argument("--tile-down", type=int, default=0)
-    ap.add_argument("--cpu-experts", type=int, default=4)
+    ap.add_argument("--cpu-experts", type=int, default=14)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--k-primary", type=int, default=None,
                     help="batch-aware routing: experts each token keeps by its own scores (default k: plain top-k)")
