@@ -174,3 +174,48 @@ def test_bf16_rounding_matches_torch_for_float32_inputs():
     mid = 1.0 + 2.0 ** -8
     assert O.round_to_bf16(np.float64(mid + 2.0 ** -40)) == 1.0 + 2.0 ** -7
     assert O.round_to_bf16(np.float64(mid)) == 1.0
+
+
+def _bf16_value(bits):
+    """Exact value of a bf16 bit pattern (the top half of a float32)."""
+    return float(np.array([bits << 16], np.uint32).view(np.float32)[0])
+
+
+def _nearest_bf16_brute(v):
+    """Nearest bfloat16 to the float64 v by exact rational comparison of the
+    bf16 patterns around it; ties to the even pattern; beyond the largest
+    finite bf16 by half a step or more, infinity."""
+    from fractions import Fraction
+    if v == 0:
+        return v
+    a = abs(v)
+    top = 0x7F7F                                     # largest finite bf16
+    if Fraction(a) >= Fraction(_bf16_value(top)) + Fraction(2) ** (127 - 8):
+        return float(np.copysign(np.inf, v))
+    f32 = np.float32(min(a, float(np.finfo(np.float32).max)))
+    b = int(np.array([f32], np.float32).view(np.uint32)[0]) >> 16
+    best = None
+    for c in range(max(0, b - 2), min(top, b + 2) + 1):
+        d = abs(Fraction(_bf16_value(c)) - Fraction(a))
+        if best is None or d < best[0] or (d == best[0] and c % 2 == 0):
+            best = (d, c)
+    return float(np.copysign(_bf16_value(best[1]), v))
+
+
+def test_bf16_rounding_of_float64_brute_force():
+    """round_to_bf16 (used on float64 GEMM sums and the finalize sum) against
+    the exact nearest bf16: normal values, the bf16 subnormal range, exact
+    midpoints, points just off them, and the overflow boundary."""
+    rng = np.random.default_rng(16)
+    vals = list(rng.standard_normal(1500) * np.exp2(rng.integers(-140, 128, 1500)))
+    for b in rng.integers(1, 0x7F7F, 300):
+        lo, hi = _bf16_value(int(b)), _bf16_value(int(b) + 1)
+        mid = (lo + hi) / 2                            # exact in float64
+        vals += [mid, np.nextafter(mid, 0), np.nextafter(mid, np.inf), -mid]
+    top = _bf16_value(0x7F7F)
+    vals += [top, top + 2.0 ** (127 - 8), np.nextafter(top + 2.0 ** (127 - 8), 0), 2.0 ** -133, 2.0 ** -134,
+             3 * 2.0 ** -135, 2.0 ** -200, -2.0 ** -126]
+    vals = np.array(vals, np.float64)
+    got = O.round_to_bf16(vals)
+    ref = np.array([_nearest_bf16_brute(float(v)) for v in vals])
+    assert np.array_equal(got, ref, equal_nan=False), vals[got != ref][:5]
