@@ -396,9 +396,9 @@ int moe_grouped_gemm_mxfp4(const uint8_t* a_packed, const uint8_t* a_scales,
                            int w_layout, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ---- a6: finalize ----------------------------------------------------------
- * Router-weighted reduce back to token order (page A, section 6: "token
- * reordering with fused reduction"; page C, Context: the finalize
- * epilogue): out[t, :] = sum_{j<k} topk_w[t, j] * y[flat_to_perm[t*k + j], :]
+ * Router-weighted reduce back to token order (page A, section 6: the
+ * technique that reorders tokens by expert and fuses the weighted sum back;
+ * page C, Context: the finalize epilogue): out[t, :] = sum_{j<k} topk_w[t, j] * y[flat_to_perm[t*k + j], :]
  * accumulated in float32 in slot order, stored as bf16.
  * y device bf16 [rows_capacity, H]; flat_to_perm device int32 [T*k];
  * topk_w device float32 [T, k]; out device bf16 [T, H].  H % 8 == 0.
