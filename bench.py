@@ -371,20 +371,30 @@ def run_ours(args, w):
 # ----------------------------------------------------------------------------
 # the CPU oracle on a bounded sample (baseline and reference arm)
 # ----------------------------------------------------------------------------
-def oracle_quantized_weights(w_gu_dev, w_d_dev, experts):
-    """Oracle NVFP4 quantisation of the weights of `experts` (untimed setup)."""
+def oracle_quantized_weights(w_gu_dev, w_d_dev, experts, fmt="nvfp4"):
+    """Oracle quantisation (NVFP4 or MXFP4) of the weights of `experts` (untimed setup)."""
     from oracle import nvfp4_moe_oracle as O
     q = {}
     for e in experts:
         for name, src in (("gu", w_gu_dev), ("d", w_d_dev)):
             a = src[int(e)].float().cpu().numpy()
-            g = O.global_scale(a)
-            p, s = O.quantize_nvfp4(a, g)
-            q[(name, int(e))] = (p, s, g)
+            if fmt == "mxfp4":
+                q[(name, int(e))] = O.quantize_mxfp4(a) + (None,)
+            else:
+                g = O.global_scale(a)
+                q[(name, int(e))] = O.quantize_nvfp4(a, g) + (g,)
     return q
 
 
-def oracle_sample(w, x32, lg, b, q, experts, islice=None):
+def oracle_route(w, lg, b, k_primary=None):
+    """The oracle router the layer uses: top-k, or batch-aware with k_primary < k."""
+    from oracle import nvfp4_moe_oracle as O
+    if k_primary is None or k_primary == w.k:
+        return O.route_topk(lg, b, w.k, w.score, w.renormalize)
+    return O.route_batch_aware(lg, b, w.k, k_primary, w.score, w.renormalize)
+
+
+def oracle_sample(w, x32, lg, b, q, experts, islice=None, fmt="nvfp4", k_primary=None, return_out=False):
     """The oracle layer restricted to the routed rows of `experts`.
 
     Times separately the batch-wide steps (routing of every token, the global
@@ -394,12 +404,14 @@ def oracle_sample(w, x32, lg, b, q, experts, islice=None):
     intermediate columns [a, b) of each expert are computed: gate rows
     [a, b), up rows [I + a, I + b) and the down GEMM over that K range (a
     partial sum of the expert's output); a and b are multiples of 64.
+    fmt "mxfp4" runs the MXFP4 layer; k_primary < k routes batch-aware.
     Returns (batch seconds, expert seconds, rows processed, number of active
-    experts)."""
+    experts), and the float64 sum before its bf16 rounding when return_out."""
     from oracle import nvfp4_moe_oracle as O
+    mx = fmt == "mxfp4"
     t0 = time.perf_counter()
-    idx, wts = O.route_topk(lg, b, w.k, w.score, w.renormalize)
-    s_x = O.global_scale(x32)
+    idx, wts = oracle_route(w, lg, b, k_primary)
+    s_x = None if mx else O.global_scale(x32)
     counts, offsets, p2f, f2p = O.permute(idx, w.E)
     t1 = time.perf_counter()
     out = np.zeros((w.T, w.H))
@@ -410,24 +422,33 @@ def oracle_sample(w, x32, lg, b, q, experts, islice=None):
         if r1 == r0:
             continue
         tok = p2f[r0:r1] // w.k
-        xq, xs = O.quantize_nvfp4(x32[tok], s_x)
         gp, gs, gg = q[("gu", e)]
         dp, ds, dg = q[("d", e)]
         a, c = (0, w.I) if islice is None else islice
+        blk = 32 if mx else 16
         if (a, c) != (0, w.I):
             sel = np.r_[a:c, w.I + a:w.I + c]
             gp, gs = gp[sel], gs[sel]
-            dp, ds = dp[:, a // 2:c // 2], ds[:, a // 16:c // 16]
+            dp, ds = dp[:, a // 2:c // 2], ds[:, a // blk:c // blk]
         sub = np.array([0, r1 - r0])
-        gu = O.grouped_gemm(xq, xs, s_x, sub, gp[None], gs[None], np.array([gg]))
-        h = O.swiglu(gu, c - a).astype(np.float32)
-        hq, hs = O.quantize_nvfp4(h, np.float32(w.h_scale))
-        y = O.round_to_bf16(O.grouped_gemm(hq, hs, np.float32(w.h_scale), sub, dp[None], ds[None], np.array([dg])))
+        if mx:
+            xq, xs = O.quantize_mxfp4(x32[tok])
+            h = O.swiglu(O.grouped_gemm_mx(xq, xs, sub, gp[None], gs[None]), c - a).astype(np.float32)
+            hq, hs = O.quantize_mxfp4(h)
+            y = O.round_to_bf16(O.grouped_gemm_mx(hq, hs, sub, dp[None], ds[None]))
+        else:
+            xq, xs = O.quantize_nvfp4(x32[tok], s_x)
+            gu = O.grouped_gemm(xq, xs, s_x, sub, gp[None], gs[None], np.array([gg]))
+            h = O.swiglu(gu, c - a).astype(np.float32)
+            hq, hs = O.quantize_nvfp4(h, np.float32(w.h_scale))
+            y = O.round_to_bf16(O.grouped_gemm(hq, hs, np.float32(w.h_scale), sub, dp[None], ds[None],
+                                               np.array([dg])))
         np.add.at(out, tok, wts.reshape(-1)[p2f[r0:r1]][:, None] * y)
         rows += r1 - r0
     O.round_to_bf16(out)
     t2 = time.perf_counter()
-    return t1 - t0, t2 - t1, rows, int((counts > 0).sum())
+    res = (t1 - t0, t2 - t1, rows, int((counts > 0).sum()))
+    return res + (out,) if return_out else res
 
 
 def cpu_baseline(w, args, layer_inputs):
@@ -438,13 +459,14 @@ def cpu_baseline(w, args, layer_inputs):
     experts = active[np.linspace(0, len(active) - 1, n).astype(int)]
     # weights in bf16 for the sampled experts, regenerated from the same seed
     inp = W.device_inputs(w, seed=args.seed, device=x.device)
-    q = oracle_quantized_weights(inp["w_gu"], inp["w_d"], experts)
+    fmt, k0 = layer.fmt, (layer.k_primary if layer.k_primary < w.k else None)
+    q = oracle_quantized_weights(inp["w_gu"], inp["w_d"], experts, fmt)
     del inp
     torch.cuda.empty_cache()
     x32 = x.float().cpu().numpy()
     lg = logits.cpu().numpy()
     b = None if bias is None else bias.cpu().numpy()
-    t_batch, t_exp, rows, n_active = oracle_sample(w, x32, lg, b, q, experts)
+    t_batch, t_exp, rows, n_active = oracle_sample(w, x32, lg, b, q, experts, fmt=fmt, k_primary=k0)
     full = t_batch + t_exp * n_active / n
     return {"value": round(w.T / full, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"batch-wide steps ({t_batch:.2f} s) plus {n} of {n_active} active experts ({rows} routed "
@@ -458,43 +480,52 @@ def run_reference(args, w):
     if rank != 0:
         return
     torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
-    inp = W.device_inputs(w, seed=args.seed, device=dev)
-    from oracle import nvfp4_moe_oracle as O
+    inp = W.device_inputs(w, seed=args.seed, device=torch.device("cuda", 0))
+    print(json.dumps(reference_steps(args, w, inp, world)), flush=True)
+
+
+def reference_steps(args, w, inp, world=1):
+    """The oracle arm: each step one bounded sample of the workload through
+    the oracle (format and routing as the layer's), extrapolated to the
+    layer.  inp: the workload's tensors on any device.  Returns the JSON
+    record."""
+    fmt = args.format
+    k0 = args.k_primary if args.k_primary is not None and args.k_primary < w.k else None
     x32 = inp["x"].float().cpu().numpy()
     lg = inp["logits"].cpu().numpy()
     b = None if inp["bias"] is None else inp["bias"].cpu().numpy()
-    idx, _ = O.route_topk(lg, b, w.k, w.score, w.renormalize)
+    idx, _ = oracle_route(w, lg, b, k0)
     active = np.unique(idx)
     # a small fixed set of experts, quantised once (untimed) and cycled through the steps
     cycle = active[np.linspace(0, len(active) - 1, min(len(active), 4)).astype(int)]
-    q = oracle_quantized_weights(inp["w_gu"], inp["w_d"], cycle)
+    q = oracle_quantized_weights(inp["w_gu"], inp["w_d"], cycle, fmt)
     del inp
     torch.cuda.empty_cache()
     times = []
     width = min(w.I, 256)
-    nsl = w.I // width
+    nsl = -(-w.I // width)                      # the last slice may be narrower
     for s in range(args.warmup + args.steps):
         j = s % (len(cycle) * nsl)
-        sl = ((j % nsl) * width, (j % nsl + 1) * width)
-        t_batch, t_exp, _, n_active = oracle_sample(w, x32, lg, b, q, [cycle[j // nsl]], islice=sl)
+        sl = ((j % nsl) * width, min(w.I, (j % nsl + 1) * width))
+        t_batch, t_exp, _, n_active = oracle_sample(w, x32, lg, b, q, [cycle[j // nsl]], islice=sl, fmt=fmt,
+                                                    k_primary=k0)
         if s >= args.warmup:
             # one slice of one expert per step, extrapolated to the layer
             times.append(t_batch + t_exp * nsl * n_active)
     ms = float(np.mean(times)) * 1e3
     val = w.T / (ms * 1e-3)
-    res = {"metric": METRIC, "impl": "reference", "value": round(val, 4), "unit": "tokens/s", "n_gpus": world,
-           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1), "higher_is_better": True,
-           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": w.name, **w.describe(), "active_experts": int(len(active))},
-           "cpu_baseline": {"value": round(val, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-                            "sample": f"per step: the batch-wide steps (routing, global scale, permutation) "
-                                      f"plus one {width}-column slice of the intermediate dimension of one active "
-                                      f"expert (of a cycled set of 4) for its routed rows through the float64 "
-                                      f"oracle; the expert part multiplied by {nsl} slices and the number of "
-                                      f"active experts"},
-           "e2e": {"value": round(val, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(res), flush=True)
+    return {"metric": METRIC, "impl": "reference", "value": round(val, 4), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, **w.describe(), "active_experts": int(len(active)), "format": fmt,
+                       "routing": "top-k" if k0 is None else f"batch-aware, k_primary={k0}"},
+            "cpu_baseline": {"value": round(val, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"per step: the batch-wide steps (routing, global scale, permutation) "
+                                       f"plus one {width}-column slice of the intermediate dimension of one active "
+                                       f"expert (of a cycled set of 4) for its routed rows through the float64 "
+                                       f"oracle; the expert part multiplied by {nsl} slices and the number of "
+                                       f"active experts"},
+            "e2e": {"value": round(val, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def main():
