@@ -175,3 +175,29 @@ def test_grouped_gemm_binding_requires_the_routed_row_count():
         B.moe_grouped_gemm_nvfp4(*([torch.zeros(1)] * 8))
     with pytest.raises(ValueError, match="m_total"):
         B.moe_grouped_gemm_mxfp4(*([torch.zeros(1)] * 6))
+
+
+@pytest.mark.parametrize("rows,cols,block", [(1, 64, 16), (130, 320, 16), (256, 1024, 16), (5, 128, 32),
+                                             (300, 640, 32)])
+def test_blocked_layout_helper_follows_the_header(lib, rows, cols, block):
+    """The test utility that reads the library's blocked scales, against the
+    layout as the header states it, written out loop by loop: 128-row x
+    (4 * block)-element groups of 512 bytes at (rb * groups_per_row + kb) *
+    512, row r of a group at (r % 32) * 16 + (r / 32) * 4, then the scale's
+    index within its group of four.  Every byte of the buffer is addressed
+    exactly once, and the buffer size is the library's."""
+    import numpy as np
+    from tests import nvfp4_testutil as U
+    rp = -(-rows // 128) * 128
+    per_row = cols // block
+    groups = cols // (4 * block)
+    idx = U.blocked_index(rp, cols, block)
+    for r in range(rp):
+        for j in range(per_row):
+            rb, kb, rr = r // 128, j // 4, r % 128
+            assert idx[r, j] == (rb * groups + kb) * 512 + (rr % 32) * 16 + (rr // 32) * 4 + j % 4
+    assert sorted(idx.ravel().tolist()) == list(range(rp * per_row))
+    q = lib.nvfp4moe_blocked_scales_bytes if block == 16 else lib.nvfp4moe_mxfp4_blocked_scales_bytes
+    q.restype = ctypes.c_size_t
+    q.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    assert q(rows, cols) == rp * per_row
