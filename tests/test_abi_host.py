@@ -201,3 +201,41 @@ def test_blocked_layout_helper_follows_the_header(lib, rows, cols, block):
     q.restype = ctypes.c_size_t
     q.argtypes = [ctypes.c_int64, ctypes.c_int64]
     assert q(rows, cols) == rp * per_row
+
+
+def _header_signatures():
+    """{name: (return kind, [argument kinds])} from the header's declarations;
+    kinds: p (pointer), i (int), i64 (int64_t), sz (size_t), cstr (const char*)."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    text = re.sub(r"^\s*#.*$", "", text, flags=re.M)
+
+    def kind(decl):
+        decl = decl.strip()
+        if decl in ("", "void"):
+            return None
+        if "*" in decl or decl.startswith("cudaStream_t"):
+            return "cstr" if decl.replace(" ", "").startswith("constchar*") and "(" not in decl else "p"
+        t = decl.split()[0] if not decl.startswith("const ") else decl.split()[1]
+        return {"int": "i", "int64_t": "i64", "size_t": "sz"}[t]
+
+    sigs = {}
+    for m in re.finditer(r"([\w\s\*]+?)\b((?:moe|nvfp4moe)_\w+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        ret = m.group(1).split("\n")[-1].strip()
+        args = [kind(a) for a in m.group(3).split(",")]
+        sigs[m.group(2)] = (kind(ret + " x") if "*" not in ret else "cstr", [a for a in args if a])
+    return sigs
+
+
+def test_binding_signatures_match_the_header():
+    """Every ctypes signature in the binding has the header's argument count
+    and kinds (a pointer, an int, an int64_t or a size_t in each place), so a
+    call can never shift its arguments."""
+    from nvfp4_block_scaled_07_gb300 import binding as B
+    kinds = {ctypes.c_void_p: "p", ctypes.c_int: "i", ctypes.c_int64: "i64", ctypes.c_size_t: "sz",
+             ctypes.c_char_p: "cstr"}
+    hdr = _header_signatures()
+    assert set(B._SIGS) == set(hdr), set(B._SIGS) ^ set(hdr)
+    for name, (res, args) in B._SIGS.items():
+        h_res, h_args = hdr[name]
+        assert [kinds[a] for a in args] == h_args, name
+        assert kinds[res] == h_res, name
