@@ -203,9 +203,11 @@ def _nearest_bf16_brute(v):
 
 
 def test_bf16_rounding_of_float64_brute_force():
-    """round_to_bf16 (used on float64 GEMM sums and the finalize sum) against
-    the exact nearest bf16: normal values, the bf16 subnormal range, exact
-    midpoints, points just off them, and the overflow boundary."""
+    """round_to_bf16 against the exact nearest bf16: normal values, the bf16
+    subnormal range, exact midpoints, points just off them, and the overflow
+    boundary.  Reading R7 rounds the down projection's float64 sum and the
+    finalize sum straight to bfloat16 (round to nearest, ties to even), so
+    the inputs here are float64, not float32."""
     rng = np.random.default_rng(16)
     vals = list(rng.standard_normal(1500) * np.exp2(rng.integers(-140, 128, 1500)))
     for b in rng.integers(1, 0x7F7F, 300):

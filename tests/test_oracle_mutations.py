@@ -6,7 +6,12 @@ divisor, a bias left out, a reversed order, a swapped gate and up, a double
 rounding -- by replacing one function of the oracle module for the duration
 of the case, and runs the pins that cover that function.  At least one of
 them must fail; otherwise that part of the oracle would be unpinned.  The
-mistakes are planted in the oracle only, never in the library.
+mistakes are planted in the oracle only, never in the library.  Each one
+breaks a reading the oracle follows: the E2M1 and ue4m3 formats ("SM120 FP4
+Kernel Research Campaign", section 1), the block scale and element code
+rules (R2, R3), the nibble order (R4), the per-tensor scale (R1), routing
+(R5), the permutation order (R6), the layer's SwiGLU, bf16 rounding and
+slot-order finalize (R7), batch-aware routing (R8) and the MX exponent (R9).
 """
 import numpy as np
 import pytest
