@@ -71,6 +71,7 @@ def test_size_queries(lib):
 
 
 def test_argument_validation_before_any_device_work(lib):
+    _no_device()
     p = ctypes.c_void_p
     lib.moe_route_topk.argtypes = [p, p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, p, p, p]
     assert lib.moe_route_topk(None, None, 4, 2048, 2, 1, 1, None, None, None) == 2    # E > 1024
@@ -239,3 +240,47 @@ def test_binding_signatures_match_the_header():
         h_res, h_args = hdr[name]
         assert [kinds[a] for a in args] == h_args, name
         assert kinds[res] == h_res, name
+
+
+def _no_device():
+    """These cases pass dummy pointers: each must be refused (or be a no-op)
+    before any device work, so they run only where no GPU could be touched."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host-validation cases with dummy pointers run only without a GPU")
+
+
+def test_validation_of_the_other_calls(lib):
+    _no_device()
+    p = ctypes.c_void_p
+    dummy = p(256)
+    r = lib.moe_route_topk
+    r.argtypes = [p, p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, p, p, p]
+    assert r(dummy, None, 4, 8, 9, 1, 1, dummy, dummy, None) == 2        # k > E
+    assert r(dummy, None, 4, 2048, 8, 1, 1, dummy, dummy, None) == 2     # E > 1024
+    assert r(dummy, None, 4, 64, 33, 1, 1, dummy, dummy, None) == 2      # k > 32
+    assert r(dummy, None, 4, 8, 2, 7, 1, dummy, dummy, None) == 1        # unknown score function
+    assert r(dummy, None, -1, 8, 2, 1, 1, dummy, dummy, None) == 1       # T < 0
+    assert r(None, None, 4, 8, 2, 1, 1, dummy, dummy, None) == 1         # null logits
+    q = lib.moe_quantize_nvfp4
+    q.argtypes = [p, ctypes.c_int64, ctypes.c_int64, p, ctypes.c_int, p, p, p, ctypes.c_size_t, p]
+    assert q(dummy, 4, 40, dummy, 0, dummy, dummy, None, 0, None) == 2   # cols % 16
+    assert q(dummy, 4, 48, dummy, 2, dummy, dummy, None, 0, None) == 2   # blocked scales need cols % 64
+    assert q(dummy, 4, 64, dummy, 8, dummy, dummy, None, 0, None) == 1   # unknown flag
+    assert q(p(258), 4, 64, dummy, 0, dummy, dummy, None, 0, None) == 1  # misaligned x
+    assert q(dummy, 4, 64, dummy, 1, dummy, dummy, None, 0, None) == 4   # global scale needs its workspace
+    f = lib.moe_finalize
+    f.argtypes = [p, p, p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, p, p]
+    assert f(dummy, dummy, dummy, 4, 2, 12, 1024, dummy, None) == 2      # H % 8
+    assert f(dummy, dummy, dummy, 4, 0, 16, 1024, dummy, None) == 1      # k < 1
+    assert f(p(264), dummy, dummy, 4, 2, 16, 1024, dummy, None) == 1     # misaligned y
+    pr = lib.moe_permute
+    pr.argtypes = [p, ctypes.c_int, ctypes.c_int, ctypes.c_int, p, p, ctypes.c_int] + [p] * 7 + [p, ctypes.c_size_t, p]
+    args = [dummy] * 7
+    assert pr(dummy, 4, 8, 2, dummy, dummy, 100, *args, dummy, 1 << 20, None) == 2    # H % 64
+    assert pr(dummy, 4, 8, 9, dummy, dummy, 128, *args, dummy, 1 << 20, None) == 2    # k > E
+    assert pr(dummy, 4, 8, 2, dummy, dummy, 128, *args, dummy, 4, None) == 4          # workspace too small
+    # empty batches are no-ops that touch nothing, also with null buffers
+    assert r(None, None, 0, 8, 2, 1, 1, None, None, None) == 0
+    assert q(None, 0, 64, None, 1, None, None, None, 0, None) == 0
+    assert f(None, None, None, 0, 2, 16, 0, None, None) == 0
