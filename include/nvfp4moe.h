@@ -236,12 +236,17 @@ int moe_permute(const int32_t* topk_idx, int T, int E, int k,
  * at most 131072 routed rows (T*k) and 65536 segment-expert counters
  * (ceil(T*k/1024) * E); larger calls return NVFP4MOE_ERR_UNSUPPORTED
  * without launching.  Nothing is allocated or freed.
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  Every call shares the one array and overwrites
- * the part it uses, so no state carries over between calls, but calls whose
- * work overlaps on the GPU (other streams, other host threads) race on it:
- * serialise them. */
+ * Each call made outside stream capture looks up the array's device address
+ * (cudaGetSymbolAddress) with the calling thread's device current.  A call
+ * made while its stream is being captured cannot do that lookup and reuses
+ * the address found by the last uncaptured call on the same CUDA context;
+ * if there was none (first call on this device, or the device was reset
+ * since, which gives it a new context and may move the array), it returns
+ * NVFP4MOE_ERR_UNSUPPORTED without launching: make one uncaptured call on
+ * each device, and again after a device reset, before capturing.
+ * Every call shares the one array and overwrites the part it uses, so no
+ * state carries over between calls, but calls whose work overlaps on the
+ * GPU (other streams, other host threads) race on it: serialise them. */
 int moe_permute_no_alloc(const int32_t* topk_idx, int T, int E, int k,
                          const uint8_t* xq, const uint8_t* xs, int H,
                          int32_t* expert_counts, int32_t* expert_offsets, int32_t* row_offsets,

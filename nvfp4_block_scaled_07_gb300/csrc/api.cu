@@ -361,9 +361,11 @@ int moe_permute_no_alloc(const int32_t* topk_idx, int T, int E, int k, const uin
                    NVFP4MOE_ERR_INVALID_ARG, "misaligned pointer");
   DeviceInfo d;
   if (int st = current_device(&d)) return st;
-  return cuda_status(launch_permute_static_scratch(topk_idx, T, E, k, xq, xs, H, expert_counts, expert_offsets,
-                                                   row_offsets, perm_to_flat, flat_to_perm, a_packed, a_scales,
-                                                   moe_permute_rows_capacity(T, E, k), d.num_sms, stream),
+  int32_t* scratch = nullptr;
+  if (int st = permute_scratch_address(stream, &scratch)) return st;
+  return cuda_status(launch_permute_static_scratch(scratch, topk_idx, T, E, k, xq, xs, H, expert_counts,
+                                                   expert_offsets, row_offsets, perm_to_flat, flat_to_perm, a_packed,
+                                                   a_scales, moe_permute_rows_capacity(T, E, k), d.num_sms, stream),
                      "permute (static scratch) launch");
 }
 

@@ -47,11 +47,16 @@ cudaError_t launch_quantize_mx(const void* x, int64_t rows, int64_t cols, bool b
 constexpr int64_t kNoAllocMaxRoutedRows = 131072;
 constexpr int64_t kNoAllocMaxSegmentExperts = 65536;
 
-cudaError_t launch_permute_static_scratch(const int32_t* topk_idx, int T, int E, int k, const uint8_t* xq,
-                                          const uint8_t* xs, int H, int32_t* counts, int32_t* offsets,
-                                          int32_t* row_offsets, int32_t* perm_to_flat, int32_t* flat_to_perm,
-                                          uint8_t* a_packed, uint8_t* a_scales, int64_t rows_capacity, int num_sms,
-                                          cudaStream_t st);
+// Device address of the static scratch for the current device and CUDA
+// context (looked up outside stream capture; during capture, the address the
+// last uncaptured call on the same context found).  Returns an NVFP4MOE
+// status, with the message set on failure.
+int permute_scratch_address(cudaStream_t st, int32_t** base);
+cudaError_t launch_permute_static_scratch(int32_t* base, const int32_t* topk_idx, int T, int E, int k,
+                                          const uint8_t* xq, const uint8_t* xs, int H, int32_t* counts,
+                                          int32_t* offsets, int32_t* row_offsets, int32_t* perm_to_flat,
+                                          int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales,
+                                          int64_t rows_capacity, int num_sms, cudaStream_t st);
 
 // Route + quantise + permute in one cooperative launch.  Workspace layout
 // (bytes from the start, 256-byte aligned pieces): grid-barrier words and

@@ -3,11 +3,14 @@
 // finalize.  All are HBM/latency bound (no contraction), so they use
 // 128-bit loads, one warp per token or row, and grid-stride loops sized to
 // a multiple of the SM count.
+#include <cuda.h>
+
 #include <cfloat>
 #include <climits>
 #include <cstdint>
 #include <mutex>
 
+#include "../../include/nvfp4moe.h"
 #include "common.cuh"
 #include "internal.h"
 #include "launch.cuh"
@@ -1167,36 +1170,96 @@ cudaError_t launch_finalize(const void* y, const int32_t* flat_to_perm, const fl
 // device memory at call time.  The scratch is one file-scope device array,
 // present on every GPU that loads the library until the process exits.
 // Host code may not use the array's name as a device address, so its
-// address is looked up once per device with cudaGetSymbolAddress.
+// address comes from cudaGetSymbolAddress, with the device current.
+// Outside stream capture the address is looked up on every call; a call
+// being captured cannot make that lookup (it may load the module) and uses
+// the address the last uncaptured call on the same CUDA context found.  The
+// cache is keyed on the context's process-unique id, so a device reset (a
+// new primary context, possibly with the array at a new address) is never
+// served a stale address.
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocMaxRoutedRows + 2 * kNoAllocMaxSegmentExperts];
 
 namespace {
 constexpr int kScratchDevices = 64;
+struct ScratchAddr {
+  unsigned long long ctx_id;  // 0: none recorded
+  int32_t* ptr;
+};
 std::mutex g_scratch_mutex;
-int32_t* g_scratch_addr[kScratchDevices] = {};
+ScratchAddr g_scratch_addr[kScratchDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Process-unique id of the calling thread's current CUDA context (the
+// driver's cuCtxGetId, reached through the runtime's entry-point table).
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS && *id != 0;
+}
 }  // namespace
 
-cudaError_t launch_permute_static_scratch(const int32_t* topk_idx, int T, int E, int k, const uint8_t* xq,
-                                          const uint8_t* xs, int H, int32_t* counts, int32_t* offsets,
-                                          int32_t* row_offsets, int32_t* perm_to_flat, int32_t* flat_to_perm,
-                                          uint8_t* a_packed, uint8_t* a_scales, int64_t rows_capacity, int num_sms,
-                                          cudaStream_t st) {
+int permute_scratch_address(cudaStream_t st, int32_t** base) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= kScratchDevices) return cudaErrorInvalidDevice;
-  int32_t* base = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
-      void* p = nullptr;
-      err = cudaGetSymbolAddress(&p, g_permute_scratch);  // device `dev` is current here
-      if (err != cudaSuccess) return err;
-      g_scratch_addr[dev] = static_cast<int32_t*>(p);
-    }
-    base = g_scratch_addr[dev];
+  if (err != cudaSuccess) {
+    set_error_detail("cudaGetDevice: %s", cudaGetErrorString(err));
+    return NVFP4MOE_ERR_CUDA;
   }
+  if (dev < 0 || dev >= kScratchDevices) {
+    set_error_detail("device %d: the static scratch keeps addresses for devices 0..%d", dev, kScratchDevices - 1);
+    return NVFP4MOE_ERR_UNSUPPORTED;
+  }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  err = cudaStreamIsCapturing(st, &cs);
+  if (err != cudaSuccess) {
+    set_error_detail("cudaStreamIsCapturing: %s", cudaGetErrorString(err));
+    return NVFP4MOE_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (cs == cudaStreamCaptureStatusNone) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_permute_scratch);  // device `dev` is current here
+    if (err != cudaSuccess) {
+      set_error_detail("cudaGetSymbolAddress of the static scratch: %s", cudaGetErrorString(err));
+      return NVFP4MOE_ERR_CUDA;
+    }
+    unsigned long long id = 0;
+    g_scratch_addr[dev] = current_context_id(&id) ? ScratchAddr{id, static_cast<int32_t*>(p)} : ScratchAddr{0, nullptr};
+    *base = static_cast<int32_t*>(p);
+    return NVFP4MOE_OK;
+  }
+  unsigned long long id = 0;
+  if (!current_context_id(&id) || g_scratch_addr[dev].ctx_id != id || !g_scratch_addr[dev].ptr) {
+    set_error_detail(
+        "moe_permute_no_alloc called during stream capture before any uncaptured call on this device's current "
+        "CUDA context: make one uncaptured call first (it looks up the static scratch's device address)");
+    return NVFP4MOE_ERR_UNSUPPORTED;
+  }
+  *base = g_scratch_addr[dev].ptr;
+  return NVFP4MOE_OK;
+}
+
+cudaError_t launch_permute_static_scratch(int32_t* base, const int32_t* topk_idx, int T, int E, int k,
+                                          const uint8_t* xq, const uint8_t* xs, int H, int32_t* counts,
+                                          int32_t* offsets, int32_t* row_offsets, int32_t* perm_to_flat,
+                                          int32_t* flat_to_perm, uint8_t* a_packed, uint8_t* a_scales,
+                                          int64_t rows_capacity, int num_sms, cudaStream_t st) {
   int32_t* rank = base;
   int32_t* seg_count = rank + kNoAllocMaxRoutedRows;
   int32_t* seg_base = seg_count + kNoAllocMaxSegmentExperts;

@@ -1,8 +1,10 @@
 """Full-size parity of the layer variants on the decode_t128 shape (T=128,
 E=256, k=8, H=6144, I=2048), in the launch configuration bench.py times:
 MXFP4 operands, and batch-aware routing (k_primary = 2).  Every token's
-routing and the whole permutation are compared exactly; one token's layer
-output is computed by the oracle, which quantises only that token's experts."""
+routing and the whole permutation are compared exactly; for 16 spread tokens
+the oracle (tests/oracle_samples.py) gives the SwiGLU requantisation of
+their routed rows, their down-projection rows and their layer output,
+quantising only the experts those tokens use."""
 import numpy as np
 import pytest
 import torch
@@ -10,10 +12,11 @@ import torch
 from oracle import nvfp4_moe_oracle as O
 from nvfp4_block_scaled_07_gb300 import workloads as W
 from tests import nvfp4_testutil as U
+from tests.oracle_samples import TokenSample
 
 pytestmark = pytest.mark.gpu
 
-TOKEN = 77
+TOKENS = np.arange(4, 128, 8)          # 16 spread tokens of the 128
 
 
 @pytest.fixture(scope="module")
@@ -67,35 +70,33 @@ def test_routing_and_permutation(run):
         assert len(np.unique(idx)) < len(np.unique(std))   # fewer experts stream their weights
 
 
-def test_one_token_output(run):
+@pytest.fixture(scope="module")
+def sample(run):
     r = run
     w = r["w"]
     idx, wts = routing(r)
     x32 = r["inp"]["x"].float().cpu().numpy()
-    if r["mx"]:
-        xq, xs = O.quantize_mxfp4(x32[TOKEN:TOKEN + 1])
-        xd = O.dequantize_mxfp4(xq, xs)
-    else:
-        s_x = O.global_scale(x32)
-        xq, xs = O.quantize_nvfp4(x32[TOKEN:TOKEN + 1], s_x)
-        xd = O.dequantize_nvfp4(xq, xs, s_x)
-    acc = np.zeros(w.H)
-    for j in range(w.k):
-        e = int(idx[TOKEN, j])
-        a_gu = r["inp"]["w_gu"][e].float().cpu().numpy()
-        a_d = r["inp"]["w_d"][e].float().cpu().numpy()
-        if r["mx"]:
-            gu = xd @ O.dequantize_mxfp4(*O.quantize_mxfp4(a_gu)).T
-            h = O.swiglu(gu, w.I).astype(np.float32)
-            hd = O.dequantize_mxfp4(*O.quantize_mxfp4(h))
-            y = O.round_to_bf16(hd @ O.dequantize_mxfp4(*O.quantize_mxfp4(a_d)).T)
-        else:
-            g_gu, g_d = O.global_scale(a_gu), O.global_scale(a_d)
-            gu = xd @ O.dequantize_nvfp4(*O.quantize_nvfp4(a_gu, g_gu), g_gu).T
-            h = O.swiglu(gu, w.I).astype(np.float32)
-            s_h = np.float32(w.h_scale)
-            hd = O.dequantize_nvfp4(*O.quantize_nvfp4(h, s_h), s_h)
-            y = O.round_to_bf16(hd @ O.dequantize_nvfp4(*O.quantize_nvfp4(a_d, g_d), g_d).T)
-        acc += wts[TOKEN, j] * y[0]
-    ref = O.round_to_bf16(acc)
-    U.check_close(r["out"][TOKEN], ref, what=("MXFP4" if r["mx"] else "batch-aware") + " layer, one token")
+    return TokenSample(TOKENS, x32, idx, wts, r["inp"]["w_gu"], r["inp"]["w_d"],
+                       fmt="mxfp4" if r["mx"] else "nvfp4", s_x=None if r["mx"] else O.global_scale(x32),
+                       s_h=w.h_scale)
+
+
+def _what(r):
+    return "MXFP4" if r["mx"] else "batch-aware"
+
+
+def test_sampled_rows_requant_and_down_projection(run, sample):
+    r = run
+    w, L = r["w"], r["layer"]
+    rows = L.perm.flat_to_perm.cpu().numpy()[sample.flat_ids(w.k)]
+    blk = 32 if r["mx"] else 16
+    got_c = O.unpack_codes(L.hq[torch.from_numpy(rows).cuda()].cpu().numpy())
+    got_s = U.from_blocked(L.hs.cpu().numpy(), L.perm.rows_capacity, w.I, blk)[rows]
+    assert got_s.size >= 1000
+    U.check_requant(got_c, got_s, sample.h_codes, sample.h_scales, block=blk)
+    got_y = L.y[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    U.check_close(got_y, sample.y, what=_what(r) + " down rows")
+
+
+def test_sampled_tokens_output(run, sample):
+    U.check_close(run["out"][TOKENS], sample.out, what=_what(run) + f" layer, {len(TOKENS)} tokens")

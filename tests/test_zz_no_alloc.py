@@ -44,6 +44,33 @@ def test_no_alloc_permute_matches_workspace_permute(B):
             assert torch.equal(getattr(got, name), getattr(ref, name)), (T, E, name)
 
 
+def test_no_alloc_permute_at_the_segment_counter_limit(B):
+    # E = 1024, k = 8, T = 8192: 64 segments of 1024 routed rows x 1024
+    # experts = 65536 per-segment counters, exactly the scratch's limit
+    T, E, k, H = 8192, 1024, 8, 64
+    rng = np.random.default_rng(4)
+    idx = torch.from_numpy(W.random_routing(T, E, k, seed=4)).cuda()
+    xq = torch.from_numpy(rng.integers(0, 256, size=(T, H // 2), dtype=np.uint8)).cuda()
+    xs = torch.from_numpy(rng.integers(0, 127, size=(T, H // 16), dtype=np.uint8)).cuda()
+    for _ in range(2):
+        ref = B.moe_permute(idx, E, xq, xs, out=_zeroed(B, T, E, k, H))
+        got = B.moe_permute_no_alloc(idx, E, xq, xs, out=_zeroed(B, T, E, k, H))
+        B.sync_status()
+        for name in ("counts", "offsets", "row_offsets", "perm_to_flat", "flat_to_perm", "a_packed", "a_scales"):
+            assert torch.equal(getattr(got, name), getattr(ref, name)), name
+
+
+def test_no_alloc_permute_rejects_one_segment_past_the_counter_limit(B):
+    T, E, k, H = 8193, 1024, 8, 64         # 65 segments x 1024 experts = 66560 counters > 65536
+    idx = torch.zeros((T, k), dtype=torch.int32, device="cuda")
+    xq = torch.zeros((T, H // 2), dtype=torch.uint8, device="cuda")
+    xs = torch.zeros((T, H // 16), dtype=torch.uint8, device="cuda")
+    with pytest.raises(B.Nvfp4MoeError) as ei:
+        B.moe_permute_no_alloc(idx, E, xq, xs)
+    assert ei.value.status == B.ERR_UNSUPPORTED
+    assert "static scratch" in str(ei.value)
+
+
 def test_no_alloc_permute_rejects_sizes_beyond_its_scratch(B):
     T, E, k, H = 16385, 64, 8, 64          # 131080 routed rows > 131072
     idx = torch.zeros((T, k), dtype=torch.int32, device="cuda")
