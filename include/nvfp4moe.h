@@ -77,8 +77,9 @@ extern "C" {
 #define NVFP4MOE_EPI_SWIGLU_F32     2  /* h = silu(gate) * up as float32 (unfused check) */
 #define NVFP4MOE_EPI_SWIGLU_MXFP4   3  /* h = silu(gate) * up, requantised to MXFP4 (MXFP4 GEMM only) */
 
-/* Grouped GEMM tile_n value for token-major tiles (see moe_grouped_gemm_nvfp4). */
+/* Grouped GEMM tile_n values for token-major tiles (see moe_grouped_gemm_nvfp4). */
 #define NVFP4MOE_TILE_TOKEN_MAJOR   (-1)
+#define NVFP4MOE_TILE_TOKEN_MAJOR_PAIR (-2)
 
 /* ---- library and device ------------------------------------------------- */
 
@@ -99,6 +100,32 @@ int nvfp4moe_device_check(int device);
  * raised by earlier calls on the current device.  Returns OK, TIMEOUT,
  * DEVICE_DATA or CUDA. */
 int nvfp4moe_sync_status(cudaStream_t stream);
+
+/* Time limit of every bounded device wait of the pipelines -- the mbarrier
+ * waits of the grouped GEMM's producer, MMA, scale-factor and epilogue
+ * roles, and the grid barriers of moe_prepare -- in microseconds, for the
+ * calls launched after it is set (process-wide, all devices).  A wait that
+ * exceeds it abandons its kernel without faulting, the kernel raises the
+ * sticky TIMEOUT flag and nvfp4moe_sync_status() returns
+ * NVFP4MOE_ERR_TIMEOUT (the opaque "Error Internal" failures that page C,
+ * "The Thinking Process", runs into are what this status replaces).  A
+ * serving loop can lower it to notice a stuck pipeline sooner; a limit
+ * shorter than a wait that legitimately occurs (a stage's operands, a
+ * tile's accumulator, a grid barrier: microseconds) aborts healthy calls.
+ * 0 restores the default, 2000000 (2 s); at most 60000000.  Returns OK or
+ * INVALID_ARG.  After a TIMEOUT, zero moe_prepare's workspace again. */
+int nvfp4moe_set_wait_limit_us(uint32_t us);
+uint32_t nvfp4moe_wait_limit_us(void);
+
+/* Self-test of the bounded waits: one CTA waits, through the grouped GEMM's
+ * bounded mbarrier wait and under the current wait limit, for the phase of
+ * a shared-memory mbarrier that expects `expected_arrivals` (1..64)
+ * arrivals and receives `arrivals` (0..32, one per thread).  With arrivals
+ * < expected_arrivals the phase can never complete: the wait gives up after
+ * the limit and the next nvfp4moe_sync_status() returns
+ * NVFP4MOE_ERR_TIMEOUT; otherwise OK.  Enqueued on `stream`; no memory is
+ * touched besides the flag.  No counterpart on the source pages. */
+int nvfp4moe_wait_selftest(uint32_t expected_arrivals, uint32_t arrivals, cudaStream_t stream);
 
 /* Bytes of a blocked scale buffer for a [rows, cols] NVFP4 matrix
  * (cols % 64 == 0): ceil(rows/128) * 128 * cols / 16.  0 on bad input. */
@@ -321,6 +348,12 @@ int moe_prepare(const float* logits, const float* bias, const void* x_bf16,
  * weight tiles (gate and up, or two consecutive output blocks) as one
  * N = 256 operand, which reads each token tile once per K step (for experts
  * with many rows; a partial tile still computes 128 token rows).
+ * NVFP4MOE_TILE_TOKEN_MAJOR_PAIR (N % 256 == 0): the same tiles on a pair
+ * of neighbouring SMs (a two-CTA cluster issuing cta_group::2 MMAs): 256
+ * tokens as M, 128 in each SM, and the 256 weight rows split between the
+ * two SMs' shared memory, so each SM stages half the weight bytes per K
+ * step; a partial tile still computes 256 token rows.  Runs the static
+ * schedule (the workspace is not used).
  * 0: token-major when N % 256 == 0 and m_total >= 64 * E, else 128.
  * The results do not depend on tile_n beyond float32 summation order.
  * Limits: K % 64 == 0; N % 128 == 0 (BF16) or N % 256 == 0 (SwiGLU);

@@ -33,6 +33,7 @@ QUANT_COMPUTE_GLOBAL = 1
 QUANT_SCALES_BLOCKED = 2
 EPI_BF16, EPI_SWIGLU_NVFP4, EPI_SWIGLU_F32, EPI_SWIGLU_MXFP4 = 0, 1, 2, 3
 TILE_TOKEN_MAJOR = -1  # grouped GEMM tile_n: 128 tokens as M, two weight tiles as one N = 256 operand
+TILE_TOKEN_MAJOR_PAIR = -2  # the same on a pair of SMs: 256 tokens as M (cta_group::2 MMAs)
 W_ROWMAJOR, W_TILED = 0, 1  # grouped GEMM weight layouts
 
 _i, _i64, _sz, _p, _f = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
@@ -42,6 +43,9 @@ _SIGS = {
     "nvfp4moe_last_error_detail": (ctypes.c_char_p, []),
     "nvfp4moe_device_check": (_i, [_i]),
     "nvfp4moe_sync_status": (_i, [_p]),
+    "nvfp4moe_set_wait_limit_us": (_i, [ctypes.c_uint32]),
+    "nvfp4moe_wait_limit_us": (ctypes.c_uint32, []),
+    "nvfp4moe_wait_selftest": (_i, [ctypes.c_uint32, ctypes.c_uint32, _p]),
     "nvfp4moe_blocked_scales_bytes": (_sz, [_i64, _i64]),
     "nvfp4moe_mxfp4_blocked_scales_bytes": (_sz, [_i64, _i64]),
     "moe_quantize_mxfp4": (_i, [_p, _i64, _i64, _i, _p, _p, _p]),
@@ -125,6 +129,21 @@ def device_check(device=None):
 def sync_status():
     """Synchronise the current stream and raise on sticky device flags."""
     _check(_lib.nvfp4moe_sync_status(_stream()), "nvfp4moe_sync_status")
+
+
+def set_wait_limit_us(us):
+    """Limit of every bounded device wait, in microseconds (0: the default, 2 s)."""
+    _check(_lib.nvfp4moe_set_wait_limit_us(int(us)), "nvfp4moe_set_wait_limit_us")
+
+
+def wait_limit_us():
+    return int(_lib.nvfp4moe_wait_limit_us())
+
+
+def wait_selftest(expected_arrivals, arrivals):
+    """Enqueue the bounded-wait self-test (see the header); a phase that can
+    never complete shows up as ERR_TIMEOUT at the next sync_status()."""
+    _check(_lib.nvfp4moe_wait_selftest(int(expected_arrivals), int(arrivals), _stream()), "nvfp4moe_wait_selftest")
 
 
 def blocked_scales_bytes(rows, cols, fmt="nvfp4"):

@@ -1,6 +1,7 @@
 // C entry points of libnvfp4moe: argument validation, the per-device
 // attribute cache and status plumbing.  The compute lives in
 // kernels_prep.cu and grouped_gemm.cu; nothing here allocates device memory.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -85,6 +86,13 @@ void set_error_detail(const char* fmt, ...) {
 
 }  // namespace nvfp4moe
 
+namespace nvfp4moe {
+namespace {
+std::atomic<uint32_t> g_wait_limit_us{kDefaultWaitUs};
+}  // namespace
+uint32_t wait_limit_us() { return g_wait_limit_us.load(std::memory_order_relaxed); }
+}  // namespace nvfp4moe
+
 using namespace nvfp4moe;
 
 #define NVFP4MOE_REQUIRE(cond, status, ...) \
@@ -116,6 +124,25 @@ int nvfp4moe_device_check(int device) {
   DeviceInfo d;
   t_detail[0] = 0;
   return check_device(device, &d);
+}
+
+int nvfp4moe_set_wait_limit_us(uint32_t us) {
+  t_detail[0] = 0;
+  NVFP4MOE_REQUIRE(us <= kMaxWaitUs, NVFP4MOE_ERR_INVALID_ARG, "wait limit %u us above the maximum %u us", us,
+                   kMaxWaitUs);
+  g_wait_limit_us.store(us == 0 ? kDefaultWaitUs : us, std::memory_order_relaxed);
+  return NVFP4MOE_OK;
+}
+
+uint32_t nvfp4moe_wait_limit_us(void) { return wait_limit_us(); }
+
+int nvfp4moe_wait_selftest(uint32_t expected_arrivals, uint32_t arrivals, cudaStream_t stream) {
+  t_detail[0] = 0;
+  NVFP4MOE_REQUIRE(expected_arrivals >= 1 && expected_arrivals <= 64 && arrivals <= 32, NVFP4MOE_ERR_INVALID_ARG,
+                   "expected_arrivals %u (1..64), arrivals %u (0..32)", expected_arrivals, arrivals);
+  DeviceInfo d;
+  if (int st = current_device(&d)) return st;
+  return cuda_status(launch_wait_selftest(expected_arrivals, arrivals, stream), "wait self-test launch");
 }
 
 int nvfp4moe_sync_status(cudaStream_t stream) {
@@ -469,9 +496,10 @@ static int grouped_gemm_common(bool mx, const uint8_t* a_packed, const uint8_t* 
                    (long long)rows_capacity);
   NVFP4MOE_REQUIRE(m_total >= 0, NVFP4MOE_ERR_INVALID_ARG, "m_total < 0");
   NVFP4MOE_REQUIRE(tile_n == 0 || tile_n == 128 || (!swiglu && tile_n == 256) ||
-                       (tile_n == NVFP4MOE_TILE_TOKEN_MAJOR && N % 256 == 0),
+                       ((tile_n == NVFP4MOE_TILE_TOKEN_MAJOR || tile_n == NVFP4MOE_TILE_TOKEN_MAJOR_PAIR) &&
+                        N % 256 == 0),
                    NVFP4MOE_ERR_UNSUPPORTED,
-                   "tile_n %d (expected 0, 128, 256 for the bf16 epilogue, or NVFP4MOE_TILE_TOKEN_MAJOR with "
+                   "tile_n %d (expected 0, 128, 256 for the bf16 epilogue, or NVFP4MOE_TILE_TOKEN_MAJOR[_PAIR] with "
                    "N %% 256 == 0)",
                    tile_n);
   NVFP4MOE_REQUIRE(a_packed && a_scales && expert_counts && row_offsets && w_packed && w_scales && c_out,

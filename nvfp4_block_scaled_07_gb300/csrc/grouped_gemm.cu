@@ -89,7 +89,8 @@ __host__ __device__ constexpr int out_stage_bytes(bool swiglu, bool tm) { return
 constexpr int kTileRing = 16;
 __host__ __device__ constexpr int tile_consumers(bool swiglu) { return 1 + 4 + epi_warps(swiglu); }  // MMA, SF and epilogue warps
 constexpr int kNumBars = 3 * kMaxStages + 5 + 2 * kMaxSfSlots + 2 * kTileRing;
-constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr uint64_t kTimeoutNs = 2000000000ull;   // drains after an abort
+constexpr uint64_t kPeerDrainNs = 30000000000ull;  // CTA 1 of a pair waiting for the pair's last MMA
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 struct Params {
@@ -109,6 +110,14 @@ struct Params {
   int w_tiled;      // weights in the tiled layout (5-D weight map coordinates below)
   int w_kc;         // 128-byte K chunks per weight row (tiled layout)
   int64_t rows_cap;
+  uint32_t wait_us;  // limit of every pipeline wait (nvfp4moe_set_wait_limit_us)
+};
+
+// Shared state of the bounded waits of one CTA: the abort flag every role
+// polls and the launch's wait limit.
+struct WaitCtl {
+  int abort;
+  uint32_t limit_us;
 };
 
 template <int BN, int NA_, bool SWIGLU>
@@ -150,14 +159,15 @@ __device__ __forceinline__ uint32_t poll_phase(uint32_t bar, uint32_t parity) {
 }
 
 template <bool SPIN>
-__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile WaitCtl* wctl) {
   const uint64_t t0 = ptx::globaltimer_ns();
+  const uint64_t limit = uint64_t(wctl->limit_us) * 1000u;
   for (uint32_t i = 0;; ++i) {
     if (poll_phase<SPIN>(bar, parity)) return true;
     if ((i & 255u) == 255u) {
-      if (*abort_flag) return false;
-      if (ptx::globaltimer_ns() - t0 > kTimeoutNs) {
-        *abort_flag = 1;
+      if (wctl->abort) return false;
+      if (ptx::globaltimer_ns() - t0 > limit) {
+        wctl->abort = 1;
         atomicOr(&g_gemm_flags, kFlagTimeout);
         return false;
       }
@@ -166,7 +176,7 @@ __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, vola
 }
 
 template <bool SPIN = false>
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile WaitCtl* abort_flag) {
   if (poll_phase<SPIN>(bar, parity)) return true;
   return wait_phase_slow<SPIN>(bar, parity, abort_flag);
 }
@@ -406,19 +416,27 @@ __device__ __forceinline__ void requant_row32_mx(const uint32_t (&h)[32], int64_
   *reinterpret_cast<uint4*>(out_codes + row * (n_out / 2) + f0 / 2) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
 }
 
-template <int BN, int NA, bool SWIGLU, bool MX, bool TM>
+template <int BN, int NA, bool SWIGLU, bool MX, bool TM, bool PAIR = false>
 __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_sf,
                         const __grid_constant__ CUtensorMap tmap_asf, const Params p) {
   using C = Cfg<BN, NA, SWIGLU>;
   static_assert(!TM || (BN == 128 && NA == 2), "token-major tiles: 128 tokens x two 128-row weight tiles");
+  static_assert(!PAIR || TM, "CTA pairs run token-major tiles");
+  // CTA pair (cluster of two, cta_group::2 MMAs): a tile is 256 tokens, 128
+  // in each CTA, against the stage's two weight tiles, one in each CTA's
+  // shared memory; CTA 0 of the pair issues the MMAs for both.
+  constexpr int TB = PAIR ? 2 * kBM : BN;      // token rows per tile
+  constexpr int NW = PAIR ? 1 : C::NA;         // weight tiles in this CTA's stage
+  const uint32_t crank = PAIR ? ptx::cluster_ctarank() : 0u;
+  uint32_t* const sched = PAIR ? nullptr : p.sched;  // pairs run static stripes
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* s_wmax = reinterpret_cast<int*>(tmem_slot + 2);
+  int* s_wmax = reinterpret_cast<int*>(tmem_slot + 1);
+  volatile WaitCtl* abort_flag = reinterpret_cast<volatile WaitCtl*>(tmem_slot + 2);
   volatile int* s_tq = reinterpret_cast<volatile int*>(tmem_slot + 4);   // claimed tile ids
   int* s_map = reinterpret_cast<int*>(tmem_slot + 4 + kTileRing);  // TileMap header
   int* s_pre = s_map + 4;
@@ -456,25 +474,31 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(accf_bar(b), 1);
-      ptx::mbar_init(acce_bar(b), epi_warps(SWIGLU));
+      ptx::mbar_init(acce_bar(b), (PAIR ? 2 : 1) * epi_warps(SWIGLU));  // both CTAs' epilogues drain it
     }
     ptx::mbar_init(drain_bar, 1);
     for (int r = 0; r < kMaxSfSlots; ++r) {
-      ptx::mbar_init(sff_bar(r), 4);  // one arrival per scale-factor warp
+      ptx::mbar_init(sff_bar(r), PAIR ? 8 : 4);  // one arrival per scale-factor warp (of both CTAs)
       ptx::mbar_init(sfe_bar(r), 1);  // MMA completion
     }
     for (int q = 0; q < kTileRing; ++q) {
       ptx::mbar_init(tqf_bar(q), 1);
       ptx::mbar_init(tqe_bar(q), tile_consumers(SWIGLU));
     }
-    *abort_flag = 0;
+    abort_flag->abort = 0;
+    abort_flag->limit_us = p.wait_us;
     ptx::fence_barrier_init();
     ptx::prefetch_tmap(&tmap_w);
     ptx::prefetch_tmap(&tmap_a);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
-    ptx::tmem_relinquish();
+    if constexpr (PAIR) {
+      ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), kTmemCols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+      ptx::tmem_relinquish();
+    }
   }
   // Everything above touches only this CTA's own resources; from here on the
   // kernel reads the previous kernel's outputs (counts, operands, scales).
@@ -498,7 +522,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       }
       s_count[e] = c;
       s_rowoff[e] = ro;
-      const int ntn = (c + BN - 1) / BN;
+      const int ntn = (c + TB - 1) / TB;
       if (ntn >= 2) ++nA, tA += MT * ntn;
       else if (ntn == 1) ++nB, tB += MT;
       int w = 32;
@@ -516,7 +540,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     const int expertsA = __shfl_sync(kFull, inA, 31);
     int posA = inA - nA, preA = itA - tA, posB = expertsA + inB - nB, preB = itB - tB;
     for (int e = beg; e < end; ++e) {
-      const int ntn = (s_count[e] + BN - 1) / BN;
+      const int ntn = (s_count[e] + TB - 1) / TB;
       if (ntn >= 2) {
         s_expt[posA] = e, s_pre[posA] = preA;
         ++posA, preA += MT * ntn;
@@ -532,6 +556,9 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
+  // A pair's CTAs signal each other's barriers from here on: both must have
+  // initialised theirs.
+  if constexpr (PAIR) ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int total = s_map[0] + s_map[1];
@@ -542,8 +569,8 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   // Stage geometry for this launch: as many stages as fit once the token
   // slot is sized for the widest tile actually present.
   const int wmax = TM ? kBM : *s_wmax;  // token-major: every token tile is 128 rows
-  const int stage = C::stage_bytes(wmax);
-  const int off_b = C::NA * kATile;
+  const int stage = NW * kATile + wmax * kBKBytes + C::NA * kSfTile + (wmax > 128 ? 2 : 1) * kSfTile;
+  const int off_b = NW * kATile;
   const int off_sfa = off_b + wmax * kBKBytes;
   const int off_sfb = off_sfa + C::NA * kSfTile;
   const int S = min(p.stage_cap, (p.smem_bytes - ctrl - out_stage_bytes(SWIGLU, TM)) / stage);
@@ -555,7 +582,8 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   // ring; lane 0 of a warp role reads it and releases the slot.  Returns -1
   // if the wait was abandoned.
   auto next_tile = [&](uint32_t i, bool whole_warp) -> int {
-    if (!p.sched) return int(blockIdx.x + i * gridDim.x);
+    if (PAIR) return int((blockIdx.x >> 1) + i * (gridDim.x >> 1));
+    if (!sched) return int(blockIdx.x + i * gridDim.x);
     const uint32_t q = i % uint32_t(kTileRing), ph = (i / uint32_t(kTileRing)) & 1u;
     int t = -1;
     if (!whole_warp || lane == 0) {
@@ -577,10 +605,10 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     bool ok = true;
     // Dynamic schedule: the next id is claimed one tile ahead, so the atomic's
     // latency overlaps the current tile's copies.
-    int next = p.sched ? int(atomicAdd(p.sched, 1u)) : int(blockIdx.x);
+    int next = sched ? int(atomicAdd(sched, 1u)) : int(PAIR ? blockIdx.x >> 1 : blockIdx.x);
     for (uint32_t i = 0; ok; ++i) {
       const int t = next;
-      if (p.sched) {
+      if (sched) {
         const uint32_t q = i % uint32_t(kTileRing), ph = (i / uint32_t(kTileRing)) & 1u;
         if (!wait_phase<true>(tqe_bar(q), ph ^ 1u, abort_flag)) {
           ok = false;
@@ -590,11 +618,11 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         ptx::mbar_arrive(tqf_bar(q));
       }
       if (t >= total) break;
-      next = p.sched ? int(atomicAdd(p.sched, 1u)) : t + int(gridDim.x);
+      next = sched ? int(atomicAdd(sched, 1u)) : t + int(PAIR ? gridDim.x >> 1 : gridDim.x);
       int e, mb, nb, w;
-      decode_tile(t, tiles, BN, e, mb, nb, w);
+      decode_tile(t, tiles, TB, e, mb, nb, w);
       if constexpr (TM) w = kBM;
-      const int arow = s_rowoff[e] + nb * BN;
+      const int arow = s_rowoff[e] + nb * TB + int(crank) * kBM;  // this CTA's token rows
       const int sfb_chunks = w > 128 ? 2 : 1;
       // weight tiles: gate/up pair rows f and I + f; otherwise NA consecutive 128-row blocks
       // The stage's NA weight tiles are one box of the 5-D weight map (see
@@ -602,15 +630,17 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       const int wdx = p.w_tiled ? 0 : kBKBytes, wdz = p.w_tiled ? 1 : 0;
       const int wblk = SWIGLU ? mb : e * (p.N / kBM) + mb * NA;  // first 128-row block of the tile
       const int wc1 = (!p.w_tiled && SWIGLU) ? mb * kBM : 0;
-      const int wc2 = p.w_tiled ? 0 : (SWIGLU ? 2 * e : wblk);
-      const int wc3 = p.w_tiled ? wblk : 0;
-      const int wc4 = (p.w_tiled && SWIGLU) ? 2 * e : 0;
+      // a pair's CTA loads one of the stage's two weight tiles: the up tile
+      // (or the second output block) in CTA 1
+      const int wc2 = p.w_tiled ? 0 : (SWIGLU ? 2 * e : wblk) + int(crank);
+      const int wc3 = p.w_tiled ? wblk + (SWIGLU ? 0 : int(crank)) : 0;
+      const int wc4 = (p.w_tiled && SWIGLU) ? 2 * e + int(crank) : 0;
       // The weight tiles' scale blocks of a stage are one box of the scale map
       // (see encode_weight_scale_map) at (64 sf_per_kt kt, sc1, sc2): a stage
       // advances sf_per_kt 512-byte blocks; the token tile's start at asf.
       const int sc1 = SWIGLU ? mb : e * (p.N / kBM) + mb * NA, sc2 = SWIGLU ? 2 * e : 0;
       const uint8_t* asf = p.a_scales + size_t(arow / kBM) * sf_k * 512;
-      const uint32_t full_bytes = uint32_t(C::NA * kATile + w * kBKBytes);
+      const uint32_t full_bytes = uint32_t(NW * kATile + w * kBKBytes);
       for (int kt = 0; kt < nkt; ++kt, ++it) {
         if (!wait_phase<true>(empty_bar(s), ph ^ 1u, abort_flag)) {
           ok = false;
@@ -636,13 +666,22 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
             ptx::bulk_load(st + off_sfb + c * kSfTile, asf + size_t(c) * sf_k * 512 + sf_off, sf_bytes, sfc_bar(s),
                            pol_a);
         }
-        ptx::mbar_arrive_expect_tx(full_bar(s), full_bytes);
-        ptx::tma_load_5d(st, &tmap_w, full_bar(s), kt * wdx, wc1, wc2 + kt * wdz, wc3, wc4, pol_w);
-        if constexpr (TM) {  // a 128-row token tile: one box (the map's box is 128 rows here)
-          ptx::tma_load_2d(st + off_b, &tmap_a, full_bar(s), kt * kBKBytes, arow, pol_a);
+        if constexpr (PAIR) {
+          // Both CTAs' operands complete on CTA 0's full barrier, which
+          // expects the bytes of both.
+          const uint32_t fb = ptx::mapa(full_bar(s), 0);
+          if (crank == 0) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * full_bytes);
+          ptx::tma_load_5d_pair(st, &tmap_w, fb, kt * wdx, wc1, wc2 + kt * wdz, wc3, wc4, pol_w);
+          ptx::tma_load_2d_pair(st + off_b, &tmap_a, fb, kt * kBKBytes, arow, pol_a);
         } else {
-          for (int r = 0; r < w; r += 32)  // the token tile in 32-row boxes
-            ptx::tma_load_2d(st + off_b + r * kBKBytes, &tmap_a, full_bar(s), kt * kBKBytes, arow + r, pol_a);
+          ptx::mbar_arrive_expect_tx(full_bar(s), full_bytes);
+          ptx::tma_load_5d(st, &tmap_w, full_bar(s), kt * wdx, wc1, wc2 + kt * wdz, wc3, wc4, pol_w);
+          if constexpr (TM) {  // a 128-row token tile: one box (the map's box is 128 rows here)
+            ptx::tma_load_2d(st + off_b, &tmap_a, full_bar(s), kt * kBKBytes, arow, pol_a);
+          } else {
+            for (int r = 0; r < w; r += 32)  // the token tile in 32-row boxes
+              ptx::tma_load_2d(st + off_b + r * kBKBytes, &tmap_a, full_bar(s), kt * kBKBytes, arow + r, pol_a);
+          }
         }
         if (++s == uint32_t(S)) s = 0, ph ^= 1u;
       }
@@ -652,7 +691,26 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       const uint32_t first = it > uint32_t(S) ? it - uint32_t(S) : 0u;
       for (uint32_t i = first; i < it; ++i) {
         drain_phase(sfc_bar(i % uint32_t(S)), (i / uint32_t(S)) & 1u);
-        drain_phase(full_bar(i % uint32_t(S)), (i / uint32_t(S)) & 1u);
+        if (crank == 0) drain_phase(full_bar(i % uint32_t(S)), (i / uint32_t(S)) & 1u);
+      }
+      if constexpr (PAIR) {
+        // CTA 1's operand copies complete on CTA 0's barriers, which CTA 1
+        // cannot wait on: give any copy still in flight 1 ms to land.
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (ptx::globaltimer_ns() - t0 < 1000000ull) {
+        }
+      }
+    }
+  } else if (PAIR && warp == 1 && lane == 0 && crank != 0) {
+    // CTA 1 of a pair issues no MMAs; its tensor memory is freed once CTA 0's
+    // last MMA (which writes it) has completed.  CTA 0 signals that at the end
+    // of its MMA role, also after an abort, so this wait spans the whole
+    // kernel: its limit is kPeerDrainNs instead of the per-stage limit.
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(drain_bar, 0)) {
+      if (ptx::globaltimer_ns() - t0 > kPeerDrainNs) {
+        atomicOr(&g_gemm_flags, kFlagTimeout);
+        break;
       }
     }
   } else if (warp == 1 && lane == 0) {
@@ -668,18 +726,23 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     uint32_t r = 0, rph = 0;  // scale-factor ring slot and its parity
     SlotSeq slots;
     bool ok = true;
+    // a pair's MMAs signal the barrier at the same offset in both CTAs
+    auto commit = [](uint32_t bar) {
+      if constexpr (PAIR) ptx::tc_commit_pair(bar);
+      else ptx::tc_commit(bar);
+    };
     for (uint32_t i = 0; ok; ++i) {
       const int t = next_tile(i, false);
       if (t < 0 || t >= total) break;
       int e, mb, nb, w;
-      decode_tile(t, tiles, BN, e, mb, nb, w);
+      decode_tile(t, tiles, TB, e, mb, nb, w);
       if constexpr (TM) w = kBM;
       int s0, s1;
       slots.pick(C::NA * w, s0, s1);
       if (!wait_phase<true>(acce_bar(s0), slots.parity(s0) ^ 1u, abort_flag)) break;
       if (s1 >= 0 && !wait_phase<true>(acce_bar(s1), slots.parity(s1) ^ 1u, abort_flag)) break;
       ptx::tc_fence_after();
-      const uint32_t idesc = TM ? ptx::idesc_nvfp4(kBM, C::NA * kBM, MX) : ptx::idesc_nvfp4(kBM, w, MX);
+      const uint32_t idesc = TM ? ptx::idesc_nvfp4(PAIR ? 2 * kBM : kBM, C::NA * kBM, MX) : ptx::idesc_nvfp4(kBM, w, MX);
       const uint32_t d0 = tmem + uint32_t(s0 * kAccSlotCols);
       // The MMAs of K stage kt from pipeline stage st and scale slot sf: a
       // full stage (4 k64 blocks) is one fully unrolled sequence.
@@ -690,12 +753,18 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
           if constexpr (TM) {
             // D[token][weight row] += tokens (A, M = 128) x weight tiles (B, N = 256);
             // scales: tokens at column 32 + 4 kb, weights at 8 kb (+4 for the second tile)
+            // (pair: M = 256 tokens, 128 per CTA; N = 256 weight rows, 128 per CTA)
             const uint64_t adesc = ptx::desc_kmajor_sw128(st + off_b) + 2 * kb;
             const uint64_t wdesc = ptx::desc_kmajor_sw128(st) + 2 * kb;
-            if constexpr (MX)
-              ptx::tc_mma_mxfp4(d0, adesc, wdesc, idesc, sf + C::NA * 16 + kb * 4, sf + kb * 8, (kt | kb) != 0 ? 1u : 0u);
+            const uint32_t acc = (kt | kb) != 0 ? 1u : 0u;
+            if constexpr (PAIR && MX)
+              ptx::tc_mma_mxfp4_pair(d0, adesc, wdesc, idesc, sf + C::NA * 16 + kb * 4, sf + kb * 8, acc);
+            else if constexpr (PAIR)
+              ptx::tc_mma_nvfp4_pair(d0, adesc, wdesc, idesc, sf + C::NA * 16 + kb * 4, sf + kb * 8, acc);
+            else if constexpr (MX)
+              ptx::tc_mma_mxfp4(d0, adesc, wdesc, idesc, sf + C::NA * 16 + kb * 4, sf + kb * 8, acc);
             else
-              ptx::tc_mma_nvfp4(d0, adesc, wdesc, idesc, sf + C::NA * 16 + kb * 4, sf + kb * 8, (kt | kb) != 0 ? 1u : 0u);
+              ptx::tc_mma_nvfp4(d0, adesc, wdesc, idesc, sf + C::NA * 16 + kb * 4, sf + kb * 8, acc);
           } else {
 #pragma unroll
             for (int j = 0; j < C::NA; ++j) {
@@ -740,12 +809,12 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         }
         ptx::tc_fence_after();
         issue_stage(kt, smem_base + s * uint32_t(stage), tmem + uint32_t(kSfColBase + r * C::SfCols));
-        ptx::tc_commit(empty_bar(s));  // frees the stage once these MMAs have read it
-        ptx::tc_commit(sfe_bar(r));
+        commit(empty_bar(s));  // frees the stage once these MMAs have read it
+        commit(sfe_bar(r));
         if (two) {
           issue_stage(kt + 1, smem_base + s2 * uint32_t(stage), tmem + uint32_t(kSfColBase + r2 * C::SfCols));
-          ptx::tc_commit(empty_bar(s2));
-          ptx::tc_commit(sfe_bar(r2));
+          commit(empty_bar(s2));
+          commit(sfe_bar(r2));
           s = s2 + 1, ph = ph2, r = r2 + 1, rph = rph2;
         } else {
           s = s2, ph = ph2, r = r2, rph = rph2;
@@ -754,11 +823,11 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         if (r == uint32_t(C::SfSlots)) r = 0, rph ^= 1u;
       }
       if (!ok) break;
-      ptx::tc_commit(accf_bar(s0));
-      if (s1 >= 0) ptx::tc_commit(accf_bar(s1));
+      commit(accf_bar(s0));
+      if (s1 >= 0) commit(accf_bar(s1));
       slots.done(s0, s1);
     }
-    ptx::tc_commit(drain_bar);  // every MMA of this CTA done before tensor memory is freed
+    commit(drain_bar);  // every MMA of this CTA (pair) done before tensor memory is freed
     drain_phase(drain_bar, 0);
   } else if (warp >= 2 + epi_warps(SWIGLU)) {
     // ---------------- scale factors: shared memory -> tensor memory ----------------
@@ -782,7 +851,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       const int t = next_tile(i, true);
       if (t < 0 || t >= total) break;
       int e, mb, nb, w;
-      decode_tile(t, tiles, BN, e, mb, nb, w);
+      decode_tile(t, tiles, TB, e, mb, nb, w);
       if constexpr (TM) w = kBM;
       const int sfb_chunks = w > 128 ? 2 : 1;
       for (int kt = 0; kt < nkt; ++kt) {
@@ -830,7 +899,10 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(sff_bar(r));
+        if (lane == 0) {
+          if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::mapa(sff_bar(r), 0));  // CTA 0 issues the MMAs
+          else ptx::mbar_arrive(sff_bar(r));
+        }
         if (++s == uint32_t(S)) s = 0, ph ^= 1u;
         if (++r == uint32_t(C::SfSlots)) r = 0, rph ^= 1u;
       }
@@ -850,15 +922,16 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       const int t = next_tile(i, true);
       if (t < 0 || t >= total) break;
       int e, mb, nb, w;
-      decode_tile(t, tiles, BN, e, mb, nb, w);
+      decode_tile(t, tiles, TB, e, mb, nb, w);
       if constexpr (TM) w = kBM;
       int s0, s1;
       slots.pick(C::NA * w, s0, s1);
       if (!wait_phase(accf_bar(s0), slots.parity(s0), abort_flag)) break;
       if (s1 >= 0 && !wait_phase(accf_bar(s1), slots.parity(s1), abort_flag)) break;
       ptx::tc_fence_after();
-      const int valid = min(w, s_count[e] - nb * BN);
-      const int64_t row0 = int64_t(s_rowoff[e]) + int64_t(nb) * BN;
+      // this CTA's token rows of the tile (a pair's CTA 1 holds rows 128..255)
+      const int valid = min(w, s_count[e] - nb * TB - int(crank) * kBM);
+      const int64_t row0 = int64_t(s_rowoff[e]) + int64_t(nb) * TB + int(crank) * kBM;
       const float scale = MX ? 1.0f : a_gs * p.w_gscale[e];
       const uint32_t tbase = tmem + (uint32_t(q * 32) << 16) + uint32_t(s0 * kAccSlotCols);
       const int f = (SWIGLU ? mb : mb * NA) * kBM + lrow;  // output column (of tile 0)
@@ -876,8 +949,13 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          ptx::mbar_arrive(acce_bar(s0));
-          if (s1 >= 0) ptx::mbar_arrive(acce_bar(s1));
+          if constexpr (PAIR) {  // CTA 0 issues the next tile's MMAs into both CTAs' accumulators
+            ptx::mbar_arrive_cluster(ptx::mapa(acce_bar(s0), 0));
+            if (s1 >= 0) ptx::mbar_arrive_cluster(ptx::mapa(acce_bar(s1), 0));
+          } else {
+            ptx::mbar_arrive(acce_bar(s0));
+            if (s1 >= 0) ptx::mbar_arrive(acce_bar(s1));
+          }
         }
       };
       if constexpr (TM) {
@@ -1051,14 +1129,20 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
 
   ptx::tc_fence_before();
   __syncthreads();
+  // A pair frees its tensor memory together (one warp of each CTA), once
+  // both CTAs are done with it.
+  if constexpr (PAIR) ptx::cluster_sync();
   if (warp == 1) {
     __syncwarp();
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, kTmemCols);
+    if constexpr (PAIR) ptx::tmem_dealloc_pair(tmem, kTmemCols);
+    else ptx::tmem_dealloc(tmem, kTmemCols);
   }
+  // Neither CTA of a pair leaves while the other may still signal its barriers.
+  if constexpr (PAIR) ptx::cluster_sync();
   // Dynamic schedule: the last CTA to finish (every producer has stopped
   // claiming by then) leaves both counters at zero for the next launch.
-  if (p.sched && threadIdx.x == 0) {
+  if (sched && threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(p.sched + 32, 1u) == gridDim.x - 1) {
       atomicExch(p.sched, 0u);
@@ -1099,8 +1183,8 @@ bool encode_kmajor_map(CUtensorMap* m, const void* base, int64_t rows, int64_t r
 }
 
 // Weight map: a 5-D byte view of the weights whose box {128 B, 128 rows, ...}
-// holds the NA weight tiles of one pipeline stage back to back (one copy per
-// stage).  Coordinates (kt * dx, c1, c2 + kt * dz, c3, c4):
+// holds the `tiles` weight tiles of one pipeline stage back to back (one copy
+// per stage; a CTA of a pair loads one of the two, tiles = 1).  Coordinates (kt * dx, c1, c2 + kt * dz, c3, c4):
 //   row-major, SwiGLU: [K/2 B][I rows][2E halves (gate, up)]   box {128, 128, 2}
 //                      at (128 kt, 128 mb, 2e)
 //   row-major, other:  [K/2 B][128 rows][E N / 128 blocks]      box {128, 128, NA}
@@ -1110,7 +1194,7 @@ bool encode_kmajor_map(CUtensorMap* m, const void* base, int64_t rows, int64_t r
 //   tiled, other:      [128 B][128 rows][kc chunks][E N / 128 blocks]
 //                      box {128, 128, 1, NA} at (0, 0, kt, first block)
 // Unit dimensions fill the view to 5-D.
-bool encode_weight_map(CUtensorMap* m, const GemmArgs& a, bool swiglu, int na) {
+bool encode_weight_map(CUtensorMap* m, const GemmArgs& a, bool swiglu, int tiles) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   const int64_t kh = a.K / 2, kc = (a.K + 255) / 256, nblk = int64_t(a.E) * a.N / kBM, half = a.N / 2;
@@ -1125,7 +1209,7 @@ bool encode_weight_map(CUtensorMap* m, const GemmArgs& a, bool swiglu, int na) {
       dims[0] = kh, dims[1] = kBM, dims[2] = nblk;
       strides[0] = kh, strides[1] = kBM * kh;
     }
-    box[2] = cuuint32_t(swiglu ? 2 : na);
+    box[2] = cuuint32_t(tiles);
     dims[3] = dims[4] = 1;
     strides[2] = strides[3] = strides[1] * dims[2];
   } else {
@@ -1134,11 +1218,11 @@ bool encode_weight_map(CUtensorMap* m, const GemmArgs& a, bool swiglu, int na) {
     if (swiglu) {
       dims[3] = half / kBM, dims[4] = 2 * int64_t(a.E);
       strides[3] = (half / kBM) * kc * kWeightBoxBytes;
-      box[4] = 2;
+      box[4] = cuuint32_t(tiles);
     } else {
       dims[3] = nblk, dims[4] = 1;
       strides[3] = nblk * kc * kWeightBoxBytes;
-      box[3] = cuuint32_t(na);
+      box[3] = cuuint32_t(tiles);
     }
   }
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
@@ -1223,14 +1307,39 @@ int stage_cap_from_env() {
   return cap;
 }
 
-template <int BN, int NA, bool SWIGLU, bool MX, bool TM = false>
+// CTA pairs of a kernel that can be resident at once (clusters of two), per
+// device, looked up once.
+template <typename K>
+int max_pairs(K kernel, int threads, size_t smem, int num_sms) {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] > 0) return cached[dev];
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) return 0;
+  cached[dev] = std::min(n, num_sms / 2);
+  return cached[dev];
+}
+
+template <int BN, int NA, bool SWIGLU, bool MX, bool TM = false, bool PAIR = false>
 int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st) {
   using C = Cfg<BN, NA, SWIGLU>;
   // The whole opt-in shared memory is requested; the kernel sizes its stages
   // for the widest token tile present.  Two stages of the widest possible
   // tile must fit.
   const int64_t usable = int64_t(smem_optin) - 1024 - ctrl_bytes(a.E);
-  const int worst = C::stage_bytes(BN);
+  const int worst = PAIR ? kATile + kBM * kBKBytes + NA * kSfTile + kSfTile : C::stage_bytes(BN);
   if (usable < 2 * int64_t(worst) + out_stage_bytes(SWIGLU, TM)) {
     set_error_detail(
         "grouped GEMM tile %dx%d (%s) needs %lld bytes of shared memory for a 2-stage pipeline; Hardware limit: %d",
@@ -1241,7 +1350,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   const size_t smem = size_t(smem_optin);
   CUtensorMap tw, ta, tc, tsf, tasf;
   const int w_kc = (a.K + 255) / 256;
-  if (!encode_weight_map(&tw, a, SWIGLU, NA) || !encode_weight_scale_map(&tsf, a, SWIGLU, NA) ||
+  if (!encode_weight_map(&tw, a, SWIGLU, PAIR ? 1 : (SWIGLU ? 2 : NA)) || !encode_weight_scale_map(&tsf, a, SWIGLU, NA) ||
       !encode_token_scale_map(&tasf, a) ||
       !encode_kmajor_map(&ta, a.a_packed, a.rows_capacity, a.K / 2, TM ? kBM : 32) ||
       !(out_stage_bytes(SWIGLU, TM) ? encode_bf16_store_map(&tc, a.c_out, a.rows_capacity, a.N)
@@ -1249,9 +1358,8 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
     set_error_detail("cuTensorMapEncodeTiled failed or is unavailable");
     return NVFP4MOE_ERR_CUDA;
   }
-  cudaError_t err =
-      cudaFuncSetAttribute(grouped_gemm_kernel<BN, NA, SWIGLU, MX, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(smem));
+  auto kernel = grouped_gemm_kernel<BN, NA, SWIGLU, MX, TM, PAIR>;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (err != cudaSuccess) {
     set_error_detail("cudaFuncSetAttribute: %s", cudaGetErrorString(err));
     return NVFP4MOE_ERR_CUDA;
@@ -1276,13 +1384,39 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   p.sched = static_cast<uint32_t*>(a.sched);
   p.w_tiled = a.w_tiled ? 1 : 0;
   p.w_kc = w_kc;
+  p.wait_us = wait_limit_us();
   // Launched without programmatic dependent launch: measured on GB300, a
   // grouped GEMM launched with it streamed its weight tiles about 2.5%
   // slower per tile, more than the few microseconds of launch latency it
   // hides.  The kernel still starts with griddepcontrol.wait (a no-op here),
   // so the kernel after it may be launched with the attribute.
-  grouped_gemm_kernel<BN, NA, SWIGLU, MX, TM><<<num_sms, num_threads(SWIGLU), smem, st>>>(tw, ta, tc, tsf, tasf, p);
-  err = cudaGetLastError();
+  if constexpr (PAIR) {
+    // Clusters of two CTAs on neighbouring SMs, as many as can be resident
+    // at once (the kernel is persistent: pair c takes tiles c, c + #pairs, ...).
+    const int pairs = max_pairs(kernel, num_threads(SWIGLU), smem, num_sms);
+    if (pairs < 1) {
+      set_error_detail("no CTA pair of the grouped GEMM fits on this device");
+      return NVFP4MOE_ERR_SMEM;
+    }
+    p.sched = nullptr;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(num_threads(SWIGLU));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, kernel, tw, ta, tc, tsf, tasf, p);
+    if (err == cudaSuccess) err = cudaGetLastError();
+  } else {
+    kernel<<<num_sms, num_threads(SWIGLU), smem, st>>>(tw, ta, tc, tsf, tasf, p);
+    err = cudaGetLastError();
+  }
   if (err != cudaSuccess) {
     set_error_detail("grouped GEMM launch: %s", cudaGetErrorString(err));
     return NVFP4MOE_ERR_CUDA;
@@ -1301,6 +1435,10 @@ int launch_format(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t s
   // loaded serves 256 output features (measured: the down GEMM at decode
   // 0.48 -> 0.30 ms, at 2048 rows per expert 4.02 -> 2.78 ms).
   const bool pair = a.N % (2 * kBM) == 0;
+  if (a.tile_n == NVFP4MOE_TILE_TOKEN_MAJOR_PAIR && pair) {
+    if (swiglu) return launch_impl<128, 2, true, MX, true, true>(a, num_sms, smem_optin, st);
+    return launch_impl<128, 2, false, MX, true, true>(a, num_sms, smem_optin, st);
+  }
   if (a.tile_n == NVFP4MOE_TILE_TOKEN_MAJOR && pair) {
     if (swiglu) return launch_impl<128, 2, true, MX, true>(a, num_sms, smem_optin, st);
     return launch_impl<128, 2, false, MX, true>(a, num_sms, smem_optin, st);
@@ -1346,6 +1484,35 @@ cudaError_t launch_tile_weights(const uint8_t* w_packed, int64_t rows, int K, ui
 
 int launch_grouped_gemm(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st) {
   return a.mx ? launch_format<true>(a, num_sms, smem_optin, st) : launch_format<false>(a, num_sms, smem_optin, st);
+}
+
+namespace {
+
+// One CTA waits, through the grouped GEMM's bounded wait, for a phase of an
+// mbarrier that expects `expected` arrivals and receives `arrivals` (one per
+// thread, arrivals <= 32): with arrivals < expected the phase never
+// completes and the wait gives up after the launch's wait limit, raising
+// the sticky timeout flag.
+__global__ void __launch_bounds__(32, 1) wait_selftest_kernel(uint32_t expected, uint32_t arrivals, uint32_t wait_us) {
+  __shared__ uint64_t bar;
+  __shared__ WaitCtl ctl;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bar), expected);
+    ctl.abort = 0;
+    ctl.limit_us = wait_us;
+    ptx::fence_barrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x < arrivals) ptx::mbar_arrive(ptx::smem_u32(&bar));
+  __syncwarp();
+  if (threadIdx.x == 0) wait_phase(ptx::smem_u32(&bar), 0, &ctl);
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(uint32_t expected, uint32_t arrivals, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(expected, arrivals, wait_limit_us());
+  return cudaGetLastError();
 }
 
 cudaError_t gemm_read_and_clear_flags(unsigned* flags) {

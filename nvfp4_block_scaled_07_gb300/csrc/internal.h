@@ -13,6 +13,17 @@ namespace nvfp4moe {
 constexpr unsigned kFlagTimeout = 1u;
 constexpr unsigned kFlagBadData = 2u;
 
+// Limit of every bounded device wait of the pipelines (mbarrier waits of
+// the grouped GEMM, grid barriers of the prepare kernel), in microseconds:
+// the value of nvfp4moe_set_wait_limit_us, read at each launch.
+constexpr uint32_t kDefaultWaitUs = 2000000;
+constexpr uint32_t kMaxWaitUs = 60000000;
+uint32_t wait_limit_us();
+
+// Runs the grouped GEMM's bounded mbarrier wait on a barrier that expects
+// `expected` arrivals and gets `arrivals` (<= 32).
+cudaError_t launch_wait_selftest(uint32_t expected, uint32_t arrivals, cudaStream_t st);
+
 // Segment of flat ids ranked by one warp in the permutation.
 constexpr int kPermuteSegment = 1024;
 

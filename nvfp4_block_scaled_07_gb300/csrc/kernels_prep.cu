@@ -631,6 +631,7 @@ struct PrepareParams {
   uint8_t* a_scales;
   int64_t rows_cap;
   uint32_t* bar;  // [0] arrivals, [32] generation: separate 128-byte lines
+  uint32_t wait_us;  // limit of each grid-barrier wait (nvfp4moe_set_wait_limit_us)
   uint32_t* active_set;  // batch-aware routing: E bits, zero between calls
   float* amax_part;
   int32_t* rank;
@@ -639,14 +640,12 @@ struct PrepareParams {
 };
 
 constexpr int kPrepThreads = 1024;
-constexpr uint64_t kPrepTimeoutNs = 2000000000ull;
-
 // All CTAs of the grid meet here.  Thread 0 of each CTA arrives on a
 // device-scope counter; the last arrival resets it and bumps the generation
-// word the others poll (bounded by kPrepTimeoutNs).  Returns false, the same
+// word the others poll (bounded by the launch's wait limit).  Returns false, the same
 // in every thread of the CTA, if the wait gave up or the counter held a
 // value no launch leaves behind; the caller then abandons the kernel.
-__device__ __forceinline__ bool grid_barrier(uint32_t* bar, int* s_ok) {
+__device__ __forceinline__ bool grid_barrier(uint32_t* bar, int* s_ok, uint32_t wait_us) {
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
@@ -665,7 +664,7 @@ __device__ __forceinline__ bool grid_barrier(uint32_t* bar, int* s_ok) {
     } else {
       const uint64_t t0 = ptx::globaltimer_ns();
       while (ptx::ld_acquire_gpu(gen) == g) {
-        if (ptx::globaltimer_ns() - t0 > kPrepTimeoutNs) {
+        if (ptx::globaltimer_ns() - t0 > uint64_t(wait_us) * 1000u) {
           atomicOr(&g_prep_flags, kFlagTimeout);
           ok = 0;
           break;
@@ -724,13 +723,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
       if (lane == 0) p.amax_part[blockIdx.x] = m;
     }
   }
-  if (!grid_barrier(p.bar, &s_ok)) return;
+  if (!grid_barrier(p.bar, &s_ok, p.wait_us)) return;
 
   // ---- A2 (batch-aware routing only): rank within the batch's active set ------
   if (batch_aware) {
     for (int64_t t = gw0; t < p.T; t += gw_stride)
       route_token<VPL>(p.logits, p.bias, int(t), p.E, p.k, p.score_fn, p.renorm, p.active_set, p.idx, p.w, lane);
-    if (!grid_barrier(p.bar, &s_ok)) return;
+    if (!grid_barrier(p.bar, &s_ok, p.wait_us)) return;
   }
 
   // ---- B: segment ranks, global scale, quantisation --------------------------
@@ -796,14 +795,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
       p.xs[b] = uint8_t(sb);
     }
   }
-  if (!grid_barrier(p.bar, &s_ok)) return;
+  if (!grid_barrier(p.bar, &s_ok, p.wait_us)) return;
 
   // ---- C: expert counts, offsets, row offsets --------------------------------
   if (blockIdx.x == 0) {
     int cnt, roff;
     scan_experts(p.seg_count, p.nseg, p.E, p.seg_base, p.counts, p.offsets, p.row_offsets, warp_tot, &cnt, &roff);
   }
-  if (!grid_barrier(p.bar, &s_ok)) return;
+  if (!grid_barrier(p.bar, &s_ok, p.wait_us)) return;
 
   // ---- D: padding rows, placement and gather ---------------------------------
   if (batch_aware && blockIdx.x == 0 && threadIdx.x < (p.E + 31) / 32) p.active_set[threadIdx.x] = 0u;  // read in A2 only
@@ -829,7 +828,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
   // block's 16-byte row i, so a warp's stores are 512 contiguous bytes.
   // Padding rows keep their bytes.
   if constexpr (kScalesByBlock) {
-    if (!grid_barrier(p.bar, &s_ok)) return;
+    if (!grid_barrier(p.bar, &s_ok, p.wait_us)) return;
     const int64_t nrb = int64_t(__ldcg(p.row_offsets + p.E)) / 128;
     const int kchunks = (sfg + 15) / 16;
     // 16-byte loads of 4 words when every row start is 16-byte aligned (xs
@@ -1136,6 +1135,7 @@ cudaError_t launch_prepare(const float* logits, const float* bias, const void* x
   p.a_scales = a_scales;
   p.rows_cap = rows_capacity;
   p.bar = reinterpret_cast<uint32_t*>(base + L.bar_off);
+  p.wait_us = wait_limit_us();
   p.active_set = reinterpret_cast<uint32_t*>(base + L.bar_off + 192);
   p.amax_part = reinterpret_cast<float*>(base + L.amax_off);
   p.rank = reinterpret_cast<int32_t*>(base + L.rank_off);

@@ -206,7 +206,7 @@ def test_blocked_layout_helper_follows_the_header(lib, rows, cols, block):
 
 def _header_signatures():
     """{name: (return kind, [argument kinds])} from the header's declarations;
-    kinds: p (pointer), i (int), i64 (int64_t), sz (size_t), cstr (const char*)."""
+    kinds: p (pointer), i (int), u32 (uint32_t), i64 (int64_t), sz (size_t), cstr (const char*)."""
     text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
     text = re.sub(r"^\s*#.*$", "", text, flags=re.M)
 
@@ -217,7 +217,7 @@ def _header_signatures():
         if "*" in decl or decl.startswith("cudaStream_t"):
             return "cstr" if decl.replace(" ", "").startswith("constchar*") and "(" not in decl else "p"
         t = decl.split()[0] if not decl.startswith("const ") else decl.split()[1]
-        return {"int": "i", "int64_t": "i64", "size_t": "sz"}[t]
+        return {"int": "i", "uint32_t": "u32", "int64_t": "i64", "size_t": "sz"}[t]
 
     sigs = {}
     for m in re.finditer(r"([\w\s\*]+?)\b((?:moe|nvfp4moe)_\w+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
@@ -232,8 +232,8 @@ def test_binding_signatures_match_the_header():
     and kinds (a pointer, an int, an int64_t or a size_t in each place), so a
     call can never shift its arguments."""
     from nvfp4_block_scaled_07_gb300 import binding as B
-    kinds = {ctypes.c_void_p: "p", ctypes.c_int: "i", ctypes.c_int64: "i64", ctypes.c_size_t: "sz",
-             ctypes.c_char_p: "cstr"}
+    kinds = {ctypes.c_void_p: "p", ctypes.c_int: "i", ctypes.c_uint32: "u32", ctypes.c_int64: "i64",
+             ctypes.c_size_t: "sz", ctypes.c_char_p: "cstr"}
     hdr = _header_signatures()
     assert set(B._SIGS) == set(hdr), set(B._SIGS) ^ set(hdr)
     for name, (res, args) in B._SIGS.items():
