@@ -424,7 +424,7 @@ def run_ours(args, w):
         res["cpu_baseline"] = cpu_baseline(w, args, layer_inputs=(inp["x"], inp["logits"], inp["bias"], layer))
     del layer, inp
     torch.cuda.empty_cache()
-    if args.secondary and args.secondary != w.name:
+    if args.secondary and args.secondary not in ("none", w.name):
         w2 = {**W.WORKLOADS, **W.PROFILE_WORKLOADS}[args.secondary]
         rec2, layer2, inp2 = measure_layer(args, w2, world, rank)
         launches += rec2.pop("gpu_launches")
@@ -647,7 +647,7 @@ def main():
     ap.add_argument("--cpu-experts", type=int, default=14,
                     help="most active experts the cpu_baseline leg samples (it stops earlier once its budget is spent)")
     ap.add_argument("--secondary", default=SECONDARY_WORKLOAD,
-                    help="workload timed after the headline one, reported under 'secondary' ('' for none)")
+                    help="workload timed after the headline one, reported under 'secondary' ('none' for none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--k-primary", type=int, default=None,
                     help="batch-aware routing: experts each token keeps by its own scores (default k: plain top-k)")

@@ -94,11 +94,15 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-// Arrive on an mbarrier that may live in another CTA of the cluster
-// (release at cluster scope: this thread's earlier writes are visible to
-// whoever completes the wait).
+// Arrive on an mbarrier that may live in another CTA of the cluster, with
+// the default CTA-scope release.  What the waiting CTA needs ordered here is
+// tensor-memory work (tcgen05.st of scale factors, tcgen05.ld of an
+// accumulator), which tcgen05.wait and tcgen05.fence::before_thread_sync
+// order before the arrival; a cluster-scope release would also wait for
+// this thread's earlier global stores (an epilogue's output) to become
+// visible to the other SM, which measured as heavy membar stalls.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // All threads of every CTA of the cluster.
 __device__ __forceinline__ void cluster_sync() {
