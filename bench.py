@@ -245,6 +245,12 @@ def kernel_names(fused_prepare):
     return head + ["gemm_gate_up_swiglu", "gemm_down", "finalize"]
 
 
+def tile_name(t):
+    return {-2: "token-major, CTA pairs (256 tokens x 256 weight rows, static schedule)",
+            -1: "token-major (128 tokens x 256 weight rows)", 0: "weight rows as M, token tiles up to 128",
+            128: "weight rows as M, token tiles up to 128", 256: "weight rows as M, token tiles up to 256"}.get(t, str(t))
+
+
 def bench_config(w, fmt, k_primary, n_active, world):
     """The `config` object of the JSON line, identical in both arms: the
     workload's shape and generator settings, its format and routing, the
@@ -416,6 +422,8 @@ def run_ours(args, w):
         **{k: rec[k] for k in ("tflops", "hbm_gbs", "layer_roofline_frac", "kernels_ms", "ms_per_step_with_events",
                                "roofline", "roofline_down", "e2e", "clocks")},
         "prepare": "fused (one launch)" if layer.fused_prepare else "separate (route, quantise, permute)",
+        "gemm_tiles": {g: tile_name(B.gemm_tile_choice(w.E, n, w.T * w.k, t)) for g, n, t in
+                       (("gate_up", 2 * w.I, layer.tile_n[0]), ("down", w.H, layer.tile_n[1]))},
         "gemm_schedule": "dynamic" if layer.g_ws is not None else "static",
         "weights": "tiled" if isinstance(layer.w_gu_packed, B.TiledWeights) else "row-major",
     }

@@ -354,7 +354,8 @@ int moe_prepare(const float* logits, const float* bias, const void* x_bf16,
  * two SMs' shared memory, so each SM stages half the weight bytes per K
  * step; a partial tile still computes 256 token rows.  Runs the static
  * schedule (the workspace is not used).
- * 0: token-major when N % 256 == 0 and m_total >= 64 * E, else 128.
+ * 0: when N % 256 == 0, token-major on CTA pairs from m_total >= 512 * E,
+ * token-major from m_total >= 64 * E; otherwise 128.
  * The results do not depend on tile_n beyond float32 summation order.
  * Limits: K % 64 == 0; N % 128 == 0 (BF16) or N % 256 == 0 (SwiGLU);
  * 1 <= E <= 1024; rows_capacity % 128 == 0.  A pipeline that does not fit the
@@ -369,6 +370,11 @@ int moe_prepare(const float* logits, const float* bias, const void* x_bf16,
  * Without one, CTA c takes tiles c, c + #SMs, ...  Results are identical
  * either way.  Calls sharing a workspace must not overlap on the GPU. */
 size_t moe_grouped_gemm_nvfp4_workspace_size(int E, int N, int K, int epilogue);
+/* The tile orientation a grouped GEMM call with these arguments runs: tile_n
+ * itself when it is not 0 (or N % 256 != 0), else the automatic choice
+ * above (NVFP4MOE_TILE_TOKEN_MAJOR_PAIR, NVFP4MOE_TILE_TOKEN_MAJOR or 0 =
+ * 128-token tiles with weight rows as M).  Host only; no device access. */
+int nvfp4moe_gemm_tile_choice(int E, int N, int64_t m_total, int tile_n);
 int moe_grouped_gemm_nvfp4(const uint8_t* a_packed, const uint8_t* a_scales, const float* a_gscale,
                            const int32_t* expert_counts, const int32_t* row_offsets,
                            int E, int64_t rows_capacity, int64_t m_total,

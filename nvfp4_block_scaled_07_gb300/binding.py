@@ -69,6 +69,7 @@ _SIGS = {
     "moe_prepare": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p,
                          _p, _sz, _p]),
     "moe_grouped_gemm_nvfp4_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "nvfp4moe_gemm_tile_choice": (_i, [_i, _i, _i64, _i]),
     "moe_grouped_gemm_nvfp4": (_i, [_p, _p, _p, _p, _p, _i, _i64, _i64, _p, _p, _p, _i, _i, _i, _p, _p, _p, _i,
                                     _i, _p, _sz, _p]),
     "moe_finalize": (_i, [_p, _p, _p, _i, _i, _i, _i64, _p, _p]),
@@ -482,6 +483,12 @@ def moe_prepare_mxfp4(logits, x, k, score_fn="sigmoid", renormalize=True, bias=N
 
 
 # ---- a4/a5 ---------------------------------------------------------------------
+def gemm_tile_choice(E, N, m_total, tile_n=0):
+    """The tile orientation a grouped GEMM call runs (see the header)."""
+    return int(_lib.nvfp4moe_gemm_tile_choice(int(E), int(N), int(m_total), int(tile_n)))
+
+
+
 def alloc_gemm_workspace(device):
     """Zero-filled tile-scheduler workspace for the grouped GEMMs (dynamic schedule)."""
     return torch.zeros((int(_lib.moe_grouped_gemm_nvfp4_workspace_size(1, 128, 64, EPI_BF16)),), dtype=torch.uint8,

@@ -468,6 +468,15 @@ size_t moe_grouped_gemm_nvfp4_workspace_size(int E, int N, int K, int epilogue) 
   return kGemmWorkspaceBytes;
 }
 
+int nvfp4moe_gemm_tile_choice(int E, int N, int64_t m_total, int tile_n) {
+  // tile_n = 0: token-major tiles once experts average kTokenMajorMinRows
+  // rows, on CTA pairs from kPairMinRows
+  if (tile_n != 0 || N % 256 != 0 || E < 1) return tile_n;
+  if (m_total >= kPairMinRows * E) return NVFP4MOE_TILE_TOKEN_MAJOR_PAIR;
+  if (m_total >= kTokenMajorMinRows * E) return NVFP4MOE_TILE_TOKEN_MAJOR;
+  return 0;
+}
+
 static int grouped_gemm_common(bool mx, const uint8_t* a_packed, const uint8_t* a_scales, const float* a_gscale,
                                const int32_t* expert_counts, const int32_t* row_offsets, int E, int64_t rows_capacity,
                                int64_t m_total, const uint8_t* w_packed, const uint8_t* w_scales,
@@ -532,8 +541,7 @@ static int grouped_gemm_common(bool mx, const uint8_t* a_packed, const uint8_t* 
   a.c_gscale = c_gscale;
   a.c_out = c_out;
   a.c_scales = c_scales;
-  // tile_n = 0: token-major tiles once experts average kTokenMajorMinRows rows
-  a.tile_n = tile_n == 0 && N % 256 == 0 && m_total >= kTokenMajorMinRows * E ? NVFP4MOE_TILE_TOKEN_MAJOR : tile_n;
+  a.tile_n = nvfp4moe_gemm_tile_choice(E, N, m_total, tile_n);
   a.mx = mx;
   a.w_tiled = w_layout == NVFP4MOE_W_TILED;
   a.sched = ws;

@@ -66,8 +66,26 @@ __device__ unsigned g_gemm_flags = 0;
 // (which also halves the registers each needs to drain its share of the
 // accumulator early); the bf16 epilogue needs one warp per quarter.
 __host__ __device__ constexpr int epi_warps(bool swiglu) { return swiglu ? 8 : 4; }
-// warp 0 producer, warp 1 MMA, then the epilogue warps, then 4 scale-factor warps
-__host__ __device__ constexpr int num_threads(bool swiglu) { return 32 * (2 + epi_warps(swiglu) + 4); }
+// warp 0 producer, warp 1 MMA, then the epilogue warps, then 4 scale-factor
+// warps.  Token-major kernels put the roles on warpgroup boundaries (warps 2
+// and 3 idle) so that setmaxnreg can move registers from the producer / MMA
+// and scale-factor warpgroups to the epilogue warpgroups.
+__host__ __device__ constexpr int epi_first(bool wg) { return wg ? 4 : 2; }
+__host__ __device__ constexpr int num_threads(bool swiglu, bool wg) {
+  return 32 * (epi_first(wg) + epi_warps(swiglu) + 4);
+}
+// Registers per thread after the split (setmaxnreg), by warpgroup: the
+// launch gives every thread 65536 / threads (128 for 512 threads, 168 for
+// 384); the split must not need more than that in total.
+__host__ __device__ constexpr int regs_launch(bool swiglu) { return 65536 / num_threads(swiglu, true) / 8 * 8; }
+// producer, MMA issuer (one lane each) and two idle warps
+__host__ __device__ constexpr int regs_control(bool swiglu) { return swiglu ? 64 : 120; }
+__host__ __device__ constexpr int regs_scale(bool swiglu) { return swiglu ? 80 : 120; }
+__host__ __device__ constexpr int regs_epilogue(bool swiglu) { return swiglu ? 184 : 256; }
+static_assert(regs_control(true) + 2 * regs_epilogue(true) + regs_scale(true) <= 4 * regs_launch(true),
+              "SwiGLU register split exceeds the launch's registers");
+static_assert(regs_control(false) + regs_epilogue(false) + regs_scale(false) <= 3 * regs_launch(false),
+              "bf16 register split exceeds the launch's registers");
 constexpr int kBM = 128;           // MMA M (weight rows per tile)
 constexpr int kBKBytes = 128;      // bytes of K per stage and row = 256 E2M1 elements
 constexpr int kATile = kBM * kBKBytes;
@@ -111,6 +129,8 @@ struct Params {
   int w_kc;         // 128-byte K chunks per weight row (tiled layout)
   int64_t rows_cap;
   uint32_t wait_us;  // limit of every pipeline wait (nvfp4moe_set_wait_limit_us)
+  int batch2;        // token-major: the MMA thread waits for and issues two stages at a time
+  int w_policy;      // L2 policy of weight copies: 0 evict_first, 1 evict_normal, 2 evict_last
 };
 
 // Shared state of the bounded waits of one CTA: the abort flag every role
@@ -158,8 +178,13 @@ __device__ __forceinline__ uint32_t poll_phase(uint32_t bar, uint32_t parity) {
   return SPIN ? ptx::mbar_test_wait(bar, parity) : ptx::mbar_try_wait(bar, parity);
 }
 
+// The slow path of a wait.  The spinning form (producer and MMA issuer,
+// both in the first warpgroup) stays out of line; the blocking form is
+// inlined into each role, since an out-of-line function shared by
+// warpgroups with different register budgets (setmaxnreg) cannot be
+// register-allocated.
 template <bool SPIN>
-__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile WaitCtl* wctl) {
+__device__ __forceinline__ bool wait_phase_loop(uint32_t bar, uint32_t parity, volatile WaitCtl* wctl) {
   const uint64_t t0 = ptx::globaltimer_ns();
   const uint64_t limit = uint64_t(wctl->limit_us) * 1000u;
   for (uint32_t i = 0;; ++i) {
@@ -174,11 +199,15 @@ __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, vola
     }
   }
 }
+__device__ __noinline__ bool wait_phase_slow_spin(uint32_t bar, uint32_t parity, volatile WaitCtl* wctl) {
+  return wait_phase_loop<true>(bar, parity, wctl);
+}
 
 template <bool SPIN = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile WaitCtl* abort_flag) {
   if (poll_phase<SPIN>(bar, parity)) return true;
-  return wait_phase_slow<SPIN>(bar, parity, abort_flag);
+  if constexpr (SPIN) return wait_phase_slow_spin(bar, parity, abort_flag);
+  else return wait_phase_loop<false>(bar, parity, abort_flag);
 }
 
 // Short bounded wait used only while draining after an abort.
@@ -417,7 +446,7 @@ __device__ __forceinline__ void requant_row32_mx(const uint32_t (&h)[32], int64_
 }
 
 template <int BN, int NA, bool SWIGLU, bool MX, bool TM, bool PAIR = false>
-__global__ void __launch_bounds__(num_threads(SWIGLU), 1)
+__global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_sf,
                         const __grid_constant__ CUtensorMap tmap_asf, const Params p) {
@@ -431,6 +460,12 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   constexpr int NW = PAIR ? 1 : C::NA;         // weight tiles in this CTA's stage
   const uint32_t crank = PAIR ? ptx::cluster_ctarank() : 0u;
   uint32_t* const sched = PAIR ? nullptr : p.sched;  // pairs run static stripes
+  // Token-major kernels tie each stage's scale-factor slot in tensor memory
+  // to its shared-memory stage, and the scale-factor warps arrive on the
+  // stage's full barrier: the MMA thread then waits on one barrier and
+  // commits once per stage.  Its MMAs queue only about one deep, so every
+  // handshake between stages leaves the tensor core idle.
+  constexpr bool kTied = TM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -468,7 +503,8 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   const int MT = SWIGLU ? p.N / 2 / kBM : p.N / (kBM * NA);  // M tiles per expert
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
-      ptx::mbar_init(full_bar(s), 1);
+      // producer's expect_tx, plus (tied scale slots) one arrival per scale-factor warp of each CTA
+      ptx::mbar_init(full_bar(s), kTied ? 1 + (PAIR ? 8 : 4) : 1);
       ptx::mbar_init(empty_bar(s), 1);
       ptx::mbar_init(sfc_bar(s), 1);
     }
@@ -573,7 +609,8 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
   const int off_b = NW * kATile;
   const int off_sfa = off_b + wmax * kBKBytes;
   const int off_sfb = off_sfa + C::NA * kSfTile;
-  const int S = min(p.stage_cap, (p.smem_bytes - ctrl - out_stage_bytes(SWIGLU, TM)) / stage);
+  const int S = min(kTied ? C::SfSlots : kMaxStages,
+                    min(p.stage_cap, (p.smem_bytes - ctrl - out_stage_bytes(SWIGLU, TM)) / stage));
   const uint32_t smem_base = ptx::smem_u32(smem) + uint32_t(ctrl);
   const uint32_t out_base = smem_base + uint32_t(S * stage);  // token-major bf16 chunk buffers
 
@@ -596,9 +633,14 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     return t;
   };
 
-  if (warp == 0 && lane == 0) {
+  // ---- warp roles (bodies as lambdas; dispatched below) ----
+  auto role_producer = [&]() {
     // ---------------- TMA producer ----------------
-    const uint64_t pol_w = ptx::policy_evict_first();  // weights stream through once
+    // weights stream through once at decode; token-major (many rows per
+    // expert) re-reads each weight tile for every token tile
+    const uint64_t pol_w = p.w_policy == 2   ? ptx::policy_evict_last()
+                           : p.w_policy == 1 ? ptx::policy_evict_normal()
+                                             : ptx::policy_evict_first();
     const uint64_t pol_a = ptx::policy_evict_last();   // token tiles are re-read by every M tile
     uint32_t it = 0;          // stages issued (for the drain after an abort)
     uint32_t s = 0, ph = 0;   // ring position of stage it and its phase parity
@@ -701,7 +743,8 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         }
       }
     }
-  } else if (PAIR && warp == 1 && lane == 0 && crank != 0) {
+  };
+  auto role_peer_wait = [&]() {
     // CTA 1 of a pair issues no MMAs; its tensor memory is freed once CTA 0's
     // last MMA (which writes it) has completed.  CTA 0 signals that at the end
     // of its MMA role, also after an abort, so this wait spans the whole
@@ -713,7 +756,8 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         break;
       }
     }
-  } else if (warp == 1 && lane == 0) {
+  };
+  auto role_mma = [&]() {
     // ---------------- MMA issuer ----------------
     // The tensor core queues about one MMA, so whatever this thread does
     // between two groups of MMAs (waits, commits, address arithmetic) leaves
@@ -788,33 +832,39 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       // per-round work, and each is issued as soon as it lands (waiting for a
       // second stage measured 2 % slower on the down GEMM); the default
       // orientation issues its N <= 128 MMAs two stages at a time.
-      constexpr bool kPairStages = !TM;
-      for (int kt = 0; kt < nkt; kt += kPairStages ? 2 : 1) {
-        const bool two = kPairStages && kt + 1 < nkt;
+      const bool pair_stages = !TM || p.batch2;
+      for (int kt = 0; kt < nkt; kt += pair_stages ? 2 : 1) {
+        const bool two = pair_stages && kt + 1 < nkt;
         uint32_t s2 = s + 1, ph2 = ph, r2 = r + 1, rph2 = rph;
         if (s2 == uint32_t(S)) s2 = 0, ph2 ^= 1u;
         if (r2 == uint32_t(C::SfSlots)) r2 = 0, rph2 ^= 1u;
         // A stage's scales are in tensor memory once the scale-factor warps
         // arrive, which they do only after its copies have landed; the
         // stage's own barrier is complete by then and is checked as well.
-        uint32_t ready = ptx::mbar_test_wait(sff_bar(r), rph) & ptx::mbar_test_wait(full_bar(s), ph);
-        if (two) ready &= ptx::mbar_test_wait(sff_bar(r2), rph2) & ptx::mbar_test_wait(full_bar(s2), ph2);
+        // (Tied slots: the scale-factor warps arrive on the stage's barrier.)
+        uint32_t ready = kTied ? ptx::mbar_test_wait(full_bar(s), ph)
+                               : ptx::mbar_test_wait(sff_bar(r), rph) & ptx::mbar_test_wait(full_bar(s), ph);
+        if (two)
+          ready &= kTied ? ptx::mbar_test_wait(full_bar(s2), ph2)
+                         : ptx::mbar_test_wait(sff_bar(r2), rph2) & ptx::mbar_test_wait(full_bar(s2), ph2);
         if (!ready) {
-          if (!wait_phase<true>(sff_bar(r), rph, abort_flag) || !wait_phase<true>(full_bar(s), ph, abort_flag) ||
-              (two && (!wait_phase<true>(sff_bar(r2), rph2, abort_flag) ||
+          if ((!kTied && !wait_phase<true>(sff_bar(r), rph, abort_flag)) ||
+              !wait_phase<true>(full_bar(s), ph, abort_flag) ||
+              (two && ((!kTied && !wait_phase<true>(sff_bar(r2), rph2, abort_flag)) ||
                        !wait_phase<true>(full_bar(s2), ph2, abort_flag)))) {
             ok = false;
             break;
           }
         }
         ptx::tc_fence_after();
-        issue_stage(kt, smem_base + s * uint32_t(stage), tmem + uint32_t(kSfColBase + r * C::SfCols));
-        commit(empty_bar(s));  // frees the stage once these MMAs have read it
-        commit(sfe_bar(r));
+        issue_stage(kt, smem_base + s * uint32_t(stage), tmem + uint32_t(kSfColBase + (kTied ? s : r) * C::SfCols));
+        commit(empty_bar(s));  // frees the stage (and, tied, its scale slot) once these MMAs have read it
+        if (!kTied) commit(sfe_bar(r));
         if (two) {
-          issue_stage(kt + 1, smem_base + s2 * uint32_t(stage), tmem + uint32_t(kSfColBase + r2 * C::SfCols));
+          issue_stage(kt + 1, smem_base + s2 * uint32_t(stage),
+                      tmem + uint32_t(kSfColBase + (kTied ? s2 : r2) * C::SfCols));
           commit(empty_bar(s2));
-          commit(sfe_bar(r2));
+          if (!kTied) commit(sfe_bar(r2));
           s = s2 + 1, ph = ph2, r = r2 + 1, rph = rph2;
         } else {
           s = s2, ph = ph2, r = r2, rph = rph2;
@@ -829,7 +879,8 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     }
     commit(drain_bar);  // every MMA of this CTA (pair) done before tensor memory is freed
     drain_phase(drain_bar, 0);
-  } else if (warp >= 2 + epi_warps(SWIGLU)) {
+  };
+  auto role_scale = [&]() {
     // ---------------- scale factors: shared memory -> tensor memory ----------------
     // Each of the four warps writes its 32-lane quarter of every scale block
     // (the tensor core reads the 512-byte block of 128 rows as four 32-bit
@@ -855,13 +906,15 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
       if constexpr (TM) w = kBM;
       const int sfb_chunks = w > 128 ? 2 : 1;
       for (int kt = 0; kt < nkt; ++kt) {
-        if (!wait_phase(sfe_bar(r), rph ^ 1u, abort_flag) || !wait_phase(sfc_bar(s), ph, abort_flag)) {
+        // Tied slots: the stage's scale copies are issued only after the MMAs
+        // that last read its slot have completed, so their arrival is enough.
+        if ((!kTied && !wait_phase(sfe_bar(r), rph ^ 1u, abort_flag)) || !wait_phase(sfc_bar(s), ph, abort_flag)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
         const uint32_t st = smem_base + s * uint32_t(stage);
-        const uint32_t sf = tmem + lane_base + uint32_t(kSfColBase + r * C::SfCols);
+        const uint32_t sf = tmem + lane_base + uint32_t(kSfColBase + (kTied ? s : r) * C::SfCols);
         const int nkb = min(4, kblocks - 4 * kt);
         if constexpr (MX) {
           // A 512-byte MXFP4 block holds 4 ue8m0 scales per row for 128 K
@@ -900,18 +953,21 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::mapa(sff_bar(r), 0));  // CTA 0 issues the MMAs
-          else ptx::mbar_arrive(sff_bar(r));
+          // CTA 0 of a pair issues the MMAs; tied slots arrive on the stage's full barrier
+          const uint32_t b = kTied ? full_bar(s) : sff_bar(r);
+          if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::mapa(b, 0));
+          else ptx::mbar_arrive(b);
         }
         if (++s == uint32_t(S)) s = 0, ph ^= 1u;
         if (++r == uint32_t(C::SfSlots)) r = 0, rph ^= 1u;
       }
     }
-  } else if (warp >= 2) {
+  };
+  auto role_epilogue = [&]() {
     // ---------------- epilogue ----------------
     const int q = warp & 3;            // tensor-memory lane quarter this warp may access
     constexpr int kParts = epi_warps(SWIGLU) / 4;  // warps sharing a quarter split the token chunks
-    const int part = (warp - 2) / 4;
+    const int part = (warp - epi_first(TM)) / 4;
     const int lrow = q * 32 + lane;    // accumulator row = output feature within the tile
     const float a_gs = MX ? 1.0f : *p.a_gscale;   // MXFP4 has no per-tensor scales
     const bool f32_out = p.epi == NVFP4MOE_EPI_SWIGLU_F32;
@@ -965,19 +1021,18 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
         const bool row_ok = q * 32 + lane < valid;
         if constexpr (SWIGLU) {
           // Features [64 part, 64 part + 64) of the tile's 128: gate in
-          // columns c, up in 128 + c; two 32-feature chunks, the accumulator
-          // released once both are in registers.
+          // columns c, up in 128 + c; both 32-feature chunks are loaded at
+          // once and the accumulator released before any arithmetic.
           static_assert(kParts == 2, "two epilogue warps per lane quarter");
           const int c0 = 64 * part;
-          uint32_t h0[32], g[32], u[32];
+          uint32_t h0[32], u0[32], g[32], u[32];
           ptx::tmem_ld_32x32b_x32(tbase + c0, h0);
-          ptx::tmem_ld_32x32b_x32(tbase + kBM + c0, u);
-          ptx::tmem_ld_wait();
-          swiglu(h0, u);
+          ptx::tmem_ld_32x32b_x32(tbase + kBM + c0, u0);
           ptx::tmem_ld_32x32b_x32(tbase + c0 + 32, g);
           ptx::tmem_ld_32x32b_x32(tbase + kBM + c0 + 32, u);
           ptx::tmem_ld_wait();
           release();
+          swiglu(h0, u0);
           swiglu(g, u);
           if (row_ok) {
             const int fo = mb * kBM + c0;  // output feature of h0[0]
@@ -1008,23 +1063,25 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
           // segments) when all 32 rows of the quarter belong to the expert;
           // a partial quarter stores per thread and leaves the padding rows
           // untouched.
+          // Four 32-column chunks per tensor-memory round trip (two round
+          // trips for the row), packed to bf16 in registers.
           constexpr int kChunks = C::NA * kBM / 32;
+          constexpr int kPerTrip = 4;
           uint32_t pk[kChunks][16];
 #pragma unroll
-          for (int c = 0; c < kChunks; c += 2) {
-            uint32_t g0[32], g1[32];
-            ptx::tmem_ld_32x32b_x32(tbase + 32 * c, g0);
-            ptx::tmem_ld_32x32b_x32(tbase + 32 * c + 32, g1);
+          for (int c = 0; c < kChunks; c += kPerTrip) {
+            uint32_t g[kPerTrip][32];
+#pragma unroll
+            for (int j = 0; j < kPerTrip; ++j) ptx::tmem_ld_32x32b_x32(tbase + 32 * (c + j), g[j]);
             ptx::tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const __nv_bfloat162 v0 = __floats2bfloat162_rn(__uint_as_float(g0[2 * i]) * scale,
-                                                              __uint_as_float(g0[2 * i + 1]) * scale);
-              const __nv_bfloat162 v1 = __floats2bfloat162_rn(__uint_as_float(g1[2 * i]) * scale,
-                                                              __uint_as_float(g1[2 * i + 1]) * scale);
-              pk[c][i] = *reinterpret_cast<const uint32_t*>(&v0);
-              pk[c + 1][i] = *reinterpret_cast<const uint32_t*>(&v1);
-            }
+            for (int j = 0; j < kPerTrip; ++j)
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(g[j][2 * i]) * scale,
+                                                               __uint_as_float(g[j][2 * i + 1]) * scale);
+                pk[c + j][i] = *reinterpret_cast<const uint32_t*>(&v);
+              }
           }
           release();
           const bool quarter_full = q * 32 + 32 <= valid;
@@ -1125,29 +1182,65 @@ __global__ void __launch_bounds__(num_threads(SWIGLU), 1)
     if constexpr (TM && !SWIGLU) {
       if (lane == 0) ptx::bulk_wait_all();  // this warp's TMA stores have completed
     }
-  }
-
-  ptx::tc_fence_before();
-  __syncthreads();
-  // A pair frees its tensor memory together (one warp of each CTA), once
-  // both CTAs are done with it.
-  if constexpr (PAIR) ptx::cluster_sync();
-  if (warp == 1) {
-    __syncwarp();
-    ptx::tc_fence_after();
-    if constexpr (PAIR) ptx::tmem_dealloc_pair(tmem, kTmemCols);
-    else ptx::tmem_dealloc(tmem, kTmemCols);
-  }
-  // Neither CTA of a pair leaves while the other may still signal its barriers.
-  if constexpr (PAIR) ptx::cluster_sync();
-  // Dynamic schedule: the last CTA to finish (every producer has stopped
-  // claiming by then) leaves both counters at zero for the next launch.
-  if (sched && threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(p.sched + 32, 1u) == gridDim.x - 1) {
-      atomicExch(p.sched, 0u);
-      atomicExch(p.sched + 32, 0u);
+  };
+  // Teardown, reached by every thread: all roles done, tensor memory freed
+  // by warp 1 (for a pair: by both CTAs together, once both are done with
+  // it), no CTA of a pair leaving while the other may still signal it.
+  auto teardown = [&]() {
+    ptx::tc_fence_before();
+    __syncthreads();
+    if constexpr (PAIR) ptx::cluster_sync();
+    if (warp == 1) {
+      __syncwarp();
+      ptx::tc_fence_after();
+      if constexpr (PAIR) ptx::tmem_dealloc_pair(tmem, kTmemCols);
+      else ptx::tmem_dealloc(tmem, kTmemCols);
     }
+    if constexpr (PAIR) ptx::cluster_sync();
+    // Dynamic schedule: the last CTA to finish (every producer has stopped
+    // claiming by then) leaves both counters at zero for the next launch.
+    if (sched && threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(p.sched + 32, 1u) == gridDim.x - 1) {
+        atomicExch(p.sched, 0u);
+        atomicExch(p.sched + 32, 0u);
+      }
+    }
+  };
+  if constexpr (TM) {
+    // Token-major kernels branch by warpgroup first: each warpgroup sets its
+    // register budget (setmaxnreg) at the top of its branch, so the
+    // epilogue warpgroups get the registers the producer / MMA and the
+    // scale-factor warpgroups leave unused and can hold their whole share of
+    // the accumulator (budgets at regs_control).  Each branch runs its own
+    // copy of the teardown, so no code is shared by warps with different
+    // budgets.
+    const int wg = warp >> 2;
+    if (wg == 0) {
+      ptx::setmaxnreg_dec<regs_control(SWIGLU)>();
+      if (warp == 0 && lane == 0) {
+        role_producer();
+      } else if (warp == 1 && lane == 0) {
+        if (PAIR && crank != 0) role_peer_wait();
+        else role_mma();
+      }
+      __syncwarp();
+      teardown();
+    } else if (wg == (epi_first(TM) + epi_warps(SWIGLU)) / 4) {
+      ptx::setmaxnreg_dec<regs_scale(SWIGLU)>();
+      role_scale();
+      teardown();
+    } else {
+      ptx::setmaxnreg_inc<regs_epilogue(SWIGLU)>();
+      role_epilogue();
+      teardown();
+    }
+  } else {
+    if (warp == 0 && lane == 0) role_producer();
+    else if (warp == 1 && lane == 0) role_mma();
+    else if (warp >= epi_first(TM) + epi_warps(SWIGLU)) role_scale();
+    else if (warp >= epi_first(TM)) role_epilogue();
+    teardown();
   }
 }
 
@@ -1332,6 +1425,26 @@ int max_pairs(K kernel, int threads, size_t smem, int num_sms) {
   return cached[dev];
 }
 
+// L2 policy of the weight copies of token-major kernels: NVFP4MOE_WPOL
+// (0 evict_first, 1 evict_normal, 2 evict_last), for cache studies.
+int w_policy_from_env(int dflt) {
+  static const int v = [] {
+    const char* e = std::getenv("NVFP4MOE_WPOL");
+    return e ? std::atoi(e) : -1;
+  }();
+  return v >= 0 && v <= 2 ? v : dflt;
+}
+
+// Token-major MMA issue in pairs of stages: NVFP4MOE_TM_BATCH=2 (1 is the
+// default), for pipeline studies.
+int tm_batch_from_env() {
+  static const int b = [] {
+    const char* v = std::getenv("NVFP4MOE_TM_BATCH");
+    return v && v[0] == '2' ? 1 : 0;
+  }();
+  return b;
+}
+
 template <int BN, int NA, bool SWIGLU, bool MX, bool TM = false, bool PAIR = false>
 int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st) {
   using C = Cfg<BN, NA, SWIGLU>;
@@ -1385,6 +1498,12 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   p.w_tiled = a.w_tiled ? 1 : 0;
   p.w_kc = w_kc;
   p.wait_us = wait_limit_us();
+  p.batch2 = tm_batch_from_env();
+  // Pair tiles serve experts with many rows: every weight tile is re-read by
+  // each of the expert's token tiles, so the weights stay in L2 (evict_last;
+  // measured at 2048 rows per expert: gate/up 2.76 -> 2.66 ms, down 1.58 ->
+  // 1.46 ms against evict_first).
+  p.w_policy = PAIR ? w_policy_from_env(2) : TM ? w_policy_from_env(0) : 0;
   // Launched without programmatic dependent launch: measured on GB300, a
   // grouped GEMM launched with it streamed its weight tiles about 2.5%
   // slower per tile, more than the few microseconds of launch latency it
@@ -1393,7 +1512,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   if constexpr (PAIR) {
     // Clusters of two CTAs on neighbouring SMs, as many as can be resident
     // at once (the kernel is persistent: pair c takes tiles c, c + #pairs, ...).
-    const int pairs = max_pairs(kernel, num_threads(SWIGLU), smem, num_sms);
+    const int pairs = max_pairs(kernel, num_threads(SWIGLU, TM), smem, num_sms);
     if (pairs < 1) {
       set_error_detail("no CTA pair of the grouped GEMM fits on this device");
       return NVFP4MOE_ERR_SMEM;
@@ -1406,7 +1525,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2 * pairs);
-    cfg.blockDim = dim3(num_threads(SWIGLU));
+    cfg.blockDim = dim3(num_threads(SWIGLU, TM));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
@@ -1414,7 +1533,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
     err = cudaLaunchKernelEx(&cfg, kernel, tw, ta, tc, tsf, tasf, p);
     if (err == cudaSuccess) err = cudaGetLastError();
   } else {
-    kernel<<<num_sms, num_threads(SWIGLU), smem, st>>>(tw, ta, tc, tsf, tasf, p);
+    kernel<<<num_sms, num_threads(SWIGLU, TM), smem, st>>>(tw, ta, tc, tsf, tasf, p);
     err = cudaGetLastError();
   }
   if (err != cudaSuccess) {

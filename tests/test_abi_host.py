@@ -284,3 +284,22 @@ def test_validation_of_the_other_calls(lib):
     assert r(None, None, 0, 8, 2, 1, 1, None, None, None) == 0
     assert q(None, 0, 64, None, 1, None, None, None, 0, None) == 0
     assert f(None, None, None, 0, 2, 16, 0, None, None) == 0
+
+
+def test_gemm_tile_choice_follows_rows_per_expert(lib):
+    """The automatic tile orientation (host logic, no device): weight rows as
+    M below 64 routed rows per expert on average, token-major from 64,
+    token-major on CTA pairs from 512; an explicit tile_n or an N that is not
+    a multiple of 256 is kept."""
+    f = lib.nvfp4moe_gemm_tile_choice
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int]
+    assert f(256, 4096, 1024, 0) == 0            # decode_t128: 4 rows per expert
+    assert f(256, 4096, 16383, 0) == 0
+    assert f(256, 4096, 16384, 0) == -1          # skewed_t2048: 64 rows per expert on average
+    assert f(64, 8192, 32767, 0) == -1
+    assert f(64, 8192, 32768, 0) == -2           # 512 rows per expert
+    assert f(64, 8192, 131072, 0) == -2          # prefill_t16384
+    assert f(64, 8192, 131072, 128) == 128       # explicit choice kept
+    assert f(64, 8192, 131072, -1) == -1
+    assert f(64, 384, 131072, 0) == 0            # N % 256 != 0: no token-major tiles
