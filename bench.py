@@ -163,86 +163,24 @@ class ClockSampler:
 # the CUDA path
 # ----------------------------------------------------------------------------
 def step_with_kernel_events(B, layer, x, logits, ev):
-    """One layer forward with events between the library calls (the same
-    calls, in the same order, as MoELayer.forward, on the current stream).
-    An event between two kernels ends their launch overlap, so these
-    per-kernel durations are those of isolated launches."""
-    p = layer.perm
-    T = x.shape[0]
-    i = 0
-    ev[i].record()
-    if layer.fmt == "mxfp4":
-        if layer.fused_prepare:
-            B.moe_prepare_mxfp4(logits, x, layer.k, layer.score_fn, layer.renormalize, layer.bias, layer.topk_idx,
-                                layer.topk_w, layer.xq, layer.xs, out=p, workspace=layer.prep_ws,
-                                k_primary=layer.k_primary)
-            i += 1
-            ev[i].record()
-        else:
-            layer._route(logits)
-            i += 1
-            ev[i].record()
-            B.moe_quantize_mxfp4(x, packed=layer.xq, scales=layer.xs)
-            i += 1
-            ev[i].record()
-            B.moe_permute_mxfp4(layer.topk_idx, layer.E, layer.xq, layer.xs, out=p, workspace=layer.p_ws)
-            i += 1
-            ev[i].record()
-        B.moe_grouped_gemm_mxfp4(p.a_packed, p.a_scales, p.counts, p.row_offsets, layer.w_gu_packed,
-                                 layer.w_gu_scales, B.EPI_SWIGLU_MXFP4, m_total=T * layer.k, tile_n=layer.tile_n[0],
-                                 out=layer.hq, out_scales=layer.hs, workspace=layer.g_ws)
-        i += 1
-        ev[i].record()
-        B.moe_grouped_gemm_mxfp4(layer.hq, layer.hs, p.counts, p.row_offsets, layer.w_d_packed, layer.w_d_scales,
-                                 B.EPI_BF16, m_total=T * layer.k, tile_n=layer.tile_n[1], out=layer.y,
-                                 workspace=layer.g_ws)
-        i += 1
-        ev[i].record()
-        B.moe_finalize(layer.y, p.flat_to_perm, layer.topk_w, out=layer.out)
-        i += 1
-        ev[i].record()
-        return
-    if layer.fused_prepare:
-        B.moe_prepare(logits, x, layer.k, layer.score_fn, layer.renormalize, layer.bias, layer.topk_idx,
-                      layer.topk_w, layer.x_gscale, layer.xq, layer.xs, out=p, workspace=layer.prep_ws,
-                      k_primary=layer.k_primary)
-        i += 1
-        ev[i].record()
-    else:
-        if layer.k_primary < layer.k:
-            B.moe_route_batch_aware(logits, layer.k, layer.k_primary, layer.score_fn, layer.renormalize, layer.bias,
-                                    layer.topk_idx, layer.topk_w, workspace=layer.r_ws)
-        else:
-            B.moe_route_topk(logits, layer.k, layer.score_fn, layer.renormalize, layer.bias, layer.topk_idx,
-                             layer.topk_w)
-        i += 1
-        ev[i].record()
-        B.moe_quantize_nvfp4(x, global_scale=layer.x_gscale, compute_global=True, packed=layer.xq,
-                             scales=layer.xs, workspace=layer.q_ws)
-        i += 1
-        ev[i].record()
-        B.moe_permute(layer.topk_idx, layer.E, layer.xq, layer.xs, out=p, workspace=layer.p_ws)
-        i += 1
-        ev[i].record()
-    B.moe_grouped_gemm_nvfp4(p.a_packed, p.a_scales, layer.x_gscale, p.counts, p.row_offsets, layer.w_gu_packed,
-                             layer.w_gu_scales, layer.w_gu_gscale, B.EPI_SWIGLU_NVFP4, c_gscale=layer.h_scale,
-                             m_total=T * layer.k, tile_n=layer.tile_n[0], out=layer.hq, out_scales=layer.hs,
-                             workspace=layer.g_ws)
-    i += 1
-    ev[i].record()
-    B.moe_grouped_gemm_nvfp4(layer.hq, layer.hs, layer.h_scale, p.counts, p.row_offsets, layer.w_d_packed,
-                             layer.w_d_scales, layer.w_d_gscale, B.EPI_BF16, m_total=T * layer.k,
-                             tile_n=layer.tile_n[1], out=layer.y, workspace=layer.g_ws)
-    i += 1
-    ev[i].record()
-    B.moe_finalize(layer.y, p.flat_to_perm, layer.topk_w, out=layer.out)
-    i += 1
-    ev[i].record()
+    """One layer forward with events between its steps (MoELayer.prepare,
+    gemm_gate_up, gemm_down, finalize: the calls forward() makes, in the
+    same order, on the current stream).  An event between two kernels ends
+    their launch overlap, so these per-kernel durations are those of
+    isolated launches."""
+    ev[0].record()
+    layer.prepare(x, logits)
+    ev[1].record()
+    layer.gemm_gate_up()
+    ev[2].record()
+    layer.gemm_down()
+    ev[3].record()
+    layer.finalize()
+    ev[4].record()
 
 
 def kernel_names(fused_prepare):
-    head = ["prepare"] if fused_prepare else ["route", "quantize", "permute"]
-    return head + ["gemm_gate_up_swiglu", "gemm_down", "finalize"]
+    return ["prepare", "gemm_gate_up_swiglu", "gemm_down", "finalize"]
 
 
 def tile_name(t):
@@ -422,8 +360,10 @@ def run_ours(args, w):
         **{k: rec[k] for k in ("tflops", "hbm_gbs", "layer_roofline_frac", "kernels_ms", "ms_per_step_with_events",
                                "roofline", "roofline_down", "e2e", "clocks")},
         "prepare": "fused (one launch)" if layer.fused_prepare else "separate (route, quantise, permute)",
-        "gemm_tiles": {g: tile_name(B.gemm_tile_choice(w.E, n, w.T * w.k, t)) for g, n, t in
-                       (("gate_up", 2 * w.I, layer.tile_n[0]), ("down", w.H, layer.tile_n[1]))},
+        "gemm_plans": {g: [{"tiles": tile_name(B.gemm_tile_choice(w.E, n, w.T * w.k, t)), "expert_rows": list(r)}
+                           for t, r in plan]
+                       for g, n, plan in (("gate_up", 2 * w.I, layer.plan()[0]), ("down", w.H, layer.plan()[1]))},
+        "autotuned": w.T in layer.plans,
         "gemm_schedule": "dynamic" if layer.g_ws is not None else "static",
         "weights": "tiled" if isinstance(layer.w_gu_packed, B.TiledWeights) else "row-major",
     }

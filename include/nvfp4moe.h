@@ -383,6 +383,26 @@ int moe_grouped_gemm_nvfp4(const uint8_t* a_packed, const uint8_t* a_scales, con
                            void* c_out, uint8_t* c_scales, int tile_n, int w_layout,
                            void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* moe_grouped_gemm_nvfp4 restricted to the experts whose row count
+ * (expert_counts[e], read on the device) lies in [min_rows, max_rows); the
+ * other experts' output rows are left untouched.  Two calls over
+ * complementary ranges, each with its own tile_n, give the same outputs as
+ * one call over all experts (up to float32 summation order): a layer with
+ * a few experts holding hundreds of rows and many holding a handful can
+ * run the first on token-major tiles and the rest with weight rows as M.
+ * m_total should then be the routed rows the call is expected to cover; it
+ * only guides tile_n = 0.  1 <= min_rows <= max_rows; otherwise as
+ * moe_grouped_gemm_nvfp4 (which is this call with [1, INT32_MAX)).  No
+ * counterpart on the source pages beyond their per-regime tile choices. */
+int moe_grouped_gemm_nvfp4_range(const uint8_t* a_packed, const uint8_t* a_scales, const float* a_gscale,
+                                 const int32_t* expert_counts, const int32_t* row_offsets,
+                                 int E, int64_t rows_capacity, int64_t m_total,
+                                 const uint8_t* w_packed, const uint8_t* w_scales, const float* w_gscale,
+                                 int N, int K, int epilogue, const float* c_gscale,
+                                 void* c_out, uint8_t* c_scales, int tile_n, int w_layout,
+                                 int32_t min_rows, int32_t max_rows,
+                                 void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* ---- MXFP4 variant of a2, a3, a4/a5 -----------------------------------------
  * MXFP4 (page A, sections 2-4: the MXFP4 grouped GEMM that works with
  * specific tile parameters; the pages give the format's name only, so the
@@ -438,6 +458,15 @@ int moe_grouped_gemm_mxfp4(const uint8_t* a_packed, const uint8_t* a_scales,
                            const uint8_t* w_packed, const uint8_t* w_scales,
                            int N, int K, int epilogue, void* c_out, uint8_t* c_scales, int tile_n,
                            int w_layout, void* ws, size_t ws_bytes, cudaStream_t stream);
+/* moe_grouped_gemm_mxfp4 restricted to experts with min_rows <= rows <
+ * max_rows (see moe_grouped_gemm_nvfp4_range). */
+int moe_grouped_gemm_mxfp4_range(const uint8_t* a_packed, const uint8_t* a_scales,
+                                 const int32_t* expert_counts, const int32_t* row_offsets,
+                                 int E, int64_t rows_capacity, int64_t m_total,
+                                 const uint8_t* w_packed, const uint8_t* w_scales,
+                                 int N, int K, int epilogue, void* c_out, uint8_t* c_scales, int tile_n,
+                                 int w_layout, int32_t min_rows, int32_t max_rows,
+                                 void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ---- a6: finalize ----------------------------------------------------------
  * Router-weighted reduce back to token order (page A, section 6: the

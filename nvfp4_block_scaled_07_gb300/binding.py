@@ -53,6 +53,8 @@ _SIGS = {
     "moe_prepare_mxfp4": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p,
                                _p, _sz, _p]),
     "moe_grouped_gemm_mxfp4": (_i, [_p, _p, _p, _p, _i, _i64, _i64, _p, _p, _i, _i, _i, _p, _p, _i, _i, _p, _sz, _p]),
+    "moe_grouped_gemm_mxfp4_range": (_i, [_p, _p, _p, _p, _i, _i64, _i64, _p, _p, _i, _i, _i, _p, _p, _i, _i,
+                                          ctypes.c_int32, ctypes.c_int32, _p, _sz, _p]),
     "nvfp4moe_tiled_weights_bytes": (_sz, [_i64, _i]),
     "nvfp4moe_tile_weights": (_i, [_p, _i64, _i, _p, _p]),
     "moe_route_topk": (_i, [_p, _p, _i, _i, _i, _i, _i, _p, _p, _p]),
@@ -72,6 +74,8 @@ _SIGS = {
     "nvfp4moe_gemm_tile_choice": (_i, [_i, _i, _i64, _i]),
     "moe_grouped_gemm_nvfp4": (_i, [_p, _p, _p, _p, _p, _i, _i64, _i64, _p, _p, _p, _i, _i, _i, _p, _p, _p, _i,
                                     _i, _p, _sz, _p]),
+    "moe_grouped_gemm_nvfp4_range": (_i, [_p, _p, _p, _p, _p, _i, _i64, _i64, _p, _p, _p, _i, _i, _i, _p, _p, _p,
+                                          _i, _i, ctypes.c_int32, ctypes.c_int32, _p, _sz, _p]),
     "moe_finalize": (_i, [_p, _p, _p, _i, _i, _i, _i64, _p, _p]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -502,13 +506,18 @@ def _ws_args(workspace):
     return _ptr(workspace), workspace.numel()
 
 
+ALL_ROWS = (1, 2 ** 31 - 1)
+
+
 def moe_grouped_gemm_nvfp4(a_packed, a_scales, a_gscale, counts, row_offsets, w_packed, w_scales, w_gscale,
                            epilogue=EPI_BF16, c_gscale=None, m_total=None, tile_n=0, out=None, out_scales=None,
-                           workspace=None):
+                           workspace=None, rows=ALL_ROWS):
     """Returns c_out (and c_scales for EPI_SWIGLU_NVFP4).  workspace: a zeroed
     alloc_gemm_workspace() for the dynamic tile schedule, None for static.
     w_packed: row-major [E, N, K/2] or TiledWeights.  m_total: the routed
-    rows (T*k), not the padded capacity; it picks the tile orientation."""
+    rows (T*k), not the padded capacity; it picks the tile orientation.
+    rows = (min_rows, max_rows): only experts with that many rows
+    (moe_grouped_gemm_nvfp4_range); the default covers every expert."""
     if m_total is None:
         raise ValueError("m_total (the routed rows, T*k) is required: it chooses the tile orientation")
     E, N, K, w_ptr, w_layout = _weights_args(w_packed)
@@ -543,16 +552,19 @@ def moe_grouped_gemm_nvfp4(a_packed, a_scales, a_gscale, counts, row_offsets, w_
     else:
         raise ValueError(f"epilogue {epilogue}")
     ws_p, ws_n = _ws_args(workspace)
-    _check(_lib.moe_grouped_gemm_nvfp4(_ptr(a_packed), _ptr(a_scales), _ptr(a_gscale), _ptr(counts),
-                                       _ptr(row_offsets), E, cap, int(m_total), w_ptr, _ptr(w_scales),
-                                       _ptr(w_gscale), N, K, epilogue, _ptr(c_gscale), _ptr(out),
-                                       _ptr(out_scales), int(tile_n), w_layout, ws_p, ws_n, _stream()),
-           "moe_grouped_gemm_nvfp4")
+    args = (_ptr(a_packed), _ptr(a_scales), _ptr(a_gscale), _ptr(counts), _ptr(row_offsets), E, cap, int(m_total),
+            w_ptr, _ptr(w_scales), _ptr(w_gscale), N, K, epilogue, _ptr(c_gscale), _ptr(out), _ptr(out_scales),
+            int(tile_n), w_layout)
+    if tuple(rows) == ALL_ROWS:
+        _check(_lib.moe_grouped_gemm_nvfp4(*args, ws_p, ws_n, _stream()), "moe_grouped_gemm_nvfp4")
+    else:
+        _check(_lib.moe_grouped_gemm_nvfp4_range(*args, int(rows[0]), int(rows[1]), ws_p, ws_n, _stream()),
+               "moe_grouped_gemm_nvfp4_range")
     return (out, out_scales) if epilogue == EPI_SWIGLU_NVFP4 else out
 
 
 def moe_grouped_gemm_mxfp4(a_packed, a_scales, counts, row_offsets, w_packed, w_scales, epilogue=EPI_BF16,
-                           m_total=None, tile_n=0, out=None, out_scales=None, workspace=None):
+                           m_total=None, tile_n=0, out=None, out_scales=None, workspace=None, rows=ALL_ROWS):
     """MXFP4 grouped GEMM.  Returns c_out (and c_scales for EPI_SWIGLU_MXFP4).
     w_packed: row-major [E, N, K/2] or TiledWeights."""
     if m_total is None:
@@ -584,10 +596,13 @@ def moe_grouped_gemm_mxfp4(a_packed, a_scales, counts, row_offsets, w_packed, w_
     else:
         raise ValueError(f"epilogue {epilogue}")
     ws_p, ws_n = _ws_args(workspace)
-    _check(_lib.moe_grouped_gemm_mxfp4(_ptr(a_packed), _ptr(a_scales), _ptr(counts), _ptr(row_offsets), E, cap,
-                                       int(m_total), w_ptr, _ptr(w_scales), N, K, epilogue, _ptr(out),
-                                       _ptr(out_scales), int(tile_n), w_layout, ws_p, ws_n, _stream()),
-           "moe_grouped_gemm_mxfp4")
+    args = (_ptr(a_packed), _ptr(a_scales), _ptr(counts), _ptr(row_offsets), E, cap, int(m_total), w_ptr,
+            _ptr(w_scales), N, K, epilogue, _ptr(out), _ptr(out_scales), int(tile_n), w_layout)
+    if tuple(rows) == ALL_ROWS:
+        _check(_lib.moe_grouped_gemm_mxfp4(*args, ws_p, ws_n, _stream()), "moe_grouped_gemm_mxfp4")
+    else:
+        _check(_lib.moe_grouped_gemm_mxfp4_range(*args, int(rows[0]), int(rows[1]), ws_p, ws_n, _stream()),
+               "moe_grouped_gemm_mxfp4_range")
     return (out, out_scales) if epilogue == EPI_SWIGLU_MXFP4 else out
 
 
@@ -614,14 +629,22 @@ class MoELayer:
     allocated for one batch size T (at construction when T is given, else at
     the first call, and again when T changes); otherwise forward() allocates
     nothing, and the tensor it returns is overwritten by the next call
-    unless the caller passes `out`.  With fused_prepare (the default): four launches --
+    unless the caller passes `out`.  With fused_prepare (the default):
     moe_prepare (route + quantise + permute; moe_prepare_mxfp4 for
-    fmt="mxfp4"), gate/up GEMM with SwiGLU and requantisation, down GEMM,
-    finalize -- otherwise the six separate calls."""
+    fmt="mxfp4"), the gate/up GEMM with SwiGLU and requantisation, the down
+    GEMM and finalize -- otherwise the six separate calls.
+
+    Each grouped GEMM runs a launch plan: a list of (tile_n, (min_rows,
+    max_rows)) launches that together cover every expert.  With autotune
+    (the default when tile_n is (0, 0)) the first forward() of a batch size
+    times the candidate plans (autotune()) on that batch and keeps the
+    fastest for the batch size: it synchronises the stream, so make that
+    first call outside stream capture.  Otherwise each GEMM is one launch
+    with the given tile_n."""
 
     def __init__(self, w_gu, w_d, k, score_fn="sigmoid", renormalize=True, h_scale=2.0 ** -4, bias=None,
                  T=None, tile_n=(0, 0), fused_prepare=True, k_primary=None, fmt="nvfp4", dynamic_schedule=True,
-                 tiled_weights=True):
+                 tiled_weights=True, autotune=True):
         if fmt not in ("nvfp4", "mxfp4"):
             raise ValueError(f"fmt {fmt}")
         self.fmt = fmt
@@ -635,7 +658,9 @@ class MoELayer:
         self.k, self.score_fn, self.renormalize = k, score_fn, renormalize
         self.device = w_gu.device
         self.bias = bias
-        self.tile_n = tile_n
+        self.tile_n = tuple(tile_n)
+        self.autotune_enabled = bool(autotune) and self.tile_n == (0, 0)
+        self.plans = {}          # batch size -> (gate/up plan, down plan), from autotune()
         if fmt == "mxfp4":
             self.w_gu_packed, self.w_gu_scales = quantize_expert_weights_mx(w_gu)
             self.w_d_packed, self.w_d_scales = quantize_expert_weights_mx(w_d)
@@ -673,10 +698,9 @@ class MoELayer:
         self.y = _empty((cap, H), torch.bfloat16, dev)
         self.out = _empty((T, H), torch.bfloat16, dev)
 
-    def forward(self, x, logits, out=None):
-        T = x.shape[0]
-        if self.T != T:
-            self._alloc(T)
+    # ---- the steps of forward() (bench.py times them one by one) ----
+    def prepare(self, x, logits):
+        """a1-a3: routing, quantisation of x and the permutation."""
         p = self.perm
         if self.fmt == "mxfp4":
             if self.fused_prepare:
@@ -686,13 +710,7 @@ class MoELayer:
                 self._route(logits)
                 moe_quantize_mxfp4(x, packed=self.xq, scales=self.xs)
                 moe_permute_mxfp4(self.topk_idx, self.E, self.xq, self.xs, out=p, workspace=self.p_ws)
-            moe_grouped_gemm_mxfp4(p.a_packed, p.a_scales, p.counts, p.row_offsets, self.w_gu_packed,
-                                   self.w_gu_scales, EPI_SWIGLU_MXFP4, m_total=T * self.k, tile_n=self.tile_n[0],
-                                   out=self.hq, out_scales=self.hs, workspace=self.g_ws)
-            moe_grouped_gemm_mxfp4(self.hq, self.hs, p.counts, p.row_offsets, self.w_d_packed, self.w_d_scales,
-                                   EPI_BF16, m_total=T * self.k, tile_n=self.tile_n[1], out=self.y,
-                                   workspace=self.g_ws)
-            return moe_finalize(self.y, p.flat_to_perm, self.topk_w, out=self.out if out is None else out)
+            return
         if self.fused_prepare:
             moe_prepare(logits, x, self.k, self.score_fn, self.renormalize, self.bias, self.topk_idx, self.topk_w,
                         self.x_gscale, self.xq, self.xs, out=p, workspace=self.prep_ws, k_primary=self.k_primary)
@@ -701,16 +719,113 @@ class MoELayer:
             moe_quantize_nvfp4(x, global_scale=self.x_gscale, compute_global=True, packed=self.xq,
                                scales=self.xs, workspace=self.q_ws)
             moe_permute(self.topk_idx, self.E, self.xq, self.xs, out=p, workspace=self.p_ws)
-        moe_grouped_gemm_nvfp4(p.a_packed, p.a_scales, self.x_gscale, p.counts, p.row_offsets, self.w_gu_packed,
-                               self.w_gu_scales, self.w_gu_gscale, EPI_SWIGLU_NVFP4, c_gscale=self.h_scale,
-                               m_total=T * self.k, tile_n=self.tile_n[0], out=self.hq, out_scales=self.hs,
-                               workspace=self.g_ws)
-        moe_grouped_gemm_nvfp4(self.hq, self.hs, self.h_scale, p.counts, p.row_offsets, self.w_d_packed,
-                               self.w_d_scales, self.w_d_gscale, EPI_BF16, m_total=T * self.k,
-                               tile_n=self.tile_n[1], out=self.y, workspace=self.g_ws)
-        return moe_finalize(self.y, p.flat_to_perm, self.topk_w, out=self.out if out is None else out)
+
+    def plan(self, T=None):
+        """(gate/up plan, down plan) of batch size T: lists of (tile_n, (min_rows, max_rows))."""
+        T = self.T if T is None else T
+        if T in self.plans:
+            return self.plans[T]
+        return [(self.tile_n[0], ALL_ROWS)], [(self.tile_n[1], ALL_ROWS)]
+
+    def _gemm(self, which, tile_n, rows):
+        p, m_total = self.perm, self.T * self.k
+        if which == "gate_up":
+            if self.fmt == "mxfp4":
+                moe_grouped_gemm_mxfp4(p.a_packed, p.a_scales, p.counts, p.row_offsets, self.w_gu_packed,
+                                       self.w_gu_scales, EPI_SWIGLU_MXFP4, m_total=m_total, tile_n=tile_n,
+                                       out=self.hq, out_scales=self.hs, workspace=self.g_ws, rows=rows)
+            else:
+                moe_grouped_gemm_nvfp4(p.a_packed, p.a_scales, self.x_gscale, p.counts, p.row_offsets,
+                                       self.w_gu_packed, self.w_gu_scales, self.w_gu_gscale, EPI_SWIGLU_NVFP4,
+                                       c_gscale=self.h_scale, m_total=m_total, tile_n=tile_n, out=self.hq,
+                                       out_scales=self.hs, workspace=self.g_ws, rows=rows)
+        elif self.fmt == "mxfp4":
+            moe_grouped_gemm_mxfp4(self.hq, self.hs, p.counts, p.row_offsets, self.w_d_packed, self.w_d_scales,
+                                   EPI_BF16, m_total=m_total, tile_n=tile_n, out=self.y, workspace=self.g_ws,
+                                   rows=rows)
+        else:
+            moe_grouped_gemm_nvfp4(self.hq, self.hs, self.h_scale, p.counts, p.row_offsets, self.w_d_packed,
+                                   self.w_d_scales, self.w_d_gscale, EPI_BF16, m_total=m_total, tile_n=tile_n,
+                                   out=self.y, workspace=self.g_ws, rows=rows)
+
+    def gemm_gate_up(self, plan=None):
+        """a4: gate/up GEMM with the fused SwiGLU + requantisation, by launch plan."""
+        for tile_n, rows in (self.plan()[0] if plan is None else plan):
+            self._gemm("gate_up", tile_n, rows)
+
+    def gemm_down(self, plan=None):
+        """a5: down GEMM to bf16, by launch plan."""
+        for tile_n, rows in (self.plan()[1] if plan is None else plan):
+            self._gemm("down", tile_n, rows)
+
+    def finalize(self, out=None):
+        """a6: the router-weighted sum back to token order."""
+        return moe_finalize(self.y, self.perm.flat_to_perm, self.topk_w, out=self.out if out is None else out)
+
+    def forward(self, x, logits, out=None):
+        T = x.shape[0]
+        if self.T != T:
+            self._alloc(T)
+        if self.autotune_enabled and T not in self.plans:
+            self.autotune(x, logits)
+        self.prepare(x, logits)
+        self.gemm_gate_up()
+        self.gemm_down()
+        return self.finalize(out)
 
     __call__ = forward
+
+    # ---- tile autotuner ----
+    def candidate_plans(self, which, T=None):
+        """Launch plans the autotuner times for one GEMM at batch size T: one
+        launch per orientation (the automatic choice, weight rows as M,
+        token-major, token-major on CTA pairs), and splits that run experts
+        with at least h rows token-major (single SM or pairs) and the rest
+        with weight rows as M."""
+        T = self.T if T is None else T
+        N = 2 * self.I if which == "gate_up" else self.H
+        plans = [[(0, ALL_ROWS)], [(128, ALL_ROWS)]]
+        if N % 256 == 0:
+            plans += [[(TILE_TOKEN_MAJOR, ALL_ROWS)], [(TILE_TOKEN_MAJOR_PAIR, ALL_ROWS)]]
+            for h in (32, 128, 512):
+                if T * self.k >= h:
+                    for tm in (TILE_TOKEN_MAJOR, TILE_TOKEN_MAJOR_PAIR):
+                        plans.append([(tm, (h, ALL_ROWS[1])), (128, (1, h))])
+        return plans
+
+    def autotune(self, x, logits, reps=5):
+        """Times every candidate plan of both GEMMs on this batch (CUDA events,
+        median of `reps` launches after one warm-up) and keeps the fastest for
+        x's batch size; returns {"gate_up": (plan, ms), "down": (plan, ms)}.
+        Every plan computes the same outputs (up to float32 summation order);
+        only the launch configuration differs.  Synchronises the stream."""
+        T = x.shape[0]
+        if self.T != T:
+            self._alloc(T)
+        self.prepare(x, logits)
+        chosen, report = [], {}
+        for which, run in (("gate_up", self.gemm_gate_up), ("down", self.gemm_down)):
+            best = None
+            for plan in self.candidate_plans(which, T):
+                times = []
+                for i in range(reps + 1):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    run(plan)
+                    e1.record()
+                    e1.synchronize()
+                    if i:
+                        times.append(e0.elapsed_time(e1))
+                ms = sorted(times)[len(times) // 2]
+                if best is None or ms < best[1]:
+                    best = (plan, ms)
+            if which == "gate_up":
+                run(best[0])             # the down GEMM's input, from the chosen plan
+            chosen.append(best[0])
+            report[which] = best
+        sync_status()
+        self.plans[T] = tuple(chosen)
+        return report
 
     def _route(self, logits):
         if self.k_primary < self.k:
@@ -719,12 +834,15 @@ class MoELayer:
         else:
             moe_route_topk(logits, self.k, self.score_fn, self.renormalize, self.bias, self.topk_idx, self.topk_w)
 
-    # kernels launched by one forward(): fused prepare 1 (else route 1, quantise 2, permute 3),
-    # GEMMs 2, finalize 1
+    # kernels launched by one forward(): fused prepare 1 (else route 1-2, quantise 1-2, permute 3),
+    # one per launch of each GEMM plan, finalize 1
     @property
     def launches_per_forward(self):
+        gu, down = self.plan()
         if self.fused_prepare:
-            return 4
-        route = 2 if self.k_primary < self.k else 1
-        quantise = 1 if self.fmt == "mxfp4" else 2
-        return route + quantise + 3 + 2 + 1
+            head = 1
+        else:
+            route = 2 if self.k_primary < self.k else 1
+            quantise = 1 if self.fmt == "mxfp4" else 2
+            head = route + quantise + 3
+        return head + len(gu) + len(down) + 1

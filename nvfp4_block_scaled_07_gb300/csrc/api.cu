@@ -2,6 +2,7 @@
 // attribute cache and status plumbing.  The compute lives in
 // kernels_prep.cu and grouped_gemm.cu; nothing here allocates device memory.
 #include <atomic>
+#include <cstdint>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -481,9 +482,11 @@ static int grouped_gemm_common(bool mx, const uint8_t* a_packed, const uint8_t* 
                                const int32_t* expert_counts, const int32_t* row_offsets, int E, int64_t rows_capacity,
                                int64_t m_total, const uint8_t* w_packed, const uint8_t* w_scales,
                                const float* w_gscale, int N, int K, int epilogue, const float* c_gscale, void* c_out,
-                               uint8_t* c_scales, int tile_n, int w_layout, void* ws, size_t ws_bytes,
-                               cudaStream_t stream) {
+                               uint8_t* c_scales, int tile_n, int w_layout, int32_t min_rows,
+                               int32_t max_rows, void* ws, size_t ws_bytes, cudaStream_t stream) {
   t_detail[0] = 0;
+  NVFP4MOE_REQUIRE(min_rows >= 1 && min_rows <= max_rows, NVFP4MOE_ERR_INVALID_ARG,
+                   "expert row range [%d, %d) must have 1 <= min_rows <= max_rows", min_rows, max_rows);
   NVFP4MOE_REQUIRE(w_layout == NVFP4MOE_W_ROWMAJOR || w_layout == NVFP4MOE_W_TILED, NVFP4MOE_ERR_INVALID_ARG,
                    "w_layout %d", w_layout);
   NVFP4MOE_REQUIRE(!ws || (ws_bytes >= kGemmWorkspaceBytes && (reinterpret_cast<uintptr_t>(ws) & 255) == 0),
@@ -545,6 +548,8 @@ static int grouped_gemm_common(bool mx, const uint8_t* a_packed, const uint8_t* 
   a.mx = mx;
   a.w_tiled = w_layout == NVFP4MOE_W_TILED;
   a.sched = ws;
+  a.min_rows = min_rows;
+  a.max_rows = max_rows;
   return launch_grouped_gemm(a, d.num_sms, d.smem_optin, stream);  // detail already set on failure
 }
 
@@ -556,7 +561,19 @@ int moe_grouped_gemm_nvfp4(const uint8_t* a_packed, const uint8_t* a_scales, con
                            cudaStream_t stream) {
   return grouped_gemm_common(false, a_packed, a_scales, a_gscale, expert_counts, row_offsets, E, rows_capacity,
                              m_total, w_packed, w_scales, w_gscale, N, K, epilogue, c_gscale, c_out, c_scales, tile_n,
-                             w_layout, ws, ws_bytes, stream);
+                             w_layout, 1, INT32_MAX, ws, ws_bytes, stream);
+}
+
+int moe_grouped_gemm_nvfp4_range(const uint8_t* a_packed, const uint8_t* a_scales, const float* a_gscale,
+                                 const int32_t* expert_counts, const int32_t* row_offsets, int E,
+                                 int64_t rows_capacity, int64_t m_total, const uint8_t* w_packed,
+                                 const uint8_t* w_scales, const float* w_gscale, int N, int K, int epilogue,
+                                 const float* c_gscale, void* c_out, uint8_t* c_scales, int tile_n, int w_layout,
+                                 int32_t min_rows, int32_t max_rows, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream) {
+  return grouped_gemm_common(false, a_packed, a_scales, a_gscale, expert_counts, row_offsets, E, rows_capacity,
+                             m_total, w_packed, w_scales, w_gscale, N, K, epilogue, c_gscale, c_out, c_scales, tile_n,
+                             w_layout, min_rows, max_rows, ws, ws_bytes, stream);
 }
 
 int moe_grouped_gemm_mxfp4(const uint8_t* a_packed, const uint8_t* a_scales, const int32_t* expert_counts,
@@ -566,7 +583,17 @@ int moe_grouped_gemm_mxfp4(const uint8_t* a_packed, const uint8_t* a_scales, con
                            cudaStream_t stream) {
   return grouped_gemm_common(true, a_packed, a_scales, nullptr, expert_counts, row_offsets, E, rows_capacity, m_total,
                              w_packed, w_scales, nullptr, N, K, epilogue, nullptr, c_out, c_scales, tile_n, w_layout,
-                             ws, ws_bytes, stream);
+                             1, INT32_MAX, ws, ws_bytes, stream);
+}
+
+int moe_grouped_gemm_mxfp4_range(const uint8_t* a_packed, const uint8_t* a_scales, const int32_t* expert_counts,
+                                 const int32_t* row_offsets, int E, int64_t rows_capacity, int64_t m_total,
+                                 const uint8_t* w_packed, const uint8_t* w_scales, int N, int K, int epilogue,
+                                 void* c_out, uint8_t* c_scales, int tile_n, int w_layout, int32_t min_rows,
+                                 int32_t max_rows, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return grouped_gemm_common(true, a_packed, a_scales, nullptr, expert_counts, row_offsets, E, rows_capacity, m_total,
+                             w_packed, w_scales, nullptr, N, K, epilogue, nullptr, c_out, c_scales, tile_n, w_layout,
+                             min_rows, max_rows, ws, ws_bytes, stream);
 }
 
 // ---- a6 ---------------------------------------------------------------------

@@ -131,6 +131,7 @@ struct Params {
   uint32_t wait_us;  // limit of every pipeline wait (nvfp4moe_set_wait_limit_us)
   int batch2;        // token-major: the MMA thread waits for and issues two stages at a time
   int w_policy;      // L2 policy of weight copies: 0 evict_first, 1 evict_normal, 2 evict_last
+  int32_t min_rows, max_rows;  // experts outside [min_rows, max_rows) get no tiles in this launch
 };
 
 // Shared state of the bounded waits of one CTA: the abort flag every role
@@ -556,6 +557,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
         atomicOr(&g_gemm_flags, kFlagBadData);
         c = 0;
       }
+      if (c < p.min_rows || c >= p.max_rows) c = 0;  // another launch covers this expert
       s_count[e] = c;
       s_rowoff[e] = ro;
       const int ntn = (c + TB - 1) / TB;
@@ -1499,6 +1501,8 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   p.w_kc = w_kc;
   p.wait_us = wait_limit_us();
   p.batch2 = tm_batch_from_env();
+  p.min_rows = a.min_rows;
+  p.max_rows = a.max_rows;
   // Pair tiles serve experts with many rows: every weight tile is re-read by
   // each of the expert's token tiles, so the weights stay in L2 (evict_last;
   // measured at 2048 rows per expert: gate/up 2.76 -> 2.66 ms, down 1.58 ->

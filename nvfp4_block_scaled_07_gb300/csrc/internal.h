@@ -115,6 +115,7 @@ struct GemmArgs {
   bool mx;  // MXFP4 operands (ue8m0 scale per 32 elements, no per-tensor scales)
   bool w_tiled;  // w_packed in the tiled layout (NVFP4MOE_W_TILED)
   void* sched;  // zero-filled 256-byte tile-scheduler workspace, or null for the static schedule
+  int32_t min_rows, max_rows;  // experts outside [min_rows, max_rows) get no tiles
 };
 
 constexpr size_t kGemmWorkspaceBytes = 256;

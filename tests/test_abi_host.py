@@ -217,7 +217,7 @@ def _header_signatures():
         if "*" in decl or decl.startswith("cudaStream_t"):
             return "cstr" if decl.replace(" ", "").startswith("constchar*") and "(" not in decl else "p"
         t = decl.split()[0] if not decl.startswith("const ") else decl.split()[1]
-        return {"int": "i", "uint32_t": "u32", "int64_t": "i64", "size_t": "sz"}[t]
+        return {"int": "i", "int32_t": "i", "uint32_t": "u32", "int64_t": "i64", "size_t": "sz"}[t]
 
     sigs = {}
     for m in re.finditer(r"([\w\s\*]+?)\b((?:moe|nvfp4moe)_\w+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
