@@ -231,7 +231,7 @@ def measure_layer(args, w, world, rank, with_e2e=True):
     layer = B.MoELayer(inp["w_gu"], inp["w_d"], w.k, w.score, w.renormalize, w.h_scale, bias=inp["bias"],
                        T=w.T, tile_n=(args.tile_gate_up, args.tile_down), fused_prepare=not args.separate_prepare,
                        k_primary=args.k_primary, fmt=args.format, dynamic_schedule=not args.static_schedule,
-                       tiled_weights=args.weights == "tiled")
+                       tiled_weights=args.weights == "tiled", fused_finalize=args.fused_finalize)
     del inp["w_gu"], inp["w_d"]
     torch.cuda.empty_cache()
     x, logits = inp["x"], inp["logits"]
@@ -360,6 +360,8 @@ def run_ours(args, w):
         **{k: rec[k] for k in ("tflops", "hbm_gbs", "layer_roofline_frac", "kernels_ms", "ms_per_step_with_events",
                                "roofline", "roofline_down", "e2e", "clocks")},
         "prepare": "fused (one launch)" if layer.fused_prepare else "separate (route, quantise, permute)",
+        "finalize": "fused into the down GEMM (float32 atomics) + conversion" if layer.fused_finalize else
+                    "separate gather-reduce in slot order",
         "gemm_plans": {g: [{"tiles": tile_name(B.gemm_tile_choice(w.E, n, w.T * w.k, t)), "expert_rows": list(r)}
                            for t, r in plan]
                        for g, n, plan in (("gate_up", 2 * w.I, layer.plan()[0]), ("down", w.H, layer.plan()[1]))},
@@ -605,6 +607,8 @@ def main():
                     help="expert weight layout of the grouped GEMMs (tiled: each 128 x 128-byte box contiguous)")
     ap.add_argument("--static-schedule", action="store_true",
                     help="grouped GEMMs on static tile stripes instead of the dynamic tile counter")
+    ap.add_argument("--fused-finalize", action="store_true",
+                    help="finalize fused into the down GEMM (float32 atomics; the sum order is not fixed)")
     ap.add_argument("--separate-prepare", action="store_true",
                     help="route, quantise and permute as separate calls instead of moe_prepare")
     args = ap.parse_args()

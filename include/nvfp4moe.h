@@ -76,6 +76,7 @@ extern "C" {
 #define NVFP4MOE_EPI_SWIGLU_NVFP4   1  /* h = silu(gate) * up, requantised to NVFP4 */
 #define NVFP4MOE_EPI_SWIGLU_F32     2  /* h = silu(gate) * up as float32 (unfused check) */
 #define NVFP4MOE_EPI_SWIGLU_MXFP4   3  /* h = silu(gate) * up, requantised to MXFP4 (MXFP4 GEMM only) */
+#define NVFP4MOE_EPI_FINALIZE_F32   4  /* out_f32[t] += w * bf16(acc) (moe_grouped_gemm_nvfp4_finalize only) */
 
 /* Grouped GEMM tile_n values for token-major tiles (see moe_grouped_gemm_nvfp4). */
 #define NVFP4MOE_TILE_TOKEN_MAJOR   (-1)
@@ -402,6 +403,31 @@ int moe_grouped_gemm_nvfp4_range(const uint8_t* a_packed, const uint8_t* a_scale
                                  void* c_out, uint8_t* c_scales, int tile_n, int w_layout,
                                  int32_t min_rows, int32_t max_rows,
                                  void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* a5 with a6 fused into its epilogue (page C, Context: the grouped GEMM's
+ * finalize epilogue; page A, section 6: token reordering with a fused
+ * reduction).  The down projection of every valid row r of the experts in
+ * [min_rows, max_rows) is rounded to bf16 as in NVFP4MOE_EPI_BF16 (Y), then
+ * topk_w[f] * Y[r] is added into out_f32[f / k] with f = perm_to_flat[r]
+ * by float32 atomic adds; nothing is written to a [rows, N] buffer.  The
+ * order of the k additions into a token's row is not fixed, so unlike
+ * moe_finalize the float32 sum is not bit-reproducible from call to call
+ * (the difference is float32 rounding).  out_f32: device float32 [T, N],
+ * zero before the call (moe_finalize_f32 converts it to bf16 and zeroes it
+ * again).  perm_to_flat [rows_capacity] and topk_w [T, k] as written by
+ * moe_permute / moe_route_topk.  Other arguments as moe_grouped_gemm_nvfp4_range
+ * with epilogue NVFP4MOE_EPI_FINALIZE_F32. */
+int moe_grouped_gemm_nvfp4_finalize(const uint8_t* a_packed, const uint8_t* a_scales, const float* a_gscale,
+                                    const int32_t* expert_counts, const int32_t* row_offsets,
+                                    int E, int64_t rows_capacity, int64_t m_total,
+                                    const uint8_t* w_packed, const uint8_t* w_scales, const float* w_gscale,
+                                    int N, int K, const int32_t* perm_to_flat, const float* topk_w, int T, int k,
+                                    float* out_f32, int tile_n, int w_layout, int32_t min_rows, int32_t max_rows,
+                                    void* ws, size_t ws_bytes, cudaStream_t stream);
+/* out_bf16 [T, H] = bf16(acc_f32 [T, H]) (round to nearest even), and
+ * acc_f32 = 0 afterwards, ready for the next moe_grouped_gemm_nvfp4_finalize.
+ * H % 8 == 0; both device pointers 16-byte aligned. */
+int moe_finalize_f32(float* acc_f32, int T, int H, void* out_bf16, cudaStream_t stream);
 
 /* ---- MXFP4 variant of a2, a3, a4/a5 -----------------------------------------
  * MXFP4 (page A, sections 2-4: the MXFP4 grouped GEMM that works with

@@ -31,7 +31,7 @@ ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_SMEM, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT
 SCORE = {"softmax": 0, "sigmoid": 1}
 QUANT_COMPUTE_GLOBAL = 1
 QUANT_SCALES_BLOCKED = 2
-EPI_BF16, EPI_SWIGLU_NVFP4, EPI_SWIGLU_F32, EPI_SWIGLU_MXFP4 = 0, 1, 2, 3
+EPI_BF16, EPI_SWIGLU_NVFP4, EPI_SWIGLU_F32, EPI_SWIGLU_MXFP4, EPI_FINALIZE_F32 = 0, 1, 2, 3, 4
 TILE_TOKEN_MAJOR = -1  # grouped GEMM tile_n: 128 tokens as M, two weight tiles as one N = 256 operand
 TILE_TOKEN_MAJOR_PAIR = -2  # the same on a pair of SMs: 256 tokens as M (cta_group::2 MMAs)
 W_ROWMAJOR, W_TILED = 0, 1  # grouped GEMM weight layouts
@@ -77,6 +77,9 @@ _SIGS = {
     "moe_grouped_gemm_nvfp4_range": (_i, [_p, _p, _p, _p, _p, _i, _i64, _i64, _p, _p, _p, _i, _i, _i, _p, _p, _p,
                                           _i, _i, ctypes.c_int32, ctypes.c_int32, _p, _sz, _p]),
     "moe_finalize": (_i, [_p, _p, _p, _i, _i, _i, _i64, _p, _p]),
+    "moe_grouped_gemm_nvfp4_finalize": (_i, [_p, _p, _p, _p, _p, _i, _i64, _i64, _p, _p, _p, _i, _i, _p, _p, _i, _i,
+                                             _p, _i, _i, ctypes.c_int32, ctypes.c_int32, _p, _sz, _p]),
+    "moe_finalize_f32": (_i, [_p, _i, _i, _p, _p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -606,6 +609,49 @@ def moe_grouped_gemm_mxfp4(a_packed, a_scales, counts, row_offsets, w_packed, w_
     return (out, out_scales) if epilogue == EPI_SWIGLU_MXFP4 else out
 
 
+def moe_grouped_gemm_nvfp4_finalize(a_packed, a_scales, a_gscale, counts, row_offsets, w_packed, w_scales, w_gscale,
+                                    perm_to_flat, topk_w, out_f32, m_total=None, tile_n=0, workspace=None,
+                                    rows=ALL_ROWS):
+    """Down projection with the finalize fused into its epilogue: adds
+    topk_w[f] * bf16(Y[r]) into out_f32[f // k] (float32 atomics, so the
+    order of a token's k additions is not fixed).  out_f32 [T, N] must be
+    zero (moe_finalize_f32 leaves it so).  Returns out_f32."""
+    if m_total is None:
+        raise ValueError("m_total (the routed rows, T*k) is required: it chooses the tile orientation")
+    E, N, K, w_ptr, w_layout = _weights_args(w_packed)
+    cap = a_packed.shape[0]
+    T, k = topk_w.shape
+    _need(a_packed, torch.uint8, (cap, K // 2), "a_packed")
+    _need(a_scales, torch.uint8, name="a_scales")
+    _need(a_gscale, torch.float32, (1,), "a_gscale")
+    _need(counts, torch.int32, (E,), "counts")
+    _need(row_offsets, torch.int32, (E + 1,), "row_offsets")
+    _need(w_scales, torch.uint8, name="w_scales")
+    _need(w_gscale, torch.float32, (E,), "w_gscale")
+    _need(perm_to_flat, torch.int32, (cap,), "perm_to_flat")
+    _need(topk_w, torch.float32, name="topk_w")
+    _need(out_f32, torch.float32, (T, N), "out_f32")
+    ws_p, ws_n = _ws_args(workspace)
+    _check(_lib.moe_grouped_gemm_nvfp4_finalize(_ptr(a_packed), _ptr(a_scales), _ptr(a_gscale), _ptr(counts),
+                                                _ptr(row_offsets), E, cap, int(m_total), w_ptr, _ptr(w_scales),
+                                                _ptr(w_gscale), N, K, _ptr(perm_to_flat), _ptr(topk_w), T, k,
+                                                _ptr(out_f32), int(tile_n), w_layout, int(rows[0]), int(rows[1]),
+                                                ws_p, ws_n, _stream()),
+           "moe_grouped_gemm_nvfp4_finalize")
+    return out_f32
+
+
+def moe_finalize_f32(acc_f32, out=None):
+    """out = bf16(acc_f32), and acc_f32 zeroed for the next fused finalize."""
+    _need(acc_f32, torch.float32, name="acc_f32")
+    T, H = acc_f32.shape
+    if out is None:
+        out = _empty((T, H), torch.bfloat16, acc_f32.device)
+    _need(out, torch.bfloat16, (T, H), "out")
+    _check(_lib.moe_finalize_f32(_ptr(acc_f32), T, H, _ptr(out), _stream()), "moe_finalize_f32")
+    return out
+
+
 # ---- a6 ------------------------------------------------------------------------
 def moe_finalize(y, flat_to_perm, topk_w, out=None):
     _need(y, torch.bfloat16, name="y")
@@ -644,7 +690,7 @@ class MoELayer:
 
     def __init__(self, w_gu, w_d, k, score_fn="sigmoid", renormalize=True, h_scale=2.0 ** -4, bias=None,
                  T=None, tile_n=(0, 0), fused_prepare=True, k_primary=None, fmt="nvfp4", dynamic_schedule=True,
-                 tiled_weights=True, autotune=True):
+                 tiled_weights=True, autotune=True, fused_finalize=False):
         if fmt not in ("nvfp4", "mxfp4"):
             raise ValueError(f"fmt {fmt}")
         self.fmt = fmt
@@ -659,6 +705,13 @@ class MoELayer:
         self.device = w_gu.device
         self.bias = bias
         self.tile_n = tuple(tile_n)
+        # Finalize fused into the down GEMM (NVFP4): float32 atomics into a
+        # zeroed [T, H] accumulator, then one conversion kernel; the order of a
+        # token's k additions is not fixed, so the output is not
+        # bit-reproducible.  Off by default.
+        if fused_finalize and fmt != "nvfp4":
+            raise ValueError("the fused finalize is built for NVFP4 layers")
+        self.fused_finalize = bool(fused_finalize)
         self.autotune_enabled = bool(autotune) and self.tile_n == (0, 0)
         self.plans = {}          # batch size -> (gate/up plan, down plan), from autotune()
         if fmt == "mxfp4":
@@ -695,7 +748,8 @@ class MoELayer:
         cap = self.perm.rows_capacity
         self.hq = _empty((cap, I // 2), torch.uint8, dev)
         self.hs = _empty((blocked_scales_bytes(cap, I, self.fmt),), torch.uint8, dev)
-        self.y = _empty((cap, H), torch.bfloat16, dev)
+        self.y = None if self.fused_finalize else _empty((cap, H), torch.bfloat16, dev)
+        self.acc = torch.zeros((T, H), dtype=torch.float32, device=dev) if self.fused_finalize else None
         self.out = _empty((T, H), torch.bfloat16, dev)
 
     # ---- the steps of forward() (bench.py times them one by one) ----
@@ -739,6 +793,10 @@ class MoELayer:
                                        self.w_gu_packed, self.w_gu_scales, self.w_gu_gscale, EPI_SWIGLU_NVFP4,
                                        c_gscale=self.h_scale, m_total=m_total, tile_n=tile_n, out=self.hq,
                                        out_scales=self.hs, workspace=self.g_ws, rows=rows)
+        elif self.fused_finalize:
+            moe_grouped_gemm_nvfp4_finalize(self.hq, self.hs, self.h_scale, p.counts, p.row_offsets, self.w_d_packed,
+                                            self.w_d_scales, self.w_d_gscale, p.perm_to_flat, self.topk_w, self.acc,
+                                            m_total=m_total, tile_n=tile_n, workspace=self.g_ws, rows=rows)
         elif self.fmt == "mxfp4":
             moe_grouped_gemm_mxfp4(self.hq, self.hs, p.counts, p.row_offsets, self.w_d_packed, self.w_d_scales,
                                    EPI_BF16, m_total=m_total, tile_n=tile_n, out=self.y, workspace=self.g_ws,
@@ -759,7 +817,10 @@ class MoELayer:
             self._gemm("down", tile_n, rows)
 
     def finalize(self, out=None):
-        """a6: the router-weighted sum back to token order."""
+        """a6: the router-weighted sum back to token order (fused finalize:
+        the conversion of the float32 accumulator, which it zeroes)."""
+        if self.fused_finalize:
+            return moe_finalize_f32(self.acc, out=self.out if out is None else out)
         return moe_finalize(self.y, self.perm.flat_to_perm, self.topk_w, out=self.out if out is None else out)
 
     def forward(self, x, logits, out=None):
@@ -823,6 +884,8 @@ class MoELayer:
                 run(best[0])             # the down GEMM's input, from the chosen plan
             chosen.append(best[0])
             report[which] = best
+        if self.fused_finalize:
+            self.acc.zero_()         # the timed down GEMMs added into the accumulator
         sync_status()
         self.plans[T] = tuple(chosen)
         return report

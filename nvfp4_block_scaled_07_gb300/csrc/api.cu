@@ -483,7 +483,9 @@ static int grouped_gemm_common(bool mx, const uint8_t* a_packed, const uint8_t* 
                                int64_t m_total, const uint8_t* w_packed, const uint8_t* w_scales,
                                const float* w_gscale, int N, int K, int epilogue, const float* c_gscale, void* c_out,
                                uint8_t* c_scales, int tile_n, int w_layout, int32_t min_rows,
-                               int32_t max_rows, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                               int32_t max_rows, void* ws, size_t ws_bytes, cudaStream_t stream,
+                               const int32_t* perm_to_flat = nullptr, const float* topk_w = nullptr, int T = 0,
+                               int k = 0) {
   t_detail[0] = 0;
   NVFP4MOE_REQUIRE(min_rows >= 1 && min_rows <= max_rows, NVFP4MOE_ERR_INVALID_ARG,
                    "expert row range [%d, %d) must have 1 <= min_rows <= max_rows", min_rows, max_rows);
@@ -493,13 +495,17 @@ static int grouped_gemm_common(bool mx, const uint8_t* a_packed, const uint8_t* 
                    NVFP4MOE_ERR_WORKSPACE, "workspace must be NULL or %zu bytes, 256-byte aligned (got %zu)",
                    kGemmWorkspaceBytes, ws_bytes);
   const int requant = mx ? NVFP4MOE_EPI_SWIGLU_MXFP4 : NVFP4MOE_EPI_SWIGLU_NVFP4;
-  NVFP4MOE_REQUIRE(epilogue == NVFP4MOE_EPI_BF16 || epilogue == requant || epilogue == NVFP4MOE_EPI_SWIGLU_F32,
+  const bool fin = epilogue == NVFP4MOE_EPI_FINALIZE_F32;
+  NVFP4MOE_REQUIRE(epilogue == NVFP4MOE_EPI_BF16 || epilogue == requant || epilogue == NVFP4MOE_EPI_SWIGLU_F32 ||
+                       (fin && !mx && perm_to_flat),
                    NVFP4MOE_ERR_INVALID_ARG, "epilogue %d", epilogue);
+  NVFP4MOE_REQUIRE(!fin || (topk_w && T >= 0 && k >= 1 && int64_t(T) * k <= rows_capacity), NVFP4MOE_ERR_INVALID_ARG,
+                   "fused finalize needs perm_to_flat, topk_w, T >= 0 and 1 <= k with T*k <= rows_capacity");
   NVFP4MOE_REQUIRE(E >= 1 && E <= 1024, NVFP4MOE_ERR_UNSUPPORTED, "E = %d outside [1, 1024]", E);
   const int kq = mx ? 128 : 64;
   NVFP4MOE_REQUIRE(K >= kq && K % kq == 0, NVFP4MOE_ERR_UNSUPPORTED, "K = %d must be a positive multiple of %d", K,
                    kq);
-  const bool swiglu = epilogue != NVFP4MOE_EPI_BF16;
+  const bool swiglu = epilogue != NVFP4MOE_EPI_BF16 && !fin;
   NVFP4MOE_REQUIRE(N > 0 && N % (swiglu ? 256 : 128) == 0, NVFP4MOE_ERR_UNSUPPORTED,
                    "N = %d must be a multiple of %d for this epilogue", N, swiglu ? 256 : 128);
   NVFP4MOE_REQUIRE(int64_t(E) * N < (int64_t(1) << 31), NVFP4MOE_ERR_UNSUPPORTED, "E*N too large");
@@ -550,6 +556,9 @@ static int grouped_gemm_common(bool mx, const uint8_t* a_packed, const uint8_t* 
   a.sched = ws;
   a.min_rows = min_rows;
   a.max_rows = max_rows;
+  a.perm_to_flat = perm_to_flat;
+  a.topk_w = topk_w;
+  a.k = k;
   return launch_grouped_gemm(a, d.num_sms, d.smem_optin, stream);  // detail already set on failure
 }
 
@@ -584,6 +593,30 @@ int moe_grouped_gemm_mxfp4(const uint8_t* a_packed, const uint8_t* a_scales, con
   return grouped_gemm_common(true, a_packed, a_scales, nullptr, expert_counts, row_offsets, E, rows_capacity, m_total,
                              w_packed, w_scales, nullptr, N, K, epilogue, nullptr, c_out, c_scales, tile_n, w_layout,
                              1, INT32_MAX, ws, ws_bytes, stream);
+}
+
+int moe_grouped_gemm_nvfp4_finalize(const uint8_t* a_packed, const uint8_t* a_scales, const float* a_gscale,
+                                    const int32_t* expert_counts, const int32_t* row_offsets, int E,
+                                    int64_t rows_capacity, int64_t m_total, const uint8_t* w_packed,
+                                    const uint8_t* w_scales, const float* w_gscale, int N, int K,
+                                    const int32_t* perm_to_flat, const float* topk_w, int T, int k, float* out_f32,
+                                    int tile_n, int w_layout, int32_t min_rows, int32_t max_rows, void* ws,
+                                    size_t ws_bytes, cudaStream_t stream) {
+  return grouped_gemm_common(false, a_packed, a_scales, a_gscale, expert_counts, row_offsets, E, rows_capacity,
+                             m_total, w_packed, w_scales, w_gscale, N, K, NVFP4MOE_EPI_FINALIZE_F32, nullptr, out_f32,
+                             nullptr, tile_n, w_layout, min_rows, max_rows, ws, ws_bytes, stream, perm_to_flat, topk_w,
+                             T, k);
+}
+
+int moe_finalize_f32(float* acc_f32, int T, int H, void* out_bf16, cudaStream_t stream) {
+  t_detail[0] = 0;
+  NVFP4MOE_REQUIRE(T >= 0 && H > 0 && H % 8 == 0, NVFP4MOE_ERR_INVALID_ARG, "T %d H %d (H %% 8 == 0)", T, H);
+  NVFP4MOE_REQUIRE(T == 0 || (acc_f32 && out_bf16 && aligned16(acc_f32) && aligned16(out_bf16)),
+                   NVFP4MOE_ERR_INVALID_ARG, "null or misaligned pointer");
+  DeviceInfo d;
+  if (int st = current_device(&d)) return st;
+  return cuda_status(launch_finalize_f32(acc_f32, int64_t(T) * H, out_bf16, d.num_sms, stream),
+                     "finalize_f32 launch");
 }
 
 int moe_grouped_gemm_mxfp4_range(const uint8_t* a_packed, const uint8_t* a_scales, const int32_t* expert_counts,

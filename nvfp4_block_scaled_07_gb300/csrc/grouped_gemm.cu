@@ -132,6 +132,9 @@ struct Params {
   int batch2;        // token-major: the MMA thread waits for and issues two stages at a time
   int w_policy;      // L2 policy of weight copies: 0 evict_first, 1 evict_normal, 2 evict_last
   int32_t min_rows, max_rows;  // experts outside [min_rows, max_rows) get no tiles in this launch
+  const int32_t* perm_to_flat;  // NVFP4MOE_EPI_FINALIZE_F32: row -> flat id t * k + j
+  const float* topk_w;          // ... and the routing weights [T, k]
+  int k;
 };
 
 // Shared state of the bounded waits of one CTA: the abort flag every role
@@ -446,7 +449,7 @@ __device__ __forceinline__ void requant_row32_mx(const uint32_t (&h)[32], int64_
   *reinterpret_cast<uint4*>(out_codes + row * (n_out / 2) + f0 / 2) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
 }
 
-template <int BN, int NA, bool SWIGLU, bool MX, bool TM, bool PAIR = false>
+template <int BN, int NA, bool SWIGLU, bool MX, bool TM, bool PAIR = false, bool FIN = false>
 __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_sf,
@@ -454,6 +457,10 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
   using C = Cfg<BN, NA, SWIGLU>;
   static_assert(!TM || (BN == 128 && NA == 2), "token-major tiles: 128 tokens x two 128-row weight tiles");
   static_assert(!PAIR || TM, "CTA pairs run token-major tiles");
+  // FIN: the bf16 epilogue adds each row, times its routing weight, into its
+  // token's float32 row (NVFP4MOE_EPI_FINALIZE_F32); its own instantiation,
+  // so the plain bf16 kernels keep their register allocation.
+  static_assert(!FIN || (!SWIGLU && !MX), "the fused finalize follows the NVFP4 down projection");
   // CTA pair (cluster of two, cta_group::2 MMAs): a tile is 256 tokens, 128
   // in each CTA, against the stage's two weight tiles, one in each CTA's
   // shared memory; CTA 0 of the pair issues the MMAs for both.
@@ -1086,6 +1093,25 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
               }
           }
           release();
+          if constexpr (FIN) {
+            // fused finalize: this thread's token row, times its routing
+            // weight, added into the token's float32 row
+            if (row_ok) {
+              const int fl = __ldg(p.perm_to_flat + row);
+              const float wt = __ldg(p.topk_w + fl);
+              float* dst = static_cast<float*>(p.c_out) + int64_t(fl / p.k) * n_out + mb * (C::NA * kBM);
+#pragma unroll
+              for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+                for (int i = 0; i < 16; i += 2) {
+                  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[c][i]));
+                  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[c][i + 1]));
+                  ptx::red_add_v4(dst + 32 * c + 2 * i, wt * a.x, wt * a.y, wt * b.x, wt * b.y);
+                }
+            }
+            slots.done(s0, s1);
+            continue;
+          }
           const bool quarter_full = q * 32 + 32 <= valid;
           const uint32_t obuf = out_base + uint32_t(q * kOutChunkBytes);
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.c_out) + row * n_out + mb * (C::NA * kBM);
@@ -1160,21 +1186,31 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
           }
         }
       } else {
+        // NVFP4MOE_EPI_FINALIZE_F32: each row's bf16 values, times the
+        // row's routing weight, are added into its token's float32 row.
+        constexpr bool scatter = FIN;
         for (int c0 = 32 * part; c0 < valid; c0 += 32 * kParts) {
-          uint32_t g[32];
-          ptx::tmem_ld_32x32b_x32(tbase + c0, g);
-          ptx::tmem_ld_wait();
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.c_out);
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c0 + i < valid) out[(row0 + c0 + i) * n_out + f] = __float2bfloat16_rn(__uint_as_float(g[i]) * scale);
-          if constexpr (NA == 2) {  // the second 128-row block of the tile
-            ptx::tmem_ld_32x32b_x32(tbase + w + c0, g);
+          for (int j = 0; j < NA; ++j) {  // NA consecutive 128-row blocks of the tile
+            uint32_t g[32];
+            ptx::tmem_ld_32x32b_x32(tbase + j * w + c0, g);
             ptx::tmem_ld_wait();
+            const int col = f + j * kBM;
+            if constexpr (scatter) {
+              float* acc = static_cast<float*>(p.c_out);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (c0 + i < valid)
-                out[(row0 + c0 + i) * n_out + f + kBM] = __float2bfloat16_rn(__uint_as_float(g[i]) * scale);
+              for (int i = 0; i < 32; ++i)
+                if (c0 + i < valid) {
+                  const int fl = __ldg(p.perm_to_flat + row0 + c0 + i);
+                  const float y = __bfloat162float(__float2bfloat16_rn(__uint_as_float(g[i]) * scale));
+                  atomicAdd(acc + int64_t(fl / p.k) * n_out + col, __ldg(p.topk_w + fl) * y);
+                }
+            } else {
+              __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.c_out);
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (c0 + i < valid) out[(row0 + c0 + i) * n_out + col] = __float2bfloat16_rn(__uint_as_float(g[i]) * scale);
+            }
           }
         }
         release();
@@ -1447,7 +1483,7 @@ int tm_batch_from_env() {
   return b;
 }
 
-template <int BN, int NA, bool SWIGLU, bool MX, bool TM = false, bool PAIR = false>
+template <int BN, int NA, bool SWIGLU, bool MX, bool TM = false, bool PAIR = false, bool FIN = false>
 int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st) {
   using C = Cfg<BN, NA, SWIGLU>;
   // The whole opt-in shared memory is requested; the kernel sizes its stages
@@ -1468,12 +1504,13 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   if (!encode_weight_map(&tw, a, SWIGLU, PAIR ? 1 : (SWIGLU ? 2 : NA)) || !encode_weight_scale_map(&tsf, a, SWIGLU, NA) ||
       !encode_token_scale_map(&tasf, a) ||
       !encode_kmajor_map(&ta, a.a_packed, a.rows_capacity, a.K / 2, TM ? kBM : 32) ||
-      !(out_stage_bytes(SWIGLU, TM) ? encode_bf16_store_map(&tc, a.c_out, a.rows_capacity, a.N)
-                                    : encode_kmajor_map(&tc, a.a_packed, a.rows_capacity, a.K / 2, 32))) {
+      !(out_stage_bytes(SWIGLU, TM) && a.epilogue != NVFP4MOE_EPI_FINALIZE_F32
+            ? encode_bf16_store_map(&tc, a.c_out, a.rows_capacity, a.N)
+            : encode_kmajor_map(&tc, a.a_packed, a.rows_capacity, a.K / 2, 32))) {
     set_error_detail("cuTensorMapEncodeTiled failed or is unavailable");
     return NVFP4MOE_ERR_CUDA;
   }
-  auto kernel = grouped_gemm_kernel<BN, NA, SWIGLU, MX, TM, PAIR>;
+  auto kernel = grouped_gemm_kernel<BN, NA, SWIGLU, MX, TM, PAIR, FIN>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (err != cudaSuccess) {
     set_error_detail("cudaFuncSetAttribute: %s", cudaGetErrorString(err));
@@ -1503,6 +1540,9 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   p.batch2 = tm_batch_from_env();
   p.min_rows = a.min_rows;
   p.max_rows = a.max_rows;
+  p.perm_to_flat = a.perm_to_flat;
+  p.topk_w = a.topk_w;
+  p.k = a.k;
   // Pair tiles serve experts with many rows: every weight tile is re-read by
   // each of the expert's token tiles, so the weights stay in L2 (evict_last;
   // measured at 2048 rows per expert: gate/up 2.76 -> 2.66 ms, down 1.58 ->
@@ -1551,13 +1591,25 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
 
 template <bool MX>
 int launch_format(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st) {
-  const bool swiglu = a.epilogue != NVFP4MOE_EPI_BF16;
+  const bool swiglu = a.epilogue != NVFP4MOE_EPI_BF16 && a.epilogue != NVFP4MOE_EPI_FINALIZE_F32;
   const int bn = a.tile_n == 0 ? 128 : a.tile_n;
   // Two 128-row weight tiles per stage whenever N allows: each stage carries
   // twice the weight bytes and two accumulation chains, and every token tile
   // loaded serves 256 output features (measured: the down GEMM at decode
   // 0.48 -> 0.30 ms, at 2048 rows per expert 4.02 -> 2.78 ms).
   const bool pair = a.N % (2 * kBM) == 0;
+  if constexpr (!MX) {
+    if (a.epilogue == NVFP4MOE_EPI_FINALIZE_F32) {
+      if (a.tile_n == NVFP4MOE_TILE_TOKEN_MAJOR_PAIR && pair)
+        return launch_impl<128, 2, false, false, true, true, true>(a, num_sms, smem_optin, st);
+      if (a.tile_n == NVFP4MOE_TILE_TOKEN_MAJOR && pair)
+        return launch_impl<128, 2, false, false, true, false, true>(a, num_sms, smem_optin, st);
+      if (bn == 128 && pair) return launch_impl<128, 2, false, false, false, false, true>(a, num_sms, smem_optin, st);
+      if (bn == 128) return launch_impl<128, 1, false, false, false, false, true>(a, num_sms, smem_optin, st);
+      set_error_detail("tile_n %d is not supported with the fused finalize", a.tile_n);
+      return NVFP4MOE_ERR_UNSUPPORTED;
+    }
+  }
   if (a.tile_n == NVFP4MOE_TILE_TOKEN_MAJOR_PAIR && pair) {
     if (swiglu) return launch_impl<128, 2, true, MX, true, true>(a, num_sms, smem_optin, st);
     return launch_impl<128, 2, false, MX, true, true>(a, num_sms, smem_optin, st);

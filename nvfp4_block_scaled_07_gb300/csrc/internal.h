@@ -91,6 +91,7 @@ cudaError_t launch_prepare(const float* logits, const float* bias, const void* x
 
 cudaError_t launch_finalize(const void* y, const int32_t* flat_to_perm, const float* w, int T, int k, int H,
                             int64_t rows_capacity, void* out, cudaStream_t st);
+cudaError_t launch_finalize_f32(float* acc, int64_t n, void* out, int num_sms, cudaStream_t st);
 
 // Reads and clears the sticky device flags of the kernels in kernels_prep.cu.
 cudaError_t prep_read_and_clear_flags(unsigned* flags);
@@ -116,6 +117,11 @@ struct GemmArgs {
   bool w_tiled;  // w_packed in the tiled layout (NVFP4MOE_W_TILED)
   void* sched;  // zero-filled 256-byte tile-scheduler workspace, or null for the static schedule
   int32_t min_rows, max_rows;  // experts outside [min_rows, max_rows) get no tiles
+  // NVFP4MOE_EPI_FINALIZE_F32: c_out is float32 [T, N]; row r adds
+  // topk_w[f] * bf16(acc) into row f / k, f = perm_to_flat[r]
+  const int32_t* perm_to_flat;
+  const float* topk_w;
+  int k;
 };
 
 constexpr size_t kGemmWorkspaceBytes = 256;

@@ -1157,6 +1157,32 @@ cudaError_t launch_prepare(const float* logits, const float* bias, const void* x
 #undef NVFP4MOE_PREP
 }
 
+namespace {
+// Float32 accumulator of the fused finalize -> bf16 output, leaving the
+// accumulator zeroed; one thread per 8 values.
+__global__ void __launch_bounds__(256) finalize_f32_kernel(float4* __restrict__ acc, int64_t n8, uint4* __restrict__ out) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += int64_t(gridDim.x) * blockDim.x) {
+    const float4 a = acc[2 * i], b = acc[2 * i + 1];
+    const __nv_bfloat162 v0 = __floats2bfloat162_rn(a.x, a.y), v1 = __floats2bfloat162_rn(a.z, a.w);
+    const __nv_bfloat162 v2 = __floats2bfloat162_rn(b.x, b.y), v3 = __floats2bfloat162_rn(b.z, b.w);
+    out[i] = make_uint4(*reinterpret_cast<const uint32_t*>(&v0), *reinterpret_cast<const uint32_t*>(&v1),
+                        *reinterpret_cast<const uint32_t*>(&v2), *reinterpret_cast<const uint32_t*>(&v3));
+    acc[2 * i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    acc[2 * i + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+}  // namespace
+
+cudaError_t launch_finalize_f32(float* acc, int64_t n, void* out, int num_sms, cudaStream_t st) {
+  const int64_t n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
+  const int64_t want = (n8 + 255) / 256, cap = int64_t(num_sms) * 8;
+  return launch_kernel(finalize_f32_kernel, dim3(unsigned(want < cap ? want : cap)), dim3(256), 0, st, false,
+                       reinterpret_cast<float4*>(acc), n8, static_cast<uint4*>(out));
+}
+
 cudaError_t launch_finalize(const void* y, const int32_t* flat_to_perm, const float* w, int T, int k, int H,
                             int64_t rows_capacity, void* out, cudaStream_t st) {
   if (T == 0) return cudaSuccess;

@@ -81,6 +81,11 @@ __device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Vector float32 reduction (atomic add without a result) into global memory.
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
 // ---- per-warpgroup register budgets --------------------------------------------
 // Executed by all threads of a warpgroup: lower (dec) or raise (inc) the
 // per-thread register count of the warpgroup; inc waits until other
