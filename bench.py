@@ -202,25 +202,6 @@ def bench_config(w, fmt, k_primary, n_active, world):
             "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
-def read_stream_gbs(dev, gib=4, reps=5):
-    """HBM read bandwidth of a plain read-only stream (a sum over `gib` GiB,
-    best of `reps`, CUDA events): the ceiling of a kernel that only reads,
-    beside the copy rate of MEASURED_PEAKS.json (which reads and writes)."""
-    buf = torch.ones(gib << 29, dtype=torch.bfloat16, device=dev)
-    best = float("inf")
-    for _ in range(reps + 1):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        buf.sum(dtype=torch.float32)
-        e1.record()
-        torch.cuda.synchronize()
-        best = min(best, e0.elapsed_time(e1))
-    n = buf.numel() * buf.element_size()
-    del buf
-    torch.cuda.empty_cache()
-    return n / (best * 1e-3) / 1e9
-
-
 def measure_layer(args, w, world, rank, with_e2e=True):
     """Times the layer of workload `w` on this rank's GPU: the device-timed
     steps, per-kernel event times, the end-to-end steps with host buffers
@@ -378,10 +359,6 @@ def run_ours(args, w):
         w2 = {**W.WORKLOADS, **W.PROFILE_WORKLOADS}[args.secondary]
         rec2, layer2, inp2 = measure_layer(args, w2, world, rank)
         launches += rec2.pop("gpu_launches")
-        rec2["read_stream_gbs"] = round(max_over_ranks(read_stream_gbs(torch.device("cuda")), world), 1) \
-            if rec2["roofline"]["bound"] == "hbm" else None
-        if rec2["read_stream_gbs"]:
-            rec2["roofline"]["frac_of_read_stream"] = round(rec2["roofline"]["achieved"] / rec2["read_stream_gbs"], 4)
         res["secondary"] = {"workload": w2.name, "unit": "tokens/s", **rec2}
         del layer2, inp2
         torch.cuda.empty_cache()
