@@ -503,15 +503,25 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
   auto tqe_bar = [&](uint32_t q) {
     return bar0 + 8u * (uint32_t(2 * kMaxStages + 5 + 2 * kMaxSfSlots + kTileRing) + q);
   };
-  // the scale blocks of stage s, copied ahead of its operands
+  // the scale blocks of stage s (token-major: of scale ring slot s), copied ahead of its operands
   auto sfc_bar = [&](uint32_t s) {
     return bar0 + 8u * (uint32_t(2 * kMaxStages + 5 + 2 * kMaxSfSlots + 2 * kTileRing) + s);
   };
 
   const int MT = SWIGLU ? p.N / 2 / kBM : p.N / (kBM * NA);  // M tiles per expert
+  // Single-CTA token-major kernels keep the scale blocks out of the operand
+  // stages, in a deeper shared-memory ring of their own that a second
+  // producer thread (lane 0 of warp 2) fills ahead of the operands, and the
+  // scale-factor warps move a slot into tensor memory as soon as the MMAs of
+  // the stage's previous use are done (measured on GB300: skewed_t2048 0.711
+  // -> 0.676 ms per layer).  Pair tiles keep them in the stage: with the
+  // ring, their copy pipeline alone ran faster (gate/up without MMAs 2.38 ->
+  // 1.87 ms at prefill) but the whole kernel slower (2.63 -> 2.76 ms).
+  constexpr bool kRing = TM && !PAIR;
+  constexpr int nprod = kRing ? 2 : 1;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
-      // producer's expect_tx, plus (tied scale slots) one arrival per scale-factor warp of each CTA
+      // the producer's expect_tx, plus (tied scale slots) one arrival per scale-factor warp of each CTA
       ptx::mbar_init(full_bar(s), kTied ? 1 + (PAIR ? 8 : 4) : 1);
       ptx::mbar_init(empty_bar(s), 1);
       ptx::mbar_init(sfc_bar(s), 1);
@@ -523,11 +533,12 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
     ptx::mbar_init(drain_bar, 1);
     for (int r = 0; r < kMaxSfSlots; ++r) {
       ptx::mbar_init(sff_bar(r), PAIR ? 8 : 4);  // one arrival per scale-factor warp (of both CTAs)
-      ptx::mbar_init(sfe_bar(r), 1);  // MMA completion
+      // MMA completion; token-major: the scale ring slot read by this CTA's 4 scale-factor warps
+      ptx::mbar_init(sfe_bar(r), kRing ? 4 : 1);
     }
     for (int q = 0; q < kTileRing; ++q) {
       ptx::mbar_init(tqf_bar(q), 1);
-      ptx::mbar_init(tqe_bar(q), tile_consumers(SWIGLU));
+      ptx::mbar_init(tqe_bar(q), tile_consumers(SWIGLU) + nprod - 1);  // (+ the scale-copy producer)
     }
     abort_flag->abort = 0;
     abort_flag->limit_us = p.wait_us;
@@ -614,14 +625,22 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
   // Stage geometry for this launch: as many stages as fit once the token
   // slot is sized for the widest tile actually present.
   const int wmax = TM ? kBM : *s_wmax;  // token-major: every token tile is 128 rows
-  const int stage = NW * kATile + wmax * kBKBytes + C::NA * kSfTile + (wmax > 128 ? 2 : 1) * kSfTile;
+  // With a scale ring: operand stages hold the weight and token tiles only,
+  // and each slot of the ring the weight tiles' and the token tile's scale
+  // blocks of one K stage (sf_slot bytes); the stages take what the ring's
+  // two slots leave, the ring what the stages leave (at most kMaxSfSlots).
+  // Otherwise the scale blocks ride in the stage.
+  const int sf_slot = (C::NA + (wmax > 128 ? 2 : 1)) * kSfTile;
+  const int stage = NW * kATile + wmax * kBKBytes + (kRing ? 0 : sf_slot);
   const int off_b = NW * kATile;
-  const int off_sfa = off_b + wmax * kBKBytes;
+  const int off_sfa = kRing ? 0 : off_b + wmax * kBKBytes;  // in the stage, or in the ring slot
   const int off_sfb = off_sfa + C::NA * kSfTile;
-  const int S = min(kTied ? C::SfSlots : kMaxStages,
-                    min(p.stage_cap, (p.smem_bytes - ctrl - out_stage_bytes(SWIGLU, TM)) / stage));
+  const int room = p.smem_bytes - ctrl - out_stage_bytes(SWIGLU, TM);
+  const int S = min(kTied ? C::SfSlots : kMaxStages, min(p.stage_cap, (room - (kRing ? 2 * sf_slot : 0)) / stage));
+  const int R = kRing ? min(kMaxSfSlots, (room - S * stage) / sf_slot) : 0;  // scale ring slots
   const uint32_t smem_base = ptx::smem_u32(smem) + uint32_t(ctrl);
-  const uint32_t out_base = smem_base + uint32_t(S * stage);  // token-major bf16 chunk buffers
+  const uint32_t sf_ring = smem_base + uint32_t(S * stage);
+  const uint32_t out_base = sf_ring + uint32_t(R * sf_slot);  // token-major bf16 chunk buffers
 
   // The i-th tile of this CTA: the static stripe blockIdx.x + i * gridDim.x,
   // or (dynamic schedule) the i-th id the producer claimed, read from the
@@ -643,8 +662,11 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
   };
 
   // ---- warp roles (bodies as lambdas; dispatched below) ----
-  auto role_producer = [&]() {
+  auto role_producer = [&](int who) {
     // ---------------- TMA producer ----------------
+    // who: 0 (lane 0 of warp 0) copies the operand stages, and their scale
+    // blocks unless the kernel has a scale ring; 1 (lane 0 of warp 2) fills
+    // the scale ring.
     // weights stream through once at decode; token-major (many rows per
     // expert) re-reads each weight tile for every token tile
     const uint64_t pol_w = p.w_policy == 2   ? ptx::policy_evict_last()
@@ -652,24 +674,33 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
                                              : ptx::policy_evict_first();
     const uint64_t pol_a = ptx::policy_evict_last();   // token tiles are re-read by every M tile
     uint32_t it = 0;          // stages issued (for the drain after an abort)
-    uint32_t s = 0, ph = 0;   // ring position of stage it and its phase parity
+    uint32_t s = 0, ph = 0;   // ring position of stage it and its phase parity (scale ring: who 1)
+    const uint32_t ring = who == 0 ? uint32_t(S) : uint32_t(R);
     bool ok = true;
-    // Dynamic schedule: the next id is claimed one tile ahead, so the atomic's
-    // latency overlaps the current tile's copies.
-    int next = sched ? int(atomicAdd(sched, 1u)) : int(PAIR ? blockIdx.x >> 1 : blockIdx.x);
+    // Dynamic schedule: producer 0 claims the next id one tile ahead, so the
+    // atomic's latency overlaps the current tile's copies; the scale ring's
+    // producer reads the ids from the ring like the other roles.
+    int next = who != 0 ? 0 : sched ? int(atomicAdd(sched, 1u)) : int(PAIR ? blockIdx.x >> 1 : blockIdx.x);
     for (uint32_t i = 0; ok; ++i) {
-      const int t = next;
-      if (sched) {
-        const uint32_t q = i % uint32_t(kTileRing), ph = (i / uint32_t(kTileRing)) & 1u;
-        if (!wait_phase<true>(tqe_bar(q), ph ^ 1u, abort_flag)) {
-          ok = false;
-          break;
+      int t;
+      if (who == 0) {
+        t = next;
+        if (sched) {
+          const uint32_t q = i % uint32_t(kTileRing), ph = (i / uint32_t(kTileRing)) & 1u;
+          if (!wait_phase<true>(tqe_bar(q), ph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          s_tq[q] = t;
+          ptx::mbar_arrive(tqf_bar(q));
         }
-        s_tq[q] = t;
-        ptx::mbar_arrive(tqf_bar(q));
+        if (t >= total) break;
+        next = sched ? int(atomicAdd(sched, 1u)) : t + int(PAIR ? gridDim.x >> 1 : gridDim.x);
+      } else {
+        t = next_tile(i, false);
+        if (t < 0) ok = false;
+        if (t < 0 || t >= total) break;
       }
-      if (t >= total) break;
-      next = sched ? int(atomicAdd(sched, 1u)) : t + int(PAIR ? gridDim.x >> 1 : gridDim.x);
       int e, mb, nb, w;
       decode_tile(t, tiles, TB, e, mb, nb, w);
       if constexpr (TM) w = kBM;
@@ -691,8 +722,25 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
       // advances sf_per_kt 512-byte blocks; the token tile's start at asf.
       const int sc1 = SWIGLU ? mb : e * (p.N / kBM) + mb * NA, sc2 = SWIGLU ? 2 * e : 0;
       const uint8_t* asf = p.a_scales + size_t(arow / kBM) * sf_k * 512;
-      const uint32_t full_bytes = uint32_t(NW * kATile + w * kBKBytes);
+      const uint32_t op_bytes = uint32_t(NW * kATile + w * kBKBytes);
       for (int kt = 0; kt < nkt; ++kt, ++it) {
+        if (who == 1) {
+          // Token-major scale ring: slot s is free once this CTA's
+          // scale-factor warps have read it into registers.  This thread
+          // runs ahead of the operands and waits with try_wait: spinning
+          // here takes issue slots from the epilogue warps on its SM
+          // sub-partition.
+          if (!wait_phase(sfe_bar(s), ph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t slot = sf_ring + s * uint32_t(sf_slot);
+          ptx::mbar_arrive_expect_tx(sfc_bar(s), uint32_t(sf_slot));
+          ptx::tma_load_3d(slot, &tmap_sf, sfc_bar(s), kt * sf_per_kt * 64, sc1, sc2, pol_w);
+          ptx::tma_load_3d(slot + C::NA * kSfTile, &tmap_asf, sfc_bar(s), kt * sf_per_kt * 64, arow / kBM, 0, pol_a);
+          if (++s == ring) s = 0, ph ^= 1u;
+          continue;
+        }
         if (!wait_phase<true>(empty_bar(s), ph ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -706,7 +754,9 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
         const uint32_t sf_bytes = uint32_t((MX ? nkb / 2 : nkb) * 512);
         const size_t sf_off = size_t(kt) * (sf_per_kt * 512);
         // scale boxes are always full (bytes past the scales read as zero)
-        if constexpr (BN == 128) {  // one 128-row token chunk: its scales are a box of the token scale map
+        if constexpr (kRing) {
+          // (the scale ring's producer copies them)
+        } else if constexpr (BN == 128) {  // one 128-row token chunk: its scales are a box of the token scale map
           ptx::mbar_arrive_expect_tx(sfc_bar(s), uint32_t((C::NA + 1) * kSfTile));
           ptx::tma_load_3d(st + off_sfa, &tmap_sf, sfc_bar(s), kt * sf_per_kt * 64, sc1, sc2, pol_w);
           ptx::tma_load_3d(st + off_sfb, &tmap_asf, sfc_bar(s), kt * sf_per_kt * 64, arow / kBM, 0, pol_a);
@@ -721,11 +771,11 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
           // Both CTAs' operands complete on CTA 0's full barrier, which
           // expects the bytes of both.
           const uint32_t fb = ptx::mapa(full_bar(s), 0);
-          if (crank == 0) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * full_bytes);
+          if (crank == 0) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * op_bytes);
           ptx::tma_load_5d_pair(st, &tmap_w, fb, kt * wdx, wc1, wc2 + kt * wdz, wc3, wc4, pol_w);
           ptx::tma_load_2d_pair(st + off_b, &tmap_a, fb, kt * kBKBytes, arow, pol_a);
         } else {
-          ptx::mbar_arrive_expect_tx(full_bar(s), full_bytes);
+          ptx::mbar_arrive_expect_tx(full_bar(s), op_bytes);
           ptx::tma_load_5d(st, &tmap_w, full_bar(s), kt * wdx, wc1, wc2 + kt * wdz, wc3, wc4, pol_w);
           if constexpr (TM) {  // a 128-row token tile: one box (the map's box is 128 rows here)
             ptx::tma_load_2d(st + off_b, &tmap_a, full_bar(s), kt * kBKBytes, arow, pol_a);
@@ -738,15 +788,19 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
       }
     }
     if (!ok) {
-      // Let every copy this thread issued land before the CTA can exit.
-      const uint32_t first = it > uint32_t(S) ? it - uint32_t(S) : 0u;
+      // Let every copy this thread issued land before the CTA can exit: the
+      // scale ring's and (not token-major) the stages' own barriers complete
+      // once the bytes are in.  A token-major stage's full barrier also waits
+      // for the scale-factor warps, and a pair's CTA 1 copies complete on CTA
+      // 0's barriers, which CTA 1 cannot wait on: there, any copy still in
+      // flight gets 1 ms to land.
+      const uint32_t first = it > ring ? it - ring : 0u;
       for (uint32_t i = first; i < it; ++i) {
-        drain_phase(sfc_bar(i % uint32_t(S)), (i / uint32_t(S)) & 1u);
-        if (crank == 0) drain_phase(full_bar(i % uint32_t(S)), (i / uint32_t(S)) & 1u);
+        if (TM && who == 0) break;
+        drain_phase(sfc_bar(i % ring), (i / ring) & 1u);
+        if (!TM && crank == 0) drain_phase(full_bar(i % ring), (i / ring) & 1u);
       }
-      if constexpr (PAIR) {
-        // CTA 1's operand copies complete on CTA 0's barriers, which CTA 1
-        // cannot wait on: give any copy still in flight 1 ms to land.
+      if (TM && who == 0) {
         const uint64_t t0 = ptx::globaltimer_ns();
         while (ptx::globaltimer_ns() - t0 < 1000000ull) {
         }
@@ -917,15 +971,75 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
       for (int kt = 0; kt < nkt; ++kt) {
         // Tied slots: the stage's scale copies are issued only after the MMAs
         // that last read its slot have completed, so their arrival is enough.
-        if ((!kTied && !wait_phase(sfe_bar(r), rph ^ 1u, abort_flag)) || !wait_phase(sfc_bar(s), ph, abort_flag)) {
+        // With a scale ring (slot r) the copies run ahead; the stage's
+        // tensor-memory slot s is free once the MMAs of its previous use have
+        // completed (its empty barrier).
+        if (kRing) {
+          if (!wait_phase(sfc_bar(r), rph, abort_flag)) {
+            ok = false;
+            break;
+          }
+        } else if ((!kTied && !wait_phase(sfe_bar(r), rph ^ 1u, abort_flag)) || !wait_phase(sfc_bar(s), ph, abort_flag)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t st = smem_base + s * uint32_t(stage);
+        const uint32_t st = kRing ? sf_ring + r * uint32_t(sf_slot) : smem_base + s * uint32_t(stage);
         const uint32_t sf = tmem + lane_base + uint32_t(kSfColBase + (kTied ? s : r) * C::SfCols);
         const int nkb = min(4, kblocks - 4 * kt);
-        if constexpr (MX) {
+        if constexpr (TM) {
+          // Token-major slots are 48 contiguous columns: the weight tiles'
+          // scales (step kb, tile j at 8 kb + 4 j) fill columns 0-31 and the
+          // token tile's (4 kb) columns 32-47, so the whole slot goes out in
+          // two stores (one 32-column and one 16-column tcgen05.st) instead
+          // of twelve 4-column ones.  All four steps are stored; the MMAs of
+          // a short last stage read only its first nkb.
+          uint32_t wv[32], av[16];
+          auto put = [](uint32_t* d, const uint4& v) { d[0] = v.x, d[1] = v.y, d[2] = v.z, d[3] = v.w; };
+          if constexpr (MX) {
+            // A 512-byte MXFP4 block holds 4 ue8m0 scales per row for 128 K
+            // elements: bytes 0-1 go to k64 step 2m, bytes 2-3 to step 2m + 1.
+            auto lo = [](const uint4& v) { return make_uint4(v.x & 0xFFFFu, v.y & 0xFFFFu, v.z & 0xFFFFu, v.w & 0xFFFFu); };
+            auto hi = [](const uint4& v) { return make_uint4(v.x >> 16, v.y >> 16, v.z >> 16, v.w >> 16); };
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const uint4 v = ptx::lds128(st + off_sfa + j * kSfTile + m * 512 + lane * 16);
+                put(wv + (2 * m) * 8 + j * 4, lo(v));
+                put(wv + (2 * m + 1) * 8 + j * 4, hi(v));
+              }
+              const uint4 v = ptx::lds128(st + off_sfb + m * 512 + lane * 16);
+              put(av + (2 * m) * 4, lo(v));
+              put(av + (2 * m + 1) * 4, hi(v));
+            }
+          } else {
+#pragma unroll
+            for (int kb = 0; kb < 4; ++kb) {
+#pragma unroll
+              for (int j = 0; j < 2; ++j) put(wv + kb * 8 + j * 4, ptx::lds128(st + off_sfa + j * kSfTile + kb * 512 + lane * 16));
+              put(av + kb * 4, ptx::lds128(st + off_sfb + kb * 512 + lane * 16));
+            }
+          }
+          if constexpr (kRing) {
+            // The ring slot is read: hand it back, then wait for the
+            // tensor-memory slot.  The proxy fence orders these generic-proxy
+            // reads before the TMA (async-proxy) writes the slot's next
+            // copies make once the arrival is seen; without it some slots
+            // were overwritten before they were read (wrong scales in whole
+            // token tiles, found by comparing tile orientations bit for bit).
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(sfe_bar(r));
+            if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+          }
+          ptx::tmem_st_32x32b_x32(sf, wv);
+          ptx::tmem_st_32x32b_x16(sf + 32, av);
+        } else if constexpr (MX) {
           // A 512-byte MXFP4 block holds 4 ue8m0 scales per row for 128 K
           // elements: bytes 0-1 go to the k64 step 2m, bytes 2-3 to 2m + 1,
           // each into bytes 0-1 of that step's cell.
@@ -968,7 +1082,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
           else ptx::mbar_arrive(b);
         }
         if (++s == uint32_t(S)) s = 0, ph ^= 1u;
-        if (++r == uint32_t(C::SfSlots)) r = 0, rph ^= 1u;
+        if (++r == uint32_t(kRing ? R : C::SfSlots)) r = 0, rph ^= 1u;
       }
     }
   };
@@ -1256,8 +1370,8 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
     const int wg = warp >> 2;
     if (wg == 0) {
       ptx::setmaxnreg_dec<regs_control(SWIGLU)>();
-      if (warp == 0 && lane == 0) {
-        role_producer();
+      if (lane == 0 && (warp == 0 || (kRing && warp == 2))) {
+        role_producer(warp == 0 ? 0 : 1);
       } else if (warp == 1 && lane == 0) {
         if (PAIR && crank != 0) role_peer_wait();
         else role_mma();
@@ -1274,7 +1388,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
       teardown();
     }
   } else {
-    if (warp == 0 && lane == 0) role_producer();
+    if (warp == 0 && lane == 0) role_producer(0);
     else if (warp == 1 && lane == 0) role_mma();
     else if (warp >= epi_first(TM) + epi_warps(SWIGLU)) role_scale();
     else if (warp >= epi_first(TM)) role_epilogue();
