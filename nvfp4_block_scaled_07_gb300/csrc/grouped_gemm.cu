@@ -891,10 +891,10 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
           for (int kb = 0; kb < nkb; ++kb) mma_block(kb);
         }
       };
-      // Token-major stages carry four N = 256 MMAs each, which cover the
-      // per-round work, and each is issued as soon as it lands (waiting for a
-      // second stage measured 2 % slower on the down GEMM); the default
-      // orientation issues its N <= 128 MMAs two stages at a time.
+      // Token-major stages carry four N = 256 MMAs each and are issued one
+      // at a time (bf16 epilogue) or two at a time (SwiGLU epilogue, see
+      // launch_impl); the default orientation issues its N <= 128 MMAs two
+      // stages at a time.
       const bool pair_stages = !TM || p.batch2;
       for (int kt = 0; kt < nkt; kt += pair_stages ? 2 : 1) {
         const bool two = pair_stages && kt + 1 < nkt;
@@ -1587,14 +1587,14 @@ int w_policy_from_env(int dflt) {
   return v >= 0 && v <= 2 ? v : dflt;
 }
 
-// Token-major MMA issue in pairs of stages: NVFP4MOE_TM_BATCH=2 (1 is the
-// default), for pipeline studies.
-int tm_batch_from_env() {
+// Token-major MMA issue in pairs of stages: NVFP4MOE_TM_BATCH=1 or 2
+// overrides the default `dflt` (0: one stage at a time, 1: two).
+int tm_batch_from_env(int dflt) {
   static const int b = [] {
     const char* v = std::getenv("NVFP4MOE_TM_BATCH");
-    return v && v[0] == '2' ? 1 : 0;
+    return v ? (v[0] == '2' ? 1 : v[0] == '1' ? 0 : -1) : -1;
   }();
-  return b;
+  return b >= 0 ? b : dflt;
 }
 
 template <int BN, int NA, bool SWIGLU, bool MX, bool TM = false, bool PAIR = false, bool FIN = false>
@@ -1651,7 +1651,13 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   p.w_tiled = a.w_tiled ? 1 : 0;
   p.w_kc = w_kc;
   p.wait_us = wait_limit_us();
-  p.batch2 = tm_batch_from_env();
+  // The gate/up kernels issue two stages' MMAs per wait: their MMA thread
+  // shares its SM sub-partition with the busy SwiGLU epilogue warps, and the
+  // instructions between two stages took ~330 cycles there (clock64 in the
+  // MMA thread at prefill), more than the ~256 cycles of MMAs still queued.
+  // Measured at prefill on CTA pairs: gate/up 2.63 -> 2.50 ms; down (bf16
+  // epilogue) unchanged, so it keeps one stage at a time.
+  p.batch2 = tm_batch_from_env(SWIGLU ? 1 : 0);
   p.min_rows = a.min_rows;
   p.max_rows = a.max_rows;
   p.perm_to_flat = a.perm_to_flat;
