@@ -129,7 +129,6 @@ struct Params {
   int w_kc;         // 128-byte K chunks per weight row (tiled layout)
   int64_t rows_cap;
   uint32_t wait_us;  // limit of every pipeline wait (nvfp4moe_set_wait_limit_us)
-  int batch2;        // token-major: the MMA thread waits for and issues two stages at a time
   int w_policy;      // L2 policy of weight copies: 0 evict_first, 1 evict_normal, 2 evict_last
   int32_t min_rows, max_rows;  // experts outside [min_rows, max_rows) get no tiles in this launch
   const int32_t* perm_to_flat;  // NVFP4MOE_EPI_FINALIZE_F32: row -> flat id t * k + j
@@ -857,22 +856,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
         const int nkb = min(4, kblocks - 4 * kt);
         const uint64_t bdesc = ptx::desc_kmajor_sw128(st + off_b);
         auto mma_block = [&](int kb) {
-          if constexpr (TM) {
-            // D[token][weight row] += tokens (A, M = 128) x weight tiles (B, N = 256);
-            // scales: tokens at column 32 + 4 kb, weights at 8 kb (+4 for the second tile)
-            // (pair: M = 256 tokens, 128 per CTA; N = 256 weight rows, 128 per CTA)
-            const uint64_t adesc = ptx::desc_kmajor_sw128(st + off_b) + 2 * kb;
-            const uint64_t wdesc = ptx::desc_kmajor_sw128(st) + 2 * kb;
-            const uint32_t acc = (kt | kb) != 0 ? 1u : 0u;
-            if constexpr (PAIR && MX)
-              ptx::tc_mma_mxfp4_pair(d0, adesc, wdesc, idesc, sf + C::NA * 16 + kb * 4, sf + kb * 8, acc);
-            else if constexpr (PAIR)
-              ptx::tc_mma_nvfp4_pair(d0, adesc, wdesc, idesc, sf + C::NA * 16 + kb * 4, sf + kb * 8, acc);
-            else if constexpr (MX)
-              ptx::tc_mma_mxfp4(d0, adesc, wdesc, idesc, sf + C::NA * 16 + kb * 4, sf + kb * 8, acc);
-            else
-              ptx::tc_mma_nvfp4(d0, adesc, wdesc, idesc, sf + C::NA * 16 + kb * 4, sf + kb * 8, acc);
-          } else {
+          {
 #pragma unroll
             for (int j = 0; j < C::NA; ++j) {
               if constexpr (MX)
@@ -891,13 +875,57 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
           for (int kb = 0; kb < nkb; ++kb) mma_block(kb);
         }
       };
-      // Token-major stages carry four N = 256 MMAs each and are issued one
-      // at a time (bf16 epilogue) or two at a time (SwiGLU epilogue, see
-      // launch_impl); the default orientation issues its N <= 128 MMAs two
-      // stages at a time.
-      const bool pair_stages = !TM || p.batch2;
-      for (int kt = 0; kt < nkt; kt += pair_stages ? 2 : 1) {
-        const bool two = pair_stages && kt + 1 < nkt;
+      if constexpr (TM) {
+        // Token-major: wait for the next stage, then issue it and every
+        // following stage of the tile whose operands and scales are already
+        // in, back to back (a test of the barrier, no wait), so the MMA
+        // queue is refilled with as little thread work between stages as
+        // the data allows.  The MMA thread shares its SM sub-partition with
+        // busy epilogue warps, and clock64 in it at prefill showed ~330
+        // cycles of loop work between two stages, more than the ~256 cycles
+        // of MMAs still queued; this loop measured (CTA pairs, prefill)
+        // gate/up 2.63 -> 2.41 ms and down 1.46 -> 1.36 ms against one stage
+        // per iteration of the general loop.  Stage s's descriptors are stage 0's plus
+        // s * stage / 16 in the start-address field (shared addresses stay
+        // below 2^18, so the 14-bit field never carries).
+        const uint64_t wdesc0 = ptx::desc_kmajor_sw128(smem_base);
+        const uint64_t adesc0 = ptx::desc_kmajor_sw128(smem_base + off_b);
+        const uint32_t stage16 = uint32_t(stage) >> 4;
+        int kt = 0;
+        while (kt < nkt) {
+          if (!ptx::mbar_test_wait(full_bar(s), ph) && !wait_phase<true>(full_bar(s), ph, abort_flag)) {
+            ok = false;
+            break;
+          }
+          do {
+            ptx::tc_fence_after();
+            const uint64_t so = uint64_t(s * stage16);
+            const uint32_t sf = tmem + uint32_t(kSfColBase) + s * uint32_t(C::SfCols);
+            const int nkb = min(4, kblocks - 4 * kt);
+            auto mma = [&](int kb) {
+              const uint64_t adesc = adesc0 + so + 2 * kb, wdesc = wdesc0 + so + 2 * kb;
+              const uint32_t acc = (kt | kb) != 0 ? 1u : 0u;
+              const uint32_t sfa = sf + C::NA * 16 + kb * 4, sfw = sf + kb * 8;
+              if constexpr (PAIR && MX) ptx::tc_mma_mxfp4_pair(d0, adesc, wdesc, idesc, sfa, sfw, acc);
+              else if constexpr (PAIR) ptx::tc_mma_nvfp4_pair(d0, adesc, wdesc, idesc, sfa, sfw, acc);
+              else if constexpr (MX) ptx::tc_mma_mxfp4(d0, adesc, wdesc, idesc, sfa, sfw, acc);
+              else ptx::tc_mma_nvfp4(d0, adesc, wdesc, idesc, sfa, sfw, acc);
+            };
+            if (nkb == 4) {
+#pragma unroll
+              for (int kb = 0; kb < 4; ++kb) mma(kb);
+            } else {
+              for (int kb = 0; kb < nkb; ++kb) mma(kb);
+            }
+            commit(empty_bar(s));  // frees the stage and its scale slot once these MMAs have read it
+            ++kt;
+            if (++s == uint32_t(S)) s = 0, ph ^= 1u;
+          } while (kt < nkt && ptx::mbar_test_wait(full_bar(s), ph));
+        }
+      } else {
+      // The default orientation issues its N <= 128 MMAs two stages at a time.
+      for (int kt = 0; kt < nkt; kt += 2) {
+        const bool two = kt + 1 < nkt;
         uint32_t s2 = s + 1, ph2 = ph, r2 = r + 1, rph2 = rph;
         if (s2 == uint32_t(S)) s2 = 0, ph2 ^= 1u;
         if (r2 == uint32_t(C::SfSlots)) r2 = 0, rph2 ^= 1u;
@@ -934,6 +962,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
         }
         if (s == uint32_t(S)) s = 0, ph ^= 1u;
         if (r == uint32_t(C::SfSlots)) r = 0, rph ^= 1u;
+      }
       }
       if (!ok) break;
       commit(accf_bar(s0));
@@ -1587,16 +1616,6 @@ int w_policy_from_env(int dflt) {
   return v >= 0 && v <= 2 ? v : dflt;
 }
 
-// Token-major MMA issue in pairs of stages: NVFP4MOE_TM_BATCH=1 or 2
-// overrides the default `dflt` (0: one stage at a time, 1: two).
-int tm_batch_from_env(int dflt) {
-  static const int b = [] {
-    const char* v = std::getenv("NVFP4MOE_TM_BATCH");
-    return v ? (v[0] == '2' ? 1 : v[0] == '1' ? 0 : -1) : -1;
-  }();
-  return b >= 0 ? b : dflt;
-}
-
 template <int BN, int NA, bool SWIGLU, bool MX, bool TM = false, bool PAIR = false, bool FIN = false>
 int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st) {
   using C = Cfg<BN, NA, SWIGLU>;
@@ -1651,13 +1670,6 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   p.w_tiled = a.w_tiled ? 1 : 0;
   p.w_kc = w_kc;
   p.wait_us = wait_limit_us();
-  // The gate/up kernels issue two stages' MMAs per wait: their MMA thread
-  // shares its SM sub-partition with the busy SwiGLU epilogue warps, and the
-  // instructions between two stages took ~330 cycles there (clock64 in the
-  // MMA thread at prefill), more than the ~256 cycles of MMAs still queued.
-  // Measured at prefill on CTA pairs: gate/up 2.63 -> 2.50 ms; down (bf16
-  // epilogue) unchanged, so it keeps one stage at a time.
-  p.batch2 = tm_batch_from_env(SWIGLU ? 1 : 0);
   p.min_rows = a.min_rows;
   p.max_rows = a.max_rows;
   p.perm_to_flat = a.perm_to_flat;
