@@ -456,34 +456,52 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot) {
   return res;
 }
 
-// One block of 1024 threads, thread e = expert e (E <= 1024): per-segment
-// bases, counts, offsets [E+1] and 128-aligned row offsets [E+1].  Returns
-// this thread's expert count and row offset.
+// One block of 1024 threads (E <= 1024): per-segment bases, counts,
+// offsets [E+1] and 128-aligned row offsets [E+1].  G threads per expert (a
+// power of two, at most 32, so a group sits in one warp) each sum a run of
+// segments, scan the runs with shuffles and write their segments' bases; the
+// per-expert totals then go through block scans, thread e = expert e.
+// (One thread per expert walking all segments took ~10 us at 128 segments.)
+// s_tot: 1024 ints of shared memory.  Returns thread e's expert count and
+// row offset.
 __device__ __forceinline__ void scan_experts(const int32_t* seg_count, int nseg, int E, int32_t* __restrict__ seg_base,
                                              int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                                             int32_t* __restrict__ row_offsets, int* warp_tot, int* cnt_out,
+                                             int32_t* __restrict__ row_offsets, int* warp_tot, int* s_tot, int* cnt_out,
                                              int* roff_out) {
-  const int e = threadIdx.x;
-  int run = 0;
-  if (e < E) {
-    int s = 0;
-    for (; s + 8 <= nseg; s += 8) {
+  int ep = 1;
+  while (ep < E) ep <<= 1;
+  const int G = min(32, 1024 / ep);
+  const int ge = threadIdx.x / G, sub = threadIdx.x % G;
+  const int chunk = (nseg + G - 1) / G;
+  const int sa = min(nseg, sub * chunk), sb = min(nseg, sa + chunk);
+  int local = 0;
+  if (ge < E) {
+    int s = sa;
+    for (; s + 8 <= sb; s += 8) {
       int c[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) c[j] = __ldcg(seg_count + int64_t(s + j) * E + e);
+      for (int j = 0; j < 8; ++j) c[j] = __ldcg(seg_count + int64_t(s + j) * E + ge);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        seg_base[int64_t(s + j) * E + e] = run;
-        run += c[j];
-      }
+      for (int j = 0; j < 8; ++j) local += c[j];
     }
-    for (; s < nseg; ++s) {
-      const int c = __ldcg(seg_count + int64_t(s) * E + e);
-      seg_base[int64_t(s) * E + e] = run;
-      run += c;
-    }
+    for (; s < sb; ++s) local += __ldcg(seg_count + int64_t(s) * E + ge);
   }
-  const int cnt = e < E ? run : 0;
+  int incl = local;
+  for (int off = 1; off < G; off <<= 1) {
+    const int o = __shfl_up_sync(kFull, incl, off, G);
+    if (sub >= off) incl += o;
+  }
+  if (ge < E) {
+    int run = incl - local;
+    for (int s = sa; s < sb; ++s) {
+      seg_base[int64_t(s) * E + ge] = run;
+      run += __ldcg(seg_count + int64_t(s) * E + ge);
+    }
+    if (sub == G - 1) s_tot[ge] = incl;
+  }
+  __syncthreads();
+  const int e = threadIdx.x;
+  const int cnt = e < E ? s_tot[e] : 0;
   const int padded = (cnt + 127) & ~127;
   const int off = block_exclusive_scan(cnt, warp_tot);
   const int roff = block_exclusive_scan(padded, warp_tot);
@@ -511,9 +529,9 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(const int32_t* __res
   ptx::grid_dep_launch();
   __shared__ int warp_tot[32];
   __shared__ int tail_start;
-  __shared__ int s_cnt[1024], s_roff[1024];
+  __shared__ int s_cnt[1024], s_roff[1024], s_tot[1024];
   int cnt, roff;
-  scan_experts(seg_count, nseg, E, seg_base, counts, offsets, row_offsets, warp_tot, &cnt, &roff);
+  scan_experts(seg_count, nseg, E, seg_base, counts, offsets, row_offsets, warp_tot, s_tot, &cnt, &roff);
   const int e = threadIdx.x;
   if (e < E) {
     s_cnt[e] = cnt;
@@ -640,6 +658,7 @@ struct PrepareParams {
 };
 
 constexpr int kPrepThreads = 1024;
+constexpr int kRouteWarps = 16;  // most routing warps per CTA in phase A (NVFP4)
 // All CTAs of the grid meet here.  Thread 0 of each CTA arrives on a
 // device-scope counter; the last arrival resets it and bumps the generation
 // word the others poll (bounded by the launch's wait limit).  Returns false, the same
@@ -684,6 +703,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
   __shared__ float s_red[32];
   __shared__ int s_ok;
   __shared__ int warp_tot[32];
+  __shared__ int s_tot[1024];
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -695,23 +715,36 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
   const int64_t R = int64_t(p.T) * p.k;
 
   // ---- A: routing (batch-aware: its first pass) and partial amax ----------
+  // The first nroute warps of every CTA route (compute and latency bound;
+  // as many as give each at most one token, up to kRouteWarps) while the
+  // others stream x for its amax (HBM bound), so the two overlap; with no
+  // amax (MXFP4) every warp routes.
   const bool batch_aware = p.k_primary < p.k;
-  for (int64_t t = gw0; t < p.T; t += gw_stride) {
-    if (batch_aware)
-      mark_primary<VPL>(p.logits, p.bias, int(t), p.E, p.k_primary, p.active_set, lane);
-    else
-      route_token<VPL>(p.logits, p.bias, int(t), p.E, p.k, p.score_fn, p.renorm, nullptr, p.idx, p.w, lane);
+  const int nroute = p.mx ? nwarp : min(kRouteWarps, max(1, int((p.T + gridDim.x - 1) / gridDim.x)));
+  if (warp < nroute) {
+    for (int64_t t = int64_t(warp) * gridDim.x + blockIdx.x; t < p.T; t += int64_t(gridDim.x) * nroute) {
+      if (batch_aware)
+        mark_primary<VPL>(p.logits, p.bias, int(t), p.E, p.k_primary, p.active_set, lane);
+      else
+        route_token<VPL>(p.logits, p.bias, int(t), p.E, p.k, p.score_fn, p.renorm, nullptr, p.idx, p.w, lane);
+    }
   }
   if (!p.mx) {
     float m = 0.f;
-    const int64_t nvec = int64_t(p.T) * p.H / 8;
-    int64_t i = tid;
-    for (; i + 3 * nthreads < nvec; i += 4 * nthreads) {
-      const uint4 q0 = __ldg(p.x + i), q1 = __ldg(p.x + i + nthreads);
-      const uint4 q2 = __ldg(p.x + i + 2 * nthreads), q3 = __ldg(p.x + i + 3 * nthreads);
-      m = amax8(q3, amax8(q2, amax8(q1, amax8(q0, m))));
+    if (warp >= nroute) {
+      // 8 independent 16-byte loads in flight per thread
+      const int64_t na = int64_t(gridDim.x) * (kPrepThreads - 32 * nroute);
+      const int64_t nvec = int64_t(p.T) * p.H / 8;
+      int64_t i = int64_t(blockIdx.x) * (kPrepThreads - 32 * nroute) + (threadIdx.x - 32 * nroute);
+      for (; i + 7 * na < nvec; i += 8 * na) {
+        uint4 q[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) q[u] = __ldg(p.x + i + u * na);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) m = amax8(q[u], m);
+      }
+      for (; i < nvec; i += na) m = amax8(__ldg(p.x + i), m);
     }
-    for (; i < nvec; i += nthreads) m = amax8(__ldg(p.x + i), m);
 #pragma unroll
     for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
     if (lane == 0) s_red[warp] = m;
@@ -733,23 +766,29 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
   }
 
   // ---- B: segment ranks, global scale, quantisation --------------------------
-  // The rank warps start at once; warp kRankWarps reduces the amax partials
-  // meanwhile (NVFP4), and the quantisation waits for its result.
-  if (warp < kRankWarps)
-    for (int64_t seg = int64_t(warp) * gridDim.x + blockIdx.x; seg < p.nseg; seg += int64_t(gridDim.x) * kRankWarps)
-      rank_segment<ITERS>(p.idx, R, p.E, seg, s_rank_cnt + warp * p.E, p.rank, p.seg_count, lane);
-  if (warp == kRankWarps && !p.mx) {
+  // Warp 0 of every CTA ranks segments while the other warps quantise, so a
+  // CTA with a segment does not start its share of the quantisation late
+  // (the rank of a 1024-id segment is a long dependent chain).  Warp 1
+  // reduces the amax partials (NVFP4); the quantising warps wait for it on a
+  // named barrier that warp 0 is not part of.
+  if (warp == 0) {
+    for (int64_t seg = blockIdx.x; seg < p.nseg; seg += gridDim.x)
+      rank_segment<ITERS>(p.idx, R, p.E, seg, s_rank_cnt, p.rank, p.seg_count, lane);
+  } else {
+  if (warp == 1 && !p.mx) {
     float m = 0.f;
     for (int i = lane; i < int(gridDim.x); i += 32) m = fmaxf(m, __ldcg(p.amax_part + i));
 #pragma unroll
     for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
     if (lane == 0) s_red[0] = global_scale_of(m);
   }
-  __syncthreads();
+  asm volatile("bar.sync 1, %0;" ::"r"(kPrepThreads - 32) : "memory");
+  const int64_t qtid = int64_t(blockIdx.x) * (kPrepThreads - 32) + (threadIdx.x - 32);
+  const int64_t nq = int64_t(gridDim.x) * (kPrepThreads - 32);
   if (p.mx) {
     // MXFP4: one thread per 32-element block, no global scale
     const int64_t nblk = int64_t(p.T) * (p.H / 32);
-    for (int64_t b = tid; b < nblk; b += nthreads) {
+    for (int64_t b = qtid; b < nblk; b += nq) {
       uint4 q[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) q[j] = __ldg(p.x + 4 * b + j);
@@ -772,12 +811,12 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
     }
   } else {
     const float s = s_red[0];
-    if (blockIdx.x == 0 && threadIdx.x == 0) *p.gscale = s;
+    if (blockIdx.x == 0 && threadIdx.x == 32) *p.gscale = s;
     // two independent blocks per iteration: their four loads are in flight together
     const int64_t nblk = int64_t(p.T) * (p.H / 16);
-    int64_t b = tid;
-    for (; b + nthreads < nblk; b += 2 * nthreads) {
-      const int64_t b1 = b + nthreads;
+    int64_t b = qtid;
+    for (; b + nq < nblk; b += 2 * nq) {
+      const int64_t b1 = b + nq;
       const uint4 l0 = __ldg(p.x + 2 * b), h0 = __ldg(p.x + 2 * b + 1);
       const uint4 l1 = __ldg(p.x + 2 * b1), h1 = __ldg(p.x + 2 * b1 + 1);
       uint2 k0, k1;
@@ -795,12 +834,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prepare_kernel(const PrepareP
       p.xs[b] = uint8_t(sb);
     }
   }
+  }
   if (!grid_barrier(p.bar, &s_ok, p.wait_us)) return;
 
   // ---- C: expert counts, offsets, row offsets --------------------------------
   if (blockIdx.x == 0) {
     int cnt, roff;
-    scan_experts(p.seg_count, p.nseg, p.E, p.seg_base, p.counts, p.offsets, p.row_offsets, warp_tot, &cnt, &roff);
+    scan_experts(p.seg_count, p.nseg, p.E, p.seg_base, p.counts, p.offsets, p.row_offsets, warp_tot, s_tot, &cnt,
+                 &roff);
   }
   if (!grid_barrier(p.bar, &s_ok, p.wait_us)) return;
 
