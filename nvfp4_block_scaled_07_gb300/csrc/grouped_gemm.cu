@@ -64,28 +64,34 @@ __device__ unsigned g_gemm_flags = 0;
 // Epilogue warps: the SwiGLU requantisation is a long dependent chain per
 // token, so two warps per tensor-memory lane quarter split the token chunks
 // (which also halves the registers each needs to drain its share of the
-// accumulator early); the bf16 epilogue needs one warp per quarter.
-__host__ __device__ constexpr int epi_warps(bool swiglu) { return swiglu ? 8 : 4; }
+// accumulator early).  The CTA-pair bf16 epilogue also takes two warps per
+// quarter, each draining half of the 256 accumulator columns in one
+// tensor-memory round trip before it releases the accumulator; the other
+// bf16 epilogues have one warp per quarter.
+__host__ __device__ constexpr int epi_warps(bool swiglu, bool pair) { return swiglu || pair ? 8 : 4; }
 // warp 0 producer, warp 1 MMA, then the epilogue warps, then 4 scale-factor
 // warps.  Token-major kernels put the roles on warpgroup boundaries (warps 2
 // and 3 idle) so that setmaxnreg can move registers from the producer / MMA
 // and scale-factor warpgroups to the epilogue warpgroups.
 __host__ __device__ constexpr int epi_first(bool wg) { return wg ? 4 : 2; }
-__host__ __device__ constexpr int num_threads(bool swiglu, bool wg) {
-  return 32 * (epi_first(wg) + epi_warps(swiglu) + 4);
+__host__ __device__ constexpr int num_threads(bool swiglu, bool wg, bool pair = false) {
+  return 32 * (epi_first(wg) + epi_warps(swiglu, pair) + 4);
 }
-// Registers per thread after the split (setmaxnreg), by warpgroup: the
-// launch gives every thread 65536 / threads (128 for 512 threads, 168 for
-// 384); the split must not need more than that in total.
-__host__ __device__ constexpr int regs_launch(bool swiglu) { return 65536 / num_threads(swiglu, true) / 8 * 8; }
-// producer, MMA issuer (one lane each) and two idle warps
-__host__ __device__ constexpr int regs_control(bool swiglu) { return swiglu ? 64 : 120; }
-__host__ __device__ constexpr int regs_scale(bool swiglu) { return swiglu ? 80 : 120; }
-__host__ __device__ constexpr int regs_epilogue(bool swiglu) { return swiglu ? 184 : 256; }
+// Registers per thread after the split (setmaxnreg) of a token-major kernel,
+// by warpgroup: with two epilogue warpgroups (512 threads, 128 registers a
+// thread at launch) or one (single-SM bf16: 384 threads, 168); the split
+// must not need more than the launch's registers in total.
+__host__ __device__ constexpr int regs_launch(bool wide) { return 65536 / (wide ? 512 : 384) / 8 * 8; }
+// producer, MMA issuer and scale-ring producer (one lane each) and an idle warp
+__host__ __device__ constexpr int regs_control(bool wide) { return wide ? 64 : 120; }
+__host__ __device__ constexpr int regs_scale(bool wide) { return wide ? 80 : 120; }
+__host__ __device__ constexpr int regs_epilogue(bool wide) { return wide ? 184 : 256; }
+static_assert(num_threads(true, true) == 512 && num_threads(false, true, true) == 512 && num_threads(false, true) == 384,
+              "token-major warp layouts");
 static_assert(regs_control(true) + 2 * regs_epilogue(true) + regs_scale(true) <= 4 * regs_launch(true),
-              "SwiGLU register split exceeds the launch's registers");
+              "register split exceeds the launch's registers");
 static_assert(regs_control(false) + regs_epilogue(false) + regs_scale(false) <= 3 * regs_launch(false),
-              "bf16 register split exceeds the launch's registers");
+              "register split exceeds the launch's registers");
 constexpr int kBM = 128;           // MMA M (weight rows per tile)
 constexpr int kBKBytes = 128;      // bytes of K per stage and row = 256 E2M1 elements
 constexpr int kATile = kBM * kBKBytes;
@@ -99,13 +105,15 @@ constexpr int kMaxStages = 16;
 // Token-major bf16 epilogue: a 2 KB shared-memory buffer per epilogue warp
 // (32 rows x 64 bytes) from which a TMA store writes each chunk.
 constexpr int kOutChunkBytes = 2048;
-__host__ __device__ constexpr int out_stage_bytes(bool swiglu, bool tm) { return tm && !swiglu ? 4 * kOutChunkBytes : 0; }
+__host__ __device__ constexpr int out_stage_bytes(bool swiglu, bool tm, bool pair) {
+  return tm && !swiglu ? epi_warps(swiglu, pair) * kOutChunkBytes : 0;
+}
 // mbarriers: full/empty per stage, acc full/empty per slot, drain, sf full/empty per ring slot,
 // the tile ring, and the scale copies of each stage
 // Ring of claimed tile ids (dynamic schedule): the producer claims ids from
 // a launch-wide counter and passes them to the other roles.
 constexpr int kTileRing = 16;
-__host__ __device__ constexpr int tile_consumers(bool swiglu) { return 1 + 4 + epi_warps(swiglu); }  // MMA, SF and epilogue warps
+__host__ __device__ constexpr int tile_consumers(bool swiglu, bool pair) { return 1 + 4 + epi_warps(swiglu, pair); }  // MMA, SF and epilogue warps
 constexpr int kNumBars = 3 * kMaxStages + 5 + 2 * kMaxSfSlots + 2 * kTileRing;
 constexpr uint64_t kTimeoutNs = 2000000000ull;   // drains after an abort
 constexpr uint64_t kPeerDrainNs = 30000000000ull;  // CTA 1 of a pair waiting for the pair's last MMA
@@ -449,7 +457,7 @@ __device__ __forceinline__ void requant_row32_mx(const uint32_t (&h)[32], int64_
 }
 
 template <int BN, int NA, bool SWIGLU, bool MX, bool TM, bool PAIR = false, bool FIN = false>
-__global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
+__global__ void __launch_bounds__(num_threads(SWIGLU, TM, PAIR), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_sf,
                         const __grid_constant__ CUtensorMap tmap_asf, const Params p) {
@@ -527,7 +535,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(accf_bar(b), 1);
-      ptx::mbar_init(acce_bar(b), (PAIR ? 2 : 1) * epi_warps(SWIGLU));  // both CTAs' epilogues drain it
+      ptx::mbar_init(acce_bar(b), (PAIR ? 2 : 1) * epi_warps(SWIGLU, PAIR));  // both CTAs' epilogues drain it
     }
     ptx::mbar_init(drain_bar, 1);
     for (int r = 0; r < kMaxSfSlots; ++r) {
@@ -537,7 +545,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
     }
     for (int q = 0; q < kTileRing; ++q) {
       ptx::mbar_init(tqf_bar(q), 1);
-      ptx::mbar_init(tqe_bar(q), tile_consumers(SWIGLU) + nprod - 1);  // (+ the scale-copy producer)
+      ptx::mbar_init(tqe_bar(q), tile_consumers(SWIGLU, PAIR) + nprod - 1);  // (+ the scale-copy producer)
     }
     abort_flag->abort = 0;
     abort_flag->limit_us = p.wait_us;
@@ -634,7 +642,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
   const int off_b = NW * kATile;
   const int off_sfa = kRing ? 0 : off_b + wmax * kBKBytes;  // in the stage, or in the ring slot
   const int off_sfb = off_sfa + C::NA * kSfTile;
-  const int room = p.smem_bytes - ctrl - out_stage_bytes(SWIGLU, TM);
+  const int room = p.smem_bytes - ctrl - out_stage_bytes(SWIGLU, TM, PAIR);
   const int S = min(kTied ? C::SfSlots : kMaxStages, min(p.stage_cap, (room - (kRing ? 2 * sf_slot : 0)) / stage));
   const int R = kRing ? min(kMaxSfSlots, (room - S * stage) / sf_slot) : 0;  // scale ring slots
   const uint32_t smem_base = ptx::smem_u32(smem) + uint32_t(ctrl);
@@ -1118,7 +1126,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
   auto role_epilogue = [&]() {
     // ---------------- epilogue ----------------
     const int q = warp & 3;            // tensor-memory lane quarter this warp may access
-    constexpr int kParts = epi_warps(SWIGLU) / 4;  // warps sharing a quarter split the token chunks
+    constexpr int kParts = epi_warps(SWIGLU, PAIR) / 4;  // warps sharing a quarter split the columns or token chunks
     const int part = (warp - epi_first(TM)) / 4;
     const int lrow = q * 32 + lane;    // accumulator row = output feature within the tile
     const float a_gs = MX ? 1.0f : *p.a_gscale;   // MXFP4 has no per-tensor scales
@@ -1206,6 +1214,83 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
             }
           }
         } else {
+          if constexpr (kParts == 2) {
+          // bf16: columns c = output features mb * 256 + c, 64 bytes per
+          // chunk and row.  Two warps per lane quarter: warp part p takes
+          // columns 128 p .. 128 p + 127 (four 32-column chunks), loads them
+          // in one tensor-memory round trip and releases the accumulator
+          // before any arithmetic (with one warp per quarter the second
+          // round trip waited for the first one's conversion, ~1.5k cycles
+          // of accumulator drain per tile at prefill), then packs them to
+          // bf16.  A thread's row is 14 KB away from its neighbour's, so each
+          // chunk is staged in this warp's 2 KB buffer and written by a TMA
+          // store (full 64-byte row segments) when all 32 rows of the quarter
+          // belong to the expert; a partial quarter stores per thread and
+          // leaves the padding rows untouched.
+          constexpr int kMine = C::NA * kBM / 32 / 2;  // this warp's 32-column chunks
+          const int cbase = kMine * part;              // its first chunk
+          uint32_t pk[kMine][16];
+          {
+            uint32_t g[kMine][32];
+#pragma unroll
+            for (int j = 0; j < kMine; ++j) ptx::tmem_ld_32x32b_x32(tbase + 32 * (cbase + j), g[j]);
+            ptx::tmem_ld_wait();
+            release();
+#pragma unroll
+            for (int j = 0; j < kMine; ++j)
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(g[j][2 * i]) * scale,
+                                                               __uint_as_float(g[j][2 * i + 1]) * scale);
+                pk[j][i] = *reinterpret_cast<const uint32_t*>(&v);
+              }
+          }
+          if constexpr (FIN) {
+            // fused finalize: this thread's token row, times its routing
+            // weight, added into the token's float32 row
+            if (row_ok) {
+              const int fl = __ldg(p.perm_to_flat + row);
+              const float wt = __ldg(p.topk_w + fl);
+              float* dst = static_cast<float*>(p.c_out) + int64_t(fl / p.k) * n_out + mb * (C::NA * kBM);
+#pragma unroll
+              for (int j = 0; j < kMine; ++j)
+#pragma unroll
+                for (int i = 0; i < 16; i += 2) {
+                  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[j][i]));
+                  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[j][i + 1]));
+                  ptx::red_add_v4(dst + 32 * (cbase + j) + 2 * i, wt * a.x, wt * a.y, wt * b.x, wt * b.y);
+                }
+            }
+            slots.done(s0, s1);
+            continue;
+          }
+          const bool quarter_full = q * 32 + 32 <= valid;
+          const uint32_t obuf = out_base + uint32_t((warp - epi_first(TM)) * kOutChunkBytes);
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.c_out) + row * n_out + mb * (C::NA * kBM);
+#pragma unroll
+          for (int j = 0; j < kMine; ++j) {
+            const int c = cbase + j;
+            if (quarter_full) {
+              if (lane == 0) ptx::bulk_wait_read_all();  // the previous chunk's store has read the buffer
+              __syncwarp();
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                ptx::sts128(obuf + uint32_t(lane * 64 + i * 16), pk[j][4 * i], pk[j][4 * i + 1], pk[j][4 * i + 2],
+                            pk[j][4 * i + 3]);
+              ptx::fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                ptx::tma_store_2d(&tmap_c, obuf, mb * (C::NA * kBM) + 32 * c, int(row0 + q * 32));
+                ptx::bulk_commit();
+              }
+            } else if (row_ok) {
+              uint4* o = reinterpret_cast<uint4*>(out + 32 * c);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                o[i] = make_uint4(pk[j][4 * i], pk[j][4 * i + 1], pk[j][4 * i + 2], pk[j][4 * i + 3]);
+            }
+          }
+          } else {
           // bf16: columns c = output features mb * 256 + c, 64 bytes per
           // chunk and row.  The whole row (256 columns) is packed to bf16 in
           // registers, two chunks per tensor-memory round trip, and the
@@ -1279,6 +1364,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
               for (int i = 0; i < 4; ++i)
                 o[i] = make_uint4(pk[c][4 * i], pk[c][4 * i + 1], pk[c][4 * i + 2], pk[c][4 * i + 3]);
             }
+          }
           }
         }
       } else if constexpr (SWIGLU) {
@@ -1398,7 +1484,7 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
     // budgets.
     const int wg = warp >> 2;
     if (wg == 0) {
-      ptx::setmaxnreg_dec<regs_control(SWIGLU)>();
+      ptx::setmaxnreg_dec<regs_control(epi_warps(SWIGLU, PAIR) == 8)>();
       if (lane == 0 && (warp == 0 || (kRing && warp == 2))) {
         role_producer(warp == 0 ? 0 : 1);
       } else if (warp == 1 && lane == 0) {
@@ -1407,19 +1493,19 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM), 1)
       }
       __syncwarp();
       teardown();
-    } else if (wg == (epi_first(TM) + epi_warps(SWIGLU)) / 4) {
-      ptx::setmaxnreg_dec<regs_scale(SWIGLU)>();
+    } else if (wg == (epi_first(TM) + epi_warps(SWIGLU, PAIR)) / 4) {
+      ptx::setmaxnreg_dec<regs_scale(epi_warps(SWIGLU, PAIR) == 8)>();
       role_scale();
       teardown();
     } else {
-      ptx::setmaxnreg_inc<regs_epilogue(SWIGLU)>();
+      ptx::setmaxnreg_inc<regs_epilogue(epi_warps(SWIGLU, PAIR) == 8)>();
       role_epilogue();
       teardown();
     }
   } else {
     if (warp == 0 && lane == 0) role_producer(0);
     else if (warp == 1 && lane == 0) role_mma();
-    else if (warp >= epi_first(TM) + epi_warps(SWIGLU)) role_scale();
+    else if (warp >= epi_first(TM) + epi_warps(SWIGLU, PAIR)) role_scale();
     else if (warp >= epi_first(TM)) role_epilogue();
     teardown();
   }
@@ -1624,11 +1710,11 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   // tile must fit.
   const int64_t usable = int64_t(smem_optin) - 1024 - ctrl_bytes(a.E);
   const int worst = PAIR ? kATile + kBM * kBKBytes + NA * kSfTile + kSfTile : C::stage_bytes(BN);
-  if (usable < 2 * int64_t(worst) + out_stage_bytes(SWIGLU, TM)) {
+  if (usable < 2 * int64_t(worst) + out_stage_bytes(SWIGLU, TM, PAIR)) {
     set_error_detail(
         "grouped GEMM tile %dx%d (%s) needs %lld bytes of shared memory for a 2-stage pipeline; Hardware limit: %d",
         kBM * NA, BN, SWIGLU ? "gate/up" : "down",
-        (long long)(1024 + ctrl_bytes(a.E) + 2 * int64_t(worst) + out_stage_bytes(SWIGLU, TM)), smem_optin);
+        (long long)(1024 + ctrl_bytes(a.E) + 2 * int64_t(worst) + out_stage_bytes(SWIGLU, TM, PAIR)), smem_optin);
     return NVFP4MOE_ERR_SMEM;
   }
   const size_t smem = size_t(smem_optin);
@@ -1637,7 +1723,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   if (!encode_weight_map(&tw, a, SWIGLU, PAIR ? 1 : (SWIGLU ? 2 : NA)) || !encode_weight_scale_map(&tsf, a, SWIGLU, NA) ||
       !encode_token_scale_map(&tasf, a) ||
       !encode_kmajor_map(&ta, a.a_packed, a.rows_capacity, a.K / 2, TM ? kBM : 32) ||
-      !(out_stage_bytes(SWIGLU, TM) && a.epilogue != NVFP4MOE_EPI_FINALIZE_F32
+      !(out_stage_bytes(SWIGLU, TM, PAIR) && a.epilogue != NVFP4MOE_EPI_FINALIZE_F32
             ? encode_bf16_store_map(&tc, a.c_out, a.rows_capacity, a.N)
             : encode_kmajor_map(&tc, a.a_packed, a.rows_capacity, a.K / 2, 32))) {
     set_error_detail("cuTensorMapEncodeTiled failed or is unavailable");
@@ -1688,7 +1774,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
   if constexpr (PAIR) {
     // Clusters of two CTAs on neighbouring SMs, as many as can be resident
     // at once (the kernel is persistent: pair c takes tiles c, c + #pairs, ...).
-    const int pairs = max_pairs(kernel, num_threads(SWIGLU, TM), smem, num_sms);
+    const int pairs = max_pairs(kernel, num_threads(SWIGLU, TM, PAIR), smem, num_sms);
     if (pairs < 1) {
       set_error_detail("no CTA pair of the grouped GEMM fits on this device");
       return NVFP4MOE_ERR_SMEM;
@@ -1701,7 +1787,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2 * pairs);
-    cfg.blockDim = dim3(num_threads(SWIGLU, TM));
+    cfg.blockDim = dim3(num_threads(SWIGLU, TM, PAIR));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
@@ -1709,7 +1795,7 @@ int launch_impl(const GemmArgs& a, int num_sms, int smem_optin, cudaStream_t st)
     err = cudaLaunchKernelEx(&cfg, kernel, tw, ta, tc, tsf, tasf, p);
     if (err == cudaSuccess) err = cudaGetLastError();
   } else {
-    kernel<<<num_sms, num_threads(SWIGLU, TM), smem, st>>>(tw, ta, tc, tsf, tasf, p);
+    kernel<<<num_sms, num_threads(SWIGLU, TM, PAIR), smem, st>>>(tw, ta, tc, tsf, tasf, p);
     err = cudaGetLastError();
   }
   if (err != cudaSuccess) {
