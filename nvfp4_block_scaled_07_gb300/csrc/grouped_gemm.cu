@@ -899,17 +899,30 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM, PAIR), 1)
         const uint64_t wdesc0 = ptx::desc_kmajor_sw128(smem_base);
         const uint64_t adesc0 = ptx::desc_kmajor_sw128(smem_base + off_b);
         const uint32_t stage16 = uint32_t(stage) >> 4;
+        // The next stage's barrier is tested before the stage's last MMA and
+        // (CTA pairs) the stage's commit is issued after the first MMA of the
+        // next stage of the group, so neither sits between two stages' MMAs:
+        // with about one MMA queued, every cycle of this thread between the
+        // last MMA of a stage and the first of the next one idles the tensor
+        // core (an extra commit or barrier test per stage each cost ~3.5 % of
+        // the prefill gate/up GEMM).  Single-SM kernels, with one stage
+        // fewer, commit at once: the later release measured 4 % slower there.
         int kt = 0;
+        uint32_t ps = 0;    // last stage whose MMAs are issued and not yet committed
+        bool pend = false;  // (within a group of stages issued back to back)
         while (kt < nkt) {
           if (!ptx::mbar_test_wait(full_bar(s), ph) && !wait_phase<true>(full_bar(s), ph, abort_flag)) {
             ok = false;
             break;
           }
+          bool more;
           do {
             ptx::tc_fence_after();
             const uint64_t so = uint64_t(s * stage16);
             const uint32_t sf = tmem + uint32_t(kSfColBase) + s * uint32_t(C::SfCols);
             const int nkb = min(4, kblocks - 4 * kt);
+            uint32_t sn = s + 1, phn = ph;
+            if (sn == uint32_t(S)) sn = 0, phn ^= 1u;
             auto mma = [&](int kb) {
               const uint64_t adesc = adesc0 + so + 2 * kb, wdesc = wdesc0 + so + 2 * kb;
               const uint32_t acc = (kt | kb) != 0 ? 1u : 0u;
@@ -919,16 +932,23 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM, PAIR), 1)
               else if constexpr (MX) ptx::tc_mma_mxfp4(d0, adesc, wdesc, idesc, sfa, sfw, acc);
               else ptx::tc_mma_nvfp4(d0, adesc, wdesc, idesc, sfa, sfw, acc);
             };
+            mma(0);
+            if (PAIR && pend) commit(empty_bar(ps));  // frees stage ps (and its scale slot) once its MMAs have read it
             if (nkb == 4) {
-#pragma unroll
-              for (int kb = 0; kb < 4; ++kb) mma(kb);
+              mma(1);
+              mma(2);
+              more = kt + 1 < nkt && ptx::mbar_test_wait(full_bar(sn), phn);
+              mma(3);
             } else {
-              for (int kb = 0; kb < nkb; ++kb) mma(kb);
+              for (int kb = 1; kb < nkb; ++kb) mma(kb);
+              more = kt + 1 < nkt && ptx::mbar_test_wait(full_bar(sn), phn);
             }
-            commit(empty_bar(s));  // frees the stage and its scale slot once these MMAs have read it
-            ++kt;
-            if (++s == uint32_t(S)) s = 0, ph ^= 1u;
-          } while (kt < nkt && ptx::mbar_test_wait(full_bar(s), ph));
+            if (!PAIR) commit(empty_bar(s));
+            ps = s, pend = PAIR;
+            ++kt, s = sn, ph = phn;
+          } while (more);
+          if (pend) commit(empty_bar(ps));  // the group's last stage
+          pend = false;
         }
       } else {
       // The default orientation issues its N <= 128 MMAs two stages at a time.
