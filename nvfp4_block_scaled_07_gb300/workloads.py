@@ -68,6 +68,10 @@ WORKLOADS = {
 PROFILE_WORKLOADS = {
     "profile_decode_e16": Workload("profile_decode_e16", T=8, E=16, k=8, H=6144, I=2048, score="sigmoid"),
     "profile_prefill_e8": Workload("profile_prefill_e8", T=2048, E=8, k=8, H=7168, I=4096, score="sigmoid"),
+    # the skewed_t2048 regime (Zipf 1.1 popularity: a few hot experts with hundreds of rows next to
+    # many cold ones with a handful) at a quarter of the experts and tokens: 1.4 GB of NVFP4 weights
+    "profile_skewed_e64": Workload("profile_skewed_e64", T=512, E=64, k=8, H=6144, I=2048, score="sigmoid",
+                                   zipf_s=1.1),
 }
 
 # Medium shapes that the oracle finishes in seconds but that still span
