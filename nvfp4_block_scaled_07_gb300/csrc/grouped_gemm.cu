@@ -915,13 +915,11 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM, PAIR), 1)
             ok = false;
             break;
           }
-          ptx::tc_fence_after();
-          // this stage's operand offset and scale slot; the next stage's are
-          // formed while this stage's MMAs are queued
-          uint64_t so = uint64_t(s * stage16);
-          uint32_t sf = tmem + uint32_t(kSfColBase) + s * uint32_t(C::SfCols);
           bool more;
           do {
+            ptx::tc_fence_after();
+            const uint64_t so = uint64_t(s * stage16);
+            const uint32_t sf = tmem + uint32_t(kSfColBase) + s * uint32_t(C::SfCols);
             const int nkb = min(4, kblocks - 4 * kt);
             uint32_t sn = s + 1, phn = ph;
             if (sn == uint32_t(S)) sn = 0, phn ^= 1u;
@@ -934,29 +932,20 @@ __global__ void __launch_bounds__(num_threads(SWIGLU, TM, PAIR), 1)
               else if constexpr (MX) ptx::tc_mma_mxfp4(d0, adesc, wdesc, idesc, sfa, sfw, acc);
               else ptx::tc_mma_nvfp4(d0, adesc, wdesc, idesc, sfa, sfw, acc);
             };
-            // the next stage: ready?  (its fence is taken here, before this
-            // stage's last MMA, so nothing but address moves sits between the
-            // two stages' MMAs)
-            auto probe_next = [&]() {
-              more = kt + 1 < nkt && ptx::mbar_test_wait(full_bar(sn), phn);
-              if (more) ptx::tc_fence_after();
-            };
             mma(0);
             if (PAIR && pend) commit(empty_bar(ps));  // frees stage ps (and its scale slot) once its MMAs have read it
             if (nkb == 4) {
               mma(1);
               mma(2);
-              probe_next();
+              more = kt + 1 < nkt && ptx::mbar_test_wait(full_bar(sn), phn);
               mma(3);
             } else {
               for (int kb = 1; kb < nkb; ++kb) mma(kb);
-              probe_next();
+              more = kt + 1 < nkt && ptx::mbar_test_wait(full_bar(sn), phn);
             }
             if (!PAIR) commit(empty_bar(s));
             ps = s, pend = PAIR;
             ++kt, s = sn, ph = phn;
-            so = uint64_t(s * stage16);
-            sf = tmem + uint32_t(kSfColBase) + s * uint32_t(C::SfCols);
           } while (more);
           if (pend) commit(empty_bar(ps));  // the group's last stage
           pend = false;
