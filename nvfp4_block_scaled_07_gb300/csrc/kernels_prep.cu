@@ -492,10 +492,24 @@ __device__ __forceinline__ void scan_experts(const int32_t* seg_count, int nseg,
     if (sub >= off) incl += o;
   }
   if (ge < E) {
+    // second pass in batches of 8 loads issued together (a load after each
+    // store would wait out a full L2 round trip per segment)
     int run = incl - local;
-    for (int s = sa; s < sb; ++s) {
+    int s = sa;
+    for (; s + 8 <= sb; s += 8) {
+      int c[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) c[j] = __ldcg(seg_count + int64_t(s + j) * E + ge);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        seg_base[int64_t(s + j) * E + ge] = run;
+        run += c[j];
+      }
+    }
+    for (; s < sb; ++s) {
+      const int c = __ldcg(seg_count + int64_t(s) * E + ge);
       seg_base[int64_t(s) * E + ge] = run;
-      run += __ldcg(seg_count + int64_t(s) * E + ge);
+      run += c;
     }
     if (sub == G - 1) s_tot[ge] = incl;
   }
