@@ -836,6 +836,31 @@ class MoELayer:
 
     __call__ = forward
 
+    def capture(self, x, logits, stream=None):
+        """Captures one forward() on the tensors x and logits into a CUDA
+        graph and returns it; graph.replay() then runs the whole layer (every
+        kernel launch of prepare, both GEMM plans and finalize) with no host
+        work per step, reading x and logits where they are and writing
+        self.out.  Copy each step's inputs into x and logits before replaying.
+        The launch plans for x's batch size are chosen first (autotune, which
+        synchronises); nothing in forward() synchronises or allocates, so the
+        capture holds exactly the eager launches."""
+        T = x.shape[0]
+        if self.T != T:
+            self._alloc(T)
+        if self.autotune_enabled and T not in self.plans:
+            self.autotune(x, logits)
+        side = torch.cuda.Stream(device=self.device) if stream is None else stream
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            self.forward(x, logits)      # one eager step on the capture stream first
+            side.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                self.forward(x, logits)
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        return graph
+
     # ---- tile autotuner ----
     def candidate_plans(self, which, T=None):
         """Launch plans the autotuner times for one GEMM at batch size T: one
