@@ -158,6 +158,32 @@ def test_layer_token_subset_matches_full_layer():
     assert inter["hs"].max() < 0x7E
 
 
+def test_finalize_hand_worked():
+    """The router-weighted sum back to token order ("SM120 FP4 Kernel Research
+    Campaign", Sections 5-6: token reordering with a fused reduction) on a
+    case worked by hand: dyadic values, so every product and sum is exact.
+
+    Y rows (expert order): r0 = (1, 2, 3), r1 = (0.5, -1, 4), r2 = (8, 0, -2),
+    r3 = (0.25, 0.25, 0.25).  Token 0 sends slot 0 to row 2 and slot 1 to row
+    0, weights 0.75 and 0.25; token 1 sends slot 0 to row 3 and slot 1 to
+    row 1, weights 0.5 and 0.5.
+      out[0] = 0.75 r2 + 0.25 r0 = (6.25, 0.5, -0.75)
+      out[1] = 0.5 r3 + 0.5 r1   = (0.375, -0.375, 2.125)"""
+    y = np.array([[1, 2, 3], [0.5, -1, 4], [8, 0, -2], [0.25, 0.25, 0.25]])
+    flat_to_perm = np.array([2, 0, 3, 1])
+    w = np.array([[0.75, 0.25], [0.5, 0.5]])
+    out = O.finalize(y, flat_to_perm, w, 2, 2)
+    assert np.array_equal(out, [[6.25, 0.5, -0.75], [0.375, -0.375, 2.125]])
+    # a one-hot weight picks out exactly the row its slot points at
+    for t in range(2):
+        for j in range(2):
+            oh = np.zeros((2, 2))
+            oh[t, j] = 1.0
+            got = O.finalize(y, flat_to_perm, oh, 2, 2)
+            assert np.array_equal(got[t], y[flat_to_perm[2 * t + j]])
+            assert not got[1 - t].any()
+
+
 def test_layer_invariant_to_token_order_within_expert():
     """Permuting tokens permutes the output rows (the layer is row-wise)."""
     w = W.TEST_WORKLOADS["many_experts"]

@@ -127,6 +127,12 @@ def finalize_reversed_weights(y, flat_to_perm, w, T, k):
     return ORIG["finalize"](y, flat_to_perm, np.asarray(w, np.float64).reshape(T, k)[:, ::-1], T, k)
 
 
+def finalize_slot_major(y, flat_to_perm, w, T, k):
+    # the flat ids read as slot-major (j * T + t) instead of token-major (t * k + j)
+    f2p = np.asarray(flat_to_perm).reshape(k, T).T.reshape(-1)
+    return ORIG["finalize"](y, f2p, w, T, k)
+
+
 def round_to_bf16_via_float32(v):
     return torch.from_numpy(np.asarray(v, np.float64).astype(np.float32)).to(torch.bfloat16).double().numpy()
 
@@ -171,7 +177,10 @@ MUTATIONS = {
     "silu without the z factor": (
         "silu", silu_without_z, [PL.test_single_expert_layer_is_dense_swiglu_ffn]),
     "finalize weights in reversed slot order": (
-        "finalize", finalize_reversed_weights, [PL.test_layer_token_subset_matches_full_layer]),
+        "finalize", finalize_reversed_weights,
+        [PL.test_layer_token_subset_matches_full_layer, PL.test_finalize_hand_worked]),
+    "finalize reads flat ids slot-major": (
+        "finalize", finalize_slot_major, [PL.test_finalize_hand_worked]),
     "bf16 rounding through float32": (
         "round_to_bf16", round_to_bf16_via_float32, [PF.test_bf16_rounding_of_float64_brute_force]),
     "MX shared exponent floor(log2 amax) - 1": (
