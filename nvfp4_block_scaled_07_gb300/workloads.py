@@ -72,6 +72,12 @@ PROFILE_WORKLOADS = {
     # many cold ones with a handful) at a quarter of the experts and tokens: 1.4 GB of NVFP4 weights
     "profile_skewed_e64": Workload("profile_skewed_e64", T=512, E=64, k=8, H=6144, I=2048, score="sigmoid",
                                    zipf_s=1.1),
+    # the prepare kernel's work of skewed_t2048 and prefill_t16384 (the same T, E, k, H and routing)
+    # with I = 128, so the weights are small and a multi-pass capture of the prepare holds little memory
+    "profile_prepare_t2048": Workload("profile_prepare_t2048", T=2048, E=256, k=8, H=6144, I=128,
+                                      score="sigmoid", zipf_s=1.1),
+    "profile_prepare_t16384": Workload("profile_prepare_t16384", T=16384, E=64, k=8, H=7168, I=128,
+                                       score="sigmoid"),
 }
 
 # Medium shapes that the oracle finishes in seconds but that still span
