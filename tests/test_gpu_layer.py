@@ -88,3 +88,28 @@ def test_layer_single_token(B):
                       *U.oracle_quantize_experts(inp["w_gu"]), *U.oracle_quantize_experts(inp["w_d"]), w.k,
                       w.score, np.float32(w.h_scale))
     U.check_close(out, ref, what="single-token layer")
+
+
+@pytest.mark.parametrize("tile_n", [(0, 0), (-1, -1), (-2, -2), (128, 128)],
+                         ids=["autotuned", "token-major", "pairs", "weight-rows-as-M"])
+def test_layer_all_tokens_on_two_experts(B, tile_n):
+    """The most skewed routing: a bias of +8 on experts 3 and 11 of 16 sends
+    every token to those two, so each holds all 600 tokens -- several token
+    tiles and a ragged last one in every tile orientation (600 = 2 x 256 + 88
+    = 4 x 128 + 88) -- and the other 14 experts are empty.  The down GEMM's K
+    (I = 384) ends in a half stage."""
+    w = W.Workload("two_hot", T=600, E=16, k=2, H=512, I=384, score="sigmoid")
+    inp = W.host_inputs(w, seed=11)
+    bias = np.zeros(w.E, np.float32)
+    bias[[3, 11]] = 8.0
+    cuda = torch.device("cuda")
+    layer = B.MoELayer(inp["w_gu"].to(cuda), inp["w_d"].to(cuda), w.k, w.score, True, w.h_scale,
+                       bias=torch.from_numpy(bias).to(cuda), tile_n=tile_n)
+    out = layer(inp["x"].to(cuda), inp["logits"].to(cuda)).float().cpu().numpy()
+    B.sync_status()
+    counts = layer.perm.counts.cpu().numpy()
+    assert counts[3] == counts[11] == w.T and counts.sum() == w.T * w.k
+    ref = O.moe_layer(inp["x"].float().numpy(), inp["logits"].numpy(), bias,
+                      *U.oracle_quantize_experts(inp["w_gu"]), *U.oracle_quantize_experts(inp["w_d"]), w.k,
+                      w.score, np.float32(w.h_scale))
+    U.check_close(out, ref, what=f"layer output, tiles {tile_n}")
