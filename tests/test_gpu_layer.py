@@ -113,3 +113,19 @@ def test_layer_all_tokens_on_two_experts(B, tile_n):
                       *U.oracle_quantize_experts(inp["w_gu"]), *U.oracle_quantize_experts(inp["w_d"]), w.k,
                       w.score, np.float32(w.h_scale))
     U.check_close(out, ref, what=f"layer output, tiles {tile_n}")
+
+
+def test_layer_most_experts(B):
+    """The largest expert count the library takes (E = 1024, k = 32): 64
+    tokens over 1024 experts leave most of them empty or with a row or two,
+    and the GEMMs' per-expert tile map fills 16 KB of their shared memory."""
+    w = W.Workload("e1024", T=64, E=1024, k=32, H=256, I=128, score="softmax")
+    inp = W.host_inputs(w, seed=13)
+    cuda = torch.device("cuda")
+    layer = B.MoELayer(inp["w_gu"].to(cuda), inp["w_d"].to(cuda), w.k, w.score, True, w.h_scale)
+    out = layer(inp["x"].to(cuda), inp["logits"].to(cuda)).float().cpu().numpy()
+    B.sync_status()
+    ref = O.moe_layer(inp["x"].float().numpy(), inp["logits"].numpy(), None,
+                      *U.oracle_quantize_experts(inp["w_gu"]), *U.oracle_quantize_experts(inp["w_d"]), w.k,
+                      w.score, np.float32(w.h_scale))
+    U.check_close(out, ref, what="E = 1024 layer output")

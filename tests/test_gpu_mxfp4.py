@@ -234,3 +234,27 @@ def test_grouped_gemm_mx_dynamic_schedule(B):
     rows = torch.from_numpy(pos).cuda()
     assert torch.equal(a[rows], b[rows]) and not ws.any().item()
     U.check_close(b.float().cpu().numpy()[pos], O.round_to_bf16(ref), what="MXFP4 GEMM, dynamic schedule")
+
+
+@pytest.mark.parametrize("tile_n", [(0, 0), (-1, -1), (-2, -2), (128, 128)],
+                         ids=["autotuned", "token-major", "pairs", "weight-rows-as-M"])
+def test_layer_mx_all_tokens_on_two_experts(B, tile_n):
+    """MXFP4 counterpart of the most skewed routing case: every one of 600
+    tokens on experts 3 and 11 of 16 (a +8 bias), ragged last tiles in each
+    orientation, 14 empty experts, a half K stage in the down GEMM."""
+    w = W.Workload("two_hot", T=600, E=16, k=2, H=512, I=384, score="sigmoid")
+    inp = W.host_inputs(w, seed=12)
+    bias = np.zeros(w.E, np.float32)
+    bias[[3, 11]] = 8.0
+    cuda = torch.device("cuda")
+    layer = B.MoELayer(inp["w_gu"].to(cuda), inp["w_d"].to(cuda), w.k, w.score, True, w.h_scale,
+                       bias=torch.from_numpy(bias).to(cuda), fmt="mxfp4", tile_n=tile_n)
+    out = layer(inp["x"].to(cuda), inp["logits"].to(cuda)).float().cpu().numpy()
+    B.sync_status()
+    counts = layer.perm.counts.cpu().numpy()
+    assert counts[3] == counts[11] == w.T and counts.sum() == w.T * w.k
+    gq = U.oracle_quantize_experts_mx(inp["w_gu"])
+    dq = U.oracle_quantize_experts_mx(inp["w_d"])
+    ref = O.moe_layer_mx(inp["x"].float().numpy(), inp["logits"].numpy(), bias, gq[0], gq[1], dq[0], dq[1], w.k,
+                         w.score)
+    U.check_close(out, ref, what=f"MXFP4 layer output, tiles {tile_n}")
